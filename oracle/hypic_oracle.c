@@ -1,0 +1,310 @@
+/*
+ * hypic_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU restatement of the linear-attention state path of
+ * HYPIC (position-independent caching for hybrid-attention models).  It is the
+ * checker that the CUDA library is compared against; it shares no code, header,
+ * table or helper with the GPU path and must never be called by the product.
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline leg use it.
+ *
+ * Sources, by page:
+ *  [AB]  aibase news article on HYPIC (Traditional Chinese), paragraph on the
+ *        linear layers ("對線性層..."): a segment C is summarised by the
+ *        segment-cumulative transition operator T_C (the ordered product of all
+ *        per-token transition matrices of C) and the zero-start end state
+ *        S(C|0); reuse composes S(C1.C2) = T(C2) S(C1) + S(C2); naive addition
+ *        S(C1)+S(C2) is exact only for plain linear attention.
+ *  [AB2] same article, paragraph on the full-attention layers ("對全注意力層..."):
+ *        the first w tokens of each internal segment form a seam window that is
+ *        not cached; at reuse the linear layers compute the window's own T and S
+ *        on the fly, advance the running state through it and emit each seam
+ *        token's output.
+ *  [AX]  arXiv abstract (2607.01299): near-exact, constant-time composition of
+ *        independently cached segments.
+ *  Per-token recurrences (the families named in [AB]); the state S is dk x dv
+ *  and is left-multiplied by the transition, latest token leftmost:
+ *    GDN    (gated delta rule, Yang/Kautz/Hatamizadeh, "Gated Delta Networks"):
+ *           S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T
+ *    RetNet (scalar decay):   S_t = g S_{t-1} + k_t v_t^T,      T = g^L
+ *    GLA    (diagonal decay): S_t = Diag(g_t) S_{t-1} + k_t v_t^T
+ *    vanilla linear attention: S_t = S_{t-1} + k_t v_t^T,       T = I
+ *    output of a token: o_t = S_t^T q_t (state after the token's own write).
+ *
+ * Everything is a token-by-token loop in double precision, exactly in the
+ * order above.  Inputs arrive as float32 arrays (bf16 inputs are upcast exactly
+ * by the caller) and are widened to double on read.
+ *
+ * Packed layouts (row-major, innermost last):
+ *   k, v, q   [n_layers][n_tokens][n_heads][d]
+ *   alpha, beta [n_layers][n_tokens][n_heads]
+ *   gamma     [n_layers][n_heads]
+ *   g         [n_layers][n_tokens][n_heads][dk]
+ *   T (GDN)   [n_items][n_layers][n_heads][dk][dk]
+ *   T (RetNet)[n_items][n_layers][n_heads]
+ *   T (GLA)   [n_items][n_layers][n_heads][dk]
+ *   S, state  [n_items][n_layers][n_heads][dk][dv]
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_GDN = 0, OR_RETNET = 1, OR_GLA = 2, OR_VANILLA = 3 };
+
+/* ---------------------------------------------------------------- tokens -- */
+
+/* Read one token's inputs for (layer, token, head) into double buffers. */
+typedef struct {
+    int family, n_layers, n_heads, dk, dv;
+    long long n_tokens;
+    const float *q, *k, *v, *alpha, *beta, *gamma, *g;
+} or_inputs;
+
+static void read_vec(const float* base, long long off, int n, double* out)
+{
+    for (int i = 0; i < n; ++i) out[i] = (double)base[off + i];
+}
+
+/* M <- A_t M for the GDN transition A_t = a (I - b k k^T), M is dk x ncols.
+   [AB]: the per-token transition matrix of the gated-delta family. */
+static void gdn_apply_transition(int dk, int ncols, double* M, const double* k,
+                                 double a, double b, double* tmp)
+{
+    for (int j = 0; j < ncols; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < dk; ++i) s += k[i] * M[(size_t)i * ncols + j];
+        tmp[j] = s; /* (k^T M)_j */
+    }
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < ncols; ++j)
+            M[(size_t)i * ncols + j] = a * (M[(size_t)i * ncols + j] - b * k[i] * tmp[j]);
+}
+
+/* S <- S + w k v^T (the write term of every family). */
+static void add_write(int dk, int dv, double* S, const double* k, const double* v, double w)
+{
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += w * k[i] * v[j];
+}
+
+/* One token of the recurrence of the chosen family, applied to the state S and,
+   when T is non-NULL, to the running transition product T (the same left
+   multiply, without the write term). */
+static void token_step(const or_inputs* in, int layer, long long tok, int head,
+                       double* S, double* T, double* Tvec, double* Tscal,
+                       double* kb, double* vb, double* gb, double* tmp)
+{
+    const int dk = in->dk, dv = in->dv, H = in->n_heads;
+    const long long row = ((long long)layer * in->n_tokens + tok) * H + head;
+    read_vec(in->k, row * dk, dk, kb);
+    read_vec(in->v, row * dv, dv, vb);
+    switch (in->family) {
+    case OR_GDN: {
+        const double a = in->alpha[row];
+        const double b = in->beta[row];
+        gdn_apply_transition(dk, dv, S, kb, a, b, tmp);
+        add_write(dk, dv, S, kb, vb, b);
+        if (T) gdn_apply_transition(dk, dk, T, kb, a, b, tmp);
+        break;
+    }
+    case OR_RETNET: {
+        const double gm = in->gamma[(size_t)layer * H + head];
+        for (size_t i = 0; i < (size_t)dk * dv; ++i) S[i] *= gm;
+        add_write(dk, dv, S, kb, vb, 1.0);
+        if (Tscal) *Tscal *= gm;
+        break;
+    }
+    case OR_GLA: {
+        read_vec(in->g, row * dk, dk, gb);
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] *= gb[i];
+        add_write(dk, dv, S, kb, vb, 1.0);
+        if (Tvec) for (int i = 0; i < dk; ++i) Tvec[i] *= gb[i];
+        break;
+    }
+    default: /* vanilla */
+        add_write(dk, dv, S, kb, vb, 1.0);
+        break;
+    }
+}
+
+static int check_common(int family, int n_layers, int n_heads, int dk, int dv)
+{
+    if (family < OR_GDN || family > OR_VANILLA) return 1;
+    if (n_layers <= 0 || n_heads <= 0 || dk <= 0 || dv <= 0) return 1;
+    if (family == OR_GDN && dk <= 0) return 1;
+    return 0;
+}
+
+/* ----------------------------------------------------------------- build -- */
+
+/*
+ * Build the cached pair (T_C, S(C|0)) of every (segment, layer, head) [AB].
+ * Segment s covers tokens [cu_seqlens[s] + skip[s], cu_seqlens[s+1]); skip
+ * (nullable) removes the seam window of an internal segment from the cached
+ * pair [AB2].  The build starts from T = I, S = 0 and runs the token loop.
+ * T_out may be NULL (vanilla: T = I is not stored).
+ */
+int oracle_build(int family, int n_layers, int n_heads, int dk, int dv,
+                 int n_seg, const int* cu_seqlens, const int* skip, long long n_tokens,
+                 const float* k, const float* v, const float* alpha, const float* beta,
+                 const float* gamma, const float* g,
+                 double* T_out, double* S_out, int n_threads)
+{
+    if (check_common(family, n_layers, n_heads, dk, dv) || n_seg < 0) return 1;
+    or_inputs in = {family, n_layers, n_heads, dk, dv, n_tokens, NULL, k, v, alpha, beta, gamma, g};
+    const long long n_items = (long long)n_seg * n_layers * n_heads;
+    int bad = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (long long it = 0; it < n_items; ++it) {
+        const int head = (int)(it % n_heads);
+        const int layer = (int)((it / n_heads) % n_layers);
+        const int seg = (int)(it / ((long long)n_heads * n_layers));
+        const long long b0 = (long long)cu_seqlens[seg] + (skip ? skip[seg] : 0);
+        const long long b1 = cu_seqlens[seg + 1];
+        double* S = (double*)calloc((size_t)dk * dv, sizeof(double));
+        double* T = (family == OR_GDN) ? (double*)calloc((size_t)dk * dk, sizeof(double)) : NULL;
+        double* Tv = (family == OR_GLA) ? (double*)malloc((size_t)dk * sizeof(double)) : NULL;
+        double Ts = 1.0;
+        double* kb = (double*)malloc(sizeof(double) * (size_t)(dk + dv + dk + (dk > dv ? dk : dv)));
+        double *vb = kb + dk, *gb = vb + dv, *tmp = gb + dk;
+        if (!S || !kb || (family == OR_GDN && !T) || (family == OR_GLA && !Tv)) { bad = 1; }
+        else {
+            if (T) for (int i = 0; i < dk; ++i) T[(size_t)i * dk + i] = 1.0;
+            if (Tv) for (int i = 0; i < dk; ++i) Tv[i] = 1.0;
+            for (long long t = b0; t < b1; ++t)
+                token_step(&in, layer, t, head, S, T, Tv, &Ts, kb, vb, gb, tmp);
+            memcpy(S_out + (size_t)it * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+            if (T_out) {
+                if (family == OR_GDN) memcpy(T_out + (size_t)it * dk * dk, T, sizeof(double) * (size_t)dk * dk);
+                else if (family == OR_GLA) memcpy(T_out + (size_t)it * dk, Tv, sizeof(double) * (size_t)dk);
+                else if (family == OR_RETNET) T_out[it] = Ts;
+            }
+        }
+        free(S); free(T); free(Tv); free(kb);
+    }
+    return bad;
+}
+
+/* --------------------------------------------------------------- compose -- */
+
+/*
+ * Compose chains of cached pairs [AB]: for chain r, starting from S0[r] (or
+ * zero), apply S <- T_i S + S_i for i = seg_idx[cu_chain[r]], ...,
+ * seg_idx[cu_chain[r+1]-1] in that order.  The product T_i S is the family's:
+ * a dk x dk matrix (GDN), a scalar (RetNet), a row scaling (GLA) or the
+ * identity (vanilla, plain addition).  T_tab holds T_C in double with any
+ * stored scale already applied; `naive` != 0 drops T entirely (the addition
+ * strawman of [AB], "--pic-mode addition" in the README's PIC modes table).
+ */
+int oracle_compose(int family, int n_layers, int n_heads, int dk, int dv, int n_pairs,
+                   const double* T_tab, const double* S_tab,
+                   int n_chains, const int* cu_chain, const int* seg_idx,
+                   const double* S0, double* S_out, int naive, int n_threads)
+{
+    if (check_common(family, n_layers, n_heads, dk, dv) || n_chains < 0 || n_pairs < 0) return 1;
+    const long long LH = (long long)n_layers * n_heads;
+    const long long n_items = (long long)n_chains * LH;
+    const size_t dd = (size_t)dk * dv;
+    int bad = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (long long it = 0; it < n_items; ++it) {
+        const long long lh = it % LH;
+        const int r = (int)(it / LH);
+        double* S = (double*)malloc(sizeof(double) * dd);
+        double* N = (double*)malloc(sizeof(double) * dd);
+        if (!S || !N) { bad = 1; free(S); free(N); continue; }
+        if (S0) memcpy(S, S0 + (size_t)it * dd, sizeof(double) * dd);
+        else memset(S, 0, sizeof(double) * dd);
+        for (int j = cu_chain[r]; j < cu_chain[r + 1]; ++j) {
+            const int p = seg_idx[j];
+            if (p < 0 || p >= n_pairs) { bad = 1; break; }
+            const double* Si = S_tab + ((size_t)p * LH + lh) * dd;
+            if (naive || family == OR_VANILLA) {
+                for (size_t e = 0; e < dd; ++e) N[e] = S[e];
+            } else if (family == OR_GDN) {
+                const double* Ti = T_tab + ((size_t)p * LH + lh) * (size_t)dk * dk;
+                for (int i = 0; i < dk; ++i)
+                    for (int c = 0; c < dv; ++c) {
+                        double s = 0.0;
+                        for (int m = 0; m < dk; ++m) s += Ti[(size_t)i * dk + m] * S[(size_t)m * dv + c];
+                        N[(size_t)i * dv + c] = s;
+                    }
+            } else if (family == OR_RETNET) {
+                const double ts = T_tab[(size_t)p * LH + lh];
+                for (size_t e = 0; e < dd; ++e) N[e] = ts * S[e];
+            } else { /* GLA */
+                const double* tv = T_tab + ((size_t)p * LH + lh) * (size_t)dk;
+                for (int i = 0; i < dk; ++i)
+                    for (int c = 0; c < dv; ++c) N[(size_t)i * dv + c] = tv[i] * S[(size_t)i * dv + c];
+            }
+            for (size_t e = 0; e < dd; ++e) S[e] = N[e] + Si[e];
+        }
+        memcpy(S_out + (size_t)it * dd, S, sizeof(double) * dd);
+        free(S); free(N);
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ seam -- */
+
+/*
+ * Seam-window advance [AB2]: for seam r, start from state_in[r] (or zero when
+ * state_in is NULL), run the family's token loop over the seam tokens
+ * [cu_seam[r], cu_seam[r+1]) of the packed seam-token arrays and emit, after
+ * each token's own write, o_t = S_t^T q_t into row t of o_out
+ * ([n_layers][n_tokens][n_heads][dv]).  The end state goes to state_out.
+ * With one seam covering a whole request from zero this is the full
+ * sequential recurrence.
+ */
+int oracle_seam(int family, int n_layers, int n_heads, int dk, int dv,
+                int n_seams, const int* cu_seam, long long n_tokens,
+                const float* q, const float* k, const float* v,
+                const float* alpha, const float* beta, const float* gamma, const float* g,
+                const double* state_in, double* state_out, double* o_out, int n_threads)
+{
+    if (check_common(family, n_layers, n_heads, dk, dv) || n_seams < 0) return 1;
+    or_inputs in = {family, n_layers, n_heads, dk, dv, n_tokens, q, k, v, alpha, beta, gamma, g};
+    const long long LH = (long long)n_layers * n_heads;
+    const long long n_items = (long long)n_seams * LH;
+    const size_t dd = (size_t)dk * dv;
+    int bad = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (long long it = 0; it < n_items; ++it) {
+        const int head = (int)(it % n_heads);
+        const int layer = (int)((it / n_heads) % n_layers);
+        const int r = (int)(it / LH);
+        double* S = (double*)malloc(sizeof(double) * dd);
+        double* kb = (double*)malloc(sizeof(double) * (size_t)(dk + dv + dk + dk + (dk > dv ? dk : dv)));
+        if (!S || !kb) { bad = 1; free(S); free(kb); continue; }
+        double *vb = kb + dk, *gb = vb + dv, *qb = gb + dk, *tmp = qb + dk;
+        if (state_in) memcpy(S, state_in + (size_t)it * dd, sizeof(double) * dd);
+        else memset(S, 0, sizeof(double) * dd);
+        for (long long t = cu_seam[r]; t < cu_seam[r + 1]; ++t) {
+            token_step(&in, layer, t, head, S, NULL, NULL, NULL, kb, vb, gb, tmp);
+            const long long row = ((long long)layer * n_tokens + t) * n_heads + head;
+            read_vec(q, row * dk, dk, qb);
+            for (int c = 0; c < dv; ++c) {
+                double s = 0.0;
+                for (int i = 0; i < dk; ++i) s += S[(size_t)i * dv + c] * qb[i];
+                o_out[row * dv + c] = s;
+            }
+        }
+        memcpy(state_out + (size_t)it * dd, S, sizeof(double) * dd);
+        free(S); free(kb);
+    }
+    return bad;
+}
+
+int oracle_version(void) { return 1; }

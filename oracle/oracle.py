@@ -1,0 +1,216 @@
+"""fp64 CPU oracle for the HYPIC linear-attention state path -- TEST INFRASTRUCTURE.
+
+This module is the checker, not the product.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import it.
+It loads ``hypic_oracle.c`` (built here with gcc, never with the CUDA
+toolchain) through ctypes and shares no code with the GPU library.
+
+What it computes (sources named in ``hypic_oracle.c``'s header):
+
+* ``build``   -- per (segment, layer, head) the cached pair (T_C, S(C|0)) of
+  the aibase article's linear-layer paragraph, by the plain token loop from
+  T = I, S = 0.
+* ``compose`` -- S(C1.C2) = T(C2) S(C1) + S(C2) along a chain (same
+  paragraph), or the naive addition strawman with ``naive=True``.
+* ``seam``    -- the seam-window advance of the full-attention paragraph:
+  the token loop from a given state, emitting o_t = S_t^T q_t per token.  One
+  seam spanning a whole request from zero is the full sequential recurrence.
+
+All arithmetic is double precision; float32 inputs (bf16 inputs upcast
+exactly) are widened on read.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+FAMILIES = {"gdn": 0, "retnet": 1, "gla": 2, "vanilla": 3}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hypic_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libhypic_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP); returns the .so path."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+            tmp = _LIB + f".tmp{os.getpid()}"
+            # -ffp-contract=off keeps each double multiply and add a separate
+            # IEEE operation, so the result does not depend on the host's FMA.
+            subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC",
+                                   "-shared", _SRC, "-o", tmp, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        LL = ctypes.c_longlong
+        lib.oracle_build.argtypes = [I, I, I, I, I, I, P, P, LL, P, P, P, P, P, P, P, P, I]
+        lib.oracle_compose.argtypes = [I, I, I, I, I, I, P, P, I, P, P, P, P, I, I]
+        lib.oracle_seam.argtypes = [I, I, I, I, I, I, P, LL, P, P, P, P, P, P, P, P, P, P, I]
+        for f in (lib.oracle_build, lib.oracle_compose, lib.oracle_seam):
+            f.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f32(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    return a
+
+
+def _i32(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def build_pairs(family, k, v, cu_seqlens, *, alpha=None, beta=None, gamma=None, g=None,
+                skip=None, n_threads=None):
+    """(T_C, S(C|0)) for every (segment, layer, head).
+
+    k: [n_layers][n_tokens][n_heads][dk], v: [..][dv]; gates as in the header.
+    Returns (T, S) in float64 with leading [n_seg][n_layers][n_heads]; T is
+    None for vanilla, shaped [...][dk][dk] (GDN), [...] (RetNet) or [...][dk]
+    (GLA).
+    """
+    fam = FAMILIES[family]
+    k, v = _f32(k), _f32(v)
+    n_layers, n_tokens, n_heads, dk = k.shape
+    dv = v.shape[-1]
+    cu = _i32(cu_seqlens)
+    n_seg = cu.shape[0] - 1
+    sk = _i32(skip)
+    alpha, beta, gamma, g = _f32(alpha), _f32(beta), _f32(gamma), _f32(g)
+    S = np.zeros((n_seg, n_layers, n_heads, dk, dv))
+    if fam == 0:
+        T = np.zeros((n_seg, n_layers, n_heads, dk, dk))
+    elif fam == 1:
+        T = np.zeros((n_seg, n_layers, n_heads))
+    elif fam == 2:
+        T = np.zeros((n_seg, n_layers, n_heads, dk))
+    else:
+        T = None
+    rc = _load().oracle_build(fam, n_layers, n_heads, dk, dv, n_seg, _ptr(cu), _ptr(sk), n_tokens,
+                              _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(g),
+                              _ptr(T), _ptr(S), n_threads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_build failed")
+    return T, S
+
+
+def compose(family, T_tab, S_tab, cu_chain, seg_idx, S0=None, *, naive=False, n_threads=None):
+    """Chain compose S <- T_i S + S_i (double precision).
+
+    T_tab / S_tab: [n_pairs][n_layers][n_heads]... as returned by build_pairs
+    (T with any storage scale already applied).  Returns S_end
+    [n_chains][n_layers][n_heads][dk][dv].
+    """
+    fam = FAMILIES[family]
+    S_tab = _f64(S_tab)
+    n_pairs, n_layers, n_heads, dk, dv = S_tab.shape
+    T_tab = _f64(T_tab)
+    cu = _i32(cu_chain)
+    idx = _i32(seg_idx)
+    n_chains = cu.shape[0] - 1
+    S0 = _f64(S0)
+    out = np.zeros((n_chains, n_layers, n_heads, dk, dv))
+    rc = _load().oracle_compose(fam, n_layers, n_heads, dk, dv, n_pairs, _ptr(T_tab), _ptr(S_tab),
+                                n_chains, _ptr(cu), _ptr(idx), _ptr(S0), _ptr(out), int(bool(naive)),
+                                n_threads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_compose failed")
+    return out
+
+
+def seam(family, q, k, v, cu_seam, state_in=None, *, alpha=None, beta=None, gamma=None, g=None,
+         n_threads=None):
+    """Seam-window advance; returns (state_out, o).
+
+    q, k: [n_layers][n_tok][n_heads][dk], v: [..][dv]; state_in
+    [n_seams][n_layers][n_heads][dk][dv] or None (zero start).  o has the
+    layout of v; rows outside every seam stay zero.
+    """
+    fam = FAMILIES[family]
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    n_layers, n_tokens, n_heads, dk = k.shape
+    dv = v.shape[-1]
+    cu = _i32(cu_seam)
+    n_seams = cu.shape[0] - 1
+    alpha, beta, gamma, g = _f32(alpha), _f32(beta), _f32(gamma), _f32(g)
+    sin = _f64(state_in)
+    sout = np.zeros((n_seams, n_layers, n_heads, dk, dv))
+    o = np.zeros((n_layers, n_tokens, n_heads, dv))
+    rc = _load().oracle_seam(fam, n_layers, n_heads, dk, dv, n_seams, _ptr(cu), n_tokens,
+                             _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(g),
+                             _ptr(sin), _ptr(sout), _ptr(o), n_threads or default_threads())
+    if rc:
+        raise RuntimeError("oracle_seam failed")
+    return sout, o
+
+
+# -------------------------------------------------------------- utilities --
+
+def rel_fro(x, ref, axes):
+    """Relative Frobenius error ||x - ref|| / ||ref|| per object, in fp64.
+
+    ``axes`` are the trailing axes that make up one object (e.g. (-2, -1) for a
+    d x d matrix).  Where ||ref|| is below 1e-30 the absolute error is
+    returned instead.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    num = np.sqrt(np.sum((x - ref) ** 2, axis=axes))
+    den = np.sqrt(np.sum(ref ** 2, axis=axes))
+    return np.where(den < 1e-30, num, num / np.where(den < 1e-30, 1.0, den))
+
+
+def scaled_to_f64(mant, exp):
+    """T = mant * 2**exp, mant float32 [..][d][d], exp int32 [..] -> float64."""
+    mant = np.asarray(mant, dtype=np.float64)
+    exp = np.asarray(exp, dtype=np.int64)
+    return np.ldexp(mant, exp[..., None, None])
+
+
+def f64_to_scaled(T):
+    """Split a float64 matrix stack into (float32 mantissa, int32 exponent).
+
+    The exponent of each matrix is that of its largest magnitude entry, so the
+    mantissa's largest entry lies in [0.5, 1); an all-zero matrix gets 0.
+    This is the storage format the GPU build emits for GDN T_C.
+    """
+    T = np.asarray(T, dtype=np.float64)
+    amax = np.max(np.abs(T), axis=(-2, -1))
+    _, e = np.frexp(np.where(amax > 0, amax, 1.0))
+    e = np.where(amax > 0, e, 0).astype(np.int32)
+    mant = np.ldexp(T, -e.astype(np.int64)[..., None, None]).astype(np.float32)
+    return mant, e
