@@ -1,0 +1,418 @@
+"""Benchmark of the HYPIC linear-attention state path on one GB300 per rank.
+
+One step = one pass of the whole hot path over the long cold request
+(30 GDN layers x 32 heads, d=128, bf16, 100,000 tokens in ~78 segments of
+512-2048 tokens, 8-token seam windows):
+  1. hypic_segment_build over every cached body (segment 0 whole, the
+     others without their seam window) -- all layers x heads in one call;
+  2. the reuse chain: state = pair(segment 0); for each internal segment,
+     hypic_seam_advance over its 8 seam tokens (emitting o_t = S_t^T q_t),
+     then hypic_compose with the segment's body pair.
+Inputs are drawn on the device (seeded) and stay resident; they total
+~50 GB, far above the 129 MB L2, so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "segment-build tokens/s (all layers×heads) + composes/s; % tensor/HBM roofline"
+WORKLOAD = dict(n_layers=30, H=32, d=128, n_tokens=100_000, seam_w=8)
+FLOP_PER_TOKEN_HEAD = 180_224      # chunk-64 low-rank GDN build (gram, W, U, two state GEMMs)
+COMPOSE_BYTES = 131_072            # T_p + S_p (fp32, d=128) streamed per head-compose
+SEAM_STATE_BYTES = 131_072         # state read + write per seam-head
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------ our arm ----
+
+class LongRequest:
+    """Device-resident inputs, outputs and argument blocks of one request."""
+
+    def __init__(self, B, seed, device):
+        import torch
+        from linear_attn_state_hypic_gb300 import synth
+        W = WORKLOAD
+        self.B, self.torch = B, torch
+        r = synth.long_request_device(seed=seed, n_layers=W["n_layers"], H=W["H"], d=W["d"],
+                                      n_tokens=W["n_tokens"], seam_w=W["seam_w"], device=device)
+        self.r = r
+        self.cu = r["cu_seqlens"]
+        self.skip = r["seam_skip"]
+        self.n_seg = len(self.cu) - 1
+        self.L, self.H, self.d = W["n_layers"], W["H"], W["d"]
+        seam_tok = torch.from_numpy(r["seam_tok"]).to(device)
+        # Seam-token inputs packed per internal segment (fresh tokens at reuse time).
+        self.k_seam = r["k"][:, seam_tok].contiguous()
+        self.v_seam = r["v"][:, seam_tok].contiguous()
+        self.a_seam = r["alpha"][:, seam_tok].contiguous()
+        self.b_seam = r["beta"][:, seam_tok].contiguous()
+        self.q_seam = r["q_seam"]
+        self.seam_off = np.concatenate([[0], np.cumsum(self.skip[1:])]).astype(np.int64)
+        self.body_tokens = int(np.sum(np.diff(self.cu) - self.skip))
+        self.T, self.T_exp, self.S = B.alloc_build_outputs("gdn", self.n_seg, self.L, self.H, self.d, self.d, device)
+        self.state = torch.empty((1, self.L, self.H, self.d, self.d), dtype=torch.float32, device=device)
+        self.state2 = torch.empty_like(self.state)
+        self.o = torch.empty((self.L, len(r["seam_tok"]), self.H, self.d), dtype=torch.float32, device=device)
+        self._make_args(device)
+
+    def _make_args(self, device):
+        B, torch = self.B, self.torch
+        r = self.r
+        self.keep = []
+        self.bargs, k1 = B.build_args("gdn", r["k"], r["v"], self.cu, alpha=r["alpha"], beta=r["beta"],
+                                      seam_skip=self.skip, T_out=self.T, T_exp_out=self.T_exp, S_out=self.S)
+        self.keep.append(k1)
+        self.ws_bytes = B.hypic_build_workspace_size(self.bargs)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        # compose arguments: one single-step chain per segment, ping-ponging the state
+        self.cargs = []
+        cu1 = np.array([0, 1], np.int32)
+        for i in range(self.n_seg):
+            src, dst = (None, self.state) if i == 0 else ((self.state, self.state2) if i % 2 == 1
+                                                         else (self.state2, self.state))
+            a, kk = B.compose_args("gdn", self.S, cu1, np.array([i], np.int32), T_tab=self.T, T_exp_tab=self.T_exp,
+                                   S0=src, S_out=dst)
+            self.cargs.append(a)
+            self.keep.append(kk)
+        self.final = self.state if (self.n_seg - 1) % 2 == 0 else self.state2
+        # Each seam's inputs get their own contiguous [L][w][H][d] buffers (made
+        # once at setup: they are the fresh seam tokens of the reuse request).
+        self.seam_bufs = []
+        for idx in range(self.n_seg - 1):
+            o0, w = int(self.seam_off[idx]), int(self.skip[idx + 1])
+            bufs = [x[:, o0:o0 + w].contiguous() for x in (self.q_seam, self.k_seam, self.v_seam)]
+            gates = [x[:, o0:o0 + w].contiguous() for x in (self.a_seam, self.b_seam)]
+            o = torch.empty((self.L, w, self.H, self.d), dtype=torch.float32, device=device)
+            i = idx + 1
+            st = self.state if i % 2 == 1 else self.state2
+            a2, kk2 = B.seam_args("gdn", bufs[0], bufs[1], bufs[2], np.array([0, w], np.int32), alpha=gates[0],
+                                  beta=gates[1], state_in=st, state_out=st, o_out=o)
+            self.seam_bufs.append((a2, kk2, bufs, gates, o))
+
+    def run_step(self, stream, ev=None):
+        """One pass of the hot path; ev = (b0, b1, c0, c1) events around the build and the chain."""
+        B = self.B
+        if ev:
+            ev[0].record()
+        st = B.hypic_segment_build(self.bargs, self.ws.data_ptr(), self.ws_bytes, stream)
+        if ev:
+            ev[1].record()
+        st |= B.hypic_compose(self.cargs[0], stream)
+        for i in range(1, self.n_seg):
+            st |= B.hypic_seam_advance(self.seam_bufs[i - 1][0], stream)
+            st |= B.hypic_compose(self.cargs[i], stream)
+        if ev:
+            ev[2].record()
+        if st != 0:
+            raise RuntimeError("a library call failed in the step")
+
+    def launches_per_step(self):
+        return 2 + 1 + 2 * (self.n_seg - 1)   # plan + build, first compose, seam + compose per seam
+
+
+def time_our_arm(args, rank, world, device):
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+
+    torch.cuda.set_device(device)
+    req = LongRequest(B, seed=rank, device=device)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    for _ in range(args.warmup):
+        req.run_step(sp)
+    B.check_device(sp)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record()
+        for s in range(args.steps):
+            req.run_step(sp, ev[s])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    B.check_device(sp)
+    ms = start.elapsed_time(stop)
+    build_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    chain_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_max = allreduce_max(ms, world)
+    res = dict(ms=ms_max, build_ms=statistics.mean(build_ms), chain_ms=statistics.mean(chain_ms),
+               clocks=clk.summary(), body_tokens=req.body_tokens, n_seg=req.n_seg,
+               launches=req.launches_per_step() * args.steps, req=req)
+    return res
+
+
+def e2e_our_arm(req, steps):
+    """Same step through the public C ABI with host inputs: every step copies
+    the request's inputs from pinned host memory to the device and reads the
+    final state and the seam outputs back."""
+    import torch
+    r = req.r
+    dev_in = [r["k"], r["v"], r["alpha"], r["beta"]] + [x for sb in req.seam_bufs for x in sb[2] + sb[3]]
+    t0 = time.time()
+    host_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in dev_in]
+    for h, d in zip(host_in, dev_in):
+        h.copy_(d)
+    outs = [req.final] + [sb[4] for sb in req.seam_bufs]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    setup_s = time.time() - t0
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    sp = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        req.run_step(sp)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return dict(ms=ms, h2d=h2d, d2h=d2h, setup_s=setup_s)
+
+
+# ------------------------------------------------------- oracle (CPU) arm --
+
+def oracle_sample(n_heads, n_seg, seed=0):
+    """Host inputs for a bounded sample of the long request: layer 0, the first
+    n_seg segments (their true lengths), n_heads heads."""
+    from linear_attn_state_hypic_gb300 import synth
+    lengths = synth.long_request_lengths(seed, WORKLOAD["n_tokens"])[:n_seg]
+    inp = synth.gdn_ragged(seed=seed, H=n_heads, d=WORKLOAD["d"], lengths=lengths, with_q=True)
+    skip = np.full(n_seg, WORKLOAD["seam_w"], np.int32)
+    skip[0] = 0
+    return inp, skip
+
+
+def run_oracle_sample(inp, skip, threads):
+    """The oracle's version of the step on the sample: build the bodies, then
+    seam-advance and compose along the chain."""
+    from oracle import oracle as orc
+    cu = inp["cu_seqlens"]
+    T, S = orc.build_pairs("gdn", inp["k"], inp["v"], cu, alpha=inp["alpha"], beta=inp["beta"], skip=skip,
+                           n_threads=threads)
+    state = orc.compose("gdn", T, S, [0, 1], [0], n_threads=threads)
+    for i in range(1, len(cu) - 1):
+        sl = slice(int(cu[i]), int(cu[i]) + int(skip[i]))
+        sub = {key: np.ascontiguousarray(inp[key][:, sl]) for key in ("q", "k", "v", "alpha", "beta")}
+        state, _ = orc.seam("gdn", sub["q"], sub["k"], sub["v"], [0, int(skip[i])], state_in=state,
+                            alpha=sub["alpha"], beta=sub["beta"], n_threads=threads)
+        state = orc.compose("gdn", T, S, [0, 1], [i], S0=state, n_threads=threads)
+    return state
+
+
+def oracle_rate(target_s, threads):
+    """Pick a sample that takes about target_s seconds; return (tokens/s
+    scaled to the whole request's layers x heads, seconds, description)."""
+    heads = max(1, min(WORKLOAD["H"], threads))
+    inp, skip = oracle_sample(heads, 1)
+    t0 = time.time()
+    run_oracle_sample(inp, skip, threads)
+    per_tok = (time.time() - t0) / float(inp["cu_seqlens"][-1])
+    lengths = np.diff(oracle_sample(1, 80)[0]["cu_seqlens"])
+    n_seg = int(np.clip(np.searchsorted(np.cumsum(lengths), target_s / max(per_tok, 1e-9)) + 1, 2, len(lengths)))
+    inp, skip = oracle_sample(heads, n_seg)
+    t0 = time.time()
+    run_oracle_sample(inp, skip, threads)
+    secs = time.time() - t0
+    toks = float(inp["cu_seqlens"][-1])
+    rate = toks * heads / secs / (WORKLOAD["n_layers"] * WORKLOAD["H"])
+    desc = (f"layer 0 of 30, heads 0-{heads - 1} of 32, first {n_seg} segments ({int(toks)} tokens): build, "
+            f"seam advance and compose in fp64; rate scaled to all 30x32 layer-heads")
+    return rate, secs, desc
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(n_seg=None):
+    W = WORKLOAD
+    return {"workload": (f"long cold request + seam: {W['n_layers']} GDN layers x {W['H']} heads, d={W['d']}, "
+                         f"bf16 k/v/q, fp32 gates/state, {W['n_tokens']} tokens in "
+                         f"{n_seg if n_seg else '~78'} segments of U[512,2048] tokens, "
+                         f"{W['seam_w']}-token seam at each internal segment start"),
+            "n_layers": W["n_layers"], "n_heads": W["H"], "d": W["d"], "n_tokens": W["n_tokens"],
+            "n_segments": n_seg, "seam_w": W["seam_w"],
+            "l2": "inputs ~50 GB resident, far above the 129 MB L2: no flush between steps",
+            "parallelism": "one independent request per GPU (replicas, no collective)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    threads = os.cpu_count() or 1
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rate0, secs, desc = oracle_rate(2.0, threads)
+        inp, skip = oracle_sample(max(1, min(WORKLOAD["H"], threads)), int(desc.split("first ")[1].split()[0]))
+        for _ in range(args.warmup):
+            run_oracle_sample(inp, skip, threads)
+        t0 = time.time()
+        for _ in range(args.steps):
+            run_oracle_sample(inp, skip, threads)
+        el = time.time() - t0
+        heads = inp["k"].shape[2]
+        rate = float(inp["cu_seqlens"][-1]) * heads * args.steps / el / (WORKLOAD["n_layers"] * WORKLOAD["H"])
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_config(),
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    res = time_our_arm(args, rank, world, device)
+    req = res.pop("req")
+    peaks, peak_src = load_peaks()
+    W = WORKLOAD
+    ms_step = res["ms"] / args.steps
+    LH = W["n_layers"] * W["H"]
+    value = world * W["n_tokens"] * args.steps / (res["ms"] / 1e3)
+    build_flop = res["body_tokens"] * LH * FLOP_PER_TOKEN_HEAD
+    build_tflops = build_flop / (res["build_ms"] / 1e3) / 1e12
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    n_comp = res["n_seg"]
+    chain_bytes = n_comp * LH * COMPOSE_BYTES + (res["n_seg"] - 1) * LH * SEAM_STATE_BYTES
+    chain_gbs = chain_bytes / (res["chain_ms"] / 1e3) / 1e9
+    e2e = None
+    if args.e2e_steps > 0:
+        try:
+            e = e2e_our_arm(req, args.e2e_steps)
+            e2e = {"value": world * W["n_tokens"] / (e["ms"] / 1e3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e["ms"],
+                   "steps": args.e2e_steps}
+        except Exception as ex:  # pinned host memory can be unavailable; report why
+            e2e = {"value": None, "unit": "tokens/s", "error": f"{type(ex).__name__}: {ex}"[:200]}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, secs, desc = oracle_rate(15.0, threads)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": round(secs, 2)}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, drawn on the device)",
+        "config": workload_config(res["n_seg"]),
+        "composes_per_s": world * n_comp * args.steps / (res["ms"] / 1e3),
+        "head_composes_per_s": world * n_comp * LH * args.steps / (res["ms"] / 1e3),
+        "phases": {"build_ms": res["build_ms"], "build_tflops": build_tflops,
+                   "chain_ms": res["chain_ms"], "chain_gbs_algorithmic": chain_gbs,
+                   "chain_frac_hbm": chain_gbs / peaks["hbm_gbs"]},
+        "roofline": {"kernel": "segment build (GDN)", "bound": "tensor", "achieved": build_tflops,
+                     "peak": peak_t, "unit": "TFLOP/s", "frac": build_tflops / peak_t, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained", "flop_per_token_head": FLOP_PER_TOKEN_HEAD},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": res["launches"], "clocks": res["clocks"],
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

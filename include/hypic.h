@@ -1,0 +1,236 @@
+/*
+ * hypic.h -- C ABI of libhypic.so, the GB300 (sm_103a) library for the
+ * linear-attention state path of HYPIC (position-independent caching for
+ * hybrid-attention LLMs).
+ *
+ * Sources (web pages on HYPIC):
+ *   [README]  "HYPIC: Accelerating Hybrid-Attention LLM Serving with
+ *             Position-Independent Caching", repository README: section "Key
+ *             techniques" (cached transition, seam window) and section "PIC
+ *             modes" (addition / transition modes, PIC_SEAM_SINK width knob).
+ *   [AIBASE]  aibase news article on HYPIC (Traditional Chinese): the
+ *             paragraph on the linear layers (segment-cumulative transition
+ *             operator T_C, zero-start end state S(C|0), composition law
+ *             S(C1.C2) = T(C2) S(C1) + S(C2)) and the paragraph on the
+ *             full-attention layers (seam window of w tokens at each internal
+ *             segment start, default w = 8, not cached; at reuse its own T and S
+ *             are computed on the fly while the running state advances and each
+ *             seam token's output is emitted).
+ *   [ARXIV]   arXiv 2607.01299 abstract: near-exact, constant-time composition
+ *             of independently cached segments.
+ *
+ * Families and per-token recurrences (state S is dk x dv, left-multiplied,
+ * latest token leftmost; the four families are among those the [AIBASE]
+ * linear-layer paragraph names):
+ *   HYPIC_GDN      S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T
+ *                  (gated delta rule); T_C is a dense dk x dk matrix.
+ *   HYPIC_RETNET   S_t = g S_{t-1} + k_t v_t^T;  T_C = g^L (a scalar).
+ *   HYPIC_GLA      S_t = Diag(g_t) S_{t-1} + k_t v_t^T;  T_C = prod g_t (dk-vector).
+ *   HYPIC_VANILLA  S_t = S_{t-1} + k_t v_t^T;  T_C = I (not stored).
+ *   Seam outputs: o_t = S_t^T q_t, with S_t the state after token t's write.
+ *
+ * Conventions common to every call
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, except the
+ *     arguments whose name ends in _host, which are host pointers read during
+ *     the call only.  The library allocates no memory; scratch memory comes
+ *     from the caller (see hypic_build_workspace_size).
+ *   - Layouts are dense row-major, innermost dimension last; every tensor
+ *     pointer must be 16-byte aligned.
+ *       k, v, q        [n_layers][n_tokens][n_heads][dk | dv]   (f32 or bf16)
+ *       alpha, beta    [n_layers][n_tokens][n_heads]             (f32)
+ *       gamma          [n_layers][n_heads]                       (f32)
+ *       g              [n_layers][n_tokens][n_heads][dk]         (f32)
+ *       per-item state [n_items][n_layers][n_heads][dk][dv]      (f32)
+ *   - Calls are asynchronous on the given stream and the library keeps no
+ *     state between calls (except the device error word, below); distinct
+ *     threads may call concurrently.
+ *   - Every argument is checked on the host before anything is launched; a
+ *     rejected call returns HYPIC_ERR_INVALID_ARG or HYPIC_ERR_UNSUPPORTED
+ *     and touches no output.  hypic_last_error_detail() then says why.
+ *   - A launch failure returns HYPIC_ERR_CUDA.  Kernels that wait on
+ *     asynchronous copies bound every wait; a wait that runs out sets the
+ *     device error word, which hypic_check_device() reports as
+ *     HYPIC_ERR_TIMEOUT.
+ *   - A zero-length segment (or body) yields the identity pair (T = I, S = 0).
+ *   - The library neither normalises k nor scales q.
+ */
+#ifndef HYPIC_H_
+#define HYPIC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HYPIC_VERSION 100 /* 1.0.0 */
+
+#if defined(__GNUC__)
+#define HYPIC_API __attribute__((visibility("default")))
+#else
+#define HYPIC_API
+#endif
+
+typedef struct CUstream_st* hypic_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    HYPIC_OK = 0,
+    HYPIC_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad offsets */
+    HYPIC_ERR_UNSUPPORTED = 2, /* valid but not implemented (family x dtype x dims) */
+    HYPIC_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    HYPIC_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+    HYPIC_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out */
+} hypic_status;
+
+typedef enum { HYPIC_GDN = 0, HYPIC_RETNET = 1, HYPIC_GLA = 2, HYPIC_VANILLA = 3 } hypic_family;
+typedef enum { HYPIC_F32 = 0, HYPIC_BF16 = 1 } hypic_dtype;
+
+/* ------------------------------------------------------------------ build --
+ * Cached pair (T_C, S(C|0)) of every (segment, layer, head) of a ragged batch
+ * ([AIBASE] linear-layer paragraph; [README] "Key techniques", cached
+ * transition).  Segment s occupies tokens [cu_seqlens[s], cu_seqlens[s+1]) of
+ * the packed token arrays; its cached pair covers the body
+ * [cu_seqlens[s] + seam_skip[s], cu_seqlens[s+1]): the leading seam_skip[s]
+ * tokens are the seam window that is not cached ([AIBASE] full-attention
+ * paragraph).  seam_skip == NULL means 0 for every segment.
+ *
+ * Inputs by family (unused ones must be NULL):
+ *   GDN      k, v (in_dtype), alpha, beta (f32)
+ *   RETNET   k, v, gamma                       (beta must be NULL: b = 1)
+ *   GLA      k, v, g
+ *   VANILLA  k, v
+ * Outputs, leading dims [n_segments][n_layers][n_heads]:
+ *   S_out   [..][dk][dv] f32
+ *   T_out   GDN: [..][dk][dk] f32 mantissa, with T_exp_out [..] int32 such that
+ *           T_C = T_out * 2^T_exp_out (the exponent keeps T_C representable
+ *           when its entries fall below the f32 range, as they do for long
+ *           segments with strong decay); RETNET: [..] f32 scalar g^L;
+ *           GLA: [..][dk] f32 vector; VANILLA: NULL.
+ *   T_exp_out  GDN only (NULL otherwise).
+ * Supported: dk, dv in {16, 32, 64, 128}; GDN requires dk == dv.
+ * Work order: segments are processed longest body first (LPT order).
+ */
+typedef struct {
+    int family;                /* hypic_family */
+    int in_dtype;              /* hypic_dtype of k and v */
+    int n_layers, n_heads, dk, dv;
+    int n_segments;
+    int64_t n_tokens;          /* rows of the packed token arrays */
+    const int32_t* cu_seqlens;       /* device [n_segments+1], non-decreasing, 0 .. n_tokens */
+    const int32_t* cu_seqlens_host;  /* host copy of the same (validation, planning) */
+    const int32_t* seam_skip;        /* device [n_segments] or NULL */
+    const int32_t* seam_skip_host;   /* host copy or NULL (must match seam_skip) */
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const float* gamma;
+    const float* g;
+    float* T_out;
+    int32_t* T_exp_out;
+    float* S_out;
+} hypic_build_args;
+
+/* Bytes of device scratch the build needs for these arguments (plan and
+   work counter).  Returns 0 when the arguments are invalid. */
+HYPIC_API size_t hypic_build_workspace_size(const hypic_build_args* args);
+
+/* Launch the build on `stream`.  `workspace` is device memory of at least
+   hypic_build_workspace_size(args) bytes, 256-byte aligned, owned by the
+   caller and not used by any other call until this one completes on the
+   stream.  Returns HYPIC_ERR_WORKSPACE when it is NULL or too small. */
+HYPIC_API hypic_status hypic_segment_build(const hypic_build_args* args, void* workspace,
+                                 size_t workspace_bytes, hypic_stream_t stream);
+
+/* ---------------------------------------------------------------- compose --
+ * Chain composition of cached pairs ([AIBASE] linear-layer paragraph:
+ * S(C1.C2) = T(C2) S(C1) + S(C2); [ARXIV] constant-time composition).  For
+ * chain r and every (layer, head): S <- S0[r] (or 0 when S0 == NULL), then
+ * S <- T_p S + S_p for p = seg_idx[cu_chain[r]], ..., seg_idx[cu_chain[r+1]-1]
+ * in that order; S_out[r] <- S.  A chain of length 0 copies its start state.
+ * T_p S is a dk x dk matrix product (GDN, with T_p = T_tab * 2^T_exp_tab;
+ * T_exp_tab == NULL means exponent 0), a scalar (RETNET), a row scaling (GLA)
+ * or the identity (VANILLA: plain addition, T_tab must be NULL).
+ * Pair tables (the build's outputs, or any cache of them):
+ *   T_tab [n_pairs][n_layers][n_heads](...) as T_out above; S_tab
+ *   [n_pairs][n_layers][n_heads][dk][dv].
+ * S_out [n_chains][n_layers][n_heads][dk][dv] must not overlap the tables or S0.
+ * Supported: dk, dv in {16, 32, 64, 128}; GDN requires dk == dv.
+ */
+typedef struct {
+    int family;
+    int n_layers, n_heads, dk, dv;
+    int n_pairs;
+    const float* T_tab;
+    const int32_t* T_exp_tab;
+    const float* S_tab;
+    int n_chains;
+    const int32_t* cu_chain;        /* device [n_chains+1], non-decreasing from 0 */
+    const int32_t* cu_chain_host;   /* host copy */
+    const int32_t* seg_idx;         /* device [cu_chain[n_chains]], each in [0, n_pairs) */
+    const int32_t* seg_idx_host;    /* host copy (validation) */
+    const float* S0;                /* device [n_chains][..] or NULL */
+    float* S_out;
+} hypic_compose_args;
+
+HYPIC_API hypic_status hypic_compose(const hypic_compose_args* args, hypic_stream_t stream);
+
+/* ------------------------------------------------------------------- seam --
+ * Seam-window advance ([AIBASE] full-attention paragraph; [README] "PIC
+ * modes", seam width PIC_SEAM_SINK, default 8).  For seam r and every
+ * (layer, head): S <- state_in[r] (or 0 when state_in == NULL), then for each
+ * token t in [cu_seam[r], cu_seam[r+1]) of the packed seam-token arrays:
+ * advance S by the family's recurrence and write o_out[layer][t][head] =
+ * S_t^T q_t; finally state_out[r] <- S.  The fraction-to-count mapping of the
+ * width knob is the caller's; the library takes explicit token ranges.
+ * Inputs: q, k (in_dtype) [n_layers][n_tokens][n_heads][dk], v [..][dv] and the
+ * family's gates as for the build (over the seam tokens).
+ * state_in, state_out [n_seams][n_layers][n_heads][dk][dv] f32; they may be
+ * the same buffer (in-place advance) but must not otherwise overlap.
+ * o_out [n_layers][n_tokens][n_heads][dv] f32.
+ * Supported: dk, dv in {16, 32, 64, 128}.
+ */
+typedef struct {
+    int family;
+    int in_dtype;
+    int n_layers, n_heads, dk, dv;
+    int n_seams;
+    int64_t n_tokens;
+    const int32_t* cu_seam;         /* device [n_seams+1], non-decreasing from 0 to n_tokens */
+    const int32_t* cu_seam_host;    /* host copy */
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const float* gamma;
+    const float* g;
+    const float* state_in;
+    float* state_out;
+    float* o_out;
+} hypic_seam_args;
+
+HYPIC_API hypic_status hypic_seam_advance(const hypic_seam_args* args, hypic_stream_t stream);
+
+/* ------------------------------------------------------------------ misc -- */
+
+/* Static, never NULL. */
+HYPIC_API const char* hypic_status_string(hypic_status status);
+
+/* Detail of the last error returned on the calling thread (thread-local,
+   overwritten by the next failing call). */
+HYPIC_API const char* hypic_last_error_detail(void);
+
+/* HYPIC_VERSION of the loaded library. */
+HYPIC_API int hypic_version(void);
+
+/* Synchronise `stream`, then read and clear the current device's error word:
+   HYPIC_ERR_TIMEOUT when a bounded device wait ran out since the last check,
+   HYPIC_ERR_CUDA when the stream reports an error, else HYPIC_OK. */
+HYPIC_API hypic_status hypic_check_device(hypic_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HYPIC_H_ */

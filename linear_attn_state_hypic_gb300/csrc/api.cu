@@ -1,0 +1,403 @@
+// api.cu -- the C ABI of libhypic.so (declared in include/hypic.h): host-side
+// argument checks, work dispatch and error reporting.  No call allocates
+// memory; all checks happen before the first launch.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/hypic.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace hypic {
+cudaError_t launch_compose_simt(const ComposeParams& p, unsigned* err, cudaStream_t s);
+cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_t s);
+bool compose_tc_supported(const ComposeParams& p);
+}  // namespace hypic
+
+using namespace hypic;
+
+// Device error word: set (first writer wins) by kernels whose bounded waits
+// ran out; read and cleared by hypic_check_device().
+__device__ unsigned g_hypic_err_word;
+
+namespace {
+
+thread_local char t_detail[512] = "";
+
+hypic_status fail(hypic_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_detail, sizeof(t_detail), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+hypic_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(HYPIC_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Address of the device error word on the current device (looked up once per
+// device; host code cannot take the address of a __device__ variable itself).
+unsigned* err_word(cudaError_t* e_out) {
+    static std::mutex mu;
+    static unsigned* cache[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 128) {
+        *e_out = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_hypic_err_word);
+        if (e != cudaSuccess) {
+            *e_out = e;
+            return nullptr;
+        }
+        cache[dev] = static_cast<unsigned*>(p);
+    }
+    *e_out = cudaSuccess;
+    return cache[dev];
+}
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [a, a + na) and [b, b + nb) (bytes) share a byte.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+const char* fam_name(int f) {
+    static const char* n[] = {"GDN", "RETNET", "GLA", "VANILLA"};
+    return (f >= 0 && f <= 3) ? n[f] : "?";
+}
+
+// Checks shared by the three calls: family, dtype, dims and the family's
+// gate pointers.  `has_tokens` is false when no token is read.
+hypic_status check_family(int family, int in_dtype, int n_layers, int n_heads, int dk, int dv, bool has_tokens,
+                          const float* alpha, const float* beta, const float* gamma, const float* g,
+                          bool check_dtype) {
+    if (family < HYPIC_GDN || family > HYPIC_VANILLA) return fail(HYPIC_ERR_INVALID_ARG, "family %d", family);
+    if (check_dtype && in_dtype != HYPIC_F32 && in_dtype != HYPIC_BF16)
+        return fail(HYPIC_ERR_INVALID_ARG, "in_dtype %d", in_dtype);
+    if (n_layers < 1 || n_heads < 1) return fail(HYPIC_ERR_INVALID_ARG, "n_layers %d n_heads %d", n_layers, n_heads);
+    if (dk < 1 || dv < 1) return fail(HYPIC_ERR_INVALID_ARG, "dk %d dv %d", dk, dv);
+    if (!dim_ok(dk) || !dim_ok(dv))
+        return fail(HYPIC_ERR_UNSUPPORTED, "dk %d dv %d (supported: 16, 32, 64, 128)", dk, dv);
+    if (family == HYPIC_GDN && dk != dv) return fail(HYPIC_ERR_UNSUPPORTED, "GDN needs dk == dv (%d, %d)", dk, dv);
+    const bool want_ab = family == HYPIC_GDN, want_gamma = family == HYPIC_RETNET, want_g = family == HYPIC_GLA;
+    if (!want_ab && (alpha || beta))
+        return fail(HYPIC_ERR_INVALID_ARG, "alpha/beta must be NULL for %s", fam_name(family));
+    if (!want_gamma && gamma) return fail(HYPIC_ERR_INVALID_ARG, "gamma must be NULL for %s", fam_name(family));
+    if (!want_g && g) return fail(HYPIC_ERR_INVALID_ARG, "g must be NULL for %s", fam_name(family));
+    if (want_gamma && !gamma) return fail(HYPIC_ERR_INVALID_ARG, "RETNET needs gamma");
+    if (has_tokens) {
+        if (want_ab && (!alpha || !beta)) return fail(HYPIC_ERR_INVALID_ARG, "GDN needs alpha and beta");
+        if (want_g && !g) return fail(HYPIC_ERR_INVALID_ARG, "GLA needs g");
+    }
+    const void* ptrs[] = {alpha, beta, gamma, g};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return fail(HYPIC_ERR_INVALID_ARG, "gate pointer %p not 16-byte aligned", q);
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ build --
+
+namespace {
+
+hypic_status check_build(const hypic_build_args* a) {
+    if (!a) return fail(HYPIC_ERR_INVALID_ARG, "args is NULL");
+    if (a->n_segments < 0) return fail(HYPIC_ERR_INVALID_ARG, "n_segments %d", a->n_segments);
+    if (a->n_tokens < 0 || a->n_tokens > INT32_MAX)
+        return fail(HYPIC_ERR_INVALID_ARG, "n_tokens %lld", (long long)a->n_tokens);
+    if (!a->cu_seqlens || !a->cu_seqlens_host) return fail(HYPIC_ERR_INVALID_ARG, "cu_seqlens (device and host) required");
+    if ((a->seam_skip == nullptr) != (a->seam_skip_host == nullptr))
+        return fail(HYPIC_ERR_INVALID_ARG, "seam_skip and seam_skip_host must both be set or both NULL");
+    const int32_t* cu = a->cu_seqlens_host;
+    if (cu[0] < 0) return fail(HYPIC_ERR_INVALID_ARG, "cu_seqlens[0] = %d", cu[0]);
+    for (int s = 0; s < a->n_segments; ++s) {
+        if (cu[s + 1] < cu[s]) return fail(HYPIC_ERR_INVALID_ARG, "cu_seqlens decreases at %d", s);
+        if (a->seam_skip_host) {
+            const int sk = a->seam_skip_host[s];
+            if (sk < 0 || sk > cu[s + 1] - cu[s])
+                return fail(HYPIC_ERR_INVALID_ARG, "seam_skip[%d] = %d outside [0, %d]", s, sk, cu[s + 1] - cu[s]);
+        }
+    }
+    if ((int64_t)cu[a->n_segments] > a->n_tokens)
+        return fail(HYPIC_ERR_INVALID_ARG, "cu_seqlens[n_segments] = %d > n_tokens %lld", cu[a->n_segments],
+                    (long long)a->n_tokens);
+    const bool has_tokens = cu[a->n_segments] > cu[0];
+    hypic_status st = check_family(a->family, a->in_dtype, a->n_layers, a->n_heads, a->dk, a->dv, has_tokens, a->alpha,
+                                   a->beta, a->gamma, a->g, true);
+    if (st != HYPIC_OK) return st;
+    if (a->family == HYPIC_RETNET || a->family == HYPIC_GLA || a->family == HYPIC_VANILLA) {
+        if (a->beta) return fail(HYPIC_ERR_INVALID_ARG, "beta must be NULL for %s", fam_name(a->family));
+    }
+    if (has_tokens && (!a->k || !a->v)) return fail(HYPIC_ERR_INVALID_ARG, "k and v required");
+    const bool any = a->n_segments > 0;
+    if (any && !a->S_out) return fail(HYPIC_ERR_INVALID_ARG, "S_out required");
+    const bool want_T = a->family != HYPIC_VANILLA, want_exp = a->family == HYPIC_GDN;
+    if (!want_T && a->T_out) return fail(HYPIC_ERR_INVALID_ARG, "T_out must be NULL for VANILLA");
+    if (!want_exp && a->T_exp_out) return fail(HYPIC_ERR_INVALID_ARG, "T_exp_out must be NULL for %s", fam_name(a->family));
+    if (any && want_T && !a->T_out) return fail(HYPIC_ERR_INVALID_ARG, "T_out required for %s", fam_name(a->family));
+    if (any && want_exp && !a->T_exp_out) return fail(HYPIC_ERR_INVALID_ARG, "T_exp_out required for GDN");
+    const void* ptrs[] = {a->k, a->v, a->T_out, a->T_exp_out, a->S_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    return HYPIC_OK;
+}
+
+BuildParams to_params(const hypic_build_args* a) {
+    BuildParams p;
+    p.family = a->family;
+    p.in_dtype = a->in_dtype;
+    p.n_layers = a->n_layers;
+    p.n_heads = a->n_heads;
+    p.dk = a->dk;
+    p.dv = a->dv;
+    p.n_seg = a->n_segments;
+    p.n_tokens = a->n_tokens;
+    p.cu = a->cu_seqlens;
+    p.skip = a->seam_skip;
+    p.k = a->k;
+    p.v = a->v;
+    p.alpha = a->alpha;
+    p.beta = a->beta;
+    p.gamma = a->gamma;
+    p.g = a->g;
+    p.T_out = a->T_out;
+    p.T_exp = a->T_exp_out;
+    p.S_out = a->S_out;
+    return p;
+}
+
+}  // namespace
+
+extern "C" size_t hypic_build_workspace_size(const hypic_build_args* args) {
+    if (check_build(args) != HYPIC_OK) return 0;
+    return build_workspace_bytes(args->n_segments);
+}
+
+extern "C" hypic_status hypic_segment_build(const hypic_build_args* args, void* workspace, size_t workspace_bytes,
+                                            hypic_stream_t stream) {
+    hypic_status st = check_build(args);
+    if (st != HYPIC_OK) return st;
+    if (args->n_segments == 0) return HYPIC_OK;
+    const size_t need = build_workspace_bytes(args->n_segments);
+    if (!workspace || workspace_bytes < need)
+        return fail(HYPIC_ERR_WORKSPACE, "workspace %p of %zu bytes, need %zu", workspace, workspace_bytes, need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(HYPIC_ERR_WORKSPACE, "workspace %p not 256-byte aligned", workspace);
+    cudaError_t e;
+    unsigned* err = err_word(&e);
+    if (!err) return cuda_fail(e, "device error word");
+    const BuildParams p = to_params(args);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = launch_build_plan(p, workspace, s);
+    if (e != cudaSuccess) return cuda_fail(e, "build plan launch");
+    if (gdn_build_tc_supported(p)) {
+        e = launch_gdn_build_tc(p, workspace, err, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core build launch");
+    } else {
+        e = launch_build_simt(p, workspace, err, s);
+        if (e != cudaSuccess) return cuda_fail(e, "build launch");
+    }
+    return HYPIC_OK;
+}
+
+// ---------------------------------------------------------------- compose --
+
+namespace {
+
+size_t T_bytes_per_obj(int family, int dk) {
+    switch (family) {
+        case HYPIC_GDN: return sizeof(float) * (size_t)dk * dk;
+        case HYPIC_RETNET: return sizeof(float);
+        case HYPIC_GLA: return sizeof(float) * (size_t)dk;
+    }
+    return 0;
+}
+
+hypic_status check_compose(const hypic_compose_args* a) {
+    if (!a) return fail(HYPIC_ERR_INVALID_ARG, "args is NULL");
+    if (a->n_pairs < 0 || a->n_chains < 0)
+        return fail(HYPIC_ERR_INVALID_ARG, "n_pairs %d n_chains %d", a->n_pairs, a->n_chains);
+    hypic_status st = check_family(a->family, 0, a->n_layers, a->n_heads, a->dk, a->dv, false, nullptr, nullptr,
+                                   nullptr, nullptr, false);
+    if (st != HYPIC_OK) return st;
+    if (!a->cu_chain || !a->cu_chain_host) return fail(HYPIC_ERR_INVALID_ARG, "cu_chain (device and host) required");
+    const int32_t* cu = a->cu_chain_host;
+    if (cu[0] != 0) return fail(HYPIC_ERR_INVALID_ARG, "cu_chain[0] = %d (must be 0)", cu[0]);
+    for (int r = 0; r < a->n_chains; ++r)
+        if (cu[r + 1] < cu[r]) return fail(HYPIC_ERR_INVALID_ARG, "cu_chain decreases at %d", r);
+    const int total = cu[a->n_chains];
+    if (total > 0) {
+        if (!a->seg_idx || !a->seg_idx_host) return fail(HYPIC_ERR_INVALID_ARG, "seg_idx (device and host) required");
+        for (int j = 0; j < total; ++j)
+            if (a->seg_idx_host[j] < 0 || a->seg_idx_host[j] >= a->n_pairs)
+                return fail(HYPIC_ERR_INVALID_ARG, "seg_idx[%d] = %d outside [0, %d)", j, a->seg_idx_host[j], a->n_pairs);
+        if (!a->S_tab) return fail(HYPIC_ERR_INVALID_ARG, "S_tab required");
+        if (a->family != HYPIC_VANILLA && !a->T_tab) return fail(HYPIC_ERR_INVALID_ARG, "T_tab required for %s", fam_name(a->family));
+    }
+    if (a->family == HYPIC_VANILLA && a->T_tab) return fail(HYPIC_ERR_INVALID_ARG, "T_tab must be NULL for VANILLA");
+    if (a->family != HYPIC_GDN && a->T_exp_tab) return fail(HYPIC_ERR_INVALID_ARG, "T_exp_tab must be NULL for %s", fam_name(a->family));
+    if (a->n_chains > 0 && !a->S_out) return fail(HYPIC_ERR_INVALID_ARG, "S_out required");
+    const void* ptrs[] = {a->T_tab, a->T_exp_tab, a->S_tab, a->S0, a->S_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    const size_t LH = (size_t)a->n_layers * a->n_heads;
+    const size_t state = sizeof(float) * (size_t)a->dk * a->dv * LH;
+    const size_t out_b = state * a->n_chains;
+    if (overlap(a->S_out, out_b, a->S_tab, state * a->n_pairs) ||
+        overlap(a->S_out, out_b, a->T_tab, T_bytes_per_obj(a->family, a->dk) * LH * a->n_pairs) ||
+        overlap(a->S_out, out_b, a->T_exp_tab, sizeof(int32_t) * LH * a->n_pairs) ||
+        overlap(a->S_out, out_b, a->S0, out_b))
+        return fail(HYPIC_ERR_INVALID_ARG, "S_out overlaps an input");
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" hypic_status hypic_compose(const hypic_compose_args* args, hypic_stream_t stream) {
+    hypic_status st = check_compose(args);
+    if (st != HYPIC_OK) return st;
+    if (args->n_chains == 0) return HYPIC_OK;
+    cudaError_t e;
+    unsigned* err = err_word(&e);
+    if (!err) return cuda_fail(e, "device error word");
+    ComposeParams p;
+    p.family = args->family;
+    p.n_layers = args->n_layers;
+    p.n_heads = args->n_heads;
+    p.dk = args->dk;
+    p.dv = args->dv;
+    p.n_pairs = args->n_pairs;
+    p.n_chains = args->n_chains;
+    p.T_tab = args->T_tab;
+    p.T_exp_tab = args->T_exp_tab;
+    p.S_tab = args->S_tab;
+    p.cu_chain = args->cu_chain;
+    p.seg_idx = args->seg_idx;
+    p.S0 = args->S0;
+    p.S_out = args->S_out;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = compose_tc_supported(p) ? launch_compose_tc(p, err, s) : launch_compose_simt(p, err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "compose launch");
+    return HYPIC_OK;
+}
+
+// ------------------------------------------------------------------- seam --
+
+namespace {
+
+hypic_status check_seam(const hypic_seam_args* a) {
+    if (!a) return fail(HYPIC_ERR_INVALID_ARG, "args is NULL");
+    if (a->n_seams < 0) return fail(HYPIC_ERR_INVALID_ARG, "n_seams %d", a->n_seams);
+    if (a->n_tokens < 0 || a->n_tokens > INT32_MAX)
+        return fail(HYPIC_ERR_INVALID_ARG, "n_tokens %lld", (long long)a->n_tokens);
+    if (!a->cu_seam || !a->cu_seam_host) return fail(HYPIC_ERR_INVALID_ARG, "cu_seam (device and host) required");
+    const int32_t* cu = a->cu_seam_host;
+    if (cu[0] != 0) return fail(HYPIC_ERR_INVALID_ARG, "cu_seam[0] = %d (must be 0)", cu[0]);
+    for (int r = 0; r < a->n_seams; ++r)
+        if (cu[r + 1] < cu[r]) return fail(HYPIC_ERR_INVALID_ARG, "cu_seam decreases at %d", r);
+    if ((int64_t)cu[a->n_seams] != a->n_tokens)
+        return fail(HYPIC_ERR_INVALID_ARG, "cu_seam[n_seams] = %d != n_tokens %lld", cu[a->n_seams], (long long)a->n_tokens);
+    const bool has_tokens = a->n_tokens > 0;
+    hypic_status st = check_family(a->family, a->in_dtype, a->n_layers, a->n_heads, a->dk, a->dv, has_tokens, a->alpha,
+                                   a->beta, a->gamma, a->g, true);
+    if (st != HYPIC_OK) return st;
+    if (has_tokens && (!a->q || !a->k || !a->v || !a->o_out))
+        return fail(HYPIC_ERR_INVALID_ARG, "q, k, v and o_out required");
+    if (a->n_seams > 0 && !a->state_out) return fail(HYPIC_ERR_INVALID_ARG, "state_out required");
+    const void* ptrs[] = {a->q, a->k, a->v, a->state_in, a->state_out, a->o_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    const size_t state = sizeof(float) * (size_t)a->dk * a->dv * a->n_layers * a->n_heads * a->n_seams;
+    const size_t o_b = sizeof(float) * (size_t)a->n_layers * a->n_tokens * a->n_heads * a->dv;
+    if (a->state_in != a->state_out && overlap(a->state_in, state, a->state_out, state))
+        return fail(HYPIC_ERR_INVALID_ARG, "state_in and state_out partially overlap");
+    if (overlap(a->o_out, o_b, a->state_out, state) || overlap(a->o_out, o_b, a->state_in, state))
+        return fail(HYPIC_ERR_INVALID_ARG, "o_out overlaps a state buffer");
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" hypic_status hypic_seam_advance(const hypic_seam_args* args, hypic_stream_t stream) {
+    hypic_status st = check_seam(args);
+    if (st != HYPIC_OK) return st;
+    if (args->n_seams == 0) return HYPIC_OK;
+    cudaError_t e;
+    unsigned* err = err_word(&e);
+    if (!err) return cuda_fail(e, "device error word");
+    SeamParams p;
+    p.family = args->family;
+    p.in_dtype = args->in_dtype;
+    p.n_layers = args->n_layers;
+    p.n_heads = args->n_heads;
+    p.dk = args->dk;
+    p.dv = args->dv;
+    p.n_seams = args->n_seams;
+    p.n_tokens = args->n_tokens;
+    p.cu_seam = args->cu_seam;
+    p.q = args->q;
+    p.k = args->k;
+    p.v = args->v;
+    p.alpha = args->alpha;
+    p.beta = args->beta;
+    p.gamma = args->gamma;
+    p.g = args->g;
+    p.state_in = args->state_in;
+    p.state_out = args->state_out;
+    p.o_out = args->o_out;
+    e = launch_seam(p, err, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "seam launch");
+    return HYPIC_OK;
+}
+
+// ------------------------------------------------------------------- misc --
+
+extern "C" const char* hypic_status_string(hypic_status s) {
+    switch (s) {
+        case HYPIC_OK: return "HYPIC_OK";
+        case HYPIC_ERR_INVALID_ARG: return "HYPIC_ERR_INVALID_ARG";
+        case HYPIC_ERR_UNSUPPORTED: return "HYPIC_ERR_UNSUPPORTED";
+        case HYPIC_ERR_WORKSPACE: return "HYPIC_ERR_WORKSPACE";
+        case HYPIC_ERR_CUDA: return "HYPIC_ERR_CUDA";
+        case HYPIC_ERR_TIMEOUT: return "HYPIC_ERR_TIMEOUT";
+    }
+    return "HYPIC_ERR_UNKNOWN";
+}
+
+extern "C" const char* hypic_last_error_detail(void) { return t_detail; }
+
+extern "C" int hypic_version(void) { return HYPIC_VERSION; }
+
+extern "C" hypic_status hypic_check_device(hypic_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned* w = err_word(&e);
+    if (!w) return cuda_fail(e, "device error word");
+    unsigned v = 0;
+    e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (v != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        if (v == kErrTimeout) return fail(HYPIC_ERR_TIMEOUT, "a bounded device wait ran out");
+        return fail(HYPIC_ERR_INVALID_ARG, "device-side index check failed (code %u)", v);
+    }
+    return HYPIC_OK;
+}

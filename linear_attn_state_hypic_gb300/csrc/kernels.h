@@ -1,0 +1,70 @@
+// kernels.h -- internal interface between the C ABI (api.cu) and the kernels.
+// Arguments reaching these launchers have already been validated on the host.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hypic {
+
+struct BuildParams {
+    int family, in_dtype, n_layers, n_heads, dk, dv, n_seg;
+    int64_t n_tokens;
+    const int32_t* cu;    // [n_seg+1]
+    const int32_t* skip;  // [n_seg] or null
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const float* gamma;
+    const float* g;
+    float* T_out;
+    int32_t* T_exp;
+    float* S_out;
+};
+
+struct ComposeParams {
+    int family, n_layers, n_heads, dk, dv, n_pairs, n_chains;
+    const float* T_tab;
+    const int32_t* T_exp_tab;
+    const float* S_tab;
+    const int32_t* cu_chain;
+    const int32_t* seg_idx;
+    const float* S0;
+    float* S_out;
+};
+
+struct SeamParams {
+    int family, in_dtype, n_layers, n_heads, dk, dv, n_seams;
+    int64_t n_tokens;
+    const int32_t* cu_seam;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const float* gamma;
+    const float* g;
+    const float* state_in;
+    float* state_out;
+    float* o_out;
+};
+
+// Workspace layout of the build: [order: n_seg int32][pad to 256 B][counter: 256 B].
+size_t build_workspace_bytes(int n_seg);
+
+// Sort segments by body length, longest first (ties: lower index first), into
+// `order`, and zero the work counter.
+cudaError_t launch_build_plan(const BuildParams& p, void* workspace, cudaStream_t s);
+
+// Token-loop build on CUDA cores (every family, every supported d).
+cudaError_t launch_build_simt(const BuildParams& p, const void* workspace, unsigned* err, cudaStream_t s);
+
+// Chunked GDN build on the tensor cores (d = 128, bf16 k/v).  Returns
+// cudaErrorNotSupported when the shape is not covered.
+cudaError_t launch_gdn_build_tc(const BuildParams& p, void* workspace, unsigned* err, cudaStream_t s);
+bool gdn_build_tc_supported(const BuildParams& p);
+
+cudaError_t launch_compose(const ComposeParams& p, unsigned* err, cudaStream_t s);
+cudaError_t launch_seam(const SeamParams& p, unsigned* err, cudaStream_t s);
+
+}  // namespace hypic

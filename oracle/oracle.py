@@ -184,14 +184,17 @@ def rel_fro(x, ref, axes):
     """Relative Frobenius error ||x - ref|| / ||ref|| per object, in fp64.
 
     ``axes`` are the trailing axes that make up one object (e.g. (-2, -1) for a
-    d x d matrix).  Where ||ref|| is below 1e-30 the absolute error is
-    returned instead.
+    d x d matrix).  The error is relative however small ||ref|| is (a T_C of
+    1e-140 is compared at its own scale); only where ref is exactly zero is
+    the absolute error returned.
     """
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    num = np.sqrt(np.sum((x - ref) ** 2, axis=axes))
-    den = np.sqrt(np.sum(ref ** 2, axis=axes))
-    return np.where(den < 1e-30, num, num / np.where(den < 1e-30, 1.0, den))
+    scale = np.max(np.abs(ref), axis=axes, keepdims=True)
+    scale = np.where(scale > 0, scale, 1.0)
+    num = np.sqrt(np.sum(((x - ref) / scale) ** 2, axis=axes))
+    den = np.sqrt(np.sum((ref / scale) ** 2, axis=axes))
+    return np.where(den == 0, num, num / np.where(den == 0, 1.0, den))
 
 
 def scaled_to_f64(mant, exp):

@@ -1,0 +1,239 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/hypic.h declares, the ctypes structs match the header's layout (as
+compiled by gcc), and every host-side validation path returns its status
+before any CUDA call is made."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hypic.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from linear_attn_state_hypic_gb300 import build_lib
+    build_lib.build()
+    from linear_attn_state_hypic_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"HYPIC_API\s+[\w\s\*]+?\b(hypic_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_three_calls():
+    fns = declared_functions()
+    for f in ("hypic_segment_build", "hypic_compose", "hypic_seam_advance", "hypic_build_workspace_size"):
+        assert f in fns
+
+
+def test_library_exports_every_declared_symbol(B):
+    fns = declared_functions()
+    assert fns, "no declarations parsed"
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(hypic_\w+)", out))
+    assert set(fns) <= exported, set(fns) - exported
+    for f in fns:
+        getattr(B.lib, f)  # resolvable through ctypes
+    assert set(B.EXPORTS) == set(fns)
+
+
+def test_struct_layout_matches_header(B, tmp_path):
+    """Compile a probe against include/hypic.h with gcc and compare sizeof and
+    every field offset with the ctypes mirrors."""
+    structs = {"hypic_build_args": B.BuildArgs, "hypic_compose_args": B.ComposeArgs, "hypic_seam_args": B.SeamArgs}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "hypic.h"', "int main(void){"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0;}")
+    c = tmp_path / "probe.c"
+    c.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.check_call(["gcc", "-I", os.path.dirname(HEADER), str(c), "-o", str(exe)])
+    got = {}
+    for ln in subprocess.check_output([str(exe)], text=True).splitlines():
+        s, f, v = ln.split()
+        got[(s, f)] = int(v)
+    for cname, py in structs.items():
+        assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)
+
+
+def test_status_strings_and_version(B):
+    assert B.hypic_version() == 100
+    for code, name in enumerate(["HYPIC_OK", "HYPIC_ERR_INVALID_ARG", "HYPIC_ERR_UNSUPPORTED", "HYPIC_ERR_WORKSPACE",
+                                 "HYPIC_ERR_CUDA", "HYPIC_ERR_TIMEOUT"]):
+        assert B.lib.hypic_status_string(code).decode() == name
+
+
+# ------------------------------------------------ host validation (no GPU) --
+# Device pointers are fake but 16-byte aligned: validation never dereferences
+# them, and every case below is rejected before the first CUDA call.
+
+FAKE = 0x7F0000000000
+
+
+def fake(i):
+    return FAKE + 0x100000 * (i + 1)
+
+
+def base_build(B, family=0, d=128, n_seg=2, lengths=(64, 80)):
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    a = B.BuildArgs()
+    a.family, a.in_dtype, a.n_layers, a.n_heads, a.dk, a.dv = family, 1, 1, 2, d, d
+    a.n_segments, a.n_tokens = n_seg, int(cu[-1])
+    a.cu_seqlens, a.cu_seqlens_host = fake(0), cu.ctypes.data
+    a.k, a.v = fake(1), fake(2)
+    if family == 0:
+        a.alpha, a.beta = fake(3), fake(4)
+        a.T_exp_out = fake(6)
+    if family == 1:
+        a.gamma = fake(3)
+    if family == 2:
+        a.g = fake(3)
+    if family != 3:
+        a.T_out = fake(5)
+    a.S_out = fake(7)
+    return a, cu
+
+
+def run_build(B, a, ws=1 << 20, ws_ptr=None):
+    return B.hypic_segment_build(a, fake(9) if ws_ptr is None else ws_ptr, ws, None)
+
+
+def test_build_valid_args_reach_workspace_check(B):
+    for fam in range(4):
+        a, keep = base_build(B, fam)
+        need = B.hypic_build_workspace_size(a)
+        assert need >= 256
+        assert run_build(B, a, ws=need - 1) == B.ERR_WORKSPACE
+        assert run_build(B, a, ws_ptr=0) == B.ERR_WORKSPACE
+        assert run_build(B, a, ws_ptr=fake(9) + 16) == B.ERR_WORKSPACE  # not 256-byte aligned
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a, c: setattr(a, "family", 7), 1),
+    (lambda a, c: setattr(a, "in_dtype", 5), 1),
+    (lambda a, c: setattr(a, "dk", 96), 2),
+    (lambda a, c: (setattr(a, "dk", 64)), 2),          # GDN dk != dv
+    (lambda a, c: setattr(a, "n_heads", 0), 1),
+    (lambda a, c: setattr(a, "n_segments", -1), 1),
+    (lambda a, c: setattr(a, "n_tokens", 10), 1),       # cu_seqlens[-1] > n_tokens
+    (lambda a, c: c.__setitem__(1, 200), 1),            # non-monotone
+    (lambda a, c: setattr(a, "cu_seqlens_host", None), 1),
+    (lambda a, c: setattr(a, "k", None), 1),
+    (lambda a, c: setattr(a, "k", fake(1) + 8), 1),     # misaligned
+    (lambda a, c: setattr(a, "alpha", None), 1),
+    (lambda a, c: setattr(a, "gamma", fake(8)), 1),     # gamma given for GDN
+    (lambda a, c: setattr(a, "T_exp_out", None), 1),
+    (lambda a, c: setattr(a, "S_out", None), 1),
+    (lambda a, c: setattr(a, "seam_skip", fake(8)), 1), # device without host copy
+])
+def test_build_rejections(B, mutate, status):
+    a, cu = base_build(B)
+    mutate(a, cu)
+    assert run_build(B, a) == status
+    assert B.lib.hypic_last_error_detail().decode()
+    assert B.hypic_build_workspace_size(a) == 0
+
+
+def test_build_seam_skip_range(B):
+    a, cu = base_build(B)
+    sk = np.array([0, 81], np.int32)   # longer than the segment
+    a.seam_skip, a.seam_skip_host = fake(8), sk.ctypes.data
+    assert run_build(B, a) == B.ERR_INVALID_ARG
+    sk[1] = 80
+    assert run_build(B, a, ws=1) == B.ERR_WORKSPACE  # valid now; stops at the workspace
+
+
+def test_build_family_specific_rejections(B):
+    a, _ = base_build(B, 3)
+    a.T_out = fake(5)
+    assert run_build(B, a) == B.ERR_INVALID_ARG   # vanilla stores no T
+    a, _ = base_build(B, 1)
+    a.beta = fake(4)
+    assert run_build(B, a) == B.ERR_INVALID_ARG   # RetNet takes no beta
+    a, _ = base_build(B, 2)
+    a.g = None
+    assert run_build(B, a) == B.ERR_INVALID_ARG
+
+
+def test_build_empty_batch_is_ok_without_gpu(B):
+    a, cu = base_build(B, n_seg=0, lengths=())
+    assert run_build(B, a, ws=0, ws_ptr=0) == B.OK
+
+
+def base_compose(B, family=0, d=128, chains=((0, 1), (1,))):
+    cu = np.array([0] + list(np.cumsum([len(c) for c in chains])), np.int32)
+    idx = np.array([i for c in chains for i in c], np.int32)
+    a = B.ComposeArgs()
+    a.family, a.n_layers, a.n_heads, a.dk, a.dv, a.n_pairs = family, 2, 2, d, d, 2
+    a.T_tab = fake(1) if family != 3 else None
+    a.S_tab = fake(2)
+    a.n_chains = len(chains)
+    a.cu_chain, a.cu_chain_host = fake(3), cu.ctypes.data
+    a.seg_idx, a.seg_idx_host = fake(4), idx.ctypes.data
+    a.S_out = fake(6)
+    return a, (cu, idx)
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a, k: k[1].__setitem__(0, 2), 1),            # pair index out of range
+    (lambda a, k: k[1].__setitem__(0, -1), 1),
+    (lambda a, k: k[0].__setitem__(0, 1), 1),            # cu_chain[0] != 0
+    (lambda a, k: setattr(a, "T_tab", None), 1),
+    (lambda a, k: setattr(a, "S_out", fake(2) + 64), 1), # output overlaps S_tab
+    (lambda a, k: setattr(a, "S0", fake(6)), 1),         # output overlaps S0
+    (lambda a, k: setattr(a, "dv", 64), 2),
+    (lambda a, k: setattr(a, "S_tab", fake(2) + 4), 1),
+])
+def test_compose_rejections(B, mutate, status):
+    a, keep = base_compose(B)
+    mutate(a, keep)
+    assert B.hypic_compose(a, None) == status
+
+
+def test_compose_vanilla_rejects_T(B):
+    a, keep = base_compose(B, 3)
+    a.T_tab = fake(1)
+    assert B.hypic_compose(a, None) == B.ERR_INVALID_ARG
+    a, keep = base_compose(B, 1)
+    a.T_exp_tab = fake(7)
+    assert B.hypic_compose(a, None) == B.ERR_INVALID_ARG
+
+
+def base_seam(B, family=0, d=128, lens=(8, 8)):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    a = B.SeamArgs()
+    a.family, a.in_dtype, a.n_layers, a.n_heads, a.dk, a.dv = family, 1, 2, 2, d, d
+    a.n_seams, a.n_tokens = len(lens), int(cu[-1])
+    a.cu_seam, a.cu_seam_host = fake(0), cu.ctypes.data
+    a.q, a.k, a.v = fake(1), fake(2), fake(3)
+    if family == 0:
+        a.alpha, a.beta = fake(4), fake(5)
+    a.state_in, a.state_out, a.o_out = fake(6), fake(6), fake(8)
+    return a, cu
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a, c: setattr(a, "n_tokens", 15), 1),        # cu_seam[-1] != n_tokens
+    (lambda a, c: setattr(a, "q", None), 1),
+    (lambda a, c: setattr(a, "state_out", None), 1),
+    (lambda a, c: setattr(a, "state_out", fake(6) + 64), 1),  # partial overlap
+    (lambda a, c: setattr(a, "o_out", fake(6)), 1),      # o_out overlaps the state
+    (lambda a, c: setattr(a, "beta", None), 1),
+    (lambda a, c: setattr(a, "dk", 48), 2),
+])
+def test_seam_rejections(B, mutate, status):
+    a, cu = base_seam(B)
+    mutate(a, cu)
+    assert B.hypic_seam_advance(a, None) == status
