@@ -99,9 +99,9 @@ hypic_status check_family(int family, int in_dtype, int n_layers, int n_heads, i
         return fail(HYPIC_ERR_INVALID_ARG, "alpha/beta must be NULL for %s", fam_name(family));
     if (!want_gamma && gamma) return fail(HYPIC_ERR_INVALID_ARG, "gamma must be NULL for %s", fam_name(family));
     if (!want_g && g) return fail(HYPIC_ERR_INVALID_ARG, "g must be NULL for %s", fam_name(family));
-    if (want_gamma && !gamma) return fail(HYPIC_ERR_INVALID_ARG, "RETNET needs gamma");
-    if (has_tokens) {
+    if (has_tokens) {  // gates are read only when tokens are
         if (want_ab && (!alpha || !beta)) return fail(HYPIC_ERR_INVALID_ARG, "GDN needs alpha and beta");
+        if (want_gamma && !gamma) return fail(HYPIC_ERR_INVALID_ARG, "RETNET needs gamma");
         if (want_g && !g) return fail(HYPIC_ERR_INVALID_ARG, "GLA needs g");
     }
     const void* ptrs[] = {alpha, beta, gamma, g};

@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
     const int64_t b0 = (int64_t)p.cu[seg] + (p.skip ? p.skip[seg] : 0), b1 = p.cu[seg + 1];
     const int c = threadIdx.x;
     const int fam = p.family;
-    const float gm = (fam == kRETNET) ? p.gamma[(int64_t)layer * p.n_heads + head] : 1.f;
+    const float gm = (fam == kRETNET && p.gamma) ? p.gamma[(int64_t)layer * p.n_heads + head] : 1.f;
     float col[DK];
 #pragma unroll
     for (int i = 0; i < DK; ++i) col[i] = 0.f;

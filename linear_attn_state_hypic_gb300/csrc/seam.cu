@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) seam_simt_kernel(SeamParams
     const int c = threadIdx.x;
     const int fam = p.family;
     const int64_t obj = (int64_t)r * LH + lh;
-    const float gm = (fam == kRETNET) ? p.gamma[(int64_t)layer * p.n_heads + head] : 1.f;
+    const float gm = (fam == kRETNET && p.gamma) ? p.gamma[(int64_t)layer * p.n_heads + head] : 1.f;
     float col[DK];
 #pragma unroll
     for (int i = 0; i < DK; ++i) col[i] = (p.state_in && c < DV) ? p.state_in[(obj * DK + i) * DV + c] : 0.f;
