@@ -1,7 +1,775 @@
-// gdn_build_tc.cu -- chunked GDN build on the tensor cores (placeholder: the
-// dispatcher falls back to the CUDA-core build until this path exists).
+// gdn_build_tc.cu -- chunked GDN build of the cached pair (T_C, S(C|0)) on the
+// sm_103a tensor cores (d = 128, bf16 keys/values).
+//
+// What it computes: for a segment C and a head, T_C = A_L ... A_1 with the
+// gated-delta transition A_t = a_t (I - b_t k_t k_t^T), and S(C|0), the state
+// after C from zero with the write term b_t k_t v_t^T (aibase article on
+// HYPIC, paragraph on the linear layers: the cached pair of a segment).
+//
+// How: tokens are taken in chunks of 64.  With g_i = a_1 ... a_i inside a
+// chunk (g_C its last value), A[i][j] = b_i (g_i/g_j) k_i.k_j for j < i,
+// That = (I + A)^-1 Diag(b), W = That Diag(g) K and U = That V, the chunk
+// maps the running pair D = [T | S] (dk x 2dk) to
+//     D <- g_C D + K^T Diag(g_C/g_t) ([0 | U] - W D),
+// which is the token recurrence applied 64 times (WY / UT form of a product
+// of generalised Householder transitions).  The state is held transposed,
+// D' = D^T (256 x 128 fp32), in tensor memory; per chunk:
+//   gram      G = K K^T                      bf16 MMA, M=64  N=64  K=128
+//   solve     That from G and the gates      CUDA cores (blocked forward substitution)
+//   W^T, U^T  K^T (That Diag(g))^T, V^T That^T   bf16 MMA, M=128 N=64 K=64
+//   GEMM1     X'_h = D'_h W^T                tf32 MMA, A read from tensor memory
+//   pass      Y'_h = -Diag(g_C/g_t) X'_h^T (bf16, smem); D' <- g_C D' (TMEM)
+//   GEMM2     D'_h += Y'_h K  (+ U~^T K for S) bf16 MMA, M=128 N=128 K=64
+// The T half is rescaled by powers of two as it decays (it falls far below the
+// fp32 range over long segments); the exponent is returned with T.
+//
+// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 the
+// state warpgroup (tensor-memory passes, epilogue), warps 6-9 the prep
+// warpgroup (gates, gram -> That, W/U conversion).  They meet on mbarriers;
+// every wait is bounded and a wait that runs out sets the device error word.
+// One CTA per SM, persistent over (segment, layer, head) items taken from an
+// atomic queue in longest-body-first order.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <float.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
+
 namespace hypic {
-bool gdn_build_tc_supported(const BuildParams&) { return false; }
-cudaError_t launch_gdn_build_tc(const BuildParams&, void*, unsigned*, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 128;           // dk = dv
+constexpr int kC = 64;            // chunk length
+constexpr int kStages = 3;        // K/V ring depth
+constexpr int kThreads = 320;
+constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6;
+
+// Shared memory map (byte offsets; every operand region is 1024-byte aligned).
+constexpr uint32_t kTile = 16384;                     // 64 tokens x 128 bf16, two 64-column TMA boxes
+constexpr uint32_t kStage = 2 * kTile;                // K then V
+constexpr uint32_t OFF_KV = 0;
+constexpr uint32_t OFF_BW = OFF_KV + kStages * kStage;  // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
+constexpr uint32_t OFF_AU = OFF_BW + 32768;             // U~^T: bf16 [128 n][64 t], K-major
+constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y'^T: bf16 2 x [128 n][64 t]
+constexpr uint32_t OFF_BT = OFF_AY + 32768;             // That Diag(g), That: bf16 2 x [64][64]; solve scratch
+constexpr uint32_t OFF_AS = OFF_BT + 16384;             // A / (I+A)^-1: fp32 [64][64], columns xor-swizzled
+constexpr uint32_t OFF_MISC = OFF_AS + 16384;
+
+struct Misc {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t g_done, that_ready, w_done, wu_cvt, x_done, y_ready, d_ready, drain;
+    float lg2[2][kC], beta[2][kC], ratio[2][kC], gam[2][kC];  // per chunk parity
+    float scan_tot;
+    float red[2][4];
+    float red_ep[4];
+    int item;
+    int abort_flag;
+    uint32_t tmem_base;
+};
+constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Tensor-memory columns.
+constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_GW = 384, TM_U = 448;
+
+constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);  // G = K K^T
+constexpr uint32_t ID_WU = idesc(1, 128, 64, true, false);    // W^T, U^T: A = K^T / V^T (MN-major)
+constexpr uint32_t ID_G1 = idesc(2, 128, 64, false, false);   // X' = D' W^T (tf32, A in TMEM)
+constexpr uint32_t ID_G2 = idesc(1, 128, 128, false, true);   // D' += Y' K (B = K, MN-major)
+
+struct TcArgs {
+    int n_layers, n_heads, n_seg, n_items;
+    int64_t n_tokens;
+    const int32_t* cu;
+    const int32_t* skip;
+    const float* alpha;
+    const float* beta;
+    float* T_out;
+    int32_t* T_exp;
+    float* S_out;
+    const int32_t* order;
+    unsigned* counter;
+    unsigned* err;
+    uint32_t wait_limit;
+};
+
+// Bounded wait shared by all roles: gives up (and raises the CTA's abort
+// flag and the device error word) after `limit` polls, or at once when
+// another role already gave up.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
+    for (uint32_t i = 0; i < a.wait_limit; i += 256) {
+        for (int j = 0; j < 256; ++j)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*(volatile int*)&ms->abort_flag) return false;
+    }
+    *(volatile int*)&ms->abort_flag = 1;
+    set_error(a.err, kErrTimeout);
+    return false;
+}
+
+__device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+// A / (I+A)^-1 scratch: element (r, j) at r*64 + (j ^ (r & 15)).
+__device__ __forceinline__ int as_idx(int r, int j) { return r * kC + (j ^ (r & 15)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// ----------------------------------------------------------- prep roles --
+// p: thread index inside the prep warpgroup (0..127); q: its tensor-memory
+// lane quarter; lane: lane in the warp.
+
+// Gates of one chunk: lg2[t] = sum_{s<=t} log2 a_s (inclusive prefix inside
+// the chunk), ratio[t] = g_C/g_t, gam[t] = g_t, beta[t].  Padded tokens
+// past the segment end get a = 1, b = 0: an identity transition, so the
+// padded rows leave the result unchanged.
+__device__ void prep_gates(Misc* ms, int par, const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end,
+                           int p, int lane) {
+    float la = 0.f, bb = 0.f;
+    if (p < kC) {
+        const int64_t t = t0 + p;
+        if (t < t_end) {
+            const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
+            la = log2f(fmaxf(a.alpha[row], FLT_MIN));
+            bb = a.beta[row];
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, la, off);
+            if (lane >= off) la += y;
+        }
+        if (p == 31) ms->scan_tot = la;
+    }
+    named_sync(1);
+    if (p < kC) {
+        if (p >= 32) la += ms->scan_tot;
+        ms->lg2[par][p] = la;
+        ms->beta[par][p] = bb;
+    }
+    named_sync(1);
+    if (p < kC) {
+        const float lc = ms->lg2[par][kC - 1];
+        ms->ratio[par][p] = exp2f(lc - la);
+        ms->gam[par][p] = exp2f(la);
+    }
+    named_sync(1);
+}
+
+// Rows of A from the gram matrix in tensor memory (M=64 accumulator layout:
+// row 16q + l sits in lane 32q + l, l < 16):
+// A[r][j] = b_r 2^(lg2_r - lg2_j) G[r][j] for j < r, 0 elsewhere.
+__device__ void prep_arows(const Misc* ms, float* As, int par, uint32_t tmem, int q, int lane) {
+    uint32_t g0[32], g1[32];
+    const uint32_t tl = tmem + ((32u * q) << 16) + TM_GW;
+    tmem_ld32(tl, g0);
+    tmem_ld32(tl + 32, g1);
+    tmem_wait_ld();
+    if (lane < 16) {
+        const int r = 16 * q + lane;
+        const float lr = ms->lg2[par][r], br = ms->beta[par][r];
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+            const float g = __uint_as_float(j < 32 ? g0[j] : g1[j - 32]);
+            As[as_idx(r, j)] = (j < r) ? br * exp2f(lr - ms->lg2[par][j]) * g : 0.f;
+        }
+    }
+}
+
+// (I + A)^-1 in place, A strictly lower triangular 64 x 64, by 16 x 16 blocks:
+// the four diagonal blocks by forward substitution (one column per thread),
+// then block rows i = 1..3 as M_ij = -M_ii sum_{k=j}^{i-1} A_ik M_kj.  Ptmp
+// (3 KB) holds the inner sums.  All 128 prep threads take part.
+__device__ void prep_solve(float* As, float* Ptmp, int p) {
+    float m[16];
+    if (p < kC) {
+        const int b = p >> 4, c = p & 15;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m[i] = (i == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < i; ++j) s = fmaf(As[as_idx(16 * b + i, 16 * b + j)], m[j], s);
+            if (i > c) m[i] = -s;
+        }
+    }
+    named_sync(1);
+    if (p < kC) {
+        const int b = p >> 4, c = p & 15;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) As[as_idx(16 * b + i, 16 * b + c)] = m[i];
+    }
+    named_sync(1);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        const int n_out = i * 256;
+#pragma unroll
+        for (int o0 = 0; o0 < n_out; o0 += 128) {
+            const int o = o0 + p, j = o >> 8, r = (o >> 4) & 15, cc = o & 15;
+            float acc = 0.f;
+            for (int k = j; k < i; ++k)
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    acc = fmaf(As[as_idx(16 * i + r, 16 * k + u)], As[as_idx(16 * k + u, 16 * j + cc)], acc);
+            Ptmp[o] = acc;
+        }
+        named_sync(1);
+        float val[6];
+#pragma unroll
+        for (int o0 = 0, n = 0; o0 < n_out; o0 += 128, ++n) {
+            const int o = o0 + p, j = o >> 8, r = (o >> 4) & 15, cc = o & 15;
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < 16; ++s) acc = fmaf(As[as_idx(16 * i + r, 16 * i + s)], Ptmp[(j << 8) + (s << 4) + cc], acc);
+            val[n] = -acc;
+        }
+        named_sync(1);
+#pragma unroll
+        for (int o0 = 0, n = 0; o0 < n_out; o0 += 128, ++n) {
+            const int o = o0 + p, j = o >> 8, r = (o >> 4) & 15, cc = o & 15;
+            As[as_idx(16 * i + r, 16 * j + cc)] = val[n];
+        }
+        named_sync(1);
+    }
+}
+
+// That Diag(g) and That = (I+A)^-1 Diag(b) as bf16 K-major 64 x 64 operands
+// (128-byte rows, 128-byte swizzle) at bt and bt + 8192.
+__device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, int par, int p) {
+    const float* beta = ms->beta[par];
+    const float* gam = ms->gam[par];
+#pragma unroll
+    for (int o0 = 0; o0 < 512; o0 += 128) {
+        const int o = o0 + p, t = o >> 3, ch = o & 7;
+        uint32_t w1[4], w2[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int c0 = 8 * ch + 2 * jj;
+            const float m0 = As[as_idx(t, c0)] * beta[c0], m1 = As[as_idx(t, c0 + 1)] * beta[c0 + 1];
+            w1[jj] = pack_bf16(m0 * gam[c0], m1 * gam[c0 + 1]);
+            w2[jj] = pack_bf16(m0, m1);
+        }
+        const uint32_t off = t * 128u + ((uint32_t)(ch ^ (t & 7)) << 4);
+        st_shared_v4(bt + off, w1[0], w1[1], w1[2], w1[3]);
+        st_shared_v4(bt + 8192u + off, w2[0], w2[1], w2[2], w2[3]);
+    }
+}
+
+// W^T (lane i holds W[.][i]) -> W as a tf32 K-major [64 t][128 i] operand;
+// U^T (lane n holds U[.][n]) -> U~^T = U^T Diag(g_C/g_t) as a bf16 K-major
+// [128 n][64 t] operand.
+__device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, int par, uint32_t tmem, int q, int lane) {
+    const int i = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    const float* ratio = ms->ratio[par];
+    uint32_t w[32];
+    uint8_t* bw = smem + OFF_BW + (i >> 5) * 8192;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + TM_GW + 32 * half, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = 32 * half + j;
+            *reinterpret_cast<float*>(bw + sw128_offset(t, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w[j]));
+        }
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + TM_U + 32 * half, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = 32 * half + 8 * jj + 2 * k;
+                pk[k] = pack_bf16(__uint_as_float(w[8 * jj + 2 * k]) * ratio[t],
+                                  __uint_as_float(w[8 * jj + 2 * k + 1]) * ratio[t + 1]);
+            }
+            const uint32_t off = i * 128u + ((uint32_t)((4 * half + jj) ^ (i & 7)) << 4);
+            st_shared_v4(au + off, pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------- state roles --
+// Thread n of the state warpgroup owns tensor-memory lane n = 32q + lane:
+// row n of D'_T (column n of T) and of D'_S (column n of S).
+
+// D' <- (I, 0): row n of D'_T is e_n.
+__device__ void state_init(uint32_t tmem, int q, int lane) {
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    const int n = 32 * q + lane;
+    uint32_t r[32];
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = (32 * cb + j == n) ? 0x3f800000u : 0u;
+        tmem_st32(tl + TM_DT + 32 * cb, r);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = 0u;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) tmem_st32(tl + TM_DS + 32 * cb, r);
+    tmem_wait_st();
+}
+
+// After GEMM1 of a chunk: Y'_h rows into shared memory (bf16, K-major
+// [128 n][64 t]) and the decay of D' in tensor memory.  The T half is also
+// scaled by 2^-e (exponent bookkeeping); returns the max |.| of the new T row.
+//   Y'_T[n][t] = -(g_C/g_t) 2^-e X'_T[n][t],  D'_T <- g_C 2^-e D'_T
+//   Y'_S[n][t] = -(g_C/g_t) X'_S[n][t],       D'_S <- g_C D'_S
+__device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_t tmem, int q, int lane) {
+    const int n = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    const float* lg2 = ms->lg2[par];
+    const float* ratio = ms->ratio[par];
+    const float lc = lg2[kC - 1];
+    float mloc = 0.f;
+    uint32_t x[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32 * half, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = 32 * half + 8 * jj + 2 * k;
+                    float f0, f1;
+                    if (h) {
+                        f0 = -ratio[t];
+                        f1 = -ratio[t + 1];
+                    } else {
+                        f0 = -exp2f(fminf(lc - lg2[t] - (float)e, 126.f));
+                        f1 = -exp2f(fminf(lc - lg2[t + 1] - (float)e, 126.f));
+                    }
+                    pk[k] = pack_bf16(f0 * __uint_as_float(x[8 * jj + 2 * k]), f1 * __uint_as_float(x[8 * jj + 2 * k + 1]));
+                }
+                const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((4 * half + jj) ^ (n & 7)) << 4);
+                st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        const float sc = h ? exp2f(lc) : exp2f(lc - (float)e);
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            const uint32_t addr = tl + (h ? TM_DS : TM_DT) + 32 * cb;
+            tmem_ld32(addr, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float v = __uint_as_float(x[j]) * sc;
+                if (!h) mloc = fmaxf(mloc, fabsf(v));
+                x[j] = __float_as_uint(v);
+            }
+            tmem_st32(addr, x);
+        }
+    }
+    tmem_wait_st();
+    return mloc;
+}
+
+// Warp max, then the 4 warps of the state warpgroup through shared memory.
+__device__ float state_reduce_max(float v, float* slot, int q, int lane) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) slot[q] = v;
+    named_sync(2);
+    return fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
+}
+
+// End of an item: T_C = mantissa * 2^exp with the mantissa's largest entry in
+// [1, 2); S(C|0) as is.  Thread n writes column n (coalesced across the warp).
+__device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, int E, uint32_t tmem, int q, int lane) {
+    const int n = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    uint32_t x[32];
+    float m = 0.f;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        tmem_ld32(tl + TM_DT + 32 * cb, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(__uint_as_float(x[j])));
+    }
+    m = state_reduce_max(m, ms->red_ep, q, lane);
+    const int ef = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
+    float* T = a.T_out + obj * kD * kD;
+    float* S = a.S_out + obj * kD * kD;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        tmem_ld32(tl + TM_DT + 32 * cb, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) T[(32 * cb + j) * kD + n] = ldexpf(__uint_as_float(x[j]), -ef);
+    }
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        tmem_ld32(tl + TM_DS + 32 * cb, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[(32 * cb + j) * kD + n] = __uint_as_float(x[j]);
+    }
+    if (n == 0) a.T_exp[obj] = E + ef;
+}
+
+// Empty body: the identity pair.
+__device__ void state_identity(const TcArgs& a, int64_t obj, int n) {
+    float* T = a.T_out + obj * kD * kD;
+    float* S = a.S_out + obj * kD * kD;
+    for (int i = 0; i < kD; ++i) {
+        T[i * kD + n] = (i == n) ? 1.f : 0.f;
+        S[i * kD + n] = 0.f;
+    }
+    if (n == 0) a.T_exp[obj] = 0;
+}
+
+// All 128 threads of named barrier `id` agree: true only if every one passed true.
+__device__ __forceinline__ bool wg_all(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.and.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+// --------------------------------------------------------- role drivers --
+// g: global chunk counter at the start of the item (barrier phases run on it
+// across items); nc: chunks of this item's body.
+
+__device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CUtensorMap* tmk,
+                              const CUtensorMap* tmv, uint32_t g, int nc, int layer, int head, int64_t b0) {
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c, s = gc % kStages, u = gc / kStages;
+        if (u >= 1 && !wait_bar(&ms->empty[s], (u - 1) & 1, ms, a)) return;
+        uint8_t* kt = smem + OFF_KV + s * kStage;
+        mbar_expect_tx(&ms->full[s], kStage);
+        const int z = (int)((int64_t)layer * a.n_tokens + b0 + (int64_t)c * kC);
+        tma_load_3d(kt, tmk, &ms->full[s], 0, head, z);
+        tma_load_3d(kt + 8192, tmk, &ms->full[s], 64, head, z);
+        tma_load_3d(kt + kTile, tmv, &ms->full[s], 0, head, z);
+        tma_load_3d(kt + kTile + 8192, tmv, &ms->full[s], 64, head, z);
+    }
+}
+
+__device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
+    if (nc == 0) return;
+    const uint32_t sb = smem_u32(smem);
+    auto ktile = [&](uint32_t gc) { return sb + OFF_KV + (gc % kStages) * kStage; };
+    // G = K K^T: K-major view of the K tile (K = feature index, two 64-wide boxes).
+    auto gram = [&](uint32_t gc) {
+        const uint32_t kt = ktile(gc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint64_t d = sdesc_sw128(kt + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024);
+            mma_bf16_ss(tmem + TM_GW, d, d, ID_GRAM, k > 0);
+        }
+        mma_commit(&ms->g_done);
+    };
+    // W^T = K^T (That Diag(g))^T and U^T = V^T That^T: K and V tiles read
+    // MN-major (M = feature, K = token).
+    auto wu = [&](uint32_t gc) {
+        const uint32_t kt = ktile(gc), vt = kt + kTile, bt = sb + OFF_BT;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mma_bf16_ss(tmem + TM_GW, sdesc_sw128(kt + k * 2048, 8192, 1024), sdesc_sw128(bt + k * 32, 0, 1024), ID_WU,
+                        k > 0);
+            mma_bf16_ss(tmem + TM_U, sdesc_sw128(vt + k * 2048, 8192, 1024),
+                        sdesc_sw128(bt + 8192 + k * 32, 0, 1024), ID_WU, k > 0);
+        }
+        mma_commit(&ms->w_done);
+    };
+    if (!wait_bar(&ms->full[g % kStages], (g / kStages) & 1, ms, a)) return;
+    tc_fence_after();
+    gram(g);
+    if (!wait_bar(&ms->that_ready, g & 1, ms, a)) return;
+    tc_fence_after();
+    wu(g);
+    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, au = sb + OFF_AU;
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c;
+        if (!wait_bar(&ms->wu_cvt, gc & 1, ms, a)) return;
+        if (c > 0 && !wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a)) return;
+        tc_fence_after();
+        // GEMM1 (tf32): X'_h = D'_h W^T, A = the state itself in tensor memory.
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k,
+                            sdesc_sw128(bw + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024), ID_G1, k > 0);
+        mma_commit(&ms->x_done);
+        if (c + 1 < nc) {  // gram of the next chunk while the state warpgroup runs its pass
+            if (!wait_bar(&ms->full[(gc + 1) % kStages], ((gc + 1) / kStages) & 1, ms, a)) return;
+            tc_fence_after();
+            gram(gc + 1);
+        }
+        if (!wait_bar(&ms->y_ready, gc & 1, ms, a)) return;
+        tc_fence_after();
+        // GEMM2 (bf16): D'_T += Y'_T K; D'_S += Y'_S K + U~^T K.
+        const uint32_t kt = ktile(gc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint64_t bk = sdesc_sw128(kt + k * 2048, 8192, 1024);
+            mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + k * 32, 0, 1024), bk, ID_G2, true);
+            mma_bf16_ss(tmem + TM_DS, sdesc_sw128(ay + 16384 + k * 32, 0, 1024), bk, ID_G2, true);
+            mma_bf16_ss(tmem + TM_DS, sdesc_sw128(au + k * 32, 0, 1024), bk, ID_G2, true);
+        }
+        mma_commit(&ms->d_ready);
+        mma_commit(&ms->empty[gc % kStages]);
+        if (c + 1 < nc) {
+            if (!wait_bar(&ms->that_ready, (gc + 1) & 1, ms, a)) return;
+            tc_fence_after();
+            wu(gc + 1);
+        }
+    }
+}
+
+__device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int layer,
+                          int head, int64_t b0, int64_t b1, int p, int q, int lane) {
+    float* As = reinterpret_cast<float*>(smem + OFF_AS);
+    float* Ptmp = reinterpret_cast<float*>(smem + OFF_BT);
+    const uint32_t sb = smem_u32(smem);
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c;
+        const int par = gc & 1;
+        prep_gates(ms, par, a, layer, head, b0 + (int64_t)c * kC, b1, p, lane);
+        if (!wg_all(1, wait_bar(&ms->g_done, gc & 1, ms, a))) return;
+        tc_fence_after();
+        prep_arows(ms, As, par, tmem, q, lane);
+        tc_fence_before();
+        named_sync(1);
+        prep_solve(As, Ptmp, p);
+        prep_write_that(ms, As, sb + OFF_BT, par, p);
+        fence_async_smem();
+        named_sync(1);
+        if (p == 0) mbar_arrive(&ms->that_ready);
+        if (!wg_all(1, wait_bar(&ms->w_done, gc & 1, ms, a))) return;
+        tc_fence_after();
+        prep_convert(ms, smem, sb + OFF_AU, par, tmem, q, lane);
+        fence_async_smem();
+        tc_fence_before();
+        named_sync(1);
+        if (p == 0) mbar_arrive(&ms->wu_cvt);
+    }
+}
+
+__device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc,
+                           int64_t obj, int q, int lane) {
+    const int n = 32 * q + lane;
+    if (nc == 0) {
+        state_identity(a, obj, n);
+        return;
+    }
+    const uint32_t ay = smem_u32(smem) + OFF_AY;
+    int E = 0;
+    float m = 1.f;
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c;
+        const int par = gc & 1;
+        bool ok = wait_bar(&ms->x_done, gc & 1, ms, a);
+        ok = ok && wait_bar(&ms->wu_cvt, gc & 1, ms, a);  // this chunk's gates are visible
+        if (!wg_all(2, ok)) return;
+        tc_fence_after();
+        const float lc = ms->lg2[par][kC - 1];
+        const int e = ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lc);
+        const float mloc = state_pass(ms, ay, par, e, tmem, q, lane);
+        fence_async_smem();
+        tc_fence_before();
+        m = state_reduce_max(mloc, ms->red[par], q, lane);
+        if (n == 0) mbar_arrive(&ms->y_ready);
+        E += e;
+    }
+    if (!wg_all(2, wait_bar(&ms->d_ready, (g + nc - 1) & 1, ms, a))) return;
+    tc_fence_after();
+    state_epilogue(ms, a, obj, E, tmem, q, lane);
+    state_init(tmem, q, lane);  // (I, 0) for the next item
+}
+
+// ---------------------------------------------------------------- kernel --
+__global__ void __launch_bounds__(kThreads, 1)
+    gdn_build_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    Misc* ms = reinterpret_cast<Misc*>(smem + OFF_MISC);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled operand layouts need 1024-byte alignment
+        if (tid == 0) set_error(a.err, kErrBadIndex);
+        return;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ms->full[s], 1);
+            mbar_init(&ms->empty[s], 1);
+        }
+        mbar_init(&ms->g_done, 1);
+        mbar_init(&ms->that_ready, 1);
+        mbar_init(&ms->w_done, 1);
+        mbar_init(&ms->wu_cvt, 1);
+        mbar_init(&ms->x_done, 1);
+        mbar_init(&ms->y_ready, 1);
+        mbar_init(&ms->d_ready, 1);
+        mbar_init(&ms->drain, 1);
+        ms->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpTMA && lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    if (warp == kWarpMMA) tmem_alloc(&ms->tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms->tmem_base;
+    const bool is_state = warp >= kWarpState0 && warp < kWarpState0 + 4;
+    const int q = warp & 3;  // tensor-memory lane quarter a warp may access
+    if (is_state) state_init(tmem, q, lane);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int LH = a.n_layers * a.n_heads;
+    uint32_t g = 0;
+    for (;;) {
+        if (tid == 0) ms->item = (int)atomicAdd(a.counter, 1u);
+        __syncthreads();
+        const int item = ms->item;
+        if (item >= a.n_items || *(volatile int*)&ms->abort_flag) break;
+        const int pos = item / LH, lh = item % LH;
+        const int seg = a.order[pos];
+        const int layer = lh / a.n_heads, head = lh % a.n_heads;
+        const int64_t b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0), b1 = a.cu[seg + 1];
+        const int nc = (int)((b1 - b0 + kC - 1) / kC);
+        const int64_t obj = ((int64_t)seg * a.n_layers + layer) * a.n_heads + head;
+        if (warp == kWarpTMA) {
+            if (lane == 0) producer_role(ms, smem, a, &tmk, &tmv, g, nc, layer, head, b0);
+        } else if (warp == kWarpMMA) {
+            if (lane == 0) mma_role(ms, smem, a, tmem, g, nc);
+        } else if (is_state) {
+            state_role(ms, smem, a, tmem, g, nc, obj, q, lane);
+        } else {
+            prep_role(ms, smem, a, tmem, g, nc, layer, head, b0, b1, tid - 32 * kWarpPrep0, q, lane);
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        g += nc;
+    }
+    // Drain: every MMA this CTA issued has completed before tensor memory is freed.
+    if (warp == kWarpMMA) {
+        if (lane == 0) {
+            mma_commit(&ms->drain);
+            for (uint32_t i = 0; i < a.wait_limit && !mbar_try_wait(&ms->drain, 0); ++i) {
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMMA) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ host --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int sm_count() {
+    static std::mutex mu;
+    static int cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+    return cache[dev];
+}
+
+// [n_layers][n_tokens][n_heads][128] bf16 as a 3-D tensor (feature, head,
+// layer-token row); box = 64 features x 1 head x 64 rows, 128-byte swizzle.
+bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, const BuildParams& p) {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.n_heads, (cuuint64_t)p.n_layers * (cuuint64_t)p.n_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.n_heads * kD * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kC}, es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gdn_build_tc_supported(const BuildParams& p) {
+    return p.family == kGDN && p.dk == kD && p.dv == kD && p.in_dtype == kBF16 && p.n_tokens > 0 &&
+           (int64_t)p.n_layers * p.n_tokens < INT32_MAX && encode_fn() != nullptr;
+}
+
+cudaError_t launch_gdn_build_tc(const BuildParams& p, void* workspace, unsigned* err, cudaStream_t s) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap tk, tv;
+    if (!make_map(enc, &tk, p.k, p) || !make_map(enc, &tv, p.v, p)) return cudaErrorInvalidValue;
+    TcArgs a;
+    a.n_layers = p.n_layers;
+    a.n_heads = p.n_heads;
+    a.n_seg = p.n_seg;
+    a.n_items = p.n_seg * p.n_layers * p.n_heads;
+    a.n_tokens = p.n_tokens;
+    a.cu = p.cu;
+    a.skip = p.skip;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.T_out = p.T_out;
+    a.T_exp = p.T_exp;
+    a.S_out = p.S_out;
+    a.order = reinterpret_cast<const int32_t*>(workspace);
+    a.counter = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(workspace) + build_workspace_bytes(p.n_seg) - 256);
+    a.err = err;
+    a.wait_limit = 1u << 26;
+    if (a.n_items == 0) return cudaSuccess;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    cudaError_t e = cudaFuncSetAttribute(gdn_build_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = a.n_items < sms ? a.n_items : sms;
+    gdn_build_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tk, tv, a);
+    return cudaGetLastError();
+}
+
 }  // namespace hypic
