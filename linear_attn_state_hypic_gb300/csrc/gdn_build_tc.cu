@@ -20,6 +20,11 @@
 //   GEMM1     X'_h = D'_h W^T                tf32 MMA, A read from tensor memory
 //   pass      Y'_h = -Diag(g_C/g_t) X'_h^T (bf16, smem); D' <- g_C D' (TMEM)
 //   GEMM2     D'_h += Y'_h K  (+ U~^T K for S) bf16 MMA, M=128 N=128 K=64
+// Two operands are carried as a pair of bf16 values (x = hi + lo, lo the
+// rounding residual of hi): That Diag(g) in the W product and Y'_T in the T
+// half of GEMM2.  Rounding either to a single bf16 alone costs T_C about
+// 7e-3 relative error over 2048-token segments with strong decay; the pair
+// brings it to ~2e-3.  Keys and values are bf16 inputs and need no split.
 // The T half is rescaled by powers of two as it decays (it falls far below the
 // fp32 range over long segments); the exponent is returned with T.
 //
@@ -49,7 +54,7 @@ using namespace tc;
 
 constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
-constexpr int kStages = 3;        // K/V ring depth
+constexpr int kStages = 2;        // K/V ring depth
 constexpr int kThreads = 320;
 constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6;
 
@@ -59,9 +64,9 @@ constexpr uint32_t kStage = 2 * kTile;                // K then V
 constexpr uint32_t OFF_KV = 0;
 constexpr uint32_t OFF_BW = OFF_KV + kStages * kStage;  // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
 constexpr uint32_t OFF_AU = OFF_BW + 32768;             // U~^T: bf16 [128 n][64 t], K-major
-constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y'^T: bf16 2 x [128 n][64 t]
-constexpr uint32_t OFF_BT = OFF_AY + 32768;             // That Diag(g), That: bf16 2 x [64][64]; solve scratch
-constexpr uint32_t OFF_AS = OFF_BT + 16384;             // A / (I+A)^-1: fp32 [64][64], columns xor-swizzled
+constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y'^T: bf16 [128 n][64 t]: T hi, S, T lo
+constexpr uint32_t OFF_BT = OFF_AY + 49152;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]; solve scratch
+constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][64], columns xor-swizzled
 constexpr uint32_t OFF_MISC = OFF_AS + 16384;
 
 struct Misc {
@@ -129,6 +134,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ float tf32_rna(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -253,25 +259,29 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
     }
 }
 
-// That Diag(g) and That = (I+A)^-1 Diag(b) as bf16 K-major 64 x 64 operands
-// (128-byte rows, 128-byte swizzle) at bt and bt + 8192.
+// That Diag(g) (bf16 hi at bt, residual lo at bt + 16384) and
+// That = (I+A)^-1 Diag(b) (bf16 at bt + 8192) as K-major 64 x 64 operands
+// (128-byte rows, 128-byte swizzle).
 __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, int par, int p) {
     const float* beta = ms->beta[par];
     const float* gam = ms->gam[par];
 #pragma unroll
     for (int o0 = 0; o0 < 512; o0 += 128) {
         const int o = o0 + p, t = o >> 3, ch = o & 7;
-        uint32_t w1[4], w2[4];
+        uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int c0 = 8 * ch + 2 * jj;
             const float m0 = As[as_idx(t, c0)] * beta[c0], m1 = As[as_idx(t, c0 + 1)] * beta[c0 + 1];
-            w1[jj] = pack_bf16(m0 * gam[c0], m1 * gam[c0 + 1]);
+            const float x0 = m0 * gam[c0], x1 = m1 * gam[c0 + 1];
+            w1[jj] = pack_bf16(x0, x1);
+            w3[jj] = pack_bf16(x0 - bf16_round(x0), x1 - bf16_round(x1));
             w2[jj] = pack_bf16(m0, m1);
         }
         const uint32_t off = t * 128u + ((uint32_t)(ch ^ (t & 7)) << 4);
         st_shared_v4(bt + off, w1[0], w1[1], w1[2], w1[3]);
         st_shared_v4(bt + 8192u + off, w2[0], w2[1], w2[2], w2[3]);
+        st_shared_v4(bt + 16384u + off, w3[0], w3[1], w3[2], w3[3]);
     }
 }
 
@@ -336,7 +346,8 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
 }
 
 // After GEMM1 of a chunk: Y'_h rows into shared memory (bf16, K-major
-// [128 n][64 t]) and the decay of D' in tensor memory.  The T half is also
+// [128 n][64 t]; Y'_T also as its bf16 residual) and the decay of D' in
+// tensor memory.  The T half is also
 // scaled by 2^-e (exponent bookkeeping); returns the max |.| of the new T row.
 //   Y'_T[n][t] = -(g_C/g_t) 2^-e X'_T[n][t],  D'_T <- g_C 2^-e D'_T
 //   Y'_S[n][t] = -(g_C/g_t) X'_S[n][t],       D'_S <- g_C D'_S
@@ -356,7 +367,7 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
             tmem_wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                uint32_t pk[4];
+                uint32_t pk[4], lo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = 32 * half + 8 * jj + 2 * k;
@@ -368,10 +379,14 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
                         f0 = -exp2f(fminf(lc - lg2[t] - (float)e, 126.f));
                         f1 = -exp2f(fminf(lc - lg2[t + 1] - (float)e, 126.f));
                     }
-                    pk[k] = pack_bf16(f0 * __uint_as_float(x[8 * jj + 2 * k]), f1 * __uint_as_float(x[8 * jj + 2 * k + 1]));
+                    const float y0 = f0 * __uint_as_float(x[8 * jj + 2 * k]);
+                    const float y1 = f1 * __uint_as_float(x[8 * jj + 2 * k + 1]);
+                    pk[k] = pack_bf16(y0, y1);
+                    lo[k] = pack_bf16(y0 - bf16_round(y0), y1 - bf16_round(y1));
                 }
                 const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((4 * half + jj) ^ (n & 7)) << 4);
                 st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
+                if (!h) st_shared_v4(ay + 32768u + off, lo[0], lo[1], lo[2], lo[3]);
             }
         }
         const float sc = h ? exp2f(lc) : exp2f(lc - (float)e);
@@ -501,6 +516,8 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
         for (int k = 0; k < 4; ++k) {
             mma_bf16_ss(tmem + TM_GW, sdesc_sw128(kt + k * 2048, 8192, 1024), sdesc_sw128(bt + k * 32, 0, 1024), ID_WU,
                         k > 0);
+            mma_bf16_ss(tmem + TM_GW, sdesc_sw128(kt + k * 2048, 8192, 1024),
+                        sdesc_sw128(bt + 16384 + k * 32, 0, 1024), ID_WU, true);
             mma_bf16_ss(tmem + TM_U, sdesc_sw128(vt + k * 2048, 8192, 1024),
                         sdesc_sw128(bt + 8192 + k * 32, 0, 1024), ID_WU, k > 0);
         }
@@ -539,6 +556,7 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
         for (int k = 0; k < 4; ++k) {
             const uint64_t bk = sdesc_sw128(kt + k * 2048, 8192, 1024);
             mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + k * 32, 0, 1024), bk, ID_G2, true);
+            mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + 32768 + k * 32, 0, 1024), bk, ID_G2, true);
             mma_bf16_ss(tmem + TM_DS, sdesc_sw128(ay + 16384 + k * 32, 0, 1024), bk, ID_G2, true);
             mma_bf16_ss(tmem + TM_DS, sdesc_sw128(au + k * 32, 0, 1024), bk, ID_G2, true);
         }
