@@ -66,13 +66,16 @@ constexpr uint32_t OFF_BW = OFF_KV + kStages * kStage;  // W: fp32 [64 t][128 i]
 constexpr uint32_t OFF_AU = OFF_BW + 32768;             // U~^T: bf16 [128 n][64 t], K-major
 constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y'^T: bf16 [128 n][64 t]: T hi, S, T lo
 constexpr uint32_t OFF_BT = OFF_AY + 49152;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]; solve scratch
-constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][64], columns xor-swizzled
-constexpr uint32_t OFF_MISC = OFF_AS + 16384;
+constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
+constexpr int kAS = 68;                                 // row stride (floats) of that scratch
+constexpr uint32_t OFF_MISC = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;
 
 struct Misc {
     uint64_t full[kStages], empty[kStages];
     uint64_t g_done, that_ready, w_done, wu_cvt, x_done, y_ready, d_ready, drain;
     float lg2[2][kC], beta[2][kC], ratio[2][kC], gam[2][kC];  // per chunk parity
+    float up[2][kC], wn[2][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
+    float fT[kC];                // state pass: -(g_C/g_t) 2^-e for the T half
     float scan_tot;
     float red[2][4];
     float red_ep[4];
@@ -123,8 +126,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
 
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
-// A / (I+A)^-1 scratch: element (r, j) at r*64 + (j ^ (r & 15)).
-__device__ __forceinline__ int as_idx(int r, int j) { return r * kC + (j ^ (r & 15)); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -149,15 +150,12 @@ __device__ __forceinline__ float tf32_rna(float x) {
 // the chunk), ratio[t] = g_C/g_t, gam[t] = g_t, beta[t].  Padded tokens
 // past the segment end get a = 1, b = 0: an identity transition, so the
 // padded rows leave the result unchanged.
-__device__ void prep_gates(Misc* ms, int par, const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end,
-                           int p, int lane) {
+__device__ void prep_gates(Misc* ms, int par, float a_raw, float b_raw, bool valid, int p, int lane) {
     float la = 0.f, bb = 0.f;
     if (p < kC) {
-        const int64_t t = t0 + p;
-        if (t < t_end) {
-            const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
-            la = log2f(fmaxf(a.alpha[row], FLT_MIN));
-            bb = a.beta[row];
+        if (valid) {
+            la = log2f(fmaxf(a_raw, FLT_MIN));
+            bb = b_raw;
         }
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -174,11 +172,27 @@ __device__ void prep_gates(Misc* ms, int par, const TcArgs& a, int layer, int he
     }
     named_sync(1);
     if (p < kC) {
-        const float lc = ms->lg2[par][kC - 1];
+        const float lc = ms->lg2[par][kC - 1], h = 0.5f * lc;
         ms->ratio[par][p] = exp2f(lc - la);
         ms->gam[par][p] = exp2f(la);
+        ms->up[par][p] = exp2f(la - h);
+        ms->wn[par][p] = exp2f(h - la);
     }
     named_sync(1);
+}
+
+// This thread's gates for token t0 + p (p < 64) of the chunk starting at t0.
+__device__ __forceinline__ void load_gates(const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end, int p,
+                                           float& ga, float& gb, bool& valid) {
+    const int64_t t = t0 + p;
+    valid = p < kC && t < t_end;
+    ga = 1.f;
+    gb = 0.f;
+    if (valid) {
+        const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
+        ga = __ldg(a.alpha + row);
+        gb = __ldg(a.beta + row);
+    }
 }
 
 // Rows of A from the gram matrix in tensor memory (M=64 accumulator layout:
@@ -192,93 +206,129 @@ __device__ void prep_arows(const Misc* ms, float* As, int par, uint32_t tmem, in
     tmem_wait_ld();
     if (lane < 16) {
         const int r = 16 * q + lane;
-        const float lr = ms->lg2[par][r], br = ms->beta[par][r];
+        const float coef = ms->beta[par][r] * ms->up[par][r];
+        const float* wn = ms->wn[par];
+        float* row = As + r * kAS;
 #pragma unroll
-        for (int j = 0; j < kC; ++j) {
-            const float g = __uint_as_float(j < 32 ? g0[j] : g1[j - 32]);
-            As[as_idx(r, j)] = (j < r) ? br * exp2f(lr - ms->lg2[par][j]) * g : 0.f;
+        for (int j = 0; j < kC; j += 4) {
+            float4 v;
+            v.x = (j < r) ? coef * wn[j] * __uint_as_float(j < 32 ? g0[j] : g1[j - 32]) : 0.f;
+            v.y = (j + 1 < r) ? coef * wn[j + 1] * __uint_as_float(j + 1 < 32 ? g0[j + 1] : g1[j - 31]) : 0.f;
+            v.z = (j + 2 < r) ? coef * wn[j + 2] * __uint_as_float(j + 2 < 32 ? g0[j + 2] : g1[j - 30]) : 0.f;
+            v.w = (j + 3 < r) ? coef * wn[j + 3] * __uint_as_float(j + 3 < 32 ? g0[j + 3] : g1[j - 29]) : 0.f;
+            *reinterpret_cast<float4*>(row + j) = v;
         }
     }
 }
 
-// (I + A)^-1 in place, A strictly lower triangular 64 x 64, by 16 x 16 blocks:
-// the four diagonal blocks by forward substitution (one column per thread),
-// then block rows i = 1..3 as M_ij = -M_ii sum_{k=j}^{i-1} A_ik M_kj.  Ptmp
-// (3 KB) holds the inner sums.  All 128 prep threads take part.
+// (I + A)^-1 in place, A strictly lower triangular 64 x 64 (row stride kAS),
+// by 16 x 16 blocks.  Diagonal blocks: forward substitution, one column per
+// thread (threads 0..63).  Block rows i = 1..3: P_ij = sum_{k=j}^{i-1} A_ik M_kj
+// into Ptmp, then M_ij = -M_ii P_ij; each thread owns a row r and a column
+// pair (2 outputs per load of A).  All loops are unrolled so every address is
+// the thread's base plus an immediate.
 __device__ void prep_solve(float* As, float* Ptmp, int p) {
     float m[16];
     if (p < kC) {
         const int b = p >> 4, c = p & 15;
+        const float* Ab = As + 16 * b * kAS + 16 * b;
 #pragma unroll
         for (int i = 0; i < 16; ++i) m[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
         for (int i = 1; i < 16; ++i) {
-            float s = 0.f;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) s = fmaf(As[as_idx(16 * b + i, 16 * b + j)], m[j], s);
-            if (i > c) m[i] = -s;
+            for (int j = 0; j < i; ++j) {
+                if (j & 1) s1 = fmaf(Ab[i * kAS + j], m[j], s1);
+                else s0 = fmaf(Ab[i * kAS + j], m[j], s0);
+            }
+            if (i > c) m[i] = -(s0 + s1);
         }
     }
     named_sync(1);
     if (p < kC) {
         const int b = p >> 4, c = p & 15;
+        float* Ab = As + 16 * b * kAS + 16 * b;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) As[as_idx(16 * b + i, 16 * b + c)] = m[i];
+        for (int i = 0; i < 16; ++i) Ab[i * kAS + c] = m[i];
     }
     named_sync(1);
+    const int r = p >> 3, cp = (p & 7) * 2;
+    const float* Arow_base = As + r * kAS;   // + (16 i) kAS selects block row i
+    const float* Mcol_base = As + cp;        // + (16 k + u) kAS + 16 j
 #pragma unroll
     for (int i = 1; i < 4; ++i) {
-        const int n_out = i * 256;
+        const float* Ar = Arow_base + 16 * i * kAS;
 #pragma unroll
-        for (int o0 = 0; o0 < n_out; o0 += 128) {
-            const int o = o0 + p, j = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-            float acc = 0.f;
+        for (int j = 0; j < i; ++j) {
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
             for (int k = j; k < i; ++k)
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    acc = fmaf(As[as_idx(16 * i + r, 16 * k + u)], As[as_idx(16 * k + u, 16 * j + cc)], acc);
-            Ptmp[o] = acc;
+                for (int u = 0; u < 16; ++u) {
+                    const float av = Ar[16 * k + u];
+                    const float2 mv = *reinterpret_cast<const float2*>(Mcol_base + (16 * k + u) * kAS + 16 * j);
+                    if (u & 1) {
+                        b0 = fmaf(av, mv.x, b0);
+                        b1 = fmaf(av, mv.y, b1);
+                    } else {
+                        a0 = fmaf(av, mv.x, a0);
+                        a1 = fmaf(av, mv.y, a1);
+                    }
+                }
+            *reinterpret_cast<float2*>(Ptmp + (j * 16 + r) * 16 + cp) = make_float2(a0 + b0, a1 + b1);
         }
         named_sync(1);
-        float val[6];
+        float2 out[3];
 #pragma unroll
-        for (int o0 = 0, n = 0; o0 < n_out; o0 += 128, ++n) {
-            const int o = o0 + p, j = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-            float acc = 0.f;
+        for (int j = 0; j < i; ++j) {
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-            for (int s = 0; s < 16; ++s) acc = fmaf(As[as_idx(16 * i + r, 16 * i + s)], Ptmp[(j << 8) + (s << 4) + cc], acc);
-            val[n] = -acc;
+            for (int u = 0; u < 16; ++u) {
+                const float mv = Ar[16 * i + u];
+                const float2 pv = *reinterpret_cast<const float2*>(Ptmp + (j * 16 + u) * 16 + cp);
+                if (u & 1) {
+                    b0 = fmaf(mv, pv.x, b0);
+                    b1 = fmaf(mv, pv.y, b1);
+                } else {
+                    a0 = fmaf(mv, pv.x, a0);
+                    a1 = fmaf(mv, pv.y, a1);
+                }
+            }
+            out[j] = make_float2(-(a0 + b0), -(a1 + b1));
         }
         named_sync(1);
+        float* Aw = As + (16 * i + r) * kAS + cp;
 #pragma unroll
-        for (int o0 = 0, n = 0; o0 < n_out; o0 += 128, ++n) {
-            const int o = o0 + p, j = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-            As[as_idx(16 * i + r, 16 * j + cc)] = val[n];
-        }
+        for (int j = 0; j < i; ++j) *reinterpret_cast<float2*>(Aw + 16 * j) = out[j];
         named_sync(1);
     }
 }
 
 // That Diag(g) (bf16 hi at bt, residual lo at bt + 16384) and
 // That = (I+A)^-1 Diag(b) (bf16 at bt + 8192) as K-major 64 x 64 operands
-// (128-byte rows, 128-byte swizzle).
+// (128-byte rows, 128-byte swizzle).  Thread p writes half a row.
 __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, int par, int p) {
     const float* beta = ms->beta[par];
     const float* gam = ms->gam[par];
+    const int t = p >> 1, half = p & 1;
+    const float* row = As + t * kAS + 32 * half;
 #pragma unroll
-    for (int o0 = 0; o0 < 512; o0 += 128) {
-        const int o = o0 + p, t = o >> 3, ch = o & 7;
+    for (int ch = 0; ch < 4; ++ch) {
+        const float4 x0 = *reinterpret_cast<const float4*>(row + 8 * ch);
+        const float4 x1 = *reinterpret_cast<const float4*>(row + 8 * ch + 4);
+        const float mv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const int c0 = 8 * ch + 2 * jj;
-            const float m0 = As[as_idx(t, c0)] * beta[c0], m1 = As[as_idx(t, c0 + 1)] * beta[c0 + 1];
-            const float x0 = m0 * gam[c0], x1 = m1 * gam[c0 + 1];
-            w1[jj] = pack_bf16(x0, x1);
-            w3[jj] = pack_bf16(x0 - bf16_round(x0), x1 - bf16_round(x1));
+            const int c0 = 32 * half + 8 * ch + 2 * jj;
+            const float m0 = mv[2 * jj] * beta[c0], m1 = mv[2 * jj + 1] * beta[c0 + 1];
+            const float z0 = m0 * gam[c0], z1 = m1 * gam[c0 + 1];
+            w1[jj] = pack_bf16(z0, z1);
+            w3[jj] = pack_bf16(z0 - bf16_round(z0), z1 - bf16_round(z1));
             w2[jj] = pack_bf16(m0, m1);
         }
-        const uint32_t off = t * 128u + ((uint32_t)(ch ^ (t & 7)) << 4);
+        const uint32_t off = t * 128u + ((uint32_t)((4 * half + ch) ^ (t & 7)) << 4);
         st_shared_v4(bt + off, w1[0], w1[1], w1[2], w1[3]);
         st_shared_v4(bt + 8192u + off, w2[0], w2[1], w2[2], w2[3]);
         st_shared_v4(bt + 16384u + off, w3[0], w3[1], w3[2], w3[3]);
@@ -354,9 +404,9 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
 __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_t tmem, int q, int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    const float* lg2 = ms->lg2[par];
     const float* ratio = ms->ratio[par];
-    const float lc = lg2[kC - 1];
+    const float* fT = ms->fT;
+    const float lc = ms->lg2[par][kC - 1];
     float mloc = 0.f;
     uint32_t x[32];
 #pragma unroll
@@ -376,8 +426,8 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
                         f0 = -ratio[t];
                         f1 = -ratio[t + 1];
                     } else {
-                        f0 = -exp2f(fminf(lc - lg2[t] - (float)e, 126.f));
-                        f1 = -exp2f(fminf(lc - lg2[t + 1] - (float)e, 126.f));
+                        f0 = fT[t];
+                        f1 = fT[t + 1];
                     }
                     const float y0 = f0 * __uint_as_float(x[8 * jj + 2 * k]);
                     const float y1 = f1 * __uint_as_float(x[8 * jj + 2 * k + 1]);
@@ -575,10 +625,16 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
     float* Ptmp = reinterpret_cast<float*>(smem + OFF_BT);
     const uint32_t sb = smem_u32(smem);
+    float ga, gb;
+    bool gv;
+    load_gates(a, layer, head, b0, b1, p, ga, gb, gv);
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
         const int par = gc & 1;
-        prep_gates(ms, par, a, layer, head, b0 + (int64_t)c * kC, b1, p, lane);
+        const float ca = ga, cb = gb;
+        const bool cv = gv;
+        if (c + 1 < nc) load_gates(a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, p, ga, gb, gv);  // next chunk
+        prep_gates(ms, par, ca, cb, cv, p, lane);
         if (!wg_all(1, wait_bar(&ms->g_done, gc & 1, ms, a))) return;
         tc_fence_after();
         prep_arows(ms, As, par, tmem, q, lane);
@@ -618,6 +674,8 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         tc_fence_after();
         const float lc = ms->lg2[par][kC - 1];
         const int e = ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lc);
+        if (n < kC) ms->fT[n] = -exp2f(fminf(lc - ms->lg2[par][n] - (float)e, 126.f));
+        named_sync(2);
         const float mloc = state_pass(ms, ay, par, e, tmem, q, lane);
         fence_async_smem();
         tc_fence_before();
