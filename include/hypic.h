@@ -213,6 +213,33 @@ typedef struct {
 
 HYPIC_API hypic_status hypic_seam_advance(const hypic_seam_args* args, hypic_stream_t stream);
 
+/* -------------------------------------------------------- no-alloc build --
+ * No counterpart in the HYPIC pages: this entry point exists for callers of the
+ * library that are not allowed to allocate device memory themselves -- for
+ * example a plugin that an inference engine hands only its input and output
+ * buffers, or a serving loop whose memory is owned by another allocator and
+ * must not grow or be synchronised by cudaMalloc in the middle of a request.
+ *
+ * It computes exactly what hypic_segment_build computes, with the same
+ * arguments and errors, but takes no workspace: its scratch (the work order
+ * and work counter, about 64 KB) is a fixed array inside this library, and
+ * every GPU that loads the library keeps that array until the process exits.
+ *   - n_segments is limited to HYPIC_NOALLOC_MAX_SEGMENTS; a larger batch is
+ *     rejected with HYPIC_ERR_WORKSPACE before anything is launched (use
+ *     hypic_segment_build with a caller workspace instead).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array.  Each call rewrites the
+ *     whole order and zeroes the counter before using them, but calls whose
+ *     work overlaps on the GPU (other streams, other threads) race on it:
+ *     serialise them.
+ *   - The call itself allocates nothing (no cudaMalloc, no allocating library
+ *     routine).
+ */
+#define HYPIC_NOALLOC_MAX_SEGMENTS 16384
+HYPIC_API hypic_status hypic_segment_build_noalloc(const hypic_build_args* args, hypic_stream_t stream);
+
 /* ------------------------------------------------------------------ misc -- */
 
 /* Static, never NULL. */

@@ -51,7 +51,9 @@ class SeamArgs(ctypes.Structure):
 
 
 EXPORTS = ["hypic_build_workspace_size", "hypic_segment_build", "hypic_compose", "hypic_seam_advance",
-           "hypic_status_string", "hypic_last_error_detail", "hypic_version", "hypic_check_device"]
+           "hypic_status_string", "hypic_last_error_detail", "hypic_version", "hypic_check_device",
+           "hypic_segment_build_noalloc"]
+NOALLOC_MAX_SEGMENTS = 16384
 
 
 def _load():
@@ -62,6 +64,8 @@ def _load():
     lib.hypic_build_workspace_size.argtypes = [ctypes.POINTER(BuildArgs)]
     lib.hypic_build_workspace_size.restype = ctypes.c_size_t
     lib.hypic_segment_build.argtypes = [ctypes.POINTER(BuildArgs), _P, ctypes.c_size_t, _P]
+    lib.hypic_segment_build_noalloc.argtypes = [ctypes.POINTER(BuildArgs), _P]
+    lib.hypic_segment_build_noalloc.restype = _I
     lib.hypic_compose.argtypes = [ctypes.POINTER(ComposeArgs), _P]
     lib.hypic_seam_advance.argtypes = [ctypes.POINTER(SeamArgs), _P]
     lib.hypic_check_device.argtypes = [_P]
@@ -97,6 +101,10 @@ def hypic_build_workspace_size(args: BuildArgs) -> int:
 
 def hypic_segment_build(args: BuildArgs, workspace: int, workspace_bytes: int, stream: int) -> int:
     return lib.hypic_segment_build(ctypes.byref(args), workspace, workspace_bytes, stream)
+
+
+def hypic_segment_build_noalloc(args: BuildArgs, stream: int) -> int:
+    return lib.hypic_segment_build_noalloc(ctypes.byref(args), stream)
 
 
 def hypic_compose(args: ComposeArgs, stream: int) -> int:

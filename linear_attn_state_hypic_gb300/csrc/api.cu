@@ -382,6 +382,10 @@ extern "C" const char* hypic_status_string(hypic_status s) {
 
 extern "C" const char* hypic_last_error_detail(void) { return t_detail; }
 
+namespace hypic {
+void set_detail(const char* msg) { snprintf(t_detail, sizeof(t_detail), "%s", msg); }
+}  // namespace hypic
+
 extern "C" int hypic_version(void) { return HYPIC_VERSION; }
 
 extern "C" hypic_status hypic_check_device(hypic_stream_t stream) {

@@ -1,0 +1,76 @@
+// build_noalloc.cu -- hypic_segment_build_noalloc: the segment build for
+// callers that may not allocate device memory.  Its scratch (the longest-
+// body-first work order and the work counter) lives in a fixed array owned
+// by this library on every device that loads it, instead of in a caller
+// workspace.  Everything else is hypic_segment_build itself.
+#include <cuda_runtime.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "../../include/hypic.h"
+#include "kernels.h"
+
+namespace hypic {
+void set_detail(const char* msg);  // api.cu: sets hypic_last_error_detail()
+}
+
+namespace {
+
+// Same layout as the caller workspace of hypic_segment_build: the order
+// (int32 per segment, padded to 256 bytes) then a 256-byte counter block.
+constexpr size_t kNoallocBytes = ((size_t)HYPIC_NOALLOC_MAX_SEGMENTS * 4 + 255) / 256 * 256 + 256;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the host-side symbol is only a stand-in for it).
+void* scratch_address(cudaError_t* err) {
+    static std::mutex mu;
+    static void* cache[128] = {};
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= 128) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (*err != cudaSuccess) return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+
+extern "C" hypic_status hypic_segment_build_noalloc(const hypic_build_args* args, hypic_stream_t stream) {
+    char msg[256];
+    if (args && args->n_segments > HYPIC_NOALLOC_MAX_SEGMENTS) {
+        snprintf(msg, sizeof(msg),
+                 "no-alloc build: %d segments exceed the fixed scratch limit of %d (use hypic_segment_build "
+                 "with a caller workspace)",
+                 args->n_segments, HYPIC_NOALLOC_MAX_SEGMENTS);
+        hypic::set_detail(msg);
+        return HYPIC_ERR_WORKSPACE;
+    }
+    const size_t need = hypic_build_workspace_size(args);
+    if (need == 0) return hypic_segment_build(args, nullptr, 0, stream);  // reports the argument error
+    if (need > kNoallocBytes) {
+        snprintf(msg, sizeof(msg), "no-alloc build: needs %zu bytes of scratch, the fixed array holds %zu", need,
+                 kNoallocBytes);
+        hypic::set_detail(msg);
+        return HYPIC_ERR_WORKSPACE;
+    }
+    cudaError_t e;
+    void* ws = scratch_address(&e);
+    if (!ws) {
+        snprintf(msg, sizeof(msg), "no-alloc build: address of the fixed scratch: %s", cudaGetErrorString(e));
+        hypic::set_detail(msg);
+        return HYPIC_ERR_CUDA;
+    }
+    return hypic_segment_build(args, ws, kNoallocBytes, stream);
+}
