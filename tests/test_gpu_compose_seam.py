@@ -169,3 +169,22 @@ def test_reuse_path_equals_full_sequential(B):
     full_s, full_o = orc.seam("gdn", inp["q"], inp["k"], inp["v"], [0, n], alpha=inp["alpha"], beta=inp["beta"])
     assert_rel(host(state), full_s, TOL_BF16, what="reuse-path end state")
     assert_rel(host(o), full_o[:, seam_tok], TOL_BF16, axes=(-1,), what="seam outputs")
+
+
+def test_gdn_compose_faithful_pairs_long_chains(B):
+    """Pairs of 512-token segments with strong decay (T_C ~ 1e-18, stored as
+    mantissa x 2^exp with exp near -60) composed along 40-step chains with
+    repeats: the stored exponent must be applied exactly, and the slice ring
+    of the tensor-core path wraps many times."""
+    d, H, P = 128, 2, 6
+    Tm, Te, S32, T64, S64 = gdn_pair_table(5, P, 1, H, d, 512, variant="faithful")
+    assert Te.min() < -40
+    rng = np.random.default_rng(6)
+    chains = [list(rng.integers(0, P, 40)), list(rng.integers(0, P, 17)), [3]]
+    cu = np.array([0] + list(np.cumsum([len(c) for c in chains])), np.int32)
+    idx = np.array([i for c in chains for i in c], np.int32)
+    S0 = (rng.standard_normal((len(chains), 1, H, d, d)) / np.sqrt(d)).astype(np.float32)
+    out = B.compose("gdn", dev(S32), cu, idx, T_tab=dev(Tm), T_exp_tab=dev(Te), S0=dev(S0))
+    B.check_device()
+    ref = orc.compose("gdn", T64, S64, cu, idx, S0=S0)
+    assert_rel(host(out), ref, TOL_F32, what="gdn compose, faithful pairs")
