@@ -188,10 +188,10 @@ __device__ __forceinline__ void load_gates(const TcArgs& a, int layer, int head,
     valid = p < kC && t < t_end;
     ga = 1.f;
     gb = 0.f;
-    if (valid) {
+    if (valid) {  // volatile asm: the loads stay here, a chunk ahead of their use
         const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
-        ga = __ldg(a.alpha + row);
-        gb = __ldg(a.beta + row);
+        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(ga) : "l"(a.alpha + row));
+        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(gb) : "l"(a.beta + row));
     }
 }
 
@@ -254,53 +254,47 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
     }
     named_sync(1);
     const int r = p >> 3, cp = (p & 7) * 2;
-    const float* Arow_base = As + r * kAS;   // + (16 i) kAS selects block row i
-    const float* Mcol_base = As + cp;        // + (16 k + u) kAS + 16 j
-#pragma unroll
+#pragma unroll 1
     for (int i = 1; i < 4; ++i) {
-        const float* Ar = Arow_base + 16 * i * kAS;
-#pragma unroll
+        const float* Ar = As + (16 * i + r) * kAS;
+#pragma unroll 1
         for (int j = 0; j < i; ++j) {
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll 1
+            for (int k = j; k < i; ++k) {
+                const float* ak = Ar + 16 * k;
+                const float* mk = As + 16 * k * kAS + 16 * j + cp;
 #pragma unroll
-            for (int k = j; k < i; ++k)
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float av = Ar[16 * k + u];
-                    const float2 mv = *reinterpret_cast<const float2*>(Mcol_base + (16 * k + u) * kAS + 16 * j);
-                    if (u & 1) {
-                        b0 = fmaf(av, mv.x, b0);
-                        b1 = fmaf(av, mv.y, b1);
-                    } else {
-                        a0 = fmaf(av, mv.x, a0);
-                        a1 = fmaf(av, mv.y, a1);
-                    }
+                for (int u = 0; u < 16; u += 2) {
+                    const float av0 = ak[u], av1 = ak[u + 1];
+                    const float2 m0 = *reinterpret_cast<const float2*>(mk + u * kAS);
+                    const float2 m1 = *reinterpret_cast<const float2*>(mk + (u + 1) * kAS);
+                    a0 = fmaf(av0, m0.x, a0);
+                    a1 = fmaf(av0, m0.y, a1);
+                    b0 = fmaf(av1, m1.x, b0);
+                    b1 = fmaf(av1, m1.y, b1);
                 }
+            }
             *reinterpret_cast<float2*>(Ptmp + (j * 16 + r) * 16 + cp) = make_float2(a0 + b0, a1 + b1);
         }
         named_sync(1);
-        float2 out[3];
-#pragma unroll
+        // Stage 2 reads only M_ii and Ptmp, so M_ij can go straight over A_ij.
+#pragma unroll 1
         for (int j = 0; j < i; ++j) {
             float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            const float* pj = Ptmp + j * 256 + cp;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float mv = Ar[16 * i + u];
-                const float2 pv = *reinterpret_cast<const float2*>(Ptmp + (j * 16 + u) * 16 + cp);
-                if (u & 1) {
-                    b0 = fmaf(mv, pv.x, b0);
-                    b1 = fmaf(mv, pv.y, b1);
-                } else {
-                    a0 = fmaf(mv, pv.x, a0);
-                    a1 = fmaf(mv, pv.y, a1);
-                }
+            for (int u = 0; u < 16; u += 2) {
+                const float m0 = Ar[16 * i + u], m1 = Ar[16 * i + u + 1];
+                const float2 p0 = *reinterpret_cast<const float2*>(pj + u * 16);
+                const float2 p1 = *reinterpret_cast<const float2*>(pj + (u + 1) * 16);
+                a0 = fmaf(m0, p0.x, a0);
+                a1 = fmaf(m0, p0.y, a1);
+                b0 = fmaf(m1, p1.x, b0);
+                b1 = fmaf(m1, p1.y, b1);
             }
-            out[j] = make_float2(-(a0 + b0), -(a1 + b1));
+            *reinterpret_cast<float2*>(As + (16 * i + r) * kAS + 16 * j + cp) = make_float2(-(a0 + b0), -(a1 + b1));
         }
-        named_sync(1);
-        float* Aw = As + (16 * i + r) * kAS + cp;
-#pragma unroll
-        for (int j = 0; j < i; ++j) *reinterpret_cast<float2*>(Aw + 16 * j) = out[j];
         named_sync(1);
     }
 }
@@ -313,7 +307,7 @@ __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, in
     const float* gam = ms->gam[par];
     const int t = p >> 1, half = p & 1;
     const float* row = As + t * kAS + 32 * half;
-#pragma unroll
+#pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
         const float4 x0 = *reinterpret_cast<const float4*>(row + 8 * ch);
         const float4 x1 = *reinterpret_cast<const float4*>(row + 8 * ch + 4);
@@ -342,22 +336,25 @@ __device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, int par
     const int i = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
     const float* ratio = ms->ratio[par];
-    uint32_t w[32];
+    uint32_t w2[2][32];
     uint8_t* bw = smem + OFF_BW + (i >> 5) * 8192;
+    tmem_ld32(tl + TM_GW, w2[0]);
+    tmem_ld32(tl + TM_GW + 32, w2[1]);
+    tmem_wait_ld();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tl + TM_GW + 32 * half, w);
-        tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int t = 32 * half + j;
-            *reinterpret_cast<float*>(bw + sw128_offset(t, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w[j]));
+            *reinterpret_cast<float*>(bw + sw128_offset(t, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w2[half][j]));
         }
     }
+    tmem_ld32(tl + TM_U, w2[0]);
+    tmem_ld32(tl + TM_U + 32, w2[1]);
+    tmem_wait_ld();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        tmem_ld32(tl + TM_U + 32 * half, w);
-        tmem_wait_ld();
+        const uint32_t* w = w2[half];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             uint32_t pk[4];
@@ -382,7 +379,7 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
     const uint32_t tl = tmem + ((32u * q) << 16);
     const int n = 32 * q + lane;
     uint32_t r[32];
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = (32 * cb + j == n) ? 0x3f800000u : 0u;
@@ -390,7 +387,7 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) r[j] = 0u;
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) tmem_st32(tl + TM_DS + 32 * cb, r);
     tmem_wait_st();
 }
@@ -408,31 +405,26 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
     const float* fT = ms->fT;
     const float lc = ms->lg2[par][kC - 1];
     float mloc = 0.f;
-    uint32_t x[32];
+    uint32_t x[2][32];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+        tmem_ld32(tl + (h ? TM_XS : TM_XT), x[0]);
+        tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32, x[1]);
+        tmem_wait_ld();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32 * half, x);
-            tmem_wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 uint32_t pk[4], lo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = 32 * half + 8 * jj + 2 * k;
-                    float f0, f1;
-                    if (h) {
-                        f0 = -ratio[t];
-                        f1 = -ratio[t + 1];
-                    } else {
-                        f0 = fT[t];
-                        f1 = fT[t + 1];
-                    }
-                    const float y0 = f0 * __uint_as_float(x[8 * jj + 2 * k]);
-                    const float y1 = f1 * __uint_as_float(x[8 * jj + 2 * k + 1]);
+                    const float f0 = h ? -ratio[t] : fT[t];
+                    const float f1 = h ? -ratio[t + 1] : fT[t + 1];
+                    const float y0 = f0 * __uint_as_float(x[half][8 * jj + 2 * k]);
+                    const float y1 = f1 * __uint_as_float(x[half][8 * jj + 2 * k + 1]);
                     pk[k] = pack_bf16(y0, y1);
-                    lo[k] = pack_bf16(y0 - bf16_round(y0), y1 - bf16_round(y1));
+                    if (!h) lo[k] = pack_bf16(y0 - bf16_round(y0), y1 - bf16_round(y1));
                 }
                 const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((4 * half + jj) ^ (n & 7)) << 4);
                 st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
@@ -441,17 +433,21 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
         }
         const float sc = h ? exp2f(lc) : exp2f(lc - (float)e);
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 0; cb < 4; cb += 2) {
             const uint32_t addr = tl + (h ? TM_DS : TM_DT) + 32 * cb;
-            tmem_ld32(addr, x);
+            tmem_ld32(addr, x[0]);
+            tmem_ld32(addr + 32, x[1]);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float v = __uint_as_float(x[j]) * sc;
-                if (!h) mloc = fmaxf(mloc, fabsf(v));
-                x[j] = __float_as_uint(v);
-            }
-            tmem_st32(addr, x);
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float v = __uint_as_float(x[b][j]) * sc;
+                    if (!h) mloc = fmaxf(mloc, fabsf(v));
+                    x[b][j] = __float_as_uint(v);
+                }
+            tmem_st32(addr, x[0]);
+            tmem_st32(addr + 32, x[1]);
         }
     }
     tmem_wait_st();
@@ -474,7 +470,7 @@ __device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, int E, ui
     const uint32_t tl = tmem + ((32u * q) << 16);
     uint32_t x[32];
     float m = 0.f;
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         tmem_ld32(tl + TM_DT + 32 * cb, x);
         tmem_wait_ld();
@@ -485,14 +481,14 @@ __device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, int E, ui
     const int ef = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
     float* T = a.T_out + obj * kD * kD;
     float* S = a.S_out + obj * kD * kD;
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         tmem_ld32(tl + TM_DT + 32 * cb, x);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) T[(32 * cb + j) * kD + n] = ldexpf(__uint_as_float(x[j]), -ef);
     }
-#pragma unroll
+#pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         tmem_ld32(tl + TM_DS + 32 * cb, x);
         tmem_wait_ld();
