@@ -35,6 +35,13 @@ WORKLOAD = dict(n_layers=30, H=32, d=128, n_tokens=100_000, seam_w=8)
 FLOP_PER_TOKEN_HEAD = 180_224      # chunk-64 low-rank GDN build (gram, W, U, two state GEMMs)
 COMPOSE_BYTES = 131_072            # T_p + S_p (fp32, d=128) streamed per head-compose
 SEAM_STATE_BYTES = 131_072         # state read + write per seam-head
+# DRAM bytes per algorithmic byte of the build kernel, from an ncu capture of
+# the 32-segment x 32-head ragged batch (830.4 MB of traffic for 815.8 MB of
+# inputs and outputs); the full launch is too large to capture, and its
+# traffic scales with the same units (token-heads in, (segment, head) out).
+BUILD_TRAFFIC_RATIO = 830.4 / 815.8
+BUILD_IN_BYTES_PER_TOKEN_HEAD = 520   # k, v bf16 (2 x 256 B) + alpha, beta fp32
+BUILD_OUT_BYTES_PER_ITEM = 131_076    # T_C and S(C|0) fp32 (2 x 64 KB) + exponent
 
 
 def load_peaks():
@@ -312,6 +319,94 @@ def allreduce_max(x, world):
     return float(t.item())
 
 
+def time_compose_table(steps, device, n_layers=30):
+    """hypic_compose on the compose-table workload: 30 layers x 32 heads, a
+    table of 128 cached pairs (fp32 T mantissa + exponent, S), 16 chains of
+    64 distinct pairs each (half from zero, half from a random start).  The
+    T values are random with spectral norm ~0.7 (the kernel's time does not
+    depend on them).  Returns timing and the algorithmic-byte roofline."""
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+    from linear_attn_state_hypic_gb300 import synth
+    L, H, d, P = n_layers, 32, 128, 128
+    ch = synth.compose_chains(seed=0, n_layers=L, with_tables=False)
+    g = torch.Generator(device=device)
+    g.manual_seed(1)
+    T_tab = torch.randn((P, L, H, d, d), generator=g, device=device) * (0.35 / np.sqrt(d))
+    S_tab = torch.randn((P, L, H, d, d), generator=g, device=device) * (1.0 / np.sqrt(d))
+    T_exp = torch.randint(-2, 2, (P, L, H), generator=g, device=device, dtype=torch.int32)
+    S0 = torch.from_numpy(ch["S0"]).to(device)
+    out = torch.empty_like(S0)
+    a, keep = B.compose_args("gdn", S_tab, ch["cu_chain"], ch["seg_idx"], T_tab=T_tab, T_exp_tab=T_exp, S0=S0,
+                             S_out=out)
+    sp = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        if B.hypic_compose(a, sp) != 0:
+            raise RuntimeError("compose failed")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        B.hypic_compose(a, sp)
+    e1.record()
+    torch.cuda.synchronize()
+    B.check_device(sp)
+    ms = e0.elapsed_time(e1) / steps
+    n_chain, n_steps = 16, 64
+    head_composes = n_chain * n_steps * L * H
+    state_bytes = d * d * 4 * L * H
+    algo = head_composes * COMPOSE_BYTES + n_chain * state_bytes + (n_chain // 2) * state_bytes
+    del keep
+    return {"workload": f"compose table: {L} layers x 32 heads, d=128, fp32 pairs (128 cached segments), "
+                        "16 chains x 64 pairs, half from a random start state",
+            "ms_per_call": ms, "head_composes_per_s": head_composes / (ms / 1e3),
+            "composes_per_s": n_chain * n_steps / (ms / 1e3),
+            "algorithmic_bytes": algo, "gbs_algorithmic": algo / (ms / 1e3) / 1e9,
+            "note": "chains that share a (layer, head) run on neighbouring SMs and re-read the same pairs, "
+                    "which then come from L2: algorithmic GB/s can exceed the DRAM traffic"}
+
+
+def run_case(args, device):
+    """Single-kernel cases used for profiling (one JSON line each):
+    ragged_build -- the build of 32 ragged segments (U[512,2048] tokens) x 32
+                    heads, d=128, bf16 (one layer);
+    compose_table -- hypic_compose on the compose table with --layers layers."""
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+    from linear_attn_state_hypic_gb300 import synth
+    torch.cuda.set_device(device)
+    peaks, peak_src = load_peaks()
+    if args.case == "compose_table":
+        r = time_compose_table(args.steps, device, n_layers=args.layers)
+        r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
+        print(json.dumps({"case": args.case, **r}))
+        return
+    inp = synth.gdn_ragged(seed=0)
+    k = torch.from_numpy(inp["k"]).to(torch.bfloat16).to(device)
+    v = torch.from_numpy(inp["v"]).to(torch.bfloat16).to(device)
+    a = torch.from_numpy(inp["alpha"]).to(device)
+    b = torch.from_numpy(inp["beta"]).to(device)
+    cu = inp["cu_seqlens"]
+    out = B.alloc_build_outputs("gdn", len(cu) - 1, 1, 32, 128, 128, device)
+    for _ in range(args.warmup):
+        B.segment_build("gdn", k, v, cu, alpha=a, beta=b, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        B.segment_build("gdn", k, v, cu, alpha=a, beta=b, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    B.check_device()
+    ms = e0.elapsed_time(e1) / args.steps
+    ntok = int(cu[-1])
+    tf = ntok * 32 * FLOP_PER_TOKEN_HEAD / (ms / 1e3) / 1e12
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    print(json.dumps({"case": args.case, "ms_per_call": ms, "tokens": ntok, "heads": 32,
+                      "tokens_per_s": ntok / (ms / 1e3), "tflops": tf, "frac_bf16": tf / peak_t,
+                      "peak_source": peak_src}))
+
+
 def workload_config(n_seg=None):
     W = WORKLOAD
     return {"workload": (f"long cold request + seam: {W['n_layers']} GDN layers x {W['H']} heads, d={W['d']}, "
@@ -332,6 +427,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-compose-table", action="store_true")
+    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table"], default="long_request",
+                    help="long_request is the benchmark; the others time one kernel (for profiling)")
+    ap.add_argument("--layers", type=int, default=30, help="layers of the compose_table case")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -361,6 +460,10 @@ def main():
         print(json.dumps(line))
         return
 
+    if args.case != "long_request":
+        if rank == 0:
+            run_case(args, int(os.environ.get("LOCAL_RANK", "0")))
+        return
     import torch
     if world > 1:
         import torch.distributed as dist
@@ -389,6 +492,13 @@ def main():
                    "steps": args.e2e_steps}
         except Exception as ex:  # pinned host memory can be unavailable; report why
             e2e = {"value": None, "unit": "tokens/s", "error": f"{type(ex).__name__}: {ex}"[:200]}
+    ctab = None
+    if not args.no_compose_table:
+        del req
+        import torch
+        torch.cuda.empty_cache()
+        ctab = time_compose_table(max(3, args.steps), device)
+        ctab["frac_hbm"] = ctab["gbs_algorithmic"] / peaks["hbm_gbs"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, secs, desc = oracle_rate(15.0, threads)
@@ -399,7 +509,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, drawn on the device)",
+        "vs_baseline": None, "dtype": "bf16",
+        "precision": "bf16 tensor-core products (tf32 / 3xtf32 where the state is an operand), fp32 accumulation, "
+                     "fp32 state and T_C (with a power-of-two exponent)",
+        "data": "synthetic (seeded, drawn on the device)",
         "config": workload_config(res["n_seg"]),
         "composes_per_s": world * n_comp * args.steps / (res["ms"] / 1e3),
         "head_composes_per_s": world * n_comp * LH * args.steps / (res["ms"] / 1e3),
@@ -407,8 +520,12 @@ def main():
                    "chain_ms": res["chain_ms"], "chain_gbs_algorithmic": chain_gbs,
                    "chain_frac_hbm": chain_gbs / peaks["hbm_gbs"]},
         "roofline": {"kernel": "segment build (GDN)", "bound": "tensor", "achieved": build_tflops,
-                     "peak": peak_t, "unit": "TFLOP/s", "frac": build_tflops / peak_t, "traffic": None,
+                     "peak": peak_t, "unit": "TFLOP/s", "frac": build_tflops / peak_t,
+                     "traffic": BUILD_TRAFFIC_RATIO * (res["body_tokens"] * LH * BUILD_IN_BYTES_PER_TOKEN_HEAD
+                                                       + res["n_seg"] * LH * BUILD_OUT_BYTES_PER_ITEM),
+                     "traffic_note": "dram bytes per launch, scaled from an ncu capture of a 32x32 ragged batch",
                      "peak_source": f"{peak_src} bf16 sustained", "flop_per_token_head": FLOP_PER_TOKEN_HEAD},
+        "compose_table": ctab,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": res["launches"], "clocks": res["clocks"],
     }
     print(json.dumps(line))
