@@ -30,7 +30,7 @@
 //
 // Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 the
 // state warpgroup (tensor-memory passes, epilogue), warps 6-9 the prep
-// warpgroup (gates, gram -> That, W/U conversion).  They meet on mbarriers;
+// warpgroup (gates, gram -> That); the state warpgroup also converts W/U.  They meet on mbarriers;
 // every wait is bounded and a wait that runs out sets the device error word.
 // One CTA per SM, persistent over (segment, layer, head) items taken from an
 // atomic queue in longest-body-first order.
@@ -55,6 +55,7 @@ using namespace tc;
 constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
 constexpr int kStages = 2;        // K/V ring depth
+constexpr int kGateSlots = 3;     // per-chunk gate tables in flight (prep runs up to two chunks ahead)
 constexpr int kThreads = 320;
 constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6;
 
@@ -73,10 +74,11 @@ constexpr uint32_t OFF_MISC = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;
 struct Misc {
     uint64_t full[kStages], empty[kStages];
     uint64_t g_done, that_ready, w_done, wu_cvt, x_done, y_ready, d_ready, drain;
-    float lg2[2][kC], beta[2][kC], ratio[2][kC], gam[2][kC];  // per chunk parity
-    float up[2][kC], wn[2][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
+    float lg2[kGateSlots][kC], beta[kGateSlots][kC], ratio[kGateSlots][kC], gam[kGateSlots][kC];  // slot gc % 3
+    float up[kGateSlots][kC], wn[kGateSlots][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
     float fT[kC];                // state pass: -(g_C/g_t) 2^-e for the T half
     float scan_tot;
+    float gstage[2][2][kC];      // next chunk's raw a, b (cp.async target), double-buffered
     float red[2][4];
     float red_ep[4];
     int item;
@@ -107,17 +109,22 @@ struct TcArgs {
     const int32_t* order;
     unsigned* counter;
     unsigned* err;
-    uint32_t wait_limit;
+    uint32_t wait_limit;  // polls of the final drain
+    uint64_t wait_ns;     // time limit of every other wait
 };
 
-// Bounded wait shared by all roles: gives up (and raises the CTA's abort
-// flag and the device error word) after `limit` polls, or at once when
-// another role already gave up.
+// Bounded wait shared by all roles: the waiting warp sleeps until the phase
+// completes (re-polling at least every few microseconds); it gives up, and
+// raises the CTA's abort flag and the device error word, once `wait_ns` of
+// GPU time have passed, or at once when another role already gave up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
-    for (uint32_t i = 0; i < a.wait_limit; i += 256) {
-        for (int j = 0; j < 256; ++j)
-            if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int j = 0; j < 16; ++j)
+            if (mbar_try_wait_sleep(bar, parity, 4000u)) return true;
         if (*(volatile int*)&ms->abort_flag) return false;
+        if (globaltimer_ns() - t0 > a.wait_ns) break;
     }
     *(volatile int*)&ms->abort_flag = 1;
     set_error(a.err, kErrTimeout);
@@ -181,19 +188,28 @@ __device__ void prep_gates(Misc* ms, int par, float a_raw, float b_raw, bool val
     named_sync(1);
 }
 
-// This thread's gates for token t0 + p (p < 64) of the chunk starting at t0.
-__device__ __forceinline__ void load_gates(const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end, int p,
-                                           float& ga, float& gb, bool& valid) {
+// Thread p (< 64) starts the copy of token t0 + p's raw gates into staging
+// buffer `buf` (cp.async: nothing is held in registers while the copy is in
+// flight).  Returns whether the token lies inside the body.
+__device__ __forceinline__ bool stage_gates(Misc* ms, const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end,
+                                            int p, int buf) {
     const int64_t t = t0 + p;
-    valid = p < kC && t < t_end;
-    ga = 1.f;
-    gb = 0.f;
-    if (valid) {  // volatile asm: the loads stay here, a chunk ahead of their use
+    const bool valid = p < kC && t < t_end;
+    if (valid) {
         const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
-        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(ga) : "l"(a.alpha + row));
-        asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(gb) : "l"(a.beta + row));
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&ms->gstage[buf][0][p])),
+                     "l"(a.alpha + row)
+                     : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&ms->gstage[buf][1][p])),
+                     "l"(a.beta + row)
+                     : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    return valid;
 }
+// Waits for this thread's copies up to (and including) the older group.
+__device__ __forceinline__ void stage_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void stage_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Rows of A from the gram matrix in tensor memory (M=64 accumulator layout:
 // row 16q + l sits in lane 32q + l, l < 16):
@@ -222,81 +238,129 @@ __device__ void prep_arows(const Misc* ms, float* As, int par, uint32_t tmem, in
 }
 
 // (I + A)^-1 in place, A strictly lower triangular 64 x 64 (row stride kAS),
-// by 16 x 16 blocks.  Diagonal blocks: forward substitution, one column per
-// thread (threads 0..63).  Block rows i = 1..3: P_ij = sum_{k=j}^{i-1} A_ik M_kj
-// into Ptmp, then M_ij = -M_ii P_ij; each thread owns a row r and a column
-// pair (2 outputs per load of A).  All loops are unrolled so every address is
-// the thread's base plus an immediate.
+// by recursive doubling on the block-triangular inverse
+//   [[L11, 0], [L21, L22]]^-1 = [[M11, 0], [-M22 L21 M11, M22]]:
+//   level 1: the four 16 x 16 diagonal blocks, forward substitution by
+//            columns (threads 0..63, one column each);
+//   level 2: blocks (1,0) and (3,2), from the level-1 inverses;
+//   level 3: the lower-left 32 x 32 block, from the two 32 x 32 inverses.
+// Each product is register-tiled (4 or 8 outputs per thread) with the inner
+// sum over the full block: the zero upper parts of the triangular factors
+// make that exact.  Ptmp holds the left products.
 __device__ void prep_solve(float* As, float* Ptmp, int p) {
-    float m[16];
-    if (p < kC) {
+    if (p < kC) {  // level 1
         const int b = p >> 4, c = p & 15;
         const float* Ab = As + 16 * b * kAS + 16 * b;
+        float s[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m[i] = (i == c) ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) s[i] = (i == c) ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 1; i < 16; ++i) {
-            float s0 = 0.f, s1 = 0.f;
+        for (int j = 0; j < 15; ++j) {
+            const float mj = s[j];
 #pragma unroll
-            for (int j = 0; j < i; ++j) {
-                if (j & 1) s1 = fmaf(Ab[i * kAS + j], m[j], s1);
-                else s0 = fmaf(Ab[i * kAS + j], m[j], s0);
-            }
-            if (i > c) m[i] = -(s0 + s1);
+            for (int i = j + 1; i < 16; ++i) s[i] = fmaf(-Ab[i * kAS + j], mj, s[i]);
         }
+        float* Mb = As + 16 * b * kAS + 16 * b + c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Mb[i * kAS] = s[i];
     }
     named_sync(1);
-    if (p < kC) {
-        const int b = p >> 4, c = p & 15;
-        float* Ab = As + 16 * b * kAS + 16 * b;
+    {  // level 2: P = A_{x+1,x} M_xx, then M_{x+1,x} = -M_{x+1,x+1} P, x = 0, 2
+        const int x = 2 * (p >> 6), r = (p >> 2) & 15, c0 = (p & 3) * 4;
+        const float* Arow = As + (16 * (x + 1) + r) * kAS + 16 * x;
+        const float* Mcol = As + 16 * x * kAS + 16 * x + c0;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) Ab[i * kAS + c] = m[i];
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(Arow + k4);
+            const float ak[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 m = *reinterpret_cast<const float4*>(Mcol + (k4 + u) * kAS);
+                acc.x = fmaf(ak[u], m.x, acc.x);
+                acc.y = fmaf(ak[u], m.y, acc.y);
+                acc.z = fmaf(ak[u], m.z, acc.z);
+                acc.w = fmaf(ak[u], m.w, acc.w);
+            }
+        }
+        float* P = Ptmp + (p >> 6) * 256;
+        *reinterpret_cast<float4*>(P + r * 16 + c0) = acc;
+        named_sync(1);
+        const float* Mrow = As + (16 * (x + 1) + r) * kAS + 16 * (x + 1);
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 mv = *reinterpret_cast<const float4*>(Mrow + k4);
+            const float mk[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 q = *reinterpret_cast<const float4*>(P + (k4 + u) * 16 + c0);
+                acc.x = fmaf(mk[u], q.x, acc.x);
+                acc.y = fmaf(mk[u], q.y, acc.y);
+                acc.z = fmaf(mk[u], q.z, acc.z);
+                acc.w = fmaf(mk[u], q.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4*>(As + (16 * (x + 1) + r) * kAS + 16 * x + c0) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     named_sync(1);
-    const int r = p >> 3, cp = (p & 7) * 2;
-#pragma unroll 1
-    for (int i = 1; i < 4; ++i) {
-        const float* Ar = As + (16 * i + r) * kAS;
-#pragma unroll 1
-        for (int j = 0; j < i; ++j) {
-            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-#pragma unroll 1
-            for (int k = j; k < i; ++k) {
-                const float* ak = Ar + 16 * k;
-                const float* mk = As + 16 * k * kAS + 16 * j + cp;
+    {  // level 3: P = A[32:64, 0:32] M[0:32, 0:32], then M[32:64, 0:32] = -M[32:64, 32:64] P
+        const int r = p >> 2, c0 = (p & 3) * 8;
+        const float* Arow = As + (32 + r) * kAS;
+        const float* Mcol = As + c0;
+        float acc[8];
 #pragma unroll
-                for (int u = 0; u < 16; u += 2) {
-                    const float av0 = ak[u], av1 = ak[u + 1];
-                    const float2 m0 = *reinterpret_cast<const float2*>(mk + u * kAS);
-                    const float2 m1 = *reinterpret_cast<const float2*>(mk + (u + 1) * kAS);
-                    a0 = fmaf(av0, m0.x, a0);
-                    a1 = fmaf(av0, m0.y, a1);
-                    b0 = fmaf(av1, m1.x, b0);
-                    b1 = fmaf(av1, m1.y, b1);
-                }
-            }
-            *reinterpret_cast<float2*>(Ptmp + (j * 16 + r) * 16 + cp) = make_float2(a0 + b0, a1 + b1);
-        }
-        named_sync(1);
-        // Stage 2 reads only M_ii and Ptmp, so M_ij can go straight over A_ij.
-#pragma unroll 1
-        for (int j = 0; j < i; ++j) {
-            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-            const float* pj = Ptmp + j * 256 + cp;
+        for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+#pragma unroll 2
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(Arow + k4);
+            const float ak[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-            for (int u = 0; u < 16; u += 2) {
-                const float m0 = Ar[16 * i + u], m1 = Ar[16 * i + u + 1];
-                const float2 p0 = *reinterpret_cast<const float2*>(pj + u * 16);
-                const float2 p1 = *reinterpret_cast<const float2*>(pj + (u + 1) * 16);
-                a0 = fmaf(m0, p0.x, a0);
-                a1 = fmaf(m0, p0.y, a1);
-                b0 = fmaf(m1, p1.x, b0);
-                b1 = fmaf(m1, p1.y, b1);
+            for (int u = 0; u < 4; ++u) {
+                const float4 m0 = *reinterpret_cast<const float4*>(Mcol + (k4 + u) * kAS);
+                const float4 m1 = *reinterpret_cast<const float4*>(Mcol + (k4 + u) * kAS + 4);
+                acc[0] = fmaf(ak[u], m0.x, acc[0]);
+                acc[1] = fmaf(ak[u], m0.y, acc[1]);
+                acc[2] = fmaf(ak[u], m0.z, acc[2]);
+                acc[3] = fmaf(ak[u], m0.w, acc[3]);
+                acc[4] = fmaf(ak[u], m1.x, acc[4]);
+                acc[5] = fmaf(ak[u], m1.y, acc[5]);
+                acc[6] = fmaf(ak[u], m1.z, acc[6]);
+                acc[7] = fmaf(ak[u], m1.w, acc[7]);
             }
-            *reinterpret_cast<float2*>(As + (16 * i + r) * kAS + 16 * j + cp) = make_float2(-(a0 + b0), -(a1 + b1));
         }
+        float* P = Ptmp + r * 36 + c0;  // 32 x 32, row stride 36 (keeps float4 rows 16-byte aligned)
+        *reinterpret_cast<float4*>(P) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(P + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         named_sync(1);
+        const float* Mrow = As + (32 + r) * kAS + 32;
+        const float* Pc = Ptmp + c0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+#pragma unroll 2
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 mv = *reinterpret_cast<const float4*>(Mrow + k4);
+            const float mk[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 q0 = *reinterpret_cast<const float4*>(Pc + (k4 + u) * 36);
+                const float4 q1 = *reinterpret_cast<const float4*>(Pc + (k4 + u) * 36 + 4);
+                acc[0] = fmaf(mk[u], q0.x, acc[0]);
+                acc[1] = fmaf(mk[u], q0.y, acc[1]);
+                acc[2] = fmaf(mk[u], q0.z, acc[2]);
+                acc[3] = fmaf(mk[u], q0.w, acc[3]);
+                acc[4] = fmaf(mk[u], q1.x, acc[4]);
+                acc[5] = fmaf(mk[u], q1.y, acc[5]);
+                acc[6] = fmaf(mk[u], q1.z, acc[6]);
+                acc[7] = fmaf(mk[u], q1.w, acc[7]);
+            }
+        }
+        float* out = As + (32 + r) * kAS + c0;
+        *reinterpret_cast<float4*>(out) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+        *reinterpret_cast<float4*>(out + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
     }
+    named_sync(1);
 }
 
 // That Diag(g) (bf16 hi at bt, residual lo at bt + 16384) and
@@ -579,6 +643,11 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
         if (!wait_bar(&ms->wu_cvt, gc & 1, ms, a)) return;
+        if (c + 1 < nc) {  // gram of the next chunk first: the prep chain is the longer one
+            if (!wait_bar(&ms->full[(gc + 1) % kStages], ((gc + 1) / kStages) & 1, ms, a)) return;
+            tc_fence_after();
+            gram(gc + 1);
+        }
         if (c > 0 && !wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a)) return;
         tc_fence_after();
         // GEMM1 (tf32): X'_h = D'_h W^T, A = the state itself in tensor memory.
@@ -589,11 +658,6 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k,
                             sdesc_sw128(bw + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024), ID_G1, k > 0);
         mma_commit(&ms->x_done);
-        if (c + 1 < nc) {  // gram of the next chunk while the state warpgroup runs its pass
-            if (!wait_bar(&ms->full[(gc + 1) % kStages], ((gc + 1) / kStages) & 1, ms, a)) return;
-            tc_fence_after();
-            gram(gc + 1);
-        }
         if (!wait_bar(&ms->y_ready, gc & 1, ms, a)) return;
         tc_fence_after();
         // GEMM2 (bf16): D'_T += Y'_T K; D'_S += Y'_S K + U~^T K.
@@ -621,15 +685,22 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
     float* Ptmp = reinterpret_cast<float*>(smem + OFF_BT);
     const uint32_t sb = smem_u32(smem);
-    float ga, gb;
-    bool gv;
-    load_gates(a, layer, head, b0, b1, p, ga, gb, gv);
+    bool gv = stage_gates(ms, a, layer, head, b0, b1, p, 0);
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
-        const int par = gc & 1;
-        const float ca = ga, cb = gb;
+        const int par = gc % kGateSlots;
         const bool cv = gv;
-        if (c + 1 < nc) load_gates(a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, p, ga, gb, gv);  // next chunk
+        float ca = 1.f, cb = 0.f;
+        if (c + 1 < nc) {  // next chunk's copy goes out before this one's is read
+            gv = stage_gates(ms, a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, p, (c + 1) & 1);
+            stage_wait_prev();
+        } else {
+            stage_wait_all();
+        }
+        if (cv) {
+            ca = ms->gstage[c & 1][0][p];
+            cb = ms->gstage[c & 1][1][p];
+        }
         prep_gates(ms, par, ca, cb, cv, p, lane);
         if (!wg_all(1, wait_bar(&ms->g_done, gc & 1, ms, a))) return;
         tc_fence_after();
@@ -641,14 +712,24 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         fence_async_smem();
         named_sync(1);
         if (p == 0) mbar_arrive(&ms->that_ready);
-        if (!wg_all(1, wait_bar(&ms->w_done, gc & 1, ms, a))) return;
-        tc_fence_after();
-        prep_convert(ms, smem, sb + OFF_AU, par, tmem, q, lane);
-        fence_async_smem();
-        tc_fence_before();
-        named_sync(1);
-        if (p == 0) mbar_arrive(&ms->wu_cvt);
     }
+}
+
+// W and U~ of chunk gc, once its W/U MMAs are done, into GEMM1's and GEMM2's
+// operands.  The state warpgroup does this between its passes: it is idle
+// while the prep warpgroup works on the next chunk's solve.
+__device__ __forceinline__ bool state_convert(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t gc,
+                                              int q, int lane) {
+    bool ok = wait_bar(&ms->that_ready, gc & 1, ms, a);  // also makes the chunk's gate tables visible
+    ok = ok && wait_bar(&ms->w_done, gc & 1, ms, a);
+    if (!wg_all(2, ok)) return false;
+    tc_fence_after();
+    prep_convert(ms, smem, smem_u32(smem) + OFF_AU, gc % kGateSlots, tmem, q, lane);
+    fence_async_smem();
+    tc_fence_before();
+    named_sync(2);
+    if (q == 0 && lane == 0) mbar_arrive(&ms->wu_cvt);
+    return true;
 }
 
 __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc,
@@ -659,14 +740,13 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         return;
     }
     const uint32_t ay = smem_u32(smem) + OFF_AY;
+    if (!state_convert(ms, smem, a, tmem, g, q, lane)) return;
     int E = 0;
     float m = 1.f;
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
-        const int par = gc & 1;
-        bool ok = wait_bar(&ms->x_done, gc & 1, ms, a);
-        ok = ok && wait_bar(&ms->wu_cvt, gc & 1, ms, a);  // this chunk's gates are visible
-        if (!wg_all(2, ok)) return;
+        const int par = gc % kGateSlots;
+        if (!wg_all(2, wait_bar(&ms->x_done, gc & 1, ms, a))) return;
         tc_fence_after();
         const float lc = ms->lg2[par][kC - 1];
         const int e = ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lc);
@@ -675,9 +755,10 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         const float mloc = state_pass(ms, ay, par, e, tmem, q, lane);
         fence_async_smem();
         tc_fence_before();
-        m = state_reduce_max(mloc, ms->red[par], q, lane);
+        m = state_reduce_max(mloc, ms->red[gc & 1], q, lane);
         if (n == 0) mbar_arrive(&ms->y_ready);
         E += e;
+        if (c + 1 < nc && !state_convert(ms, smem, a, tmem, gc + 1, q, lane)) return;
     }
     if (!wg_all(2, wait_bar(&ms->d_ready, (g + nc - 1) & 1, ms, a))) return;
     tc_fence_after();
@@ -834,6 +915,7 @@ cudaError_t launch_gdn_build_tc(const BuildParams& p, void* workspace, unsigned*
     a.counter = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(workspace) + build_workspace_bytes(p.n_seg) - 256);
     a.err = err;
     a.wait_limit = 1u << 26;
+    a.wait_ns = 2000000000ull;  // 2 s
     if (a.n_items == 0) return cudaSuccess;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
