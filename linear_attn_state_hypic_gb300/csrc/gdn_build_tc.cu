@@ -74,9 +74,10 @@ constexpr uint32_t OFF_MISC = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;
 struct Misc {
     uint64_t full[kStages], empty[kStages];
     uint64_t g_done, that_ready, w_done, wu_cvt, x_done, y_ready, d_ready, drain;
-    float lg2[kGateSlots][kC], beta[kGateSlots][kC], ratio[kGateSlots][kC], gam[kGateSlots][kC];  // slot gc % 3
+    float lg2[kGateSlots][kC], beta[kGateSlots][kC], gam[kGateSlots][kC];  // slot gc % 3
     float up[kGateSlots][kC], wn[kGateSlots][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
-    float fT[kC];                // state pass: -(g_C/g_t) 2^-e for the T half
+    float fT[kC], fS[kC];        // state pass: Y'' = f X'' for the T and S halves
+    float uf[kC];                // U~ = Diag(uf) U
     float scan_tot;
     float gstage[2][2][kC];      // next chunk's raw a, b (cp.async target), double-buffered
     float red[2][4];
@@ -154,7 +155,7 @@ __device__ __forceinline__ float tf32_rna(float x) {
 // lane quarter; lane: lane in the warp.
 
 // Gates of one chunk: lg2[t] = sum_{s<=t} log2 a_s (inclusive prefix inside
-// the chunk), ratio[t] = g_C/g_t, gam[t] = g_t, beta[t].  Padded tokens
+// the chunk), gam[t] = g_t, beta[t].  Padded tokens
 // past the segment end get a = 1, b = 0: an identity transition, so the
 // padded rows leave the result unchanged.
 __device__ void prep_gates(Misc* ms, int par, float a_raw, float b_raw, bool valid, int p, int lane) {
@@ -180,7 +181,6 @@ __device__ void prep_gates(Misc* ms, int par, float a_raw, float b_raw, bool val
     named_sync(1);
     if (p < kC) {
         const float lc = ms->lg2[par][kC - 1], h = 0.5f * lc;
-        ms->ratio[par][p] = exp2f(lc - la);
         ms->gam[par][p] = exp2f(la);
         ms->up[par][p] = exp2f(la - h);
         ms->wn[par][p] = exp2f(h - la);
@@ -394,12 +394,12 @@ __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, in
 }
 
 // W^T (lane i holds W[.][i]) -> W as a tf32 K-major [64 t][128 i] operand;
-// U^T (lane n holds U[.][n]) -> U~^T = U^T Diag(g_C/g_t) as a bf16 K-major
-// [128 n][64 t] operand.
-__device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, int par, uint32_t tmem, int q, int lane) {
+// U^T (lane n holds U[.][n]) -> U~^T = U^T Diag(uf) as a bf16 K-major
+// [128 n][64 t] operand (uf: the chunk's U factors, see state_plan).
+__device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, uint32_t tmem, int q, int lane) {
     const int i = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    const float* ratio = ms->ratio[par];
+    const float* uf = ms->uf;
     uint32_t w2[2][32];
     uint8_t* bw = smem + OFF_BW + (i >> 5) * 8192;
     tmem_ld32(tl + TM_GW, w2[0]);
@@ -425,8 +425,8 @@ __device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, int par
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = 32 * half + 8 * jj + 2 * k;
-                pk[k] = pack_bf16(__uint_as_float(w[8 * jj + 2 * k]) * ratio[t],
-                                  __uint_as_float(w[8 * jj + 2 * k + 1]) * ratio[t + 1]);
+                pk[k] = pack_bf16(__uint_as_float(w[8 * jj + 2 * k]) * uf[t],
+                                  __uint_as_float(w[8 * jj + 2 * k + 1]) * uf[t + 1]);
             }
             const uint32_t off = i * 128u + ((uint32_t)((4 * half + jj) ^ (i & 7)) << 4);
             st_shared_v4(au + off, pk[0], pk[1], pk[2], pk[3]);
@@ -456,22 +456,21 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
     tmem_wait_st();
 }
 
-// After GEMM1 of a chunk: Y'_h rows into shared memory (bf16, K-major
-// [128 n][64 t]; Y'_T also as its bf16 residual) and the decay of D' in
-// tensor memory.  The T half is also
-// scaled by 2^-e (exponent bookkeeping); returns the max |.| of the new T row.
-//   Y'_T[n][t] = -(g_C/g_t) 2^-e X'_T[n][t],  D'_T <- g_C 2^-e D'_T
-//   Y'_S[n][t] = -(g_C/g_t) X'_S[n][t],       D'_S <- g_C D'_S
-__device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_t tmem, int q, int lane) {
+// After GEMM1 of a chunk: Y''_h = Diag-scaled X''_h rows into shared memory
+// (bf16, K-major [128 n][64 t]; Y''_T also as its bf16 residual):
+//   Y''_T[n][t] = fT[t] X''_T[n][t],  Y''_S[n][t] = fS[t] X''_S[n][t].
+// On a renormalisation chunk the stored state is also rescaled in tensor
+// memory, D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new
+// T rows is returned (else 0).
+__device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, float dS, uint32_t tmem, int q,
+                            int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    const float* ratio = ms->ratio[par];
-    const float* fT = ms->fT;
-    const float lc = ms->lg2[par][kC - 1];
     float mloc = 0.f;
     uint32_t x[2][32];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+        const float* f = h ? ms->fS : ms->fT;
         tmem_ld32(tl + (h ? TM_XS : TM_XT), x[0]);
         tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32, x[1]);
         tmem_wait_ld();
@@ -483,10 +482,8 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = 32 * half + 8 * jj + 2 * k;
-                    const float f0 = h ? -ratio[t] : fT[t];
-                    const float f1 = h ? -ratio[t + 1] : fT[t + 1];
-                    const float y0 = f0 * __uint_as_float(x[half][8 * jj + 2 * k]);
-                    const float y1 = f1 * __uint_as_float(x[half][8 * jj + 2 * k + 1]);
+                    const float y0 = f[t] * __uint_as_float(x[half][8 * jj + 2 * k]);
+                    const float y1 = f[t + 1] * __uint_as_float(x[half][8 * jj + 2 * k + 1]);
                     pk[k] = pack_bf16(y0, y1);
                     if (!h) lo[k] = pack_bf16(y0 - bf16_round(y0), y1 - bf16_round(y1));
                 }
@@ -495,26 +492,28 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, int par, int e, uint32_
                 if (!h) st_shared_v4(ay + 32768u + off, lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        const float sc = h ? exp2f(lc) : exp2f(lc - (float)e);
+        if (rn) {
+            const float sc = h ? dS : dT;
 #pragma unroll
-        for (int cb = 0; cb < 4; cb += 2) {
-            const uint32_t addr = tl + (h ? TM_DS : TM_DT) + 32 * cb;
-            tmem_ld32(addr, x[0]);
-            tmem_ld32(addr + 32, x[1]);
-            tmem_wait_ld();
+            for (int cb = 0; cb < 4; cb += 2) {
+                const uint32_t addr = tl + (h ? TM_DS : TM_DT) + 32 * cb;
+                tmem_ld32(addr, x[0]);
+                tmem_ld32(addr + 32, x[1]);
+                tmem_wait_ld();
 #pragma unroll
-            for (int b = 0; b < 2; ++b)
+                for (int b = 0; b < 2; ++b)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float v = __uint_as_float(x[b][j]) * sc;
-                    if (!h) mloc = fmaxf(mloc, fabsf(v));
-                    x[b][j] = __float_as_uint(v);
-                }
-            tmem_st32(addr, x[0]);
-            tmem_st32(addr + 32, x[1]);
+                    for (int j = 0; j < 32; ++j) {
+                        const float v = __uint_as_float(x[b][j]) * sc;
+                        if (!h) mloc = fmaxf(mloc, fabsf(v));
+                        x[b][j] = __float_as_uint(v);
+                    }
+                tmem_st32(addr, x[0]);
+                tmem_st32(addr + 32, x[1]);
+            }
         }
     }
-    tmem_wait_st();
+    if (rn) tmem_wait_st();
     return mloc;
 }
 
@@ -715,16 +714,66 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
     }
 }
 
+// Lazy decay.  The true state is D = sigma_h D''_h per half (h = T, S); the
+// stored D'' is not rescaled on an ordinary chunk: its decay g_C goes into
+// sigma (sigma_T = 2^(E + lsT), sigma_S = 2^lsS), so that with g_t the
+// in-chunk decay prefix
+//   D''_T += sum_t -(1/g_t) X''_T[:, t] k_t,
+//   D''_S += sum_t -(1/g_t) X''_S[:, t] k_t + (1/(g_t sigma_S)) u_t k_t.
+// A renormalisation chunk folds sigma back: D''_T <- 2^(lsT + lc - e) D''_T
+// with e = ilogb(max |D''_T|) + floor(lsT + lc) (E += e), D''_S <- 2^(lsS + lc)
+// D''_S, and the factors of that chunk carry the same scales.  It comes every
+// kRenormEvery chunks, on an item's last chunk, and whenever sigma_S or the
+// chunk's own decay would pass 2^-kLazyMax, which bounds every factor and the
+// growth of D''_S by 2^(2 kLazyMax).
+constexpr int kRenormEvery = 8;
+constexpr float kLazyMax = 40.f;
+
+struct StatePlan {
+    bool rn;
+    int e;
+    float dT, dS, lc;
+};
+
+// The factor tables of chunk gc (threads n < 64 write entry n) and its plan.
+__device__ __forceinline__ StatePlan state_plan(Misc* ms, uint32_t gc, bool last, int since, float lsT, float lsS,
+                                                float m, int n) {
+    const int slot = gc % kGateSlots;
+    StatePlan pl;
+    pl.lc = ms->lg2[slot][kC - 1];
+    pl.rn = last || since + 1 >= kRenormEvery || lsS + pl.lc < -kLazyMax || pl.lc < -kLazyMax;
+    pl.e = pl.rn ? ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lsT + pl.lc) : 0;
+    pl.dT = exp2f(lsT + pl.lc - (float)pl.e);
+    pl.dS = exp2f(lsS + pl.lc);
+    if (n < kC) {
+        const float l = ms->lg2[slot][n];
+        if (pl.rn) {
+            ms->fT[n] = -exp2f(fminf(lsT + pl.lc - (float)pl.e - l, 126.f));
+            ms->fS[n] = -exp2f(lsS + pl.lc - l);
+            ms->uf[n] = exp2f(pl.lc - l);
+        } else {
+            const float r = exp2f(-l);
+            ms->fT[n] = -r;
+            ms->fS[n] = -r;
+            ms->uf[n] = exp2f(-l - lsS);
+        }
+    }
+    return pl;
+}
+
 // W and U~ of chunk gc, once its W/U MMAs are done, into GEMM1's and GEMM2's
 // operands.  The state warpgroup does this between its passes: it is idle
 // while the prep warpgroup works on the next chunk's solve.
 __device__ __forceinline__ bool state_convert(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t gc,
-                                              int q, int lane) {
+                                              bool last, int since, float lsT, float lsS, float m, int q, int lane,
+                                              StatePlan& pl) {
     bool ok = wait_bar(&ms->that_ready, gc & 1, ms, a);  // also makes the chunk's gate tables visible
-    ok = ok && wait_bar(&ms->w_done, gc & 1, ms, a);
-    if (!wg_all(2, ok)) return false;
+    if (!wg_all(2, ok)) return false;                      // (and every thread is past the previous pass)
+    pl = state_plan(ms, gc, last, since, lsT, lsS, m, 32 * q + lane);
+    ok = wait_bar(&ms->w_done, gc & 1, ms, a);
+    if (!wg_all(2, ok)) return false;  // (this barrier also publishes the factor tables)
     tc_fence_after();
-    prep_convert(ms, smem, smem_u32(smem) + OFF_AU, gc % kGateSlots, tmem, q, lane);
+    prep_convert(ms, smem, smem_u32(smem) + OFF_AU, tmem, q, lane);
     fence_async_smem();
     tc_fence_before();
     named_sync(2);
@@ -740,25 +789,32 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         return;
     }
     const uint32_t ay = smem_u32(smem) + OFF_AY;
-    if (!state_convert(ms, smem, a, tmem, g, q, lane)) return;
-    int E = 0;
-    float m = 1.f;
+    int E = 0, since = 0;
+    float m = 1.f, lsT = 0.f, lsS = 0.f;
+    StatePlan pl;
+    if (!state_convert(ms, smem, a, tmem, g, nc == 1, since, lsT, lsS, m, q, lane, pl)) return;
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
-        const int par = gc % kGateSlots;
         if (!wg_all(2, wait_bar(&ms->x_done, gc & 1, ms, a))) return;
         tc_fence_after();
-        const float lc = ms->lg2[par][kC - 1];
-        const int e = ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lc);
-        if (n < kC) ms->fT[n] = -exp2f(fminf(lc - ms->lg2[par][n] - (float)e, 126.f));
-        named_sync(2);
-        const float mloc = state_pass(ms, ay, par, e, tmem, q, lane);
+        const float mloc = state_pass(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
         fence_async_smem();
         tc_fence_before();
-        m = state_reduce_max(mloc, ms->red[gc & 1], q, lane);
+        if (pl.rn) {
+            m = state_reduce_max(mloc, ms->red[gc & 1], q, lane);
+            E += pl.e;
+            lsT = 0.f;
+            lsS = 0.f;
+            since = 0;
+        } else {
+            named_sync(2);
+            lsT += pl.lc;
+            lsS += pl.lc;
+            ++since;
+        }
         if (n == 0) mbar_arrive(&ms->y_ready);
-        E += e;
-        if (c + 1 < nc && !state_convert(ms, smem, a, tmem, gc + 1, q, lane)) return;
+        if (c + 1 < nc && !state_convert(ms, smem, a, tmem, gc + 1, c + 2 == nc, since, lsT, lsS, m, q, lane, pl))
+            return;
     }
     if (!wg_all(2, wait_bar(&ms->d_ready, (g + nc - 1) & 1, ms, a))) return;
     tc_fence_after();
