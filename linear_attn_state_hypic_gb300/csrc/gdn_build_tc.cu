@@ -13,25 +13,34 @@
 //     D <- g_C D + K^T Diag(g_C/g_t) ([0 | U] - W D),
 // which is the token recurrence applied 64 times (WY / UT form of a product
 // of generalised Householder transitions).  The state is held transposed,
-// D' = D^T (256 x 128 fp32), in tensor memory; per chunk:
+// D'' = D^T / sigma (256 x 128 fp32, sigma a per-half scale, see "Lazy
+// decay" below), in tensor memory; per chunk:
 //   gram      G = K K^T                      bf16 MMA, M=64  N=64  K=128
-//   solve     That from G and the gates      CUDA cores (blocked forward substitution)
-//   W^T, U^T  K^T (That Diag(g))^T, V^T That^T   bf16 MMA, M=128 N=64 K=64
-//   GEMM1     X'_h = D'_h W^T                tf32 MMA, A read from tensor memory
-//   pass      Y'_h = -Diag(g_C/g_t) X'_h^T (bf16, smem); D' <- g_C D' (TMEM)
-//   GEMM2     D'_h += Y'_h K  (+ U~^T K for S) bf16 MMA, M=128 N=128 K=64
+//   solve     That from G and the gates      CUDA cores + warp MMAs (block-triangular inverse)
+//   W'^T, U^T K^T (That Diag(up))^T, V^T That^T   bf16 MMA, M=128 N=64 K=64
+//   GEMM1     X''_h = D''_h W'^T             tf32 MMA, A read from tensor memory
+//   pass      Y''_h = Diag(f_h) X''_h^T (bf16, smem)
+//   GEMM2     D''_h += Y''_h K  (+ U~^T K for S) bf16 MMA, M=128 N=128 K=64
+// with up_t = g_t / g_C^(1/2) in W' = W / g_C^(1/2) and f_h = -g_C^(1/2)/g_t
+// (times the renormalisation factor): the in-chunk decay is centred on the
+// middle of its range so that neither factor leaves the float32 range for
+// chunk decays down to 2^-252.
 // Two operands are carried as a pair of bf16 values (x = hi + lo, lo the
-// rounding residual of hi): That Diag(g) in the W product and Y'_T in the T
-// half of GEMM2.  Rounding either to a single bf16 alone costs T_C about
+// rounding residual of hi): That Diag(up) in the W product and Y''_T in the
+// T half of GEMM2.  Rounding either to a single bf16 alone costs T_C about
 // 7e-3 relative error over 2048-token segments with strong decay; the pair
 // brings it to ~2e-3.  Keys and values are bf16 inputs and need no split.
-// The T half is rescaled by powers of two as it decays (it falls far below the
-// fp32 range over long segments); the exponent is returned with T.
+// T_C falls far below the fp32 range over long segments: it is returned as a
+// mantissa and a power-of-two exponent.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 the
-// state warpgroup (tensor-memory passes, epilogue), warps 6-9 the prep
-// warpgroup (gates, gram -> That); the state warpgroup also converts W/U.  They meet on mbarriers;
-// every wait is bounded and a wait that runs out sets the device error word.
+// Roles (320 threads): warp 0 loads keys and values (TMA) and writes the gate
+// tables; warp 1 issues the MMAs as their inputs become ready; warps 6-9 (the
+// prep warpgroup) turn each gram into That; warps 2-5 (the state warpgroup)
+// run the pass between GEMM1 and GEMM2, convert W/U into MMA operands and
+// write the result.  The prep warpgroup runs ahead of the state chain: only
+// the pass, the W conversion and the two state GEMMs are serial per chunk.
+// They meet on mbarriers; every wait is bounded and a wait that runs out sets
+// the device error word.
 // One CTA per SM, persistent over (segment, layer, head) items taken from an
 // atomic queue in longest-body-first order.
 #include <cuda.h>
@@ -54,32 +63,36 @@ using namespace tc;
 
 constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
-constexpr int kStages = 2;        // K/V ring depth
-constexpr int kGateSlots = 3;     // per-chunk gate tables in flight (prep runs up to two chunks ahead)
+constexpr int kKStages = 3;       // K ring depth (the gram of a chunk wants its keys early)
+constexpr int kGateSlots = 4;     // per-chunk gate tables in flight
 constexpr int kThreads = 320;
 constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6;
 
 // Shared memory map (byte offsets; every operand region is 1024-byte aligned).
-constexpr uint32_t kTile = 16384;                     // 64 tokens x 128 bf16, two 64-column TMA boxes
-constexpr uint32_t kStage = 2 * kTile;                // K then V
-constexpr uint32_t OFF_KV = 0;
-constexpr uint32_t OFF_BW = OFF_KV + kStages * kStage;  // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
+constexpr uint32_t kTile = 16384;                       // 64 tokens x 128 bf16, two 64-column TMA boxes
+constexpr uint32_t OFF_K = 0;                           // K ring
+constexpr uint32_t OFF_V = OFF_K + kKStages * kTile;    // V (one chunk: read only by the U^T MMA)
+constexpr uint32_t OFF_BW = OFF_V + kTile;              // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
 constexpr uint32_t OFF_AU = OFF_BW + 32768;             // U~^T: bf16 [128 n][64 t], K-major
-constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y'^T: bf16 [128 n][64 t]: T hi, S, T lo
-constexpr uint32_t OFF_BT = OFF_AY + 49152;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]; solve scratch
+constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y''^T: bf16 [128 n][64 t]: T hi, S, T lo
+constexpr uint32_t OFF_BT = OFF_AY + 49152;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
 constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
 constexpr int kAS = 68;                                 // row stride (floats) of that scratch
-constexpr uint32_t OFF_MISC = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;
+constexpr uint32_t OFF_PT = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;  // solve scratch: 32 x 36 fp32
+constexpr uint32_t OFF_MISC = OFF_PT + 5120;
 
 struct Misc {
-    uint64_t full[kStages], empty[kStages];
-    uint64_t g_done, that_ready, w_done, wu_cvt, x_done, y_ready, d_ready, drain;
-    float lg2[kGateSlots][kC], beta[kGateSlots][kC], gam[kGateSlots][kC];  // slot gc % 3
+    uint64_t fullK[kKStages], emptyK[kKStages], fullV, emptyV;
+    uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables of a chunk written
+    uint64_t g_done, g_read;      // gram committed; gram read by the prep warpgroup
+    uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done
+    uint64_t u_done, w_done;      // U^T, W^T committed
+    uint64_t u_cvt, w_cvt;        // U~ and W operands written
+    uint64_t x_done, y_ready, d_ready, drain;
+    float lg2[kGateSlots][kC], beta[kGateSlots][kC];  // slot gc % kGateSlots
     float up[kGateSlots][kC], wn[kGateSlots][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
     float fT[kC], fS[kC];        // state pass: Y'' = f X'' for the T and S halves
     float uf[kC];                // U~ = Diag(uf) U
-    float scan_tot;
-    float gstage[2][2][kC];      // next chunk's raw a, b (cp.async target), double-buffered
     float red[2][4];
     float red_ep[4];
     int item;
@@ -90,7 +103,8 @@ constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Tensor-memory columns.
-constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_GW = 384, TM_U = 448;
+// W^T is staged in the X_T columns: it is converted before GEMM1 writes X.
+constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_U = 384, TM_G = 448;
 
 constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);  // G = K K^T
 constexpr uint32_t ID_WU = idesc(1, 128, 64, true, false);    // W^T, U^T: A = K^T / V^T (MN-major)
@@ -154,86 +168,145 @@ __device__ __forceinline__ float tf32_rna(float x) {
 // p: thread index inside the prep warpgroup (0..127); q: its tensor-memory
 // lane quarter; lane: lane in the warp.
 
-// Gates of one chunk: lg2[t] = sum_{s<=t} log2 a_s (inclusive prefix inside
-// the chunk), gam[t] = g_t, beta[t].  Padded tokens
-// past the segment end get a = 1, b = 0: an identity transition, so the
-// padded rows leave the result unchanged.
-__device__ void prep_gates(Misc* ms, int par, float a_raw, float b_raw, bool valid, int p, int lane) {
-    float la = 0.f, bb = 0.f;
-    if (p < kC) {
-        if (valid) {
-            la = log2f(fmaxf(a_raw, FLT_MIN));
-            bb = b_raw;
-        }
+// Raw gates of tokens t0 + 2 lane + {0, 1} (a = 1, b = 0 past the body end:
+// an identity transition, so padded rows leave the result unchanged).
+__device__ __forceinline__ void gate_load(const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end, int lane,
+                                          float (&ra)[2], float (&rb)[2]) {
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, la, off);
-            if (lane >= off) la += y;
+    for (int u = 0; u < 2; ++u) {
+        const int64_t t = t0 + 2 * lane + u;
+        ra[u] = 1.f;
+        rb[u] = 0.f;
+        if (t < t_end) {
+            const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
+            ra[u] = a.alpha[row];
+            rb[u] = a.beta[row];
         }
-        if (p == 31) ms->scan_tot = la;
     }
-    named_sync(1);
-    if (p < kC) {
-        if (p >= 32) la += ms->scan_tot;
-        ms->lg2[par][p] = la;
-        ms->beta[par][p] = bb;
-    }
-    named_sync(1);
-    if (p < kC) {
-        const float lc = ms->lg2[par][kC - 1], h = 0.5f * lc;
-        ms->gam[par][p] = exp2f(la);
-        ms->up[par][p] = exp2f(la - h);
-        ms->wn[par][p] = exp2f(h - la);
-    }
-    named_sync(1);
 }
 
-// Thread p (< 64) starts the copy of token t0 + p's raw gates into staging
-// buffer `buf` (cp.async: nothing is held in registers while the copy is in
-// flight).  Returns whether the token lies inside the body.
-__device__ __forceinline__ bool stage_gates(Misc* ms, const TcArgs& a, int layer, int head, int64_t t0, int64_t t_end,
-                                            int p, int buf) {
-    const int64_t t = t0 + p;
-    const bool valid = p < kC && t < t_end;
-    if (valid) {
-        const int64_t row = tok_row(layer, t, head, a.n_tokens, a.n_heads);
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&ms->gstage[buf][0][p])),
-                     "l"(a.alpha + row)
-                     : "memory");
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&ms->gstage[buf][1][p])),
-                     "l"(a.beta + row)
-                     : "memory");
+// Gate tables of one chunk (one warp, two tokens a lane): lg2[t] = sum_{s<=t}
+// log2 a_s (inclusive prefix inside the chunk), beta[t], and
+// up[t] = g_t / g_C^(1/2), wn[t] = g_C^(1/2) / g_t: the in-chunk decay
+// centred on the middle of its range, so that both stay in float32 range for
+// chunk decays g_C down to 2^-252 (g_t itself underflows below 2^-126).  The
+// exponents are clamped to +-126, which only matters beyond that.
+__device__ void gate_tables(Misc* ms, int slot, const float (&ra)[2], const float (&rb)[2], int lane) {
+    const float l0 = log2f(fmaxf(ra[0], FLT_MIN)), l1 = log2f(fmaxf(ra[1], FLT_MIN));
+    float s = l0 + l1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    return valid;
+    const float before = __shfl_up_sync(0xffffffffu, s, 1);
+    const float e0 = (lane > 0 ? before : 0.f) + l0, e1 = e0 + l1;
+    const float h = 0.5f * __shfl_sync(0xffffffffu, e1, 31);
+    const int t = 2 * lane;
+    *reinterpret_cast<float2*>(&ms->lg2[slot][t]) = make_float2(e0, e1);
+    *reinterpret_cast<float2*>(&ms->beta[slot][t]) = make_float2(rb[0], rb[1]);
+    auto ex = [](float x) { return exp2f(fminf(fmaxf(x, -126.f), 126.f)); };
+    *reinterpret_cast<float2*>(&ms->up[slot][t]) = make_float2(ex(e0 - h), ex(e1 - h));
+    *reinterpret_cast<float2*>(&ms->wn[slot][t]) = make_float2(ex(h - e0), ex(h - e1));
 }
-// Waits for this thread's copies up to (and including) the older group.
-__device__ __forceinline__ void stage_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void stage_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Rows of A from the gram matrix in tensor memory (M=64 accumulator layout:
 // row 16q + l sits in lane 32q + l, l < 16):
 // A[r][j] = b_r 2^(lg2_r - lg2_j) G[r][j] for j < r, 0 elsewhere.
-__device__ void prep_arows(const Misc* ms, float* As, int par, uint32_t tmem, int q, int lane) {
+// Lane l < 16 writes columns 0..31 of its row; lane l + 16, which holds no
+// row, takes columns 32..63 of the same row from lane l by a shuffle.
+__device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, int q, int lane) {
     uint32_t g0[32], g1[32];
-    const uint32_t tl = tmem + ((32u * q) << 16) + TM_GW;
+    const uint32_t tl = tmem + ((32u * q) << 16) + TM_G;
     tmem_ld32(tl, g0);
     tmem_ld32(tl + 32, g1);
     tmem_wait_ld();
-    if (lane < 16) {
-        const int r = 16 * q + lane;
-        const float coef = ms->beta[par][r] * ms->up[par][r];
-        const float* wn = ms->wn[par];
-        float* row = As + r * kAS;
+    const bool upper = lane >= 16;
 #pragma unroll
-        for (int j = 0; j < kC; j += 4) {
-            float4 v;
-            v.x = (j < r) ? coef * wn[j] * __uint_as_float(j < 32 ? g0[j] : g1[j - 32]) : 0.f;
-            v.y = (j + 1 < r) ? coef * wn[j + 1] * __uint_as_float(j + 1 < 32 ? g0[j + 1] : g1[j - 31]) : 0.f;
-            v.z = (j + 2 < r) ? coef * wn[j + 2] * __uint_as_float(j + 2 < 32 ? g0[j + 2] : g1[j - 30]) : 0.f;
-            v.w = (j + 3 < r) ? coef * wn[j + 3] * __uint_as_float(j + 3 < 32 ? g0[j + 3] : g1[j - 29]) : 0.f;
-            *reinterpret_cast<float4*>(row + j) = v;
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t x = __shfl_xor_sync(0xffffffffu, g1[j], 16);
+        if (upper) g0[j] = x;
+    }
+    const int r = 16 * q + (lane & 15), cb = upper ? 32 : 0;
+    const float coef = ms->beta[slot][r] * ms->up[slot][r];
+    const float* wn = ms->wn[slot] + cb;
+    float* row = As + r * kAS + cb;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 w = *reinterpret_cast<const float4*>(wn + j);
+        float4 v;
+        v.x = (cb + j < r) ? coef * w.x * __uint_as_float(g0[j]) : 0.f;
+        v.y = (cb + j + 1 < r) ? coef * w.y * __uint_as_float(g0[j + 1]) : 0.f;
+        v.z = (cb + j + 2 < r) ? coef * w.z * __uint_as_float(g0[j + 2]) : 0.f;
+        v.w = (cb + j + 3 < r) ? coef * w.w * __uint_as_float(g0[j + 3]) : 0.f;
+        *reinterpret_cast<float4*>(row + j) = v;
+    }
+}
+
+// Warp-level block products for the solve (mma.sync m16n8k16, bf16 with
+// fp32 accumulation).  Each fp32 operand is carried as a pair of bf16 values
+// (x = hi + lo, lo the rounding residual of hi) and a product as
+// hi*hi + hi*lo + lo*hi, which keeps about 16 bits of every operand: the
+// solve then matches an fp32 one to ~3e-6 relative.
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const float hx = bf16_round(x), hy = bf16_round(y);
+    hi = pack_bf16(hx, hy);
+    lo = pack_bf16(x - hx, y - hy);
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// C (16 x 8NT) = A (16 x 16KS, row stride lda) B (16KS x 8NT, row stride
+// ldb), one warp; lane (g, t) = (lane / 4, lane % 4) holds rows g, g + 8 and
+// columns 2t, 2t + 1 of each 8-column tile (the m16n8k16 layouts).
+template <int KS, int NT>
+__device__ __forceinline__ void warp_gemm(float (&c)[NT][4], const float* A, int lda, const float* B, int ldb,
+                                          int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float c1[NT][4], c2[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[nt][e] = c1[nt][e] = c2[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        uint32_t ah[4], al[4];
+        const float* a0 = A + g * lda + 16 * ks + 2 * t;
+        const float2 x0 = *reinterpret_cast<const float2*>(a0);
+        const float2 x1 = *reinterpret_cast<const float2*>(a0 + 8 * lda);
+        const float2 x2 = *reinterpret_cast<const float2*>(a0 + 8);
+        const float2 x3 = *reinterpret_cast<const float2*>(a0 + 8 * lda + 8);
+        split_bf16(x0.x, x0.y, ah[0], al[0]);
+        split_bf16(x1.x, x1.y, ah[1], al[1]);
+        split_bf16(x2.x, x2.y, ah[2], al[2]);
+        split_bf16(x3.x, x3.y, ah[3], al[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float* b = B + (16 * ks + 2 * t) * ldb + 8 * nt + g;
+            uint32_t bh0, bl0, bh1, bl1;
+            split_bf16(b[0], b[ldb], bh0, bl0);
+            split_bf16(b[8 * ldb], b[9 * ldb], bh1, bl1);
+            mma16816(c1[nt], al, bh0, bh1);  // three accumulators: no chain through one register set
+            mma16816(c2[nt], ah, bl0, bl1);
+            mma16816(c[nt], ah, bh0, bh1);
         }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[nt][e] += c1[nt][e] + c2[nt][e];
+}
+template <int NT>
+__device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, int ldd, float sgn, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        *reinterpret_cast<float2*>(D + g * ldd + 8 * nt + 2 * t) = make_float2(sgn * c[nt][0], sgn * c[nt][1]);
+        *reinterpret_cast<float2*>(D + (g + 8) * ldd + 8 * nt + 2 * t) = make_float2(sgn * c[nt][2], sgn * c[nt][3]);
     }
 }
 
@@ -242,12 +315,14 @@ __device__ void prep_arows(const Misc* ms, float* As, int par, uint32_t tmem, in
 //   [[L11, 0], [L21, L22]]^-1 = [[M11, 0], [-M22 L21 M11, M22]]:
 //   level 1: the four 16 x 16 diagonal blocks, forward substitution by
 //            columns (threads 0..63, one column each);
-//   level 2: blocks (1,0) and (3,2), from the level-1 inverses;
-//   level 3: the lower-left 32 x 32 block, from the two 32 x 32 inverses.
-// Each product is register-tiled (4 or 8 outputs per thread) with the inner
-// sum over the full block: the zero upper parts of the triangular factors
-// make that exact.  Ptmp holds the left products.
+//   level 2: blocks (1,0) and (3,2), from the level-1 inverses (warp w:
+//            block pair w / 2, 8-column tile w % 2);
+//   level 3: the lower-left 32 x 32 block, from the two 32 x 32 inverses
+//            (warp w: its 16 x 16 quarter w).
+// The products run over full blocks: the zero upper parts of the triangular
+// factors make that exact.  Ptmp holds the left products.
 __device__ void prep_solve(float* As, float* Ptmp, int p) {
+    const int w = p >> 5, lane = p & 31;
     if (p < kC) {  // level 1
         const int b = p >> 4, c = p & 15;
         const float* Ab = As + 16 * b * kAS + 16 * b;
@@ -266,122 +341,52 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
     }
     named_sync(1);
     {  // level 2: P = A_{x+1,x} M_xx, then M_{x+1,x} = -M_{x+1,x+1} P, x = 0, 2
-        const int x = 2 * (p >> 6), r = (p >> 2) & 15, c0 = (p & 3) * 4;
-        const float* Arow = As + (16 * (x + 1) + r) * kAS + 16 * x;
-        const float* Mcol = As + 16 * x * kAS + 16 * x + c0;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k4 = 0; k4 < 16; k4 += 4) {
-            const float4 av = *reinterpret_cast<const float4*>(Arow + k4);
-            const float ak[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 m = *reinterpret_cast<const float4*>(Mcol + (k4 + u) * kAS);
-                acc.x = fmaf(ak[u], m.x, acc.x);
-                acc.y = fmaf(ak[u], m.y, acc.y);
-                acc.z = fmaf(ak[u], m.z, acc.z);
-                acc.w = fmaf(ak[u], m.w, acc.w);
-            }
-        }
-        float* P = Ptmp + (p >> 6) * 256;
-        *reinterpret_cast<float4*>(P + r * 16 + c0) = acc;
+        const int x = 2 * (w >> 1), nt = w & 1;
+        float c[1][4];
+        warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * x, kAS, As + 16 * x * kAS + 16 * x + 8 * nt, kAS, lane);
+        float* P = Ptmp + (w >> 1) * 320;  // 16 x 16, row stride 20
+        warp_store<1>(c, P + 8 * nt, 20, 1.f, lane);
         named_sync(1);
-        const float* Mrow = As + (16 * (x + 1) + r) * kAS + 16 * (x + 1);
-        acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k4 = 0; k4 < 16; k4 += 4) {
-            const float4 mv = *reinterpret_cast<const float4*>(Mrow + k4);
-            const float mk[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 q = *reinterpret_cast<const float4*>(P + (k4 + u) * 16 + c0);
-                acc.x = fmaf(mk[u], q.x, acc.x);
-                acc.y = fmaf(mk[u], q.y, acc.y);
-                acc.z = fmaf(mk[u], q.z, acc.z);
-                acc.w = fmaf(mk[u], q.w, acc.w);
-            }
-        }
-        *reinterpret_cast<float4*>(As + (16 * (x + 1) + r) * kAS + 16 * x + c0) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * (x + 1), kAS, P + 8 * nt, 20, lane);
+        warp_store<1>(c, As + 16 * (x + 1) * kAS + 16 * x + 8 * nt, kAS, -1.f, lane);
     }
     named_sync(1);
     {  // level 3: P = A[32:64, 0:32] M[0:32, 0:32], then M[32:64, 0:32] = -M[32:64, 32:64] P
-        const int r = p >> 2, c0 = (p & 3) * 8;
-        const float* Arow = As + (32 + r) * kAS;
-        const float* Mcol = As + c0;
-        float acc[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-#pragma unroll 2
-        for (int k4 = 0; k4 < 32; k4 += 4) {
-            const float4 av = *reinterpret_cast<const float4*>(Arow + k4);
-            const float ak[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 m0 = *reinterpret_cast<const float4*>(Mcol + (k4 + u) * kAS);
-                const float4 m1 = *reinterpret_cast<const float4*>(Mcol + (k4 + u) * kAS + 4);
-                acc[0] = fmaf(ak[u], m0.x, acc[0]);
-                acc[1] = fmaf(ak[u], m0.y, acc[1]);
-                acc[2] = fmaf(ak[u], m0.z, acc[2]);
-                acc[3] = fmaf(ak[u], m0.w, acc[3]);
-                acc[4] = fmaf(ak[u], m1.x, acc[4]);
-                acc[5] = fmaf(ak[u], m1.y, acc[5]);
-                acc[6] = fmaf(ak[u], m1.z, acc[6]);
-                acc[7] = fmaf(ak[u], m1.w, acc[7]);
-            }
-        }
-        float* P = Ptmp + r * 36 + c0;  // 32 x 32, row stride 36 (keeps float4 rows 16-byte aligned)
-        *reinterpret_cast<float4*>(P) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4*>(P + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        const int r0 = 16 * (w >> 1), c0 = 16 * (w & 1);
+        float c[2][4];
+        warp_gemm<2, 2>(c, As + (32 + r0) * kAS, kAS, As + c0, kAS, lane);
+        warp_store<2>(c, Ptmp + r0 * 36 + c0, 36, 1.f, lane);  // 32 x 32, row stride 36
         named_sync(1);
-        const float* Mrow = As + (32 + r) * kAS + 32;
-        const float* Pc = Ptmp + c0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-#pragma unroll 2
-        for (int k4 = 0; k4 < 32; k4 += 4) {
-            const float4 mv = *reinterpret_cast<const float4*>(Mrow + k4);
-            const float mk[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 q0 = *reinterpret_cast<const float4*>(Pc + (k4 + u) * 36);
-                const float4 q1 = *reinterpret_cast<const float4*>(Pc + (k4 + u) * 36 + 4);
-                acc[0] = fmaf(mk[u], q0.x, acc[0]);
-                acc[1] = fmaf(mk[u], q0.y, acc[1]);
-                acc[2] = fmaf(mk[u], q0.z, acc[2]);
-                acc[3] = fmaf(mk[u], q0.w, acc[3]);
-                acc[4] = fmaf(mk[u], q1.x, acc[4]);
-                acc[5] = fmaf(mk[u], q1.y, acc[5]);
-                acc[6] = fmaf(mk[u], q1.z, acc[6]);
-                acc[7] = fmaf(mk[u], q1.w, acc[7]);
-            }
-        }
-        float* out = As + (32 + r) * kAS + c0;
-        *reinterpret_cast<float4*>(out) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-        *reinterpret_cast<float4*>(out + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+        warp_gemm<2, 2>(c, As + (32 + r0) * kAS + 32, kAS, Ptmp + c0, 36, lane);
+        warp_store<2>(c, As + (32 + r0) * kAS + c0, kAS, -1.f, lane);
     }
     named_sync(1);
 }
 
-// That Diag(g) (bf16 hi at bt, residual lo at bt + 16384) and
-// That = (I+A)^-1 Diag(b) (bf16 at bt + 8192) as K-major 64 x 64 operands
+// That Diag(up) (bf16 hi at bt, residual lo at bt + 16384; up = g / g_C^(1/2))
+// and That = (I+A)^-1 Diag(b) (bf16 at bt + 8192) as K-major 64 x 64 operands
 // (128-byte rows, 128-byte swizzle).  Thread p writes half a row.
 __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, int par, int p) {
-    const float* beta = ms->beta[par];
-    const float* gam = ms->gam[par];
     const int t = p >> 1, half = p & 1;
     const float* row = As + t * kAS + 32 * half;
+    const float* beta = ms->beta[par] + 32 * half;
+    const float* gam = ms->up[par] + 32 * half;  // That Diag(g / g_C^(1/2))
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
         const float4 x0 = *reinterpret_cast<const float4*>(row + 8 * ch);
         const float4 x1 = *reinterpret_cast<const float4*>(row + 8 * ch + 4);
-        const float mv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float4 b0 = *reinterpret_cast<const float4*>(beta + 8 * ch);
+        const float4 b1 = *reinterpret_cast<const float4*>(beta + 8 * ch + 4);
+        const float4 y0 = *reinterpret_cast<const float4*>(gam + 8 * ch);
+        const float4 y1 = *reinterpret_cast<const float4*>(gam + 8 * ch + 4);
+        const float mv[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
+                             x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
+        const float gv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
         uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const int c0 = 32 * half + 8 * ch + 2 * jj;
-            const float m0 = mv[2 * jj] * beta[c0], m1 = mv[2 * jj + 1] * beta[c0 + 1];
-            const float z0 = m0 * gam[c0], z1 = m1 * gam[c0 + 1];
+            const float m0 = mv[2 * jj], m1 = mv[2 * jj + 1];
+            const float z0 = m0 * gv[2 * jj], z1 = m1 * gv[2 * jj + 1];
             w1[jj] = pack_bf16(z0, z1);
             w3[jj] = pack_bf16(z0 - bf16_round(z0), z1 - bf16_round(z1));
             w2[jj] = pack_bf16(m0, m1);
@@ -393,17 +398,15 @@ __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, in
     }
 }
 
-// W^T (lane i holds W[.][i]) -> W as a tf32 K-major [64 t][128 i] operand;
-// U^T (lane n holds U[.][n]) -> U~^T = U^T Diag(uf) as a bf16 K-major
-// [128 n][64 t] operand (uf: the chunk's U factors, see state_plan).
-__device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, uint32_t tmem, int q, int lane) {
+// W^T (lane i holds W[.][i], staged in the X_T columns) -> W as a tf32
+// K-major [64 t][128 i] operand.
+__device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
     const int i = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    const float* uf = ms->uf;
     uint32_t w2[2][32];
     uint8_t* bw = smem + OFF_BW + (i >> 5) * 8192;
-    tmem_ld32(tl + TM_GW, w2[0]);
-    tmem_ld32(tl + TM_GW + 32, w2[1]);
+    tmem_ld32(tl + TM_XT, w2[0]);
+    tmem_ld32(tl + TM_XT + 32, w2[1]);
     tmem_wait_ld();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -413,6 +416,15 @@ __device__ void prep_convert(const Misc* ms, uint8_t* smem, uint32_t au, uint32_
             *reinterpret_cast<float*>(bw + sw128_offset(t, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w2[half][j]));
         }
     }
+}
+
+// U^T (lane n holds U[.][n]) -> U~^T = U^T Diag(uf) as a bf16 K-major
+// [128 n][64 t] operand (uf: the chunk's U factors, see state_plan).
+__device__ void convert_u(const Misc* ms, uint32_t au, uint32_t tmem, int q, int lane) {
+    const int i = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    const float* uf = ms->uf;
+    uint32_t w2[2][32];
     tmem_ld32(tl + TM_U, w2[0]);
     tmem_ld32(tl + TM_U + 32, w2[1]);
     tmem_wait_ld();
@@ -586,128 +598,177 @@ __device__ __forceinline__ bool wg_all(int id, bool v) {
 
 // --------------------------------------------------------- role drivers --
 // g: global chunk counter at the start of the item (barrier phases run on it
-// across items); nc: chunks of this item's body.
+// across items); nc: chunks of this item's body.  Every barrier completes
+// once per chunk (the ring and gate-slot barriers once per use of their slot).
 
+// Warp 0: keys (3-deep ring) and values (one buffer) by TMA from lane 0, and
+// the gate tables of each chunk from the whole warp (a chunk ahead of the
+// prep warpgroup, the loads of the next chunk's gates in flight meanwhile).
 __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CUtensorMap* tmk,
-                              const CUtensorMap* tmv, uint32_t g, int nc, int layer, int head, int64_t b0) {
+                              const CUtensorMap* tmv, uint32_t g, int nc, int layer, int head, int64_t b0, int64_t b1,
+                              int lane) {
+    float ra[2], rb[2];
+    if (nc > 0) gate_load(a, layer, head, b0, b1, lane, ra, rb);
     for (int c = 0; c < nc; ++c) {
-        const uint32_t gc = g + c, s = gc % kStages, u = gc / kStages;
-        if (u >= 1 && !wait_bar(&ms->empty[s], (u - 1) & 1, ms, a)) return;
-        uint8_t* kt = smem + OFF_KV + s * kStage;
-        mbar_expect_tx(&ms->full[s], kStage);
+        const uint32_t gc = g + c, s = gc % kKStages, u = gc / kKStages;
         const int z = (int)((int64_t)layer * a.n_tokens + b0 + (int64_t)c * kC);
-        tma_load_3d(kt, tmk, &ms->full[s], 0, head, z);
-        tma_load_3d(kt + 8192, tmk, &ms->full[s], 64, head, z);
-        tma_load_3d(kt + kTile, tmv, &ms->full[s], 0, head, z);
-        tma_load_3d(kt + kTile + 8192, tmv, &ms->full[s], 64, head, z);
+        if (u >= 1 && !wait_bar(&ms->emptyK[s], (u - 1) & 1, ms, a)) return;
+        if (lane == 0) {
+            uint8_t* kt = smem + OFF_K + s * kTile;
+            mbar_expect_tx(&ms->fullK[s], kTile);
+            tma_load_3d(kt, tmk, &ms->fullK[s], 0, head, z);
+            tma_load_3d(kt + 8192, tmk, &ms->fullK[s], 64, head, z);
+        }
+        // The slot of chunk gc was last read for chunk gc - 4, whose GEMM2
+        // completed before that of gc - 3 (waited above).
+        gate_tables(ms, gc % kGateSlots, ra, rb, lane);
+        if (c + 1 < nc) gate_load(a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, lane, ra, rb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->gready[gc % kGateSlots]);
+        if (gc >= 1 && !wait_bar(&ms->emptyV, (gc - 1) & 1, ms, a)) return;
+        if (lane == 0) {
+            uint8_t* vt = smem + OFF_V;
+            mbar_expect_tx(&ms->fullV, kTile);
+            tma_load_3d(vt, tmv, &ms->fullV, 0, head, z);
+            tma_load_3d(vt + 8192, tmv, &ms->fullV, 64, head, z);
+        }
     }
 }
 
+// Warp 1, lane 0: issues every MMA of the item as soon as its inputs are
+// ready, in this priority: W^T, GEMM2, GEMM1, U^T, gram.  W^T of the next
+// chunk and GEMM2 of this one wait for the same pass; W^T goes first so that
+// its conversion runs while GEMM2 executes.  A readiness test
+// of a barrier's phase k is only made once its phase k - 1 is known to be
+// complete (by an earlier test or an earlier item), so a parity test cannot
+// mistake an old phase for a new one.
 __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
     if (nc == 0) return;
     const uint32_t sb = smem_u32(smem);
-    auto ktile = [&](uint32_t gc) { return sb + OFF_KV + (gc % kStages) * kStage; };
-    // G = K K^T: K-major view of the K tile (K = feature index, two 64-wide boxes).
-    auto gram = [&](uint32_t gc) {
-        const uint32_t kt = ktile(gc);
+    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, au = sb + OFF_AU, bt = sb + OFF_BT, vt = sb + OFF_V;
+    auto ktile = [&](uint32_t gc) { return sb + OFF_K + (gc % kKStages) * kTile; };
+    int ig = 0, iu = 0, iw = 0, i1 = 0, i2 = 0;
+    uint64_t t_idle = 0;
+    while (i2 < nc) {
+        bool any = false;
+        if (iw < iu && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_T columns
+            const uint32_t gc = g + iw;
+            if (iw == 0 || mbar_test(&ms->y_ready, (gc - 1) & 1)) {  // X of the previous chunk has been read
+                tc_fence_after();
+                const uint32_t kt = ktile(gc);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint64_t d = sdesc_sw128(kt + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024);
-            mma_bf16_ss(tmem + TM_GW, d, d, ID_GRAM, k > 0);
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t ak = sdesc_sw128(kt + k * 2048, 8192, 1024);
+                    mma_bf16_ss(tmem + TM_XT, ak, sdesc_sw128(bt + k * 32, 0, 1024), ID_WU, k > 0);
+                    mma_bf16_ss(tmem + TM_XT, ak, sdesc_sw128(bt + 16384 + k * 32, 0, 1024), ID_WU, true);
+                }
+                mma_commit(&ms->w_done);
+                mma_commit(&ms->bt_free);  // (the U^T MMAs of this chunk were issued before)
+                ++iw;
+                any = true;
+            }
         }
-        mma_commit(&ms->g_done);
-    };
-    // W^T = K^T (That Diag(g))^T and U^T = V^T That^T: K and V tiles read
-    // MN-major (M = feature, K = token).
-    auto wu = [&](uint32_t gc) {
-        const uint32_t kt = ktile(gc), vt = kt + kTile, bt = sb + OFF_BT;
+        if (i2 < i1) {  // GEMM2 (bf16): D''_T += Y''_T K; D''_S += Y''_S K + U~^T K
+            const uint32_t gc = g + i2;
+            if (mbar_test(&ms->y_ready, gc & 1) && mbar_test(&ms->u_cvt, gc & 1)) {
+                tc_fence_after();
+                const uint32_t kt = ktile(gc);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            mma_bf16_ss(tmem + TM_GW, sdesc_sw128(kt + k * 2048, 8192, 1024), sdesc_sw128(bt + k * 32, 0, 1024), ID_WU,
-                        k > 0);
-            mma_bf16_ss(tmem + TM_GW, sdesc_sw128(kt + k * 2048, 8192, 1024),
-                        sdesc_sw128(bt + 16384 + k * 32, 0, 1024), ID_WU, true);
-            mma_bf16_ss(tmem + TM_U, sdesc_sw128(vt + k * 2048, 8192, 1024),
-                        sdesc_sw128(bt + 8192 + k * 32, 0, 1024), ID_WU, k > 0);
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t bk = sdesc_sw128(kt + k * 2048, 8192, 1024);
+                    mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + k * 32, 0, 1024), bk, ID_G2, true);
+                    mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + 32768 + k * 32, 0, 1024), bk, ID_G2, true);
+                    mma_bf16_ss(tmem + TM_DS, sdesc_sw128(ay + 16384 + k * 32, 0, 1024), bk, ID_G2, true);
+                    mma_bf16_ss(tmem + TM_DS, sdesc_sw128(au + k * 32, 0, 1024), bk, ID_G2, true);
+                }
+                mma_commit(&ms->d_ready);
+                mma_commit(&ms->emptyK[gc % kKStages]);
+                ++i2;
+                any = true;
+            }
         }
-        mma_commit(&ms->w_done);
-    };
-    if (!wait_bar(&ms->full[g % kStages], (g / kStages) & 1, ms, a)) return;
-    tc_fence_after();
-    gram(g);
-    if (!wait_bar(&ms->that_ready, g & 1, ms, a)) return;
-    tc_fence_after();
-    wu(g);
-    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, au = sb + OFF_AU;
-    for (int c = 0; c < nc; ++c) {
-        const uint32_t gc = g + c;
-        if (!wait_bar(&ms->wu_cvt, gc & 1, ms, a)) return;
-        if (c + 1 < nc) {  // gram of the next chunk first: the prep chain is the longer one
-            if (!wait_bar(&ms->full[(gc + 1) % kStages], ((gc + 1) / kStages) & 1, ms, a)) return;
-            tc_fence_after();
-            gram(gc + 1);
+        if (i1 < iw && i2 == i1) {  // GEMM1 (tf32): X''_h = D''_h W^T, A = the state in tensor memory
+            const uint32_t gc = g + i1;
+            if (mbar_test(&ms->w_cvt, gc & 1) && (i1 == 0 || mbar_test(&ms->d_ready, (gc - 1) & 1))) {
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k,
+                                    sdesc_sw128(bw + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024), ID_G1, k > 0);
+                mma_commit(&ms->x_done);
+                ++i1;
+                any = true;
+            }
         }
-        if (c > 0 && !wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a)) return;
-        tc_fence_after();
-        // GEMM1 (tf32): X'_h = D'_h W^T, A = the state itself in tensor memory.
+        if (iu < ig) {  // U^T = V^T That^T
+            const uint32_t gc = g + iu;
+            if (mbar_test(&ms->that_ready, gc & 1) && mbar_test(&ms->fullV, gc & 1) &&
+                (iu == 0 || mbar_test(&ms->u_cvt, (gc - 1) & 1))) {
+                tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k,
-                            sdesc_sw128(bw + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024), ID_G1, k > 0);
-        mma_commit(&ms->x_done);
-        if (!wait_bar(&ms->y_ready, gc & 1, ms, a)) return;
-        tc_fence_after();
-        // GEMM2 (bf16): D'_T += Y'_T K; D'_S += Y'_S K + U~^T K.
-        const uint32_t kt = ktile(gc);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint64_t bk = sdesc_sw128(kt + k * 2048, 8192, 1024);
-            mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + k * 32, 0, 1024), bk, ID_G2, true);
-            mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + 32768 + k * 32, 0, 1024), bk, ID_G2, true);
-            mma_bf16_ss(tmem + TM_DS, sdesc_sw128(ay + 16384 + k * 32, 0, 1024), bk, ID_G2, true);
-            mma_bf16_ss(tmem + TM_DS, sdesc_sw128(au + k * 32, 0, 1024), bk, ID_G2, true);
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_ss(tmem + TM_U, sdesc_sw128(vt + k * 2048, 8192, 1024),
+                                sdesc_sw128(bt + 8192 + k * 32, 0, 1024), ID_WU, k > 0);
+                mma_commit(&ms->u_done);
+                mma_commit(&ms->emptyV);
+                ++iu;
+                any = true;
+            }
         }
-        mma_commit(&ms->d_ready);
-        mma_commit(&ms->empty[gc % kStages]);
-        if (c + 1 < nc) {
-            if (!wait_bar(&ms->that_ready, (gc + 1) & 1, ms, a)) return;
-            tc_fence_after();
-            wu(gc + 1);
+        if (ig < nc) {  // G = K K^T: K-major view of the K tile (K = feature index, two 64-wide boxes)
+            const uint32_t gc = g + ig;
+            if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
+                (ig == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
+                tc_fence_after();
+                const uint32_t kt = ktile(gc);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t d = sdesc_sw128(kt + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024);
+                    mma_bf16_ss(tmem + TM_G, d, d, ID_GRAM, k > 0);
+                }
+                mma_commit(&ms->g_done);
+                ++ig;
+                any = true;
+            }
+        }
+        if (any) {  // (no sleep when idle: a sleeping issuer answers its barriers late)
+            t_idle = 0;
+        } else {
+            if (*(volatile int*)&ms->abort_flag) return;
+            const uint64_t now = globaltimer_ns();
+            if (t_idle == 0) {
+                t_idle = now;
+            } else if (now - t_idle > a.wait_ns) {
+                *(volatile int*)&ms->abort_flag = 1;
+                set_error(a.err, kErrTimeout);
+                return;
+            }
         }
     }
 }
 
-__device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int layer,
-                          int head, int64_t b0, int64_t b1, int p, int q, int lane) {
+// Warps 6-9: gram -> A -> (I + A)^-1 -> That, chunk after chunk.
+__device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int p, int q,
+                          int lane) {
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
-    float* Ptmp = reinterpret_cast<float*>(smem + OFF_BT);
-    const uint32_t sb = smem_u32(smem);
-    bool gv = stage_gates(ms, a, layer, head, b0, b1, p, 0);
+    float* Ptmp = reinterpret_cast<float*>(smem + OFF_PT);
+    const uint32_t bt = smem_u32(smem) + OFF_BT;
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
-        const int par = gc % kGateSlots;
-        const bool cv = gv;
-        float ca = 1.f, cb = 0.f;
-        if (c + 1 < nc) {  // next chunk's copy goes out before this one's is read
-            gv = stage_gates(ms, a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, p, (c + 1) & 1);
-            stage_wait_prev();
-        } else {
-            stage_wait_all();
-        }
-        if (cv) {
-            ca = ms->gstage[c & 1][0][p];
-            cb = ms->gstage[c & 1][1][p];
-        }
-        prep_gates(ms, par, ca, cb, cv, p, lane);
-        if (!wg_all(1, wait_bar(&ms->g_done, gc & 1, ms, a))) return;
+        const int slot = gc % kGateSlots;
+        bool ok = wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a);
+        ok = ok && wait_bar(&ms->g_done, gc & 1, ms, a);
+        if (!wg_all(1, ok)) return;
         tc_fence_after();
-        prep_arows(ms, As, par, tmem, q, lane);
+        prep_arows(ms, As, slot, tmem, q, lane);
         tc_fence_before();
         named_sync(1);
+        if (p == 0) mbar_arrive(&ms->g_read);
         prep_solve(As, Ptmp, p);
-        prep_write_that(ms, As, sb + OFF_BT, par, p);
+        if (!wg_all(1, gc == 0 || wait_bar(&ms->bt_free, (gc - 1) & 1, ms, a))) return;
+        prep_write_that(ms, As, bt, slot, p);
         fence_async_smem();
         named_sync(1);
         if (p == 0) mbar_arrive(&ms->that_ready);
@@ -717,9 +778,9 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
 // Lazy decay.  The true state is D = sigma_h D''_h per half (h = T, S); the
 // stored D'' is not rescaled on an ordinary chunk: its decay g_C goes into
 // sigma (sigma_T = 2^(E + lsT), sigma_S = 2^lsS), so that with g_t the
-// in-chunk decay prefix
-//   D''_T += sum_t -(1/g_t) X''_T[:, t] k_t,
-//   D''_S += sum_t -(1/g_t) X''_S[:, t] k_t + (1/(g_t sigma_S)) u_t k_t.
+// in-chunk decay prefix and X''_h = D''_h W'^T,
+//   D''_T += sum_t -(g_C^(1/2)/g_t) X''_T[:, t] k_t,
+//   D''_S += sum_t -(g_C^(1/2)/g_t) X''_S[:, t] k_t + (1/(g_t sigma_S)) u_t k_t.
 // A renormalisation chunk folds sigma back: D''_T <- 2^(lsT + lc - e) D''_T
 // with e = ilogb(max |D''_T|) + floor(lsT + lc) (E += e), D''_S <- 2^(lsS + lc)
 // D''_S, and the factors of that chunk carry the same scales.  It comes every
@@ -745,14 +806,14 @@ __device__ __forceinline__ StatePlan state_plan(Misc* ms, uint32_t gc, bool last
     pl.e = pl.rn ? ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lsT + pl.lc) : 0;
     pl.dT = exp2f(lsT + pl.lc - (float)pl.e);
     pl.dS = exp2f(lsS + pl.lc);
-    if (n < kC) {
-        const float l = ms->lg2[slot][n];
+    if (n < kC) {  // (W carries g_t / g_C^(1/2), so the Y factors carry g_C^(1/2) / g_t)
+        const float l = ms->lg2[slot][n], h = 0.5f * pl.lc;
         if (pl.rn) {
-            ms->fT[n] = -exp2f(fminf(lsT + pl.lc - (float)pl.e - l, 126.f));
-            ms->fS[n] = -exp2f(lsS + pl.lc - l);
+            ms->fT[n] = -exp2f(fminf(lsT + pl.lc - (float)pl.e + h - l, 126.f));
+            ms->fS[n] = -exp2f(fminf(lsS + pl.lc + h - l, 126.f));
             ms->uf[n] = exp2f(pl.lc - l);
         } else {
-            const float r = exp2f(-l);
+            const float r = ms->wn[slot][n];
             ms->fT[n] = -r;
             ms->fS[n] = -r;
             ms->uf[n] = exp2f(-l - lsS);
@@ -761,26 +822,37 @@ __device__ __forceinline__ StatePlan state_plan(Misc* ms, uint32_t gc, bool last
     return pl;
 }
 
-// W and U~ of chunk gc, once its W/U MMAs are done, into GEMM1's and GEMM2's
-// operands.  The state warpgroup does this between its passes: it is idle
-// while the prep warpgroup works on the next chunk's solve.
-__device__ __forceinline__ bool state_convert(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t gc,
+// Chunk gc's factor tables and plan, then its W operand (on the chain to
+// GEMM1), then its U~ operand (off it: only GEMM2 reads it, once the previous
+// GEMM2 has).
+__device__ __forceinline__ bool state_prepare(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t gc,
                                               bool last, int since, float lsT, float lsS, float m, int q, int lane,
                                               StatePlan& pl) {
-    bool ok = wait_bar(&ms->that_ready, gc & 1, ms, a);  // also makes the chunk's gate tables visible
-    if (!wg_all(2, ok)) return false;                      // (and every thread is past the previous pass)
+    const int slot = gc % kGateSlots;
+    bool ok = wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a);
+    if (!wg_all(2, ok)) return false;  // (and every thread is past the previous pass)
     pl = state_plan(ms, gc, last, since, lsT, lsS, m, 32 * q + lane);
-    ok = wait_bar(&ms->w_done, gc & 1, ms, a);
-    if (!wg_all(2, ok)) return false;  // (this barrier also publishes the factor tables)
+    if (!wg_all(2, wait_bar(&ms->w_done, gc & 1, ms, a))) return false;  // (also publishes the factor tables)
     tc_fence_after();
-    prep_convert(ms, smem, smem_u32(smem) + OFF_AU, tmem, q, lane);
+    convert_w(smem, tmem, q, lane);
     fence_async_smem();
     tc_fence_before();
     named_sync(2);
-    if (q == 0 && lane == 0) mbar_arrive(&ms->wu_cvt);
+    if (q == 0 && lane == 0) mbar_arrive(&ms->w_cvt);
+    ok = wait_bar(&ms->u_done, gc & 1, ms, a);
+    ok = ok && (gc == 0 || wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a));  // the previous GEMM2 has read U~
+    if (!wg_all(2, ok)) return false;
+    tc_fence_after();
+    convert_u(ms, smem_u32(smem) + OFF_AU, tmem, q, lane);
+    fence_async_smem();
+    tc_fence_before();
+    named_sync(2);
+    if (q == 0 && lane == 0) mbar_arrive(&ms->u_cvt);
     return true;
 }
 
+// Warps 2-5: per chunk the pass (Y'' and, on renormalisation chunks, the
+// state rescale), then the next chunk's operands; the epilogue at the end.
 __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc,
                            int64_t obj, int q, int lane) {
     const int n = 32 * q + lane;
@@ -792,7 +864,7 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
     int E = 0, since = 0;
     float m = 1.f, lsT = 0.f, lsS = 0.f;
     StatePlan pl;
-    if (!state_convert(ms, smem, a, tmem, g, nc == 1, since, lsT, lsS, m, q, lane, pl)) return;
+    if (!state_prepare(ms, smem, a, tmem, g, nc == 1, since, lsT, lsS, m, q, lane, pl)) return;
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
         if (!wg_all(2, wait_bar(&ms->x_done, gc & 1, ms, a))) return;
@@ -813,7 +885,7 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
             ++since;
         }
         if (n == 0) mbar_arrive(&ms->y_ready);
-        if (c + 1 < nc && !state_convert(ms, smem, a, tmem, gc + 1, c + 2 == nc, since, lsT, lsS, m, q, lane, pl))
+        if (c + 1 < nc && !state_prepare(ms, smem, a, tmem, gc + 1, c + 2 == nc, since, lsT, lsS, m, q, lane, pl))
             return;
     }
     if (!wg_all(2, wait_bar(&ms->d_ready, (g + nc - 1) & 1, ms, a))) return;
@@ -834,18 +906,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ms->full[s], 1);
-            mbar_init(&ms->empty[s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&ms->fullK[s], 1);
+            mbar_init(&ms->emptyK[s], 1);
         }
-        mbar_init(&ms->g_done, 1);
-        mbar_init(&ms->that_ready, 1);
-        mbar_init(&ms->w_done, 1);
-        mbar_init(&ms->wu_cvt, 1);
-        mbar_init(&ms->x_done, 1);
-        mbar_init(&ms->y_ready, 1);
-        mbar_init(&ms->d_ready, 1);
-        mbar_init(&ms->drain, 1);
+        for (int s = 0; s < kGateSlots; ++s) mbar_init(&ms->gready[s], 1);
+        uint64_t* one[] = {&ms->fullV, &ms->emptyV, &ms->g_done, &ms->g_read, &ms->that_ready, &ms->bt_free,
+                           &ms->u_done, &ms->w_done, &ms->u_cvt, &ms->w_cvt, &ms->x_done, &ms->y_ready,
+                           &ms->d_ready, &ms->drain};
+        for (uint64_t* b : one) mbar_init(b, 1);
         ms->abort_flag = 0;
         fence_mbar_init();
     }
@@ -878,13 +947,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nc = (int)((b1 - b0 + kC - 1) / kC);
         const int64_t obj = ((int64_t)seg * a.n_layers + layer) * a.n_heads + head;
         if (warp == kWarpTMA) {
-            if (lane == 0) producer_role(ms, smem, a, &tmk, &tmv, g, nc, layer, head, b0);
+            producer_role(ms, smem, a, &tmk, &tmv, g, nc, layer, head, b0, b1, lane);
         } else if (warp == kWarpMMA) {
             if (lane == 0) mma_role(ms, smem, a, tmem, g, nc);
         } else if (is_state) {
             state_role(ms, smem, a, tmem, g, nc, obj, q, lane);
         } else {
-            prep_role(ms, smem, a, tmem, g, nc, layer, head, b0, b1, tid - 32 * kWarpPrep0, q, lane);
+            prep_role(ms, smem, a, tmem, g, nc, tid - 32 * kWarpPrep0, q, lane);
         }
         tc_fence_before();
         __syncthreads();

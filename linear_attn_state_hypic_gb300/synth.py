@@ -32,7 +32,12 @@ from __future__ import annotations
 
 import numpy as np
 
-GATES = {"faithful": (0.85, 1.0, 0.0, 1.0), "highret": (0.999, 1.0, 0.0, 0.1)}
+# alpha range, beta range.  "faithful" and "highret" are the two gate mixes of
+# the build workload; "middecay" and "fastdecay" (a chunk of 64 tokens decays
+# by ~2^-32 and ~2^-115) reach the builds' renormalisation and strong-decay
+# branches.
+GATES = {"faithful": (0.85, 1.0, 0.0, 1.0), "highret": (0.999, 1.0, 0.0, 0.1),
+         "middecay": (0.5, 1.0, 0.0, 1.0), "fastdecay": (0.05, 0.6, 0.0, 1.0)}
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

@@ -57,7 +57,7 @@ def test_gdn_fp32_dims_ragged(B, d):
     check_build(B, "gdn", inp, "f32", TOL_F32)
 
 
-@pytest.mark.parametrize("variant", ["faithful", "highret"])
+@pytest.mark.parametrize("variant", ["faithful", "highret", "middecay", "fastdecay"])
 def test_gdn_bf16_d128_ragged(B, variant):
     lengths = [700, 1, 64, 129, 0, 2048, 513]
     inp = synth.gdn_ragged(seed=3, H=4, d=128, lengths=lengths, variant=variant)
@@ -72,6 +72,15 @@ def test_gdn_multi_layer_and_seam_skip(B):
     # the empty body is the identity pair
     np.testing.assert_array_equal(gdn_T64(T, T_exp)[2], np.broadcast_to(np.eye(128), (3, 2, 128, 128)))
     assert np.all(host(S)[2] == 0)
+
+
+def test_gdn_tc_long_segments(B):
+    """Tensor-core path over 4096- and 3000-token bodies (64 and 47 chunks):
+    many renormalisations of the stored state, T_C far below float32 range
+    (kept through the stored exponent)."""
+    inp = synth.gdn_ragged(seed=6, H=2, d=128, lengths=[4096, 3000])
+    T, T_exp, S = check_build(B, "gdn", inp, "bf16", TOL_BF16)
+    assert int(T_exp.cpu().numpy().min()) < -300
 
 
 def test_gdn_long_segment_T_exponent(B):
