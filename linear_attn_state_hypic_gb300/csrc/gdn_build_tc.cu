@@ -48,6 +48,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <float.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -89,10 +90,13 @@ struct Misc {
     uint64_t u_done, w_done;      // U^T, W^T committed
     uint64_t u_cvt, w_cvt;        // U~ and W operands written
     uint64_t x_done, y_ready, d_ready, drain;
-    float lg2[kGateSlots][kC], beta[kGateSlots][kC];  // slot gc % kGateSlots
-    float up[kGateSlots][kC], wn[kGateSlots][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
-    float fT[kC], fS[kC];        // state pass: Y'' = f X'' for the T and S halves
-    float uf[kC];                // U~ = Diag(uf) U
+    alignas(16) float lg2[kGateSlots][kC];  // slot gc % kGateSlots; every table is read as float4
+    alignas(16) float beta[kGateSlots][kC];
+    alignas(16) float up[kGateSlots][kC];
+    alignas(16) float wn[kGateSlots][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
+    alignas(16) float fT[kC];    // state pass: Y'' = f X'' for the T and S halves
+    alignas(16) float fS[kC];
+    alignas(16) float uf[kC];    // U~ = Diag(uf) U
     float red[2][4];
     float red_ep[4];
     int item;
@@ -100,6 +104,9 @@ struct Misc {
     uint32_t tmem_base;
 };
 constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
+static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, lg2) % 16 == 0 && offsetof(Misc, beta) % 16 == 0 &&
+                  offsetof(Misc, up) % 16 == 0 && offsetof(Misc, wn) % 16 == 0 && offsetof(Misc, fT) % 16 == 0,
+              "float4 / float2 accesses of the gate tables need 16-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Tensor-memory columns.
@@ -468,20 +475,21 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
     tmem_wait_st();
 }
 
-// After GEMM1 of a chunk: Y''_h = Diag-scaled X''_h rows into shared memory
+// After GEMM1 of a chunk, half h (0 = T, 1 = S): Y''_h = Diag-scaled X''_h
+// rows into shared memory
 // (bf16, K-major [128 n][64 t]; Y''_T also as its bf16 residual):
 //   Y''_T[n][t] = fT[t] X''_T[n][t],  Y''_S[n][t] = fS[t] X''_S[n][t].
 // On a renormalisation chunk the stored state is also rescaled in tensor
 // memory, D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new
 // T rows is returned (else 0).
+template <int h>
 __device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, float dS, uint32_t tmem, int q,
                             int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
     float mloc = 0.f;
     uint32_t x[2][32];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    {
         const float* f = h ? ms->fS : ms->fT;
         tmem_ld32(tl + (h ? TM_XS : TM_XT), x[0]);
         tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32, x[1]);
@@ -869,7 +877,8 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         const uint32_t gc = g + c;
         if (!wg_all(2, wait_bar(&ms->x_done, gc & 1, ms, a))) return;
         tc_fence_after();
-        const float mloc = state_pass(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
+        const float mloc = state_pass<0>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
+        state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
         fence_async_smem();
         tc_fence_before();
         if (pl.rn) {
