@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_VERSION 100 /* 1.0.0 */
+#define HYPIC_VERSION 110 /* 1.1.0: hypic_reuse_chain */
 
 #if defined(__GNUC__)
 #define HYPIC_API __attribute__((visibility("default")))
@@ -212,6 +212,62 @@ typedef struct {
 } hypic_seam_args;
 
 HYPIC_API hypic_status hypic_seam_advance(const hypic_seam_args* args, hypic_stream_t stream);
+
+/* ------------------------------------------------------------ reuse chain --
+ * The reuse path of a request in one call ([AIBASE] linear-layer paragraph:
+ * the seam tokens after each cached segment are recomputed live and advance
+ * the running state, and the cached pairs are composed onto it).  For chain r
+ * and every (layer, head): S <- S0[r] (or 0 when S0 == NULL), then for each
+ * step j in [cu_chain[r], cu_chain[r+1]):
+ *   (1) advance S over the seam tokens [cu_step[j], cu_step[j+1]) of the
+ *       packed seam-token arrays, writing o_out[layer][t][head] = S_t^T q_t
+ *       for each, exactly as hypic_seam_advance;
+ *   (2) S <- T_p S + S_p with p = seg_idx[j], exactly as hypic_compose.
+ * Finally S_out[r] <- S.  A step without seam tokens is a plain compose step.
+ * Pair tables, T_exp_tab, seg_idx, S0 and S_out: as for hypic_compose.
+ * Seam tokens (n_tokens = cu_step[n_steps], n_steps = cu_chain[n_chains]):
+ * q, k, v, the gates and o_out as for hypic_seam_advance.
+ * GDN with dk = dv = 128 runs as one fused kernel that keeps every running
+ * state on chip from the first step to the last (no workspace).  Every other
+ * supported case runs the two calls step by step and needs a workspace of
+ * hypic_chain_workspace_size(args) bytes (two states of one chain), 256-byte
+ * aligned, owned by the caller until the call completes on the stream;
+ * HYPIC_ERR_WORKSPACE when it is needed and NULL or too small.
+ * Supported: as hypic_seam_advance and hypic_compose together.
+ */
+typedef struct {
+    int family;
+    int in_dtype;                   /* of q, k, v */
+    int n_layers, n_heads, dk, dv;
+    int n_pairs;
+    const float* T_tab;
+    const int32_t* T_exp_tab;
+    const float* S_tab;
+    int n_chains;
+    const int32_t* cu_chain;        /* device [n_chains+1], non-decreasing from 0 */
+    const int32_t* cu_chain_host;   /* host copy */
+    const int32_t* seg_idx;         /* device [n_steps], each in [0, n_pairs) */
+    const int32_t* seg_idx_host;    /* host copy (validation) */
+    const int32_t* cu_step;         /* device [n_steps+1], non-decreasing from 0 to n_tokens */
+    const int32_t* cu_step_host;    /* host copy */
+    int64_t n_tokens;               /* seam tokens in all */
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const float* gamma;
+    const float* g;
+    const float* S0;                /* device [n_chains][n_layers][n_heads][dk][dv] or NULL */
+    float* S_out;                   /* device [n_chains][n_layers][n_heads][dk][dv] */
+    float* o_out;                   /* device [n_layers][n_tokens][n_heads][dv] */
+} hypic_chain_args;
+
+/* Workspace bytes hypic_reuse_chain needs for these arguments (0 on the
+   fused path); 0 also when the arguments are invalid (the call reports why). */
+HYPIC_API size_t hypic_chain_workspace_size(const hypic_chain_args* args);
+HYPIC_API hypic_status hypic_reuse_chain(const hypic_chain_args* args, void* workspace, size_t workspace_bytes,
+                                         hypic_stream_t stream);
 
 /* -------------------------------------------------------- no-alloc build --
  * No counterpart in the HYPIC pages: this entry point exists for callers of the

@@ -50,9 +50,18 @@ class SeamArgs(ctypes.Structure):
                 ("state_in", _P), ("state_out", _P), ("o_out", _P)]
 
 
+class ChainArgs(ctypes.Structure):
+    _fields_ = [("family", _I), ("in_dtype", _I), ("n_layers", _I), ("n_heads", _I), ("dk", _I), ("dv", _I),
+                ("n_pairs", _I), ("T_tab", _P), ("T_exp_tab", _P), ("S_tab", _P), ("n_chains", _I),
+                ("cu_chain", _P), ("cu_chain_host", _P), ("seg_idx", _P), ("seg_idx_host", _P),
+                ("cu_step", _P), ("cu_step_host", _P), ("n_tokens", _LL),
+                ("q", _P), ("k", _P), ("v", _P), ("alpha", _P), ("beta", _P), ("gamma", _P), ("g", _P),
+                ("S0", _P), ("S_out", _P), ("o_out", _P)]
+
+
 EXPORTS = ["hypic_build_workspace_size", "hypic_segment_build", "hypic_compose", "hypic_seam_advance",
            "hypic_status_string", "hypic_last_error_detail", "hypic_version", "hypic_check_device",
-           "hypic_segment_build_noalloc"]
+           "hypic_segment_build_noalloc", "hypic_chain_workspace_size", "hypic_reuse_chain"]
 NOALLOC_MAX_SEGMENTS = 16384
 
 
@@ -69,7 +78,11 @@ def _load():
     lib.hypic_compose.argtypes = [ctypes.POINTER(ComposeArgs), _P]
     lib.hypic_seam_advance.argtypes = [ctypes.POINTER(SeamArgs), _P]
     lib.hypic_check_device.argtypes = [_P]
-    for f in (lib.hypic_segment_build, lib.hypic_compose, lib.hypic_seam_advance, lib.hypic_check_device):
+    lib.hypic_chain_workspace_size.argtypes = [ctypes.POINTER(ChainArgs)]
+    lib.hypic_chain_workspace_size.restype = ctypes.c_size_t
+    lib.hypic_reuse_chain.argtypes = [ctypes.POINTER(ChainArgs), _P, ctypes.c_size_t, _P]
+    for f in (lib.hypic_segment_build, lib.hypic_compose, lib.hypic_seam_advance, lib.hypic_check_device,
+              lib.hypic_reuse_chain):
         f.restype = _I
     lib.hypic_status_string.argtypes = [_I]
     lib.hypic_status_string.restype = ctypes.c_char_p
@@ -289,6 +302,61 @@ def seam_advance(family, q, k, v, cu_seam, *, alpha=None, beta=None, gamma=None,
     _check(hypic_seam_advance(a, _stream(stream)))
     del keep
     return state_out, o_out
+
+
+def hypic_chain_workspace_size(args: ChainArgs) -> int:
+    return lib.hypic_chain_workspace_size(ctypes.byref(args))
+
+
+def hypic_reuse_chain(args: ChainArgs, workspace, workspace_bytes: int, stream) -> int:
+    return lib.hypic_reuse_chain(ctypes.byref(args), workspace, workspace_bytes, stream)
+
+
+def chain_args(family, S_tab, cu_chain, seg_idx, cu_step, q, k, v, *, T_tab=None, T_exp_tab=None, alpha=None,
+               beta=None, gamma=None, g=None, S0=None, S_out=None, o_out=None, cu_chain_dev=None, seg_idx_dev=None,
+               cu_step_dev=None):
+    fam = FAMILY[family] if isinstance(family, str) else family
+    cu = _host_i32(cu_chain)
+    idx = _host_i32(seg_idx)
+    cs = _host_i32(cu_step)
+    dev = S_tab.device
+    cu_d = _dev_i32(cu, cu_chain_dev, dev)
+    idx_d = _dev_i32(idx, seg_idx_dev, dev) if len(idx) else None
+    cs_d = _dev_i32(cs, cu_step_dev, dev)
+    a = ChainArgs()
+    a.family, a.in_dtype = fam, _dtype_code(k)
+    a.n_pairs, a.n_layers, a.n_heads, a.dk, a.dv = S_tab.shape
+    a.T_tab, a.T_exp_tab, a.S_tab = _ptr(T_tab), _ptr(T_exp_tab), _ptr(S_tab)
+    a.n_chains = len(cu) - 1
+    a.cu_chain, a.cu_chain_host = _ptr(cu_d), _hptr(cu)
+    a.seg_idx, a.seg_idx_host = _ptr(idx_d), _hptr(idx) if len(idx) else None
+    a.cu_step, a.cu_step_host = _ptr(cs_d), _hptr(cs)
+    a.n_tokens = int(cs[-1])
+    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.alpha, a.beta, a.gamma, a.g = _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(g)
+    a.S0, a.S_out, a.o_out = _ptr(S0), _ptr(S_out), _ptr(o_out)
+    return a, (cu, idx, cs, cu_d, idx_d, cs_d)
+
+
+def reuse_chain(family, S_tab, cu_chain, seg_idx, cu_step, q, k, v, *, T_tab=None, T_exp_tab=None, alpha=None,
+                beta=None, gamma=None, g=None, S0=None, out=None, o_out=None, stream=None):
+    """(end states [n_chains][L][H][dk][dv], seam outputs [L][n_tokens][H][dv]) via
+    hypic_reuse_chain; q, k, v: [L][n_tokens][H][d] seam tokens, packed by step."""
+    import torch
+    n_chains = len(cu_chain) - 1
+    L, N, H, dk = k.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((n_chains,) + tuple(S_tab.shape[1:]), dtype=torch.float32, device=S_tab.device)
+    if o_out is None:
+        o_out = torch.empty((L, N, H, dv), dtype=torch.float32, device=S_tab.device)
+    a, keep = chain_args(family, S_tab, cu_chain, seg_idx, cu_step, q, k, v, T_tab=T_tab, T_exp_tab=T_exp_tab,
+                         alpha=alpha, beta=beta, gamma=gamma, g=g, S0=S0, S_out=out, o_out=o_out)
+    nbytes = hypic_chain_workspace_size(a)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=S_tab.device) if nbytes else None
+    _check(hypic_reuse_chain(a, _ptr(ws), nbytes, _stream(stream)))
+    del keep
+    return out, o_out
 
 
 def check_device(stream=None):

@@ -366,6 +366,198 @@ extern "C" hypic_status hypic_seam_advance(const hypic_seam_args* args, hypic_st
     return HYPIC_OK;
 }
 
+// ------------------------------------------------------------ reuse chain --
+
+namespace {
+
+// The chain as the compose call it contains (same tables and chains).
+hypic_compose_args chain_compose_view(const hypic_chain_args* a) {
+    hypic_compose_args c;
+    c.family = a->family;
+    c.n_layers = a->n_layers;
+    c.n_heads = a->n_heads;
+    c.dk = a->dk;
+    c.dv = a->dv;
+    c.n_pairs = a->n_pairs;
+    c.T_tab = a->T_tab;
+    c.T_exp_tab = a->T_exp_tab;
+    c.S_tab = a->S_tab;
+    c.n_chains = a->n_chains;
+    c.cu_chain = a->cu_chain;
+    c.cu_chain_host = a->cu_chain_host;
+    c.seg_idx = a->seg_idx;
+    c.seg_idx_host = a->seg_idx_host;
+    c.S0 = a->S0;
+    c.S_out = a->S_out;
+    return c;
+}
+
+hypic_status check_chain(const hypic_chain_args* a) {
+    if (!a) return fail(HYPIC_ERR_INVALID_ARG, "args is NULL");
+    const hypic_compose_args c = chain_compose_view(a);
+    hypic_status st = check_compose(&c);
+    if (st != HYPIC_OK) return st;
+    const int n_steps = a->cu_chain_host[a->n_chains];
+    if (a->n_tokens < 0 || a->n_tokens > INT32_MAX)
+        return fail(HYPIC_ERR_INVALID_ARG, "n_tokens %lld", (long long)a->n_tokens);
+    if (!a->cu_step || !a->cu_step_host) return fail(HYPIC_ERR_INVALID_ARG, "cu_step (device and host) required");
+    const int32_t* cu = a->cu_step_host;
+    if (cu[0] != 0) return fail(HYPIC_ERR_INVALID_ARG, "cu_step[0] = %d (must be 0)", cu[0]);
+    for (int j = 0; j < n_steps; ++j)
+        if (cu[j + 1] < cu[j]) return fail(HYPIC_ERR_INVALID_ARG, "cu_step decreases at %d", j);
+    if ((int64_t)cu[n_steps] != a->n_tokens)
+        return fail(HYPIC_ERR_INVALID_ARG, "cu_step[n_steps] = %d != n_tokens %lld", cu[n_steps], (long long)a->n_tokens);
+    const bool has_tokens = a->n_tokens > 0;
+    st = check_family(a->family, a->in_dtype, a->n_layers, a->n_heads, a->dk, a->dv, has_tokens, a->alpha, a->beta,
+                      a->gamma, a->g, true);
+    if (st != HYPIC_OK) return st;
+    if (has_tokens && (!a->q || !a->k || !a->v || !a->o_out))
+        return fail(HYPIC_ERR_INVALID_ARG, "q, k, v and o_out required");
+    const void* ptrs[] = {a->q, a->k, a->v, a->o_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    const size_t LH = (size_t)a->n_layers * a->n_heads;
+    const size_t state = sizeof(float) * (size_t)a->dk * a->dv * LH;
+    const size_t o_b = sizeof(float) * (size_t)a->n_layers * a->n_tokens * a->n_heads * a->dv;
+    if (overlap(a->o_out, o_b, a->S_out, state * a->n_chains) || overlap(a->o_out, o_b, a->S0, state * a->n_chains) ||
+        overlap(a->o_out, o_b, a->S_tab, state * a->n_pairs) ||
+        overlap(a->o_out, o_b, a->T_tab, T_bytes_per_obj(a->family, a->dk) * LH * a->n_pairs))
+        return fail(HYPIC_ERR_INVALID_ARG, "o_out overlaps another buffer");
+    return HYPIC_OK;
+}
+
+ChainParams chain_params(const hypic_chain_args* a) {
+    ChainParams p;
+    p.c.family = a->family;
+    p.c.n_layers = a->n_layers;
+    p.c.n_heads = a->n_heads;
+    p.c.dk = a->dk;
+    p.c.dv = a->dv;
+    p.c.n_pairs = a->n_pairs;
+    p.c.n_chains = a->n_chains;
+    p.c.T_tab = a->T_tab;
+    p.c.T_exp_tab = a->T_exp_tab;
+    p.c.S_tab = a->S_tab;
+    p.c.cu_chain = a->cu_chain;
+    p.c.seg_idx = a->seg_idx;
+    p.c.S0 = a->S0;
+    p.c.S_out = a->S_out;
+    p.in_dtype = a->in_dtype;
+    p.n_tokens = a->n_tokens;
+    p.cu_step = a->cu_step;
+    p.q = a->q;
+    p.k = a->k;
+    p.v = a->v;
+    p.alpha = a->alpha;
+    p.beta = a->beta;
+    p.o_out = a->o_out;
+    return p;
+}
+
+size_t chain_state_floats(const hypic_chain_args* a) {
+    return (size_t)a->dk * a->dv * a->n_layers * a->n_heads;
+}
+
+// Step-by-step path: two ping-pong states of one chain, then the indices
+// 0..n_steps (each step's compose is a one-step chain [j, j + 1) of seg_idx).
+size_t chain_ws_bytes(const hypic_chain_args* a) {
+    const size_t st = (sizeof(float) * chain_state_floats(a) + 255) / 256 * 256;
+    const size_t n_steps = (size_t)a->cu_chain_host[a->n_chains];
+    return 2 * st + (sizeof(int32_t) * (n_steps + 1) + 255) / 256 * 256;
+}
+
+__global__ void iota_kernel(int32_t* x, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) x[i] = i;
+}
+
+}  // namespace
+
+extern "C" size_t hypic_chain_workspace_size(const hypic_chain_args* args) {
+    if (check_chain(args) != HYPIC_OK) return 0;
+    if (args->n_chains == 0 || chain_tc_supported(chain_params(args))) return 0;
+    return chain_ws_bytes(args);
+}
+
+extern "C" hypic_status hypic_reuse_chain(const hypic_chain_args* args, void* workspace, size_t workspace_bytes,
+                                          hypic_stream_t stream) {
+    hypic_status st = check_chain(args);
+    if (st != HYPIC_OK) return st;
+    if (args->n_chains == 0) return HYPIC_OK;
+    const ChainParams cp = chain_params(args);
+    const bool fused = chain_tc_supported(cp);
+    const size_t need = fused ? 0 : chain_ws_bytes(args);
+    if (!fused && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(HYPIC_ERR_WORKSPACE, "workspace of %zu bytes (256-byte aligned) required, got %zu at %p", need,
+                    workspace_bytes, workspace);
+    cudaError_t e;
+    unsigned* err = err_word(&e);
+    if (!err) return cuda_fail(e, "device error word");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fused) {
+        e = launch_chain_tc(cp, err, s);
+        if (e != cudaSuccess) return cuda_fail(e, "reuse chain launch");
+        return HYPIC_OK;
+    }
+    const size_t sf = chain_state_floats(args);
+    const size_t st_b = (sizeof(float) * sf + 255) / 256 * 256;
+    float* buf[2] = {reinterpret_cast<float*>(workspace),
+                     reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + st_b)};
+    int32_t* iota = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + 2 * st_b);
+    const int n_steps = args->cu_chain_host[args->n_chains];
+    iota_kernel<<<(n_steps + 1 + 255) / 256, 256, 0, s>>>(iota, n_steps + 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "reuse chain launch");
+    for (int r = 0; r < args->n_chains; ++r) {
+        const float* cur = args->S0 ? args->S0 + r * sf : nullptr;
+        float* out = args->S_out + r * sf;
+        const int c0 = args->cu_chain_host[r], c1 = args->cu_chain_host[r + 1];
+        if (c0 == c1) {  // no steps: the start state
+            e = cur ? cudaMemcpyAsync(out, cur, sizeof(float) * sf, cudaMemcpyDeviceToDevice, s)
+                    : cudaMemsetAsync(out, 0, sizeof(float) * sf, s);
+            if (e != cudaSuccess) return cuda_fail(e, "reuse chain copy");
+            continue;
+        }
+        int nb = 0;
+        for (int j = c0; j < c1; ++j) {
+            if (args->cu_step_host[j + 1] > args->cu_step_host[j]) {  // seam tokens of step j
+                SeamParams sp;
+                sp.family = args->family;
+                sp.in_dtype = args->in_dtype;
+                sp.n_layers = args->n_layers;
+                sp.n_heads = args->n_heads;
+                sp.dk = args->dk;
+                sp.dv = args->dv;
+                sp.n_seams = 1;
+                sp.n_tokens = args->n_tokens;
+                sp.cu_seam = args->cu_step + j;  // tokens [cu_step[j], cu_step[j+1])
+                sp.q = args->q;
+                sp.k = args->k;
+                sp.v = args->v;
+                sp.alpha = args->alpha;
+                sp.beta = args->beta;
+                sp.gamma = args->gamma;
+                sp.g = args->g;
+                sp.state_in = cur;
+                sp.state_out = buf[nb];
+                sp.o_out = args->o_out;
+                if ((e = launch_seam(sp, err, s)) != cudaSuccess) return cuda_fail(e, "reuse chain seam");
+                cur = buf[nb];
+                nb ^= 1;
+            }
+            ComposeParams cp1 = cp.c;
+            cp1.n_chains = 1;
+            cp1.cu_chain = iota + j;  // the one-step chain [j, j + 1)
+            cp1.S0 = cur;
+            cp1.S_out = j + 1 == c1 ? out : buf[nb];
+            e = compose_tc_supported(cp1) ? launch_compose_tc(cp1, err, s) : launch_compose_simt(cp1, err, s);
+            if (e != cudaSuccess) return cuda_fail(e, "reuse chain compose");
+            cur = cp1.S_out;
+            nb ^= 1;
+        }
+    }
+    return HYPIC_OK;
+}
+
 // ------------------------------------------------------------------- misc --
 
 extern "C" const char* hypic_status_string(hypic_status s) {

@@ -22,7 +22,9 @@
 // One CTA per SM, persistent over (chain, layer, head) items ordered
 // (layer, head)-major so that chains sharing a pair table run together.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <float.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
@@ -46,11 +48,25 @@ constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpCvt0 = 2, kWarpEpi0 = 6;
 constexpr uint32_t kSliceBytes = kD * 32 * 4;                    // 128 rows x 32 fp32 = 16 KB
 constexpr uint32_t OFF_RING = 0;                                 // kRing x (hi 16 KB, lo 16 KB)
 constexpr uint32_t OFF_SP = OFF_RING + kRing * 2 * kSliceBytes;  // S_p: 4 blocks [128 rows][32 cols] fp32
-constexpr uint32_t OFF_MISC = OFF_SP + 4 * kSliceBytes;
+// Reuse chain only: one seam unit (up to kU seam tokens) as the epilogue reads it.
+constexpr int kU = 8;
+constexpr uint32_t kUnitRows = kU * kD * 4;                      // [kU][128] fp32 = 4 KB
+constexpr uint32_t OFF_SK = OFF_SP + 4 * kSliceBytes;            // k rows
+constexpr uint32_t OFF_SQ = OFF_SK + kUnitRows;                  // g_t q_t rows
+constexpr uint32_t OFF_SW = OFF_SQ + kUnitRows;                  // W = That Diag(g) K rows
+constexpr uint32_t OFF_SU = OFF_SW + kUnitRows;                  // U = That V rows
+constexpr uint32_t OFF_MISC = OFF_SU + kUnitRows;
 
 struct Misc {
     uint64_t full[kRing], cvt[kRing], empty[kRing];
     uint64_t sp_full, sp_empty, d_done, a_ready, drain;
+    uint64_t seam_ready, seam_free;  // unit tables written / read
+    // the current seam unit: tokens [tok0, tok0 + nv); g = in-unit decay prefix
+    float kk[kU][kU], qk[kU][kU], th[kU][kU];  // k.k, q.k, That
+    float M[kU][kU];                 // (q_t . k_s) g_t / g_s, s <= t
+    float g[kU], lg[kU], sc[kU];     // g_t, log2 g_t, g_w / g_s
+    float beta[kU];
+    int tok0, nv;
     int item;
     int abort_flag;
     uint32_t tmem_base;
@@ -71,7 +87,23 @@ struct CtArgs {
     unsigned* counter;
     unsigned* err;
     uint32_t wait_limit;
+    // reuse chain: seam tokens before each step
+    int in_bf16;
+    int64_t n_tokens;
+    const int32_t* cu_step;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    float* o_out;
 };
+
+// Seam units of step j: ceil(w / kU) for its w seam tokens.
+__device__ __forceinline__ int step_units(const CtArgs& a, int j, int& tb) {
+    tb = a.cu_step[j];
+    return (a.cu_step[j + 1] - tb + kU - 1) / kU;
+}
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const CtArgs& a) {
     for (uint32_t i = 0; i < a.wait_limit; i += 256) {
@@ -153,8 +185,222 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem
     }
 }
 
+// ------------------------------------------------------------ seam units --
+// Reuse chain: before compose step j the running state advances over the
+// seam tokens of step j, taken kU at a time.  For a unit of tokens 1..w with
+// in-unit decay prefix g_t = a_1 ... a_t, A[t][s] = b_t (g_t/g_s) k_t.k_s
+// (s < t), That = (I + A)^-1 Diag(b), W = That Diag(g) K and U = That V (the
+// WY form of the token recurrence, as in the build), the state column
+// x = S[:, n] becomes, with u'_t = U[t][n] - W_t . x,
+//     S_t[:, n] = g_t x + sum_{s<=t} (g_t/g_s) k_s u'_s,
+//     o_t[n] = S_t[:, n] . q_t = g_t q_t . x + sum_{s<=t} (q_t . k_s)(g_t/g_s) u'_s,
+// and the unit ends at t = w (the padded tokens past w have a = 1, b = 0,
+// k = q = v = 0: identity steps).  The converter warpgroup builds the unit's
+// tables in shared memory while the MMAs of the previous compose run; the
+// epilogue applies them column by column.
+
+__device__ __forceinline__ float load_tok(const void* base, int bf16, int64_t row, int i) {
+    return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[row * kD + i])
+                : reinterpret_cast<const float*>(base)[row * kD + i];
+}
+
+// The tables of unit gu (tokens [tok0, tok0 + nv) of (layer, head) lh).
+// t: converter thread 0..127 (= feature index for the row loads).
+__device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int tok0, int nv, uint32_t gu, int t) {
+    if (gu >= 1 && !wg_all(3, wait_bar(&ms->seam_free, (gu - 1) & 1, ms, a))) return false;
+    const int layer = lh / a.n_heads, head = lh % a.n_heads;
+    float* Kf = reinterpret_cast<float*>(smem + OFF_SK);
+    float* Qf = reinterpret_cast<float*>(smem + OFF_SQ);
+    float* Wf = reinterpret_cast<float*>(smem + OFF_SW);
+    float* Uf = reinterpret_cast<float*>(smem + OFF_SU);
+    float vr[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const bool valid = u < nv;
+        const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head;
+        Kf[u * kD + t] = valid ? load_tok(a.k, a.in_bf16, row, t) : 0.f;
+        Qf[u * kD + t] = valid ? load_tok(a.q, a.in_bf16, row, t) : 0.f;
+        vr[u] = valid ? load_tok(a.v, a.in_bf16, row, t) : 0.f;
+    }
+    if (t < kU) {
+        const bool valid = t < nv;
+        const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + t) * a.n_heads + head;
+        ms->lg[t] = valid ? log2f(fmaxf(a.alpha[row], FLT_MIN)) : 0.f;
+        ms->beta[t] = valid ? a.beta[row] : 0.f;
+    }
+    named_sync(3);
+    {  // k_r . k_c (threads 0..63), q_r . k_c (threads 64..127)
+        const int r = (t >> 3) & 7, c = t & 7;
+        const float* x = (t < 64 ? Kf : Qf) + r * kD;
+        const float* y = Kf + c * kD;
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < kD; i += 8) {
+            const float4 x0 = *reinterpret_cast<const float4*>(x + i), x1 = *reinterpret_cast<const float4*>(x + i + 4);
+            const float4 y0 = *reinterpret_cast<const float4*>(y + i), y1 = *reinterpret_cast<const float4*>(y + i + 4);
+            d0 = fmaf(x0.x, y0.x, fmaf(x0.y, y0.y, fmaf(x0.z, y0.z, fmaf(x0.w, y0.w, d0))));
+            d1 = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, d1))));
+        }
+        (t < 64 ? ms->kk : ms->qk)[r][c] = d0 + d1;
+        if (t == 0) {  // in-unit log-decay prefix
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                acc += ms->lg[u];
+                ms->lg[u] = acc;
+            }
+        }
+    }
+    named_sync(3);
+    if (t < kU) {  // column c of (I + A)^-1 by forward substitution, then That = (.) Diag(b)
+        const int c = t;
+        float m[kU];
+#pragma unroll
+        for (int r = 0; r < kU; ++r) {
+            float acc = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < r; ++s2)
+                acc -= ms->beta[r] * exp2f(ms->lg[r] - ms->lg[s2]) * ms->kk[r][s2] * m[s2];
+            m[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < kU; ++r) ms->th[r][c] = m[r] * ms->beta[c];
+        ms->g[t] = exp2f(ms->lg[t]);
+        ms->sc[t] = exp2f(ms->lg[kU - 1] - ms->lg[t]);
+    } else if (t >= 64) {
+        const int r = (t - 64) >> 3, c = t & 7;
+        ms->M[r][c] = c <= r ? ms->qk[r][c] * exp2f(ms->lg[r] - ms->lg[c]) : 0.f;
+    }
+    named_sync(3);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {  // W, U and g_u q_u: column t
+        float w = 0.f, uu = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 <= u; ++s2) {
+            w = fmaf(ms->th[u][s2] * ms->g[s2], Kf[s2 * kD + t], w);
+            uu = fmaf(ms->th[u][s2], vr[s2], uu);
+        }
+        Wf[u * kD + t] = w;
+        Uf[u * kD + t] = uu;
+        Qf[u * kD + t] *= ms->g[u];
+    }
+    if (t == 0) {
+        ms->tok0 = tok0;
+        ms->nv = nv;
+    }
+    named_sync(3);
+    if (t == 0) mbar_arrive(&ms->seam_ready);
+    return true;
+}
+
+// The units of step js (global unit counter gu) for (layer, head) lh.
+__device__ bool prep_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int js, uint32_t& gu, int t) {
+    int tb;
+    const int nu = step_units(a, js, tb);
+    const int w = a.cu_step[js + 1] - tb;
+    for (int k = 0; k < nu; ++k) {
+        const int nv = w - kU * k < kU ? w - kU * k : kU;
+        if (!prep_unit(ms, smem, a, lh, tb + kU * k, nv, gu, t)) return false;
+        ++gu;
+    }
+    return true;
+}
+
+// Applies the units of step js to the column in TM_D (epilogue thread n);
+// the last unit writes the split A operand of the next compose instead.
+__device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tl, int lh, int js, uint32_t& gu,
+                                 int n) {
+    int tb;
+    const int nu = step_units(a, js, tb);
+    const int layer = lh / a.n_heads, head = lh % a.n_heads;
+    const float* Kf = reinterpret_cast<const float*>(smem + OFF_SK);
+    const float* Qf = reinterpret_cast<const float*>(smem + OFF_SQ);
+    const float* Wf = reinterpret_cast<const float*>(smem + OFF_SW);
+    const float* Uf = reinterpret_cast<const float*>(smem + OFF_SU);
+    for (int k = 0; k < nu; ++k) {
+        if (!wg_all(4, wait_bar(&ms->seam_ready, gu & 1, ms, a))) return false;
+        float wt[kU], qs[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) wt[u] = qs[u] = 0.f;
+#pragma unroll 1
+        for (int cb = 0; cb < 8; ++cb) {  // pass 1: W_u . x and g_u q_u . x
+            uint32_t x[16];
+            tmem_ld16(tl + TM_D + 16 * cb, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4) {
+                const int i = 16 * cb + jj;
+                const float x0 = __uint_as_float(x[jj]), x1 = __uint_as_float(x[jj + 1]);
+                const float x2 = __uint_as_float(x[jj + 2]), x3 = __uint_as_float(x[jj + 3]);
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const float4 w4 = *reinterpret_cast<const float4*>(Wf + u * kD + i);
+                    const float4 q4 = *reinterpret_cast<const float4*>(Qf + u * kD + i);
+                    wt[u] = fmaf(w4.x, x0, fmaf(w4.y, x1, fmaf(w4.z, x2, fmaf(w4.w, x3, wt[u]))));
+                    qs[u] = fmaf(q4.x, x0, fmaf(q4.y, x1, fmaf(q4.z, x2, fmaf(q4.w, x3, qs[u]))));
+                }
+            }
+        }
+        float up[kU], c[kU];
+        const int nv = ms->nv, tok0 = ms->tok0;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) up[u] = Uf[u * kD + n] - wt[u];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            float o = qs[u];
+#pragma unroll
+            for (int s2 = 0; s2 <= u; ++s2) o = fmaf(ms->M[u][s2], up[s2], o);
+            if (u < nv) a.o_out[(((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head) * kD + n] = o;
+            c[u] = ms->sc[u] * up[u];
+        }
+        const float gw = ms->g[kU - 1];
+        const bool last = k + 1 == nu;
+#pragma unroll 1
+        for (int cb = 0; cb < 8; ++cb) {  // pass 2: x <- g_w x + sum_s (g_w/g_s) k_s u'_s
+            uint32_t x[16];
+            tmem_ld16(tl + TM_D + 16 * cb, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4) {
+                const int i = 16 * cb + jj;
+                float y[4] = {gw * __uint_as_float(x[jj]), gw * __uint_as_float(x[jj + 1]),
+                              gw * __uint_as_float(x[jj + 2]), gw * __uint_as_float(x[jj + 3])};
+#pragma unroll
+                for (int s2 = 0; s2 < kU; ++s2) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(Kf + s2 * kD + i);
+                    y[0] = fmaf(k4.x, c[s2], y[0]);
+                    y[1] = fmaf(k4.y, c[s2], y[1]);
+                    y[2] = fmaf(k4.z, c[s2], y[2]);
+                    y[3] = fmaf(k4.w, c[s2], y[3]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[jj + e] = __float_as_uint(y[e]);
+            }
+            if (last) {  // the A operand of the next compose, split hi/lo
+                uint32_t h[16], l[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) split_tf32(__uint_as_float(x[e]), h[e], l[e]);
+                tmem_st16(tl + TM_AB + 16 * cb, h);
+                tmem_st16(tl + TM_AS + 16 * cb, l);
+            } else {
+                tmem_st16(tl + TM_D + 16 * cb, x);
+            }
+            tmem_wait_st();
+        }
+        named_sync(4);  // every column has read the unit's tables
+        if (n == 0) mbar_arrive(&ms->seam_free);
+        ++gu;
+    }
+    return true;
+}
+
 // Split each T slice into hi (in place) and lo (beside it).  t: 0..127.
-__device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t gs, int len, int t) {
+// Reuse chain: also the seam units, those of step 0 first and those of step
+// j + 1 while the MMAs of step j run.
+template <bool kSeam>
+__device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t gs, uint32_t gu, int c0, int len,
+                             int lh, int t) {
+    if (kSeam && len > 0 && !prep_step_units(ms, smem, a, lh, c0, gu, t)) return;
     for (int j = 0; j < len; ++j) {
         for (int s = 0; s < kSlices; ++s) {
             const uint32_t gsi = gs + kSlices * j + s, buf = gsi % kRing;
@@ -177,6 +423,7 @@ __device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t 
             named_sync(3);
             if (t == 0) mbar_arrive(&ms->cvt[buf]);
         }
+        if (kSeam && j + 1 < len && !prep_step_units(ms, smem, a, lh, c0 + j + 1, gu, t)) return;
     }
 }
 
@@ -243,7 +490,92 @@ __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t
     }
 }
 
+// Reuse-chain epilogue: as epilogue_role, with the seam units of step j + 1
+// applied to the composed column before it becomes the A operand of step
+// j + 1 (and those of step 0 to the start state).
+__device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gj,
+                                   uint32_t gu, int c0, int len, int lh, int64_t obj, int q, int lane) {
+    const int n = 32 * q + lane;
+    const int LH = a.n_layers * a.n_heads;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    float* out = a.S_out + obj * kD * kD;
+    const float* s0 = a.S0 ? a.S0 + obj * kD * kD : nullptr;
+    if (len == 0) {
+        for (int i = 0; i < kD; ++i) out[i * kD + n] = s0 ? s0[i * kD + n] : 0.f;
+        return;
+    }
+    int tb;
+    if (step_units(a, c0, tb) == 0) {  // A for the first step: the start state, split hi/lo
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t h[32], l[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) split_tf32(s0 ? s0[(32 * cb + jj) * kD + n] : 0.f, h[jj], l[jj]);
+            tmem_st32(tl + TM_AB + 32 * cb, h);
+            tmem_st32(tl + TM_AS + 32 * cb, l);
+        }
+        tmem_wait_st();
+    } else {  // the start state through the seam of step 0
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t x[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(s0 ? s0[(32 * cb + jj) * kD + n] : 0.f);
+            tmem_st32(tl + TM_D + 32 * cb, x);
+        }
+        tmem_wait_st();
+        if (!apply_step_units(ms, smem, a, tl, lh, c0, gu, n)) return;
+    }
+    tc_fence_before();
+    named_sync(4);
+    if (n == 0) mbar_arrive(&ms->a_ready);
+    const float* sp = reinterpret_cast<const float*>(smem + OFF_SP) + (n >> 5) * (kSliceBytes / 4) + (n & 31);
+    for (int j = 0; j < len; ++j) {
+        const uint32_t g = gj + j;
+        const int p = a.seg_idx[c0 + j];
+        const int e = a.T_exp ? a.T_exp[p * LH + lh] : 0;
+        bool ok = wait_bar(&ms->d_done, g & 1, ms, a);
+        ok = ok && wait_bar(&ms->sp_full, g & 1, ms, a);
+        if (!wg_all(4, ok)) return;
+        tc_fence_after();
+        const bool last = j + 1 == len;
+        const bool seam = !last && step_units(a, c0 + j + 1, tb) > 0;
+#pragma unroll 1
+        for (int cb = 0; cb < 8; ++cb) {
+            uint32_t x[16];
+            tmem_ld16(tl + TM_D + 16 * cb, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int i = 16 * cb + jj;
+                const float v = ldexpf(__uint_as_float(x[jj]), e) + sp[i * 32];
+                if (last) out[i * kD + n] = v;
+                x[jj] = __float_as_uint(v);
+            }
+            if (seam) {
+                tmem_st16(tl + TM_D + 16 * cb, x);
+            } else if (!last) {
+                uint32_t h[16], l[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[jj]), h[jj], l[jj]);
+                tmem_st16(tl + TM_AB + 16 * cb, h);
+                tmem_st16(tl + TM_AS + 16 * cb, l);
+            }
+        }
+        tmem_wait_st();
+        named_sync(4);
+        if (n == 0) mbar_arrive(&ms->sp_empty);  // S_p has been read
+        if (seam && !apply_step_units(ms, smem, a, tl, lh, c0 + j + 1, gu, n)) return;
+        if (!last) {
+            tc_fence_before();
+            named_sync(4);
+            if (n == 0) mbar_arrive(&ms->a_ready);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- kernel --
+template <bool kSeam>
 __global__ void __launch_bounds__(kThreads, 1)
     compose_tc_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmS, const CtArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -264,6 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms->d_done, 1);
         mbar_init(&ms->a_ready, 1);
         mbar_init(&ms->drain, 1);
+        mbar_init(&ms->seam_ready, 1);
+        mbar_init(&ms->seam_free, 1);
         ms->abort_flag = 0;
         fence_mbar_init();
     }
@@ -277,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
     const int LH = a.n_layers * a.n_heads;
-    uint32_t gs = 0, gj = 0;
+    uint32_t gs = 0, gj = 0, gu = 0;
     for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
         if (*(volatile int*)&ms->abort_flag) break;
         const int lh = item / a.n_chains, chain = item % a.n_chains;
@@ -288,7 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kWarpMMA) {
             if (lane == 0) mma_role(ms, smem, a, tmem, gs, gj, len);
         } else if (warp < kWarpEpi0) {
-            convert_role(ms, smem, a, gs, len, tid - 32 * kWarpCvt0);
+            convert_role<kSeam>(ms, smem, a, gs, gu, c0, len, lh, tid - 32 * kWarpCvt0);
+        } else if (kSeam) {
+            epilogue_role_seam(ms, smem, a, tmem, gj, gu, c0, len, lh, obj, warp & 3, lane);
         } else {
             epilogue_role(ms, smem, a, tmem, gj, c0, len, lh, obj, warp & 3, lane);
         }
@@ -297,6 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         gs += kSlices * len;
         gj += len;
+        if (kSeam)
+            for (int j = 0; j < len; ++j) {
+                int tb;
+                gu += step_units(a, c0 + j, tb);
+            }
     }
     if (warp == kWarpMMA) {
         if (lane == 0) {
@@ -354,14 +695,16 @@ bool compose_tc_supported(const ComposeParams& p) {
            (int64_t)p.n_pairs * p.n_layers * p.n_heads * kD < INT32_MAX && encode_fn() != nullptr;
 }
 
-cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_t s) {
+namespace {
+
+template <bool kSeam>
+cudaError_t launch_tc(const ComposeParams& p, CtArgs a, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const uint64_t rows = (uint64_t)p.n_pairs * p.n_layers * p.n_heads * kD;
     CUtensorMap tT, tS;
     if (!make_map(enc, &tT, p.T_tab, rows, true) || !make_map(enc, &tS, p.S_tab, rows, false))
         return cudaErrorInvalidValue;
-    CtArgs a;
     a.n_layers = p.n_layers;
     a.n_heads = p.n_heads;
     a.n_pairs = p.n_pairs;
@@ -373,16 +716,41 @@ cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_
     a.S0 = p.S0;
     a.S_out = p.S_out;
     a.counter = nullptr;
-    a.err = err;
     a.wait_limit = 1u << 26;
     if (a.n_items == 0) return cudaSuccess;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel<kSeam>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = a.n_items < sms ? a.n_items : sms;
-    compose_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tT, tS, a);
+    compose_tc_kernel<kSeam><<<grid, kThreads, kSmemBytes, s>>>(tT, tS, a);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_t s) {
+    CtArgs a = {};
+    a.err = err;
+    return launch_tc<false>(p, a, s);
+}
+
+bool chain_tc_supported(const ChainParams& p) { return compose_tc_supported(p.c) && p.c.n_pairs > 0; }
+
+cudaError_t launch_chain_tc(const ChainParams& p, unsigned* err, cudaStream_t s) {
+    CtArgs a = {};
+    a.err = err;
+    a.in_bf16 = p.in_dtype == kBF16;
+    a.n_tokens = p.n_tokens;
+    a.cu_step = p.cu_step;
+    a.q = p.q;
+    a.k = p.k;
+    a.v = p.v;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.o_out = p.o_out;
+    return launch_tc<true>(p.c, a, s);
 }
 
 }  // namespace hypic

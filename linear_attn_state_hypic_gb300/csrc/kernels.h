@@ -67,4 +67,22 @@ bool gdn_build_tc_supported(const BuildParams& p);
 cudaError_t launch_compose(const ComposeParams& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_seam(const SeamParams& p, unsigned* err, cudaStream_t s);
 
+// Reuse chain: the compose chain of `c` with, before step j, a seam advance
+// over the seam tokens [cu_step[j], cu_step[j+1]) (layouts as SeamParams).
+struct ChainParams {
+    ComposeParams c;
+    int in_dtype;
+    int64_t n_tokens;
+    const int32_t* cu_step;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    float* o_out;
+};
+// GDN, d = 128: one fused tensor-core kernel (state on chip for the whole chain).
+bool chain_tc_supported(const ChainParams& p);
+cudaError_t launch_chain_tc(const ChainParams& p, unsigned* err, cudaStream_t s);
+
 }  // namespace hypic

@@ -29,7 +29,8 @@ def declared_functions():
 
 def test_header_declares_the_three_calls():
     fns = declared_functions()
-    for f in ("hypic_segment_build", "hypic_compose", "hypic_seam_advance", "hypic_build_workspace_size"):
+    for f in ("hypic_segment_build", "hypic_compose", "hypic_seam_advance", "hypic_build_workspace_size",
+              "hypic_reuse_chain", "hypic_chain_workspace_size"):
         assert f in fns
 
 
@@ -47,7 +48,8 @@ def test_library_exports_every_declared_symbol(B):
 def test_struct_layout_matches_header(B, tmp_path):
     """Compile a probe against include/hypic.h with gcc and compare sizeof and
     every field offset with the ctypes mirrors."""
-    structs = {"hypic_build_args": B.BuildArgs, "hypic_compose_args": B.ComposeArgs, "hypic_seam_args": B.SeamArgs}
+    structs = {"hypic_build_args": B.BuildArgs, "hypic_compose_args": B.ComposeArgs, "hypic_seam_args": B.SeamArgs,
+               "hypic_chain_args": B.ChainArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "hypic.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
@@ -69,7 +71,7 @@ def test_struct_layout_matches_header(B, tmp_path):
 
 
 def test_status_strings_and_version(B):
-    assert B.hypic_version() == 100
+    assert B.hypic_version() == 110
     for code, name in enumerate(["HYPIC_OK", "HYPIC_ERR_INVALID_ARG", "HYPIC_ERR_UNSUPPORTED", "HYPIC_ERR_WORKSPACE",
                                  "HYPIC_ERR_CUDA", "HYPIC_ERR_TIMEOUT"]):
         assert B.lib.hypic_status_string(code).decode() == name
@@ -237,3 +239,51 @@ def test_seam_rejections(B, mutate, status):
     a, cu = base_seam(B)
     mutate(a, cu)
     assert B.hypic_seam_advance(a, None) == status
+
+
+def base_chain(B, family=0, d=64, chains=((0, 1), (1,)), widths=(8, 0, 3)):
+    cu = np.array([0] + list(np.cumsum([len(c) for c in chains])), np.int32)
+    idx = np.array([i for c in chains for i in c], np.int32)
+    cs = np.concatenate([[0], np.cumsum(widths)]).astype(np.int32)
+    a = B.ChainArgs()
+    a.family, a.in_dtype, a.n_layers, a.n_heads, a.dk, a.dv, a.n_pairs = family, 1, 2, 2, d, d, 2
+    a.T_tab = fake(1) if family != 3 else None
+    a.S_tab = fake(2)
+    a.n_chains = len(chains)
+    a.cu_chain, a.cu_chain_host = fake(3), cu.ctypes.data
+    a.seg_idx, a.seg_idx_host = fake(4), idx.ctypes.data
+    a.cu_step, a.cu_step_host = fake(5), cs.ctypes.data
+    a.n_tokens = int(cs[-1])
+    a.q, a.k, a.v = fake(7), fake(8), fake(9)
+    if family == 0:
+        a.alpha, a.beta = fake(10), fake(11)
+    a.S_out, a.o_out = fake(12), fake(13)
+    return a, (cu, idx, cs)
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a, k: setattr(a, "n_tokens", 10), 1),         # cu_step[-1] != n_tokens
+    (lambda a, k: k[2].__setitem__(1, -1), 1),            # cu_step decreases
+    (lambda a, k: k[1].__setitem__(0, 2), 1),             # pair index out of range
+    (lambda a, k: setattr(a, "q", None), 1),
+    (lambda a, k: setattr(a, "beta", None), 1),
+    (lambda a, k: setattr(a, "o_out", fake(12)), 1),      # o_out overlaps S_out
+    (lambda a, k: setattr(a, "dk", 48), 2),
+])
+def test_chain_rejections(B, mutate, status):
+    a, keep = base_chain(B)
+    mutate(a, keep)
+    assert B.hypic_reuse_chain(a, fake(20), 1 << 24, None) == status
+    assert B.hypic_chain_workspace_size(a) == 0
+
+
+def test_chain_step_by_step_path_needs_its_workspace(B):
+    """d = 64 runs step by step through a workspace of two states of one
+    chain plus the step indices; without it the call is refused before any
+    GPU work."""
+    a, keep = base_chain(B)
+    need = B.hypic_chain_workspace_size(a)
+    assert need >= 2 * 4 * 64 * 64 * 2 * 2
+    assert B.hypic_reuse_chain(a, None, 0, None) == B.ERR_WORKSPACE
+    assert B.hypic_reuse_chain(a, fake(20), need - 1, None) == B.ERR_WORKSPACE
+    assert B.hypic_reuse_chain(a, fake(20) + 16, need, None) == B.ERR_WORKSPACE  # not 256-byte aligned
