@@ -34,7 +34,7 @@ METRIC = "segment-build tokens/s (all layers×heads) + composes/s; % tensor/HBM 
 WORKLOAD = dict(n_layers=30, H=32, d=128, n_tokens=100_000, seam_w=8)
 FLOP_PER_TOKEN_HEAD = 180_224      # chunk-64 low-rank GDN build (gram, W, U, two state GEMMs)
 COMPOSE_BYTES = 131_072            # T_p + S_p (fp32, d=128) streamed per head-compose
-SEAM_STATE_BYTES = 131_072         # state read + write per seam-head
+SEAM_TOKEN_BYTES = 3 * 256 + 8 + 512  # per seam token-head: q, k, v bf16 in, a, b fp32 in, o fp32 out
 # DRAM bytes per algorithmic byte of the build kernel, from an ncu capture of
 # the 32-segment x 32-head ragged batch (822.2 MB of traffic for 815.8 MB of
 # inputs and outputs); the full launch is too large to capture, and its
@@ -141,30 +141,17 @@ class LongRequest:
         self.keep.append(k1)
         self.ws_bytes = B.hypic_build_workspace_size(self.bargs)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
-        # compose arguments: one single-step chain per segment, ping-ponging the state
-        self.cargs = []
-        cu1 = np.array([0, 1], np.int32)
-        for i in range(self.n_seg):
-            src, dst = (None, self.state) if i == 0 else ((self.state, self.state2) if i % 2 == 1
-                                                         else (self.state2, self.state))
-            a, kk = B.compose_args("gdn", self.S, cu1, np.array([i], np.int32), T_tab=self.T, T_exp_tab=self.T_exp,
-                                   S0=src, S_out=dst)
-            self.cargs.append(a)
-            self.keep.append(kk)
-        self.final = self.state if (self.n_seg - 1) % 2 == 0 else self.state2
-        # Each seam's inputs get their own contiguous [L][w][H][d] buffers (made
-        # once at setup: they are the fresh seam tokens of the reuse request).
-        self.seam_bufs = []
-        for idx in range(self.n_seg - 1):
-            o0, w = int(self.seam_off[idx]), int(self.skip[idx + 1])
-            bufs = [x[:, o0:o0 + w].contiguous() for x in (self.q_seam, self.k_seam, self.v_seam)]
-            gates = [x[:, o0:o0 + w].contiguous() for x in (self.a_seam, self.b_seam)]
-            o = torch.empty((self.L, w, self.H, self.d), dtype=torch.float32, device=device)
-            i = idx + 1
-            st = self.state if i % 2 == 1 else self.state2
-            a2, kk2 = B.seam_args("gdn", bufs[0], bufs[1], bufs[2], np.array([0, w], np.int32), alpha=gates[0],
-                                  beta=gates[1], state_in=st, state_out=st, o_out=o)
-            self.seam_bufs.append((a2, kk2, bufs, gates, o))
+        # The reuse chain: step 0 composes the first segment's pair onto a zero
+        # state; step i >= 1 advances over the seam tokens of segment i and then
+        # composes its body's pair (hypic_reuse_chain, one launch).
+        cu_step = np.concatenate([[0, 0], np.cumsum(self.skip[1:])]).astype(np.int32)
+        self.chain_args, k2 = B.chain_args("gdn", self.S, np.array([0, self.n_seg], np.int32),
+                                           np.arange(self.n_seg, dtype=np.int32), cu_step,
+                                           self.q_seam, self.k_seam, self.v_seam, T_tab=self.T, T_exp_tab=self.T_exp,
+                                           alpha=self.a_seam, beta=self.b_seam, S_out=self.state, o_out=self.o)
+        self.keep.append(k2)
+        assert B.hypic_chain_workspace_size(self.chain_args) == 0, "the fused chain path needs no workspace"
+        self.final = self.state
 
     def run_step(self, stream, ev=None):
         """One pass of the hot path; ev = (b0, b1, c0, c1) events around the build and the chain."""
@@ -174,17 +161,14 @@ class LongRequest:
         st = B.hypic_segment_build(self.bargs, self.ws.data_ptr(), self.ws_bytes, stream)
         if ev:
             ev[1].record()
-        st |= B.hypic_compose(self.cargs[0], stream)
-        for i in range(1, self.n_seg):
-            st |= B.hypic_seam_advance(self.seam_bufs[i - 1][0], stream)
-            st |= B.hypic_compose(self.cargs[i], stream)
+        st |= B.hypic_reuse_chain(self.chain_args, None, 0, stream)
         if ev:
             ev[2].record()
         if st != 0:
             raise RuntimeError("a library call failed in the step")
 
     def launches_per_step(self):
-        return 2 + 1 + 2 * (self.n_seg - 1)   # plan + build, first compose, seam + compose per seam
+        return 3   # build plan + build, reuse chain
 
 
 def time_our_arm(args, rank, world, device):
@@ -216,6 +200,7 @@ def time_our_arm(args, rank, world, device):
     ms_max = allreduce_max(ms, world)
     res = dict(ms=ms_max, build_ms=statistics.mean(build_ms), chain_ms=statistics.mean(chain_ms),
                clocks=clk.summary(), body_tokens=req.body_tokens, n_seg=req.n_seg,
+               seam_tokens=int(req.q_seam.shape[1]),
                launches=req.launches_per_step() * args.steps, req=req)
     return res
 
@@ -226,12 +211,12 @@ def e2e_our_arm(req, steps):
     final state and the seam outputs back."""
     import torch
     r = req.r
-    dev_in = [r["k"], r["v"], r["alpha"], r["beta"]] + [x for sb in req.seam_bufs for x in sb[2] + sb[3]]
+    dev_in = [r["k"], r["v"], r["alpha"], r["beta"], req.q_seam, req.k_seam, req.v_seam, req.a_seam, req.b_seam]
     t0 = time.time()
     host_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in dev_in]
     for h, d in zip(host_in, dev_in):
         h.copy_(d)
-    outs = [req.final] + [sb[4] for sb in req.seam_bufs]
+    outs = [req.final, req.o]
     host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
     setup_s = time.time() - t0
     h2d = sum(x.numel() * x.element_size() for x in host_in)
@@ -481,7 +466,10 @@ def main():
     build_tflops = build_flop / (res["build_ms"] / 1e3) / 1e12
     peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     n_comp = res["n_seg"]
-    chain_bytes = n_comp * LH * COMPOSE_BYTES + (res["n_seg"] - 1) * LH * SEAM_STATE_BYTES
+    # the fused chain keeps the running state on chip: the pair stream, the
+    # seam tokens and their outputs, and the end state
+    chain_bytes = (n_comp * LH * COMPOSE_BYTES + res["seam_tokens"] * LH * SEAM_TOKEN_BYTES
+                   + LH * WORKLOAD["d"] ** 2 * 4)
     chain_gbs = chain_bytes / (res["chain_ms"] / 1e3) / 1e9
     e2e = None
     if args.e2e_steps > 0:

@@ -50,7 +50,8 @@ constexpr uint32_t OFF_RING = 0;                                 // kRing x (hi 
 constexpr uint32_t OFF_SP = OFF_RING + kRing * 2 * kSliceBytes;  // S_p: 4 blocks [128 rows][32 cols] fp32
 // Reuse chain only: one seam unit (up to kU seam tokens) as the epilogue reads it.
 constexpr int kU = 8;
-constexpr uint32_t kUnitRows = kU * kD * 4;                      // [kU][128] fp32 = 4 KB
+constexpr int kUR = kD + 4;                                      // row stride (floats): rows fall in distinct banks
+constexpr uint32_t kUnitRows = kU * kUR * 4;                     // [kU][kUR] fp32
 constexpr uint32_t OFF_SK = OFF_SP + 4 * kSliceBytes;            // k rows
 constexpr uint32_t OFF_SQ = OFF_SK + kUnitRows;                  // g_t q_t rows
 constexpr uint32_t OFF_SW = OFF_SQ + kUnitRows;                  // W = That Diag(g) K rows
@@ -62,7 +63,7 @@ struct Misc {
     uint64_t sp_full, sp_empty, d_done, a_ready, drain;
     uint64_t seam_ready, seam_free;  // unit tables written / read
     // the current seam unit: tokens [tok0, tok0 + nv); g = in-unit decay prefix
-    float kk[kU][kU], qk[kU][kU], th[kU][kU];  // k.k, q.k, That
+    float kk[kU][kU], qk[kU][kU], th[kU][kU], thg[kU][kU];  // k.k then A, q.k, That, That Diag(g)
     float M[kU][kU];                 // (q_t . k_s) g_t / g_s, s <= t
     float g[kU], lg[kU], sc[kU];     // g_t, log2 g_t, g_w / g_s
     float beta[kU];
@@ -200,8 +201,8 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem
 // epilogue applies them column by column.
 
 __device__ __forceinline__ float load_tok(const void* base, int bf16, int64_t row, int i) {
-    return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[row * kD + i])
-                : reinterpret_cast<const float*>(base)[row * kD + i];
+    return bf16 ? __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(base) + row * kD + i))
+                : __ldg(reinterpret_cast<const float*>(base) + row * kD + i);
 }
 
 // The tables of unit gu (tokens [tok0, tok0 + nv) of (layer, head) lh).
@@ -213,26 +214,37 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
     float* Qf = reinterpret_cast<float*>(smem + OFF_SQ);
     float* Wf = reinterpret_cast<float*>(smem + OFF_SW);
     float* Uf = reinterpret_cast<float*>(smem + OFF_SU);
-    float vr[kU];
+    // every load is issued before any shared-memory store (the stores could
+    // otherwise alias the loads for the compiler and serialise them)
+    float kr[kU], qr[kU], vr[kU], ga = 1.f, gb = 0.f;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + (u < nv ? u : 0)) * a.n_heads + head;
+        kr[u] = load_tok(a.k, a.in_bf16, row, t);
+        qr[u] = load_tok(a.q, a.in_bf16, row, t);
+        vr[u] = load_tok(a.v, a.in_bf16, row, t);
+    }
+    if (t < kU && t < nv) {
+        const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + t) * a.n_heads + head;
+        ga = __ldg(a.alpha + row);
+        gb = __ldg(a.beta + row);
+    }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
         const bool valid = u < nv;
-        const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head;
-        Kf[u * kD + t] = valid ? load_tok(a.k, a.in_bf16, row, t) : 0.f;
-        Qf[u * kD + t] = valid ? load_tok(a.q, a.in_bf16, row, t) : 0.f;
-        vr[u] = valid ? load_tok(a.v, a.in_bf16, row, t) : 0.f;
+        Kf[u * kUR + t] = valid ? kr[u] : 0.f;
+        Qf[u * kUR + t] = valid ? qr[u] : 0.f;
+        vr[u] = valid ? vr[u] : 0.f;
     }
     if (t < kU) {
-        const bool valid = t < nv;
-        const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + t) * a.n_heads + head;
-        ms->lg[t] = valid ? log2f(fmaxf(a.alpha[row], FLT_MIN)) : 0.f;
-        ms->beta[t] = valid ? a.beta[row] : 0.f;
+        ms->lg[t] = log2f(fmaxf(ga, FLT_MIN));
+        ms->beta[t] = gb;
     }
     named_sync(3);
     {  // k_r . k_c (threads 0..63), q_r . k_c (threads 64..127)
         const int r = (t >> 3) & 7, c = t & 7;
-        const float* x = (t < 64 ? Kf : Qf) + r * kD;
-        const float* y = Kf + c * kD;
+        const float* x = (t < 64 ? Kf : Qf) + r * kUR;
+        const float* y = Kf + c * kUR;
         float d0 = 0.f, d1 = 0.f;
 #pragma unroll 4
         for (int i = 0; i < kD; i += 8) {
@@ -252,6 +264,17 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
         }
     }
     named_sync(3);
+    {  // A[r][s] = b_r (g_r/g_s) k_r.k_s (s < r) in place of k.k; M[r][s] = (g_r/g_s) q_r.k_s (s <= r)
+        const int r = (t >> 3) & 7, c = t & 7;
+        const float ratio = exp2f(ms->lg[r] - ms->lg[c]);
+        if (t < 64) ms->kk[r][c] = c < r ? ms->beta[r] * ratio * ms->kk[r][c] : 0.f;
+        else ms->M[r][c] = c <= r ? ms->qk[r][c] * ratio : 0.f;
+        if (t < kU) {
+            ms->g[t] = exp2f(ms->lg[t]);
+            ms->sc[t] = exp2f(ms->lg[kU - 1] - ms->lg[t]);
+        }
+    }
+    named_sync(3);
     if (t < kU) {  // column c of (I + A)^-1 by forward substitution, then That = (.) Diag(b)
         const int c = t;
         float m[kU];
@@ -259,17 +282,15 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
         for (int r = 0; r < kU; ++r) {
             float acc = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < r; ++s2)
-                acc -= ms->beta[r] * exp2f(ms->lg[r] - ms->lg[s2]) * ms->kk[r][s2] * m[s2];
+            for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-ms->kk[r][s2], m[s2], acc);
             m[r] = acc;
         }
+        const float bc = ms->beta[c], gc = ms->g[c];
 #pragma unroll
-        for (int r = 0; r < kU; ++r) ms->th[r][c] = m[r] * ms->beta[c];
-        ms->g[t] = exp2f(ms->lg[t]);
-        ms->sc[t] = exp2f(ms->lg[kU - 1] - ms->lg[t]);
-    } else if (t >= 64) {
-        const int r = (t - 64) >> 3, c = t & 7;
-        ms->M[r][c] = c <= r ? ms->qk[r][c] * exp2f(ms->lg[r] - ms->lg[c]) : 0.f;
+        for (int r = 0; r < kU; ++r) {
+            ms->th[r][c] = m[r] * bc;
+            ms->thg[r][c] = m[r] * bc * gc;
+        }
     }
     named_sync(3);
 #pragma unroll
@@ -277,12 +298,12 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
         float w = 0.f, uu = 0.f;
 #pragma unroll
         for (int s2 = 0; s2 <= u; ++s2) {
-            w = fmaf(ms->th[u][s2] * ms->g[s2], Kf[s2 * kD + t], w);
+            w = fmaf(ms->thg[u][s2], Kf[s2 * kUR + t], w);
             uu = fmaf(ms->th[u][s2], vr[s2], uu);
         }
-        Wf[u * kD + t] = w;
-        Uf[u * kD + t] = uu;
-        Qf[u * kD + t] *= ms->g[u];
+        Wf[u * kUR + t] = w;
+        Uf[u * kUR + t] = uu;
+        Qf[u * kUR + t] *= ms->g[u];
     }
     if (t == 0) {
         ms->tok0 = tok0;
@@ -323,19 +344,19 @@ __device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint3
 #pragma unroll
         for (int u = 0; u < kU; ++u) wt[u] = qs[u] = 0.f;
 #pragma unroll 1
-        for (int cb = 0; cb < 8; ++cb) {  // pass 1: W_u . x and g_u q_u . x
-            uint32_t x[16];
-            tmem_ld16(tl + TM_D + 16 * cb, x);
+        for (int cb = 0; cb < 4; ++cb) {  // pass 1: W_u . x and g_u q_u . x
+            uint32_t x[32];
+            tmem_ld32(tl + TM_D + 32 * cb, x);
             tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {
-                const int i = 16 * cb + jj;
+            for (int jj = 0; jj < 32; jj += 4) {
+                const int i = 32 * cb + jj;
                 const float x0 = __uint_as_float(x[jj]), x1 = __uint_as_float(x[jj + 1]);
                 const float x2 = __uint_as_float(x[jj + 2]), x3 = __uint_as_float(x[jj + 3]);
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
-                    const float4 w4 = *reinterpret_cast<const float4*>(Wf + u * kD + i);
-                    const float4 q4 = *reinterpret_cast<const float4*>(Qf + u * kD + i);
+                    const float4 w4 = *reinterpret_cast<const float4*>(Wf + u * kUR + i);
+                    const float4 q4 = *reinterpret_cast<const float4*>(Qf + u * kUR + i);
                     wt[u] = fmaf(w4.x, x0, fmaf(w4.y, x1, fmaf(w4.z, x2, fmaf(w4.w, x3, wt[u]))));
                     qs[u] = fmaf(q4.x, x0, fmaf(q4.y, x1, fmaf(q4.z, x2, fmaf(q4.w, x3, qs[u]))));
                 }
@@ -344,7 +365,7 @@ __device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint3
         float up[kU], c[kU];
         const int nv = ms->nv, tok0 = ms->tok0;
 #pragma unroll
-        for (int u = 0; u < kU; ++u) up[u] = Uf[u * kD + n] - wt[u];
+        for (int u = 0; u < kU; ++u) up[u] = Uf[u * kUR + n] - wt[u];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             float o = qs[u];
@@ -367,7 +388,7 @@ __device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint3
                               gw * __uint_as_float(x[jj + 2]), gw * __uint_as_float(x[jj + 3])};
 #pragma unroll
                 for (int s2 = 0; s2 < kU; ++s2) {
-                    const float4 k4 = *reinterpret_cast<const float4*>(Kf + s2 * kD + i);
+                    const float4 k4 = *reinterpret_cast<const float4*>(Kf + s2 * kUR + i);
                     y[0] = fmaf(k4.x, c[s2], y[0]);
                     y[1] = fmaf(k4.y, c[s2], y[1]);
                     y[2] = fmaf(k4.z, c[s2], y[2]);
@@ -540,26 +561,32 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
         tc_fence_after();
         const bool last = j + 1 == len;
         const bool seam = !last && step_units(a, c0 + j + 1, tb) > 0;
+        // 2^e as two factors (each exact for |e| <= 252): T~ S 2^e underflows
+        // only where it is negligible against S_p
+        const float f1 = exp2f((float)(e / 2)), f2 = exp2f((float)(e - e / 2));
 #pragma unroll 1
-        for (int cb = 0; cb < 8; ++cb) {
-            uint32_t x[16];
-            tmem_ld16(tl + TM_D + 16 * cb, x);
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t x[32];
+            tmem_ld32(tl + TM_D + 32 * cb, x);
             tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int i = 16 * cb + jj;
-                const float v = ldexpf(__uint_as_float(x[jj]), e) + sp[i * 32];
+            for (int jj = 0; jj < 32; ++jj) {
+                const int i = 32 * cb + jj;
+                const float v = fmaf(__uint_as_float(x[jj]) * f1, f2, sp[i * 32]);
                 if (last) out[i * kD + n] = v;
                 x[jj] = __float_as_uint(v);
             }
             if (seam) {
-                tmem_st16(tl + TM_D + 16 * cb, x);
+                tmem_st32(tl + TM_D + 32 * cb, x);
             } else if (!last) {
-                uint32_t h[16], l[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[jj]), h[jj], l[jj]);
-                tmem_st16(tl + TM_AB + 16 * cb, h);
-                tmem_st16(tl + TM_AS + 16 * cb, l);
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t h[16], l[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]), h[jj], l[jj]);
+                    tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
+                    tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
+                }
             }
         }
         tmem_wait_st();

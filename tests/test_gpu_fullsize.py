@@ -2,7 +2,8 @@
 
 * The long cold request (30 GDN layers x 32 heads, d=128, bf16, 100,000
   tokens, 8-token seams): one build call over every body, then the reuse
-  chain of seam advances and one-step composes.  Sampled (layer, head)
+  chain as one hypic_reuse_chain call (the fused kernel) and, as a cross
+  check, as separate seam-advance and one-step compose calls.  Sampled (layer, head)
   objects are checked against the fp64 sequential recurrence over the whole
   request (end state and every seam output) and against the oracle's pairs
   for sampled segments.
@@ -35,21 +36,28 @@ def test_long_request_full_size_sampled(B):
     T, T_exp, S = B.segment_build("gdn", r["k"], r["v"], cu, alpha=r["alpha"], beta=r["beta"], seam_skip=skip)
     st = torch.as_tensor(seam_tok, device="cuda")
     ks, vs, a_s, b_s = (x[:, st].contiguous() for x in (r["k"], r["v"], r["alpha"], r["beta"]))
-    state = B.compose("gdn", S, [0, 1], [0], T_tab=T, T_exp_tab=T_exp)
-    nxt = torch.empty_like(state)
+    # the product path: one reuse chain (compose segment 0, then seam i + compose i)
+    cu_step = np.concatenate([[0, 0], np.cumsum(skip[1:])]).astype(np.int32)
+    state, o_all = B.reuse_chain("gdn", S, [0, n_seg], np.arange(n_seg, dtype=np.int32), cu_step, r["q_seam"], ks, vs,
+                                 T_tab=T, T_exp_tab=T_exp, alpha=a_s, beta=b_s)
+    # the same chain as separate seam-advance and compose calls
+    st1 = B.compose("gdn", S, [0, 1], [0], T_tab=T, T_exp_tab=T_exp)
+    nxt = torch.empty_like(st1)
     outs, pos = [], 0
     for i in range(1, n_seg):
         w = int(skip[i])
         sl = slice(pos, pos + w)
         _, o = B.seam_advance("gdn", r["q_seam"][:, sl].contiguous(), ks[:, sl].contiguous(), vs[:, sl].contiguous(),
                               [0, w], alpha=a_s[:, sl].contiguous(), beta=b_s[:, sl].contiguous(),
-                              state_in=state, state_out=state)
+                              state_in=st1, state_out=st1)
         outs.append(o)
-        B.compose("gdn", S, [0, 1], [i], T_tab=T, T_exp_tab=T_exp, S0=state, out=nxt)
-        state, nxt = nxt, state
+        B.compose("gdn", S, [0, 1], [i], T_tab=T, T_exp_tab=T_exp, S0=st1, out=nxt)
+        st1, nxt = nxt, st1
         pos += w
     B.check_device()
-    o_all = torch.cat(outs, dim=1)
+    o_steps = torch.cat(outs, dim=1)
+    assert_rel(host(state), host(st1), TOL_F32, what="fused chain vs step-by-step calls: end states")
+    assert_rel(host(o_all), host(o_steps), TOL_F32, axes=(-1,), what="fused chain vs step-by-step calls: outputs")
     samples = [(0, 0), (29, 31), (13, 7), (29, 2)]
     # The sampled (layer, head) pairs become the heads of one 1-layer problem,
     # so the oracle runs them in parallel.
