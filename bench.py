@@ -351,6 +351,49 @@ def time_compose_table(steps, device, n_layers=30):
                     "which then come from L2: algorithmic GB/s can exceed the DRAM traffic"}
 
 
+def time_reuse_chain(steps, warmup, device, n_layers=30, H=32, d=128, n_steps=77, w=8):
+    """hypic_reuse_chain over one request's chain (the long request's shape:
+    n_steps cached pairs, a w-token seam before every step but the first) for
+    n_layers x H heads; random pair tables (T with spectral norm ~0.7)."""
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    T = torch.randn((n_steps, n_layers, H, d, d), generator=g, device=device) * (0.35 / d ** 0.5)
+    S = torch.randn((n_steps, n_layers, H, d, d), generator=g, device=device) / d ** 0.5
+    Te = torch.zeros((n_steps, n_layers, H), dtype=torch.int32, device=device)
+    N = (n_steps - 1) * w
+    q = torch.randn((n_layers, N, H, d), generator=g, device=device)
+    k = torch.randn((n_layers, N, H, d), generator=g, device=device)
+    q = (q / q.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn((n_layers, N, H, d), generator=g, device=device).to(torch.bfloat16)
+    al = torch.rand((n_layers, N, H), generator=g, device=device) * 0.15 + 0.85
+    be = torch.rand((n_layers, N, H), generator=g, device=device)
+    cu_step = np.concatenate([[0, 0], np.cumsum([w] * (n_steps - 1))]).astype(np.int32)
+    out = torch.empty((1, n_layers, H, d, d), device=device)
+    o = torch.empty((n_layers, N, H, d), device=device)
+    a, keep = B.chain_args("gdn", S, np.array([0, n_steps], np.int32), np.arange(n_steps, dtype=np.int32), cu_step,
+                           q, k, v, T_tab=T, T_exp_tab=Te, alpha=al, beta=be, S_out=out, o_out=o)
+    sp = torch.cuda.current_stream().cuda_stream
+    for _ in range(warmup):
+        B._check(B.hypic_reuse_chain(a, None, 0, sp))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        B._check(B.hypic_reuse_chain(a, None, 0, sp))
+    e1.record()
+    torch.cuda.synchronize()
+    B.check_device()
+    del keep
+    ms = e0.elapsed_time(e1) / steps
+    LH = n_layers * H
+    algo = n_steps * LH * COMPOSE_BYTES + N * LH * SEAM_TOKEN_BYTES + LH * d * d * 4
+    return {"workload": f"reuse chain: {n_layers} layers x {H} heads, d={d}, {n_steps} steps, {w}-token seams",
+            "ms_per_call": ms, "algorithmic_bytes": algo, "gbs_algorithmic": algo / (ms / 1e3) / 1e9}
+
+
 def run_case(args, device):
     """Single-kernel cases used for profiling (one JSON line each):
     ragged_build -- the build of 32 ragged segments (U[512,2048] tokens) x 32
@@ -363,6 +406,11 @@ def run_case(args, device):
     peaks, peak_src = load_peaks()
     if args.case == "compose_table":
         r = time_compose_table(args.steps, device, n_layers=args.layers)
+        r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
+        print(json.dumps({"case": args.case, **r}))
+        return
+    if args.case == "reuse_chain":
+        r = time_reuse_chain(args.steps, args.warmup, device, n_layers=args.layers)
         r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
         print(json.dumps({"case": args.case, **r}))
         return
@@ -413,9 +461,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-compose-table", action="store_true")
-    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table"], default="long_request",
+    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table", "reuse_chain"],
+                    default="long_request",
                     help="long_request is the benchmark; the others time one kernel (for profiling)")
-    ap.add_argument("--layers", type=int, default=30, help="layers of the compose_table case")
+    ap.add_argument("--layers", type=int, default=30, help="layers of the compose_table and reuse_chain cases")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
