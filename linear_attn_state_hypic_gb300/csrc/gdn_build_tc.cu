@@ -89,7 +89,7 @@ struct Misc {
     uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done
     uint64_t u_done, w_done;      // U^T, W^T committed
     uint64_t u_cvt, w_cvt;        // U~ and W operands written
-    uint64_t x_done, y_ready, d_ready, drain;
+    uint64_t x_done, xt_free, y_ready, d_ready, drain;  // xt_free: the pass has read X''_T
     alignas(16) float lg2[kGateSlots][kC];  // slot gc % kGateSlots; every table is read as float4
     alignas(16) float beta[kGateSlots][kC];
     alignas(16) float up[kGateSlots][kC];
@@ -645,8 +645,8 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CU
 
 // Warp 1, lane 0: issues every MMA of the item as soon as its inputs are
 // ready, in this priority: W^T, GEMM2, GEMM1, U^T, gram.  W^T of the next
-// chunk and GEMM2 of this one wait for the same pass; W^T goes first so that
-// its conversion runs while GEMM2 executes.  A readiness test
+// chunk reuses the X''_T columns and waits only for the T half of this
+// chunk's pass, so it runs while the pass does the S half.  A readiness test
 // of a barrier's phase k is only made once its phase k - 1 is known to be
 // complete (by an earlier test or an earlier item), so a parity test cannot
 // mistake an old phase for a new one.
@@ -661,7 +661,7 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
         bool any = false;
         if (iw < iu && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_T columns
             const uint32_t gc = g + iw;
-            if (iw == 0 || mbar_test(&ms->y_ready, (gc - 1) & 1)) {  // X of the previous chunk has been read
+            if (iw == 0 || mbar_test(&ms->xt_free, (gc - 1) & 1)) {  // the pass has read the previous X''_T
                 tc_fence_after();
                 const uint32_t kt = ktile(gc);
 #pragma unroll
@@ -878,6 +878,9 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         if (!wg_all(2, wait_bar(&ms->x_done, gc & 1, ms, a))) return;
         tc_fence_after();
         const float mloc = state_pass<0>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
+        tc_fence_before();
+        named_sync(2);  // every lane has read X''_T: the next W'^T may overwrite those columns
+        if (n == 0) mbar_arrive(&ms->xt_free);
         state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
         fence_async_smem();
         tc_fence_before();
@@ -921,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kGateSlots; ++s) mbar_init(&ms->gready[s], 1);
         uint64_t* one[] = {&ms->fullV, &ms->emptyV, &ms->g_done, &ms->g_read, &ms->that_ready, &ms->bt_free,
-                           &ms->u_done, &ms->w_done, &ms->u_cvt, &ms->w_cvt, &ms->x_done, &ms->y_ready,
+                           &ms->u_done, &ms->w_done, &ms->u_cvt, &ms->w_cvt, &ms->x_done, &ms->xt_free, &ms->y_ready,
                            &ms->d_ready, &ms->drain};
         for (uint64_t* b : one) mbar_init(b, 1);
         ms->abort_flag = 0;
