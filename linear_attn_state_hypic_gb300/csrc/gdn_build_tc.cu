@@ -25,9 +25,9 @@
 // (times the renormalisation factor): the in-chunk decay is centred on the
 // middle of its range so that neither factor leaves the float32 range for
 // chunk decays down to 2^-252.
-// Two operands are carried as a pair of bf16 values (x = hi + lo, lo the
-// rounding residual of hi): That Diag(up) in the W product and Y''_T in the
-// T half of GEMM2.  Rounding either to a single bf16 alone costs T_C about
+// Two operands are carried as a pair of bf16 values (x = hi + lo, hi the
+// truncation of x and lo the rest): That Diag(up) in the W product and Y''_T
+// in the T half of GEMM2.  Rounding either to a single bf16 alone costs T_C about
 // 7e-3 relative error over 2048-token segments with strong decay; the pair
 // brings it to ~2e-3.  Keys and values are bf16 inputs and need no split.
 // T_C falls far below the fp32 range over long segments: it is returned as a
@@ -66,8 +66,9 @@ constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
 constexpr int kKStages = 3;       // K ring depth (the gram of a chunk wants its keys early)
 constexpr int kGateSlots = 4;     // per-chunk gate tables in flight
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6;
+constexpr int kPrepThreads = 256;  // warps 6-13: two warps per tensor-memory lane quarter
 
 // Shared memory map (byte offsets; every operand region is 1024-byte aligned).
 constexpr uint32_t kTile = 16384;                       // 64 tokens x 128 bf16, two 64-column TMA boxes
@@ -139,21 +140,31 @@ struct TcArgs {
 // completes (re-polling at least every few microseconds); it gives up, and
 // raises the CTA's abort flag and the device error word, once `wait_ns` of
 // GPU time have passed, or at once when another role already gave up.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
-    if (mbar_try_wait(bar, parity)) return true;
+// (The slow path is a call: one copy of it instead of one per wait keeps the
+// kernel's code, which every role's warps share in the instruction cache,
+// small.)
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, int* abort_flag, uint64_t wait_ns,
+                                           unsigned* err) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
+#pragma unroll 1
         for (int j = 0; j < 16; ++j)
             if (mbar_try_wait_sleep(bar, parity, 4000u)) return true;
-        if (*(volatile int*)&ms->abort_flag) return false;
-        if (globaltimer_ns() - t0 > a.wait_ns) break;
+        if (*(volatile int*)abort_flag) return false;
+        if (globaltimer_ns() - t0 > wait_ns) break;
     }
-    *(volatile int*)&ms->abort_flag = 1;
-    set_error(a.err, kErrTimeout);
+    *(volatile int*)abort_flag = 1;
+    set_error(err, kErrTimeout);
     return false;
 }
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
+}
 
-__device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ void named_sync(int id, int n = 128) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -165,6 +176,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+// Two values as bf16 pairs x = hi + lo: hi is x with its low 16 bits cleared
+// (exact; two values packed by one byte permute) and lo = x - hi (exact in
+// fp32) rounded to bf16, so hi + lo keeps about 16 significant bits of x.
+__device__ __forceinline__ void split2_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const uint32_t hx = __float_as_uint(x) & 0xffff0000u, hy = __float_as_uint(y) & 0xffff0000u;
+    hi = __byte_perm(hx, hy, 0x7632);
+    lo = pack_bf16(x - __uint_as_float(hx), y - __uint_as_float(hy));
+}
 __device__ __forceinline__ float tf32_rna(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -220,32 +239,32 @@ __device__ void gate_tables(Misc* ms, int slot, const float (&ra)[2], const floa
 // Rows of A from the gram matrix in tensor memory (M=64 accumulator layout:
 // row 16q + l sits in lane 32q + l, l < 16):
 // A[r][j] = b_r 2^(lg2_r - lg2_j) G[r][j] for j < r, 0 elsewhere.
-// Lane l < 16 writes columns 0..31 of its row; lane l + 16, which holds no
-// row, takes columns 32..63 of the same row from lane l by a shuffle.
-__device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, int q, int lane) {
-    uint32_t g0[32], g1[32];
-    const uint32_t tl = tmem + ((32u * q) << 16) + TM_G;
-    tmem_ld32(tl, g0);
-    tmem_ld32(tl + 32, g1);
+// Half h of the prep warps reads columns 32h..32h+31; lane l < 16 writes the
+// first 16 of them in its row, lane l + 16, which holds no row, takes the
+// other 16 of the same row from lane l by a shuffle.
+__device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, int q, int h, int lane) {
+    uint32_t g0[32];
+    tmem_ld32(tmem + ((32u * q) << 16) + TM_G + 32 * h, g0);
     tmem_wait_ld();
     const bool upper = lane >= 16;
+    uint32_t gv[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const uint32_t x = __shfl_xor_sync(0xffffffffu, g1[j], 16);
-        if (upper) g0[j] = x;
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t x = __shfl_xor_sync(0xffffffffu, g0[16 + j], 16);
+        gv[j] = upper ? x : g0[j];
     }
-    const int r = 16 * q + (lane & 15), cb = upper ? 32 : 0;
+    const int r = 16 * q + (lane & 15), cb = 32 * h + (upper ? 16 : 0);
     const float coef = ms->beta[slot][r] * ms->up[slot][r];
     const float* wn = ms->wn[slot] + cb;
     float* row = As + r * kAS + cb;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
+    for (int j = 0; j < 16; j += 4) {
         const float4 w = *reinterpret_cast<const float4*>(wn + j);
         float4 v;
-        v.x = (cb + j < r) ? coef * w.x * __uint_as_float(g0[j]) : 0.f;
-        v.y = (cb + j + 1 < r) ? coef * w.y * __uint_as_float(g0[j + 1]) : 0.f;
-        v.z = (cb + j + 2 < r) ? coef * w.z * __uint_as_float(g0[j + 2]) : 0.f;
-        v.w = (cb + j + 3 < r) ? coef * w.w * __uint_as_float(g0[j + 3]) : 0.f;
+        v.x = (cb + j < r) ? coef * w.x * __uint_as_float(gv[j]) : 0.f;
+        v.y = (cb + j + 1 < r) ? coef * w.y * __uint_as_float(gv[j + 1]) : 0.f;
+        v.z = (cb + j + 2 < r) ? coef * w.z * __uint_as_float(gv[j + 2]) : 0.f;
+        v.w = (cb + j + 3 < r) ? coef * w.w * __uint_as_float(gv[j + 3]) : 0.f;
         *reinterpret_cast<float4*>(row + j) = v;
     }
 }
@@ -322,10 +341,10 @@ __device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, in
 //   [[L11, 0], [L21, L22]]^-1 = [[M11, 0], [-M22 L21 M11, M22]]:
 //   level 1: the four 16 x 16 diagonal blocks, forward substitution by
 //            columns (threads 0..63, one column each);
-//   level 2: blocks (1,0) and (3,2), from the level-1 inverses (warp w:
-//            block pair w / 2, 8-column tile w % 2);
+//   level 2: blocks (1,0) and (3,2), from the level-1 inverses (warps
+//            w < 4: block pair w / 2, 8-column tile w % 2);
 //   level 3: the lower-left 32 x 32 block, from the two 32 x 32 inverses
-//            (warp w: its 16 x 16 quarter w).
+//            (warp w: 16 x 8 tile w of it).
 // The products run over full blocks: the zero upper parts of the triangular
 // factors make that exact.  Ptmp holds the left products.
 __device__ void prep_solve(float* As, float* Ptmp, int p) {
@@ -346,40 +365,44 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) Mb[i * kAS] = s[i];
     }
-    named_sync(1);
+    named_sync(1, kPrepThreads);
     {  // level 2: P = A_{x+1,x} M_xx, then M_{x+1,x} = -M_{x+1,x+1} P, x = 0, 2
-        const int x = 2 * (w >> 1), nt = w & 1;
+        const int x = 2 * ((w >> 1) & 1), nt = w & 1;
+        float* P = Ptmp + ((w >> 1) & 1) * 320;  // 16 x 16, row stride 20
         float c[1][4];
-        warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * x, kAS, As + 16 * x * kAS + 16 * x + 8 * nt, kAS, lane);
-        float* P = Ptmp + (w >> 1) * 320;  // 16 x 16, row stride 20
-        warp_store<1>(c, P + 8 * nt, 20, 1.f, lane);
-        named_sync(1);
-        warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * (x + 1), kAS, P + 8 * nt, 20, lane);
-        warp_store<1>(c, As + 16 * (x + 1) * kAS + 16 * x + 8 * nt, kAS, -1.f, lane);
+        if (w < 4) {
+            warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * x, kAS, As + 16 * x * kAS + 16 * x + 8 * nt, kAS, lane);
+            warp_store<1>(c, P + 8 * nt, 20, 1.f, lane);
+        }
+        named_sync(1, kPrepThreads);
+        if (w < 4) {
+            warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * (x + 1), kAS, P + 8 * nt, 20, lane);
+            warp_store<1>(c, As + 16 * (x + 1) * kAS + 16 * x + 8 * nt, kAS, -1.f, lane);
+        }
     }
-    named_sync(1);
+    named_sync(1, kPrepThreads);
     {  // level 3: P = A[32:64, 0:32] M[0:32, 0:32], then M[32:64, 0:32] = -M[32:64, 32:64] P
-        const int r0 = 16 * (w >> 1), c0 = 16 * (w & 1);
-        float c[2][4];
-        warp_gemm<2, 2>(c, As + (32 + r0) * kAS, kAS, As + c0, kAS, lane);
-        warp_store<2>(c, Ptmp + r0 * 36 + c0, 36, 1.f, lane);  // 32 x 32, row stride 36
-        named_sync(1);
-        warp_gemm<2, 2>(c, As + (32 + r0) * kAS + 32, kAS, Ptmp + c0, 36, lane);
-        warp_store<2>(c, As + (32 + r0) * kAS + c0, kAS, -1.f, lane);
+        const int r0 = 16 * (w >> 2), c0 = 8 * (w & 3);
+        float c[1][4];
+        warp_gemm<2, 1>(c, As + (32 + r0) * kAS, kAS, As + c0, kAS, lane);
+        warp_store<1>(c, Ptmp + r0 * 36 + c0, 36, 1.f, lane);  // 32 x 32, row stride 36
+        named_sync(1, kPrepThreads);
+        warp_gemm<2, 1>(c, As + (32 + r0) * kAS + 32, kAS, Ptmp + c0, 36, lane);
+        warp_store<1>(c, As + (32 + r0) * kAS + c0, kAS, -1.f, lane);
     }
-    named_sync(1);
+    named_sync(1, kPrepThreads);
 }
 
 // That Diag(up) (bf16 hi at bt, residual lo at bt + 16384; up = g / g_C^(1/2))
 // and That = (I+A)^-1 Diag(b) (bf16 at bt + 8192) as K-major 64 x 64 operands
-// (128-byte rows, 128-byte swizzle).  Thread p writes half a row.
+// (128-byte rows, 128-byte swizzle).  Thread p writes a quarter of a row.
 __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, int par, int p) {
-    const int t = p >> 1, half = p & 1;
-    const float* row = As + t * kAS + 32 * half;
-    const float* beta = ms->beta[par] + 32 * half;
-    const float* gam = ms->up[par] + 32 * half;  // That Diag(g / g_C^(1/2))
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    const int t = p >> 2, qr = p & 3;
+    const float* row = As + t * kAS + 16 * qr;
+    const float* beta = ms->beta[par] + 16 * qr;
+    const float* gam = ms->up[par] + 16 * qr;  // That Diag(g / g_C^(1/2))
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
         const float4 x0 = *reinterpret_cast<const float4*>(row + 8 * ch);
         const float4 x1 = *reinterpret_cast<const float4*>(row + 8 * ch + 4);
         const float4 b0 = *reinterpret_cast<const float4*>(beta + 8 * ch);
@@ -394,11 +417,10 @@ __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, in
         for (int jj = 0; jj < 4; ++jj) {
             const float m0 = mv[2 * jj], m1 = mv[2 * jj + 1];
             const float z0 = m0 * gv[2 * jj], z1 = m1 * gv[2 * jj + 1];
-            w1[jj] = pack_bf16(z0, z1);
-            w3[jj] = pack_bf16(z0 - bf16_round(z0), z1 - bf16_round(z1));
+            split2_bf16(z0, z1, w1[jj], w3[jj]);
             w2[jj] = pack_bf16(m0, m1);
         }
-        const uint32_t off = t * 128u + ((uint32_t)((4 * half + ch) ^ (t & 7)) << 4);
+        const uint32_t off = t * 128u + ((uint32_t)((2 * qr + ch) ^ (t & 7)) << 4);
         st_shared_v4(bt + off, w1[0], w1[1], w1[2], w1[3]);
         st_shared_v4(bt + 8192u + off, w2[0], w2[1], w2[2], w2[3]);
         st_shared_v4(bt + 16384u + off, w3[0], w3[1], w3[2], w3[3]);
@@ -410,18 +432,16 @@ __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, in
 __device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
     const int i = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    uint32_t w2[2][32];
     uint8_t* bw = smem + OFF_BW + (i >> 5) * 8192;
-    tmem_ld32(tl + TM_XT, w2[0]);
-    tmem_ld32(tl + TM_XT + 32, w2[1]);
-    tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
     for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+        tmem_ld32(tl + TM_XT + 32 * half, w);
+        tmem_wait_ld();
+        uint8_t* b = bw + 32 * half * 128;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int t = 32 * half + j;
-            *reinterpret_cast<float*>(bw + sw128_offset(t, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w2[half][j]));
-        }
+        for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<float*>(b + sw128_offset(j, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w[j]));
     }
 }
 
@@ -431,13 +451,11 @@ __device__ void convert_u(const Misc* ms, uint32_t au, uint32_t tmem, int q, int
     const int i = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
     const float* uf = ms->uf;
-    uint32_t w2[2][32];
-    tmem_ld32(tl + TM_U, w2[0]);
-    tmem_ld32(tl + TM_U + 32, w2[1]);
-    tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-        const uint32_t* w = w2[half];
+        uint32_t w[32];
+        tmem_ld32(tl + TM_U + 32 * half, w);
+        tmem_wait_ld();
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             uint32_t pk[4];
@@ -475,6 +493,28 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
     tmem_wait_st();
 }
 
+// D''_h <- sc D''_h in tensor memory (this thread's row), returning the max
+// |.| of the new row when want_max: the rescale of a renormalisation chunk.
+// (Rare: out of line, so that it stays out of the pass's instruction stream.)
+__device__ __noinline__ float state_rescale(uint32_t addr, float sc, bool want_max) {
+    float mloc = 0.f;
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32];
+        tmem_ld32(addr + 32 * cb, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float v = __uint_as_float(x[j]) * sc;
+            if (want_max) mloc = fmaxf(mloc, fabsf(v));
+            x[j] = __float_as_uint(v);
+        }
+        tmem_st32(addr + 32 * cb, x);
+    }
+    tmem_wait_st();
+    return mloc;
+}
+
 // After GEMM1 of a chunk, half h (0 = T, 1 = S): Y''_h = Diag-scaled X''_h
 // rows into shared memory
 // (bf16, K-major [128 n][64 t]; Y''_T also as its bf16 residual):
@@ -487,54 +527,31 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, floa
                             int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    float mloc = 0.f;
-    uint32_t x[2][32];
-    {
-        const float* f = h ? ms->fS : ms->fT;
-        tmem_ld32(tl + (h ? TM_XS : TM_XT), x[0]);
-        tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32, x[1]);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        const float* f = (h ? ms->fS : ms->fT) + 32 * half;
+        uint32_t x[32];
+        tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32 * half, x);
         tmem_wait_ld();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int jj = 0; jj < 4; ++jj) {
+            uint32_t pk[4], lo[4];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                uint32_t pk[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int t = 32 * half + 8 * jj + 2 * k;
-                    const float y0 = f[t] * __uint_as_float(x[half][8 * jj + 2 * k]);
-                    const float y1 = f[t + 1] * __uint_as_float(x[half][8 * jj + 2 * k + 1]);
+            for (int k = 0; k < 4; ++k) {
+                const int t = 8 * jj + 2 * k;
+                const float y0 = f[t] * __uint_as_float(x[t]);
+                const float y1 = f[t + 1] * __uint_as_float(x[t + 1]);
+                if (h)
                     pk[k] = pack_bf16(y0, y1);
-                    if (!h) lo[k] = pack_bf16(y0 - bf16_round(y0), y1 - bf16_round(y1));
-                }
-                const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((4 * half + jj) ^ (n & 7)) << 4);
-                st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
-                if (!h) st_shared_v4(ay + 32768u + off, lo[0], lo[1], lo[2], lo[3]);
+                else
+                    split2_bf16(y0, y1, pk[k], lo[k]);
             }
-        }
-        if (rn) {
-            const float sc = h ? dS : dT;
-#pragma unroll
-            for (int cb = 0; cb < 4; cb += 2) {
-                const uint32_t addr = tl + (h ? TM_DS : TM_DT) + 32 * cb;
-                tmem_ld32(addr, x[0]);
-                tmem_ld32(addr + 32, x[1]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int b = 0; b < 2; ++b)
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float v = __uint_as_float(x[b][j]) * sc;
-                        if (!h) mloc = fmaxf(mloc, fabsf(v));
-                        x[b][j] = __float_as_uint(v);
-                    }
-                tmem_st32(addr, x[0]);
-                tmem_st32(addr + 32, x[1]);
-            }
+            const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((4 * half + jj) ^ (n & 7)) << 4);
+            st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
+            if (!h) st_shared_v4(ay + 32768u + off, lo[0], lo[1], lo[2], lo[3]);
         }
     }
-    if (rn) tmem_wait_st();
-    return mloc;
+    return rn ? state_rescale(tl + (h ? TM_DS : TM_DT), h ? dS : dT, !h) : 0.f;
 }
 
 // Warp max, then the 4 warps of the state warpgroup through shared memory.
@@ -592,14 +609,14 @@ __device__ void state_identity(const TcArgs& a, int64_t obj, int n) {
     if (n == 0) a.T_exp[obj] = 0;
 }
 
-// All 128 threads of named barrier `id` agree: true only if every one passed true.
-__device__ __forceinline__ bool wg_all(int id, bool v) {
+// All n threads of named barrier `id` agree: true only if every one passed true.
+__device__ __forceinline__ bool wg_all(int id, bool v, int n = 128) {
     uint32_t r;
     asm volatile(
         "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-        " bar.red.and.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
-        : "r"((uint32_t)v), "r"(id)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
         : "memory");
     return r != 0;
 }
@@ -663,12 +680,12 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
             const uint32_t gc = g + iw;
             if (iw == 0 || mbar_test(&ms->xt_free, (gc - 1) & 1)) {  // the pass has read the previous X''_T
                 tc_fence_after();
-                const uint32_t kt = ktile(gc);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t ak = sdesc_sw128(kt + k * 2048, 8192, 1024);
-                    mma_bf16_ss(tmem + TM_XT, ak, sdesc_sw128(bt + k * 32, 0, 1024), ID_WU, k > 0);
-                    mma_bf16_ss(tmem + TM_XT, ak, sdesc_sw128(bt + 16384 + k * 32, 0, 1024), ID_WU, true);
+                const uint64_t a0 = sdesc_sw128(ktile(gc), 8192, 1024), bh = sdesc_sw128(bt, 0, 1024),
+                               bl = sdesc_sw128(bt + 16384, 0, 1024);
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {  // (a descriptor's address field counts 16-byte units)
+                    mma_bf16_ss(tmem + TM_XT, a0 + 128 * k, bh + 2 * k, ID_WU, k > 0);
+                    mma_bf16_ss(tmem + TM_XT, a0 + 128 * k, bl + 2 * k, ID_WU, true);
                 }
                 mma_commit(&ms->w_done);
                 mma_commit(&ms->bt_free);  // (the U^T MMAs of this chunk were issued before)
@@ -680,14 +697,16 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
             const uint32_t gc = g + i2;
             if (mbar_test(&ms->y_ready, gc & 1) && mbar_test(&ms->u_cvt, gc & 1)) {
                 tc_fence_after();
-                const uint32_t kt = ktile(gc);
-#pragma unroll
+                const uint64_t b0 = sdesc_sw128(ktile(gc), 8192, 1024), yh = sdesc_sw128(ay, 0, 1024),
+                               yl = sdesc_sw128(ay + 32768, 0, 1024), ys = sdesc_sw128(ay + 16384, 0, 1024),
+                               uu = sdesc_sw128(au, 0, 1024);
+#pragma unroll 1
                 for (int k = 0; k < 4; ++k) {
-                    const uint64_t bk = sdesc_sw128(kt + k * 2048, 8192, 1024);
-                    mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + k * 32, 0, 1024), bk, ID_G2, true);
-                    mma_bf16_ss(tmem + TM_DT, sdesc_sw128(ay + 32768 + k * 32, 0, 1024), bk, ID_G2, true);
-                    mma_bf16_ss(tmem + TM_DS, sdesc_sw128(ay + 16384 + k * 32, 0, 1024), bk, ID_G2, true);
-                    mma_bf16_ss(tmem + TM_DS, sdesc_sw128(au + k * 32, 0, 1024), bk, ID_G2, true);
+                    const uint64_t bk = b0 + 128 * k;
+                    mma_bf16_ss(tmem + TM_DT, yh + 2 * k, bk, ID_G2, true);
+                    mma_bf16_ss(tmem + TM_DT, yl + 2 * k, bk, ID_G2, true);
+                    mma_bf16_ss(tmem + TM_DS, ys + 2 * k, bk, ID_G2, true);
+                    mma_bf16_ss(tmem + TM_DS, uu + 2 * k, bk, ID_G2, true);
                 }
                 mma_commit(&ms->d_ready);
                 mma_commit(&ms->emptyK[gc % kKStages]);
@@ -699,12 +718,13 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
             const uint32_t gc = g + i1;
             if (mbar_test(&ms->w_cvt, gc & 1) && (i1 == 0 || mbar_test(&ms->d_ready, (gc - 1) & 1))) {
                 tc_fence_after();
+                const uint64_t b0 = sdesc_sw128(bw, 0, 1024);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-#pragma unroll
+#pragma unroll 1
                     for (int k = 0; k < 16; ++k)
-                        mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k,
-                                    sdesc_sw128(bw + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024), ID_G1, k > 0);
+                        mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3),
+                                    ID_G1, k > 0);
                 mma_commit(&ms->x_done);
                 ++i1;
                 any = true;
@@ -715,10 +735,9 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
             if (mbar_test(&ms->that_ready, gc & 1) && mbar_test(&ms->fullV, gc & 1) &&
                 (iu == 0 || mbar_test(&ms->u_cvt, (gc - 1) & 1))) {
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ss(tmem + TM_U, sdesc_sw128(vt + k * 2048, 8192, 1024),
-                                sdesc_sw128(bt + 8192 + k * 32, 0, 1024), ID_WU, k > 0);
+                const uint64_t a0 = sdesc_sw128(vt, 8192, 1024), b0 = sdesc_sw128(bt + 8192, 0, 1024);
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_U, a0 + 128 * k, b0 + 2 * k, ID_WU, k > 0);
                 mma_commit(&ms->u_done);
                 mma_commit(&ms->emptyV);
                 ++iu;
@@ -730,10 +749,10 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
             if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
                 (ig == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
                 tc_fence_after();
-                const uint32_t kt = ktile(gc);
-#pragma unroll
+                const uint64_t d0 = sdesc_sw128(ktile(gc), 0, 1024);
+#pragma unroll 1
                 for (int k = 0; k < 8; ++k) {
-                    const uint64_t d = sdesc_sw128(kt + (k >> 2) * 8192 + (k & 3) * 32, 0, 1024);
+                    const uint64_t d = d0 + 512 * (k >> 2) + 2 * (k & 3);
                     mma_bf16_ss(tmem + TM_G, d, d, ID_GRAM, k > 0);
                 }
                 mma_commit(&ms->g_done);
@@ -757,7 +776,7 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
     }
 }
 
-// Warps 6-9: gram -> A -> (I + A)^-1 -> That, chunk after chunk.
+// Warps 6-13: gram -> A -> (I + A)^-1 -> That, chunk after chunk.
 __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int p, int q,
                           int lane) {
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
@@ -768,17 +787,17 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         const int slot = gc % kGateSlots;
         bool ok = wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a);
         ok = ok && wait_bar(&ms->g_done, gc & 1, ms, a);
-        if (!wg_all(1, ok)) return;
+        if (!wg_all(1, ok, kPrepThreads)) return;
         tc_fence_after();
-        prep_arows(ms, As, slot, tmem, q, lane);
+        prep_arows(ms, As, slot, tmem, q, p >> 7, lane);
         tc_fence_before();
-        named_sync(1);
+        named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->g_read);
         prep_solve(As, Ptmp, p);
-        if (!wg_all(1, gc == 0 || wait_bar(&ms->bt_free, (gc - 1) & 1, ms, a))) return;
+        if (!wg_all(1, gc == 0 || wait_bar(&ms->bt_free, (gc - 1) & 1, ms, a), kPrepThreads)) return;
         prep_write_that(ms, As, bt, slot, p);
         fence_async_smem();
-        named_sync(1);
+        named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->that_ready);
     }
 }
@@ -872,33 +891,36 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
     int E = 0, since = 0;
     float m = 1.f, lsT = 0.f, lsS = 0.f;
     StatePlan pl;
-    if (!state_prepare(ms, smem, a, tmem, g, nc == 1, since, lsT, lsS, m, q, lane, pl)) return;
-    for (int c = 0; c < nc; ++c) {
+    // Step c runs the pass of chunk c - 1 (none for c = 0), then prepares
+    // chunk c (none for c = nc): one call site per stage keeps the code small.
+    for (int c = 0; c <= nc; ++c) {
         const uint32_t gc = g + c;
-        if (!wg_all(2, wait_bar(&ms->x_done, gc & 1, ms, a))) return;
-        tc_fence_after();
-        const float mloc = state_pass<0>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
-        tc_fence_before();
-        named_sync(2);  // every lane has read X''_T: the next W'^T may overwrite those columns
-        if (n == 0) mbar_arrive(&ms->xt_free);
-        state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
-        fence_async_smem();
-        tc_fence_before();
-        if (pl.rn) {
-            m = state_reduce_max(mloc, ms->red[gc & 1], q, lane);
-            E += pl.e;
-            lsT = 0.f;
-            lsS = 0.f;
-            since = 0;
-        } else {
-            named_sync(2);
-            lsT += pl.lc;
-            lsS += pl.lc;
-            ++since;
+        if (c > 0) {
+            const uint32_t gp = gc - 1;
+            if (!wg_all(2, wait_bar(&ms->x_done, gp & 1, ms, a))) return;
+            tc_fence_after();
+            const float mloc = state_pass<0>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
+            tc_fence_before();
+            named_sync(2);  // every lane has read X''_T: the next W'^T may overwrite those columns
+            if (n == 0) mbar_arrive(&ms->xt_free);
+            state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
+            fence_async_smem();
+            tc_fence_before();
+            if (pl.rn) {
+                m = state_reduce_max(mloc, ms->red[gp & 1], q, lane);
+                E += pl.e;
+                lsT = 0.f;
+                lsS = 0.f;
+                since = 0;
+            } else {
+                named_sync(2);
+                lsT += pl.lc;
+                lsS += pl.lc;
+                ++since;
+            }
+            if (n == 0) mbar_arrive(&ms->y_ready);
         }
-        if (n == 0) mbar_arrive(&ms->y_ready);
-        if (c + 1 < nc && !state_prepare(ms, smem, a, tmem, gc + 1, c + 2 == nc, since, lsT, lsS, m, q, lane, pl))
-            return;
+        if (c < nc && !state_prepare(ms, smem, a, tmem, gc, c + 1 == nc, since, lsT, lsS, m, q, lane, pl)) return;
     }
     if (!wg_all(2, wait_bar(&ms->d_ready, (g + nc - 1) & 1, ms, a))) return;
     tc_fence_after();
