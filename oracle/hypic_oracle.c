@@ -28,7 +28,17 @@
  *    RetNet (scalar decay):   S_t = g S_{t-1} + k_t v_t^T,      T = g^L
  *    GLA    (diagonal decay): S_t = Diag(g_t) S_{t-1} + k_t v_t^T
  *    vanilla linear attention: S_t = S_{t-1} + k_t v_t^T,       T = I
+ *    KDA    (Kimi delta attention, a delta rule with a per-channel gate):
+ *           S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T,
+ *           a_t in (0, 1]^dk: the gate acts first, then the delta projection
+ *    Mamba2 (scalar decay per token, the SSD scan as linear attention):
+ *           S_t = a_t S_{t-1} + k_t v_t^T,                     T = prod a_t
  *    output of a token: o_t = S_t^T q_t (state after the token's own write).
+ *  [AB] names RetNet, Mamba2, GLA, DeltaNet, GDN and KDA as the families whose
+ *  pair needs T_C; it prints none of their recurrences.  The two above are the
+ *  published forms read as left-multiplied transitions on a dk x dv state:
+ *  Mamba2's input scaling (dt) is taken as already folded into k, and KDA's
+ *  gate vector is read from the same per-channel gate array as GLA's.
  *
  * Everything is a token-by-token loop in double precision, exactly in the
  * order above.  Inputs arrive as float32 arrays (bf16 inputs are upcast exactly
@@ -38,9 +48,10 @@
  *   k, v, q   [n_layers][n_tokens][n_heads][d]
  *   alpha, beta [n_layers][n_tokens][n_heads]
  *   gamma     [n_layers][n_heads]
- *   g         [n_layers][n_tokens][n_heads][dk]
- *   T (GDN)   [n_items][n_layers][n_heads][dk][dk]
- *   T (RetNet)[n_items][n_layers][n_heads]
+ *   g         [n_layers][n_tokens][n_heads][dk]   (GLA, KDA)
+ *   alpha     also the per-token decay of Mamba2; beta also KDA's
+ *   T (GDN, KDA)      [n_items][n_layers][n_heads][dk][dk]
+ *   T (RetNet, Mamba2)[n_items][n_layers][n_heads]
  *   T (GLA)   [n_items][n_layers][n_heads][dk]
  *   S, state  [n_items][n_layers][n_heads][dk][dv]
  */
@@ -51,7 +62,11 @@
 #include <omp.h>
 #endif
 
-enum { OR_GDN = 0, OR_RETNET = 1, OR_GLA = 2, OR_VANILLA = 3 };
+enum { OR_GDN = 0, OR_RETNET = 1, OR_GLA = 2, OR_VANILLA = 3, OR_KDA = 4, OR_MAMBA2 = 5 };
+
+/* Families whose T_C is a dk x dk matrix, and those whose T_C is a scalar. */
+static int dense_T(int family) { return family == OR_GDN || family == OR_KDA; }
+static int scalar_T(int family) { return family == OR_RETNET || family == OR_MAMBA2; }
 
 /* ---------------------------------------------------------------- tokens -- */
 
@@ -80,6 +95,22 @@ static void gdn_apply_transition(int dk, int ncols, double* M, const double* k,
     for (int i = 0; i < dk; ++i)
         for (int j = 0; j < ncols; ++j)
             M[(size_t)i * ncols + j] = a * (M[(size_t)i * ncols + j] - b * k[i] * tmp[j]);
+}
+
+/* M <- (I - b k k^T) Diag(a) M for the KDA transition, M is dk x ncols:
+   the per-channel gate scales row i of M by a[i], then the delta projection. */
+static void kda_apply_transition(int dk, int ncols, double* M, const double* k,
+                                 const double* a, double b, double* tmp)
+{
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < ncols; ++j) M[(size_t)i * ncols + j] *= a[i];
+    for (int j = 0; j < ncols; ++j) {
+        double s = 0.0;
+        for (int i = 0; i < dk; ++i) s += k[i] * M[(size_t)i * ncols + j];
+        tmp[j] = s; /* (k^T Diag(a) M)_j */
+    }
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < ncols; ++j) M[(size_t)i * ncols + j] -= b * k[i] * tmp[j];
 }
 
 /* S <- S + w k v^T (the write term of every family). */
@@ -124,6 +155,21 @@ static void token_step(const or_inputs* in, int layer, long long tok, int head,
         if (Tvec) for (int i = 0; i < dk; ++i) Tvec[i] *= gb[i];
         break;
     }
+    case OR_KDA: {
+        read_vec(in->g, row * dk, dk, gb);
+        const double b = in->beta[row];
+        kda_apply_transition(dk, dv, S, kb, gb, b, tmp);
+        add_write(dk, dv, S, kb, vb, b);
+        if (T) kda_apply_transition(dk, dk, T, kb, gb, b, tmp);
+        break;
+    }
+    case OR_MAMBA2: {
+        const double a = in->alpha[row];
+        for (size_t i = 0; i < (size_t)dk * dv; ++i) S[i] *= a;
+        add_write(dk, dv, S, kb, vb, 1.0);
+        if (Tscal) *Tscal *= a;
+        break;
+    }
     default: /* vanilla */
         add_write(dk, dv, S, kb, vb, 1.0);
         break;
@@ -132,9 +178,8 @@ static void token_step(const or_inputs* in, int layer, long long tok, int head,
 
 static int check_common(int family, int n_layers, int n_heads, int dk, int dv)
 {
-    if (family < OR_GDN || family > OR_VANILLA) return 1;
+    if (family < OR_GDN || family > OR_MAMBA2) return 1;
     if (n_layers <= 0 || n_heads <= 0 || dk <= 0 || dv <= 0) return 1;
-    if (family == OR_GDN && dk <= 0) return 1;
     return 0;
 }
 
@@ -168,12 +213,12 @@ int oracle_build(int family, int n_layers, int n_heads, int dk, int dv,
         const long long b0 = (long long)cu_seqlens[seg] + (skip ? skip[seg] : 0);
         const long long b1 = cu_seqlens[seg + 1];
         double* S = (double*)calloc((size_t)dk * dv, sizeof(double));
-        double* T = (family == OR_GDN) ? (double*)calloc((size_t)dk * dk, sizeof(double)) : NULL;
+        double* T = dense_T(family) ? (double*)calloc((size_t)dk * dk, sizeof(double)) : NULL;
         double* Tv = (family == OR_GLA) ? (double*)malloc((size_t)dk * sizeof(double)) : NULL;
         double Ts = 1.0;
         double* kb = (double*)malloc(sizeof(double) * (size_t)(dk + dv + dk + (dk > dv ? dk : dv)));
         double *vb = kb + dk, *gb = vb + dv, *tmp = gb + dk;
-        if (!S || !kb || (family == OR_GDN && !T) || (family == OR_GLA && !Tv)) { bad = 1; }
+        if (!S || !kb || (dense_T(family) && !T) || (family == OR_GLA && !Tv)) { bad = 1; }
         else {
             if (T) for (int i = 0; i < dk; ++i) T[(size_t)i * dk + i] = 1.0;
             if (Tv) for (int i = 0; i < dk; ++i) Tv[i] = 1.0;
@@ -181,9 +226,9 @@ int oracle_build(int family, int n_layers, int n_heads, int dk, int dv,
                 token_step(&in, layer, t, head, S, T, Tv, &Ts, kb, vb, gb, tmp);
             memcpy(S_out + (size_t)it * dk * dv, S, sizeof(double) * (size_t)dk * dv);
             if (T_out) {
-                if (family == OR_GDN) memcpy(T_out + (size_t)it * dk * dk, T, sizeof(double) * (size_t)dk * dk);
+                if (dense_T(family)) memcpy(T_out + (size_t)it * dk * dk, T, sizeof(double) * (size_t)dk * dk);
                 else if (family == OR_GLA) memcpy(T_out + (size_t)it * dk, Tv, sizeof(double) * (size_t)dk);
-                else if (family == OR_RETNET) T_out[it] = Ts;
+                else if (scalar_T(family)) T_out[it] = Ts;
             }
         }
         free(S); free(T); free(Tv); free(kb);
@@ -197,7 +242,7 @@ int oracle_build(int family, int n_layers, int n_heads, int dk, int dv,
  * Compose chains of cached pairs [AB]: for chain r, starting from S0[r] (or
  * zero), apply S <- T_i S + S_i for i = seg_idx[cu_chain[r]], ...,
  * seg_idx[cu_chain[r+1]-1] in that order.  The product T_i S is the family's:
- * a dk x dk matrix (GDN), a scalar (RetNet), a row scaling (GLA) or the
+ * a dk x dk matrix (GDN, KDA), a scalar (RetNet, Mamba2), a row scaling (GLA) or the
  * identity (vanilla, plain addition).  T_tab holds T_C in double with any
  * stored scale already applied; `naive` != 0 drops T entirely (the addition
  * strawman of [AB], "--pic-mode addition" in the README's PIC modes table).
@@ -230,7 +275,7 @@ int oracle_compose(int family, int n_layers, int n_heads, int dk, int dv, int n_
             const double* Si = S_tab + ((size_t)p * LH + lh) * dd;
             if (naive || family == OR_VANILLA) {
                 for (size_t e = 0; e < dd; ++e) N[e] = S[e];
-            } else if (family == OR_GDN) {
+            } else if (dense_T(family)) {
                 const double* Ti = T_tab + ((size_t)p * LH + lh) * (size_t)dk * dk;
                 for (int i = 0; i < dk; ++i)
                     for (int c = 0; c < dv; ++c) {
@@ -238,7 +283,7 @@ int oracle_compose(int family, int n_layers, int n_heads, int dk, int dv, int n_
                         for (int m = 0; m < dk; ++m) s += Ti[(size_t)i * dk + m] * S[(size_t)m * dv + c];
                         N[(size_t)i * dv + c] = s;
                     }
-            } else if (family == OR_RETNET) {
+            } else if (scalar_T(family)) {
                 const double ts = T_tab[(size_t)p * LH + lh];
                 for (size_t e = 0; e < dd; ++e) N[e] = ts * S[e];
             } else { /* GLA */
@@ -307,4 +352,4 @@ int oracle_seam(int family, int n_layers, int n_heads, int dk, int dv,
     return bad;
 }
 
-int oracle_version(void) { return 1; }
+int oracle_version(void) { return 2; }

@@ -28,7 +28,7 @@ import threading
 
 import numpy as np
 
-FAMILIES = {"gdn": 0, "retnet": 1, "gla": 2, "vanilla": 3}
+FAMILIES = {"gdn": 0, "retnet": 1, "gla": 2, "vanilla": 3, "kda": 4, "mamba2": 5}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hypic_oracle.c")
@@ -100,8 +100,8 @@ def build_pairs(family, k, v, cu_seqlens, *, alpha=None, beta=None, gamma=None, 
 
     k: [n_layers][n_tokens][n_heads][dk], v: [..][dv]; gates as in the header.
     Returns (T, S) in float64 with leading [n_seg][n_layers][n_heads]; T is
-    None for vanilla, shaped [...][dk][dk] (GDN), [...] (RetNet) or [...][dk]
-    (GLA).
+    None for vanilla, shaped [...][dk][dk] (GDN, KDA), [...] (RetNet, Mamba2)
+    or [...][dk] (GLA).
     """
     fam = FAMILIES[family]
     k, v = _f32(k), _f32(v)
@@ -112,9 +112,9 @@ def build_pairs(family, k, v, cu_seqlens, *, alpha=None, beta=None, gamma=None, 
     sk = _i32(skip)
     alpha, beta, gamma, g = _f32(alpha), _f32(beta), _f32(gamma), _f32(g)
     S = np.zeros((n_seg, n_layers, n_heads, dk, dv))
-    if fam == 0:
+    if fam in (0, 4):
         T = np.zeros((n_seg, n_layers, n_heads, dk, dk))
-    elif fam == 1:
+    elif fam in (1, 5):
         T = np.zeros((n_seg, n_layers, n_heads))
     elif fam == 2:
         T = np.zeros((n_seg, n_layers, n_heads, dk))

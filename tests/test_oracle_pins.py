@@ -165,17 +165,22 @@ def _family_inputs(fam, rng, n, d, H=2):
         kw["gamma"] = np.array([[0.97, 0.995]], np.float32)[:, :H]
     elif fam == "gla":
         kw["g"] = rng.uniform(0.9, 1.0, (1, n, H, d)).astype(np.float32)
+    elif fam == "kda":
+        kw["g"] = rng.uniform(0.9, 1.0, (1, n, H, d)).astype(np.float32)
+        kw["beta"] = rng.uniform(0.0, 0.5, (1, n, H)).astype(np.float32)
+    elif fam == "mamba2":
+        kw["alpha"] = rng.uniform(0.9, 1.0, (1, n, H)).astype(np.float32)
     return k, v, kw
 
 
 def _T_apply(fam, T2, T1):
     """T(C1.C2) from T(C2), T(C1) by the family's product (T2 applied last)."""
-    if fam == "gdn":
+    if fam in ("gdn", "kda"):
         return T2 @ T1
     return T2 * T1
 
 
-@pytest.mark.parametrize("fam", ["gdn", "retnet", "gla", "vanilla"])
+@pytest.mark.parametrize("fam", ["gdn", "retnet", "gla", "vanilla", "kda", "mamba2"])
 def test_associativity_build_equals_compose(fam):
     """The composition law of the aibase article: building C1.C2 in one pass
     equals composing the separately built pairs, S(C1.C2) = T(C2) S(C1) + S(C2),
@@ -346,3 +351,89 @@ def test_rel_fro():
     x[1] *= 1.01
     r = orc.rel_fro(x, ref, (-2, -1))
     np.testing.assert_allclose(r, [0.0, 0.01], atol=1e-15)
+
+
+# ------------------------------------------------------------ KDA, Mamba2 ----
+
+def test_kda_brute_force_explicit_matrices():
+    """KDA: T_C = A_L ... A_1 with explicit per-token matrices
+    A_t = (I - b_t k_t k_t^T) Diag(a_t) (the gate first, then the delta
+    projection), S(C|0) = sum_t (A_L ... A_{t+1}) b_t k_t v_t^T."""
+    rng = np.random.default_rng(21)
+    d, L = 8, 24
+    k = unit_rows(rng, (L, d))
+    v = rng.standard_normal((L, d)).astype(np.float32)
+    a = rng.uniform(0.5, 1.0, (L, d)).astype(np.float32)
+    b = rng.uniform(0.0, 1.0, L).astype(np.float32)
+    T, S = orc.build_pairs("kda", one_head(k), one_head(v), [0, L], g=one_head(a), beta=gates(b))
+    kd, vd, ad = k.astype(np.float64), v.astype(np.float64), a.astype(np.float64)
+    A = [(np.eye(d) - float(b[t]) * np.outer(kd[t], kd[t])) @ np.diag(ad[t]) for t in range(L)]
+    def ordered_product(mats):
+        P = np.eye(d)
+        for M in mats:
+            P = M @ P
+        return P
+
+    S_bf = np.zeros((d, d))
+    for t in range(L):
+        S_bf += ordered_product(A[t + 1:]) @ (float(b[t]) * np.outer(kd[t], vd[t]))
+    np.testing.assert_allclose(T[0, 0, 0], ordered_product(A), atol=1e-13)
+    np.testing.assert_allclose(S[0, 0, 0], S_bf, atol=1e-12)
+    # the gate does not commute with the projection: the other order differs
+    A_swapped = [np.diag(ad[t]) @ (np.eye(d) - float(b[t]) * np.outer(kd[t], kd[t])) for t in range(L)]
+    Tsw = ordered_product(A_swapped)
+    assert np.linalg.norm(Tsw - T[0, 0, 0]) > 1e-2 * np.linalg.norm(T[0, 0, 0])
+
+
+def test_kda_with_a_uniform_gate_is_gdn():
+    """A per-channel gate equal in every channel is GDN's scalar gate:
+    (I - b k k^T) (a I) = a (I - b k k^T); pair and seam outputs agree."""
+    rng = np.random.default_rng(22)
+    d, L = 16, 70
+    k = unit_rows(rng, (1, L, 2, d))
+    v = rng.standard_normal((1, L, 2, d)).astype(np.float32)
+    q = unit_rows(rng, (1, L, 2, d))
+    a = rng.uniform(0.8, 1.0, (1, L, 2)).astype(np.float32)
+    b = rng.uniform(0.0, 1.0, (1, L, 2)).astype(np.float32)
+    g = np.repeat(a[..., None], d, axis=-1)
+    Tk, Sk = orc.build_pairs("kda", k, v, [0, 30, L], g=g, beta=b)
+    Tg, Sg = orc.build_pairs("gdn", k, v, [0, 30, L], alpha=a, beta=b)
+    np.testing.assert_allclose(Tk, Tg, atol=1e-13)
+    np.testing.assert_allclose(Sk, Sg, atol=1e-12)
+    _, ok = orc.seam("kda", q, k, v, [0, L], g=g, beta=b)
+    _, og = orc.seam("gdn", q, k, v, [0, L], alpha=a, beta=b)
+    np.testing.assert_allclose(ok, og, atol=1e-12)
+
+
+def test_kda_without_writes_is_the_gate_product():
+    """b = 0: no erase and no write, so T = Diag(prod_t a_t) and S = 0."""
+    rng = np.random.default_rng(23)
+    d, L = 16, 40
+    k = unit_rows(rng, (L, d))
+    v = rng.standard_normal((L, d)).astype(np.float32)
+    a = rng.uniform(0.8, 1.0, (L, d)).astype(np.float32)
+    T, S = orc.build_pairs("kda", one_head(k), one_head(v), [0, L], g=one_head(a),
+                           beta=gates(np.zeros(L)))
+    np.testing.assert_allclose(T[0, 0, 0], np.diag(np.prod(a.astype(np.float64), axis=0)), rtol=1e-13, atol=0)
+    assert np.all(S == 0)
+
+
+def test_mamba2_closed_forms_and_retnet_special_case():
+    """Mamba2: T = prod_t a_t, S = sum_t (prod_{s>t} a_s) k_t v_t^T; with a
+    constant gate it is RetNet."""
+    rng = np.random.default_rng(24)
+    d, L = 16, 60
+    k = unit_rows(rng, (L, d))
+    v = rng.standard_normal((L, d)).astype(np.float32)
+    a = rng.uniform(0.7, 1.0, L).astype(np.float32)
+    T, S = orc.build_pairs("mamba2", one_head(k), one_head(v), [0, L], alpha=gates(a))
+    ad = a.astype(np.float64)
+    np.testing.assert_allclose(T[0, 0, 0], np.prod(ad), rtol=1e-13)
+    later = np.concatenate([np.cumprod(ad[::-1])[::-1][1:], [1.0]])  # prod_{s>t} a_s
+    S_want = (later[:, None] * k.astype(np.float64)).T @ v.astype(np.float64)
+    np.testing.assert_allclose(S[0, 0, 0], S_want, atol=1e-12)
+    gm = np.float32(0.95)
+    Tm, Sm = orc.build_pairs("mamba2", one_head(k), one_head(v), [0, L], alpha=gates(np.full(L, gm)))
+    Tr, Sr = orc.build_pairs("retnet", one_head(k), one_head(v), [0, L], gamma=np.array([[gm]]))
+    np.testing.assert_allclose(Tm, Tr, rtol=1e-13)
+    np.testing.assert_allclose(Sm, Sr, atol=1e-13)
