@@ -20,13 +20,21 @@
  *             of independently cached segments.
  *
  * Families and per-token recurrences (state S is dk x dv, left-multiplied,
- * latest token leftmost; the four families are among those the [AIBASE]
- * linear-layer paragraph names):
+ * latest token leftmost; all six are among the families the [AIBASE]
+ * linear-layer paragraph names, which prints none of their recurrences: the
+ * forms below are the published ones read as left-multiplied transitions):
  *   HYPIC_GDN      S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T
  *                  (gated delta rule); T_C is a dense dk x dk matrix.
  *   HYPIC_RETNET   S_t = g S_{t-1} + k_t v_t^T;  T_C = g^L (a scalar).
  *   HYPIC_GLA      S_t = Diag(g_t) S_{t-1} + k_t v_t^T;  T_C = prod g_t (dk-vector).
  *   HYPIC_VANILLA  S_t = S_{t-1} + k_t v_t^T;  T_C = I (not stored).
+ *   HYPIC_KDA      S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T
+ *                  (Kimi delta attention: a per-channel gate a_t, read from g,
+ *                  acts before the delta projection); T_C is a dense dk x dk
+ *                  matrix stored like GDN's.
+ *   HYPIC_MAMBA2   S_t = a_t S_{t-1} + k_t v_t^T with a scalar decay a_t per
+ *                  token and head (read from alpha; the input step size is
+ *                  taken as folded into k);  T_C = prod a_t (a scalar).
  *   Seam outputs: o_t = S_t^T q_t, with S_t the state after token t's write.
  *
  * Conventions common to every call
@@ -38,8 +46,9 @@
  *     pointer must be 16-byte aligned.
  *       k, v, q        [n_layers][n_tokens][n_heads][dk | dv]   (f32 or bf16)
  *       alpha, beta    [n_layers][n_tokens][n_heads]             (f32)
+ *                      (alpha: GDN's gate, MAMBA2's decay; beta: GDN, KDA)
  *       gamma          [n_layers][n_heads]                       (f32)
- *       g              [n_layers][n_tokens][n_heads][dk]         (f32)
+ *       g              [n_layers][n_tokens][n_heads][dk]         (f32; GLA, KDA)
  *       per-item state [n_items][n_layers][n_heads][dk][dv]      (f32)
  *   - Calls are asynchronous on the given stream and the library keeps no
  *     state between calls (except the device error word, below); distinct
@@ -64,7 +73,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_VERSION 110 /* 1.1.0: hypic_reuse_chain */
+#define HYPIC_VERSION 120 /* 1.2.0: KDA and MAMBA2 families */
 
 #if defined(__GNUC__)
 #define HYPIC_API __attribute__((visibility("default")))
@@ -83,7 +92,14 @@ typedef enum {
     HYPIC_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out */
 } hypic_status;
 
-typedef enum { HYPIC_GDN = 0, HYPIC_RETNET = 1, HYPIC_GLA = 2, HYPIC_VANILLA = 3 } hypic_family;
+typedef enum {
+    HYPIC_GDN = 0,
+    HYPIC_RETNET = 1,
+    HYPIC_GLA = 2,
+    HYPIC_VANILLA = 3,
+    HYPIC_KDA = 4,
+    HYPIC_MAMBA2 = 5
+} hypic_family;
 typedef enum { HYPIC_F32 = 0, HYPIC_BF16 = 1 } hypic_dtype;
 
 /* ------------------------------------------------------------------ build --
@@ -100,15 +116,18 @@ typedef enum { HYPIC_F32 = 0, HYPIC_BF16 = 1 } hypic_dtype;
  *   RETNET   k, v, gamma                       (beta must be NULL: b = 1)
  *   GLA      k, v, g
  *   VANILLA  k, v
+ *   KDA      k, v, g (the per-channel gate a_t), beta
+ *   MAMBA2   k, v, alpha (the per-token decay a_t)
  * Outputs, leading dims [n_segments][n_layers][n_heads]:
  *   S_out   [..][dk][dv] f32
- *   T_out   GDN: [..][dk][dk] f32 mantissa, with T_exp_out [..] int32 such that
- *           T_C = T_out * 2^T_exp_out (the exponent keeps T_C representable
+ *   T_out   GDN, KDA: [..][dk][dk] f32 mantissa, with T_exp_out [..] int32 such
+ *           that T_C = T_out * 2^T_exp_out (the exponent keeps T_C representable
  *           when its entries fall below the f32 range, as they do for long
  *           segments with strong decay); RETNET: [..] f32 scalar g^L;
- *           GLA: [..][dk] f32 vector; VANILLA: NULL.
- *   T_exp_out  GDN only (NULL otherwise).
- * Supported: dk, dv in {16, 32, 64, 128}; GDN requires dk == dv.
+ *           MAMBA2: [..] f32 scalar prod a_t; GLA: [..][dk] f32 vector;
+ *           VANILLA: NULL.
+ *   T_exp_out  GDN and KDA only (NULL otherwise).
+ * Supported: dk, dv in {16, 32, 64, 128}; GDN and KDA require dk == dv.
  * Work order: segments are processed longest body first (LPT order).
  */
 typedef struct {
@@ -149,14 +168,15 @@ HYPIC_API hypic_status hypic_segment_build(const hypic_build_args* args, void* w
  * chain r and every (layer, head): S <- S0[r] (or 0 when S0 == NULL), then
  * S <- T_p S + S_p for p = seg_idx[cu_chain[r]], ..., seg_idx[cu_chain[r+1]-1]
  * in that order; S_out[r] <- S.  A chain of length 0 copies its start state.
- * T_p S is a dk x dk matrix product (GDN, with T_p = T_tab * 2^T_exp_tab;
- * T_exp_tab == NULL means exponent 0), a scalar (RETNET), a row scaling (GLA)
- * or the identity (VANILLA: plain addition, T_tab must be NULL).
+ * T_p S is a dk x dk matrix product (GDN and KDA, with T_p = T_tab *
+ * 2^T_exp_tab; T_exp_tab == NULL means exponent 0), a scalar (RETNET,
+ * MAMBA2), a row scaling (GLA) or the identity (VANILLA: plain addition,
+ * T_tab must be NULL).
  * Pair tables (the build's outputs, or any cache of them):
  *   T_tab [n_pairs][n_layers][n_heads](...) as T_out above; S_tab
  *   [n_pairs][n_layers][n_heads][dk][dv].
  * S_out [n_chains][n_layers][n_heads][dk][dv] must not overlap the tables or S0.
- * Supported: dk, dv in {16, 32, 64, 128}; GDN requires dk == dv.
+ * Supported: dk, dv in {16, 32, 64, 128}; GDN and KDA require dk == dv.
  */
 typedef struct {
     int family;

@@ -17,8 +17,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libhypic.so")
 
-GDN, RETNET, GLA, VANILLA = 0, 1, 2, 3
-FAMILY = {"gdn": GDN, "retnet": RETNET, "gla": GLA, "vanilla": VANILLA}
+GDN, RETNET, GLA, VANILLA, KDA, MAMBA2 = 0, 1, 2, 3, 4, 5
+FAMILY = {"gdn": GDN, "retnet": RETNET, "gla": GLA, "vanilla": VANILLA, "kda": KDA, "mamba2": MAMBA2}
 F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 
@@ -203,10 +203,10 @@ def alloc_build_outputs(family, n_seg, n_layers, n_heads, dk, dv, device):
     lead = (n_seg, n_layers, n_heads)
     S = torch.empty(lead + (dk, dv), dtype=torch.float32, device=device)
     T = T_exp = None
-    if fam == GDN:
+    if fam in (GDN, KDA):
         T = torch.empty(lead + (dk, dk), dtype=torch.float32, device=device)
         T_exp = torch.empty(lead, dtype=torch.int32, device=device)
-    elif fam == RETNET:
+    elif fam in (RETNET, MAMBA2):
         T = torch.empty(lead, dtype=torch.float32, device=device)
     elif fam == GLA:
         T = torch.empty(lead + (dk,), dtype=torch.float32, device=device)
@@ -218,7 +218,7 @@ def segment_build(family, k, v, cu_seqlens, *, alpha=None, beta=None, gamma=None
     """(T, T_exp, S) per (segment, layer, head) via hypic_segment_build.
 
     k, v: CUDA tensors [n_layers][n_tokens][n_heads][d]; cu_seqlens (and
-    seam_skip) host int arrays.  For GDN the transition product is
+    seam_skip) host int arrays.  For GDN and KDA the transition product is
     T_C = T * 2**T_exp.  ``out`` = (T, T_exp, S) preallocated, optional.
     """
     import torch

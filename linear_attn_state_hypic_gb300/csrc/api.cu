@@ -77,32 +77,39 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 const char* fam_name(int f) {
-    static const char* n[] = {"GDN", "RETNET", "GLA", "VANILLA"};
-    return (f >= 0 && f <= 3) ? n[f] : "?";
+    static const char* n[] = {"GDN", "RETNET", "GLA", "VANILLA", "KDA", "MAMBA2"};
+    return (f >= 0 && f <= 5) ? n[f] : "?";
 }
+
+// T_C is a dense dk x dk matrix (stored with an exponent) / a scalar.
+bool dense_T(int family) { return family == HYPIC_GDN || family == HYPIC_KDA; }
 
 // Checks shared by the three calls: family, dtype, dims and the family's
 // gate pointers.  `has_tokens` is false when no token is read.
 hypic_status check_family(int family, int in_dtype, int n_layers, int n_heads, int dk, int dv, bool has_tokens,
                           const float* alpha, const float* beta, const float* gamma, const float* g,
                           bool check_dtype) {
-    if (family < HYPIC_GDN || family > HYPIC_VANILLA) return fail(HYPIC_ERR_INVALID_ARG, "family %d", family);
+    if (family < HYPIC_GDN || family > HYPIC_MAMBA2) return fail(HYPIC_ERR_INVALID_ARG, "family %d", family);
     if (check_dtype && in_dtype != HYPIC_F32 && in_dtype != HYPIC_BF16)
         return fail(HYPIC_ERR_INVALID_ARG, "in_dtype %d", in_dtype);
     if (n_layers < 1 || n_heads < 1) return fail(HYPIC_ERR_INVALID_ARG, "n_layers %d n_heads %d", n_layers, n_heads);
     if (dk < 1 || dv < 1) return fail(HYPIC_ERR_INVALID_ARG, "dk %d dv %d", dk, dv);
     if (!dim_ok(dk) || !dim_ok(dv))
         return fail(HYPIC_ERR_UNSUPPORTED, "dk %d dv %d (supported: 16, 32, 64, 128)", dk, dv);
-    if (family == HYPIC_GDN && dk != dv) return fail(HYPIC_ERR_UNSUPPORTED, "GDN needs dk == dv (%d, %d)", dk, dv);
-    const bool want_ab = family == HYPIC_GDN, want_gamma = family == HYPIC_RETNET, want_g = family == HYPIC_GLA;
-    if (!want_ab && (alpha || beta))
-        return fail(HYPIC_ERR_INVALID_ARG, "alpha/beta must be NULL for %s", fam_name(family));
+    if (dense_T(family) && dk != dv)
+        return fail(HYPIC_ERR_UNSUPPORTED, "%s needs dk == dv (%d, %d)", fam_name(family), dk, dv);
+    const bool want_alpha = family == HYPIC_GDN || family == HYPIC_MAMBA2;
+    const bool want_beta = family == HYPIC_GDN || family == HYPIC_KDA;
+    const bool want_gamma = family == HYPIC_RETNET, want_g = family == HYPIC_GLA || family == HYPIC_KDA;
+    if (!want_alpha && alpha) return fail(HYPIC_ERR_INVALID_ARG, "alpha must be NULL for %s", fam_name(family));
+    if (!want_beta && beta) return fail(HYPIC_ERR_INVALID_ARG, "beta must be NULL for %s", fam_name(family));
     if (!want_gamma && gamma) return fail(HYPIC_ERR_INVALID_ARG, "gamma must be NULL for %s", fam_name(family));
     if (!want_g && g) return fail(HYPIC_ERR_INVALID_ARG, "g must be NULL for %s", fam_name(family));
     if (has_tokens) {  // gates are read only when tokens are
-        if (want_ab && (!alpha || !beta)) return fail(HYPIC_ERR_INVALID_ARG, "GDN needs alpha and beta");
+        if (want_alpha && !alpha) return fail(HYPIC_ERR_INVALID_ARG, "%s needs alpha", fam_name(family));
+        if (want_beta && !beta) return fail(HYPIC_ERR_INVALID_ARG, "%s needs beta", fam_name(family));
         if (want_gamma && !gamma) return fail(HYPIC_ERR_INVALID_ARG, "RETNET needs gamma");
-        if (want_g && !g) return fail(HYPIC_ERR_INVALID_ARG, "GLA needs g");
+        if (want_g && !g) return fail(HYPIC_ERR_INVALID_ARG, "%s needs g", fam_name(family));
     }
     const void* ptrs[] = {alpha, beta, gamma, g};
     for (const void* q : ptrs)
@@ -141,17 +148,15 @@ hypic_status check_build(const hypic_build_args* a) {
     hypic_status st = check_family(a->family, a->in_dtype, a->n_layers, a->n_heads, a->dk, a->dv, has_tokens, a->alpha,
                                    a->beta, a->gamma, a->g, true);
     if (st != HYPIC_OK) return st;
-    if (a->family == HYPIC_RETNET || a->family == HYPIC_GLA || a->family == HYPIC_VANILLA) {
-        if (a->beta) return fail(HYPIC_ERR_INVALID_ARG, "beta must be NULL for %s", fam_name(a->family));
-    }
     if (has_tokens && (!a->k || !a->v)) return fail(HYPIC_ERR_INVALID_ARG, "k and v required");
     const bool any = a->n_segments > 0;
     if (any && !a->S_out) return fail(HYPIC_ERR_INVALID_ARG, "S_out required");
-    const bool want_T = a->family != HYPIC_VANILLA, want_exp = a->family == HYPIC_GDN;
+    const bool want_T = a->family != HYPIC_VANILLA, want_exp = dense_T(a->family);
     if (!want_T && a->T_out) return fail(HYPIC_ERR_INVALID_ARG, "T_out must be NULL for VANILLA");
     if (!want_exp && a->T_exp_out) return fail(HYPIC_ERR_INVALID_ARG, "T_exp_out must be NULL for %s", fam_name(a->family));
     if (any && want_T && !a->T_out) return fail(HYPIC_ERR_INVALID_ARG, "T_out required for %s", fam_name(a->family));
-    if (any && want_exp && !a->T_exp_out) return fail(HYPIC_ERR_INVALID_ARG, "T_exp_out required for GDN");
+    if (any && want_exp && !a->T_exp_out)
+        return fail(HYPIC_ERR_INVALID_ARG, "T_exp_out required for %s", fam_name(a->family));
     const void* ptrs[] = {a->k, a->v, a->T_out, a->T_exp_out, a->S_out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
@@ -222,8 +227,10 @@ namespace {
 
 size_t T_bytes_per_obj(int family, int dk) {
     switch (family) {
-        case HYPIC_GDN: return sizeof(float) * (size_t)dk * dk;
-        case HYPIC_RETNET: return sizeof(float);
+        case HYPIC_GDN:
+        case HYPIC_KDA: return sizeof(float) * (size_t)dk * dk;
+        case HYPIC_RETNET:
+        case HYPIC_MAMBA2: return sizeof(float);
         case HYPIC_GLA: return sizeof(float) * (size_t)dk;
     }
     return 0;
@@ -251,7 +258,8 @@ hypic_status check_compose(const hypic_compose_args* a) {
         if (a->family != HYPIC_VANILLA && !a->T_tab) return fail(HYPIC_ERR_INVALID_ARG, "T_tab required for %s", fam_name(a->family));
     }
     if (a->family == HYPIC_VANILLA && a->T_tab) return fail(HYPIC_ERR_INVALID_ARG, "T_tab must be NULL for VANILLA");
-    if (a->family != HYPIC_GDN && a->T_exp_tab) return fail(HYPIC_ERR_INVALID_ARG, "T_exp_tab must be NULL for %s", fam_name(a->family));
+    if (!dense_T(a->family) && a->T_exp_tab)
+        return fail(HYPIC_ERR_INVALID_ARG, "T_exp_tab must be NULL for %s", fam_name(a->family));
     if (a->n_chains > 0 && !a->S_out) return fail(HYPIC_ERR_INVALID_ARG, "S_out required");
     const void* ptrs[] = {a->T_tab, a->T_exp_tab, a->S_tab, a->S0, a->S_out};
     for (const void* p : ptrs)

@@ -61,10 +61,11 @@ __device__ __forceinline__ float block_max(float v, float* red) {
     return m;
 }
 
-// ------------------------------------------------------------ GDN (SIMT) --
+// ------------------------------------------------------ GDN, KDA (SIMT) --
 // Thread c < DK owns column c of T (starts as e_c); thread DK + j owns column j
 // of S (starts at 0).  Per token: u = k^T col, col <- a (col - b u k) + b v_j k
-// (the write term only in the S columns).  After every staged chunk the T
+// (the write term only in the S columns).  KDA first scales the column by its
+// per-channel gate, col_i <- a_t[i] col_i, then takes the same step with a = 1.  After every staged chunk the T
 // columns are rescaled by a power of two so that their largest entry lies in
 // [1, 2); the exponent is accumulated and stored with T (T_C = T_out 2^T_exp).
 template <int DK, int DV>
@@ -75,6 +76,8 @@ __global__ void __launch_bounds__(DK + DV) gdn_build_simt_kernel(BuildParams p, 
     float* as = vs + kChunk * DV;      // [kChunk]
     float* bs = as + kChunk;           // [kChunk]
     float* red = bs + kChunk;          // [32]
+    float* gs = red + 32;              // [kChunk][DK] (KDA)
+    const bool kda = p.family == kKDA;
     const int LH = p.n_layers * p.n_heads;
     const int seg = order[blockIdx.x / LH];
     const int lh = blockIdx.x % LH, layer = lh / p.n_heads, head = lh % p.n_heads;
@@ -90,11 +93,19 @@ __global__ void __launch_bounds__(DK + DV) gdn_build_simt_kernel(BuildParams p, 
         __syncthreads();
         stage_rows<DK>(ks, p.k, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
         stage_rows<DV>(vs, p.v, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
-        stage_gate(as, p.alpha, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
+        if (kda)
+            stage_rows<DK>(gs, p.g, kF32, layer, t0, n, head, p.n_tokens, p.n_heads);
+        else
+            stage_gate(as, p.alpha, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
         stage_gate(bs, p.beta, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
         __syncthreads();
         for (int t = 0; t < n; ++t) {
             const float* kt = ks + t * DK;
+            if (kda) {
+                const float* gt = gs + t * DK;
+#pragma unroll
+                for (int i = 0; i < DK; ++i) col[i] *= gt[i];
+            }
             float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
 #pragma unroll
             for (int i = 0; i < DK; i += 4) {
@@ -104,7 +115,7 @@ __global__ void __launch_bounds__(DK + DV) gdn_build_simt_kernel(BuildParams p, 
                 u3 = fmaf(kt[i + 3], col[i + 3], u3);
             }
             const float u = (u0 + u1) + (u2 + u3);
-            const float a = as[t], b = bs[t];
+            const float a = kda ? 1.f : as[t], b = bs[t];
             const float w = isT ? -a * b * u : b * (vs[t * DV + (c - DK)] - a * u);
 #pragma unroll
             for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], w, a * col[i]);
@@ -138,9 +149,10 @@ __global__ void __launch_bounds__(DK + DV) gdn_build_simt_kernel(BuildParams p, 
 }
 
 // ------------------------------------------------- decay families (SIMT) --
-// Thread j < DV owns column j of S.  RetNet: col <- g col + v_j k; GLA:
-// col_i <- g_t[i] col_i + v_j k_i; vanilla: col <- col + v_j k.  T: RetNet
-// g^L, GLA prod_t g_t (thread i < DK keeps row i's product in double).
+// Thread j < DV owns column j of S.  RetNet: col <- g col + v_j k; Mamba2:
+// col <- a_t col + v_j k; GLA: col_i <- g_t[i] col_i + v_j k_i; vanilla:
+// col <- col + v_j k.  T: RetNet g^L, Mamba2 prod_t a_t (thread 0, in
+// double), GLA prod_t g_t (thread i < DK keeps row i's product in double).
 template <int DK, int DV>
 __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(BuildParams p,
                                                                              const int32_t* __restrict__ order) {
@@ -148,6 +160,7 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
     float* ks = sm;                // [kChunk][DK]
     float* vs = ks + kChunk * DK;  // [kChunk][DV]
     float* gs = vs + kChunk * DV;  // [kChunk][DK] (GLA)
+    float* as = gs + kChunk * DK;  // [kChunk] (Mamba2)
     const int LH = p.n_layers * p.n_heads;
     const int seg = order[blockIdx.x / LH];
     const int lh = blockIdx.x % LH, layer = lh / p.n_heads, head = lh % p.n_heads;
@@ -165,6 +178,7 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
         stage_rows<DK>(ks, p.k, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
         stage_rows<DV>(vs, p.v, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
         if (fam == kGLA) stage_rows<DK>(gs, p.g, kF32, layer, t0, n, head, p.n_tokens, p.n_heads);
+        if (fam == kMAMBA2) stage_gate(as, p.alpha, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
         __syncthreads();
         if (c < DV) {
             for (int t = 0; t < n; ++t) {
@@ -174,6 +188,10 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
                     const float* gt = gs + t * DK;
 #pragma unroll
                     for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, gt[i] * col[i]);
+                } else if (fam == kMAMBA2) {
+                    const float at = as[t];
+#pragma unroll
+                    for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, at * col[i]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, gm * col[i]);
@@ -182,6 +200,8 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
         }
         if (fam == kGLA && c < DK)
             for (int t = 0; t < n; ++t) tprod *= (double)gs[t * DK + c];
+        if (fam == kMAMBA2 && c == 0)
+            for (int t = 0; t < n; ++t) tprod *= (double)as[t];
     }
     const int64_t obj = ((int64_t)seg * p.n_layers + layer) * p.n_heads + head;
     if (c < DV) {
@@ -191,20 +211,21 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
     }
     if (fam == kGLA && c < DK) p.T_out[obj * DK + c] = (float)tprod;
     if (fam == kRETNET && c == 0) p.T_out[obj] = (float)pow((double)gm, (double)(b1 - b0));
+    if (fam == kMAMBA2 && c == 0) p.T_out[obj] = (float)tprod;
 }
 
 template <int DK, int DV>
 static cudaError_t launch_simt_dims(const BuildParams& p, const int32_t* order, cudaStream_t s) {
     const int64_t grid = (int64_t)p.n_seg * p.n_layers * p.n_heads;
     if (grid == 0) return cudaSuccess;
-    if (p.family == kGDN) {
-        const size_t smem = sizeof(float) * (kChunk * (DK + DV) + 2 * kChunk + 32);
+    if (p.family == kGDN || p.family == kKDA) {
+        const size_t smem = sizeof(float) * (kChunk * (DK + DV) + 2 * kChunk + 32 + (p.family == kKDA ? kChunk * DK : 0));
         auto kern = gdn_build_simt_kernel<DK, DV>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         kern<<<(unsigned)grid, DK + DV, smem, s>>>(p, order);
     } else {
-        const size_t smem = sizeof(float) * kChunk * (2 * DK + DV);
+        const size_t smem = sizeof(float) * (kChunk * (2 * DK + DV) + kChunk);
         auto kern = decay_build_simt_kernel<DK, DV>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -6,7 +6,7 @@
 
 namespace hypic {
 
-enum : int { kGDN = 0, kRETNET = 1, kGLA = 2, kVANILLA = 3 };
+enum : int { kGDN = 0, kRETNET = 1, kGLA = 2, kVANILLA = 3, kKDA = 4, kMAMBA2 = 5 };
 enum : int { kF32 = 0, kBF16 = 1 };
 
 // Codes written to the device error word (first writer wins).

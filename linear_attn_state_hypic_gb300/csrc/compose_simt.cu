@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(DV) compose_decay_simt_kernel(ComposeParams p,
         }
         const int64_t pobj = (int64_t)pi * LH + lh;
         const float* Sp = p.S_tab + pobj * DK * DV;
-        if (p.family == kRETNET) {
+        if (p.family == kRETNET || p.family == kMAMBA2) {
             const float t = p.T_tab[pobj];
 #pragma unroll
             for (int i = 0; i < DK; ++i) col[i] = fmaf(t, col[i], Sp[i * DV + c]);
@@ -103,7 +103,7 @@ template <int DK, int DV>
 static cudaError_t launch_compose_dims(const ComposeParams& p, unsigned* err, cudaStream_t s) {
     const int64_t grid = (int64_t)p.n_chains * p.n_layers * p.n_heads;
     if (grid == 0) return cudaSuccess;
-    if (p.family == kGDN) {
+    if (p.family == kGDN || p.family == kKDA) {
         if constexpr (DK == DV) {
             const size_t smem = sizeof(float) * 2 * DK * DK;
             auto kern = compose_gdn_simt_kernel<DK>;

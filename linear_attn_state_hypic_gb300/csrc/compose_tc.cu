@@ -718,7 +718,7 @@ bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const float
 }  // namespace
 
 bool compose_tc_supported(const ComposeParams& p) {
-    return p.family == kGDN && p.dk == kD && p.dv == kD && p.n_pairs > 0 &&
+    return (p.family == kGDN || p.family == kKDA) && p.dk == kD && p.dv == kD && p.n_pairs > 0 &&
            (int64_t)p.n_pairs * p.n_layers * p.n_heads * kD < INT32_MAX && encode_fn() != nullptr;
 }
 
@@ -763,7 +763,9 @@ cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_
     return launch_tc<false>(p, a, s);
 }
 
-bool chain_tc_supported(const ChainParams& p) { return compose_tc_supported(p.c) && p.c.n_pairs > 0; }
+bool chain_tc_supported(const ChainParams& p) {  // (the fused seam units run the GDN recurrence)
+    return p.c.family == kGDN && compose_tc_supported(p.c) && p.c.n_pairs > 0;
+}
 
 cudaError_t launch_chain_tc(const ChainParams& p, unsigned* err, cudaStream_t s) {
     CtArgs a = {};

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) seam_simt_kernel(SeamParams
     float* qs = sm;                    // [kSeamChunk][DK]
     float* ks = qs + kSeamChunk * DK;  // [kSeamChunk][DK]
     float* vs = ks + kSeamChunk * DK;  // [kSeamChunk][DV]
-    float* gs = vs + kSeamChunk * DV;  // [kSeamChunk][DK] (GLA)
+    float* gs = vs + kSeamChunk * DV;  // [kSeamChunk][DK] (GLA, KDA)
     float* as = gs + kSeamChunk * DK;  // [kSeamChunk]
     float* bs = as + kSeamChunk;       // [kSeamChunk]
     const int LH = p.n_layers * p.n_heads;
@@ -43,25 +43,28 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) seam_simt_kernel(SeamParams
         stage_rows<DK>(qs, p.q, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
         stage_rows<DK>(ks, p.k, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
         stage_rows<DV>(vs, p.v, p.in_dtype, layer, t0, n, head, p.n_tokens, p.n_heads);
-        if (fam == kGLA) stage_rows<DK>(gs, p.g, kF32, layer, t0, n, head, p.n_tokens, p.n_heads);
-        if (fam == kGDN) {
-            stage_gate(as, p.alpha, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
-            stage_gate(bs, p.beta, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
-        }
+        if (fam == kGLA || fam == kKDA) stage_rows<DK>(gs, p.g, kF32, layer, t0, n, head, p.n_tokens, p.n_heads);
+        if (fam == kGDN || fam == kMAMBA2) stage_gate(as, p.alpha, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
+        if (fam == kGDN || fam == kKDA) stage_gate(bs, p.beta, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
         __syncthreads();
         if (c < DV) {
             for (int t = 0; t < n; ++t) {
                 const float* kt = ks + t * DK;
                 const float* qt = qs + t * DK;
                 const float vj = vs[t * DV + c];
-                if (fam == kGDN) {
+                if (fam == kGDN || fam == kKDA) {  // KDA: the per-channel gate first, then a = 1
+                    if (fam == kKDA) {
+                        const float* gt = gs + t * DK;
+#pragma unroll
+                        for (int i = 0; i < DK; ++i) col[i] *= gt[i];
+                    }
                     float u0 = 0.f, u1 = 0.f;
 #pragma unroll
                     for (int i = 0; i < DK; i += 2) {
                         u0 = fmaf(kt[i], col[i], u0);
                         u1 = fmaf(kt[i + 1], col[i + 1], u1);
                     }
-                    const float a = as[t], b = bs[t];
+                    const float a = fam == kKDA ? 1.f : as[t], b = bs[t];
                     const float w = b * (vj - a * (u0 + u1));
 #pragma unroll
                     for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], w, a * col[i]);
@@ -69,9 +72,10 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) seam_simt_kernel(SeamParams
                     const float* gt = gs + t * DK;
 #pragma unroll
                     for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, gt[i] * col[i]);
-                } else {
+                } else {  // RetNet (gamma), Mamba2 (a_t), vanilla (1)
+                    const float d = fam == kMAMBA2 ? as[t] : gm;
 #pragma unroll
-                    for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, gm * col[i]);
+                    for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, d * col[i]);
                 }
                 float o0 = 0.f, o1 = 0.f;
 #pragma unroll

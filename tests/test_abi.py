@@ -71,7 +71,7 @@ def test_struct_layout_matches_header(B, tmp_path):
 
 
 def test_status_strings_and_version(B):
-    assert B.hypic_version() == 110
+    assert B.hypic_version() == 120
     for code, name in enumerate(["HYPIC_OK", "HYPIC_ERR_INVALID_ARG", "HYPIC_ERR_UNSUPPORTED", "HYPIC_ERR_WORKSPACE",
                                  "HYPIC_ERR_CUDA", "HYPIC_ERR_TIMEOUT"]):
         assert B.lib.hypic_status_string(code).decode() == name
@@ -102,6 +102,11 @@ def base_build(B, family=0, d=128, n_seg=2, lengths=(64, 80)):
         a.gamma = fake(3)
     if family == 2:
         a.g = fake(3)
+    if family == 4:  # KDA: per-channel gate g and beta; dense T with exponent
+        a.g, a.beta = fake(3), fake(4)
+        a.T_exp_out = fake(6)
+    if family == 5:  # Mamba2: per-token decay in alpha; scalar T
+        a.alpha = fake(3)
     if family != 3:
         a.T_out = fake(5)
     a.S_out = fake(7)
@@ -113,7 +118,7 @@ def run_build(B, a, ws=1 << 20, ws_ptr=None):
 
 
 def test_build_valid_args_reach_workspace_check(B):
-    for fam in range(4):
+    for fam in range(6):
         a, keep = base_build(B, fam)
         need = B.hypic_build_workspace_size(a)
         assert need >= 256
@@ -167,6 +172,17 @@ def test_build_family_specific_rejections(B):
     a, _ = base_build(B, 2)
     a.g = None
     assert run_build(B, a) == B.ERR_INVALID_ARG
+    for mut in (lambda a: setattr(a, "g", None), lambda a: setattr(a, "beta", None),
+                lambda a: setattr(a, "alpha", fake(8)), lambda a: setattr(a, "T_exp_out", None),
+                lambda a: setattr(a, "dk", 64)):
+        a, _ = base_build(B, 4)
+        mut(a)
+        assert run_build(B, a) != B.OK   # KDA needs g, beta, T_exp_out, dk == dv; takes no alpha
+    for mut in (lambda a: setattr(a, "alpha", None), lambda a: setattr(a, "beta", fake(8)),
+                lambda a: setattr(a, "T_exp_out", fake(6)), lambda a: setattr(a, "g", fake(8))):
+        a, _ = base_build(B, 5)
+        mut(a)
+        assert run_build(B, a) == B.ERR_INVALID_ARG  # Mamba2 needs alpha only; scalar T, no exponent
 
 
 def test_build_empty_batch_is_ok_without_gpu(B):
