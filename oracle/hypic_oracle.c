@@ -246,16 +246,22 @@ int oracle_build(int family, int n_layers, int n_heads, int dk, int dv,
  * identity (vanilla, plain addition).  T_tab holds T_C in double with any
  * stored scale already applied; `naive` != 0 drops T entirely (the addition
  * strawman of [AB], "--pic-mode addition" in the README's PIC modes table).
+ * T_out (nullable, not with `naive` or vanilla) receives each chain's own
+ * transition, the ordered product T_{p_n} ... T_{p_1} (identity for an empty
+ * chain), in the family's T layout: with it the chain is itself a cached pair
+ * (T_out, S_out from a zero start) that composes like any other [AB].
  */
 int oracle_compose(int family, int n_layers, int n_heads, int dk, int dv, int n_pairs,
                    const double* T_tab, const double* S_tab,
                    int n_chains, const int* cu_chain, const int* seg_idx,
-                   const double* S0, double* S_out, int naive, int n_threads)
+                   const double* S0, double* S_out, int naive, int n_threads, double* T_out)
 {
     if (check_common(family, n_layers, n_heads, dk, dv) || n_chains < 0 || n_pairs < 0) return 1;
+    if (T_out && (naive || family == OR_VANILLA)) return 1;
     const long long LH = (long long)n_layers * n_heads;
     const long long n_items = (long long)n_chains * LH;
     const size_t dd = (size_t)dk * dv;
+    const size_t tn = dense_T(family) ? (size_t)dk * dk : (family == OR_GLA ? (size_t)dk : 1);
     int bad = 0;
 #ifdef _OPENMP
     if (n_threads > 0) omp_set_num_threads(n_threads);
@@ -266,12 +272,34 @@ int oracle_compose(int family, int n_layers, int n_heads, int dk, int dv, int n_
         const int r = (int)(it / LH);
         double* S = (double*)malloc(sizeof(double) * dd);
         double* N = (double*)malloc(sizeof(double) * dd);
-        if (!S || !N) { bad = 1; free(S); free(N); continue; }
+        double* Tc = (double*)malloc(sizeof(double) * tn * 2);  /* chain product, and its update */
+        if (!S || !N || !Tc) { bad = 1; free(S); free(N); free(Tc); continue; }
         if (S0) memcpy(S, S0 + (size_t)it * dd, sizeof(double) * dd);
         else memset(S, 0, sizeof(double) * dd);
+        if (dense_T(family)) {
+            memset(Tc, 0, sizeof(double) * tn);
+            for (int i = 0; i < dk; ++i) Tc[(size_t)i * dk + i] = 1.0;
+        } else {
+            for (size_t e = 0; e < tn; ++e) Tc[e] = 1.0;
+        }
         for (int j = cu_chain[r]; j < cu_chain[r + 1]; ++j) {
             const int p = seg_idx[j];
             if (p < 0 || p >= n_pairs) { bad = 1; break; }
+            if (T_out) { /* Tc <- T_p Tc */
+                const double* Tp = T_tab + ((size_t)p * LH + lh) * tn;
+                double* Tn = Tc + tn;
+                if (dense_T(family)) {
+                    for (int i = 0; i < dk; ++i)
+                        for (int c = 0; c < dk; ++c) {
+                            double acc = 0.0;
+                            for (int m = 0; m < dk; ++m) acc += Tp[(size_t)i * dk + m] * Tc[(size_t)m * dk + c];
+                            Tn[(size_t)i * dk + c] = acc;
+                        }
+                } else {
+                    for (size_t e = 0; e < tn; ++e) Tn[e] = Tp[e] * Tc[e];
+                }
+                memcpy(Tc, Tn, sizeof(double) * tn);
+            }
             const double* Si = S_tab + ((size_t)p * LH + lh) * dd;
             if (naive || family == OR_VANILLA) {
                 for (size_t e = 0; e < dd; ++e) N[e] = S[e];
@@ -294,7 +322,8 @@ int oracle_compose(int family, int n_layers, int n_heads, int dk, int dv, int n_
             for (size_t e = 0; e < dd; ++e) S[e] = N[e] + Si[e];
         }
         memcpy(S_out + (size_t)it * dd, S, sizeof(double) * dd);
-        free(S); free(N);
+        if (T_out) memcpy(T_out + (size_t)it * tn, Tc, sizeof(double) * tn);
+        free(S); free(N); free(Tc);
     }
     return bad;
 }
@@ -352,4 +381,4 @@ int oracle_seam(int family, int n_layers, int n_heads, int dk, int dv,
     return bad;
 }
 
-int oracle_version(void) { return 2; }
+int oracle_version(void) { return 3; }

@@ -59,7 +59,7 @@ def _load():
         I = ctypes.c_int
         LL = ctypes.c_longlong
         lib.oracle_build.argtypes = [I, I, I, I, I, I, P, P, LL, P, P, P, P, P, P, P, P, I]
-        lib.oracle_compose.argtypes = [I, I, I, I, I, I, P, P, I, P, P, P, P, I, I]
+        lib.oracle_compose.argtypes = [I, I, I, I, I, I, P, P, I, P, P, P, P, I, I, P]
         lib.oracle_seam.argtypes = [I, I, I, I, I, I, P, LL, P, P, P, P, P, P, P, P, P, P, I]
         for f in (lib.oracle_build, lib.oracle_compose, lib.oracle_seam):
             f.restype = ctypes.c_int
@@ -128,12 +128,14 @@ def build_pairs(family, k, v, cu_seqlens, *, alpha=None, beta=None, gamma=None, 
     return T, S
 
 
-def compose(family, T_tab, S_tab, cu_chain, seg_idx, S0=None, *, naive=False, n_threads=None):
+def compose(family, T_tab, S_tab, cu_chain, seg_idx, S0=None, *, naive=False, n_threads=None, want_T=False):
     """Chain compose S <- T_i S + S_i (double precision).
 
     T_tab / S_tab: [n_pairs][n_layers][n_heads]... as returned by build_pairs
     (T with any storage scale already applied).  Returns S_end
-    [n_chains][n_layers][n_heads][dk][dv].
+    [n_chains][n_layers][n_heads][dk][dv]; with ``want_T`` it returns
+    (S_end, T_chain), T_chain being each chain's transition product
+    T_{p_n} ... T_{p_1} in the family's T layout.
     """
     fam = FAMILIES[family]
     S_tab = _f64(S_tab)
@@ -144,12 +146,16 @@ def compose(family, T_tab, S_tab, cu_chain, seg_idx, S0=None, *, naive=False, n_
     n_chains = cu.shape[0] - 1
     S0 = _f64(S0)
     out = np.zeros((n_chains, n_layers, n_heads, dk, dv))
+    T_out = None
+    if want_T:
+        shape = {0: (dk, dk), 4: (dk, dk), 1: (), 5: (), 2: (dk,)}[fam]
+        T_out = np.zeros((n_chains, n_layers, n_heads) + shape)
     rc = _load().oracle_compose(fam, n_layers, n_heads, dk, dv, n_pairs, _ptr(T_tab), _ptr(S_tab),
                                 n_chains, _ptr(cu), _ptr(idx), _ptr(S0), _ptr(out), int(bool(naive)),
-                                n_threads or default_threads())
+                                n_threads or default_threads(), _ptr(T_out))
     if rc:
         raise RuntimeError("oracle_compose failed")
-    return out
+    return (out, T_out) if want_T else out
 
 
 def seam(family, q, k, v, cu_seam, state_in=None, *, alpha=None, beta=None, gamma=None, g=None,

@@ -437,3 +437,36 @@ def test_mamba2_closed_forms_and_retnet_special_case():
     Tr, Sr = orc.build_pairs("retnet", one_head(k), one_head(v), [0, L], gamma=np.array([[gm]]))
     np.testing.assert_allclose(Tm, Tr, rtol=1e-13)
     np.testing.assert_allclose(Sm, Sr, atol=1e-13)
+
+
+# ------------------------------------------------- chain transition (T out) ----
+
+@pytest.mark.parametrize("fam", ["gdn", "retnet", "gla", "kda", "mamba2"])
+def test_chain_transition_is_the_pair_of_the_concatenation(fam):
+    """A chain's own transition product is the T_C of the concatenated
+    segments (one-pass build), its zero-start S is their S(C|0), so the chain
+    is itself a cached pair: from a start S0 it gives T_chain S0 + S_chain, and
+    pairs of chains compose like pairs (tree reduction).  An empty chain is
+    the identity pair."""
+    rng = np.random.default_rng(41)
+    d, lens = 8, [20, 7, 33, 15]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    k, v, kw = _family_inputs(fam, rng, int(cu[-1]), d)
+    T_all, S_all = orc.build_pairs(fam, k, v, [0, int(cu[-1])], **kw)
+    T, S = orc.build_pairs(fam, k, v, cu, **kw)
+    S_c, T_c = orc.compose(fam, T, S, [0, 4, 4], [0, 1, 2, 3], want_T=True)
+    np.testing.assert_allclose(T_c[0], T_all[0], atol=1e-13)
+    np.testing.assert_allclose(S_c[0], S_all[0], atol=1e-12)
+    eye = np.broadcast_to(np.eye(d), T_c[1].shape) if fam in ("gdn", "kda") else np.ones_like(T_c[1])
+    np.testing.assert_array_equal(T_c[1], eye)
+    assert np.all(S_c[1] == 0)
+    S0 = rng.standard_normal((1,) + S.shape[1:])
+    S_from = orc.compose(fam, T, S, [0, 4], [0, 1, 2, 3], S0=S0)
+    TS0 = np.einsum("lhij,lhjc->lhic", T_c[0], S0[0]) if fam in ("gdn", "kda") else (
+        T_c[0][..., None] * S0[0] if fam == "gla" else T_c[0][..., None, None] * S0[0])
+    np.testing.assert_allclose(S_from[0], TS0 + S_c[0], atol=1e-12)
+    # pair of pairs: (p0 p1) and (p2 p3) as two chains, then their two pairs
+    S_h, T_h = orc.compose(fam, T, S, [0, 2, 4], [0, 1, 2, 3], want_T=True)
+    S_t, T_t = orc.compose(fam, T_h, S_h, [0, 2], [0, 1], want_T=True)
+    np.testing.assert_allclose(T_t[0], T_all[0], atol=1e-13)
+    np.testing.assert_allclose(S_t[0], S_all[0], atol=1e-12)
