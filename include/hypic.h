@@ -73,7 +73,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_VERSION 120 /* 1.2.0: KDA and MAMBA2 families */
+#define HYPIC_VERSION 130 /* 1.3.0: compose returns the chain's own transition (T_out) */
 
 #if defined(__GNUC__)
 #define HYPIC_API __attribute__((visibility("default")))
@@ -176,6 +176,15 @@ HYPIC_API hypic_status hypic_segment_build(const hypic_build_args* args, void* w
  *   T_tab [n_pairs][n_layers][n_heads](...) as T_out above; S_tab
  *   [n_pairs][n_layers][n_heads][dk][dv].
  * S_out [n_chains][n_layers][n_heads][dk][dv] must not overlap the tables or S0.
+ * T_out (optional, NULL for VANILLA) receives each chain's own transition
+ * T_chain = T_{p_n} ... T_{p_1} (the identity for an empty chain), laid out
+ * like the build's T_out with leading dims [n_chains][n_layers][n_heads];
+ * GDN and KDA also need T_exp_out [n_chains][n_layers][n_heads] int32
+ * (T_chain = T_out * 2^T_exp_out).  With S0 == NULL the chain's result is
+ * then itself a cached pair (T_out, S_out) of the concatenated segments, so
+ * chains of chains compose like pairs ([AIBASE] composition law applied to a
+ * tree of segments).  Neither may overlap an input or S_out.  With T_out the
+ * dense families run on CUDA cores at every d.
  * Supported: dk, dv in {16, 32, 64, 128}; GDN and KDA require dk == dv.
  */
 typedef struct {
@@ -192,6 +201,8 @@ typedef struct {
     const int32_t* seg_idx_host;    /* host copy (validation) */
     const float* S0;                /* device [n_chains][..] or NULL */
     float* S_out;
+    float* T_out;                   /* device, optional: each chain's own transition (above) */
+    int32_t* T_exp_out;             /* device [n_chains][n_layers][n_heads]: with T_out, GDN / KDA */
 } hypic_compose_args;
 
 HYPIC_API hypic_status hypic_compose(const hypic_compose_args* args, hypic_stream_t stream);

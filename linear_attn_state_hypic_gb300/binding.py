@@ -39,7 +39,7 @@ class ComposeArgs(ctypes.Structure):
     _fields_ = [("family", _I), ("n_layers", _I), ("n_heads", _I), ("dk", _I), ("dv", _I), ("n_pairs", _I),
                 ("T_tab", _P), ("T_exp_tab", _P), ("S_tab", _P), ("n_chains", _I),
                 ("cu_chain", _P), ("cu_chain_host", _P), ("seg_idx", _P), ("seg_idx_host", _P),
-                ("S0", _P), ("S_out", _P)]
+                ("S0", _P), ("S_out", _P), ("T_out", _P), ("T_exp_out", _P)]
 
 
 class SeamArgs(ctypes.Structure):
@@ -238,7 +238,7 @@ def segment_build(family, k, v, cu_seqlens, *, alpha=None, beta=None, gamma=None
 
 
 def compose_args(family, S_tab, cu_chain, seg_idx, *, T_tab=None, T_exp_tab=None, S0=None, S_out=None,
-                 cu_chain_dev=None, seg_idx_dev=None):
+                 T_out=None, T_exp_out=None, cu_chain_dev=None, seg_idx_dev=None):
     fam = FAMILY[family] if isinstance(family, str) else family
     cu = _host_i32(cu_chain)
     idx = _host_i32(seg_idx)
@@ -252,21 +252,31 @@ def compose_args(family, S_tab, cu_chain, seg_idx, *, T_tab=None, T_exp_tab=None
     a.cu_chain, a.cu_chain_host = _ptr(cu_d), _hptr(cu)
     a.seg_idx, a.seg_idx_host = _ptr(idx_d), _hptr(idx) if len(idx) else None
     a.S0, a.S_out = _ptr(S0), _ptr(S_out)
+    a.T_out, a.T_exp_out = _ptr(T_out), _ptr(T_exp_out)
     return a, (cu, idx, cu_d, idx_d)
 
 
 def compose(family, S_tab, cu_chain, seg_idx, *, T_tab=None, T_exp_tab=None, S0=None, out=None, stream=None,
-            cu_chain_dev=None, seg_idx_dev=None):
-    """End state of every chain via hypic_compose: [n_chains][L][H][dk][dv]."""
+            cu_chain_dev=None, seg_idx_dev=None, want_T=False):
+    """End state of every chain via hypic_compose: [n_chains][L][H][dk][dv].
+
+    With ``want_T`` returns (S_end, T_chain, T_chain_exp): each chain's own
+    transition product, laid out like the build's T (T_chain_exp only for the
+    dense families, else None)."""
     import torch
+    fam = FAMILY[family] if isinstance(family, str) else family
     n_chains = len(cu_chain) - 1
     if out is None:
         out = torch.empty((n_chains,) + tuple(S_tab.shape[1:]), dtype=torch.float32, device=S_tab.device)
+    T_out = T_exp_out = None
+    if want_T:
+        T_out, T_exp_out, _ = alloc_build_outputs(fam, n_chains, S_tab.shape[1], S_tab.shape[2], S_tab.shape[3],
+                                                  S_tab.shape[4], S_tab.device)
     a, keep = compose_args(family, S_tab, cu_chain, seg_idx, T_tab=T_tab, T_exp_tab=T_exp_tab, S0=S0, S_out=out,
-                           cu_chain_dev=cu_chain_dev, seg_idx_dev=seg_idx_dev)
+                           T_out=T_out, T_exp_out=T_exp_out, cu_chain_dev=cu_chain_dev, seg_idx_dev=seg_idx_dev)
     _check(hypic_compose(a, _stream(stream)))
     del keep
-    return out
+    return (out, T_out, T_exp_out) if want_T else out
 
 
 def seam_args(family, q, k, v, cu_seam, *, alpha=None, beta=None, gamma=None, g=None, state_in=None,

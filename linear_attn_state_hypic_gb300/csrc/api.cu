@@ -261,7 +261,12 @@ hypic_status check_compose(const hypic_compose_args* a) {
     if (!dense_T(a->family) && a->T_exp_tab)
         return fail(HYPIC_ERR_INVALID_ARG, "T_exp_tab must be NULL for %s", fam_name(a->family));
     if (a->n_chains > 0 && !a->S_out) return fail(HYPIC_ERR_INVALID_ARG, "S_out required");
-    const void* ptrs[] = {a->T_tab, a->T_exp_tab, a->S_tab, a->S0, a->S_out};
+    if (a->family == HYPIC_VANILLA && a->T_out) return fail(HYPIC_ERR_INVALID_ARG, "T_out must be NULL for VANILLA");
+    if (a->T_exp_out && !(a->T_out && dense_T(a->family)))
+        return fail(HYPIC_ERR_INVALID_ARG, "T_exp_out goes with T_out for GDN / KDA only");
+    if (a->T_out && dense_T(a->family) && !a->T_exp_out)
+        return fail(HYPIC_ERR_INVALID_ARG, "T_out for %s needs T_exp_out", fam_name(a->family));
+    const void* ptrs[] = {a->T_tab, a->T_exp_tab, a->S_tab, a->S0, a->S_out, a->T_out, a->T_exp_out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
     const size_t LH = (size_t)a->n_layers * a->n_heads;
@@ -272,6 +277,16 @@ hypic_status check_compose(const hypic_compose_args* a) {
         overlap(a->S_out, out_b, a->T_exp_tab, sizeof(int32_t) * LH * a->n_pairs) ||
         overlap(a->S_out, out_b, a->S0, out_b))
         return fail(HYPIC_ERR_INVALID_ARG, "S_out overlaps an input");
+    if (a->T_out) {  // the chain transition outputs overlap nothing else
+        const size_t tb = T_bytes_per_obj(a->family, a->dk) * LH * a->n_chains, eb = sizeof(int32_t) * LH * a->n_chains;
+        const void* ins[] = {a->T_tab, a->T_exp_tab, a->S_tab, a->S0, a->S_out};
+        const size_t in_b[] = {T_bytes_per_obj(a->family, a->dk) * LH * a->n_pairs, sizeof(int32_t) * LH * a->n_pairs,
+                               state * a->n_pairs, out_b, out_b};
+        for (int i = 0; i < 5; ++i)
+            if (overlap(a->T_out, tb, ins[i], in_b[i]) || overlap(a->T_exp_out, eb, ins[i], in_b[i]))
+                return fail(HYPIC_ERR_INVALID_ARG, "T_out / T_exp_out overlaps another buffer");
+        if (overlap(a->T_out, tb, a->T_exp_out, eb)) return fail(HYPIC_ERR_INVALID_ARG, "T_out overlaps T_exp_out");
+    }
     return HYPIC_OK;
 }
 
@@ -299,6 +314,8 @@ extern "C" hypic_status hypic_compose(const hypic_compose_args* args, hypic_stre
     p.seg_idx = args->seg_idx;
     p.S0 = args->S0;
     p.S_out = args->S_out;
+    p.T_out = args->T_out;
+    p.T_exp_out = args->T_exp_out;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = compose_tc_supported(p) ? launch_compose_tc(p, err, s) : launch_compose_simt(p, err, s);
     if (e != cudaSuccess) return cuda_fail(e, "compose launch");
@@ -397,6 +414,8 @@ hypic_compose_args chain_compose_view(const hypic_chain_args* a) {
     c.seg_idx_host = a->seg_idx_host;
     c.S0 = a->S0;
     c.S_out = a->S_out;
+    c.T_out = nullptr;
+    c.T_exp_out = nullptr;
     return c;
 }
 

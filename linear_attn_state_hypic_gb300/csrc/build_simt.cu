@@ -49,18 +49,6 @@ cudaError_t launch_build_plan(const BuildParams& p, void* workspace, cudaStream_
     return cudaGetLastError();
 }
 
-// Block-wide max over the first `nthreads_active` threads' values (others pass 0).
-__device__ __forceinline__ float block_max(float v, float* red) {
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[w] = v;
-    __syncthreads();
-    float m = 0.f;
-    for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
-    return m;
-}
-
 // ------------------------------------------------------ GDN, KDA (SIMT) --
 // Thread c < DK owns column c of T (starts as e_c); thread DK + j owns column j
 // of S (starts at 0).  Per token: u = k^T col, col <- a (col - b u k) + b v_j k

@@ -9,6 +9,19 @@ namespace hypic {
 enum : int { kGDN = 0, kRETNET = 1, kGLA = 2, kVANILLA = 3, kKDA = 4, kMAMBA2 = 5 };
 enum : int { kF32 = 0, kBF16 = 1 };
 
+// Max of v over the block (every thread takes part; `red` holds one float per
+// warp).  Threads with nothing to contribute pass 0.
+__device__ __forceinline__ float block_max(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float m = 0.f;
+    for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
+    return m;
+}
+
 // Codes written to the device error word (first writer wins).
 enum : unsigned { kErrNone = 0, kErrTimeout = 1, kErrBadIndex = 2 };
 

@@ -13,21 +13,29 @@
 
 namespace hypic {
 
-// GDN: dense T_p (dk x dk, stored as mantissa * 2^exp).  The new column is
-// written to the thread's own column of a shared buffer and read back, which
-// keeps only one column in registers.
+// GDN, KDA: dense T_p (dk x dk, stored as mantissa * 2^exp).  The new column
+// is written to the thread's own column of a shared buffer and read back,
+// which keeps only one column in registers.  With T_out, threads D..2D-1 also
+// carry the chain's own transition T_chain <- T_p T_chain (from I), one column
+// each, renormalised by a power of two after every step (its exponent
+// accumulated like the build's).
 template <int D>
-__global__ void __launch_bounds__(D) compose_gdn_simt_kernel(ComposeParams p, unsigned* err) {
+__global__ void __launch_bounds__(2 * D) compose_gdn_simt_kernel(ComposeParams p, unsigned* err) {
     extern __shared__ float sm[];
     float* Ts = sm;          // [D][D]
     float* Sn = Ts + D * D;  // [D][D], column c private to thread c
+    float* Tn = Sn + D * D;  // [D][D] (T_chain, with T_out)
+    float* red = Tn + (p.T_out ? D * D : 0);  // [8]
+    const bool want_T = p.T_out != nullptr;
     const int LH = p.n_layers * p.n_heads;
     const int chain = blockIdx.x / LH, lh = blockIdx.x % LH;
-    const int c = threadIdx.x;
+    const bool isT = threadIdx.x >= D;
+    const int c = isT ? threadIdx.x - D : threadIdx.x;
     const int64_t obj = (int64_t)chain * LH + lh;
     float col[D];
 #pragma unroll
-    for (int i = 0; i < D; ++i) col[i] = p.S0 ? p.S0[(obj * D + i) * D + c] : 0.f;
+    for (int i = 0; i < D; ++i) col[i] = isT ? (i == c ? 1.f : 0.f) : p.S0 ? p.S0[(obj * D + i) * D + c] : 0.f;
+    int texp = 0;
     const int j0 = p.cu_chain[chain], j1 = p.cu_chain[chain + 1];
     for (int j = j0; j < j1; ++j) {
         const int pi = p.seg_idx[j];
@@ -38,7 +46,7 @@ __global__ void __launch_bounds__(D) compose_gdn_simt_kernel(ComposeParams p, un
         const int64_t pobj = (int64_t)pi * LH + lh;
         const float4* Tg = reinterpret_cast<const float4*>(p.T_tab + pobj * D * D);
         __syncthreads();
-        for (int e = c; e < D * D / 4; e += D) reinterpret_cast<float4*>(Ts)[e] = Tg[e];
+        for (int e = threadIdx.x; e < D * D / 4; e += blockDim.x) reinterpret_cast<float4*>(Ts)[e] = Tg[e];
         __syncthreads();
         const int ex = p.T_exp_tab ? p.T_exp_tab[pobj] : 0;
         const float* Sp = p.S_tab + pobj * D * D;
@@ -52,26 +60,56 @@ __global__ void __launch_bounds__(D) compose_gdn_simt_kernel(ComposeParams p, un
                 a2 = fmaf(Ti[m + 2], col[m + 2], a2);
                 a3 = fmaf(Ti[m + 3], col[m + 3], a3);
             }
-            Sn[i * D + c] = ldexpf((a0 + a1) + (a2 + a3), ex) + Sp[i * D + c];
+            const float acc = (a0 + a1) + (a2 + a3);
+            if (isT)
+                Tn[i * D + c] = acc;
+            else
+                Sn[i * D + c] = ldexpf(acc, ex) + Sp[i * D + c];
         }
 #pragma unroll
-        for (int i = 0; i < D; ++i) col[i] = Sn[i * D + c];
-    }
-    float* out = p.S_out + obj * D * D;
+        for (int i = 0; i < D; ++i) col[i] = (isT ? Tn : Sn)[i * D + c];
+        if (want_T) {
+            float m = 0.f;
+            if (isT)
 #pragma unroll
-    for (int i = 0; i < D; ++i) out[i * D + c] = col[i];
+                for (int i = 0; i < D; ++i) m = fmaxf(m, fabsf(col[i]));
+            m = block_max(m, red);
+            int e = (m > 0.f && isfinite(m)) ? ilogbf(m) : 0;
+            if (isT && e != 0)
+#pragma unroll
+                for (int i = 0; i < D; ++i) col[i] = ldexpf(col[i], -e);
+            texp += ex + e;
+        }
+    }
+    if (isT) {
+        float* To = p.T_out + obj * D * D;
+#pragma unroll
+        for (int i = 0; i < D; ++i) To[i * D + c] = col[i];
+        if (c == 0) p.T_exp_out[obj] = texp;
+    } else {
+        float* out = p.S_out + obj * D * D;
+#pragma unroll
+        for (int i = 0; i < D; ++i) out[i * D + c] = col[i];
+    }
 }
 
-// RetNet (scalar T), GLA (row scaling by a dk-vector), vanilla (addition).
+// RetNet, Mamba2 (scalar T), GLA (row scaling by a dk-vector), vanilla
+// (addition).  Thread c < DV owns column c of S; with T_out, the chain's own
+// transition is the product of the T_p in double (thread 0 for a scalar,
+// thread i < DK for entry i of GLA's vector).
 template <int DK, int DV>
-__global__ void __launch_bounds__(DV) compose_decay_simt_kernel(ComposeParams p, unsigned* err) {
+__global__ void __launch_bounds__(DK > DV ? DK : DV) compose_decay_simt_kernel(ComposeParams p, unsigned* err) {
     const int LH = p.n_layers * p.n_heads;
     const int chain = blockIdx.x / LH, lh = blockIdx.x % LH;
     const int c = threadIdx.x;
+    const bool scol = c < DV;
+    const bool scalar = p.family == kRETNET || p.family == kMAMBA2;
+    const bool tcol = p.T_out && (scalar ? c == 0 : (p.family == kGLA && c < DK));
     const int64_t obj = (int64_t)chain * LH + lh;
     float col[DK];
 #pragma unroll
-    for (int i = 0; i < DK; ++i) col[i] = p.S0 ? p.S0[(obj * DK + i) * DV + c] : 0.f;
+    for (int i = 0; i < DK; ++i) col[i] = (p.S0 && scol) ? p.S0[(obj * DK + i) * DV + c] : 0.f;
+    double tprod = 1.0;
     const int j0 = p.cu_chain[chain], j1 = p.cu_chain[chain + 1];
     for (int j = j0; j < j1; ++j) {
         const int pi = p.seg_idx[j];
@@ -81,6 +119,8 @@ __global__ void __launch_bounds__(DV) compose_decay_simt_kernel(ComposeParams p,
         }
         const int64_t pobj = (int64_t)pi * LH + lh;
         const float* Sp = p.S_tab + pobj * DK * DV;
+        if (tcol) tprod *= (double)(scalar ? p.T_tab[pobj] : p.T_tab[pobj * DK + c]);
+        if (!scol) continue;
         if (p.family == kRETNET || p.family == kMAMBA2) {
             const float t = p.T_tab[pobj];
 #pragma unroll
@@ -94,6 +134,8 @@ __global__ void __launch_bounds__(DV) compose_decay_simt_kernel(ComposeParams p,
             for (int i = 0; i < DK; ++i) col[i] += Sp[i * DV + c];
         }
     }
+    if (tcol) p.T_out[scalar ? obj : obj * DK + c] = (float)tprod;
+    if (!scol) return;
     float* out = p.S_out + obj * DK * DV;
 #pragma unroll
     for (int i = 0; i < DK; ++i) out[i * DV + c] = col[i];
@@ -105,16 +147,16 @@ static cudaError_t launch_compose_dims(const ComposeParams& p, unsigned* err, cu
     if (grid == 0) return cudaSuccess;
     if (p.family == kGDN || p.family == kKDA) {
         if constexpr (DK == DV) {
-            const size_t smem = sizeof(float) * 2 * DK * DK;
+            const size_t smem = sizeof(float) * ((p.T_out ? 3 : 2) * DK * DK + 8);
             auto kern = compose_gdn_simt_kernel<DK>;
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            kern<<<(unsigned)grid, DK, smem, s>>>(p, err);
+            kern<<<(unsigned)grid, p.T_out ? 2 * DK : DK, smem, s>>>(p, err);
         } else {
             return cudaErrorInvalidValue;
         }
     } else {
-        compose_decay_simt_kernel<DK, DV><<<(unsigned)grid, DV, 0, s>>>(p, err);
+        compose_decay_simt_kernel<DK, DV><<<(unsigned)grid, DK > DV ? DK : DV, 0, s>>>(p, err);
     }
     return cudaGetLastError();
 }

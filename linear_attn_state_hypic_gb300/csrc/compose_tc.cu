@@ -718,7 +718,7 @@ bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const float
 }  // namespace
 
 bool compose_tc_supported(const ComposeParams& p) {
-    return (p.family == kGDN || p.family == kKDA) && p.dk == kD && p.dv == kD && p.n_pairs > 0 &&
+    return (p.family == kGDN || p.family == kKDA) && !p.T_out && p.dk == kD && p.dv == kD && p.n_pairs > 0 &&
            (int64_t)p.n_pairs * p.n_layers * p.n_heads * kD < INT32_MAX && encode_fn() != nullptr;
 }
 

@@ -31,6 +31,8 @@ struct ComposeParams {
     const int32_t* seg_idx;
     const float* S0;
     float* S_out;
+    float* T_out = nullptr;        // optional: each chain's own transition (T_chain)
+    int32_t* T_exp_out = nullptr;  // its exponent (dense families)
 };
 
 struct SeamParams {

@@ -71,7 +71,7 @@ def test_struct_layout_matches_header(B, tmp_path):
 
 
 def test_status_strings_and_version(B):
-    assert B.hypic_version() == 120
+    assert B.hypic_version() == 130
     for code, name in enumerate(["HYPIC_OK", "HYPIC_ERR_INVALID_ARG", "HYPIC_ERR_UNSUPPORTED", "HYPIC_ERR_WORKSPACE",
                                  "HYPIC_ERR_CUDA", "HYPIC_ERR_TIMEOUT"]):
         assert B.lib.hypic_status_string(code).decode() == name
@@ -213,6 +213,10 @@ def base_compose(B, family=0, d=128, chains=((0, 1), (1,))):
     (lambda a, k: setattr(a, "S0", fake(6)), 1),         # output overlaps S0
     (lambda a, k: setattr(a, "dv", 64), 2),
     (lambda a, k: setattr(a, "S_tab", fake(2) + 4), 1),
+    (lambda a, k: setattr(a, "T_out", fake(8)), 1),           # GDN T_out needs T_exp_out
+    (lambda a, k: setattr(a, "T_exp_out", fake(9)), 1),       # ... and T_exp_out needs T_out
+    (lambda a, k: (setattr(a, "T_out", fake(1)), setattr(a, "T_exp_out", fake(9))), 1),  # T_out overlaps T_tab
+    (lambda a, k: (setattr(a, "T_out", fake(8)), setattr(a, "T_exp_out", fake(6))), 1),  # T_exp_out overlaps S_out
 ])
 def test_compose_rejections(B, mutate, status):
     a, keep = base_compose(B)
@@ -227,6 +231,12 @@ def test_compose_vanilla_rejects_T(B):
     a, keep = base_compose(B, 1)
     a.T_exp_tab = fake(7)
     assert B.hypic_compose(a, None) == B.ERR_INVALID_ARG
+    a, keep = base_compose(B, 3)
+    a.T_out = fake(8)
+    assert B.hypic_compose(a, None) == B.ERR_INVALID_ARG   # vanilla has no transition
+    a, keep = base_compose(B, 5)
+    a.T_out, a.T_exp_out = fake(8), fake(9)
+    assert B.hypic_compose(a, None) == B.ERR_INVALID_ARG   # scalar T: no exponent
 
 
 def base_seam(B, family=0, d=128, lens=(8, 8)):
