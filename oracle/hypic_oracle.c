@@ -381,4 +381,73 @@ int oracle_seam(int family, int n_layers, int n_heads, int dk, int dv,
     return bad;
 }
 
-int oracle_version(void) { return 3; }
+/* ------------------------------------------------------------ re-rotation -- */
+
+/*
+ * State re-rotation for variants whose keys carry RoPE ([AB]: the "state
+ * re-rotation" patch).  The page names the patch only; this restates it from
+ * the recurrences.  A segment moved by delta positions sees every key as
+ * R k, R = R(delta) the rotary rotation; for a family whose per-token
+ * transition is built from k k^T and scalars (GDN, RetNet, Mamba2, vanilla)
+ * that maps each transition A to R A R^T and each write k v^T to R k v^T, so
+ * the cached pair becomes (R T R^T, R S).  R acts on the first rotary_dim
+ * features in rotate-half pairs: for i < h = rotary_dim / 2 the pair
+ * (x_i, x_{i+h}) turns by the angle delta * base^(-2i / rotary_dim).
+ * R is formed here as an explicit dk x dk matrix and applied by plain matrix
+ * products.  T (dense families only, else NULL) and S are rewritten in place:
+ *   T [n_pairs][n_layers][n_heads][dk][dk], S [...][dk][dv], delta [n_pairs].
+ */
+int oracle_rope(int family, int n_layers, int n_heads, int dk, int dv, int n_pairs,
+                int rotary_dim, double base, const long long* delta, double* T, double* S)
+{
+    if (check_common(family, n_layers, n_heads, dk, dv) || n_pairs < 0) return 1;
+    if (family == OR_GLA || family == OR_KDA) return 1; /* per-channel gates do not commute with R */
+    if (rotary_dim < 2 || rotary_dim > dk || (rotary_dim & 1)) return 1;
+    if (dense_T(family) != (T != NULL)) return 1;
+    const long long LH = (long long)n_layers * n_heads;
+    const int h = rotary_dim / 2;
+    int bad = 0;
+    for (int p = 0; p < n_pairs && !bad; ++p) {
+        double* R = (double*)calloc((size_t)dk * dk, sizeof(double));
+        double* tmp = (double*)malloc(sizeof(double) * (size_t)dk * (dk > dv ? dk : dv));
+        if (!R || !tmp) { bad = 1; free(R); free(tmp); break; }
+        for (int i = 0; i < dk; ++i) R[(size_t)i * dk + i] = 1.0;
+        for (int i = 0; i < h; ++i) {
+            const double a = (double)delta[p] * pow(base, -2.0 * i / rotary_dim);
+            const double c = cos(a), sn = sin(a);
+            R[(size_t)i * dk + i] = c;
+            R[(size_t)i * dk + i + h] = -sn;
+            R[(size_t)(i + h) * dk + i] = sn;
+            R[(size_t)(i + h) * dk + i + h] = c;
+        }
+        for (long long lh = 0; lh < LH; ++lh) {
+            double* Sp = S + ((size_t)p * LH + lh) * (size_t)dk * dv;
+            for (int i = 0; i < dk; ++i) /* tmp = R S */
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int m = 0; m < dk; ++m) acc += R[(size_t)i * dk + m] * Sp[(size_t)m * dv + j];
+                    tmp[(size_t)i * dv + j] = acc;
+                }
+            memcpy(Sp, tmp, sizeof(double) * (size_t)dk * dv);
+            if (T) {
+                double* Tp = T + ((size_t)p * LH + lh) * (size_t)dk * dk;
+                for (int i = 0; i < dk; ++i) /* tmp = R T */
+                    for (int j = 0; j < dk; ++j) {
+                        double acc = 0.0;
+                        for (int m = 0; m < dk; ++m) acc += R[(size_t)i * dk + m] * Tp[(size_t)m * dk + j];
+                        tmp[(size_t)i * dk + j] = acc;
+                    }
+                for (int i = 0; i < dk; ++i) /* T = tmp R^T */
+                    for (int j = 0; j < dk; ++j) {
+                        double acc = 0.0;
+                        for (int m = 0; m < dk; ++m) acc += tmp[(size_t)i * dk + m] * R[(size_t)j * dk + m];
+                        Tp[(size_t)i * dk + j] = acc;
+                    }
+            }
+        }
+        free(R); free(tmp);
+    }
+    return bad;
+}
+
+int oracle_version(void) { return 4; }

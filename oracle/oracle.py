@@ -61,7 +61,8 @@ def _load():
         lib.oracle_build.argtypes = [I, I, I, I, I, I, P, P, LL, P, P, P, P, P, P, P, P, I]
         lib.oracle_compose.argtypes = [I, I, I, I, I, I, P, P, I, P, P, P, P, I, I, P]
         lib.oracle_seam.argtypes = [I, I, I, I, I, I, P, LL, P, P, P, P, P, P, P, P, P, P, I]
-        for f in (lib.oracle_build, lib.oracle_compose, lib.oracle_seam):
+        lib.oracle_rope.argtypes = [I, I, I, I, I, I, I, ctypes.c_double, P, P, P]
+        for f in (lib.oracle_build, lib.oracle_compose, lib.oracle_seam, lib.oracle_rope):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -185,6 +186,22 @@ def seam(family, q, k, v, cu_seam, state_in=None, *, alpha=None, beta=None, gamm
 
 
 # -------------------------------------------------------------- utilities --
+
+def rope(family, T, S, delta, *, rotary_dim=None, base=10000.0):
+    """Cached pairs re-rotated for a shift of delta[p] positions (the state
+    re-rotation patch, restated in hypic_oracle.c): returns (R T R^T, R S) in
+    float64 (T None for the scalar families and vanilla)."""
+    fam = FAMILIES[family]
+    S = np.array(S, dtype=np.float64, copy=True, order="C")
+    n_pairs, n_layers, n_heads, dk, dv = S.shape
+    T = None if T is None else np.array(T, dtype=np.float64, copy=True, order="C")
+    d = np.ascontiguousarray(np.asarray(delta, dtype=np.int64))
+    rc = _load().oracle_rope(fam, n_layers, n_heads, dk, dv, n_pairs, int(rotary_dim or dk), float(base),
+                             _ptr(d), _ptr(T), _ptr(S))
+    if rc:
+        raise RuntimeError("oracle_rope failed")
+    return T, S
+
 
 def rel_fro(x, ref, axes):
     """Relative Frobenius error ||x - ref|| / ||ref|| per object, in fp64.

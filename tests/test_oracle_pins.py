@@ -470,3 +470,70 @@ def test_chain_transition_is_the_pair_of_the_concatenation(fam):
     S_t, T_t = orc.compose(fam, T_h, S_h, [0, 2], [0, 1], want_T=True)
     np.testing.assert_allclose(T_t[0], T_all[0], atol=1e-13)
     np.testing.assert_allclose(S_t[0], S_all[0], atol=1e-12)
+
+
+# ------------------------------------------------------- RoPE re-rotation ----
+
+def rope_matrix(d, rdim, delta, base=10000.0):
+    """The rotary rotation as an explicit matrix, built from its definition
+    x -> x cos(a) + rotate_half(x) sin(a) on the first rdim features."""
+    h = rdim // 2
+    ang = delta * base ** (-2.0 * np.arange(h) / rdim)
+    R = np.eye(d)
+    for i in range(h):
+        x = np.zeros(d); x[i] = 1.0
+        y = np.zeros(d); y[i + h] = 1.0
+        # images of the basis vectors e_i and e_{i+h}
+        R[:, i] = x * np.cos(ang[i]) + y * np.sin(ang[i])
+        R[:, i + h] = y * np.cos(ang[i]) - x * np.sin(ang[i])
+    return R
+
+
+@pytest.mark.parametrize("fam", ["gdn", "retnet", "mamba2", "vanilla"])
+@pytest.mark.parametrize("rdim", [16, 8])
+def test_rope_rerotation_equals_building_with_rotated_keys(fam, rdim):
+    """Moving a segment by delta positions rotates every key by R(delta);
+    building the pair from the rotated keys gives the re-rotated pair
+    (R T R^T, R S), whatever the segment's content.  (The rotated keys are
+    rounded to float32 when the oracle reads them: the two sides then differ
+    by that rounding, ~1e-7 relative.)"""
+    rng = np.random.default_rng(51)
+    d, n = 16, 40
+    k, v, kw = _family_inputs(fam, rng, n, d)
+    cu = [0, 25, n]
+    deltas = [1000, -37]
+    T, S = orc.build_pairs(fam, k, v, cu, **kw)
+    dense = fam == "gdn"
+    Tr, Sr = orc.rope(fam, T if dense else None, S, deltas, rotary_dim=rdim)
+    for p, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        R = rope_matrix(d, rdim, deltas[p])
+        k_rot = np.einsum("ij,lthj->lthi", R, k[:, a:b].astype(np.float64)).astype(np.float32)
+        sl = {key: (val[:, a:b] if val.ndim >= 3 else val) for key, val in kw.items()}
+        T2, S2 = orc.build_pairs(fam, k_rot, v[:, a:b], [0, b - a], **sl)
+        np.testing.assert_allclose(Sr[p], S2[0], rtol=0, atol=2e-6 * np.abs(S2[0]).max())
+        if dense:
+            np.testing.assert_allclose(Tr[p], T2[0], rtol=0, atol=2e-6)
+        elif T is not None:
+            np.testing.assert_array_equal(T2[0], T[p])  # a scalar transition does not see R
+
+
+def test_rope_rotation_properties():
+    """R is orthogonal, R(0) = I, R(d1) R(d2) = R(d1 + d2), and re-rotating
+    twice equals re-rotating once by the summed shift."""
+    rng = np.random.default_rng(52)
+    d = 16
+    for rdim in (16, 10):
+        R1, R2 = rope_matrix(d, rdim, 123), rope_matrix(d, rdim, -40)
+        np.testing.assert_allclose(R1 @ R1.T, np.eye(d), atol=1e-12)
+        np.testing.assert_allclose(R1 @ R2, rope_matrix(d, rdim, 83), atol=1e-9)
+        np.testing.assert_allclose(rope_matrix(d, rdim, 0), np.eye(d), atol=0)
+    T = rng.standard_normal((1, 1, 2, d, d))
+    S = rng.standard_normal((1, 1, 2, d, d))
+    Ta, Sa = orc.rope("gdn", T, S, [123], rotary_dim=10)
+    Tb, Sb = orc.rope("gdn", Ta, Sa, [-40], rotary_dim=10)
+    Tc, Sc = orc.rope("gdn", T, S, [83], rotary_dim=10)
+    np.testing.assert_allclose(Tb, Tc, atol=1e-9)
+    np.testing.assert_allclose(Sb, Sc, atol=1e-9)
+    R = rope_matrix(d, 10, 123)
+    np.testing.assert_allclose(Sa[0, 0, 1], R @ S[0, 0, 1], atol=1e-12)
+    np.testing.assert_allclose(Ta[0, 0, 1], R @ T[0, 0, 1] @ R.T, atol=1e-12)
