@@ -73,7 +73,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_VERSION 130 /* 1.3.0: compose returns the chain's own transition (T_out) */
+#define HYPIC_VERSION 140 /* 1.4.0: hypic_rope_rerotate */
 
 #if defined(__GNUC__)
 #define HYPIC_API __attribute__((visibility("default")))
@@ -326,6 +326,39 @@ HYPIC_API hypic_status hypic_reuse_chain(const hypic_chain_args* args, void* wor
  */
 #define HYPIC_NOALLOC_MAX_SEGMENTS 16384
 HYPIC_API hypic_status hypic_segment_build_noalloc(const hypic_build_args* args, hypic_stream_t stream);
+
+/* ------------------------------------------------------------ re-rotation --
+ * State re-rotation for variants whose keys carry rotary position embeddings
+ * ([AIBASE] linear-layer paragraph: the "state re-rotation" patch, named but
+ * not spelled out there).  A cached segment reused delta positions away sees
+ * each of its keys as R k, R = R(delta) the rotary rotation.  For a family
+ * whose per-token transition is built from k k^T and scalars (GDN, RETNET,
+ * MAMBA2, VANILLA) each transition A becomes R A R^T and each write k v^T
+ * becomes R k v^T, so the pair becomes (R T R^T, R S); this call applies that
+ * in place.  GLA and KDA return HYPIC_ERR_UNSUPPORTED: their per-channel gates
+ * do not commute with R, so no re-rotation of the pair is exact.
+ * R turns the first rotary_dim features in rotate-half pairs: for
+ * i < h = rotary_dim / 2, (x_i, x_{i+h}) -> (x_i cos a - x_{i+h} sin a,
+ * x_{i+h} cos a + x_i sin a) with a = delta * base^(-2i / rotary_dim); the other
+ * features are unchanged.  Angles are formed in double.
+ *   delta  device int64 [n_pairs]: the position shift of each pair.
+ *   T      device [n_pairs][n_layers][n_heads][dk][dk] f32 mantissa (GDN; its
+ *          T_exp is unchanged, R being orthogonal), NULL for the other families.
+ *   S      device [n_pairs][n_layers][n_heads][dk][dv] f32.
+ * Supported: dk, dv in {16, 32, 64, 128}, rotary_dim even in [2, dk], base > 0.
+ */
+typedef struct {
+    int family;
+    int n_layers, n_heads, dk, dv;
+    int n_pairs;
+    int rotary_dim;
+    double base;
+    const int64_t* delta;
+    float* T;
+    float* S;
+} hypic_rope_args;
+
+HYPIC_API hypic_status hypic_rope_rerotate(const hypic_rope_args* args, hypic_stream_t stream);
 
 /* ------------------------------------------------------------------ misc -- */
 

@@ -59,9 +59,14 @@ class ChainArgs(ctypes.Structure):
                 ("S0", _P), ("S_out", _P), ("o_out", _P)]
 
 
+class RopeArgs(ctypes.Structure):
+    _fields_ = [("family", _I), ("n_layers", _I), ("n_heads", _I), ("dk", _I), ("dv", _I), ("n_pairs", _I),
+                ("rotary_dim", _I), ("base", ctypes.c_double), ("delta", _P), ("T", _P), ("S", _P)]
+
+
 EXPORTS = ["hypic_build_workspace_size", "hypic_segment_build", "hypic_compose", "hypic_seam_advance",
            "hypic_status_string", "hypic_last_error_detail", "hypic_version", "hypic_check_device",
-           "hypic_segment_build_noalloc", "hypic_chain_workspace_size", "hypic_reuse_chain"]
+           "hypic_segment_build_noalloc", "hypic_chain_workspace_size", "hypic_reuse_chain", "hypic_rope_rerotate"]
 NOALLOC_MAX_SEGMENTS = 16384
 
 
@@ -81,8 +86,9 @@ def _load():
     lib.hypic_chain_workspace_size.argtypes = [ctypes.POINTER(ChainArgs)]
     lib.hypic_chain_workspace_size.restype = ctypes.c_size_t
     lib.hypic_reuse_chain.argtypes = [ctypes.POINTER(ChainArgs), _P, ctypes.c_size_t, _P]
+    lib.hypic_rope_rerotate.argtypes = [ctypes.POINTER(RopeArgs), _P]
     for f in (lib.hypic_segment_build, lib.hypic_compose, lib.hypic_seam_advance, lib.hypic_check_device,
-              lib.hypic_reuse_chain):
+              lib.hypic_reuse_chain, lib.hypic_rope_rerotate):
         f.restype = _I
     lib.hypic_status_string.argtypes = [_I]
     lib.hypic_status_string.restype = ctypes.c_char_p
@@ -130,6 +136,10 @@ def hypic_seam_advance(args: SeamArgs, stream: int) -> int:
 
 def hypic_check_device(stream: int) -> int:
     return lib.hypic_check_device(stream)
+
+
+def hypic_rope_rerotate(args: RopeArgs, stream: int) -> int:
+    return lib.hypic_rope_rerotate(ctypes.byref(args), stream)
 
 
 def hypic_version() -> int:
@@ -367,6 +377,23 @@ def reuse_chain(family, S_tab, cu_chain, seg_idx, cu_step, q, k, v, *, T_tab=Non
     _check(hypic_reuse_chain(a, _ptr(ws), nbytes, _stream(stream)))
     del keep
     return out, o_out
+
+
+def rope_rerotate(family, S, delta, *, T=None, rotary_dim=None, base=10000.0, stream=None):
+    """Re-rotate cached pairs in place for position shifts delta[p]
+    (hypic_rope_rerotate): S [n_pairs][L][H][dk][dv] and, for GDN, the T
+    mantissa [n_pairs][L][H][dk][dk].  delta: host ints."""
+    import torch
+    fam = FAMILY[family] if isinstance(family, str) else family
+    d = torch.as_tensor(np.asarray(delta, dtype=np.int64)).to(S.device)
+    a = RopeArgs()
+    a.family = fam
+    a.n_pairs, a.n_layers, a.n_heads, a.dk, a.dv = S.shape
+    a.rotary_dim = int(rotary_dim or S.shape[3])
+    a.base = float(base)
+    a.delta, a.T, a.S = _ptr(d), _ptr(T), _ptr(S)
+    _check(hypic_rope_rerotate(a, _stream(stream)))
+    return T, S
 
 
 def check_device(stream=None):

@@ -2,6 +2,7 @@
 // argument checks, work dispatch and error reporting.  No call allocates
 // memory; all checks happen before the first launch.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -582,6 +583,59 @@ extern "C" hypic_status hypic_reuse_chain(const hypic_chain_args* args, void* wo
             nb ^= 1;
         }
     }
+    return HYPIC_OK;
+}
+
+// ------------------------------------------------------------ re-rotation --
+
+namespace {
+
+hypic_status check_rope(const hypic_rope_args* a) {
+    if (!a) return fail(HYPIC_ERR_INVALID_ARG, "args is NULL");
+    if (a->n_pairs < 0) return fail(HYPIC_ERR_INVALID_ARG, "n_pairs %d", a->n_pairs);
+    hypic_status st = check_family(a->family, 0, a->n_layers, a->n_heads, a->dk, a->dv, false, nullptr, nullptr,
+                                   nullptr, nullptr, false);
+    if (st != HYPIC_OK) return st;
+    if (a->family == HYPIC_GLA || a->family == HYPIC_KDA)
+        return fail(HYPIC_ERR_UNSUPPORTED, "%s: per-channel gates do not commute with the rotation", fam_name(a->family));
+    if (a->rotary_dim < 2 || a->rotary_dim > a->dk || (a->rotary_dim & 1))
+        return fail(HYPIC_ERR_INVALID_ARG, "rotary_dim %d (even, in [2, dk = %d])", a->rotary_dim, a->dk);
+    if (!(a->base > 0.0) || !isfinite(a->base)) return fail(HYPIC_ERR_INVALID_ARG, "base %g", a->base);
+    if (a->n_pairs > 0) {
+        if (!a->delta || !a->S) return fail(HYPIC_ERR_INVALID_ARG, "delta and S required");
+        if (dense_T(a->family) != (a->T != nullptr))
+            return fail(HYPIC_ERR_INVALID_ARG, "T must be given for GDN and only for GDN");
+    }
+    const void* ptrs[] = {a->delta, a->T, a->S};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    const size_t LH = (size_t)a->n_layers * a->n_heads * a->n_pairs;
+    if (overlap(a->T, sizeof(float) * LH * a->dk * a->dk, a->S, sizeof(float) * LH * a->dk * a->dv) ||
+        overlap(a->delta, sizeof(int64_t) * a->n_pairs, a->S, sizeof(float) * LH * a->dk * a->dv) ||
+        overlap(a->delta, sizeof(int64_t) * a->n_pairs, a->T, sizeof(float) * LH * a->dk * a->dk))
+        return fail(HYPIC_ERR_INVALID_ARG, "T, S and delta overlap");
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" hypic_status hypic_rope_rerotate(const hypic_rope_args* args, hypic_stream_t stream) {
+    hypic_status st = check_rope(args);
+    if (st != HYPIC_OK) return st;
+    if (args->n_pairs == 0) return HYPIC_OK;
+    RopeParams p;
+    p.n_layers = args->n_layers;
+    p.n_heads = args->n_heads;
+    p.dk = args->dk;
+    p.dv = args->dv;
+    p.n_pairs = args->n_pairs;
+    p.rotary_dim = args->rotary_dim;
+    p.base = args->base;
+    p.delta = args->delta;
+    p.T = args->T;
+    p.S = args->S;
+    cudaError_t e = launch_rope(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "re-rotation launch");
     return HYPIC_OK;
 }
 

@@ -87,4 +87,14 @@ struct ChainParams {
 bool chain_tc_supported(const ChainParams& p);
 cudaError_t launch_chain_tc(const ChainParams& p, unsigned* err, cudaStream_t s);
 
+// State re-rotation of cached pairs (rope.cu), in place.
+struct RopeParams {
+    int n_layers, n_heads, dk, dv, n_pairs, rotary_dim;
+    double base;
+    const int64_t* delta;  // [n_pairs] position shift
+    float* T;              // [n_pairs][L][H][dk][dk] (dense families) or nullptr
+    float* S;              // [n_pairs][L][H][dk][dv]
+};
+cudaError_t launch_rope(const RopeParams& p, cudaStream_t s);
+
 }  // namespace hypic

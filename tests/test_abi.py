@@ -49,7 +49,7 @@ def test_struct_layout_matches_header(B, tmp_path):
     """Compile a probe against include/hypic.h with gcc and compare sizeof and
     every field offset with the ctypes mirrors."""
     structs = {"hypic_build_args": B.BuildArgs, "hypic_compose_args": B.ComposeArgs, "hypic_seam_args": B.SeamArgs,
-               "hypic_chain_args": B.ChainArgs}
+               "hypic_chain_args": B.ChainArgs, "hypic_rope_args": B.RopeArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "hypic.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
@@ -71,7 +71,7 @@ def test_struct_layout_matches_header(B, tmp_path):
 
 
 def test_status_strings_and_version(B):
-    assert B.hypic_version() == 130
+    assert B.hypic_version() == 140
     for code, name in enumerate(["HYPIC_OK", "HYPIC_ERR_INVALID_ARG", "HYPIC_ERR_UNSUPPORTED", "HYPIC_ERR_WORKSPACE",
                                  "HYPIC_ERR_CUDA", "HYPIC_ERR_TIMEOUT"]):
         assert B.lib.hypic_status_string(code).decode() == name
@@ -313,3 +313,40 @@ def test_chain_step_by_step_path_needs_its_workspace(B):
     assert B.hypic_reuse_chain(a, None, 0, None) == B.ERR_WORKSPACE
     assert B.hypic_reuse_chain(a, fake(20), need - 1, None) == B.ERR_WORKSPACE
     assert B.hypic_reuse_chain(a, fake(20) + 16, need, None) == B.ERR_WORKSPACE  # not 256-byte aligned
+
+
+def base_rope(B, family=0, d=64, n_pairs=3):
+    a = B.RopeArgs()
+    a.family, a.n_layers, a.n_heads, a.dk, a.dv, a.n_pairs = family, 2, 2, d, d, n_pairs
+    a.rotary_dim, a.base = d, 10000.0
+    a.delta, a.S = fake(1), fake(2)
+    a.T = fake(3) if family == 0 else None
+    return a
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a: setattr(a, "family", 2), 2),            # GLA: gates do not commute with R
+    (lambda a: setattr(a, "family", 4), 2),            # KDA: same
+    (lambda a: setattr(a, "rotary_dim", 63), 1),       # odd
+    (lambda a: setattr(a, "rotary_dim", 0), 1),
+    (lambda a: setattr(a, "rotary_dim", 66), 1),       # > dk
+    (lambda a: setattr(a, "base", 0.0), 1),
+    (lambda a: setattr(a, "base", float("nan")), 1),
+    (lambda a: setattr(a, "T", None), 1),              # GDN needs T
+    (lambda a: setattr(a, "delta", None), 1),
+    (lambda a: setattr(a, "S", fake(3) + 256), 1),     # S overlaps T
+    (lambda a: setattr(a, "S", fake(2) + 8), 1),       # misaligned
+])
+def test_rope_rejections(B, mutate, status):
+    a = base_rope(B)
+    mutate(a)
+    assert B.hypic_rope_rerotate(a, None) == status
+    assert B.lib.hypic_last_error_detail().decode()
+
+
+def test_rope_scalar_family_takes_no_T_and_empty_is_ok(B):
+    a = base_rope(B, family=1)
+    a.T = fake(3)
+    assert B.hypic_rope_rerotate(a, None) == B.ERR_INVALID_ARG
+    a = base_rope(B, family=1, n_pairs=0)
+    assert B.hypic_rope_rerotate(a, None) == B.OK
