@@ -450,4 +450,45 @@ int oracle_rope(int family, int n_layers, int n_heads, int dk, int dv, int n_pai
     return bad;
 }
 
-int oracle_version(void) { return 4; }
+/* ------------------------------------------------------ conv-state warm-up -- */
+
+/*
+ * Conv-state warm-up for variants with a short causal convolution on the
+ * inputs of the linear layers ([AB]: the "conv-state warm-up" patch, named
+ * only).  A depthwise causal convolution of width K gives token t of channel
+ * c the value y_t = act(bias_c + sum_{j<K} w[c][j] x_{t-K+1+j}); at a seam
+ * window the K-1 inputs before the window come from the NEW prefix (hist),
+ * not from the cached segment's own past.  Inputs, fp32 widened to double:
+ *   x     [n_layers][n_tokens][C]  the windows' raw inputs, packed by window
+ *   hist  [n_seams][n_layers][K-1][C]  the K-1 raw inputs before each window
+ *         (oldest first), NULL for zeros (a sequence start)
+ *   w     [n_layers][C][K] (tap K-1 multiplies the current token), bias
+ *         [n_layers][C] or NULL; act 0 = identity, 1 = SiLU x / (1 + e^-x).
+ * Output y [n_layers][n_tokens][C].
+ */
+int oracle_conv(int n_layers, int C, int K, int n_seams, const int* cu_seam, long long n_tokens,
+                const float* x, const float* hist, const float* w, const float* bias, int act, double* y)
+{
+    if (n_layers <= 0 || C <= 0 || K < 1 || n_seams < 0) return 1;
+    for (int r = 0; r < n_seams; ++r)
+        for (int l = 0; l < n_layers; ++l)
+            for (long long t = cu_seam[r]; t < cu_seam[r + 1]; ++t)
+                for (int c = 0; c < C; ++c) {
+                    double acc = bias ? (double)bias[(size_t)l * C + c] : 0.0;
+                    for (int j = 0; j < K; ++j) {
+                        const long long src = t - (K - 1) + j; /* token index in the window's frame */
+                        double xv;
+                        if (src >= cu_seam[r]) {
+                            xv = (double)x[((size_t)l * n_tokens + src) * C + c];
+                        } else {
+                            const long long hi = (K - 1) - (cu_seam[r] - src); /* 0 = oldest */
+                            xv = hist ? (double)hist[(((size_t)r * n_layers + l) * (K - 1) + hi) * C + c] : 0.0;
+                        }
+                        acc += (double)w[((size_t)l * C + c) * K + j] * xv;
+                    }
+                    y[((size_t)l * n_tokens + t) * C + c] = act ? acc / (1.0 + exp(-acc)) : acc;
+                }
+    return 0;
+}
+
+int oracle_version(void) { return 5; }

@@ -62,7 +62,8 @@ def _load():
         lib.oracle_compose.argtypes = [I, I, I, I, I, I, P, P, I, P, P, P, P, I, I, P]
         lib.oracle_seam.argtypes = [I, I, I, I, I, I, P, LL, P, P, P, P, P, P, P, P, P, P, I]
         lib.oracle_rope.argtypes = [I, I, I, I, I, I, I, ctypes.c_double, P, P, P]
-        for f in (lib.oracle_build, lib.oracle_compose, lib.oracle_seam, lib.oracle_rope):
+        lib.oracle_conv.argtypes = [I, I, I, I, P, LL, P, P, P, P, I, P]
+        for f in (lib.oracle_build, lib.oracle_compose, lib.oracle_seam, lib.oracle_rope, lib.oracle_conv):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -201,6 +202,23 @@ def rope(family, T, S, delta, *, rotary_dim=None, base=10000.0):
     if rc:
         raise RuntimeError("oracle_rope failed")
     return T, S
+
+
+def conv(x, cu_seam, w, *, hist=None, bias=None, act=1):
+    """Conv-state warm-up (restated in hypic_oracle.c): the depthwise causal
+    convolution of each window's inputs x [L][n_tok][C] with the K-1 inputs
+    before it taken from hist [n_seams][L][K-1][C] (zeros when None);
+    w [L][C][K], bias [L][C].  Returns y [L][n_tok][C] in float64."""
+    x, w = _f32(x), _f32(w)
+    n_layers, n_tokens, C = x.shape
+    K = w.shape[-1]
+    cu = _i32(cu_seam)
+    y = np.zeros((n_layers, n_tokens, C))
+    rc = _load().oracle_conv(n_layers, C, K, cu.shape[0] - 1, _ptr(cu), n_tokens, _ptr(x), _ptr(_f32(hist)),
+                             _ptr(w), _ptr(_f32(bias)), int(act), _ptr(y))
+    if rc:
+        raise RuntimeError("oracle_conv failed")
+    return y
 
 
 def rel_fro(x, ref, axes):

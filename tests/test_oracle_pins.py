@@ -537,3 +537,36 @@ def test_rope_rotation_properties():
     R = rope_matrix(d, 10, 123)
     np.testing.assert_allclose(Sa[0, 0, 1], R @ S[0, 0, 1], atol=1e-12)
     np.testing.assert_allclose(Ta[0, 0, 1], R @ T[0, 0, 1] @ R.T, atol=1e-12)
+
+
+# ------------------------------------------------------ conv-state warm-up ----
+
+def test_conv_warmup_equals_convolution_of_the_whole_sequence():
+    """A window whose history is the true K-1 inputs before it gets the same
+    outputs as the causal convolution of the whole sequence (np.convolve per
+    channel, zero padding at the start); with SiLU, y = z / (1 + e^-z)."""
+    rng = np.random.default_rng(61)
+    L, C, K, n = 2, 6, 4, 50
+    xs = rng.standard_normal((L, n, C)).astype(np.float32)
+    w = rng.standard_normal((L, C, K)).astype(np.float32)
+    b = rng.standard_normal((L, C)).astype(np.float32)
+    # the whole sequence as windows: [0, 20) from a sequence start, [20, 28), [28, 50)
+    starts = [0, 20, 28, 50]
+    hist = np.zeros((3, L, K - 1, C), np.float32)
+    for r, s0 in enumerate(starts[:-1]):
+        for j in range(K - 1):
+            src = s0 - (K - 1) + j
+            if src >= 0:
+                hist[r, :, j] = xs[:, src]
+    for act in (0, 1):
+        y = orc.conv(xs, starts, w, hist=hist, bias=b, act=act)
+        for l in range(L):
+            for c in range(C):
+                z = np.convolve(xs[l, :, c].astype(np.float64), w[l, c, ::-1].astype(np.float64))[:n] + b[l, c]
+                want = z / (1.0 + np.exp(-z)) if act else z
+                np.testing.assert_allclose(y[l, :, c], want, atol=1e-12)
+    # without the true history the first K-1 outputs of a window differ, the rest do not
+    y0 = orc.conv(xs, starts, w, hist=None, bias=b, act=0)
+    y1 = orc.conv(xs, starts, w, hist=hist, bias=b, act=0)
+    assert np.abs(y0[:, 20:23] - y1[:, 20:23]).max() > 1e-3
+    np.testing.assert_array_equal(y0[:, 23:28], y1[:, 23:28])
