@@ -73,7 +73,7 @@
 extern "C" {
 #endif
 
-#define HYPIC_VERSION 140 /* 1.4.0: hypic_rope_rerotate */
+#define HYPIC_VERSION 150 /* 1.5.0: hypic_conv_warmup */
 
 #if defined(__GNUC__)
 #define HYPIC_API __attribute__((visibility("default")))
@@ -359,6 +359,41 @@ typedef struct {
 } hypic_rope_args;
 
 HYPIC_API hypic_status hypic_rope_rerotate(const hypic_rope_args* args, hypic_stream_t stream);
+
+/* ------------------------------------------------------- conv warm-up --
+ * Conv-state warm-up for variants with a short causal convolution on the
+ * linear layers' inputs ([AIBASE] linear-layer paragraph: the "conv-state
+ * warm-up" patch, named only there).  At a seam window the K - 1 inputs
+ * before the window come from the new prefix, not from the cached segment's
+ * past.  A depthwise causal convolution of width K gives token t (of window r)
+ * and channel c
+ *     y_t = act(bias_c + sum_{j<K} w[c][j] x_{t-K+1+j}),
+ * with the inputs before cu_seam[r] taken from hist[r] (oldest first).
+ *   x      device [n_layers][n_tokens][C] f32: the windows' raw inputs, packed
+ *          by window (window r = tokens [cu_seam[r], cu_seam[r+1])).
+ *   hist   device [n_seams][n_layers][K-1][C] f32, or NULL for zeros (a
+ *          window at a sequence start).
+ *   w      device [n_layers][C][K] f32 (tap K-1 multiplies the current token);
+ *   bias   device [n_layers][C] f32 or NULL.
+ *   act    0 = identity, 1 = SiLU (x / (1 + e^-x)).
+ *   y      device [n_layers][n_tokens][C] f32; must not overlap the inputs.
+ * Supported: 1 <= K <= 16.
+ */
+typedef struct {
+    int n_layers, C, K;
+    int n_seams;
+    int64_t n_tokens;
+    const int32_t* cu_seam;       /* device [n_seams+1], from 0 to n_tokens */
+    const int32_t* cu_seam_host;  /* host copy (validation) */
+    const float* x;
+    const float* hist;
+    const float* w;
+    const float* bias;
+    int act;
+    float* y;
+} hypic_conv_args;
+
+HYPIC_API hypic_status hypic_conv_warmup(const hypic_conv_args* args, hypic_stream_t stream);
 
 /* ------------------------------------------------------------------ misc -- */
 

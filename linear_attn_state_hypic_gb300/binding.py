@@ -64,9 +64,16 @@ class RopeArgs(ctypes.Structure):
                 ("rotary_dim", _I), ("base", ctypes.c_double), ("delta", _P), ("T", _P), ("S", _P)]
 
 
+class ConvArgs(ctypes.Structure):
+    _fields_ = [("n_layers", _I), ("C", _I), ("K", _I), ("n_seams", _I), ("n_tokens", _LL),
+                ("cu_seam", _P), ("cu_seam_host", _P), ("x", _P), ("hist", _P), ("w", _P), ("bias", _P),
+                ("act", _I), ("y", _P)]
+
+
 EXPORTS = ["hypic_build_workspace_size", "hypic_segment_build", "hypic_compose", "hypic_seam_advance",
            "hypic_status_string", "hypic_last_error_detail", "hypic_version", "hypic_check_device",
-           "hypic_segment_build_noalloc", "hypic_chain_workspace_size", "hypic_reuse_chain", "hypic_rope_rerotate"]
+           "hypic_segment_build_noalloc", "hypic_chain_workspace_size", "hypic_reuse_chain", "hypic_rope_rerotate",
+           "hypic_conv_warmup"]
 NOALLOC_MAX_SEGMENTS = 16384
 
 
@@ -87,8 +94,9 @@ def _load():
     lib.hypic_chain_workspace_size.restype = ctypes.c_size_t
     lib.hypic_reuse_chain.argtypes = [ctypes.POINTER(ChainArgs), _P, ctypes.c_size_t, _P]
     lib.hypic_rope_rerotate.argtypes = [ctypes.POINTER(RopeArgs), _P]
+    lib.hypic_conv_warmup.argtypes = [ctypes.POINTER(ConvArgs), _P]
     for f in (lib.hypic_segment_build, lib.hypic_compose, lib.hypic_seam_advance, lib.hypic_check_device,
-              lib.hypic_reuse_chain, lib.hypic_rope_rerotate):
+              lib.hypic_reuse_chain, lib.hypic_rope_rerotate, lib.hypic_conv_warmup):
         f.restype = _I
     lib.hypic_status_string.argtypes = [_I]
     lib.hypic_status_string.restype = ctypes.c_char_p
@@ -140,6 +148,10 @@ def hypic_check_device(stream: int) -> int:
 
 def hypic_rope_rerotate(args: RopeArgs, stream: int) -> int:
     return lib.hypic_rope_rerotate(ctypes.byref(args), stream)
+
+
+def hypic_conv_warmup(args: ConvArgs, stream: int) -> int:
+    return lib.hypic_conv_warmup(ctypes.byref(args), stream)
 
 
 def hypic_version() -> int:
@@ -394,6 +406,26 @@ def rope_rerotate(family, S, delta, *, T=None, rotary_dim=None, base=10000.0, st
     a.delta, a.T, a.S = _ptr(d), _ptr(T), _ptr(S)
     _check(hypic_rope_rerotate(a, _stream(stream)))
     return T, S
+
+
+def conv_warmup(x, cu_seam, w, *, hist=None, bias=None, act=1, out=None, stream=None):
+    """Conv-state warm-up of seam windows (hypic_conv_warmup): x [L][n_tok][C]
+    CUDA f32, cu_seam host ints, w [L][C][K], hist [n_seams][L][K-1][C] or
+    None, bias [L][C] or None.  Returns y [L][n_tok][C]."""
+    import torch
+    cu = _host_i32(cu_seam)
+    cu_d = _dev_i32(cu, None, x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    a = ConvArgs()
+    a.n_layers, a.n_tokens, a.C = x.shape
+    a.K = w.shape[-1]
+    a.n_seams = len(cu) - 1
+    a.cu_seam, a.cu_seam_host = _ptr(cu_d), _hptr(cu)
+    a.x, a.hist, a.w, a.bias, a.act, a.y = _ptr(x), _ptr(hist), _ptr(w), _ptr(bias), int(act), _ptr(out)
+    _check(hypic_conv_warmup(a, _stream(stream)))
+    del cu, cu_d
+    return out
 
 
 def check_device(stream=None):

@@ -639,6 +639,62 @@ extern "C" hypic_status hypic_rope_rerotate(const hypic_rope_args* args, hypic_s
     return HYPIC_OK;
 }
 
+// ----------------------------------------------------------- conv warm-up --
+
+namespace {
+
+hypic_status check_conv(const hypic_conv_args* a) {
+    if (!a) return fail(HYPIC_ERR_INVALID_ARG, "args is NULL");
+    if (a->n_layers < 1 || a->C < 1 || a->n_seams < 0)
+        return fail(HYPIC_ERR_INVALID_ARG, "n_layers %d C %d n_seams %d", a->n_layers, a->C, a->n_seams);
+    if (a->K < 1 || a->K > 16) return fail(HYPIC_ERR_UNSUPPORTED, "K %d (supported: 1..16)", a->K);
+    if (a->act != 0 && a->act != 1) return fail(HYPIC_ERR_INVALID_ARG, "act %d", a->act);
+    if (a->n_tokens < 0 || a->n_tokens > INT32_MAX)
+        return fail(HYPIC_ERR_INVALID_ARG, "n_tokens %lld", (long long)a->n_tokens);
+    if (!a->cu_seam || !a->cu_seam_host) return fail(HYPIC_ERR_INVALID_ARG, "cu_seam (device and host) required");
+    const int32_t* cu = a->cu_seam_host;
+    if (cu[0] != 0) return fail(HYPIC_ERR_INVALID_ARG, "cu_seam[0] = %d (must be 0)", cu[0]);
+    for (int r = 0; r < a->n_seams; ++r)
+        if (cu[r + 1] < cu[r]) return fail(HYPIC_ERR_INVALID_ARG, "cu_seam decreases at %d", r);
+    if ((int64_t)cu[a->n_seams] != a->n_tokens)
+        return fail(HYPIC_ERR_INVALID_ARG, "cu_seam[n_seams] = %d != n_tokens %lld", cu[a->n_seams],
+                    (long long)a->n_tokens);
+    if (a->n_tokens > 0 && (!a->x || !a->w || !a->y)) return fail(HYPIC_ERR_INVALID_ARG, "x, w and y required");
+    const void* ptrs[] = {a->x, a->hist, a->w, a->bias, a->y};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(HYPIC_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    const size_t L = (size_t)a->n_layers, C = (size_t)a->C, K = (size_t)a->K;
+    const size_t yb = sizeof(float) * L * a->n_tokens * C;
+    if (overlap(a->y, yb, a->x, yb) || overlap(a->y, yb, a->hist, sizeof(float) * a->n_seams * L * (K - 1) * C) ||
+        overlap(a->y, yb, a->w, sizeof(float) * L * C * K) || overlap(a->y, yb, a->bias, sizeof(float) * L * C))
+        return fail(HYPIC_ERR_INVALID_ARG, "y overlaps an input");
+    return HYPIC_OK;
+}
+
+}  // namespace
+
+extern "C" hypic_status hypic_conv_warmup(const hypic_conv_args* args, hypic_stream_t stream) {
+    hypic_status st = check_conv(args);
+    if (st != HYPIC_OK) return st;
+    if (args->n_tokens == 0 || args->n_seams == 0) return HYPIC_OK;
+    ConvParams p;
+    p.n_layers = args->n_layers;
+    p.C = args->C;
+    p.K = args->K;
+    p.n_seams = args->n_seams;
+    p.act = args->act;
+    p.n_tokens = args->n_tokens;
+    p.cu_seam = args->cu_seam;
+    p.x = args->x;
+    p.hist = args->hist;
+    p.w = args->w;
+    p.bias = args->bias;
+    p.y = args->y;
+    cudaError_t e = launch_conv_warmup(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "conv warm-up launch");
+    return HYPIC_OK;
+}
+
 // ------------------------------------------------------------------- misc --
 
 extern "C" const char* hypic_status_string(hypic_status s) {

@@ -97,4 +97,17 @@ struct RopeParams {
 };
 cudaError_t launch_rope(const RopeParams& p, cudaStream_t s);
 
+// Conv-state warm-up of seam windows (conv.cu).
+struct ConvParams {
+    int n_layers, C, K, n_seams, act;
+    int64_t n_tokens;
+    const int32_t* cu_seam;
+    const float* x;     // [L][n_tokens][C]
+    const float* hist;  // [n_seams][L][K-1][C] or nullptr
+    const float* w;     // [L][C][K]
+    const float* bias;  // [L][C] or nullptr
+    float* y;           // [L][n_tokens][C]
+};
+cudaError_t launch_conv_warmup(const ConvParams& p, cudaStream_t s);
+
 }  // namespace hypic

@@ -49,7 +49,7 @@ def test_struct_layout_matches_header(B, tmp_path):
     """Compile a probe against include/hypic.h with gcc and compare sizeof and
     every field offset with the ctypes mirrors."""
     structs = {"hypic_build_args": B.BuildArgs, "hypic_compose_args": B.ComposeArgs, "hypic_seam_args": B.SeamArgs,
-               "hypic_chain_args": B.ChainArgs, "hypic_rope_args": B.RopeArgs}
+               "hypic_chain_args": B.ChainArgs, "hypic_rope_args": B.RopeArgs, "hypic_conv_args": B.ConvArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "hypic.h"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
@@ -71,7 +71,7 @@ def test_struct_layout_matches_header(B, tmp_path):
 
 
 def test_status_strings_and_version(B):
-    assert B.hypic_version() == 140
+    assert B.hypic_version() == 150
     for code, name in enumerate(["HYPIC_OK", "HYPIC_ERR_INVALID_ARG", "HYPIC_ERR_UNSUPPORTED", "HYPIC_ERR_WORKSPACE",
                                  "HYPIC_ERR_CUDA", "HYPIC_ERR_TIMEOUT"]):
         assert B.lib.hypic_status_string(code).decode() == name
@@ -350,3 +350,29 @@ def test_rope_scalar_family_takes_no_T_and_empty_is_ok(B):
     assert B.hypic_rope_rerotate(a, None) == B.ERR_INVALID_ARG
     a = base_rope(B, family=1, n_pairs=0)
     assert B.hypic_rope_rerotate(a, None) == B.OK
+
+
+def base_conv(B, lens=(8, 8, 0)):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    a = B.ConvArgs()
+    a.n_layers, a.C, a.K, a.n_seams, a.n_tokens = 2, 64, 4, len(lens), int(cu[-1])
+    a.cu_seam, a.cu_seam_host = fake(0), cu.ctypes.data
+    a.x, a.w, a.y, a.act = fake(1), fake(2), fake(3), 1
+    return a, cu
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a, c: setattr(a, "K", 0), 2),
+    (lambda a, c: setattr(a, "K", 17), 2),
+    (lambda a, c: setattr(a, "act", 2), 1),
+    (lambda a, c: setattr(a, "n_tokens", 15), 1),      # cu_seam[-1] != n_tokens
+    (lambda a, c: c.__setitem__(0, 1), 1),             # cu_seam[0] != 0
+    (lambda a, c: setattr(a, "x", None), 1),
+    (lambda a, c: setattr(a, "y", fake(1) + 16), 1),   # y overlaps x
+    (lambda a, c: setattr(a, "w", fake(2) + 4), 1),    # misaligned
+])
+def test_conv_rejections(B, mutate, status):
+    a, cu = base_conv(B)
+    mutate(a, cu)
+    assert B.hypic_conv_warmup(a, None) == status
+    assert B.lib.hypic_last_error_detail().decode()
