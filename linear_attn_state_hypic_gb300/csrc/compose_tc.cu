@@ -106,15 +106,23 @@ __device__ __forceinline__ int step_units(const CtArgs& a, int j, int& tb) {
     return (a.cu_step[j + 1] - tb + kU - 1) / kU;
 }
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const CtArgs& a) {
-    for (uint32_t i = 0; i < a.wait_limit; i += 256) {
+// Bounded wait: the fast path inline, the polling loop out of line (one copy
+// of it keeps the kernel's code small in the instruction cache).
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t limit,
+                                           unsigned* err) {
+    for (uint32_t i = 0; i < limit; i += 256) {
+#pragma unroll 1
         for (int j = 0; j < 256; ++j)
             if (mbar_try_wait(bar, parity)) return true;
-        if (*(volatile int*)&ms->abort_flag) return false;
+        if (*(volatile int*)abort_flag) return false;
     }
-    *(volatile int*)&ms->abort_flag = 1;
-    set_error(a.err, kErrTimeout);
+    *(volatile int*)abort_flag = 1;
+    set_error(err, kErrTimeout);
     return false;
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const CtArgs& a) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, &ms->abort_flag, a.wait_limit, a.err);
 }
 
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
