@@ -815,7 +815,7 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
 // chunk's own decay would pass 2^-kLazyMax, which bounds every factor and the
 // growth of D''_S by 2^(2 kLazyMax).
 constexpr int kRenormEvery = 8;
-constexpr float kLazyMax = 40.f;
+constexpr float kLazyMax = 56.f;  // (2^112 x the state stays far inside float32 range)
 
 struct StatePlan {
     bool rn;
