@@ -90,7 +90,7 @@ struct Misc {
     uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done
     uint64_t u_done, w_done;      // U^T, W^T committed
     uint64_t u_cvt, w_cvt;        // U~ and W operands written
-    uint64_t x_done, xt_free, y_ready, d_ready, drain;  // xt_free: the pass has read X''_T
+    uint64_t x_done_s, x_done, xs_free, y_ready, d_ready, drain;  // GEMM1 S half / all done; X''_S read
     alignas(16) float lg2[kGateSlots][kC];  // slot gc % kGateSlots; every table is read as float4
     alignas(16) float beta[kGateSlots][kC];
     alignas(16) float up[kGateSlots][kC];
@@ -111,7 +111,7 @@ static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, lg2) % 16 == 0 && offsetof(Mi
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Tensor-memory columns.
-// W^T is staged in the X_T columns: it is converted before GEMM1 writes X.
+// W^T is staged in the X_S columns: it is converted before GEMM1 writes X.
 constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_U = 384, TM_G = 448;
 
 constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);  // G = K K^T
@@ -427,7 +427,7 @@ __device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, in
     }
 }
 
-// W^T (lane i holds W[.][i], staged in the X_T columns) -> W as a tf32
+// W^T (lane i holds W[.][i], staged in the X_S columns) -> W as a tf32
 // K-major [64 t][128 i] operand.
 __device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
     const int i = 32 * q + lane;
@@ -436,7 +436,7 @@ __device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
         uint32_t w[32];
-        tmem_ld32(tl + TM_XT + 32 * half, w);
+        tmem_ld32(tl + TM_XS + 32 * half, w);
         tmem_wait_ld();
         uint8_t* b = bw + 32 * half * 128;
 #pragma unroll
@@ -661,9 +661,10 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CU
 }
 
 // Warp 1, lane 0: issues every MMA of the item as soon as its inputs are
-// ready, in this priority: W^T, GEMM2, GEMM1, U^T, gram.  W^T of the next
-// chunk reuses the X''_T columns and waits only for the T half of this
-// chunk's pass, so it runs while the pass does the S half.  A readiness test
+// ready, in this priority: W^T, GEMM2, GEMM1, U^T, gram.  GEMM1 runs its S
+// half first; W^T of the next chunk reuses the X''_S columns and waits only
+// for the S half of this chunk's pass, so it runs while the pass does the T
+// half.  A readiness test
 // of a barrier's phase k is only made once its phase k - 1 is known to be
 // complete (by an earlier test or an earlier item), so a parity test cannot
 // mistake an old phase for a new one.
@@ -676,16 +677,16 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
     uint64_t t_idle = 0;
     while (i2 < nc) {
         bool any = false;
-        if (iw < iu && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_T columns
+        if (iw < iu && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_S columns
             const uint32_t gc = g + iw;
-            if (iw == 0 || mbar_test(&ms->xt_free, (gc - 1) & 1)) {  // the pass has read the previous X''_T
+            if (iw == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1)) {  // the pass has read the previous X''_S
                 tc_fence_after();
                 const uint64_t a0 = sdesc_sw128(ktile(gc), 8192, 1024), bh = sdesc_sw128(bt, 0, 1024),
                                bl = sdesc_sw128(bt + 16384, 0, 1024);
 #pragma unroll 2
                 for (int k = 0; k < 4; ++k) {  // (a descriptor's address field counts 16-byte units)
-                    mma_bf16_ss(tmem + TM_XT, a0 + 128 * k, bh + 2 * k, ID_WU, k > 0);
-                    mma_bf16_ss(tmem + TM_XT, a0 + 128 * k, bl + 2 * k, ID_WU, true);
+                    mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bh + 2 * k, ID_WU, k > 0);
+                    mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bl + 2 * k, ID_WU, true);
                 }
                 mma_commit(&ms->w_done);
                 mma_commit(&ms->bt_free);  // (the U^T MMAs of this chunk were issued before)
@@ -720,12 +721,14 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 tc_fence_after();
                 const uint64_t b0 = sdesc_sw128(bw, 0, 1024);
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int hh = 0; hh < 2; ++hh) {  // the S half first: its pass frees the W^T columns
+                    const int h = 1 - hh;
 #pragma unroll 4  // (a measured balance of issue rate and code size)
                     for (int k = 0; k < 16; ++k)
                         mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3),
                                     ID_G1, k > 0);
-                mma_commit(&ms->x_done);
+                    mma_commit(hh ? &ms->x_done : &ms->x_done_s);
+                }
                 ++i1;
                 any = true;
             }
@@ -897,13 +900,15 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         const uint32_t gc = g + c;
         if (c > 0) {
             const uint32_t gp = gc - 1;
+            if (!wg_all(2, wait_bar(&ms->x_done_s, gp & 1, ms, a))) return;
+            tc_fence_after();
+            state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
+            tc_fence_before();
+            named_sync(2);  // every lane has read X''_S: the next W'^T may overwrite those columns
+            if (n == 0) mbar_arrive(&ms->xs_free);
             if (!wg_all(2, wait_bar(&ms->x_done, gp & 1, ms, a))) return;
             tc_fence_after();
             const float mloc = state_pass<0>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
-            tc_fence_before();
-            named_sync(2);  // every lane has read X''_T: the next W'^T may overwrite those columns
-            if (n == 0) mbar_arrive(&ms->xt_free);
-            state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
             fence_async_smem();
             tc_fence_before();
             if (pl.rn) {
@@ -946,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kGateSlots; ++s) mbar_init(&ms->gready[s], 1);
         uint64_t* one[] = {&ms->fullV, &ms->emptyV, &ms->g_done, &ms->g_read, &ms->that_ready, &ms->bt_free,
-                           &ms->u_done, &ms->w_done, &ms->u_cvt, &ms->w_cvt, &ms->x_done, &ms->xt_free, &ms->y_ready,
+                           &ms->u_done, &ms->w_done, &ms->u_cvt, &ms->w_cvt, &ms->x_done_s, &ms->x_done, &ms->xs_free, &ms->y_ready,
                            &ms->d_ready, &ms->drain};
         for (uint64_t* b : one) mbar_init(b, 1);
         ms->abort_flag = 0;
