@@ -335,8 +335,13 @@ __device__ bool prep_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, int lh
     return true;
 }
 
-// Applies the units of step js to the column in TM_D (epilogue thread n);
-// the last unit writes the split A operand of the next compose instead.
+// Applies the units of step js to the state in TM_D; the last unit writes the
+// split A operand of the next compose instead.  The two passes read the
+// state in the .16x256b shape: thread t of warp q holds lanes (columns of the
+// state) L_j = 32q + t/4 + 8j, j = 0..3, at a quarter of the rows i, so every
+// table value it loads from shared memory serves four columns.  The dot
+// products are then summed over the four threads that share t/4 (a
+// reduce-scatter by shuffles) and thread t finishes column L_{t%4}.
 __device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tl, int lh, int js, uint32_t& gu,
                                  int n) {
     int tb;
@@ -346,76 +351,120 @@ __device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint3
     const float* Qf = reinterpret_cast<const float*>(smem + OFF_SQ);
     const float* Wf = reinterpret_cast<const float*>(smem + OFF_SW);
     const float* Uf = reinterpret_cast<const float*>(smem + OFF_SU);
+    const int t = n & 31, r4 = t >> 2, c4 = t & 3;
+    const int nl = (n & ~31) + r4 + 8 * c4;       // the column this thread finishes
+    const uint32_t lb0 = tl, lb1 = tl + (16u << 16);  // lanes +0..15 and +16..31 of the quarter
     for (int k = 0; k < nu; ++k) {
         if (!wg_all(4, wait_bar(&ms->seam_ready, gu & 1, ms, a))) return false;
-        float wt[kU], qs[kU];
+        float acc[4][2 * kU];  // [column L_j][W_u . x for u < kU, g_u q_u . x after]
 #pragma unroll
-        for (int u = 0; u < kU; ++u) wt[u] = qs[u] = 0.f;
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int d = 0; d < 2 * kU; ++d) acc[j][d] = 0.f;
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {  // pass 1: W_u . x and g_u q_u . x
-            uint32_t x[32];
-            tmem_ld32(tl + TM_D + 32 * cb, x);
+        for (int bb = 0; bb < 16; ++bb) {  // pass 1, 8 rows at a time
+            uint32_t xa[4], xb[4];
+            tmem_ld16x256b_x1(lb0 + TM_D + 8 * bb, xa);
+            tmem_ld16x256b_x1(lb1 + TM_D + 8 * bb, xb);
             tmem_wait_ld();
+            const int i0 = 8 * bb + 2 * c4;
+            const float x[4][2] = {{__uint_as_float(xa[0]), __uint_as_float(xa[1])},
+                                   {__uint_as_float(xa[2]), __uint_as_float(xa[3])},
+                                   {__uint_as_float(xb[0]), __uint_as_float(xb[1])},
+                                   {__uint_as_float(xb[2]), __uint_as_float(xb[3])}};
 #pragma unroll
-            for (int jj = 0; jj < 32; jj += 4) {
-                const int i = 32 * cb + jj;
-                const float x0 = __uint_as_float(x[jj]), x1 = __uint_as_float(x[jj + 1]);
-                const float x2 = __uint_as_float(x[jj + 2]), x3 = __uint_as_float(x[jj + 3]);
+            for (int dd = 0; dd < 2 * kU; ++dd) {
+                const float2 w = *reinterpret_cast<const float2*>((dd < kU ? Wf + dd * kUR : Qf + (dd - kU) * kUR) + i0);
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const float4 w4 = *reinterpret_cast<const float4*>(Wf + u * kUR + i);
-                    const float4 q4 = *reinterpret_cast<const float4*>(Qf + u * kUR + i);
-                    wt[u] = fmaf(w4.x, x0, fmaf(w4.y, x1, fmaf(w4.z, x2, fmaf(w4.w, x3, wt[u]))));
-                    qs[u] = fmaf(q4.x, x0, fmaf(q4.y, x1, fmaf(q4.z, x2, fmaf(q4.w, x3, qs[u]))));
-                }
+                for (int j = 0; j < 4; ++j) acc[j][dd] = fmaf(w.x, x[j][0], fmaf(w.y, x[j][1], acc[j][dd]));
             }
+        }
+        // reduce-scatter over the four threads of the row group: thread c4 ends
+        // with the full sums of column L_{c4}
+        const bool h2 = c4 & 2, h1 = c4 & 1;
+        float pr[2][2 * kU];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int d = 0; d < 2 * kU; ++d) {
+                const float mine = h2 ? acc[2 + j][d] : acc[j][d];
+                const float other = h2 ? acc[j][d] : acc[2 + j][d];
+                pr[j][d] = mine + __shfl_xor_sync(0xffffffffu, other, 2);
+            }
+        float fin[2 * kU];
+#pragma unroll
+        for (int d = 0; d < 2 * kU; ++d) {
+            const float mine = h1 ? pr[1][d] : pr[0][d];
+            const float other = h1 ? pr[0][d] : pr[1][d];
+            fin[d] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
         }
         float up[kU], c[kU];
         const int nv = ms->nv, tok0 = ms->tok0;
 #pragma unroll
-        for (int u = 0; u < kU; ++u) up[u] = Uf[u * kUR + n] - wt[u];
+        for (int u = 0; u < kU; ++u) up[u] = Uf[u * kUR + nl] - fin[u];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            float o = qs[u];
+            float o = fin[kU + u];
 #pragma unroll
             for (int s2 = 0; s2 <= u; ++s2) o = fmaf(ms->M[u][s2], up[s2], o);
-            if (u < nv) a.o_out[(((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head) * kD + n] = o;
+            if (u < nv) a.o_out[(((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head) * kD + nl] = o;
             c[u] = ms->sc[u] * up[u];
         }
+        float cc[4][kU];  // the coefficients of this thread's four columns
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < kU; ++u) cc[j][u] = __shfl_sync(0xffffffffu, c[u], (t & ~3) | j);
         const float gw = ms->g[kU - 1];
         const bool last = k + 1 == nu;
 #pragma unroll 1
-        for (int cb = 0; cb < 8; ++cb) {  // pass 2: x <- g_w x + sum_s (g_w/g_s) k_s u'_s
-            uint32_t x[16];
-            tmem_ld16(tl + TM_D + 16 * cb, x);
+        for (int bb = 0; bb < 16; ++bb) {  // pass 2: x <- g_w x + sum_s (g_w/g_s) k_s u'_s, 8 rows at a time
+            uint32_t xa[4], xb[4];
+            tmem_ld16x256b_x1(lb0 + TM_D + 8 * bb, xa);
+            tmem_ld16x256b_x1(lb1 + TM_D + 8 * bb, xb);
             tmem_wait_ld();
+            const int i0 = 8 * bb + 2 * c4;
+            float y[4][2];
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {
-                const int i = 16 * cb + jj;
-                float y[4] = {gw * __uint_as_float(x[jj]), gw * __uint_as_float(x[jj + 1]),
-                              gw * __uint_as_float(x[jj + 2]), gw * __uint_as_float(x[jj + 3])};
+            for (int e = 0; e < 2; ++e) {
+                y[0][e] = gw * __uint_as_float(xa[e]);
+                y[1][e] = gw * __uint_as_float(xa[2 + e]);
+                y[2][e] = gw * __uint_as_float(xb[e]);
+                y[3][e] = gw * __uint_as_float(xb[2 + e]);
+            }
 #pragma unroll
-                for (int s2 = 0; s2 < kU; ++s2) {
-                    const float4 k4 = *reinterpret_cast<const float4*>(Kf + s2 * kUR + i);
-                    y[0] = fmaf(k4.x, c[s2], y[0]);
-                    y[1] = fmaf(k4.y, c[s2], y[1]);
-                    y[2] = fmaf(k4.z, c[s2], y[2]);
-                    y[3] = fmaf(k4.w, c[s2], y[3]);
+            for (int s2 = 0; s2 < kU; ++s2) {
+                const float2 k2 = *reinterpret_cast<const float2*>(Kf + s2 * kUR + i0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    y[j][0] = fmaf(k2.x, cc[j][s2], y[j][0]);
+                    y[j][1] = fmaf(k2.y, cc[j][s2], y[j][1]);
                 }
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) x[jj + e] = __float_as_uint(y[e]);
+            for (int e = 0; e < 2; ++e) {
+                xa[e] = __float_as_uint(y[0][e]);
+                xa[2 + e] = __float_as_uint(y[1][e]);
+                xb[e] = __float_as_uint(y[2][e]);
+                xb[2 + e] = __float_as_uint(y[3][e]);
             }
             if (last) {  // the A operand of the next compose, split hi/lo
-                uint32_t h[16], l[16];
+                uint32_t ha[4], la[4], hb[4], lbv[4];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) split_tf32(__uint_as_float(x[e]), h[e], l[e]);
-                tmem_st16(tl + TM_AB + 16 * cb, h);
-                tmem_st16(tl + TM_AS + 16 * cb, l);
+                for (int e = 0; e < 4; ++e) {
+                    split_tf32(__uint_as_float(xa[e]), ha[e], la[e]);
+                    split_tf32(__uint_as_float(xb[e]), hb[e], lbv[e]);
+                }
+                tmem_st16x256b_x1(lb0 + TM_AB + 8 * bb, ha);
+                tmem_st16x256b_x1(lb1 + TM_AB + 8 * bb, hb);
+                tmem_st16x256b_x1(lb0 + TM_AS + 8 * bb, la);
+                tmem_st16x256b_x1(lb1 + TM_AS + 8 * bb, lbv);
             } else {
-                tmem_st16(tl + TM_D + 16 * cb, x);
+                tmem_st16x256b_x1(lb0 + TM_D + 8 * bb, xa);
+                tmem_st16x256b_x1(lb1 + TM_D + 8 * bb, xb);
             }
-            tmem_wait_st();
         }
+        tmem_wait_st();
         named_sync(4);  // every column has read the unit's tables
         if (n == 0) mbar_arrive(&ms->seam_free);
         ++gu;
