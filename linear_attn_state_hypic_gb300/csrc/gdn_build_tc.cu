@@ -747,7 +747,9 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 any = true;
             }
         }
-        if (ig < nc) {  // G = K K^T: K-major view of the K tile (K = feature index, two 64-wide boxes)
+        // G = K K^T (K-major view of the K tile, K = feature index, two 64-wide boxes); the gram of
+        // chunk c + 2 waits for W^T of chunk c + 1 so that it fills a gap of the pipe (measured)
+        if (ig < nc && ig <= iw + 1) {
             const uint32_t gc = g + ig;
             if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
                 (ig == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
