@@ -33,14 +33,17 @@
 // T_C falls far below the fp32 range over long segments: it is returned as a
 // mantissa and a power-of-two exponent.
 //
-// Roles (320 threads): warp 0 loads keys and values (TMA) and writes the gate
-// tables; warp 1 issues the MMAs as their inputs become ready; warps 6-9 (the
-// prep warpgroup) turn each gram into That; warps 2-5 (the state warpgroup)
-// run the pass between GEMM1 and GEMM2, convert W/U into MMA operands and
-// write the result.  The prep warpgroup runs ahead of the state chain: only
-// the pass, the W conversion and the two state GEMMs are serial per chunk.
-// They meet on mbarriers; every wait is bounded and a wait that runs out sets
-// the device error word.
+// Roles (480 threads): warp 0 loads keys and values (TMA) and writes the gate
+// tables.  Two single-thread issuers send the MMAs as their inputs become
+// ready: warp 1 W'^T, GEMM1 of the T half and GEMM2, warp 14 GEMM1 of the S
+// half, U^T and the gram (one thread issues a small MMA only about every 60
+// cycles; two come closer to the tensor pipe's own rate).  Warps 6-13 (the
+// prep warps) turn each gram into That; warps 2-5 (the state warpgroup) run
+// the pass between GEMM1 and GEMM2, convert W/U into MMA operands and write
+// the result.  The prep warps run ahead of the state chain: only the pass,
+// the W conversion and the two state GEMMs are serial per chunk.  The roles
+// meet on mbarriers; every wait is bounded and a wait that runs out sets the
+// device error word.
 // One CTA per SM, persistent over (segment, layer, head) items taken from an
 // atomic queue in longest-body-first order.
 #include <cuda.h>
@@ -66,8 +69,8 @@ constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
 constexpr int kKStages = 3;       // K ring depth (the gram of a chunk wants its keys early)
 constexpr int kGateSlots = 4;     // per-chunk gate tables in flight
-constexpr int kThreads = 448;
-constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6;
+constexpr int kThreads = 480;
+constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6, kWarpMMA2 = 14;
 constexpr int kPrepThreads = 256;  // warps 6-13: two warps per tensor-memory lane quarter
 
 // Shared memory map (byte offsets; every operand region is 1024-byte aligned).
@@ -87,10 +90,10 @@ struct Misc {
     uint64_t fullK[kKStages], emptyK[kKStages], fullV, emptyV;
     uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables of a chunk written
     uint64_t g_done, g_read;      // gram committed; gram read by the prep warpgroup
-    uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done
+    uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done (one commit per issuer)
     uint64_t u_done, w_done;      // U^T, W^T committed
     uint64_t u_cvt, w_cvt;        // U~ and W operands written
-    uint64_t x_done_s, x_done, xs_free, y_ready, d_ready, drain;  // GEMM1 S half / all done; X''_S read
+    uint64_t x_done_s, x_done, xs_free, y_ready, d_ready, drain;  // GEMM1 S half / T half done; X''_S read
     alignas(16) float lg2[kGateSlots][kC];  // slot gc % kGateSlots; every table is read as float4
     alignas(16) float beta[kGateSlots][kC];
     alignas(16) float up[kGateSlots][kC];
@@ -668,18 +671,36 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CU
 // of a barrier's phase k is only made once its phase k - 1 is known to be
 // complete (by an earlier test or an earlier item), so a parity test cannot
 // mistake an old phase for a new one.
+// An issuer's idle step: the start of its idle time (t_idle, 0 if it was
+// busy), or 0 once the CTA aborted or this wait ran out (which sets the abort
+// flag and the device error word).
+__device__ __forceinline__ uint64_t issuer_idle(Misc* ms, const TcArgs& a, uint64_t t_idle) {
+    if (*(volatile int*)&ms->abort_flag) return 0;
+    const uint64_t now = globaltimer_ns();
+    if (t_idle != 0 && now - t_idle > a.wait_ns) {
+        *(volatile int*)&ms->abort_flag = 1;
+        set_error(a.err, kErrTimeout);
+        return 0;
+    }
+    return t_idle != 0 ? t_idle : now;
+}
+
+// Warp 1, one thread: the state chain's MMAs, each group as soon as its
+// inputs are ready (a dataflow loop that tests barrier phases without
+// blocking); priority W'^T, GEMM2, GEMM1 (T half).
 __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
     if (nc == 0) return;
     const uint32_t sb = smem_u32(smem);
-    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, au = sb + OFF_AU, bt = sb + OFF_BT, vt = sb + OFF_V;
+    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, au = sb + OFF_AU, bt = sb + OFF_BT;
     auto ktile = [&](uint32_t gc) { return sb + OFF_K + (gc % kKStages) * kTile; };
-    int ig = 0, iu = 0, iw = 0, i1 = 0, i2 = 0;
+    int iw = 0, i1 = 0, i2 = 0;
     uint64_t t_idle = 0;
     while (i2 < nc) {
         bool any = false;
-        if (iw < iu && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_S columns
+        if (iw < nc && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_S columns
             const uint32_t gc = g + iw;
-            if (iw == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1)) {  // the pass has read the previous X''_S
+            if (mbar_test(&ms->that_ready, gc & 1) &&
+                (iw == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the pass has read the previous X''_S
                 tc_fence_after();
                 const uint64_t a0 = sdesc_sw128(ktile(gc), 8192, 1024), bh = sdesc_sw128(bt, 0, 1024),
                                bl = sdesc_sw128(bt + 16384, 0, 1024);
@@ -689,7 +710,7 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                     mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bl + 2 * k, ID_WU, true);
                 }
                 mma_commit(&ms->w_done);
-                mma_commit(&ms->bt_free);  // (the U^T MMAs of this chunk were issued before)
+                mma_commit(&ms->bt_free);
                 ++iw;
                 any = true;
             }
@@ -709,26 +730,55 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                     mma_bf16_ss(tmem + TM_DS, ys + 2 * k, bk, ID_G2, true);
                     mma_bf16_ss(tmem + TM_DS, uu + 2 * k, bk, ID_G2, true);
                 }
+                // (the gram of this K tile completed before That, hence before W'^T and this GEMM2)
                 mma_commit(&ms->d_ready);
                 mma_commit(&ms->emptyK[gc % kKStages]);
                 ++i2;
                 any = true;
             }
         }
-        if (i1 < iw && i2 == i1) {  // GEMM1 (tf32): X''_h = D''_h W^T, A = the state in tensor memory
+        if (i1 < iw && i2 == i1) {  // GEMM1 (tf32), T half: X''_T = D''_T W^T, A = the state in tensor memory
             const uint32_t gc = g + i1;
             if (mbar_test(&ms->w_cvt, gc & 1) && (i1 == 0 || mbar_test(&ms->d_ready, (gc - 1) & 1))) {
                 tc_fence_after();
                 const uint64_t b0 = sdesc_sw128(bw, 0, 1024);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {  // the S half first: its pass frees the W^T columns
-                    const int h = 1 - hh;
 #pragma unroll 4  // (a measured balance of issue rate and code size)
-                    for (int k = 0; k < 16; ++k)
-                        mma_tf32_ts(tmem + TM_XT + 64 * h, tmem + 128 * h + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3),
-                                    ID_G1, k > 0);
-                    mma_commit(hh ? &ms->x_done : &ms->x_done_s);
-                }
+                for (int k = 0; k < 16; ++k)
+                    mma_tf32_ts(tmem + TM_XT, tmem + TM_DT + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3), ID_G1, k > 0);
+                mma_commit(&ms->x_done);
+                ++i1;
+                any = true;
+            }
+        }
+        if (any) {  // (no sleep when idle: a sleeping issuer answers its barriers late)
+            t_idle = 0;
+        } else if ((t_idle = issuer_idle(ms, a, t_idle)) == 0) {
+            return;
+        }
+    }
+}
+
+// Warp 14, one thread: GEMM1 of the S half (on the state chain), then the
+// prep chain's U^T and gram.  Its commits cover only its own MMAs: every
+// reader of their results waits on its barriers (x_done_s, u_done, g_done,
+// and bt_free, which takes one commit from each issuer).
+__device__ void mma_role2(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
+    if (nc == 0) return;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bw = sb + OFF_BW, bt = sb + OFF_BT, vt = sb + OFF_V;
+    int ig = 0, iu = 0, i1 = 0;
+    uint64_t t_idle = 0;
+    while (i1 < nc || ig < nc) {
+        bool any = false;
+        if (i1 < iu) {  // GEMM1 (tf32), S half: X''_S = D''_S W^T (the W^T staged in X_S has been converted)
+            const uint32_t gc = g + i1;
+            if (mbar_test(&ms->w_cvt, gc & 1) && (i1 == 0 || mbar_test(&ms->d_ready, (gc - 1) & 1))) {
+                tc_fence_after();
+                const uint64_t b0 = sdesc_sw128(bw, 0, 1024);
+#pragma unroll 4
+                for (int k = 0; k < 16; ++k)
+                    mma_tf32_ts(tmem + TM_XS, tmem + TM_DS + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3), ID_G1, k > 0);
+                mma_commit(&ms->x_done_s);
                 ++i1;
                 any = true;
             }
@@ -743,18 +793,20 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_U, a0 + 128 * k, b0 + 2 * k, ID_WU, k > 0);
                 mma_commit(&ms->u_done);
                 mma_commit(&ms->emptyV);
+                mma_commit(&ms->bt_free);
                 ++iu;
                 any = true;
             }
         }
         // G = K K^T (K-major view of the K tile, K = feature index, two 64-wide boxes); the gram of
-        // chunk c + 2 waits for W^T of chunk c + 1 so that it fills a gap of the pipe (measured)
-        if (ig < nc && ig <= iw + 1) {
+        // chunk c + 2 waits until GEMM1 (S half) of chunk c is issued, so that it fills a gap of the
+        // pipe (measured against gating it on W^T: -0.4 %)
+        if (ig < nc && ig <= i1 + 1) {
             const uint32_t gc = g + ig;
             if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
                 (ig == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
                 tc_fence_after();
-                const uint64_t d0 = sdesc_sw128(ktile(gc), 0, 1024);
+                const uint64_t d0 = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 0, 1024);
 #pragma unroll 2
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t d = d0 + 512 * (k >> 2) + 2 * (k & 3);
@@ -765,18 +817,10 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 any = true;
             }
         }
-        if (any) {  // (no sleep when idle: a sleeping issuer answers its barriers late)
+        if (any) {
             t_idle = 0;
-        } else {
-            if (*(volatile int*)&ms->abort_flag) return;
-            const uint64_t now = globaltimer_ns();
-            if (t_idle == 0) {
-                t_idle = now;
-            } else if (now - t_idle > a.wait_ns) {
-                *(volatile int*)&ms->abort_flag = 1;
-                set_error(a.err, kErrTimeout);
-                return;
-            }
+        } else if ((t_idle = issuer_idle(ms, a, t_idle)) == 0) {
+            return;
         }
     }
 }
@@ -951,11 +995,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ms->fullK[s], 1);
             mbar_init(&ms->emptyK[s], 1);
         }
-        for (int s = 0; s < kGateSlots; ++s) mbar_init(&ms->gready[s], 1);
-        uint64_t* one[] = {&ms->fullV, &ms->emptyV, &ms->g_done, &ms->g_read, &ms->that_ready, &ms->bt_free,
-                           &ms->u_done, &ms->w_done, &ms->u_cvt, &ms->w_cvt, &ms->x_done_s, &ms->x_done, &ms->xs_free, &ms->y_ready,
-                           &ms->d_ready, &ms->drain};
-        for (uint64_t* b : one) mbar_init(b, 1);
+        // fullV .. drain (gready included) are consecutive in Misc: one arrival each, but bt_free (both
+        // issuers read That) and drain (both issuers' MMAs) take two
+        for (uint64_t* b = &ms->fullV; b <= &ms->drain; ++b) mbar_init(b, b == &ms->bt_free || b == &ms->drain ? 2 : 1);
         ms->abort_flag = 0;
         fence_mbar_init();
     }
@@ -991,6 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             producer_role(ms, smem, a, &tmk, &tmv, g, nc, layer, head, b0, b1, lane);
         } else if (warp == kWarpMMA) {
             if (lane == 0) mma_role(ms, smem, a, tmem, g, nc);
+        } else if (warp == kWarpMMA2) {
+            if (lane == 0) mma_role2(ms, smem, a, tmem, g, nc);
         } else if (is_state) {
             state_role(ms, smem, a, tmem, g, nc, obj, q, lane);
         } else {
@@ -1001,8 +1045,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         g += nc;
     }
-    // Drain: every MMA this CTA issued has completed before tensor memory is freed.
-    if (warp == kWarpMMA) {
+    // Drain: every MMA this CTA issued (from both issuers) has completed before tensor memory is freed.
+    if (warp == kWarpMMA || warp == kWarpMMA2) {
         if (lane == 0) {
             mma_commit(&ms->drain);
             for (uint32_t i = 0; i < a.wait_limit && !mbar_try_wait(&ms->drain, 0); ++i) {
