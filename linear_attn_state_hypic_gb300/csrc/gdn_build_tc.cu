@@ -19,8 +19,8 @@
 //   solve     That from G and the gates      CUDA cores + warp MMAs (block-triangular inverse)
 //   W'^T, U^T K^T (That Diag(up))^T, V^T That^T   bf16 MMA, M=128 N=64 K=64
 //   GEMM1     X''_h = D''_h W'^T             tf32 MMA, A read from tensor memory
-//   pass      Y''_h = Diag(f_h) X''_h^T (bf16, smem)
-//   GEMM2     D''_h += Y''_h K  (+ U~^T K for S) bf16 MMA, M=128 N=128 K=64
+//   pass      Y''_T = Diag(f_T) X''_T^T, Y''_S = Diag(f_S) X''_S^T + U~ (bf16, smem)
+//   GEMM2     D''_h += Y''_h K                bf16 MMA, M=128 N=128 K=64
 // with up_t = g_t / g_C^(1/2) in W' = W / g_C^(1/2) and f_h = -g_C^(1/2)/g_t
 // (times the renormalisation factor): the in-chunk decay is centred on the
 // middle of its range so that neither factor leaves the float32 range for
@@ -78,8 +78,7 @@ constexpr uint32_t kTile = 16384;                       // 64 tokens x 128 bf16,
 constexpr uint32_t OFF_K = 0;                           // K ring
 constexpr uint32_t OFF_V = OFF_K + kKStages * kTile;    // V (one chunk: read only by the U^T MMA)
 constexpr uint32_t OFF_BW = OFF_V + kTile;              // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
-constexpr uint32_t OFF_AU = OFF_BW + 32768;             // U~^T: bf16 [128 n][64 t], K-major
-constexpr uint32_t OFF_AY = OFF_AU + 16384;             // Y''^T: bf16 [128 n][64 t]: T hi, S, T lo
+constexpr uint32_t OFF_AY = OFF_BW + 32768;             // Y''^T: bf16 [128 n][64 t]: T hi, S (with U~), T lo
 constexpr uint32_t OFF_BT = OFF_AY + 49152;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
 constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
 constexpr int kAS = 68;                                 // row stride (floats) of that scratch
@@ -92,7 +91,7 @@ struct Misc {
     uint64_t g_done, g_read;      // gram committed; gram read by the prep warpgroup
     uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done (one commit per issuer)
     uint64_t u_done, w_done;      // U^T, W^T committed
-    uint64_t u_cvt, w_cvt;        // U~ and W operands written
+    uint64_t w_cvt;               // W operand written
     uint64_t x_done_s, x_done, xs_free, y_ready, d_ready, drain;  // GEMM1 S half / T half done; X''_S read
     alignas(16) float lg2[kGateSlots][kC];  // slot gc % kGateSlots; every table is read as float4
     alignas(16) float beta[kGateSlots][kC];
@@ -448,32 +447,6 @@ __device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
     }
 }
 
-// U^T (lane n holds U[.][n]) -> U~^T = U^T Diag(uf) as a bf16 K-major
-// [128 n][64 t] operand (uf: the chunk's U factors, see state_plan).
-__device__ void convert_u(const Misc* ms, uint32_t au, uint32_t tmem, int q, int lane) {
-    const int i = 32 * q + lane;
-    const uint32_t tl = tmem + ((32u * q) << 16);
-    const float* uf = ms->uf;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
-        tmem_ld32(tl + TM_U + 32 * half, w);
-        tmem_wait_ld();
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = 32 * half + 8 * jj + 2 * k;
-                pk[k] = pack_bf16(__uint_as_float(w[8 * jj + 2 * k]) * uf[t],
-                                  __uint_as_float(w[8 * jj + 2 * k + 1]) * uf[t + 1]);
-            }
-            const uint32_t off = i * 128u + ((uint32_t)((4 * half + jj) ^ (i & 7)) << 4);
-            st_shared_v4(au + off, pk[0], pk[1], pk[2], pk[3]);
-        }
-    }
-}
-
 // ---------------------------------------------------------- state roles --
 // Thread n of the state warpgroup owns tensor-memory lane n = 32q + lane:
 // row n of D'_T (column n of T) and of D'_S (column n of S).
@@ -518,38 +491,45 @@ __device__ __noinline__ float state_rescale(uint32_t addr, float sc, bool want_m
     return mloc;
 }
 
-// After GEMM1 of a chunk, half h (0 = T, 1 = S): Y''_h = Diag-scaled X''_h
-// rows into shared memory
+// After GEMM1 of a chunk, half h (0 = T, 1 = S): Y''_h into shared memory
 // (bf16, K-major [128 n][64 t]; Y''_T also as its bf16 residual):
-//   Y''_T[n][t] = fT[t] X''_T[n][t],  Y''_S[n][t] = fS[t] X''_S[n][t].
-// On a renormalisation chunk the stored state is also rescaled in tensor
-// memory, D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new
-// T rows is returned (else 0).
+//   Y''_T[n][t] = fT[t] X''_T[n][t],
+//   Y''_S[n][t] = fS[t] X''_S[n][t] + uf[t] U^T[n][t]
+// (the S half of GEMM2 multiplies both terms by the same keys, so U~ rides in
+// Y''_S and is rounded to bf16 once, with the correction).  On a
+// renormalisation chunk the stored state is also rescaled in tensor memory,
+// D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new T rows
+// is returned (else 0).
 template <int h>
 __device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, float dS, uint32_t tmem, int q,
                             int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        const float* f = (h ? ms->fS : ms->fT) + 32 * half;
-        uint32_t x[32];
-        tmem_ld32(tl + (h ? TM_XS : TM_XT) + 32 * half, x);
+    for (int qt = 0; qt < 4; ++qt) {  // 16 columns (tokens) at a time
+        const float* f = (h ? ms->fS : ms->fT) + 16 * qt;
+        const float* uf = ms->uf + 16 * qt;
+        uint32_t x[16], u[16];
+        tmem_ld16(tl + (h ? TM_XS : TM_XT) + 16 * qt, x);
+        if (h) tmem_ld16(tl + TM_U + 16 * qt, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < 2; ++jj) {
             uint32_t pk[4], lo[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = 8 * jj + 2 * k;
-                const float y0 = f[t] * __uint_as_float(x[t]);
-                const float y1 = f[t + 1] * __uint_as_float(x[t + 1]);
-                if (h)
+                float y0 = f[t] * __uint_as_float(x[t]);
+                float y1 = f[t + 1] * __uint_as_float(x[t + 1]);
+                if (h) {
+                    y0 = fmaf(uf[t], __uint_as_float(u[t]), y0);
+                    y1 = fmaf(uf[t + 1], __uint_as_float(u[t + 1]), y1);
                     pk[k] = pack_bf16(y0, y1);
-                else
+                } else {
                     split2_bf16(y0, y1, pk[k], lo[k]);
+                }
             }
-            const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((4 * half + jj) ^ (n & 7)) << 4);
+            const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((2 * qt + jj) ^ (n & 7)) << 4);
             st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
             if (!h) st_shared_v4(ay + 32768u + off, lo[0], lo[1], lo[2], lo[3]);
         }
@@ -691,7 +671,7 @@ __device__ __forceinline__ uint64_t issuer_idle(Misc* ms, const TcArgs& a, uint6
 __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
     if (nc == 0) return;
     const uint32_t sb = smem_u32(smem);
-    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, au = sb + OFF_AU, bt = sb + OFF_BT;
+    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, bt = sb + OFF_BT;
     auto ktile = [&](uint32_t gc) { return sb + OFF_K + (gc % kKStages) * kTile; };
     int iw = 0, i1 = 0, i2 = 0;
     uint64_t t_idle = 0;
@@ -715,20 +695,18 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 any = true;
             }
         }
-        if (i2 < i1) {  // GEMM2 (bf16): D''_T += Y''_T K; D''_S += Y''_S K + U~^T K
+        if (i2 < i1) {  // GEMM2 (bf16): D''_T += Y''_T K (hi + lo); D''_S += Y''_S K
             const uint32_t gc = g + i2;
-            if (mbar_test(&ms->y_ready, gc & 1) && mbar_test(&ms->u_cvt, gc & 1)) {
+            if (mbar_test(&ms->y_ready, gc & 1)) {
                 tc_fence_after();
                 const uint64_t b0 = sdesc_sw128(ktile(gc), 8192, 1024), yh = sdesc_sw128(ay, 0, 1024),
-                               yl = sdesc_sw128(ay + 32768, 0, 1024), ys = sdesc_sw128(ay + 16384, 0, 1024),
-                               uu = sdesc_sw128(au, 0, 1024);
+                               yl = sdesc_sw128(ay + 32768, 0, 1024), ys = sdesc_sw128(ay + 16384, 0, 1024);
 #pragma unroll 2
                 for (int k = 0; k < 4; ++k) {
                     const uint64_t bk = b0 + 128 * k;
                     mma_bf16_ss(tmem + TM_DT, yh + 2 * k, bk, ID_G2, true);
                     mma_bf16_ss(tmem + TM_DT, yl + 2 * k, bk, ID_G2, true);
                     mma_bf16_ss(tmem + TM_DS, ys + 2 * k, bk, ID_G2, true);
-                    mma_bf16_ss(tmem + TM_DS, uu + 2 * k, bk, ID_G2, true);
                 }
                 // (the gram of this K tile completed before That, hence before W'^T and this GEMM2)
                 mma_commit(&ms->d_ready);
@@ -786,7 +764,7 @@ __device__ void mma_role2(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         if (iu < ig) {  // U^T = V^T That^T
             const uint32_t gc = g + iu;
             if (mbar_test(&ms->that_ready, gc & 1) && mbar_test(&ms->fullV, gc & 1) &&
-                (iu == 0 || mbar_test(&ms->u_cvt, (gc - 1) & 1))) {
+                (iu == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the S pass has read the previous U^T
                 tc_fence_after();
                 const uint64_t a0 = sdesc_sw128(vt, 8192, 1024), b0 = sdesc_sw128(bt + 8192, 0, 1024);
 #pragma unroll 1
@@ -899,8 +877,7 @@ __device__ __forceinline__ StatePlan state_plan(Misc* ms, uint32_t gc, bool last
 }
 
 // Chunk gc's factor tables and plan, then its W operand (on the chain to
-// GEMM1), then its U~ operand (off it: only GEMM2 reads it, once the previous
-// GEMM2 has).
+// GEMM1).
 __device__ __forceinline__ bool state_prepare(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t gc,
                                               bool last, int since, float lsT, float lsS, float m, int q, int lane,
                                               StatePlan& pl) {
@@ -915,15 +892,6 @@ __device__ __forceinline__ bool state_prepare(Misc* ms, uint8_t* smem, const TcA
     tc_fence_before();
     named_sync(2);
     if (q == 0 && lane == 0) mbar_arrive(&ms->w_cvt);
-    ok = wait_bar(&ms->u_done, gc & 1, ms, a);
-    ok = ok && (gc == 0 || wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a));  // the previous GEMM2 has read U~
-    if (!wg_all(2, ok)) return false;
-    tc_fence_after();
-    convert_u(ms, smem_u32(smem) + OFF_AU, tmem, q, lane);
-    fence_async_smem();
-    tc_fence_before();
-    named_sync(2);
-    if (q == 0 && lane == 0) mbar_arrive(&ms->u_cvt);
     return true;
 }
 
@@ -946,11 +914,13 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         const uint32_t gc = g + c;
         if (c > 0) {
             const uint32_t gp = gc - 1;
-            if (!wg_all(2, wait_bar(&ms->x_done_s, gp & 1, ms, a))) return;
+            bool ok = wait_bar(&ms->x_done_s, gp & 1, ms, a);
+            ok = ok && wait_bar(&ms->u_done, gp & 1, ms, a);
+            if (!wg_all(2, ok)) return;
             tc_fence_after();
             state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
             tc_fence_before();
-            named_sync(2);  // every lane has read X''_S: the next W'^T may overwrite those columns
+            named_sync(2);  // every lane has read X''_S and U^T: the next W'^T and U^T may overwrite them
             if (n == 0) mbar_arrive(&ms->xs_free);
             if (!wg_all(2, wait_bar(&ms->x_done, gp & 1, ms, a))) return;
             tc_fence_after();
