@@ -19,8 +19,10 @@
 //   solve     That from G and the gates      CUDA cores + warp MMAs (block-triangular inverse)
 //   W'^T, U^T K^T (That Diag(up))^T, V^T That^T   bf16 MMA, M=128 N=64 K=64
 //   GEMM1     X''_h = D''_h W'^T             tf32 MMA, A read from tensor memory
-//   pass      Y''_T = Diag(f_T) X''_T^T, Y''_S = Diag(f_S) X''_S^T + U~ (bf16, smem)
-//   GEMM2     D''_h += Y''_h K                bf16 MMA, M=128 N=128 K=64
+//   pass      Y''_T = Diag(f_T) X''_T^T (bf16, in place of X''_T in tensor memory),
+//             Y''_S = Diag(f_S) X''_S^T + U~ (bf16, smem)
+//   GEMM2     D''_h += Y''_h K                bf16 MMA, M=128 N=128 K=64 (A of the T half
+//                                             read from tensor memory)
 // with up_t = g_t / g_C^(1/2) in W' = W / g_C^(1/2) and f_h = -g_C^(1/2)/g_t
 // (times the renormalisation factor): the in-chunk decay is centred on the
 // middle of its range so that neither factor leaves the float32 range for
@@ -78,8 +80,8 @@ constexpr uint32_t kTile = 16384;                       // 64 tokens x 128 bf16,
 constexpr uint32_t OFF_K = 0;                           // K ring
 constexpr uint32_t OFF_V = OFF_K + kKStages * kTile;    // V (one chunk: read only by the U^T MMA)
 constexpr uint32_t OFF_BW = OFF_V + kTile;              // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
-constexpr uint32_t OFF_AY = OFF_BW + 32768;             // Y''^T: bf16 [128 n][64 t]: T hi, S (with U~), T lo
-constexpr uint32_t OFF_BT = OFF_AY + 49152;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
+constexpr uint32_t OFF_AY = OFF_BW + 32768;             // Y''_S (with U~): bf16 [128 n][64 t], K-major
+constexpr uint32_t OFF_BT = OFF_AY + 16384;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
 constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
 constexpr int kAS = 68;                                 // row stride (floats) of that scratch
 constexpr uint32_t OFF_PT = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;  // solve scratch: 32 x 36 fp32
@@ -491,15 +493,17 @@ __device__ __noinline__ float state_rescale(uint32_t addr, float sc, bool want_m
     return mloc;
 }
 
-// After GEMM1 of a chunk, half h (0 = T, 1 = S): Y''_h into shared memory
-// (bf16, K-major [128 n][64 t]; Y''_T also as its bf16 residual):
-//   Y''_T[n][t] = fT[t] X''_T[n][t],
-//   Y''_S[n][t] = fS[t] X''_S[n][t] + uf[t] U^T[n][t]
-// (the S half of GEMM2 multiplies both terms by the same keys, so U~ rides in
-// Y''_S and is rounded to bf16 once, with the correction).  On a
-// renormalisation chunk the stored state is also rescaled in tensor memory,
-// D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new T rows
-// is returned (else 0).
+// After GEMM1 of a chunk, half h (0 = T, 1 = S), the A operand of GEMM2:
+//   Y''_T[n][t] = fT[t] X''_T[n][t] as bf16 hi + lo, written over X''_T in
+//     tensor memory: lane n, tokens 16k..16k+15 in columns 16k..16k+7 (hi)
+//     and 16k+8..16k+15 (lo), two tokens per column, so that each group of
+//     16 columns is read and then rewritten in place;
+//   Y''_S[n][t] = fS[t] X''_S[n][t] + uf[t] U^T[n][t] as bf16 into shared
+//     memory (K-major [128 n][64 t]); the S half of GEMM2 multiplies both
+//     terms by the same keys, so U~ rides in Y''_S, rounded once.
+// On a renormalisation chunk the stored state is also rescaled in tensor
+// memory, D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new
+// T rows is returned (else 0).
 template <int h>
 __device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, float dS, uint32_t tmem, int q,
                             int lane) {
@@ -513,9 +517,10 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, floa
         tmem_ld16(tl + (h ? TM_XS : TM_XT) + 16 * qt, x);
         if (h) tmem_ld16(tl + TM_U + 16 * qt, u);
         tmem_wait_ld();
+        uint32_t hl[16];  // (T half: hi in [0, 8), lo in [8, 16))
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-            uint32_t pk[4], lo[4];
+            uint32_t pk[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int t = 8 * jj + 2 * k;
@@ -526,14 +531,17 @@ __device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, floa
                     y1 = fmaf(uf[t + 1], __uint_as_float(u[t + 1]), y1);
                     pk[k] = pack_bf16(y0, y1);
                 } else {
-                    split2_bf16(y0, y1, pk[k], lo[k]);
+                    split2_bf16(y0, y1, hl[4 * jj + k], hl[8 + 4 * jj + k]);
                 }
             }
-            const uint32_t off = h * 16384u + n * 128u + ((uint32_t)((2 * qt + jj) ^ (n & 7)) << 4);
-            st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
-            if (!h) st_shared_v4(ay + 32768u + off, lo[0], lo[1], lo[2], lo[3]);
+            if (h) {
+                const uint32_t off = n * 128u + ((uint32_t)((2 * qt + jj) ^ (n & 7)) << 4);
+                st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
+            }
         }
+        if (!h) tmem_st16(tl + TM_XT + 16 * qt, hl);
     }
+    if (!h) tmem_wait_st();
     return rn ? state_rescale(tl + (h ? TM_DS : TM_DT), h ? dS : dT, !h) : 0.f;
 }
 
@@ -695,17 +703,16 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
                 any = true;
             }
         }
-        if (i2 < i1) {  // GEMM2 (bf16): D''_T += Y''_T K (hi + lo); D''_S += Y''_S K
+        if (i2 < i1) {  // GEMM2 (bf16): D''_T += Y''_T K (hi + lo, A in the X_T columns); D''_S += Y''_S K
             const uint32_t gc = g + i2;
             if (mbar_test(&ms->y_ready, gc & 1)) {
                 tc_fence_after();
-                const uint64_t b0 = sdesc_sw128(ktile(gc), 8192, 1024), yh = sdesc_sw128(ay, 0, 1024),
-                               yl = sdesc_sw128(ay + 32768, 0, 1024), ys = sdesc_sw128(ay + 16384, 0, 1024);
+                const uint64_t b0 = sdesc_sw128(ktile(gc), 8192, 1024), ys = sdesc_sw128(ay, 0, 1024);
 #pragma unroll 2
                 for (int k = 0; k < 4; ++k) {
                     const uint64_t bk = b0 + 128 * k;
-                    mma_bf16_ss(tmem + TM_DT, yh + 2 * k, bk, ID_G2, true);
-                    mma_bf16_ss(tmem + TM_DT, yl + 2 * k, bk, ID_G2, true);
+                    mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 16 * k, bk, ID_G2, true);
+                    mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 16 * k + 8, bk, ID_G2, true);
                     mma_bf16_ss(tmem + TM_DS, ys + 2 * k, bk, ID_G2, true);
                 }
                 // (the gram of this K tile completed before That, hence before W'^T and this GEMM2)
