@@ -651,14 +651,12 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CU
     }
 }
 
-// Warp 1, lane 0: issues every MMA of the item as soon as its inputs are
-// ready, in this priority: W^T, GEMM2, GEMM1, U^T, gram.  GEMM1 runs its S
-// half first; W^T of the next chunk reuses the X''_S columns and waits only
-// for the S half of this chunk's pass, so it runs while the pass does the T
-// half.  A readiness test
-// of a barrier's phase k is only made once its phase k - 1 is known to be
-// complete (by an earlier test or an earlier item), so a parity test cannot
-// mistake an old phase for a new one.
+// The MMA issuers.  W^T of the next chunk reuses the X''_S columns and waits
+// only for the S half of this chunk's pass, so it runs while the pass does the
+// T half.  A readiness test of a barrier's phase k is only made once its phase
+// k - 1 is known to be complete (by an earlier test or an earlier item), so a
+// parity test cannot mistake an old phase for a new one.
+
 // An issuer's idle step: the start of its idle time (t_idle, 0 if it was
 // busy), or 0 once the CTA aborted or this wait ran out (which sets the abort
 // flag and the device error word).
