@@ -81,17 +81,31 @@ constexpr uint32_t OFF_K = 0;                           // K ring
 constexpr uint32_t OFF_V = OFF_K + kKStages * kTile;    // V (one chunk: read only by the U^T MMA)
 constexpr uint32_t OFF_BW = OFF_V + kTile;              // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
 constexpr uint32_t OFF_AY = OFF_BW + 32768;             // Y''_S (with U~): bf16 [128 n][64 t], K-major
-constexpr uint32_t OFF_BT = OFF_AY + 16384;             // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
-constexpr uint32_t OFF_AS = OFF_BT + 24576;             // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
+constexpr uint32_t kBT = 24576;                         // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
+constexpr uint32_t OFF_BT = OFF_AY + 16384;             // two of them: chunk gc uses buffer gc % 2
+constexpr uint32_t OFF_AS = OFF_BT + 2 * kBT;           // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
 constexpr int kAS = 68;                                 // row stride (floats) of that scratch
 constexpr uint32_t OFF_PT = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;  // solve scratch: 32 x 36 fp32
 constexpr uint32_t OFF_MISC = OFF_PT + 5120;
+
+// An item of the queue as the producer publishes it to the other roles.
+struct ItemSlot {
+    int64_t b0, b1, obj;  // body [b0, b1) in the token index, output object
+    uint32_t g;           // CTA-wide index of the item's first chunk
+    int nc, layer, head;  // nc < 0: the queue is exhausted
+};
+constexpr int kItemSlots = 4;
+constexpr int kSlotReaders = 4;  // warp 1, warp 14, the state warpgroup, the prep warps
 
 struct Misc {
     uint64_t fullK[kKStages], emptyK[kKStages], fullV, emptyV;
     uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables of a chunk written
     uint64_t g_done, g_read;      // gram committed; gram read by the prep warpgroup
-    uint64_t that_ready, bt_free; // That written; the W/U MMAs that read it are done (one commit per issuer)
+    // That of chunk gc written (that_ready[gc % 2]); the W/U MMAs that read it are done (bt_free[gc % 2],
+    // one commit from each issuer).  One barrier per That buffer: the prep may run two chunks ahead of
+    // an issuer, and an issuer one chunk ahead of the other, so a shared barrier could be two phases
+    // ahead of a parity wait or mix the commits of two chunks in one phase.
+    uint64_t that_ready[2], bt_free[2];
     uint64_t u_done, w_done;      // U^T, W^T committed
     uint64_t w_cvt;               // W operand written
     uint64_t x_done_s, x_done, xs_free, y_ready, d_ready, drain;  // GEMM1 S half / T half done; X''_S read
@@ -104,7 +118,8 @@ struct Misc {
     alignas(16) float uf[kC];    // U~ = Diag(uf) U
     float red[2][4];
     float red_ep[4];
-    int item;
+    uint64_t slot_full[kItemSlots], slot_read[kItemSlots];  // item slot written / copied by every reader
+    ItemSlot slots[kItemSlots];
     int abort_flag;
     uint32_t tmem_base;
 };
@@ -685,18 +700,19 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem
         bool any = false;
         if (iw < nc && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_S columns
             const uint32_t gc = g + iw;
-            if (mbar_test(&ms->that_ready, gc & 1) &&
-                (iw == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the pass has read the previous X''_S
+            if (mbar_test(&ms->that_ready[gc & 1], (gc >> 1) & 1) &&
+                (gc == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the pass has read the previous X''_S
                 tc_fence_after();
-                const uint64_t a0 = sdesc_sw128(ktile(gc), 8192, 1024), bh = sdesc_sw128(bt, 0, 1024),
-                               bl = sdesc_sw128(bt + 16384, 0, 1024);
+                const uint32_t btc = bt + (gc & 1) * kBT;
+                const uint64_t a0 = sdesc_sw128(ktile(gc), 8192, 1024), bh = sdesc_sw128(btc, 0, 1024),
+                               bl = sdesc_sw128(btc + 16384, 0, 1024);
 #pragma unroll 2
                 for (int k = 0; k < 4; ++k) {  // (a descriptor's address field counts 16-byte units)
                     mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bh + 2 * k, ID_WU, k > 0);
                     mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bl + 2 * k, ID_WU, true);
                 }
                 mma_commit(&ms->w_done);
-                mma_commit(&ms->bt_free);
+                mma_commit(&ms->bt_free[gc & 1]);
                 ++iw;
                 any = true;
             }
@@ -768,26 +784,26 @@ __device__ void mma_role2(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         }
         if (iu < ig) {  // U^T = V^T That^T
             const uint32_t gc = g + iu;
-            if (mbar_test(&ms->that_ready, gc & 1) && mbar_test(&ms->fullV, gc & 1) &&
-                (iu == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the S pass has read the previous U^T
+            if (mbar_test(&ms->that_ready[gc & 1], (gc >> 1) & 1) && mbar_test(&ms->fullV, gc & 1) &&
+                (gc == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the S pass has read the previous U^T
                 tc_fence_after();
-                const uint64_t a0 = sdesc_sw128(vt, 8192, 1024), b0 = sdesc_sw128(bt + 8192, 0, 1024);
+                const uint64_t a0 = sdesc_sw128(vt, 8192, 1024), b0 = sdesc_sw128(bt + (gc & 1) * kBT + 8192, 0, 1024);
 #pragma unroll 1
                 for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_U, a0 + 128 * k, b0 + 2 * k, ID_WU, k > 0);
                 mma_commit(&ms->u_done);
                 mma_commit(&ms->emptyV);
-                mma_commit(&ms->bt_free);
+                mma_commit(&ms->bt_free[gc & 1]);
                 ++iu;
                 any = true;
             }
         }
         // G = K K^T (K-major view of the K tile, K = feature index, two 64-wide boxes); the gram of
-        // chunk c + 2 waits until GEMM1 (S half) of chunk c is issued, so that it fills a gap of the
-        // pipe (measured against gating it on W^T: -0.4 %)
-        if (ig < nc && ig <= i1 + 1) {
+        // chunk c + 3 waits until GEMM1 (S half) of chunk c is issued, so that it fills a gap of the
+        // pipe (measured: one chunk less lookahead +0.7 %, two less +16 %)
+        if (ig < nc && ig <= i1 + 2) {
             const uint32_t gc = g + ig;
             if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
-                (ig == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
+                (gc == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
                 tc_fence_after();
                 const uint64_t d0 = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 0, 1024);
 #pragma unroll 2
@@ -826,11 +842,13 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->g_read);
         prep_solve(As, Ptmp, p);
-        if (!wg_all(1, gc == 0 || wait_bar(&ms->bt_free, (gc - 1) & 1, ms, a), kPrepThreads)) return;
-        prep_write_that(ms, As, bt, slot, p);
+        // the buffer's previous That (chunk gc - 2) has been read (the buffer's phases are waited in order)
+        if (!wg_all(1, gc < 2 || wait_bar(&ms->bt_free[gc & 1], ((gc >> 1) - 1) & 1, ms, a), kPrepThreads))
+            return;
+        prep_write_that(ms, As, bt + (gc & 1) * kBT, slot, p);
         fence_async_smem();
         named_sync(1, kPrepThreads);
-        if (p == 0) mbar_arrive(&ms->that_ready);
+        if (p == 0) mbar_arrive(&ms->that_ready[gc & 1]);
     }
 }
 
@@ -959,6 +977,32 @@ __device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
     state_init(tmem, q, lane);  // (I, 0) for the next item
 }
 
+// Producer, lane 0: the k-th item of this CTA into slot s (nc = -1 once the
+// queue is exhausted or the CTA aborted); the slot's previous item has been
+// copied by every reader.  Items are (segment, layer, head), segments in
+// longest-body-first order.
+__device__ __forceinline__ void publish_item(Misc* ms, const TcArgs& a, int k, int s) {
+    const int LH = a.n_layers * a.n_heads;
+    const ItemSlot& prev = ms->slots[(s + kItemSlots - 1) % kItemSlots];
+    const uint32_t g = k == 0 ? 0u : prev.g + (uint32_t)(prev.nc > 0 ? prev.nc : 0);
+    const int item = *(volatile int*)&ms->abort_flag ? a.n_items : (int)atomicAdd(a.counter, 1u);
+    ItemSlot& it = ms->slots[s];
+    if (item >= a.n_items) {
+        it.nc = -1;
+    } else {
+        const int pos = item / LH, lh = item % LH;
+        const int seg = a.order[pos];
+        it.layer = lh / a.n_heads;
+        it.head = lh % a.n_heads;
+        it.b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0);
+        it.b1 = a.cu[seg + 1];
+        it.nc = (int)((it.b1 - it.b0 + kC - 1) / kC);
+        it.obj = ((int64_t)seg * a.n_layers + it.layer) * a.n_heads + it.head;
+        it.g = g;
+    }
+    mbar_arrive(&ms->slot_full[s]);  // (release: the slot is visible to the readers that wait on it)
+}
+
 // ---------------------------------------------------------------- kernel --
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_build_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -977,7 +1021,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // fullV .. drain (gready included) are consecutive in Misc: one arrival each, but bt_free (both
         // issuers read That) and drain (both issuers' MMAs) take two
-        for (uint64_t* b = &ms->fullV; b <= &ms->drain; ++b) mbar_init(b, b == &ms->bt_free || b == &ms->drain ? 2 : 1);
+        for (uint64_t* b = &ms->fullV; b <= &ms->drain; ++b)
+            mbar_init(b, b == &ms->bt_free[0] || b == &ms->bt_free[1] || b == &ms->drain ? 2 : 1);
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(&ms->slot_full[s], 1);
+            mbar_init(&ms->slot_read[s], kSlotReaders);
+        }
         ms->abort_flag = 0;
         fence_mbar_init();
     }
@@ -996,35 +1045,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const int LH = a.n_layers * a.n_heads;
-    uint32_t g = 0;
-    for (;;) {
-        if (tid == 0) ms->item = (int)atomicAdd(a.counter, 1u);
-        __syncthreads();
-        const int item = ms->item;
-        if (item >= a.n_items || *(volatile int*)&ms->abort_flag) break;
-        const int pos = item / LH, lh = item % LH;
-        const int seg = a.order[pos];
-        const int layer = lh / a.n_heads, head = lh % a.n_heads;
-        const int64_t b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0), b1 = a.cu[seg + 1];
-        const int nc = (int)((b1 - b0 + kC - 1) / kC);
-        const int64_t obj = ((int64_t)seg * a.n_layers + layer) * a.n_heads + head;
+    // Every role runs through the items at its own pace: the producer takes
+    // them from the queue into a ring of kItemSlots slots, and the other roles
+    // copy them from there, so the next item's loads, gram, solve and W'^T
+    // overlap this item's last chunks and epilogue.  Across items the roles
+    // meet on the same barriers as within one (chunks are numbered CTA-wide).
+    for (int k = 0;; ++k) {
+        const int s = k % kItemSlots;
+        ItemSlot it;
         if (warp == kWarpTMA) {
-            producer_role(ms, smem, a, &tmk, &tmv, g, nc, layer, head, b0, b1, lane);
-        } else if (warp == kWarpMMA) {
-            if (lane == 0) mma_role(ms, smem, a, tmem, g, nc);
-        } else if (warp == kWarpMMA2) {
-            if (lane == 0) mma_role2(ms, smem, a, tmem, g, nc);
-        } else if (is_state) {
-            state_role(ms, smem, a, tmem, g, nc, obj, q, lane);
+            if (k >= kItemSlots && !wait_bar(&ms->slot_read[s], (k / kItemSlots - 1) & 1, ms, a)) break;
+            if (lane == 0) publish_item(ms, a, k, s);
+            __syncwarp();
+            it = ms->slots[s];
         } else {
-            prep_role(ms, smem, a, tmem, g, nc, tid - 32 * kWarpPrep0, q, lane);
+            const bool one = warp == kWarpMMA || warp == kWarpMMA2;
+            if (one && lane != 0) break;
+            const int id = is_state ? 2 : 1, cnt = is_state ? 128 : kPrepThreads;
+            const bool ok = wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a);
+            if (one ? !ok : !wg_all(id, ok, cnt)) break;
+            it = ms->slots[s];
+            if (!one) named_sync(id, cnt);
+            if (one || (tid & (cnt - 1)) == ((32 * (is_state ? kWarpState0 : kWarpPrep0)) & (cnt - 1)))
+                mbar_arrive(&ms->slot_read[s]);
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        g += nc;
+        if (it.nc < 0) break;
+        if (warp == kWarpTMA) {
+            producer_role(ms, smem, a, &tmk, &tmv, it.g, it.nc, it.layer, it.head, it.b0, it.b1, lane);
+        } else if (warp == kWarpMMA) {
+            mma_role(ms, smem, a, tmem, it.g, it.nc);
+        } else if (warp == kWarpMMA2) {
+            mma_role2(ms, smem, a, tmem, it.g, it.nc);
+        } else if (is_state) {
+            state_role(ms, smem, a, tmem, it.g, it.nc, it.obj, q, lane);
+        } else {
+            prep_role(ms, smem, a, tmem, it.g, it.nc, tid - 32 * kWarpPrep0, q, lane);
+        }
+        if (*(volatile int*)&ms->abort_flag) break;
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     // Drain: every MMA this CTA issued (from both issuers) has completed before tensor memory is freed.
     if (warp == kWarpMMA || warp == kWarpMMA2) {
         if (lane == 0) {
