@@ -41,13 +41,15 @@
 // half, U^T and the gram (one thread issues a small MMA only about every 60
 // cycles; two come closer to the tensor pipe's own rate).  Warps 6-13 (the
 // prep warps) turn each gram into That; warps 2-5 (the state warpgroup) run
-// the pass between GEMM1 and GEMM2, convert W/U into MMA operands and write
+// the pass between GEMM1 and GEMM2, convert W into an MMA operand and write
 // the result.  The prep warps run ahead of the state chain: only the pass,
 // the W conversion and the two state GEMMs are serial per chunk.  The roles
 // meet on mbarriers; every wait is bounded and a wait that runs out sets the
 // device error word.
 // One CTA per SM, persistent over (segment, layer, head) items taken from an
-// atomic queue in longest-body-first order.
+// atomic queue in longest-body-first order.  Warp 0 publishes them through a
+// ring of item slots and each role runs through them at its own pace, so one
+// item's first chunks overlap the previous item's last ones.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
