@@ -314,9 +314,10 @@ HYPIC_API hypic_status hypic_reuse_chain(const hypic_chain_args* args, void* wor
  *   - n_segments is limited to HYPIC_NOALLOC_MAX_SEGMENTS; a larger batch is
  *     rejected with HYPIC_ERR_WORKSPACE before anything is launched (use
  *     hypic_segment_build with a caller workspace instead).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *     with the calling thread's current device.  The first call on a device
+ *     may also make the CUDA runtime load this library's device code there
+ *     (lazy module loading); make that first call before any stream capture.
  *   - Every call on a device shares the one array.  Each call rewrites the
  *     whole order and zeroes the counter before using them, but calls whose
  *     work overlaps on the GPU (other streams, other threads) race on it:

@@ -8,7 +8,6 @@
 #include <string.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "../../include/hypic.h"
 #include "common.cuh"
@@ -42,29 +41,15 @@ hypic_status cuda_fail(cudaError_t e, const char* where) {
     return fail(HYPIC_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
-// Address of the device error word on the current device (looked up once per
-// device; host code cannot take the address of a __device__ variable itself).
+// Address of the device error word on the current device.  Host code cannot
+// take the address of a __device__ variable itself, so it is looked up on every
+// call (a cheap host-side query): an address cached per device ordinal would go
+// stale once the device's primary context is reset and the module reloaded.
 unsigned* err_word(cudaError_t* e_out) {
-    static std::mutex mu;
-    static unsigned* cache[128] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 128) {
-        *e_out = e != cudaSuccess ? e : cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lk(mu);
-    if (!cache[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_hypic_err_word);
-        if (e != cudaSuccess) {
-            *e_out = e;
-            return nullptr;
-        }
-        cache[dev] = static_cast<unsigned*>(p);
-    }
-    *e_out = cudaSuccess;
-    return cache[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_hypic_err_word);
+    *e_out = e;
+    return e == cudaSuccess ? static_cast<unsigned*>(p) : nullptr;
 }
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }

@@ -6,8 +6,6 @@
 #include <cuda_runtime.h>
 #include <stdio.h>
 
-#include <mutex>
-
 #include "../../include/hypic.h"
 #include "kernels.h"
 
@@ -23,26 +21,13 @@ constexpr size_t kNoallocBytes = ((size_t)HYPIC_NOALLOC_MAX_SEGMENTS * 4 + 255) 
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the host-side symbol is only a stand-in for it).
+// Device address of g_noalloc_scratch on the current device (the host-side
+// symbol is only a stand-in for it), looked up on every call with that device
+// current: a cheap host-side query, and never stale after a device reset.
 void* scratch_address(cudaError_t* err) {
-    static std::mutex mu;
-    static void* cache[128] = {};
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= 128) {
-        *err = cudaErrorInvalidDevice;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lk(mu);
-    if (!cache[dev]) {
-        void* p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        cache[dev] = p;
-    }
-    return cache[dev];
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    return *err == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace

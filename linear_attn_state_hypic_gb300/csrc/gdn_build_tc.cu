@@ -6,52 +6,51 @@
 // after C from zero with the write term b_t k_t v_t^T (aibase article on
 // HYPIC, paragraph on the linear layers: the cached pair of a segment).
 //
-// How: tokens are taken in chunks of 64.  With g_i = a_1 ... a_i inside a
-// chunk (g_C its last value), A[i][j] = b_i (g_i/g_j) k_i.k_j for j < i,
-// That = (I + A)^-1 Diag(b), W = That Diag(g) K and U = That V, the chunk
-// maps the running pair D = [T | S] (dk x 2dk) to
-//     D <- g_C D + K^T Diag(g_C/g_t) ([0 | U] - W D),
-// which is the token recurrence applied 64 times (WY / UT form of a product
-// of generalised Householder transitions).  The state is held transposed,
-// D'' = D^T / sigma (256 x 128 fp32, sigma a per-half scale, see "Lazy
-// decay" below), in tensor memory; per chunk:
-//   gram      G = K K^T                      bf16 MMA, M=64  N=64  K=128
-//   solve     That from G and the gates      CUDA cores + warp MMAs (block-triangular inverse)
-//   W'^T, U^T K^T (That Diag(up))^T, V^T That^T   bf16 MMA, M=128 N=64 K=64
-//   GEMM1     X''_h = D''_h W'^T             tf32 MMA, A read from tensor memory
-//   pass      Y''_T = Diag(f_T) X''_T^T (bf16, in place of X''_T in tensor memory),
-//             Y''_S = Diag(f_S) X''_S^T + U~ (bf16, smem)
-//   GEMM2     D''_h += Y''_h K                bf16 MMA, M=128 N=128 K=64 (A of the T half
-//                                             read from tensor memory)
-// with up_t = g_t / g_C^(1/2) in W' = W / g_C^(1/2) and f_h = -g_C^(1/2)/g_t
-// (times the renormalisation factor): the in-chunk decay is centred on the
-// middle of its range so that neither factor leaves the float32 range for
-// chunk decays down to 2^-252.
-// Two operands are carried as a pair of bf16 values (x = hi + lo, hi the
-// truncation of x and lo the rest): That Diag(up) in the W product and Y''_T
-// in the T half of GEMM2.  Rounding either to a single bf16 alone costs T_C about
-// 7e-3 relative error over 2048-token segments with strong decay; the pair
-// brings it to ~2e-3.  Keys and values are bf16 inputs and need no split.
+// How: tokens are taken in chunks of 64.  The scalar gate a_t commutes with
+// the delta projection, so the chunk's UT transform needs no decay at all:
+// with A^[i][j] = b_i k_i.k_j for j < i, M = (I + A^)^-1, g_t = a_1 ... a_t
+// inside the chunk and g_C its last value,
+//     W^ = M Diag(b) K,   U^ = M Diag(b / g) V,
+//     T <- g_C (I - K^T W^) T,   S <- g_C (S + K^T (U^ - W^ S)),
+// which is the token recurrence applied 64 times (WY form of a product of
+// generalised Householder transitions; the decay reaches S only through the
+// per-token weights 1/g_t of the values).  The state is held transposed in
+// tensor memory, D'' = [T^T ; S^T] scaled per half (256 x 128 fp32): the T
+// half carries no decay (its exponent is kept apart), the S half a lazy
+// power-of-two scale 2^lsS set from the gates alone.  Per chunk:
+//   gram    G = K K^T                              bf16 MMA, M=64  N=64  K=128
+//   solve   M from G and b                         CUDA cores + warp MMAs (block-triangular inverse)
+//   W^T     -(M Diag(b) K)^T                       fp16 MMA, M=128 N=64  K=64 (keys converted to fp16)
+//   U~      V^T (M Diag(b uf))^T into X_S          bf16 MMA, M=128 N=64  K=64 (uf = 2^(-lg2 g_t - lsS))
+//   GEMM1   X_h (+)= D''_h (-W^)^T                 tf32 MMA, A read from tensor memory
+//   pass    X_T -> fp16, X_S -> bf16 in place     (a format conversion, nothing else)
+//   GEMM2   D''_h += X_h K                         fp16 (T) / bf16 (S) MMA, M=128 N=128 K=64,
+//                                                  A read from tensor memory
+// A renormalisation chunk (every 16 chunks, the last chunk of a segment, and
+// chunks whose decay would push the S scale past 2^-112) first rescales the
+// stored state: T by a power of two to a maximum below 2, S to its true scale
+// times g_C, so that the chunk ends with S at its true scale.  The largest U~
+// factor of an ordinary chunk is then below 2^112, and that of a
+// renormalisation chunk below 1.
 // T_C falls far below the fp32 range over long segments: it is returned as a
 // mantissa and a power-of-two exponent.
 //
-// Roles (480 threads): warp 0 loads keys and values (TMA) and writes the gate
-// tables.  Two single-thread issuers send the MMAs as their inputs become
-// ready: warp 1 W'^T, GEMM1 of the T half and GEMM2, warp 14 GEMM1 of the S
-// half, U^T and the gram (one thread issues a small MMA only about every 60
-// cycles; two come closer to the tensor pipe's own rate).  Warps 6-13 (the
-// prep warps) turn each gram into That; warps 2-5 (the state warpgroup) run
-// the pass between GEMM1 and GEMM2, convert W into an MMA operand and write
-// the result.  The prep warps run ahead of the state chain: only the pass,
-// the W conversion and the two state GEMMs are serial per chunk.  The roles
-// meet on mbarriers; every wait is bounded and a wait that runs out sets the
-// device error word.
+// Roles (512 threads): warp 0 loads keys and values (TMA), writes the gate
+// tables and plans each chunk's scales; warp 3 converts each key tile to
+// fp16; two single-thread MMA issuers: warp 1 the prep stream (gram, W^T),
+// warp 2 the state stream (U~, GEMM1, GEMM2); warps 4-11 (prep) turn each
+// gram into the two M forms; warps 12-15 (state) run the passes, convert W^
+// into a tf32 operand, renormalise and write the result.  Only the two state
+// GEMMs and the (cheap) passes are serial per chunk; the prep runs ahead.  The
+// roles meet on mbarriers; every wait is bounded and a wait that runs out
+// sets the device error word.
 // One CTA per SM, persistent over (segment, layer, head) items taken from an
 // atomic queue in longest-body-first order.  Warp 0 publishes them through a
 // ring of item slots and each role runs through them at its own pace, so one
 // item's first chunks overlap the previous item's last ones.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <float.h>
@@ -71,22 +70,23 @@ using namespace tc;
 
 constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
-constexpr int kKStages = 3;       // K ring depth (the gram of a chunk wants its keys early)
+constexpr int kKStages = 3;       // key tiles in flight (bf16 and their fp16 copies)
+constexpr int kVStages = 2;
 constexpr int kGateSlots = 4;     // per-chunk gate tables in flight
-constexpr int kThreads = 480;
-constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpState0 = 2, kWarpPrep0 = 6, kWarpMMA2 = 14;
-constexpr int kPrepThreads = 256;  // warps 6-13: two warps per tensor-memory lane quarter
+constexpr int kThreads = 512;
+constexpr int kWarpTMA = 0, kWarpIssP = 1, kWarpIssS = 2, kWarpCvt = 3, kWarpPrep0 = 4, kWarpState0 = 12;
+constexpr int kPrepThreads = 256;  // warps 4-11: two warps per tensor-memory lane quarter
 
 // Shared memory map (byte offsets; every operand region is 1024-byte aligned).
-constexpr uint32_t kTile = 16384;                       // 64 tokens x 128 bf16, two 64-column TMA boxes
-constexpr uint32_t OFF_K = 0;                           // K ring
-constexpr uint32_t OFF_V = OFF_K + kKStages * kTile;    // V (one chunk: read only by the U^T MMA)
-constexpr uint32_t OFF_BW = OFF_V + kTile;              // W: fp32 [64 t][128 i], K-major, 4 blocks of 32 i
-constexpr uint32_t OFF_AY = OFF_BW + 32768;             // Y''_S (with U~): bf16 [128 n][64 t], K-major
-constexpr uint32_t kBT = 24576;                         // That Diag(g) hi, That, That Diag(g) lo: bf16 [64][64]
-constexpr uint32_t OFF_BT = OFF_AY + 16384;             // two of them: chunk gc uses buffer gc % 2
-constexpr uint32_t OFF_AS = OFF_BT + 2 * kBT;           // A / (I+A)^-1: fp32 [64][kAS] (padded rows)
-constexpr int kAS = 68;                                 // row stride (floats) of that scratch
+constexpr uint32_t kTile = 16384;                        // 64 tokens x 128 (b)f16, two 64-column TMA boxes
+constexpr uint32_t OFF_K = 0;                            // bf16 key ring
+constexpr uint32_t OFF_K16 = OFF_K + kKStages * kTile;   // fp16 copies of the same tiles
+constexpr uint32_t OFF_V = OFF_K16 + kKStages * kTile;   // value ring
+constexpr uint32_t OFF_W = OFF_V + kVStages * kTile;     // -W^: tf32 [64 t][128 i], K-major, 4 blocks of 32 i
+constexpr uint32_t kBT = 16384;                          // -M Diag(b) fp16 [64][64], then M Diag(b uf) bf16
+constexpr uint32_t OFF_BT = OFF_W + 32768;               // two of them: chunk gc uses buffer gc % 2
+constexpr uint32_t OFF_AS = OFF_BT + 2 * kBT;            // A^ / M: fp32 [64][kAS] (padded rows)
+constexpr int kAS = 68;
 constexpr uint32_t OFF_PT = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;  // solve scratch: 32 x 36 fp32
 constexpr uint32_t OFF_MISC = OFF_PT + 5120;
 
@@ -94,51 +94,54 @@ constexpr uint32_t OFF_MISC = OFF_PT + 5120;
 struct ItemSlot {
     int64_t b0, b1, obj;  // body [b0, b1) in the token index, output object
     uint32_t g;           // CTA-wide index of the item's first chunk
-    int nc, layer, head;  // nc < 0: the queue is exhausted
+    int nc, layer, head;  // nc > 0, or nc < 0: the queue is exhausted
 };
 constexpr int kItemSlots = 4;
-constexpr int kSlotReaders = 4;  // warp 1, warp 14, the state warpgroup, the prep warps
+constexpr int kSlotReaders = 5;  // warp 1, warp 2, warp 3, the prep warps, the state warps
+
+// The scales of one chunk, planned by the producer from the gates.
+struct ChunkPlan {
+    float preS;    // renormalisation chunk: D''_S <- 2^preS D''_S first
+    float sum_lc;  // log2 of the item's decay up to and including this chunk
+    int rn;        // renormalisation chunk
+    int pad;
+};
 
 struct Misc {
-    uint64_t fullK[kKStages], emptyK[kKStages], fullV, emptyV;
-    uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables of a chunk written
-    uint64_t g_done, g_read;      // gram committed; gram read by the prep warpgroup
-    // That of chunk gc written (that_ready[gc % 2]); the W/U MMAs that read it are done (bt_free[gc % 2],
-    // one commit from each issuer).  One barrier per That buffer: the prep may run two chunks ahead of
-    // an issuer, and an issuer one chunk ahead of the other, so a shared barrier could be two phases
-    // ahead of a parity wait or mix the commits of two chunks in one phase.
+    uint64_t fullK[kKStages], emptyK[kKStages], k16_full[kKStages], k16_empty[kKStages];
+    uint64_t fullV[kVStages], emptyV[kVStages];
+    uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables and plan of a chunk written
+    uint64_t g_done, g_read;      // gram committed; gram read by the prep warps
+    // M forms of chunk gc written (that_ready[gc % 2]); the W^T and U~ MMAs that read them are done
+    // (bt_free[gc % 2], one commit from each issuer).
     uint64_t that_ready[2], bt_free[2];
-    uint64_t u_done, w_done;      // U^T, W^T committed
-    uint64_t w_cvt;               // W operand written
-    uint64_t x_done_s, x_done, xs_free, y_ready, d_ready, drain;  // GEMM1 S half / T half done; X''_S read
-    alignas(16) float lg2[kGateSlots][kC];  // slot gc % kGateSlots; every table is read as float4
+    uint64_t w_done, w_read, w_cvt;  // W^T committed; read from tensor memory; tf32 operand written
+    uint64_t pre_done;               // state ready for GEMM1 (initialised or renormalised)
+    uint64_t x_done_s, x_done_t, y_ready, d_ready, drain;
     alignas(16) float beta[kGateSlots][kC];
-    alignas(16) float up[kGateSlots][kC];
-    alignas(16) float wn[kGateSlots][kC];  // 2^(lg2_t - lg2_C/2), 2^(lg2_C/2 - lg2_t): g_r/g_j = up_r wn_j
-    alignas(16) float fT[kC];    // state pass: Y'' = f X'' for the T and S halves
-    alignas(16) float fS[kC];
-    alignas(16) float uf[kC];    // U~ = Diag(uf) U
-    float red[2][4];
-    float red_ep[4];
+    alignas(16) float uf[kGateSlots][kC];  // 2^(-lg2 g_t - lsS): the U~ weight of token t
+    ChunkPlan plan[kGateSlots];
+    float red[4];
     uint64_t slot_full[kItemSlots], slot_read[kItemSlots];  // item slot written / copied by every reader
     ItemSlot slots[kItemSlots];
     int abort_flag;
     uint32_t tmem_base;
 };
 constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
-static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, lg2) % 16 == 0 && offsetof(Misc, beta) % 16 == 0 &&
-                  offsetof(Misc, up) % 16 == 0 && offsetof(Misc, wn) % 16 == 0 && offsetof(Misc, fT) % 16 == 0,
-              "float4 / float2 accesses of the gate tables need 16-byte alignment");
+static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, beta) % 16 == 0 && offsetof(Misc, uf) % 16 == 0,
+              "float4 accesses of the gate tables need 16-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Tensor-memory columns.
-// W^T is staged in the X_S columns: it is converted before GEMM1 writes X.
-constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_U = 384, TM_G = 448;
+constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_G = 384, TM_W = 448;
 
-constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);  // G = K K^T
-constexpr uint32_t ID_WU = idesc(1, 128, 64, true, false);    // W^T, U^T: A = K^T / V^T (MN-major)
-constexpr uint32_t ID_G1 = idesc(2, 128, 64, false, false);   // X' = D' W^T (tf32, A in TMEM)
-constexpr uint32_t ID_G2 = idesc(1, 128, 128, false, true);   // D' += Y' K (B = K, MN-major)
+constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+constexpr uint32_t ID_GRAM = idesc(kFmtBF16, 64, 64, false, false);   // G = K K^T
+constexpr uint32_t ID_W = idesc(kFmtF16, 128, 64, true, false);       // W^T: A = K^T (MN-major)
+constexpr uint32_t ID_U = idesc(kFmtBF16, 128, 64, true, false);      // U~: A = V^T (MN-major)
+constexpr uint32_t ID_G1 = idesc(kFmtTF32, 128, 64, false, false);    // X = D'' W^T (A in TMEM)
+constexpr uint32_t ID_G2T = idesc(kFmtF16, 128, 128, false, true);    // D''_T += X_T K (B = K, MN-major)
+constexpr uint32_t ID_G2S = idesc(kFmtBF16, 128, 128, false, true);   // D''_S += X_S K
 
 struct TcArgs {
     int n_layers, n_heads, n_seg, n_items;
@@ -182,28 +185,44 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
     if (mbar_try_wait(bar, parity)) return true;
     return wait_bar_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
 }
+// The state-stream issuer's wait: it spins on the phase (a sleeping thread
+// answers a completed phase late, and this thread's MMAs are the chain).
+__device__ __noinline__ bool spin_bar_slow(uint64_t* bar, uint32_t parity, int* abort_flag, uint64_t wait_ns,
+                                           unsigned* err) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int j = 0; j < 64; ++j)
+            if (mbar_test(bar, parity)) return true;
+        if (*(volatile int*)abort_flag) return false;
+        if (globaltimer_ns() - t0 > wait_ns) break;
+    }
+    *(volatile int*)abort_flag = 1;
+    set_error(err, kErrTimeout);
+    return false;
+}
+__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
+    if (mbar_test(bar, parity)) return true;
+    return spin_bar_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
+}
 
 __device__ __forceinline__ void named_sync(int id, int n = 128) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
+// Two floats as fp16 (round to nearest, saturating to the largest finite value).
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
-}
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-// Two values as bf16 pairs x = hi + lo: hi is x with its low 16 bits cleared
-// (exact; two values packed by one byte permute) and lo = x - hi (exact in
-// fp32) rounded to bf16, so hi + lo keeps about 16 significant bits of x.
-__device__ __forceinline__ void split2_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
-    const uint32_t hx = __float_as_uint(x) & 0xffff0000u, hy = __float_as_uint(y) & 0xffff0000u;
-    hi = __byte_perm(hx, hy, 0x7632);
-    lo = pack_bf16(x - __uint_as_float(hx), y - __uint_as_float(hy));
 }
 __device__ __forceinline__ float tf32_rna(float x) {
     uint32_t r;
@@ -211,9 +230,7 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
-// ----------------------------------------------------------- prep roles --
-// p: thread index inside the prep warpgroup (0..127); q: its tensor-memory
-// lane quarter; lane: lane in the warp.
+// ------------------------------------------------------------ producer --
 
 // Raw gates of tokens t0 + 2 lane + {0, 1} (a = 1, b = 0 past the body end:
 // an identity transition, so padded rows leave the result unchanged).
@@ -232,13 +249,23 @@ __device__ __forceinline__ void gate_load(const TcArgs& a, int layer, int head, 
     }
 }
 
-// Gate tables of one chunk (one warp, two tokens a lane): lg2[t] = sum_{s<=t}
-// log2 a_s (inclusive prefix inside the chunk), beta[t], and
-// up[t] = g_t / g_C^(1/2), wn[t] = g_C^(1/2) / g_t: the in-chunk decay
-// centred on the middle of its range, so that both stay in float32 range for
-// chunk decays g_C down to 2^-252 (g_t itself underflows below 2^-126).  The
-// exponents are clamped to +-126, which only matters beyond that.
-__device__ void gate_tables(Misc* ms, int slot, const float (&ra)[2], const float (&rb)[2], int lane) {
+// The producer's running scale state of an item (identical in every lane).
+struct PlanState {
+    float lsS;     // log2 of the stored S scale before the next chunk
+    float sum_lc;  // log2 of the decay so far
+    int since;     // chunks since the last renormalisation
+};
+constexpr int kRenormEvery = 16;
+constexpr float kLazyMax = 56.f;  // (the stored S stays below 2^112 times the true one)
+
+// Gate tables and plan of one chunk (one warp, two tokens a lane): b_t, the
+// U~ weight uf_t = 2^(-lg2 g_t - lsS) (g_t the inclusive in-chunk decay), and
+// the chunk's plan.  A renormalisation chunk first brings the stored S to
+// its true scale times g_C (preS = lsS + lg2 g_C) and then takes the weights
+// g_C / g_t <= 1, so that it ends at the true scale (lsS = 0); an ordinary
+// chunk keeps the decay in the scale (lsS += lg2 g_C).
+__device__ void gate_tables(Misc* ms, int slot, const float (&ra)[2], const float (&rb)[2], bool last,
+                            PlanState& st, int lane) {
     const float l0 = log2f(fmaxf(ra[0], FLT_MIN)), l1 = log2f(fmaxf(ra[1], FLT_MIN));
     float s = l0 + l1;
 #pragma unroll
@@ -248,21 +275,101 @@ __device__ void gate_tables(Misc* ms, int slot, const float (&ra)[2], const floa
     }
     const float before = __shfl_up_sync(0xffffffffu, s, 1);
     const float e0 = (lane > 0 ? before : 0.f) + l0, e1 = e0 + l1;
-    const float h = 0.5f * __shfl_sync(0xffffffffu, e1, 31);
+    const float lc = __shfl_sync(0xffffffffu, e1, 31);
+    const bool rn = last || st.since + 1 >= kRenormEvery || st.lsS + lc < -2.f * kLazyMax || lc < -kLazyMax;
+    float ls_use, preS = 0.f;
+    if (rn) {
+        preS = st.lsS + lc;
+        ls_use = -lc;
+        st.lsS = 0.f;
+        st.since = 0;
+    } else {
+        ls_use = st.lsS;
+        st.lsS += lc;
+        ++st.since;
+    }
+    st.sum_lc += lc;
     const int t = 2 * lane;
-    *reinterpret_cast<float2*>(&ms->lg2[slot][t]) = make_float2(e0, e1);
-    *reinterpret_cast<float2*>(&ms->beta[slot][t]) = make_float2(rb[0], rb[1]);
     auto ex = [](float x) { return exp2f(fminf(fmaxf(x, -126.f), 126.f)); };
-    *reinterpret_cast<float2*>(&ms->up[slot][t]) = make_float2(ex(e0 - h), ex(e1 - h));
-    *reinterpret_cast<float2*>(&ms->wn[slot][t]) = make_float2(ex(h - e0), ex(h - e1));
+    *reinterpret_cast<float2*>(&ms->beta[slot][t]) = make_float2(rb[0], rb[1]);
+    *reinterpret_cast<float2*>(&ms->uf[slot][t]) = make_float2(ex(-e0 - ls_use), ex(-e1 - ls_use));
+    if (lane == 0) {
+        ChunkPlan& p = ms->plan[slot];
+        p.preS = preS;
+        p.sum_lc = st.sum_lc;
+        p.rn = rn ? 1 : 0;
+    }
 }
 
-// Rows of A from the gram matrix in tensor memory (M=64 accumulator layout:
-// row 16q + l sits in lane 32q + l, l < 16):
-// A[r][j] = b_r 2^(lg2_r - lg2_j) G[r][j] for j < r, 0 elsewhere.
-// Half h of the prep warps reads columns 32h..32h+31; lane l < 16 writes the
-// first 16 of them in its row, lane l + 16, which holds no row, takes the
-// other 16 of the same row from lane l by a shuffle.
+// Warp 0: keys (ring) and values (ring) by TMA from lane 0, and the gate
+// tables of each chunk from the whole warp (the loads of the next chunk's
+// gates in flight meanwhile).
+__device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CUtensorMap* tmk,
+                              const CUtensorMap* tmv, uint32_t g, int nc, int layer, int head, int64_t b0, int64_t b1,
+                              int lane) {
+    float ra[2], rb[2];
+    PlanState st{0.f, 0.f, 0};
+    gate_load(a, layer, head, b0, b1, lane, ra, rb);
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c, s = gc % kKStages, u = gc / kKStages;
+        const int z = (int)((int64_t)layer * a.n_tokens + b0 + (int64_t)c * kC);
+        if (u >= 1 && !wait_bar(&ms->emptyK[s], (u - 1) & 1, ms, a)) return;
+        if (lane == 0) {
+            uint8_t* kt = smem + OFF_K + s * kTile;
+            mbar_expect_tx(&ms->fullK[s], kTile);
+            tma_load_3d(kt, tmk, &ms->fullK[s], 0, head, z);
+            tma_load_3d(kt + 8192, tmk, &ms->fullK[s], 64, head, z);
+        }
+        // The slot of chunk gc was last read for chunk gc - 4: by the prep before its M forms, by the
+        // state warps at the start of that chunk, both before GEMM2 of chunk gc - 3 (waited above).
+        gate_tables(ms, gc % kGateSlots, ra, rb, c + 1 == nc, st, lane);
+        if (c + 1 < nc) gate_load(a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, lane, ra, rb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->gready[gc % kGateSlots]);
+        const uint32_t vs = gc % kVStages, vu = gc / kVStages;
+        if (vu >= 1 && !wait_bar(&ms->emptyV[vs], (vu - 1) & 1, ms, a)) return;
+        if (lane == 0) {
+            uint8_t* vt = smem + OFF_V + vs * kTile;
+            mbar_expect_tx(&ms->fullV[vs], kTile);
+            tma_load_3d(vt, tmv, &ms->fullV[vs], 0, head, z);
+            tma_load_3d(vt + 8192, tmv, &ms->fullV[vs], 64, head, z);
+        }
+    }
+}
+
+// Warp 3: each key tile converted to fp16 in the same (swizzled) layout.
+// bf16 -> fp16 is exact for |k| >= 2^-14 and loses at most 2^-25 below.
+__device__ void convert_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t g, int nc, int lane) {
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c, s = gc % kKStages, u = gc / kKStages;
+        bool ok = wait_bar(&ms->fullK[s], u & 1, ms, a);
+        ok = ok && (u == 0 || wait_bar(&ms->k16_empty[s], (u - 1) & 1, ms, a));
+        if (!__all_sync(0xffffffffu, ok)) return;
+        const uint4* src = reinterpret_cast<const uint4*>(smem + OFF_K + s * kTile);
+        uint4* dst = reinterpret_cast<uint4*>(smem + OFF_K16 + s * kTile);
+#pragma unroll 4
+        for (int j = 0; j < (int)(kTile / 16 / 32); ++j) {
+            const uint4 x = src[32 * j + lane];
+            auto cv = [](uint32_t w) {  // two bf16 (low = first) -> two fp16
+                return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            };
+            dst[32 * j + lane] = make_uint4(cv(x.x), cv(x.y), cv(x.z), cv(x.w));
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->k16_full[s]);
+    }
+}
+
+// ----------------------------------------------------------- prep roles --
+// p: thread index inside the prep warps (0..255); q: its tensor-memory lane
+// quarter; lane: lane in the warp.
+
+// Rows of A^ from the gram matrix in tensor memory (M=64 accumulator layout:
+// row 16q + l sits in lane 32q + l, l < 16): A^[r][j] = b_r G[r][j] for
+// j < r, 0 elsewhere.  Half h of the prep warps reads columns 32h..32h+31;
+// lane l < 16 writes the first 16 of them in its row, lane l + 16, which holds
+// no row, takes the other 16 of the same row from lane l by a shuffle.
 __device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, int q, int h, int lane) {
     uint32_t g0[32];
     tmem_ld32(tmem + ((32u * q) << 16) + TM_G + 32 * h, g0);
@@ -275,17 +382,15 @@ __device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, i
         gv[j] = upper ? x : g0[j];
     }
     const int r = 16 * q + (lane & 15), cb = 32 * h + (upper ? 16 : 0);
-    const float coef = ms->beta[slot][r] * ms->up[slot][r];
-    const float* wn = ms->wn[slot] + cb;
+    const float coef = ms->beta[slot][r];
     float* row = As + r * kAS + cb;
 #pragma unroll
     for (int j = 0; j < 16; j += 4) {
-        const float4 w = *reinterpret_cast<const float4*>(wn + j);
         float4 v;
-        v.x = (cb + j < r) ? coef * w.x * __uint_as_float(gv[j]) : 0.f;
-        v.y = (cb + j + 1 < r) ? coef * w.y * __uint_as_float(gv[j + 1]) : 0.f;
-        v.z = (cb + j + 2 < r) ? coef * w.z * __uint_as_float(gv[j + 2]) : 0.f;
-        v.w = (cb + j + 3 < r) ? coef * w.w * __uint_as_float(gv[j + 3]) : 0.f;
+        v.x = (cb + j < r) ? coef * __uint_as_float(gv[j]) : 0.f;
+        v.y = (cb + j + 1 < r) ? coef * __uint_as_float(gv[j + 1]) : 0.f;
+        v.z = (cb + j + 2 < r) ? coef * __uint_as_float(gv[j + 2]) : 0.f;
+        v.w = (cb + j + 3 < r) ? coef * __uint_as_float(gv[j + 3]) : 0.f;
         *reinterpret_cast<float4*>(row + j) = v;
     }
 }
@@ -295,6 +400,7 @@ __device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, i
 // (x = hi + lo, lo the rounding residual of hi) and a product as
 // hi*hi + hi*lo + lo*hi, which keeps about 16 bits of every operand: the
 // solve then matches an fp32 one to ~3e-6 relative.
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
     const float hx = bf16_round(x), hy = bf16_round(y);
     hi = pack_bf16(hx, hy);
@@ -414,63 +520,43 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
     named_sync(1, kPrepThreads);
 }
 
-// That Diag(up) (bf16 hi at bt, residual lo at bt + 16384; up = g / g_C^(1/2))
-// and That = (I+A)^-1 Diag(b) (bf16 at bt + 8192) as K-major 64 x 64 operands
-// (128-byte rows, 128-byte swizzle).  Thread p writes a quarter of a row.
-__device__ void prep_write_that(const Misc* ms, const float* As, uint32_t bt, int par, int p) {
+// The two forms of M as K-major 64 x 64 operands (128-byte rows, 128-byte
+// swizzle): -M Diag(b) in fp16 at bt (the W^T product; negated so that GEMM1
+// yields -X) and M Diag(b uf) in bf16 at bt + 8192 (the U~ product; the
+// weights span up to 2^112, beyond fp16).  Thread p writes a quarter of a row.
+__device__ void prep_write_forms(const Misc* ms, const float* As, uint32_t bt, int slot, int p) {
     const int t = p >> 2, qr = p & 3;
     const float* row = As + t * kAS + 16 * qr;
-    const float* beta = ms->beta[par] + 16 * qr;
-    const float* gam = ms->up[par] + 16 * qr;  // That Diag(g / g_C^(1/2))
+    const float* beta = ms->beta[slot] + 16 * qr;
+    const float* uf = ms->uf[slot] + 16 * qr;
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const float4 x0 = *reinterpret_cast<const float4*>(row + 8 * ch);
         const float4 x1 = *reinterpret_cast<const float4*>(row + 8 * ch + 4);
         const float4 b0 = *reinterpret_cast<const float4*>(beta + 8 * ch);
         const float4 b1 = *reinterpret_cast<const float4*>(beta + 8 * ch + 4);
-        const float4 y0 = *reinterpret_cast<const float4*>(gam + 8 * ch);
-        const float4 y1 = *reinterpret_cast<const float4*>(gam + 8 * ch + 4);
+        const float4 u0 = *reinterpret_cast<const float4*>(uf + 8 * ch);
+        const float4 u1 = *reinterpret_cast<const float4*>(uf + 8 * ch + 4);
         const float mv[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
                              x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
-        const float gv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-        uint32_t w1[4], w2[4], w3[4];
+        const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t wf[4], wu[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const float m0 = mv[2 * jj], m1 = mv[2 * jj + 1];
-            const float z0 = m0 * gv[2 * jj], z1 = m1 * gv[2 * jj + 1];
-            split2_bf16(z0, z1, w1[jj], w3[jj]);
-            w2[jj] = pack_bf16(m0, m1);
+            wf[jj] = pack_f16(-mv[2 * jj], -mv[2 * jj + 1]);
+            wu[jj] = pack_bf16(mv[2 * jj] * uv[2 * jj], mv[2 * jj + 1] * uv[2 * jj + 1]);
         }
         const uint32_t off = t * 128u + ((uint32_t)((2 * qr + ch) ^ (t & 7)) << 4);
-        st_shared_v4(bt + off, w1[0], w1[1], w1[2], w1[3]);
-        st_shared_v4(bt + 8192u + off, w2[0], w2[1], w2[2], w2[3]);
-        st_shared_v4(bt + 16384u + off, w3[0], w3[1], w3[2], w3[3]);
-    }
-}
-
-// W^T (lane i holds W[.][i], staged in the X_S columns) -> W as a tf32
-// K-major [64 t][128 i] operand.
-__device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
-    const int i = 32 * q + lane;
-    const uint32_t tl = tmem + ((32u * q) << 16);
-    uint8_t* bw = smem + OFF_BW + (i >> 5) * 8192;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
-        tmem_ld32(tl + TM_XS + 32 * half, w);
-        tmem_wait_ld();
-        uint8_t* b = bw + 32 * half * 128;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            *reinterpret_cast<float*>(b + sw128_offset(j, i & 31, 4, 0)) = tf32_rna(__uint_as_float(w[j]));
+        st_shared_v4(bt + off, wf[0], wf[1], wf[2], wf[3]);
+        st_shared_v4(bt + 8192u + off, wu[0], wu[1], wu[2], wu[3]);
     }
 }
 
 // ---------------------------------------------------------- state roles --
-// Thread n of the state warpgroup owns tensor-memory lane n = 32q + lane:
-// row n of D'_T (column n of T) and of D'_S (column n of S).
+// Thread n of the state warps owns tensor-memory lane n = 32q + lane: row n
+// of D''_T (column n of T) and of D''_S (column n of S).
 
-// D' <- (I, 0): row n of D'_T is e_n.
+// D'' <- (I, 0): row n of D''_T is e_n.
 __device__ void state_init(uint32_t tmem, int q, int lane) {
     const uint32_t tl = tmem + ((32u * q) << 16);
     const int n = 32 * q + lane;
@@ -488,113 +574,105 @@ __device__ void state_init(uint32_t tmem, int q, int lane) {
     tmem_wait_st();
 }
 
-// D''_h <- sc D''_h in tensor memory (this thread's row), returning the max
-// |.| of the new row when want_max: the rescale of a renormalisation chunk.
-// (Rare: out of line, so that it stays out of the pass's instruction stream.)
-__device__ __noinline__ float state_rescale(uint32_t addr, float sc, bool want_max) {
-    float mloc = 0.f;
+// Max |.| of this thread's row of a 128-column tensor-memory block.
+__device__ __noinline__ float row_absmax(uint32_t addr) {
+    float m = 0.f;
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         uint32_t x[32];
         tmem_ld32(addr + 32 * cb, x);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float v = __uint_as_float(x[j]) * sc;
-            if (want_max) mloc = fmaxf(mloc, fabsf(v));
-            x[j] = __float_as_uint(v);
-        }
+        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(__uint_as_float(x[j])));
+    }
+    return m;
+}
+// This thread's row of a 128-column tensor-memory block times sc.
+__device__ __noinline__ void row_scale(uint32_t addr, float sc) {
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32];
+        tmem_ld32(addr + 32 * cb, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * sc);
         tmem_st32(addr + 32 * cb, x);
     }
     tmem_wait_st();
-    return mloc;
 }
 
-// After GEMM1 of a chunk, half h (0 = T, 1 = S), the A operand of GEMM2:
-//   Y''_T[n][t] = fT[t] X''_T[n][t] as bf16 hi + lo, written over X''_T in
-//     tensor memory: lane n, tokens 16k..16k+15 in columns 16k..16k+7 (hi)
-//     and 16k+8..16k+15 (lo), two tokens per column, so that each group of
-//     16 columns is read and then rewritten in place;
-//   Y''_S[n][t] = fS[t] X''_S[n][t] + uf[t] U^T[n][t] as bf16 into shared
-//     memory (K-major [128 n][64 t]); the S half of GEMM2 multiplies both
-//     terms by the same keys, so U~ rides in Y''_S, rounded once.
-// On a renormalisation chunk the stored state is also rescaled in tensor
-// memory, D''_T <- dT D''_T and D''_S <- dS D''_S, and the max |.| of the new
-// T rows is returned (else 0).
-template <int h>
-__device__ float state_pass(const Misc* ms, uint32_t ay, bool rn, float dT, float dS, uint32_t tmem, int q,
-                            int lane) {
-    const int n = 32 * q + lane;
-    const uint32_t tl = tmem + ((32u * q) << 16);
-#pragma unroll 1
-    for (int qt = 0; qt < 4; ++qt) {  // 16 columns (tokens) at a time
-        const float* f = (h ? ms->fS : ms->fT) + 16 * qt;
-        const float* uf = ms->uf + 16 * qt;
-        uint32_t x[16], u[16];
-        tmem_ld16(tl + (h ? TM_XS : TM_XT) + 16 * qt, x);
-        if (h) tmem_ld16(tl + TM_U + 16 * qt, u);
-        tmem_wait_ld();
-        uint32_t hl[16];  // (T half: hi in [0, 8), lo in [8, 16))
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = 8 * jj + 2 * k;
-                float y0 = f[t] * __uint_as_float(x[t]);
-                float y1 = f[t + 1] * __uint_as_float(x[t + 1]);
-                if (h) {
-                    y0 = fmaf(uf[t], __uint_as_float(u[t]), y0);
-                    y1 = fmaf(uf[t + 1], __uint_as_float(u[t + 1]), y1);
-                    pk[k] = pack_bf16(y0, y1);
-                } else {
-                    split2_bf16(y0, y1, hl[4 * jj + k], hl[8 + 4 * jj + k]);
-                }
-            }
-            if (h) {
-                const uint32_t off = n * 128u + ((uint32_t)((2 * qt + jj) ^ (n & 7)) << 4);
-                st_shared_v4(ay + off, pk[0], pk[1], pk[2], pk[3]);
-            }
-        }
-        if (!h) tmem_st16(tl + TM_XT + 16 * qt, hl);
-    }
-    if (!h) tmem_wait_st();
-    return rn ? state_rescale(tl + (h ? TM_DS : TM_DT), h ? dS : dT, !h) : 0.f;
-}
-
-// Warp max, then the 4 warps of the state warpgroup through shared memory.
+// Warp max, then the 4 state warps through shared memory.
 __device__ float state_reduce_max(float v, float* slot, int q, int lane) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    named_sync(2);  // (the slots' previous values have been read)
     if (lane == 0) slot[q] = v;
     named_sync(2);
     return fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
 }
 
+// The pass of one half after GEMM1: X (64 fp32 columns) rewritten in place as
+// the A operand of GEMM2, two tokens per column (the lower token in the low
+// half): fp16 for T (values of order one: the T half carries no decay), bf16
+// for S (its lazy scale spans up to 2^112).
+template <bool kHalfT>
+__device__ __forceinline__ void state_pass(uint32_t addr) {
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m) {
+        uint32_t x[32], y[16];
+        tmem_ld32(addr + 32 * m, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float lo = __uint_as_float(x[2 * j]), hi = __uint_as_float(x[2 * j + 1]);
+            y[j] = kHalfT ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+        }
+        tmem_st16(addr + 16 * m, y);
+    }
+    tmem_wait_st();
+}
+
+// -W^T of the next chunk (lane i holds column i of it, in the W columns) ->
+// the tf32 K-major [64 t][128 i] operand of GEMM1.
+__device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
+    const int i = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    uint8_t* bw = smem + OFF_W + (i >> 5) * 8192 + (i & 3) * 4;
+    const uint32_t c4 = (uint32_t)((i & 31) >> 2);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+        tmem_ld32(tl + TM_W + 32 * half, w);
+        tmem_wait_ld();
+        uint8_t* b = bw + 32 * half * 128;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<float*>(b + j * 128 + ((c4 ^ (uint32_t)(j & 7)) << 4)) =
+                tf32_rna(__uint_as_float(w[j]));
+    }
+}
+
 // End of an item: T_C = mantissa * 2^exp with the mantissa's largest entry in
-// [1, 2); S(C|0) as is.  Thread n writes column n (coalesced across the warp).
-__device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, int E, uint32_t tmem, int q, int lane) {
+// [1, 2), from D''_T and its scale 2^F; S(C|0) as is (the last chunk ends at
+// the true scale).  Thread n writes column n (coalesced across the warp).
+__device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, float F, uint32_t tmem, int q, int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
-    uint32_t x[32];
-    float m = 0.f;
-#pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
-        tmem_ld32(tl + TM_DT + 32 * cb, x);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(__uint_as_float(x[j])));
-    }
-    m = state_reduce_max(m, ms->red_ep, q, lane);
-    const int ef = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
+    const float m = state_reduce_max(row_absmax(tl + TM_DT), ms->red, q, lane);
+    const float Fi = floorf(F);
+    const float sc = exp2f(F - Fi);  // in [1, 2)
+    const float ms_ = m * sc;
+    const int ef = (ms_ > 0.f && ms_ < INFINITY) ? ilogbf(ms_) : 0;
+    const float f = ldexpf(sc, -ef);
     float* T = a.T_out + obj * kD * kD;
     float* S = a.S_out + obj * kD * kD;
+    uint32_t x[32];
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         tmem_ld32(tl + TM_DT + 32 * cb, x);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) T[(32 * cb + j) * kD + n] = ldexpf(__uint_as_float(x[j]), -ef);
+        for (int j = 0; j < 32; ++j) T[(32 * cb + j) * kD + n] = __uint_as_float(x[j]) * f;
     }
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
@@ -603,18 +681,7 @@ __device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, int E, ui
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[(32 * cb + j) * kD + n] = __uint_as_float(x[j]);
     }
-    if (n == 0) a.T_exp[obj] = E + ef;
-}
-
-// Empty body: the identity pair.
-__device__ void state_identity(const TcArgs& a, int64_t obj, int n) {
-    float* T = a.T_out + obj * kD * kD;
-    float* S = a.S_out + obj * kD * kD;
-    for (int i = 0; i < kD; ++i) {
-        T[i * kD + n] = (i == n) ? 1.f : 0.f;
-        S[i * kD + n] = 0.f;
-    }
-    if (n == 0) a.T_exp[obj] = 0;
+    if (n == 0) a.T_exp[obj] = (int)Fi + ef;
 }
 
 // All n threads of named barrier `id` agree: true only if every one passed true.
@@ -630,49 +697,11 @@ __device__ __forceinline__ bool wg_all(int id, bool v, int n = 128) {
 }
 
 // --------------------------------------------------------- role drivers --
-// g: global chunk counter at the start of the item (barrier phases run on it
+// g: CTA-wide index of the item's first chunk (barrier phases run on it
 // across items); nc: chunks of this item's body.  Every barrier completes
-// once per chunk (the ring and gate-slot barriers once per use of their slot).
-
-// Warp 0: keys (3-deep ring) and values (one buffer) by TMA from lane 0, and
-// the gate tables of each chunk from the whole warp (a chunk ahead of the
-// prep warpgroup, the loads of the next chunk's gates in flight meanwhile).
-__device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CUtensorMap* tmk,
-                              const CUtensorMap* tmv, uint32_t g, int nc, int layer, int head, int64_t b0, int64_t b1,
-                              int lane) {
-    float ra[2], rb[2];
-    if (nc > 0) gate_load(a, layer, head, b0, b1, lane, ra, rb);
-    for (int c = 0; c < nc; ++c) {
-        const uint32_t gc = g + c, s = gc % kKStages, u = gc / kKStages;
-        const int z = (int)((int64_t)layer * a.n_tokens + b0 + (int64_t)c * kC);
-        if (u >= 1 && !wait_bar(&ms->emptyK[s], (u - 1) & 1, ms, a)) return;
-        if (lane == 0) {
-            uint8_t* kt = smem + OFF_K + s * kTile;
-            mbar_expect_tx(&ms->fullK[s], kTile);
-            tma_load_3d(kt, tmk, &ms->fullK[s], 0, head, z);
-            tma_load_3d(kt + 8192, tmk, &ms->fullK[s], 64, head, z);
-        }
-        // The slot of chunk gc was last read for chunk gc - 4, whose GEMM2
-        // completed before that of gc - 3 (waited above).
-        gate_tables(ms, gc % kGateSlots, ra, rb, lane);
-        if (c + 1 < nc) gate_load(a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, lane, ra, rb);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->gready[gc % kGateSlots]);
-        if (gc >= 1 && !wait_bar(&ms->emptyV, (gc - 1) & 1, ms, a)) return;
-        if (lane == 0) {
-            uint8_t* vt = smem + OFF_V;
-            mbar_expect_tx(&ms->fullV, kTile);
-            tma_load_3d(vt, tmv, &ms->fullV, 0, head, z);
-            tma_load_3d(vt + 8192, tmv, &ms->fullV, 64, head, z);
-        }
-    }
-}
-
-// The MMA issuers.  W^T of the next chunk reuses the X''_S columns and waits
-// only for the S half of this chunk's pass, so it runs while the pass does the
-// T half.  A readiness test of a barrier's phase k is only made once its phase
-// k - 1 is known to be complete (by an earlier test or an earlier item), so a
-// parity test cannot mistake an old phase for a new one.
+// once per chunk (the ring and gate-slot barriers once per use of their
+// slot).  A thread waits for phase k of a barrier only once it has seen
+// phase k - 1 complete, or knows it from the order of the other roles.
 
 // An issuer's idle step: the start of its idle time (t_idle, 0 if it was
 // busy), or 0 once the CTA aborted or this wait ran out (which sets the abort
@@ -688,121 +717,17 @@ __device__ __forceinline__ uint64_t issuer_idle(Misc* ms, const TcArgs& a, uint6
     return t_idle != 0 ? t_idle : now;
 }
 
-// Warp 1, one thread: the state chain's MMAs, each group as soon as its
-// inputs are ready (a dataflow loop that tests barrier phases without
-// blocking); priority W'^T, GEMM2, GEMM1 (T half).
-__device__ void mma_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
-    if (nc == 0) return;
+// Warp 1, one thread: the prep stream.  The gram of a chunk as soon as its
+// keys are in and the prep warps have read the previous gram (up to three
+// chunks ahead of W^T), and W^T = -(M Diag(b) K)^T of a chunk as soon as its
+// M forms, its fp16 keys and a free W block are there.
+__device__ void issue_prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
     const uint32_t sb = smem_u32(smem);
-    const uint32_t bw = sb + OFF_BW, ay = sb + OFF_AY, bt = sb + OFF_BT;
-    auto ktile = [&](uint32_t gc) { return sb + OFF_K + (gc % kKStages) * kTile; };
-    int iw = 0, i1 = 0, i2 = 0;
+    int ig = 0, iw = 0;
     uint64_t t_idle = 0;
-    while (i2 < nc) {
+    while (iw < nc) {
         bool any = false;
-        if (iw < nc && i1 == iw) {  // W^T = K^T (That Diag(g))^T (hi + lo) into the X_S columns
-            const uint32_t gc = g + iw;
-            if (mbar_test(&ms->that_ready[gc & 1], (gc >> 1) & 1) &&
-                (gc == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the pass has read the previous X''_S
-                tc_fence_after();
-                const uint32_t btc = bt + (gc & 1) * kBT;
-                const uint64_t a0 = sdesc_sw128(ktile(gc), 8192, 1024), bh = sdesc_sw128(btc, 0, 1024),
-                               bl = sdesc_sw128(btc + 16384, 0, 1024);
-#pragma unroll 2
-                for (int k = 0; k < 4; ++k) {  // (a descriptor's address field counts 16-byte units)
-                    mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bh + 2 * k, ID_WU, k > 0);
-                    mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, bl + 2 * k, ID_WU, true);
-                }
-                mma_commit(&ms->w_done);
-                mma_commit(&ms->bt_free[gc & 1]);
-                ++iw;
-                any = true;
-            }
-        }
-        if (i2 < i1) {  // GEMM2 (bf16): D''_T += Y''_T K (hi + lo, A in the X_T columns); D''_S += Y''_S K
-            const uint32_t gc = g + i2;
-            if (mbar_test(&ms->y_ready, gc & 1)) {
-                tc_fence_after();
-                const uint64_t b0 = sdesc_sw128(ktile(gc), 8192, 1024), ys = sdesc_sw128(ay, 0, 1024);
-#pragma unroll 2
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t bk = b0 + 128 * k;
-                    mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 16 * k, bk, ID_G2, true);
-                    mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 16 * k + 8, bk, ID_G2, true);
-                    mma_bf16_ss(tmem + TM_DS, ys + 2 * k, bk, ID_G2, true);
-                }
-                // (the gram of this K tile completed before That, hence before W'^T and this GEMM2)
-                mma_commit(&ms->d_ready);
-                mma_commit(&ms->emptyK[gc % kKStages]);
-                ++i2;
-                any = true;
-            }
-        }
-        if (i1 < iw && i2 == i1) {  // GEMM1 (tf32), T half: X''_T = D''_T W^T, A = the state in tensor memory
-            const uint32_t gc = g + i1;
-            if (mbar_test(&ms->w_cvt, gc & 1) && (i1 == 0 || mbar_test(&ms->d_ready, (gc - 1) & 1))) {
-                tc_fence_after();
-                const uint64_t b0 = sdesc_sw128(bw, 0, 1024);
-#pragma unroll 4  // (a measured balance of issue rate and code size)
-                for (int k = 0; k < 16; ++k)
-                    mma_tf32_ts(tmem + TM_XT, tmem + TM_DT + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3), ID_G1, k > 0);
-                mma_commit(&ms->x_done);
-                ++i1;
-                any = true;
-            }
-        }
-        if (any) {  // (no sleep when idle: a sleeping issuer answers its barriers late)
-            t_idle = 0;
-        } else if ((t_idle = issuer_idle(ms, a, t_idle)) == 0) {
-            return;
-        }
-    }
-}
-
-// Warp 14, one thread: GEMM1 of the S half (on the state chain), then the
-// prep chain's U^T and gram.  Its commits cover only its own MMAs: every
-// reader of their results waits on its barriers (x_done_s, u_done, g_done,
-// and bt_free, which takes one commit from each issuer).
-__device__ void mma_role2(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
-    if (nc == 0) return;
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t bw = sb + OFF_BW, bt = sb + OFF_BT, vt = sb + OFF_V;
-    int ig = 0, iu = 0, i1 = 0;
-    uint64_t t_idle = 0;
-    while (i1 < nc || ig < nc) {
-        bool any = false;
-        if (i1 < iu) {  // GEMM1 (tf32), S half: X''_S = D''_S W^T (the W^T staged in X_S has been converted)
-            const uint32_t gc = g + i1;
-            if (mbar_test(&ms->w_cvt, gc & 1) && (i1 == 0 || mbar_test(&ms->d_ready, (gc - 1) & 1))) {
-                tc_fence_after();
-                const uint64_t b0 = sdesc_sw128(bw, 0, 1024);
-#pragma unroll 4
-                for (int k = 0; k < 16; ++k)
-                    mma_tf32_ts(tmem + TM_XS, tmem + TM_DS + 8 * k, b0 + 512 * (k >> 2) + 2 * (k & 3), ID_G1, k > 0);
-                mma_commit(&ms->x_done_s);
-                ++i1;
-                any = true;
-            }
-        }
-        if (iu < ig) {  // U^T = V^T That^T
-            const uint32_t gc = g + iu;
-            if (mbar_test(&ms->that_ready[gc & 1], (gc >> 1) & 1) && mbar_test(&ms->fullV, gc & 1) &&
-                (gc == 0 || mbar_test(&ms->xs_free, (gc - 1) & 1))) {  // the S pass has read the previous U^T
-                tc_fence_after();
-                const uint64_t a0 = sdesc_sw128(vt, 8192, 1024), b0 = sdesc_sw128(bt + (gc & 1) * kBT + 8192, 0, 1024);
-#pragma unroll 1
-                for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_U, a0 + 128 * k, b0 + 2 * k, ID_WU, k > 0);
-                mma_commit(&ms->u_done);
-                mma_commit(&ms->emptyV);
-                mma_commit(&ms->bt_free[gc & 1]);
-                ++iu;
-                any = true;
-            }
-        }
-        // G = K K^T (K-major view of the K tile, K = feature index, two 64-wide boxes); the gram of
-        // chunk c + 3 waits until GEMM1 (S half) of chunk c is issued, so that it fills a gap of the
-        // pipe (measured: one chunk less lookahead +0.7 %, two less +16 %)
-        if (ig < nc && ig <= i1 + 2) {
+        if (ig < nc && ig <= iw + 2) {  // G = K K^T (K-major view of the key tile, two 64-wide boxes)
             const uint32_t gc = g + ig;
             if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
                 (gc == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
@@ -818,6 +743,22 @@ __device__ void mma_role2(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
                 any = true;
             }
         }
+        if (iw < ig) {  // W^T = K^T (-M Diag(b))^T into the W columns (a descriptor's address counts 16 B)
+            const uint32_t gc = g + iw;
+            if (mbar_test(&ms->that_ready[gc & 1], (gc >> 1) & 1) &&
+                mbar_test(&ms->k16_full[gc % kKStages], (gc / kKStages) & 1) &&
+                (gc == 0 || mbar_test(&ms->w_read, (gc - 1) & 1))) {
+                tc_fence_after();
+                const uint64_t a0 = sdesc_sw128(sb + OFF_K16 + (gc % kKStages) * kTile, 8192, 1024),
+                               b0 = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT, 0, 1024);
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_W, a0 + 128 * k, b0 + 2 * k, ID_W, k > 0);
+                mma_commit(&ms->w_done);
+                mma_commit(&ms->bt_free[gc & 1]);
+                ++iw;
+                any = true;
+            }
+        }
         if (any) {
             t_idle = 0;
         } else if ((t_idle = issuer_idle(ms, a, t_idle)) == 0) {
@@ -826,7 +767,60 @@ __device__ void mma_role2(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
     }
 }
 
-// Warps 6-13: gram -> A -> (I + A)^-1 -> That, chunk after chunk.
+// Warp 2, one thread: the state stream, in chunk order: U~ into X_S, GEMM1 of
+// both halves, then (after the passes) GEMM2 of both halves.
+__device__ void issue_state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
+    const uint32_t sb = smem_u32(smem);
+    const uint64_t bw = sdesc_sw128(sb + OFF_W, 0, 1024);
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c;
+        // U~ = V^T (M Diag(b uf))^T: needs the M forms, the values and a free X_S (GEMM2 of the previous
+        // chunk has read it)
+        if (!spin_bar(&ms->that_ready[gc & 1], (gc >> 1) & 1, ms, a)) return;
+        if (!spin_bar(&ms->fullV[gc % kVStages], (gc / kVStages) & 1, ms, a)) return;
+        if (gc >= 1 && !spin_bar(&ms->d_ready, (gc - 1) & 1, ms, a)) return;
+        tc_fence_after();
+        {
+            const uint64_t a0 = sdesc_sw128(sb + OFF_V + (gc % kVStages) * kTile, 8192, 1024),
+                           b0 = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT + 8192, 0, 1024);
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, b0 + 2 * k, ID_U, k > 0);
+        }
+        mma_commit(&ms->emptyV[gc % kVStages]);
+        mma_commit(&ms->bt_free[gc & 1]);
+        // GEMM1 (tf32, A = the state in tensor memory): X_S += D''_S (-W^)^T, X_T = D''_T (-W^)^T
+        if (!spin_bar(&ms->w_cvt, gc & 1, ms, a)) return;
+        if (!spin_bar(&ms->pre_done, gc & 1, ms, a)) return;
+        tc_fence_after();
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k)
+            mma_tf32_ts(tmem + TM_XS, tmem + TM_DS + 8 * k, bw + 512 * (k >> 2) + 2 * (k & 3), ID_G1, true);
+        mma_commit(&ms->x_done_s);
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k)
+            mma_tf32_ts(tmem + TM_XT, tmem + TM_DT + 8 * k, bw + 512 * (k >> 2) + 2 * (k & 3), ID_G1, k > 0);
+        mma_commit(&ms->x_done_t);
+        // GEMM2: D''_T += X_T K (fp16), D''_S += X_S K (bf16), A from the passes' output in tensor memory
+        if (!spin_bar(&ms->y_ready, gc & 1, ms, a)) return;
+        if (!spin_bar(&ms->k16_full[gc % kKStages], (gc / kKStages) & 1, ms, a)) return;
+        tc_fence_after();
+        {
+            const uint64_t kt = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 8192, 1024),
+                           kh = sdesc_sw128(sb + OFF_K16 + (gc % kKStages) * kTile, 8192, 1024);
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {
+                mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 8 * k, kh + 128 * k, ID_G2T, true);
+                mma_bf16_ts(tmem + TM_DS, tmem + TM_XS + 8 * k, kt + 128 * k, ID_G2S, true);
+            }
+        }
+        mma_commit(&ms->d_ready);
+        mma_commit(&ms->emptyK[gc % kKStages]);
+        mma_commit(&ms->k16_empty[gc % kKStages]);
+    }
+}
+
+// Warps 4-11: gram -> A^ -> M = (I + A^)^-1 -> its two operand forms, chunk
+// after chunk.
 __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int p, int q,
                           int lane) {
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
@@ -844,165 +838,135 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->g_read);
         prep_solve(As, Ptmp, p);
-        // the buffer's previous That (chunk gc - 2) has been read (the buffer's phases are waited in order)
+        // the buffer's previous forms (chunk gc - 2) have been read (the buffer's phases are waited in order)
         if (!wg_all(1, gc < 2 || wait_bar(&ms->bt_free[gc & 1], ((gc >> 1) - 1) & 1, ms, a), kPrepThreads))
             return;
-        prep_write_that(ms, As, bt + (gc & 1) * kBT, slot, p);
+        prep_write_forms(ms, As, bt + (gc & 1) * kBT, slot, p);
         fence_async_smem();
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->that_ready[gc & 1]);
     }
 }
 
-// Lazy decay.  The true state is D = sigma_h D''_h per half (h = T, S); the
-// stored D'' is not rescaled on an ordinary chunk: its decay g_C goes into
-// sigma (sigma_T = 2^(E + lsT), sigma_S = 2^lsS), so that with g_t the
-// in-chunk decay prefix and X''_h = D''_h W'^T,
-//   D''_T += sum_t -(g_C^(1/2)/g_t) X''_T[:, t] k_t,
-//   D''_S += sum_t -(g_C^(1/2)/g_t) X''_S[:, t] k_t + (1/(g_t sigma_S)) u_t k_t.
-// A renormalisation chunk folds sigma back: D''_T <- 2^(lsT + lc - e) D''_T
-// with e = ilogb(max |D''_T|) + floor(lsT + lc) (E += e), D''_S <- 2^(lsS + lc)
-// D''_S, and the factors of that chunk carry the same scales.  It comes on an
-// item's last chunk, every kRenormEvery chunks (which bounds how far T's
-// stored magnitude drifts between exponent updates), when the chunk's own
-// decay passes 2^-kLazyMax, and when sigma_S times the chunk's decay would pass
-// 2^-(2 kLazyMax).  The largest factor of an ordinary chunk, U~'s
-// 2^(-lg2_t - lsS), then stays below 2^(2 kLazyMax), and so does the growth
-// of D''_S.  (Bounding sigma_S and the chunk decay by 2^-kLazyMax each, and
-// renormalising every 8 chunks, gave the same bound with twice the
-// renormalisations: 1.7 % slower.)
-constexpr int kRenormEvery = 16;
-constexpr float kLazyMax = 56.f;  // (2^112 x the state stays far inside float32 range)
-
-struct StatePlan {
-    bool rn;
-    int e;
-    float dT, dS, lc;
-};
-
-// The factor tables of chunk gc (threads n < 64 write entry n) and its plan.
-__device__ __forceinline__ StatePlan state_plan(Misc* ms, uint32_t gc, bool last, int since, float lsT, float lsS,
-                                                float m, int n) {
-    const int slot = gc % kGateSlots;
-    StatePlan pl;
-    pl.lc = ms->lg2[slot][kC - 1];
-    pl.rn = last || since + 1 >= kRenormEvery || lsS + pl.lc < -2.f * kLazyMax || pl.lc < -kLazyMax;
-    pl.e = pl.rn ? ((m > 0.f && m < INFINITY) ? ilogbf(m) : 0) + (int)floorf(lsT + pl.lc) : 0;
-    pl.dT = exp2f(lsT + pl.lc - (float)pl.e);
-    pl.dS = exp2f(lsS + pl.lc);
-    if (n < kC) {  // (W carries g_t / g_C^(1/2), so the Y factors carry g_C^(1/2) / g_t)
-        const float l = ms->lg2[slot][n], h = 0.5f * pl.lc;
-        if (pl.rn) {
-            ms->fT[n] = -exp2f(fminf(lsT + pl.lc - (float)pl.e + h - l, 126.f));
-            ms->fS[n] = -exp2f(fminf(lsS + pl.lc + h - l, 126.f));
-            ms->uf[n] = exp2f(pl.lc - l);
-        } else {
-            const float r = ms->wn[slot][n];
-            ms->fT[n] = -r;
-            ms->fS[n] = -r;
-            ms->uf[n] = exp2f(-l - lsS);
-        }
-    }
-    return pl;
-}
-
-// Chunk gc's factor tables and plan, then its W operand (on the chain to
-// GEMM1).
-__device__ __forceinline__ bool state_prepare(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t gc,
-                                              bool last, int since, float lsT, float lsS, float m, int q, int lane,
-                                              StatePlan& pl) {
-    const int slot = gc % kGateSlots;
-    bool ok = wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a);
-    if (!wg_all(2, ok)) return false;  // (and every thread is past the previous pass)
-    pl = state_plan(ms, gc, last, since, lsT, lsS, m, 32 * q + lane);
-    if (!wg_all(2, wait_bar(&ms->w_done, gc & 1, ms, a))) return false;  // (also publishes the factor tables)
-    tc_fence_after();
-    convert_w(smem, tmem, q, lane);
-    fence_async_smem();
-    tc_fence_before();
-    named_sync(2);
-    if (q == 0 && lane == 0) mbar_arrive(&ms->w_cvt);
-    return true;
-}
-
-// Warps 2-5: per chunk the pass (Y'' and, on renormalisation chunks, the
-// state rescale), then the next chunk's operands; the epilogue at the end.
-__device__ void state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc,
-                           int64_t obj, int q, int lane) {
-    const int n = 32 * q + lane;
-    if (nc == 0) {
-        state_identity(a, obj, n);
-        return;
-    }
-    const uint32_t ay = smem_u32(smem) + OFF_AY;
-    int E = 0, since = 0;
-    float m = 1.f, lsT = 0.f, lsS = 0.f;
-    StatePlan pl;
-    // Step c runs the pass of chunk c - 1 (none for c = 0), then prepares
-    // chunk c (none for c = nc): one call site per stage keeps the code small.
-    for (int c = 0; c <= nc; ++c) {
-        const uint32_t gc = g + c;
-        if (c > 0) {
-            const uint32_t gp = gc - 1;
-            bool ok = wait_bar(&ms->x_done_s, gp & 1, ms, a);
-            ok = ok && wait_bar(&ms->u_done, gp & 1, ms, a);
-            if (!wg_all(2, ok)) return;
-            tc_fence_after();
-            state_pass<1>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
-            tc_fence_before();
-            named_sync(2);  // every lane has read X''_S and U^T: the next W'^T and U^T may overwrite them
-            if (n == 0) mbar_arrive(&ms->xs_free);
-            if (!wg_all(2, wait_bar(&ms->x_done, gp & 1, ms, a))) return;
-            tc_fence_after();
-            const float mloc = state_pass<0>(ms, ay, pl.rn, pl.dT, pl.dS, tmem, q, lane);
-            fence_async_smem();
-            tc_fence_before();
-            if (pl.rn) {
-                m = state_reduce_max(mloc, ms->red[gp & 1], q, lane);
-                E += pl.e;
-                lsT = 0.f;
-                lsS = 0.f;
-                since = 0;
-            } else {
-                named_sync(2);
-                lsT += pl.lc;
-                lsS += pl.lc;
-                ++since;
-            }
-            if (n == 0) mbar_arrive(&ms->y_ready);
-        }
-        if (c < nc && !state_prepare(ms, smem, a, tmem, gc, c + 1 == nc, since, lsT, lsS, m, q, lane, pl)) return;
-    }
-    if (!wg_all(2, wait_bar(&ms->d_ready, (g + nc - 1) & 1, ms, a))) return;
-    tc_fence_after();
-    state_epilogue(ms, a, obj, E, tmem, q, lane);
-    state_init(tmem, q, lane);  // (I, 0) for the next item
-}
-
-// Producer, lane 0: the k-th item of this CTA into slot s (nc = -1 once the
-// queue is exhausted or the CTA aborted); the slot's previous item has been
-// copied by every reader.  Items are (segment, layer, head), segments in
-// longest-body-first order.
-__device__ __forceinline__ void publish_item(Misc* ms, const TcArgs& a, int k, int s) {
+// Producer, lane 0: the next non-empty item of this CTA into slot s (nc = -1
+// once the queue is exhausted or the CTA aborted); the slot's previous item
+// has been copied by every reader.  Items are (segment, layer, head),
+// segments in longest-body-first order.  An item with an empty body is the
+// identity pair (I, 0): the whole warp writes it here and takes the next.
+__device__ void publish_item(Misc* ms, const TcArgs& a, int k, int s, int lane) {
     const int LH = a.n_layers * a.n_heads;
-    const ItemSlot& prev = ms->slots[(s + kItemSlots - 1) % kItemSlots];
-    const uint32_t g = k == 0 ? 0u : prev.g + (uint32_t)(prev.nc > 0 ? prev.nc : 0);
-    const int item = *(volatile int*)&ms->abort_flag ? a.n_items : (int)atomicAdd(a.counter, 1u);
-    ItemSlot& it = ms->slots[s];
-    if (item >= a.n_items) {
-        it.nc = -1;
-    } else {
+    uint32_t g = 0;
+    if (k > 0) {
+        const ItemSlot& prev = ms->slots[(s + kItemSlots - 1) % kItemSlots];
+        g = prev.g + (uint32_t)prev.nc;
+    }
+    for (;;) {
+        int item = 0;
+        if (lane == 0) item = *(volatile int*)&ms->abort_flag ? a.n_items : (int)atomicAdd(a.counter, 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= a.n_items) {
+            if (lane == 0) ms->slots[s].nc = -1;
+            break;
+        }
         const int pos = item / LH, lh = item % LH;
         const int seg = a.order[pos];
-        it.layer = lh / a.n_heads;
-        it.head = lh % a.n_heads;
-        it.b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0);
-        it.b1 = a.cu[seg + 1];
-        it.nc = (int)((it.b1 - it.b0 + kC - 1) / kC);
-        it.obj = ((int64_t)seg * a.n_layers + it.layer) * a.n_heads + it.head;
-        it.g = g;
+        const int64_t b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0), b1 = a.cu[seg + 1];
+        const int64_t obj = ((int64_t)seg * a.n_layers + lh / a.n_heads) * a.n_heads + lh % a.n_heads;
+        const int nc = (int)((b1 - b0 + kC - 1) / kC);
+        if (nc <= 0) {
+            float4* T = reinterpret_cast<float4*>(a.T_out + obj * kD * kD);
+            float4* S = reinterpret_cast<float4*>(a.S_out + obj * kD * kD);
+            for (int e = lane; e < kD * kD / 4; e += 32) {
+                const int i = (4 * e) / kD, j = (4 * e) % kD;  // row i, columns j..j+3
+                T[e] = make_float4(i == j, i == j + 1, i == j + 2, i == j + 3);
+                S[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (lane == 0) a.T_exp[obj] = 0;
+            continue;
+        }
+        if (lane == 0) {
+            ItemSlot& it = ms->slots[s];
+            it.layer = lh / a.n_heads;
+            it.head = lh % a.n_heads;
+            it.b0 = b0;
+            it.b1 = b1;
+            it.nc = nc;
+            it.obj = obj;
+            it.g = g;
+        }
+        break;
     }
-    mbar_arrive(&ms->slot_full[s]);  // (release: the slot is visible to the readers that wait on it)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->slot_full[s]);  // (release: the slot is visible to the readers that wait on it)
+}
+
+// Warps 12-15: per chunk the renormalisation (if planned), the two passes,
+// and the next chunk's W operand; the epilogue at the end of an item.
+// Returns false once the CTA aborted.
+__device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, const ItemSlot& it, ItemSlot& next,
+                           int k, int q, int lane) {
+    const int n = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    int E = 0;
+    float sum_lc = 0.f;
+    for (int c = 0; c < it.nc; ++c) {
+        const uint32_t gc = it.g + c;
+        const int slot = gc % kGateSlots;
+        if (!wg_all(2, wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a))) return false;
+        const ChunkPlan pl = ms->plan[slot];
+        sum_lc = pl.sum_lc;
+        if (pl.rn && c > 0) {  // renormalise the state GEMM2 of the previous chunk left
+            if (!wg_all(2, wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a))) return false;
+            tc_fence_after();
+            row_scale(tl + TM_DS, exp2f(fmaxf(pl.preS, -149.f)));
+            const float m = state_reduce_max(row_absmax(tl + TM_DT), ms->red, q, lane);
+            const int e = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
+            row_scale(tl + TM_DT, ldexpf(1.f, -e));
+            E += e;
+        }
+        tc_fence_before();
+        named_sync(2);
+        if (n == 0) mbar_arrive(&ms->pre_done);
+        if (!wg_all(2, wait_bar(&ms->x_done_s, gc & 1, ms, a))) return false;
+        tc_fence_after();
+        state_pass<false>(tl + TM_XS);
+        if (!wg_all(2, wait_bar(&ms->x_done_t, gc & 1, ms, a))) return false;
+        tc_fence_after();
+        state_pass<true>(tl + TM_XT);
+        tc_fence_before();
+        named_sync(2);
+        if (n == 0) mbar_arrive(&ms->y_ready);
+        // The W operand of the next chunk (GEMM1 of this one is done with the buffer): the next chunk of
+        // this item, or the first of the next item.
+        uint32_t ng = gc + 1;
+        bool has_next = c + 1 < it.nc;
+        if (!has_next) {
+            const int s = (k + 1) % kItemSlots;
+            if (!wg_all(2, wait_bar(&ms->slot_full[s], ((k + 1) / kItemSlots) & 1, ms, a))) return false;
+            next = ms->slots[s];
+            named_sync(2);
+            if (n == 0) mbar_arrive(&ms->slot_read[s]);
+            has_next = next.nc > 0;
+            ng = next.g;
+        }
+        if (has_next) {
+            if (!wg_all(2, wait_bar(&ms->w_done, ng & 1, ms, a))) return false;
+            tc_fence_after();
+            convert_w(smem, tmem, q, lane);
+            fence_async_smem();
+            tc_fence_before();
+            named_sync(2);
+            if (n == 0) {
+                mbar_arrive(&ms->w_cvt);
+                mbar_arrive(&ms->w_read);
+            }
+        }
+    }
+    if (!wg_all(2, wait_bar(&ms->d_ready, (it.g + it.nc - 1) & 1, ms, a))) return false;
+    tc_fence_after();
+    state_epilogue(ms, a, it.obj, (float)E + sum_lc, tmem, q, lane);
+    state_init(tmem, q, lane);  // (I, 0) for the next item
+    return true;
 }
 
 // ---------------------------------------------------------------- kernel --
@@ -1020,10 +984,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&ms->fullK[s], 1);
             mbar_init(&ms->emptyK[s], 1);
+            mbar_init(&ms->k16_full[s], 1);
+            mbar_init(&ms->k16_empty[s], 1);
         }
-        // fullV .. drain (gready included) are consecutive in Misc: one arrival each, but bt_free (both
-        // issuers read That) and drain (both issuers' MMAs) take two
-        for (uint64_t* b = &ms->fullV; b <= &ms->drain; ++b)
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&ms->fullV[s], 1);
+            mbar_init(&ms->emptyV[s], 1);
+        }
+        // gready .. drain are consecutive in Misc: one arrival each, but bt_free (both issuers read the M
+        // forms) and drain (both issuers' MMAs) take two
+        for (uint64_t* b = &ms->gready[0]; b <= &ms->drain; ++b)
             mbar_init(b, b == &ms->bt_free[0] || b == &ms->bt_free[1] || b == &ms->drain ? 2 : 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&ms->slot_full[s], 1);
@@ -1036,71 +1006,112 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
-    if (warp == kWarpMMA) tmem_alloc(&ms->tmem_base, 512);
+    if (warp == kWarpIssP) tmem_alloc(&ms->tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
-    const bool is_state = warp >= kWarpState0 && warp < kWarpState0 + 4;
+    const bool is_state = warp >= kWarpState0;
+    const bool is_prep = warp >= kWarpPrep0 && warp < kWarpState0;
     const int q = warp & 3;  // tensor-memory lane quarter a warp may access
     if (is_state) state_init(tmem, q, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Every role runs through the items at its own pace: the producer takes
-    // them from the queue into a ring of kItemSlots slots, and the other roles
-    // copy them from there, so the next item's loads, gram, solve and W'^T
-    // overlap this item's last chunks and epilogue.  Across items the roles
-    // meet on the same barriers as within one (chunks are numbered CTA-wide).
-    for (int k = 0;; ++k) {
-        const int s = k % kItemSlots;
-        ItemSlot it;
-        if (warp == kWarpTMA) {
-            if (k >= kItemSlots && !wait_bar(&ms->slot_read[s], (k / kItemSlots - 1) & 1, ms, a)) break;
-            if (lane == 0) publish_item(ms, a, k, s);
-            __syncwarp();
-            it = ms->slots[s];
-        } else {
-            const bool one = warp == kWarpMMA || warp == kWarpMMA2;
-            if (one && lane != 0) break;
-            const int id = is_state ? 2 : 1, cnt = is_state ? 128 : kPrepThreads;
-            const bool ok = wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a);
-            if (one ? !ok : !wg_all(id, ok, cnt)) break;
-            it = ms->slots[s];
-            if (!one) named_sync(id, cnt);
-            if (one || (tid & (cnt - 1)) == ((32 * (is_state ? kWarpState0 : kWarpPrep0)) & (cnt - 1)))
+    if (is_state) {
+        // The state warps read item k + 1 from the ring during the last chunk of item k (to convert its
+        // first W operand early); the first item before the loop.
+        ItemSlot it, next;
+        bool ok = wg_all(2, wait_bar(&ms->slot_full[0], 0, ms, a));
+        if (ok) {
+            it = ms->slots[0];
+            named_sync(2);
+            if (tid == 32 * kWarpState0) mbar_arrive(&ms->slot_read[0]);
+            if (it.nc > 0) {
+                ok = wg_all(2, wait_bar(&ms->w_done, it.g & 1, ms, a));
+                if (ok) {
+                    tc_fence_after();
+                    convert_w(smem, tmem, q, lane);
+                    fence_async_smem();
+                    tc_fence_before();
+                    named_sync(2);
+                    if (tid == 32 * kWarpState0) {
+                        mbar_arrive(&ms->w_cvt);
+                        mbar_arrive(&ms->w_read);
+                    }
+                }
+            }
+        }
+        for (int k = 0; ok && it.nc > 0; ++k) {
+            if (!state_item(ms, smem, a, tmem, it, next, k, q, lane)) break;
+            it = next;
+            if (*(volatile int*)&ms->abort_flag) break;
+        }
+    } else {
+        // Every other role runs through the items at its own pace: the producer takes them from the
+        // queue into a ring of kItemSlots slots, and the other roles copy them from there, so the next
+        // item's loads, gram, solve and W^T overlap this item's last chunks and epilogue.  Across items
+        // the roles meet on the same barriers as within one (chunks are numbered CTA-wide).
+        for (int k = 0;; ++k) {
+            const int s = k % kItemSlots;
+            ItemSlot it;
+            if (warp == kWarpTMA) {
+                if (k >= kItemSlots && !wait_bar(&ms->slot_read[s], (k / kItemSlots - 1) & 1, ms, a)) break;
+                publish_item(ms, a, k, s, lane);
+                __syncwarp();
+                it = ms->slots[s];
+            } else if (warp == kWarpCvt) {
+                const bool ok = wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                it = ms->slots[s];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ms->slot_read[s]);
+            } else if (is_prep) {
+                const bool ok = wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a);
+                if (!wg_all(1, ok, kPrepThreads)) break;
+                it = ms->slots[s];
+                named_sync(1, kPrepThreads);
+                if (tid == 32 * kWarpPrep0) mbar_arrive(&ms->slot_read[s]);
+            } else {  // the issuers, one thread each
+                if (lane != 0) break;
+                if (!wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a)) break;
+                it = ms->slots[s];
                 mbar_arrive(&ms->slot_read[s]);
+            }
+            if (it.nc < 0) break;
+            if (warp == kWarpTMA) {
+                producer_role(ms, smem, a, &tmk, &tmv, it.g, it.nc, it.layer, it.head, it.b0, it.b1, lane);
+            } else if (warp == kWarpIssP) {
+                issue_prep_role(ms, smem, a, tmem, it.g, it.nc);
+            } else if (warp == kWarpIssS) {
+                issue_state_role(ms, smem, a, tmem, it.g, it.nc);
+            } else if (warp == kWarpCvt) {
+                convert_role(ms, smem, a, it.g, it.nc, lane);
+            } else {
+                prep_role(ms, smem, a, tmem, it.g, it.nc, tid - 32 * kWarpPrep0, q, lane);
+            }
+            if (*(volatile int*)&ms->abort_flag) break;
         }
-        if (it.nc < 0) break;
-        if (warp == kWarpTMA) {
-            producer_role(ms, smem, a, &tmk, &tmv, it.g, it.nc, it.layer, it.head, it.b0, it.b1, lane);
-        } else if (warp == kWarpMMA) {
-            mma_role(ms, smem, a, tmem, it.g, it.nc);
-        } else if (warp == kWarpMMA2) {
-            mma_role2(ms, smem, a, tmem, it.g, it.nc);
-        } else if (is_state) {
-            state_role(ms, smem, a, tmem, it.g, it.nc, it.obj, q, lane);
-        } else {
-            prep_role(ms, smem, a, tmem, it.g, it.nc, tid - 32 * kWarpPrep0, q, lane);
-        }
-        if (*(volatile int*)&ms->abort_flag) break;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Drain: every MMA this CTA issued (from both issuers) has completed before tensor memory is freed.
-    if (warp == kWarpMMA || warp == kWarpMMA2) {
+    // Drain: every MMA this CTA issued (from both issuers) has completed before tensor memory is freed.  A
+    // drain that runs out of polls is reported (the result is then not to be trusted); the memory is freed
+    // all the same, since the kernel is about to exit either way.
+    if (warp == kWarpIssP || warp == kWarpIssS) {
         if (lane == 0) {
             mma_commit(&ms->drain);
-            for (uint32_t i = 0; i < a.wait_limit && !mbar_try_wait(&ms->drain, 0); ++i) {
-            }
+            uint32_t i = 0;
+            while (i < a.wait_limit && !mbar_try_wait(&ms->drain, 0)) ++i;
+            if (i >= a.wait_limit) set_error(a.err, kErrTimeout);
         }
         __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kWarpMMA) tmem_dealloc(tmem, 512);
+    if (warp == kWarpIssP) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ host --

@@ -4,13 +4,15 @@ hypic_segment_build call (as each rank would), the pairs placed into one
 table by segment (what the pair gather produces), then the reuse chain run
 on that table -- all equal to the single build call and the same chain,
 bit for bit: a pair depends only on its own segment and every kernel reduces
-in a fixed order."""
+in a fixed order.  The chain itself is checked against the fp64 token loop
+over the whole request."""
 import numpy as np
 import pytest
 import torch
 
 from linear_attn_state_hypic_gb300 import shard, synth
-from tests.helpers import dev, host
+from oracle import oracle as orc
+from tests.helpers import TOL_BF16, TOL_F32, assert_rel, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -51,13 +53,14 @@ def test_disjoint_builds_then_chain_equal_one_call(B, d, dtype, world):
     np.testing.assert_array_equal(host(E2), host(E1))
     np.testing.assert_array_equal(host(S2), host(S1))
 
-    # one chain over every segment in order, the seam windows being each
-    # segment's skipped tail
+    # one chain over every segment in order, as the reuse path runs it: step s
+    # advances the state through segment s's seam window (its first skip[s]
+    # tokens, left out of the cached pair) and then composes the body pair
     seg_idx = np.arange(n_seg, dtype=np.int32)
     cu_chain = np.array([0, n_seg], np.int32)
-    tails = np.concatenate([np.arange(cu[s + 1] - skip[s], cu[s + 1]) for s in range(n_seg)])
+    heads = np.concatenate([np.arange(cu[s], cu[s] + skip[s]) for s in range(n_seg)])
     cu_step = np.concatenate([[0], np.cumsum(skip)]).astype(np.int32)
-    tt = torch.as_tensor(tails, device="cuda")
+    tt = torch.as_tensor(heads, device="cuda")
     q = dev(inp["q"], dtype)
     sq, sk, sv, sa, sb = (x.index_select(1, tt).contiguous() for x in (q, k, v, al, be))
     outs = []
@@ -68,4 +71,10 @@ def test_disjoint_builds_then_chain_equal_one_call(B, d, dtype, world):
     B.check_device()
     np.testing.assert_array_equal(outs[1][0], outs[0][0])
     np.testing.assert_array_equal(outs[1][1], outs[0][1])
-    assert np.all(np.isfinite(outs[0][0]))
+    # and the chain is the request's own recurrence: its end state and seam
+    # outputs are those of the fp64 token loop over all tokens
+    n = int(cu[-1])
+    ref_s, ref_o = orc.seam("gdn", inp["q"], inp["k"], inp["v"], [0, n], alpha=inp["alpha"], beta=inp["beta"])
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    assert_rel(outs[0][0][0], ref_s[0], tol, what="chain end state vs the full-sequence oracle")
+    assert_rel(outs[0][1], ref_o[:, heads], tol, axes=(-1,), what="seam outputs vs the full-sequence oracle")

@@ -70,3 +70,55 @@ def test_noalloc_rejects_batches_beyond_its_fixed_scratch(B):
     a.k = fake + 0x100008  # misaligned: the regular argument checks still apply
     a.n_segments, a.n_tokens = 2, 2
     assert B.hypic_segment_build_noalloc(a, None) == B.ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_segment_limit(B):
+    """Exactly HYPIC_NOALLOC_MAX_SEGMENTS short segments (lengths 0..8, one
+    layer and head, d=16, fp32): the order fills the fixed array to its end
+    and the counter block right after it is used.  The pairs must equal the
+    workspace build's; the time of the call (mostly the single-CTA ordering
+    of 16,384 segments) is printed."""
+    import torch
+    n = B.NOALLOC_MAX_SEGMENTS
+    rng = np.random.default_rng(77)
+    lengths = rng.integers(0, 9, n)
+    lengths[:4] = [0, 8, 1, 0]
+    inp = synth.gdn_ragged(seed=34, H=1, d=16, lengths=lengths, dtype="f32")
+    (T, Te, S), (T2, Te2, S2) = run_both(B, inp, "f32")
+    assert_rel(host(S2), host(S), TOL_F32, what="no-alloc S vs workspace S at the segment limit")
+    assert_rel(gdn_T64(T2, Te2), gdn_T64(T, Te), TOL_F32, what="no-alloc T vs workspace T at the segment limit")
+    k, v = dev(inp["k"], "f32"), dev(inp["v"], "f32")
+    a, b = dev(inp["alpha"]), dev(inp["beta"])
+    args, keep = B.build_args("gdn", k, v, inp["cu_seqlens"], alpha=a, beta=b, T_out=T2, T_exp_out=Te2, S_out=S2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    assert B.hypic_segment_build_noalloc(args, B._stream(None)) == B.OK
+    e1.record()
+    torch.cuda.synchronize()
+    B.check_device()
+    print(f"no-alloc build of {n} segments ({int(lengths.sum())} tokens, d=16): {e0.elapsed_time(e1):.3f} ms")
+
+
+@pytest.mark.gpu
+def test_noalloc_call_allocates_nothing(B):
+    """Around a warmed-up call, torch's allocator sees no new allocation or
+    segment: the call's only scratch is the library's fixed array."""
+    import torch
+    inp = synth.gdn_ragged(seed=35, H=2, d=128, lengths=[300, 65, 0])
+    k, v = dev(inp["k"], "bf16"), dev(inp["v"], "bf16")
+    a, b = dev(inp["alpha"]), dev(inp["beta"])
+    cu = inp["cu_seqlens"]
+    out = B.alloc_build_outputs("gdn", len(cu) - 1, k.shape[0], k.shape[2], k.shape[3], v.shape[3], k.device)
+    args, keep = B.build_args("gdn", k, v, cu, alpha=a, beta=b, T_out=out[0], T_exp_out=out[1], S_out=out[2])
+    assert B.hypic_segment_build_noalloc(args, B._stream(None)) == B.OK  # warm-up (module load, first lookup)
+    torch.cuda.synchronize()
+    before = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(),
+              len(torch.cuda.memory_snapshot()))
+    for _ in range(3):
+        assert B.hypic_segment_build_noalloc(args, B._stream(None)) == B.OK
+    torch.cuda.synchronize()
+    after = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved(), len(torch.cuda.memory_snapshot()))
+    B.check_device()
+    assert after == before, f"allocator state changed around the no-alloc call: {before} -> {after}"
+    del keep
