@@ -1,12 +1,14 @@
 """Segment parallelism, host side (CPU only): the LPT partition of a
-request's segments across ranks, the token gather of a rank's sub-batch, and
-the pair gather itself over two real torch.distributed ranks (gloo).
+request's segments across ranks, the token gather of a rank's sub-batch, the
+combine rank's table layout, and the pair stream itself over real
+torch.distributed ranks (gloo).
 
-In the two-rank test each rank builds the pairs of its own segments (with the
-oracle: there is no GPU here), the ranks exchange them with gather_pairs, and
-the gathered tables -- and the reuse chain composed from them -- must equal
-the single-process build of the whole batch exactly: every pair depends only
-on its own segment."""
+In the multi-rank test each rank builds the pairs of its own segments batch by
+batch (with the oracle: there is no GPU here) and streams each finished batch
+to the combine rank, which builds its own share in place.  The combine rank's
+table -- read through its segment index -- and the chain composed from it must
+equal the single-process build of the whole batch exactly: every pair depends
+only on its own segment.  The other ranks receive nothing."""
 import os
 import socket
 import sys
@@ -56,7 +58,7 @@ def _case():
     return inp
 
 
-def _rank_main(rank, world, port, out_dir):
+def _rank_main(rank, world, port, out_dir, n_batches):
     sys.path.insert(0, REPO)
     import torch
     import torch.distributed as dist
@@ -70,33 +72,55 @@ def _rank_main(rank, world, port, out_dir):
     segs = parts[rank]
     sub_cu, sub_skip, tok = sh.local_inputs(cu, skip, segs)
     pick = lambda x: np.ascontiguousarray(x[:, tok])
-    T, S = o.build_pairs("gdn", pick(inp["k"]), pick(inp["v"]), sub_cu, alpha=pick(inp["alpha"]),
-                         beta=pick(inp["beta"]), skip=sub_skip, n_threads=1)
-    T_full, S_full = sh.gather_pairs([torch.from_numpy(T), torch.from_numpy(S)], segs, n_seg)
-    np.save(os.path.join(out_dir, f"T{rank}.npy"), T_full.numpy())
-    np.save(os.path.join(out_dir, f"S{rank}.npy"), S_full.numpy())
+    k, v, al, be = (pick(inp[key]) for key in ("k", "v", "alpha", "beta"))
+    d = k.shape[-1]
+
+    def build_batch(lo, hi, views):  # the pairs of segs[lo:hi], from their own tokens only
+        a, b = int(sub_cu[lo]), int(sub_cu[hi])
+        T, S = o.build_pairs("gdn", k[:, a:b], v[:, a:b], sub_cu[lo:hi + 1] - a, alpha=al[:, a:b], beta=be[:, a:b],
+                             skip=sub_skip[lo:hi], n_threads=1)
+        views[0].copy_(torch.from_numpy(T))
+        views[1].copy_(torch.from_numpy(S))
+
+    rows = n_seg if rank == 0 else len(segs)
+    tables = [torch.full((rows, 1, 2, d, d), float("nan"), dtype=torch.float64) for _ in range(2)]
+    sh.stream_pairs(build_batch, tables, parts, rank, dst=0, n_batches=n_batches)
+    if rank == 0:
+        np.save(os.path.join(out_dir, "T.npy"), tables[0].numpy())
+        np.save(os.path.join(out_dir, "S.npy"), tables[1].numpy())
     dist.destroy_process_group()
 
 
-def test_two_gloo_ranks_gather_equals_one_build(tmp_path):
+@pytest.mark.parametrize("world,n_batches", [(2, 1), (2, 3), (3, 2)])
+def test_gloo_ranks_stream_pairs_equal_one_build(tmp_path, world, n_batches):
     torch = pytest.importorskip("torch")
     import torch.multiprocessing as mp
-    world = 2
-    ctx = mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=False,
-                             start_method="spawn")
+    ctx = mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path), n_batches), nprocs=world,
+                             join=False, start_method="spawn")
     while not ctx.join(timeout=120):
         pass
     inp = _case()
     cu, skip = inp["cu_seqlens"], inp["seam_skip"]
+    n_seg = len(cu) - 1
     T1, S1 = orc.build_pairs("gdn", inp["k"], inp["v"], cu, alpha=inp["alpha"], beta=inp["beta"], skip=skip,
                              n_threads=1)
-    for r in range(world):
-        Tg, Sg = np.load(tmp_path / f"T{r}.npy"), np.load(tmp_path / f"S{r}.npy")
-        np.testing.assert_array_equal(Tg, T1)
-        np.testing.assert_array_equal(Sg, S1)
-    # the chain composed from the gathered tables is the single-process one
-    n_seg = len(cu) - 1
-    Tg, Sg = np.load(tmp_path / "T0.npy"), np.load(tmp_path / "S0.npy")
+    parts = shard.lpt_partition(np.diff(cu) - skip, world)
+    _, row_of = shard.combine_rows(parts)
+    Tg, Sg = np.load(tmp_path / "T.npy"), np.load(tmp_path / "S.npy")
+    np.testing.assert_array_equal(Tg[row_of], T1)
+    np.testing.assert_array_equal(Sg[row_of], S1)
+    # the chain composed on the combine rank, through its segment index, is the single-process one
     ref = orc.compose("gdn", T1, S1, [0, n_seg], np.arange(n_seg))
-    got = orc.compose("gdn", Tg, Sg, [0, n_seg], np.arange(n_seg))
+    got = orc.compose("gdn", Tg, Sg, [0, n_seg], row_of)
     np.testing.assert_array_equal(got, ref)
+
+
+def test_combine_rows_and_batches():
+    offsets, row_of = shard.combine_rows([[0, 3], [1], [2, 4, 5]])
+    assert offsets.tolist() == [0, 2, 3, 6]
+    assert row_of.tolist() == [0, 2, 3, 1, 4, 5]
+    with pytest.raises(ValueError):
+        shard.combine_rows([[0], [0]])
+    assert shard.batch_bounds(7, 3) == [(0, 2), (2, 5), (5, 7)]
+    assert shard.batch_bounds(2, 4) == [(0, 1), (1, 2)]
+    assert shard.batch_bounds(0, 4) == []
