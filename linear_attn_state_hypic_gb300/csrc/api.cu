@@ -200,6 +200,9 @@ extern "C" hypic_status hypic_segment_build(const hypic_build_args* args, void* 
     if (gdn_build_tc_supported(p)) {
         e = launch_gdn_build_tc(p, workspace, err, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core build launch");
+    } else if (decay_build_tc_supported(p)) {
+        e = launch_decay_build_tc(p, workspace, err, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core decay-family build launch");
     } else {
         e = launch_build_simt(p, workspace, err, s);
         if (e != cudaSuccess) return cuda_fail(e, "build launch");

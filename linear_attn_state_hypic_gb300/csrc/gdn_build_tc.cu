@@ -20,11 +20,12 @@
 // power-of-two scale 2^lsS set from the gates alone.  Per chunk:
 //   gram    G = K K^T                              bf16 MMA, M=64  N=64  K=128
 //   solve   M from G and b                         CUDA cores + warp MMAs (block-triangular inverse)
-//   W^T     -(M Diag(b) K)^T                       fp16 MMA, M=128 N=64  K=64 (keys converted to fp16)
+//   W^T     -(M Diag(b) K)^T                       bf16 MMA, M=128 N=64  K=64, twice (M form as hi + lo)
 //   U~      V^T (M Diag(b uf))^T into X_S          bf16 MMA, M=128 N=64  K=64 (uf = 2^(-lg2 g_t - lsS))
+//   convert W^T -> tf32 operand in shared memory   (CUDA cores)
 //   GEMM1   X_h (+)= D''_h (-W^)^T                 tf32 MMA, A read from tensor memory
-//   pass    X_T -> fp16, X_S -> bf16 in place     (a format conversion, nothing else)
-//   GEMM2   D''_h += X_h K                         fp16 (T) / bf16 (S) MMA, M=128 N=128 K=64,
+//   pass    X_T -> bf16 hi + lo, X_S -> bf16       in place (a format conversion, nothing else)
+//   GEMM2   D''_h += X_h K                         bf16 MMA, M=128 N=128 K=64 (twice for T: hi, lo),
 //                                                  A read from tensor memory
 // A renormalisation chunk (every 16 chunks, the last chunk of a segment, and
 // chunks whose decay would push the S scale past 2^-112) first rescales the
@@ -36,14 +37,15 @@
 // mantissa and a power-of-two exponent.
 //
 // Roles (512 threads): warp 0 loads keys and values (TMA), writes the gate
-// tables and plans each chunk's scales; warp 3 converts each key tile to
-// fp16; two single-thread MMA issuers: warp 1 the prep stream (gram, W^T),
-// warp 2 the state stream (U~, GEMM1, GEMM2); warps 4-11 (prep) turn each
-// gram into the two M forms; warps 12-15 (state) run the passes, convert W^
-// into a tf32 operand, renormalise and write the result.  Only the two state
-// GEMMs and the (cheap) passes are serial per chunk; the prep runs ahead.  The
-// roles meet on mbarriers; every wait is bounded and a wait that runs out
-// sets the device error word.
+// tables and plans each chunk's scales; three single-thread MMA issuers (a
+// thread sends a small MMA only about every 60 cycles): warp 1 the prep
+// stream (gram, W^T), warp 2 the S half (U~, GEMM1, GEMM2), warp 3 the T half
+// (GEMM1, GEMM2); warps 4-11 (prep) turn each gram into the M forms; warps
+// 12-15 (state) run the passes, convert W^ into the tf32 operand, renormalise
+// and write the result.  Per chunk the state stream is serial (GEMM1, passes,
+// W operand, GEMM2); the prep runs up to two chunks ahead.  The roles meet on
+// mbarriers; every wait is bounded and a wait that runs out sets the device
+// error word.
 // One CTA per SM, persistent over (segment, layer, head) items taken from an
 // atomic queue in longest-body-first order.  Warp 0 publishes them through a
 // ring of item slots and each role runs through them at its own pace, so one
@@ -70,21 +72,21 @@ using namespace tc;
 
 constexpr int kD = 128;           // dk = dv
 constexpr int kC = 64;            // chunk length
-constexpr int kKStages = 3;       // key tiles in flight (bf16 and their fp16 copies)
+constexpr int kKStages = 4;       // key tiles in flight (from the gram, issued early, to GEMM2)
 constexpr int kVStages = 2;
 constexpr int kGateSlots = 4;     // per-chunk gate tables in flight
 constexpr int kThreads = 512;
-constexpr int kWarpTMA = 0, kWarpIssP = 1, kWarpIssS = 2, kWarpCvt = 3, kWarpPrep0 = 4, kWarpState0 = 12;
+constexpr int kWarpTMA = 0, kWarpIssP = 1, kWarpIssS = 2, kWarpIssT = 3, kWarpPrep0 = 4, kWarpState0 = 12;
 constexpr int kPrepThreads = 256;  // warps 4-11: two warps per tensor-memory lane quarter
 
 // Shared memory map (byte offsets; every operand region is 1024-byte aligned).
 constexpr uint32_t kTile = 16384;                        // 64 tokens x 128 (b)f16, two 64-column TMA boxes
 constexpr uint32_t OFF_K = 0;                            // bf16 key ring
-constexpr uint32_t OFF_K16 = OFF_K + kKStages * kTile;   // fp16 copies of the same tiles
-constexpr uint32_t OFF_V = OFF_K16 + kKStages * kTile;   // value ring
-constexpr uint32_t OFF_W = OFF_V + kVStages * kTile;     // -W^: tf32 [64 t][128 i], K-major, 4 blocks of 32 i
-constexpr uint32_t kBT = 16384;                          // -M Diag(b) fp16 [64][64], then M Diag(b uf) bf16
-constexpr uint32_t OFF_BT = OFF_W + 32768;               // two of them: chunk gc uses buffer gc % 2
+constexpr uint32_t OFF_V = OFF_K + kKStages * kTile;     // value ring
+constexpr uint32_t kWBytes = 32768;                      // -W^: tf32 [64 t][128 i], K-major, 4 blocks of 32 i
+constexpr uint32_t OFF_W = OFF_V + kVStages * kTile;     // one: rewritten only after both GEMM1s that read it
+constexpr uint32_t kBT = 24576;                          // -M Diag(b) hi, lo, then M Diag(b uf): bf16 [64][64]
+constexpr uint32_t OFF_BT = OFF_W + kWBytes;             // two of them: chunk gc uses buffer gc % 2
 constexpr uint32_t OFF_AS = OFF_BT + 2 * kBT;            // A^ / M: fp32 [64][kAS] (padded rows)
 constexpr int kAS = 68;
 constexpr uint32_t OFF_PT = OFF_AS + ((64 * kAS * 4 + 1023) / 1024) * 1024;  // solve scratch: 32 x 36 fp32
@@ -97,7 +99,7 @@ struct ItemSlot {
     int nc, layer, head;  // nc > 0, or nc < 0: the queue is exhausted
 };
 constexpr int kItemSlots = 4;
-constexpr int kSlotReaders = 5;  // warp 1, warp 2, warp 3, the prep warps, the state warps
+constexpr int kSlotReaders = 5;  // the three issuers, the prep warps, the state warps
 
 // The scales of one chunk, planned by the producer from the gates.
 struct ChunkPlan {
@@ -108,16 +110,22 @@ struct ChunkPlan {
 };
 
 struct Misc {
-    uint64_t fullK[kKStages], emptyK[kKStages], k16_full[kKStages], k16_empty[kKStages];
+    uint64_t fullK[kKStages], emptyK[kKStages];
     uint64_t fullV[kVStages], emptyV[kVStages];
     uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables and plan of a chunk written
-    uint64_t g_done, g_read;      // gram committed; gram read by the prep warps
+    uint64_t g_done, g_read;        // gram committed; gram read by the prep warps
     // M forms of chunk gc written (that_ready[gc % 2]); the W^T and U~ MMAs that read them are done
     // (bt_free[gc % 2], one commit from each issuer).
     uint64_t that_ready[2], bt_free[2];
-    uint64_t w_done, w_read, w_cvt;  // W^T committed; read from tensor memory; tf32 operand written
+    // W^T committed; read from tensor memory; the tf32 operand of chunk gc written (w_cvt[gc % 2]: the
+    // operand of chunk gc + 1 may be written before the issuer of one half has waited for that of chunk
+    // gc, so consecutive chunks signal on different barriers)
+    uint64_t w_done, w_read, w_cvt[2];
     uint64_t pre_done;               // state ready for GEMM1 (initialised or renormalised)
-    uint64_t x_done_s, x_done_t, y_ready, d_ready, drain;
+    uint64_t x_done_s, x_done_t;     // GEMM1 of the S / T half committed
+    uint64_t y_ready_s, y_ready_t;   // pass of the S / T half done
+    uint64_t d_ready_s, d_ready_t;   // GEMM2 of the S / T half committed
+    uint64_t drain;
     alignas(16) float beta[kGateSlots][kC];
     alignas(16) float uf[kGateSlots][kC];  // 2^(-lg2 g_t - lsS): the U~ weight of token t
     ChunkPlan plan[kGateSlots];
@@ -135,12 +143,12 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // Tensor-memory columns.
 constexpr uint32_t TM_DT = 0, TM_DS = 128, TM_XT = 256, TM_XS = 320, TM_G = 384, TM_W = 448;
 
-constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+constexpr uint32_t kFmtBF16 = 1, kFmtTF32 = 2;
 constexpr uint32_t ID_GRAM = idesc(kFmtBF16, 64, 64, false, false);   // G = K K^T
-constexpr uint32_t ID_W = idesc(kFmtF16, 128, 64, true, false);       // W^T: A = K^T (MN-major)
+constexpr uint32_t ID_W = idesc(kFmtBF16, 128, 64, true, false);      // W^T: A = K^T (MN-major)
 constexpr uint32_t ID_U = idesc(kFmtBF16, 128, 64, true, false);      // U~: A = V^T (MN-major)
 constexpr uint32_t ID_G1 = idesc(kFmtTF32, 128, 64, false, false);    // X = D'' W^T (A in TMEM)
-constexpr uint32_t ID_G2T = idesc(kFmtF16, 128, 128, false, true);    // D''_T += X_T K (B = K, MN-major)
+constexpr uint32_t ID_G2T = idesc(kFmtBF16, 128, 128, false, true);   // D''_T += X_T K (B = K, MN-major)
 constexpr uint32_t ID_G2S = idesc(kFmtBF16, 128, 128, false, true);   // D''_S += X_S K
 
 struct TcArgs {
@@ -159,6 +167,7 @@ struct TcArgs {
     uint32_t wait_limit;  // polls of the final drain
     uint64_t wait_ns;     // time limit of every other wait
 };
+
 
 // Bounded wait shared by all roles: the waiting warp sleeps until the phase
 // completes (re-polling at least every few microseconds); it gives up, and
@@ -185,27 +194,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
     if (mbar_try_wait(bar, parity)) return true;
     return wait_bar_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
 }
-// The state-stream issuer's wait: it spins on the phase (a sleeping thread
-// answers a completed phase late, and this thread's MMAs are the chain).
-__device__ __noinline__ bool spin_bar_slow(uint64_t* bar, uint32_t parity, int* abort_flag, uint64_t wait_ns,
-                                           unsigned* err) {
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int j = 0; j < 64; ++j)
-            if (mbar_test(bar, parity)) return true;
-        if (*(volatile int*)abort_flag) return false;
-        if (globaltimer_ns() - t0 > wait_ns) break;
-    }
-    *(volatile int*)abort_flag = 1;
-    set_error(err, kErrTimeout);
-    return false;
-}
-__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
-    if (mbar_test(bar, parity)) return true;
-    return spin_bar_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
-}
-
 __device__ __forceinline__ void named_sync(int id, int n = 128) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -214,20 +202,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
-// Two floats as fp16 (round to nearest, saturating to the largest finite value).
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
+// Two values as bf16 pairs x = hi + lo: hi is x with its 16 low bits cleared
+// (exact; two values packed by one byte permute), lo = x - hi (exact in fp32)
+// rounded to bf16, so hi + lo keeps about 16 significant bits of x.
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const uint32_t hx = __float_as_uint(x) & 0xffff0000u, hy = __float_as_uint(y) & 0xffff0000u;
+    hi = __byte_perm(hx, hy, 0x7632);
+    lo = pack_bf16(x - __uint_as_float(hx), y - __uint_as_float(hy));
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
-__device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+// x rounded to tf32 (nearest, ties away from zero) by integer arithmetic on
+// its bits: add half a tf32 unit of the last place, then clear the 13 low bits.
+__device__ __forceinline__ float tf32_round(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 // ------------------------------------------------------------ producer --
@@ -337,30 +327,6 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CU
     }
 }
 
-// Warp 3: each key tile converted to fp16 in the same (swizzled) layout.
-// bf16 -> fp16 is exact for |k| >= 2^-14 and loses at most 2^-25 below.
-__device__ void convert_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t g, int nc, int lane) {
-    for (int c = 0; c < nc; ++c) {
-        const uint32_t gc = g + c, s = gc % kKStages, u = gc / kKStages;
-        bool ok = wait_bar(&ms->fullK[s], u & 1, ms, a);
-        ok = ok && (u == 0 || wait_bar(&ms->k16_empty[s], (u - 1) & 1, ms, a));
-        if (!__all_sync(0xffffffffu, ok)) return;
-        const uint4* src = reinterpret_cast<const uint4*>(smem + OFF_K + s * kTile);
-        uint4* dst = reinterpret_cast<uint4*>(smem + OFF_K16 + s * kTile);
-#pragma unroll 4
-        for (int j = 0; j < (int)(kTile / 16 / 32); ++j) {
-            const uint4 x = src[32 * j + lane];
-            auto cv = [](uint32_t w) {  // two bf16 (low = first) -> two fp16
-                return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-            };
-            dst[32 * j + lane] = make_uint4(cv(x.x), cv(x.y), cv(x.z), cv(x.w));
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->k16_full[s]);
-    }
-}
-
 // ----------------------------------------------------------- prep roles --
 // p: thread index inside the prep warps (0..255); q: its tensor-memory lane
 // quarter; lane: lane in the warp.
@@ -400,12 +366,6 @@ __device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, i
 // (x = hi + lo, lo the rounding residual of hi) and a product as
 // hi*hi + hi*lo + lo*hi, which keeps about 16 bits of every operand: the
 // solve then matches an fp32 one to ~3e-6 relative.
-__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
-    const float hx = bf16_round(x), hy = bf16_round(y);
-    hi = pack_bf16(hx, hy);
-    lo = pack_bf16(x - hx, y - hy);
-}
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -474,7 +434,7 @@ __device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, in
 //            (warp w: 16 x 8 tile w of it).
 // The products run over full blocks: the zero upper parts of the triangular
 // factors make that exact.  Ptmp holds the left products.
-__device__ void prep_solve(float* As, float* Ptmp, int p) {
+__device__ void prep_solve(float* As, float* Ptmp, int p, int bar) {
     const int w = p >> 5, lane = p & 31;
     if (p < kC) {  // level 1
         const int b = p >> 4, c = p & 15;
@@ -492,7 +452,7 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) Mb[i * kAS] = s[i];
     }
-    named_sync(1, kPrepThreads);
+    named_sync(bar, kPrepThreads);
     {  // level 2: P = A_{x+1,x} M_xx, then M_{x+1,x} = -M_{x+1,x+1} P, x = 0, 2
         const int x = 2 * ((w >> 1) & 1), nt = w & 1;
         float* P = Ptmp + ((w >> 1) & 1) * 320;  // 16 x 16, row stride 20
@@ -501,31 +461,50 @@ __device__ void prep_solve(float* As, float* Ptmp, int p) {
             warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * x, kAS, As + 16 * x * kAS + 16 * x + 8 * nt, kAS, lane);
             warp_store<1>(c, P + 8 * nt, 20, 1.f, lane);
         }
-        named_sync(1, kPrepThreads);
+        named_sync(bar, kPrepThreads);
         if (w < 4) {
             warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * (x + 1), kAS, P + 8 * nt, 20, lane);
             warp_store<1>(c, As + 16 * (x + 1) * kAS + 16 * x + 8 * nt, kAS, -1.f, lane);
         }
     }
-    named_sync(1, kPrepThreads);
+    named_sync(bar, kPrepThreads);
     {  // level 3: P = A[32:64, 0:32] M[0:32, 0:32], then M[32:64, 0:32] = -M[32:64, 32:64] P
-        const int r0 = 16 * (w >> 2), c0 = 8 * (w & 3);
-        float c[1][4];
-        warp_gemm<2, 1>(c, As + (32 + r0) * kAS, kAS, As + c0, kAS, lane);
-        warp_store<1>(c, Ptmp + r0 * 36 + c0, 36, 1.f, lane);  // 32 x 32, row stride 36
-        named_sync(1, kPrepThreads);
-        warp_gemm<2, 1>(c, As + (32 + r0) * kAS + 32, kAS, Ptmp + c0, 36, lane);
-        warp_store<1>(c, As + (32 + r0) * kAS + c0, kAS, -1.f, lane);
+        // (8 tiles of 16 x 8, taken in turn by the group's warps)
+        constexpr int kWarps = kPrepThreads / 32;
+        float c[8 / kWarps][1][4];
+#pragma unroll
+        for (int i = 0; i < 8 / kWarps; ++i) {
+            const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
+            warp_gemm<2, 1>(c[i], As + (32 + r0) * kAS, kAS, As + c0, kAS, lane);
+        }
+#pragma unroll
+        for (int i = 0; i < 8 / kWarps; ++i) {
+            const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
+            warp_store<1>(c[i], Ptmp + r0 * 36 + c0, 36, 1.f, lane);  // 32 x 32, row stride 36
+        }
+        named_sync(bar, kPrepThreads);
+#pragma unroll
+        for (int i = 0; i < 8 / kWarps; ++i) {
+            const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
+            warp_gemm<2, 1>(c[i], As + (32 + r0) * kAS + 32, kAS, Ptmp + c0, 36, lane);
+        }
+#pragma unroll
+        for (int i = 0; i < 8 / kWarps; ++i) {
+            const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
+            warp_store<1>(c[i], As + (32 + r0) * kAS + c0, kAS, -1.f, lane);
+        }
     }
-    named_sync(1, kPrepThreads);
+    named_sync(bar, kPrepThreads);
 }
 
-// The two forms of M as K-major 64 x 64 operands (128-byte rows, 128-byte
-// swizzle): -M Diag(b) in fp16 at bt (the W^T product; negated so that GEMM1
-// yields -X) and M Diag(b uf) in bf16 at bt + 8192 (the U~ product; the
-// weights span up to 2^112, beyond fp16).  Thread p writes a quarter of a row.
+// The forms of M as K-major 64 x 64 bf16 operands (128-byte rows, 128-byte
+// swizzle): -M Diag(b) as a hi + lo pair at bt and bt + 8192 (the W^T
+// product, to about 16 bits; negated so that GEMM1 yields -X), and M Diag(b uf)
+// at bt + 16384 (the U~ product).  Thread p writes a quarter of a row.
 __device__ void prep_write_forms(const Misc* ms, const float* As, uint32_t bt, int slot, int p) {
-    const int t = p >> 2, qr = p & 3;
+#pragma unroll 1
+  for (int u = p; u < 256; u += kPrepThreads) {
+    const int t = u >> 2, qr = u & 3;
     const float* row = As + t * kAS + 16 * qr;
     const float* beta = ms->beta[slot] + 16 * qr;
     const float* uf = ms->uf[slot] + 16 * qr;
@@ -540,16 +519,18 @@ __device__ void prep_write_forms(const Misc* ms, const float* As, uint32_t bt, i
         const float mv[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
                              x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
         const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t wf[4], wu[4];
+        uint32_t wh[4], wl[4], wu[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            wf[jj] = pack_f16(-mv[2 * jj], -mv[2 * jj + 1]);
+            split_bf16(-mv[2 * jj], -mv[2 * jj + 1], wh[jj], wl[jj]);
             wu[jj] = pack_bf16(mv[2 * jj] * uv[2 * jj], mv[2 * jj + 1] * uv[2 * jj + 1]);
         }
         const uint32_t off = t * 128u + ((uint32_t)((2 * qr + ch) ^ (t & 7)) << 4);
-        st_shared_v4(bt + off, wf[0], wf[1], wf[2], wf[3]);
-        st_shared_v4(bt + 8192u + off, wu[0], wu[1], wu[2], wu[3]);
+        st_shared_v4(bt + off, wh[0], wh[1], wh[2], wh[3]);
+        st_shared_v4(bt + 8192u + off, wl[0], wl[1], wl[2], wl[3]);
+        st_shared_v4(bt + 16384u + off, wu[0], wu[1], wu[2], wu[3]);
     }
+  }
 }
 
 // ---------------------------------------------------------- state roles --
@@ -613,21 +594,34 @@ __device__ float state_reduce_max(float v, float* slot, int q, int lane) {
 
 // The pass of one half after GEMM1: X (64 fp32 columns) rewritten in place as
 // the A operand of GEMM2, two tokens per column (the lower token in the low
-// half): fp16 for T (values of order one: the T half carries no decay), bf16
-// for S (its lazy scale spans up to 2^112).
+// half).  S half: bf16 (its lazy scale spans up to 2^112), tokens 2j, 2j + 1 in
+// column j.  T half: a bf16 hi + lo pair (about 16 bits; T_C over long
+// segments needs more than one bf16), tokens 16k..16k+15 as hi in columns
+// 16k..16k+7 and lo in 16k+8..16k+15, each group of 16 columns read and then
+// rewritten in place.
 template <bool kHalfT>
 __device__ __forceinline__ void state_pass(uint32_t addr) {
+    if (kHalfT) {
 #pragma unroll 1
-    for (int m = 0; m < 2; ++m) {
-        uint32_t x[32], y[16];
-        tmem_ld32(addr + 32 * m, x);
-        tmem_wait_ld();
+        for (int k = 0; k < 4; ++k) {
+            uint32_t x[16], y[16];
+            tmem_ld16(addr + 16 * k, x);
+            tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float lo = __uint_as_float(x[2 * j]), hi = __uint_as_float(x[2 * j + 1]);
-            y[j] = kHalfT ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+            for (int j = 0; j < 8; ++j)
+                split_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]), y[j], y[8 + j]);
+            tmem_st16(addr + 16 * k, y);
         }
-        tmem_st16(addr + 16 * m, y);
+    } else {
+#pragma unroll 1
+        for (int m = 0; m < 2; ++m) {
+            uint32_t x[32], y[16];
+            tmem_ld32(addr + 32 * m, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+            tmem_st16(addr + 16 * m, y);
+        }
     }
     tmem_wait_st();
 }
@@ -648,7 +642,7 @@ __device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             *reinterpret_cast<float*>(b + j * 128 + ((c4 ^ (uint32_t)(j & 7)) << 4)) =
-                tf32_rna(__uint_as_float(w[j]));
+                tf32_round(__uint_as_float(w[j]));
     }
 }
 
@@ -727,7 +721,7 @@ __device__ void issue_prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32
     uint64_t t_idle = 0;
     while (iw < nc) {
         bool any = false;
-        if (ig < nc && ig <= iw + 2) {  // G = K K^T (K-major view of the key tile, two 64-wide boxes)
+        if (ig < nc && ig <= iw + 3) {  // G = K K^T (K-major view of the key tile, two 64-wide boxes)
             const uint32_t gc = g + ig;
             if (mbar_test(&ms->fullK[gc % kKStages], (gc / kKStages) & 1) &&
                 (gc == 0 || mbar_test(&ms->g_read, (gc - 1) & 1))) {
@@ -743,16 +737,19 @@ __device__ void issue_prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32
                 any = true;
             }
         }
-        if (iw < ig) {  // W^T = K^T (-M Diag(b))^T into the W columns (a descriptor's address counts 16 B)
+        if (iw < ig) {  // W^T = K^T (-M Diag(b))^T (hi + lo) into the W columns (a descriptor's address counts 16 B)
             const uint32_t gc = g + iw;
             if (mbar_test(&ms->that_ready[gc & 1], (gc >> 1) & 1) &&
-                mbar_test(&ms->k16_full[gc % kKStages], (gc / kKStages) & 1) &&
                 (gc == 0 || mbar_test(&ms->w_read, (gc - 1) & 1))) {
                 tc_fence_after();
-                const uint64_t a0 = sdesc_sw128(sb + OFF_K16 + (gc % kKStages) * kTile, 8192, 1024),
-                               b0 = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT, 0, 1024);
+                const uint64_t a0 = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 8192, 1024),
+                               bh = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT, 0, 1024),
+                               bl = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT + 8192, 0, 1024);
 #pragma unroll 1
-                for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_W, a0 + 128 * k, b0 + 2 * k, ID_W, k > 0);
+                for (int k = 0; k < 4; ++k) {
+                    mma_bf16_ss(tmem + TM_W, a0 + 128 * k, bh + 2 * k, ID_W, k > 0);
+                    mma_bf16_ss(tmem + TM_W, a0 + 128 * k, bl + 2 * k, ID_W, true);
+                }
                 mma_commit(&ms->w_done);
                 mma_commit(&ms->bt_free[gc & 1]);
                 ++iw;
@@ -767,60 +764,104 @@ __device__ void issue_prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32
     }
 }
 
-// Warp 2, one thread: the state stream, in chunk order: U~ into X_S, GEMM1 of
-// both halves, then (after the passes) GEMM2 of both halves.
-__device__ void issue_state_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
+// The state-stream issuers' wait: a spin on the phase (a suspended thread
+// answers a completed phase late, and these threads' MMAs are the chain).
+__device__ __noinline__ bool issuer_wait_slow(uint64_t* bar, uint32_t parity, int* abort_flag, uint64_t wait_ns,
+                                              unsigned* err) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int j = 0; j < 64; ++j)
+            if (mbar_test(bar, parity)) return true;
+        if (*(volatile int*)abort_flag) return false;
+        if (globaltimer_ns() - t0 > wait_ns) break;
+    }
+    *(volatile int*)abort_flag = 1;
+    set_error(err, kErrTimeout);
+    return false;
+}
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, Misc* ms, const TcArgs& a) {
+    if (mbar_test(bar, parity)) return true;
+    return issuer_wait_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
+}
+
+// Warp 2, one thread: the S half in chunk order -- U~ into X_S, GEMM1, then
+// (after the S pass) GEMM2.  A thread issues a small MMA only every ~60
+// cycles, so the two halves have an issuer each; every accumulator's MMAs
+// come from one thread, in order.
+__device__ void issue_s_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
     const uint32_t sb = smem_u32(smem);
-    const uint64_t bw = sdesc_sw128(sb + OFF_W, 0, 1024);
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
+        const uint64_t bw = sdesc_sw128(sb + OFF_W, 0, 1024);
         // U~ = V^T (M Diag(b uf))^T: needs the M forms, the values and a free X_S (GEMM2 of the previous
         // chunk has read it)
-        if (!spin_bar(&ms->that_ready[gc & 1], (gc >> 1) & 1, ms, a)) return;
-        if (!spin_bar(&ms->fullV[gc % kVStages], (gc / kVStages) & 1, ms, a)) return;
-        if (gc >= 1 && !spin_bar(&ms->d_ready, (gc - 1) & 1, ms, a)) return;
+        if (!issuer_wait(&ms->that_ready[gc & 1], (gc >> 1) & 1, ms, a)) return;
+        if (!issuer_wait(&ms->fullV[gc % kVStages], (gc / kVStages) & 1, ms, a)) return;
+        if (gc >= 1 && !issuer_wait(&ms->d_ready_s, (gc - 1) & 1, ms, a)) return;
         tc_fence_after();
         {
             const uint64_t a0 = sdesc_sw128(sb + OFF_V + (gc % kVStages) * kTile, 8192, 1024),
-                           b0 = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT + 8192, 0, 1024);
+                           b0 = sdesc_sw128(sb + OFF_BT + (gc & 1) * kBT + 16384, 0, 1024);
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) mma_bf16_ss(tmem + TM_XS, a0 + 128 * k, b0 + 2 * k, ID_U, k > 0);
         }
         mma_commit(&ms->emptyV[gc % kVStages]);
         mma_commit(&ms->bt_free[gc & 1]);
-        // GEMM1 (tf32, A = the state in tensor memory): X_S += D''_S (-W^)^T, X_T = D''_T (-W^)^T
-        if (!spin_bar(&ms->w_cvt, gc & 1, ms, a)) return;
-        if (!spin_bar(&ms->pre_done, gc & 1, ms, a)) return;
+        // GEMM1 (tf32, A = the state in tensor memory): X_S += D''_S (-W^)^T
+        if (!issuer_wait(&ms->w_cvt[gc & 1], (gc >> 1) & 1, ms, a)) return;
+        if (!issuer_wait(&ms->pre_done, gc & 1, ms, a)) return;
         tc_fence_after();
 #pragma unroll 4
         for (int k = 0; k < 16; ++k)
             mma_tf32_ts(tmem + TM_XS, tmem + TM_DS + 8 * k, bw + 512 * (k >> 2) + 2 * (k & 3), ID_G1, true);
         mma_commit(&ms->x_done_s);
+        // GEMM2 (bf16, A = the pass's output in tensor memory): D''_S += X_S K
+        if (!issuer_wait(&ms->y_ready_s, gc & 1, ms, a)) return;
+        tc_fence_after();
+        {
+            const uint64_t kt = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 8192, 1024);
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) mma_bf16_ts(tmem + TM_DS, tmem + TM_XS + 8 * k, kt + 128 * k, ID_G2S, true);
+        }
+        mma_commit(&ms->d_ready_s);
+        mma_commit(&ms->emptyK[gc % kKStages]);
+    }
+}
+
+// Warp 3, one thread: the T half in chunk order -- GEMM1, then (after the T
+// pass) GEMM2.
+__device__ void issue_t_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc) {
+    const uint32_t sb = smem_u32(smem);
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t gc = g + c;
+        const uint64_t bw = sdesc_sw128(sb + OFF_W, 0, 1024);
+        // GEMM1 (tf32): X_T = D''_T (-W^)^T; X_T is free once GEMM2 of the previous chunk has read it
+        if (!issuer_wait(&ms->w_cvt[gc & 1], (gc >> 1) & 1, ms, a)) return;
+        if (!issuer_wait(&ms->pre_done, gc & 1, ms, a)) return;
+        if (gc >= 1 && !issuer_wait(&ms->d_ready_t, (gc - 1) & 1, ms, a)) return;
+        tc_fence_after();
 #pragma unroll 4
         for (int k = 0; k < 16; ++k)
             mma_tf32_ts(tmem + TM_XT, tmem + TM_DT + 8 * k, bw + 512 * (k >> 2) + 2 * (k & 3), ID_G1, k > 0);
         mma_commit(&ms->x_done_t);
-        // GEMM2: D''_T += X_T K (fp16), D''_S += X_S K (bf16), A from the passes' output in tensor memory
-        if (!spin_bar(&ms->y_ready, gc & 1, ms, a)) return;
-        if (!spin_bar(&ms->k16_full[gc % kKStages], (gc / kKStages) & 1, ms, a)) return;
+        // GEMM2 (bf16, hi + lo): D''_T += X_T K
+        if (!issuer_wait(&ms->y_ready_t, gc & 1, ms, a)) return;
         tc_fence_after();
         {
-            const uint64_t kt = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 8192, 1024),
-                           kh = sdesc_sw128(sb + OFF_K16 + (gc % kKStages) * kTile, 8192, 1024);
+            const uint64_t kt = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 8192, 1024);
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) {
-                mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 8 * k, kh + 128 * k, ID_G2T, true);
-                mma_bf16_ts(tmem + TM_DS, tmem + TM_XS + 8 * k, kt + 128 * k, ID_G2S, true);
+                mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 16 * k, kt + 128 * k, ID_G2T, true);
+                mma_bf16_ts(tmem + TM_DT, tmem + TM_XT + 16 * k + 8, kt + 128 * k, ID_G2T, true);
             }
         }
-        mma_commit(&ms->d_ready);
-        mma_commit(&ms->emptyK[gc % kKStages]);
-        mma_commit(&ms->k16_empty[gc % kKStages]);
+        mma_commit(&ms->d_ready_t);
     }
 }
 
-// Warps 4-11: gram -> A^ -> M = (I + A^)^-1 -> its two operand forms, chunk
-// after chunk.
+// Warps 4-11: gram -> A^ -> M = (I + A^)^-1 -> its operand forms, chunk
+// after chunk (p: thread index among them).
 __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int p, int q,
                           int lane) {
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
@@ -837,7 +878,7 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         tc_fence_before();
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->g_read);
-        prep_solve(As, Ptmp, p);
+        prep_solve(As, Ptmp, p, 1);
         // the buffer's previous forms (chunk gc - 2) have been read (the buffer's phases are waited in order)
         if (!wg_all(1, gc < 2 || wait_bar(&ms->bt_free[gc & 1], ((gc >> 1) - 1) & 1, ms, a), kPrepThreads))
             return;
@@ -900,44 +941,72 @@ __device__ void publish_item(Misc* ms, const TcArgs& a, int k, int s, int lane) 
     if (lane == 0) mbar_arrive(&ms->slot_full[s]);  // (release: the slot is visible to the readers that wait on it)
 }
 
-// Warps 12-15: per chunk the renormalisation (if planned), the two passes,
-// and the next chunk's W operand; the epilogue at the end of an item.
-// Returns false once the CTA aborted.
+// Warps 12-15, per chunk: the renormalisation (if planned), the S and T
+// passes, then the next chunk's W operand (converted while GEMM2 of this chunk
+// runs; the buffers alternate); the epilogue at the end of an item.  Unless the
+// next chunk renormalises, its state is ready for GEMM1 once GEMM2 of this one
+// is done (its issuers wait for that themselves), so pre_done is signalled as
+// soon as the W operand is written.  Returns false once the CTA aborted.
+// (Converting the next W before the passes, to overlap GEMM1, measured slower:
+// the next W^T is then seldom ready and the passes wait for it.)
+__device__ void convert_next_w(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t ng, int q, int lane,
+                               bool& ok) {
+    // (the buffer was last read by GEMM1 of chunk ng - 1, whose completion the passes of that chunk waited for)
+    ok = wg_all(2, wait_bar(&ms->w_done, ng & 1, ms, a));
+    if (!ok) return;
+    tc_fence_after();
+    convert_w(smem, tmem, q, lane);
+    fence_async_smem();
+    tc_fence_before();
+    named_sync(2);
+    if (q == 0 && lane == 0) {
+        mbar_arrive(&ms->w_cvt[ng & 1]);
+        mbar_arrive(&ms->w_read);
+    }
+}
+
 __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, const ItemSlot& it, ItemSlot& next,
                            int k, int q, int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
     int E = 0;
     float sum_lc = 0.f;
+    bool ready = false;  // pre_done of the current chunk already signalled
     for (int c = 0; c < it.nc; ++c) {
         const uint32_t gc = it.g + c;
         const int slot = gc % kGateSlots;
         if (!wg_all(2, wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a))) return false;
         const ChunkPlan pl = ms->plan[slot];
         sum_lc = pl.sum_lc;
-        if (pl.rn && c > 0) {  // renormalise the state GEMM2 of the previous chunk left
-            if (!wg_all(2, wait_bar(&ms->d_ready, (gc - 1) & 1, ms, a))) return false;
-            tc_fence_after();
-            row_scale(tl + TM_DS, exp2f(fmaxf(pl.preS, -149.f)));
-            const float m = state_reduce_max(row_absmax(tl + TM_DT), ms->red, q, lane);
-            const int e = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
-            row_scale(tl + TM_DT, ldexpf(1.f, -e));
-            E += e;
+        if (!ready) {
+            if (pl.rn && c > 0) {  // renormalise the state GEMM2 of the previous chunk left
+                bool ok = wait_bar(&ms->d_ready_s, (gc - 1) & 1, ms, a);
+                ok = ok && wait_bar(&ms->d_ready_t, (gc - 1) & 1, ms, a);
+                if (!wg_all(2, ok)) return false;
+                tc_fence_after();
+                row_scale(tl + TM_DS, exp2f(fmaxf(pl.preS, -149.f)));
+                const float m = state_reduce_max(row_absmax(tl + TM_DT), ms->red, q, lane);
+                const int e = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
+                row_scale(tl + TM_DT, ldexpf(1.f, -e));
+                E += e;
+            }
+            tc_fence_before();
+            named_sync(2);
+            if (n == 0) mbar_arrive(&ms->pre_done);
         }
-        tc_fence_before();
-        named_sync(2);
-        if (n == 0) mbar_arrive(&ms->pre_done);
         if (!wg_all(2, wait_bar(&ms->x_done_s, gc & 1, ms, a))) return false;
         tc_fence_after();
         state_pass<false>(tl + TM_XS);
+        tc_fence_before();
+        named_sync(2);
+        if (n == 0) mbar_arrive(&ms->y_ready_s);
         if (!wg_all(2, wait_bar(&ms->x_done_t, gc & 1, ms, a))) return false;
         tc_fence_after();
         state_pass<true>(tl + TM_XT);
         tc_fence_before();
         named_sync(2);
-        if (n == 0) mbar_arrive(&ms->y_ready);
-        // The W operand of the next chunk (GEMM1 of this one is done with the buffer): the next chunk of
-        // this item, or the first of the next item.
+        if (n == 0) mbar_arrive(&ms->y_ready_t);
+        // The W operand of the next chunk: the next chunk of this item, or the first of the next item.
         uint32_t ng = gc + 1;
         bool has_next = c + 1 < it.nc;
         if (!has_next) {
@@ -950,19 +1019,25 @@ __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
             ng = next.g;
         }
         if (has_next) {
-            if (!wg_all(2, wait_bar(&ms->w_done, ng & 1, ms, a))) return false;
-            tc_fence_after();
-            convert_w(smem, tmem, q, lane);
-            fence_async_smem();
-            tc_fence_before();
-            named_sync(2);
-            if (n == 0) {
-                mbar_arrive(&ms->w_cvt);
-                mbar_arrive(&ms->w_read);
+            bool ok;
+            convert_next_w(ms, smem, a, tmem, ng, q, lane, ok);
+            if (!ok) return false;
+        }
+        ready = false;
+        if (c + 1 < it.nc) {  // the next chunk of this item: ready at once unless it renormalises
+            const uint32_t g1 = gc + 1;
+            const int s1 = g1 % kGateSlots;
+            if (!wg_all(2, wait_bar(&ms->gready[s1], (g1 / kGateSlots) & 1, ms, a))) return false;
+            if (!ms->plan[s1].rn) {
+                if (n == 0) mbar_arrive(&ms->pre_done);
+                ready = true;
             }
         }
     }
-    if (!wg_all(2, wait_bar(&ms->d_ready, (it.g + it.nc - 1) & 1, ms, a))) return false;
+    const uint32_t last = it.g + it.nc - 1;
+    bool ok = wait_bar(&ms->d_ready_s, last & 1, ms, a);
+    ok = ok && wait_bar(&ms->d_ready_t, last & 1, ms, a);
+    if (!wg_all(2, ok)) return false;
     tc_fence_after();
     state_epilogue(ms, a, it.obj, (float)E + sum_lc, tmem, q, lane);
     state_init(tmem, q, lane);  // (I, 0) for the next item
@@ -984,17 +1059,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&ms->fullK[s], 1);
             mbar_init(&ms->emptyK[s], 1);
-            mbar_init(&ms->k16_full[s], 1);
-            mbar_init(&ms->k16_empty[s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&ms->fullV[s], 1);
             mbar_init(&ms->emptyV[s], 1);
         }
-        // gready .. drain are consecutive in Misc: one arrival each, but bt_free (both issuers read the M
-        // forms) and drain (both issuers' MMAs) take two
+        // gready .. drain are consecutive in Misc: one arrival each, but bt_free (two issuers read the M
+        // forms) takes two and drain (every issuer's MMAs) three
         for (uint64_t* b = &ms->gready[0]; b <= &ms->drain; ++b)
-            mbar_init(b, b == &ms->bt_free[0] || b == &ms->bt_free[1] || b == &ms->drain ? 2 : 1);
+            mbar_init(b, b == &ms->bt_free[0] || b == &ms->bt_free[1] ? 2 : b == &ms->drain ? 3 : 1);
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(&ms->slot_full[s], 1);
             mbar_init(&ms->slot_read[s], kSlotReaders);
@@ -1027,20 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             it = ms->slots[0];
             named_sync(2);
             if (tid == 32 * kWarpState0) mbar_arrive(&ms->slot_read[0]);
-            if (it.nc > 0) {
-                ok = wg_all(2, wait_bar(&ms->w_done, it.g & 1, ms, a));
-                if (ok) {
-                    tc_fence_after();
-                    convert_w(smem, tmem, q, lane);
-                    fence_async_smem();
-                    tc_fence_before();
-                    named_sync(2);
-                    if (tid == 32 * kWarpState0) {
-                        mbar_arrive(&ms->w_cvt);
-                        mbar_arrive(&ms->w_read);
-                    }
-                }
-            }
+            if (it.nc > 0) convert_next_w(ms, smem, a, tmem, it.g, q, lane, ok);
         }
         for (int k = 0; ok && it.nc > 0; ++k) {
             if (!state_item(ms, smem, a, tmem, it, next, k, q, lane)) break;
@@ -1060,12 +1120,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 publish_item(ms, a, k, s, lane);
                 __syncwarp();
                 it = ms->slots[s];
-            } else if (warp == kWarpCvt) {
-                const bool ok = wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a);
-                if (!__all_sync(0xffffffffu, ok)) break;
-                it = ms->slots[s];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ms->slot_read[s]);
             } else if (is_prep) {
                 const bool ok = wait_bar(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a);
                 if (!wg_all(1, ok, kPrepThreads)) break;
@@ -1084,9 +1138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (warp == kWarpIssP) {
                 issue_prep_role(ms, smem, a, tmem, it.g, it.nc);
             } else if (warp == kWarpIssS) {
-                issue_state_role(ms, smem, a, tmem, it.g, it.nc);
-            } else if (warp == kWarpCvt) {
-                convert_role(ms, smem, a, it.g, it.nc, lane);
+                issue_s_role(ms, smem, a, tmem, it.g, it.nc);
+            } else if (warp == kWarpIssT) {
+                issue_t_role(ms, smem, a, tmem, it.g, it.nc);
             } else {
                 prep_role(ms, smem, a, tmem, it.g, it.nc, tid - 32 * kWarpPrep0, q, lane);
             }
@@ -1096,10 +1150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // Drain: every MMA this CTA issued (from both issuers) has completed before tensor memory is freed.  A
+    // Drain: every MMA this CTA issued (from every issuer) has completed before tensor memory is freed.  A
     // drain that runs out of polls is reported (the result is then not to be trusted); the memory is freed
     // all the same, since the kernel is about to exit either way.
-    if (warp == kWarpIssP || warp == kWarpIssS) {
+    if (warp == kWarpIssP || warp == kWarpIssS || warp == kWarpIssT) {
         if (lane == 0) {
             mma_commit(&ms->drain);
             uint32_t i = 0;

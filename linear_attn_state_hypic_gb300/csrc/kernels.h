@@ -66,6 +66,12 @@ cudaError_t launch_build_simt(const BuildParams& p, const void* workspace, unsig
 cudaError_t launch_gdn_build_tc(const BuildParams& p, void* workspace, unsigned* err, cudaStream_t s);
 bool gdn_build_tc_supported(const BuildParams& p);
 
+// The decay families (RetNet, Mamba2, GLA, vanilla) on the tensor cores (d =
+// 128, bf16 k/v): the closed form S = sum_t Diag(w_t) k_t v_t^T as a
+// contraction.  Returns cudaErrorNotSupported when the shape is not covered.
+cudaError_t launch_decay_build_tc(const BuildParams& p, void* workspace, unsigned* err, cudaStream_t s);
+bool decay_build_tc_supported(const BuildParams& p);
+
 cudaError_t launch_compose(const ComposeParams& p, unsigned* err, cudaStream_t s);
 cudaError_t launch_seam(const SeamParams& p, unsigned* err, cudaStream_t s);
 
