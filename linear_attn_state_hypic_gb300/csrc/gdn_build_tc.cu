@@ -110,7 +110,7 @@ struct ChunkPlan {
 };
 
 struct Misc {
-    uint64_t fullK[kKStages], emptyK[kKStages];
+    uint64_t fullK[kKStages], emptyK[kKStages];  // emptyK: one commit from each half's issuer after its GEMM2
     uint64_t fullV[kVStages], emptyV[kVStages];
     uint64_t gready[kGateSlots];  // producer -> prep, state: gate tables and plan of a chunk written
     uint64_t g_done, g_read;        // gram committed; gram read by the prep warps
@@ -311,7 +311,7 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const TcArgs& a, const CU
             tma_load_3d(kt + 8192, tmk, &ms->fullK[s], 64, head, z);
         }
         // The slot of chunk gc was last read for chunk gc - 4: by the prep before its M forms, by the
-        // state warps at the start of that chunk, both before GEMM2 of chunk gc - 3 (waited above).
+        // state warps at the start of that chunk, both before GEMM2 of chunk gc - 4 (waited above).
         gate_tables(ms, gc % kGateSlots, ra, rb, c + 1 == nc, st, lane);
         if (c + 1 < nc) gate_load(a, layer, head, b0 + (int64_t)(c + 1) * kC, b1, lane, ra, rb);
         __syncwarp();
@@ -857,6 +857,7 @@ __device__ void issue_t_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t 
             }
         }
         mma_commit(&ms->d_ready_t);
+        mma_commit(&ms->emptyK[gc % kKStages]);
     }
 }
 
@@ -1058,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&ms->fullK[s], 1);
-            mbar_init(&ms->emptyK[s], 1);
+            mbar_init(&ms->emptyK[s], 2);  // GEMM2 of both halves read the key tile
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&ms->fullV[s], 1);
