@@ -13,7 +13,8 @@
 // How: the closed form as a contraction.  Chunks of 64 tokens are taken from
 // the segment's end backwards, so that the weight of a token is its in-chunk
 // suffix decay times the running decay of the chunks already taken (a scan of
-// log2 decays, per feature for GLA); no accumulator is ever rescaled.  The
+// log2 decays for the scalar families, suffix products of the gates per
+// feature for GLA); no accumulator is ever rescaled.  The
 // weighted keys K~ = Diag(w) K are formed in shared memory as a pair of bf16
 // values (hi + lo, about 16 significant bits) and S^T += V^T K~ runs as bf16
 // MMAs (M = N = 128, K = 64 per chunk) into a tensor-memory accumulator; the
@@ -22,10 +23,11 @@
 // (1 KB with GLA's per-feature gates): the kernel is bound by HBM, not by the
 // tensor pipe.
 //
-// Roles (192 threads): warp 0 takes items from the queue and loads keys,
-// values (and GLA gates) by TMA into a ring; warps 1-4 scan the gates, form
-// K~ and write the result; warp 5 issues the MMAs (one thread), so that the
-// workers never wait on MMA issue.  One CTA per SM,
+// Roles (320 threads): warp 0 takes items from the queue and loads keys,
+// values (and GLA gates) by TMA into a ring; warps 1-8 form the weights and
+// K~ and write the result (eight warps, so that the latency of one chunk's
+// shared-memory traffic is hidden); warp 9 issues the MMAs (one thread), so
+// that the workers never wait on MMA issue.  One CTA per SM,
 // persistent over (segment, layer, head) items in longest-body-first order;
 // every wait is bounded and a wait that runs out sets the device error word.
 #include <cuda.h>
@@ -49,14 +51,18 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 128, kC = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kWorkers = 256;   // warps 1-8
+constexpr int kWarpMma = 9;
 constexpr uint32_t kTile = 16384;   // 64 tokens x 128 bf16: two 64-column TMA boxes, 128-byte swizzle
 constexpr uint32_t kGTile = 32768;  // 64 tokens x 128 fp32 gates: four 32-column boxes, unswizzled
 constexpr int kItemSlots = 2;
+constexpr int kMaxStages = 5;
 
 template <bool kGla>
 struct Layout {
-    static constexpr int kStages = kGla ? 2 : 3;
+    static constexpr int kStages = kGla ? 2 : 4;
+    static_assert(kStages <= kMaxStages, "stage barriers");
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + kStages * kTile;
     static constexpr uint32_t OFF_KT = OFF_V + kStages * kTile;      // K~ hi, then lo: two buffers
@@ -71,13 +77,14 @@ struct DecSlot {
 };
 
 struct DecMisc {
-    uint64_t full[3], done[3];          // stage landed; the MMAs that read the stage (and its K~) finished
+    uint64_t full[kMaxStages], done[kMaxStages];  // stage landed; the MMAs that read it (and its K~) finished
     uint64_t kt_ready[2];               // K~ buffer j % 2 formed for chunk j (workers -> MMA warp)
     uint64_t acc_free;                  // the epilogue has read the accumulator (workers -> MMA warp)
     uint64_t drain;
     uint64_t slot_full[kItemSlots], slot_read[kItemSlots];
     DecSlot slots[kItemSlots];
     alignas(16) float w[kC];            // scalar families: the weights of the current chunk
+    alignas(16) float gprod[2][kD];     // GLA: the gate product of each half chunk, per feature
     int abort_flag;
     uint32_t tmem_base;
 };
@@ -119,11 +126,11 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, DecMisc
     if (mbar_try_wait(bar, parity)) return true;
     return dec_wait_slow(bar, parity, &ms->abort_flag, a.wait_ns, a.err);
 }
-__device__ __forceinline__ void wsync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void wsync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ bool wall(bool v) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
         : "r"((uint32_t)v)
         : "memory");
@@ -200,9 +207,9 @@ __device__ void dec_producer(DecMisc* ms, uint8_t* smem, const DecArgs& a, const
 // t.  wt(t, i0, f[8]) fills the eight weights.
 template <typename WF>
 __device__ __forceinline__ void form_kt(const uint8_t* ktile, uint8_t* hi, uint8_t* lo, int w, WF wt) {
-#pragma unroll 2
-    for (int m = 0; m < 8; ++m) {
-        const int q = w + 128 * m, t = q >> 4, cc = q & 15;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int q = w + kWorkers * m, t = q >> 4, cc = q & 15;
         const uint32_t off = (cc >> 3) * 8192 + t * 128 + ((((uint32_t)cc & 7) ^ (t & 7)) << 4);
         const uint4 x = *reinterpret_cast<const uint4*>(ktile + off);
         float f[8];
@@ -226,14 +233,18 @@ __device__ __forceinline__ void form_kt(const uint8_t* ktile, uint8_t* hi, uint8
 
 constexpr uint32_t kIdesc = idesc(1, 128, 128, true, true);  // S^T += V^T K~: both operands MN-major
 
-// Warps 1-4 (w = 0..127).  The accumulator holds S^T: its lane n is column n
-// of S.  Log2 decays are summed in float within a chunk and across chunks in
-// double (the running decay of the chunks already taken); T is 2 to the total.
+// Warps 1-8 (w = 0..255).  The accumulator holds S^T: its lane n is column n
+// of S.  The scalar families sum log2 decays in float within a chunk and
+// across chunks in double (the running decay of the chunks already taken); T
+// is 2 to the total.  GLA multiplies: thread w takes feature w % 128 over half
+// w / 128 of the chunk's tokens, the weights are suffix products of the gates
+// in fp32 (the two halves joined through shared memory) times the running
+// product of the chunks already taken, kept in double; T is that product.
 template <bool kGla>
 __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32_t tmem, int w) {
     using Ly = Layout<kGla>;
     const int fam = a.family;
-    const int tq = (1 + (w >> 5)) & 3;  // warps 1, 2, 3, 4 access tensor-memory lane quarters 1, 2, 3, 0
+    const int tq = (1 + (w >> 5)) & 3;  // warps 1..8 access tensor-memory lane quarters 1, 2, 3, 0, 1, 2, 3, 0
     for (int k = 0;; ++k) {
         const int s = k % kItemSlots;
         if (!wall(dec_wait(&ms->slot_full[s], (k / kItemSlots) & 1, ms, a))) return;
@@ -242,7 +253,8 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
         if (w == 0) mbar_arrive(&ms->slot_read[s]);
         if (it.nc < 0) return;
         const float lg = fam == kRETNET ? log2f(fmaxf(a.gamma[(int64_t)it.layer * a.n_heads + it.head], FLT_MIN)) : 0.f;
-        double racc = 0.0;  // log2 decay of the chunks taken so far (feature w for GLA; all threads alike otherwise)
+        double racc = 0.0;   // scalar families: log2 decay of the chunks taken so far
+        double rprod = 1.0;  // GLA: the decay of feature w % 128 over the chunks taken so far
         float apre[2] = {1.f, 1.f};  // Mamba2: the gates of the next chunk to take (prefetched one chunk ahead)
         if (fam == kMAMBA2 && w < 32) {
             const int c0 = it.nc - 1;
@@ -264,21 +276,26 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
             uint8_t* hi = smem + Ly::OFF_KT + (j & 1) * 2 * kTile;
             uint8_t* lo = hi + kTile;
             if (fam == kGLA) {
-                // feature w: exclusive suffix sums of log2 g over the chunk, after the chunks already taken;
-                // the gate tile (box w / 32 holds [64 t][32 features]) is rewritten in place with the weights
+                // feature f, tokens [32 hf, 32 hf + 32): the gate tile (box f / 32 holds [64 t][32 features])
+                // is rewritten in place with the weights
                 float* gt = reinterpret_cast<float*>(smem + Ly::OFF_G + st * kGTile);
-                float* col = gt + (w >> 5) * 2048 + (w & 31);
-                float l2[kC];
-#pragma unroll
-                for (int t = 0; t < kC; ++t) l2[t] = t < nvalid ? log2f(fmaxf(col[t * 32], FLT_MIN)) : 0.f;
-                const float base = (float)racc;
-                float acc = 0.f;
-#pragma unroll
-                for (int t = kC - 1; t >= 0; --t) {
-                    col[t * 32] = t < nvalid ? exp2f(fmaxf(base + acc, -149.f)) : 0.f;
-                    acc += l2[t];
+                const int f = w & (kD - 1), hf = w >> 7;
+                float* col = gt + (f >> 5) * 2048 + (f & 31);
+                float ph = 1.f;
+#pragma unroll 8
+                for (int t = 32 * hf; t < 32 * hf + 32; ++t)
+                    if (t < nvalid) ph *= col[t * 32];
+                ms->gprod[hf][f] = ph;
+                wsync();
+                const float p0 = ms->gprod[0][f], p1 = ms->gprod[1][f];
+                float suf = (float)rprod * (hf == 0 ? p1 : 1.f);
+#pragma unroll 8
+                for (int t = 32 * hf + 31; t >= 32 * hf; --t) {
+                    const float g = col[t * 32];
+                    col[t * 32] = t < nvalid ? suf : 0.f;
+                    if (t < nvalid) suf *= g;
                 }
-                racc += (double)acc;
+                rprod *= (double)p0 * (double)p1;
                 wsync();
                 form_kt(ktile, hi, lo, w, [&](int t, int i0, float (&f)[8]) {
                     const float* src = gt + (i0 >> 5) * 2048 + t * 32 + (i0 & 31);
@@ -329,7 +346,7 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
             } else if (nvalid < kC) {
                 // vanilla: the MMA reads the key tile itself, so the rows past the body end are cleared
                 uint8_t* kw = smem + Ly::OFF_K + st * kTile;
-                for (int e = w; e < (kC - nvalid) * 16; e += 128) {
+                for (int e = w; e < (kC - nvalid) * 16; e += kWorkers) {
                     const int t = nvalid + e / 16, cc = e % 16;
                     const uint32_t off = (cc >> 3) * 8192 + t * 128 + ((((uint32_t)cc & 7) ^ (t & 7)) << 4);
                     *reinterpret_cast<uint4*>(kw + off) = make_uint4(0u, 0u, 0u, 0u);
@@ -343,18 +360,18 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
         const uint32_t jl = it.j0 + it.nc - 1;
         if (!wall(dec_wait(&ms->done[jl % Ly::kStages], (jl / Ly::kStages) & 1, ms, a))) return;
         tc_fence_after();
-        const int n = 32 * tq + (w & 31);
+        const int n = 32 * tq + (w & 31), ch = w >> 7;  // warps 1-4 write rows 0-63 of S, warps 5-8 the rest
         float* S = a.S_out + it.obj * kD * kD;
         const uint32_t tl = tmem + ((32u * tq) << 16);
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 2 * ch; cb < 2 * ch + 2; ++cb) {
             uint32_t x[32];
             tmem_ld32(tl + 32 * cb, x);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) S[(32 * cb + e) * kD + n] = __uint_as_float(x[e]);
         }
-        if (fam == kGLA) a.T_out[it.obj * kD + w] = (float)exp2(fmax(racc, -1100.0));
+        if (fam == kGLA && w < kD) a.T_out[it.obj * kD + w] = (float)rprod;
         if (fam == kRETNET && w == 0)
             a.T_out[it.obj] = (float)pow((double)a.gamma[(int64_t)it.layer * a.n_heads + it.head], (double)(it.b1 - it.b0));
         if (fam == kMAMBA2 && w == 0) a.T_out[it.obj] = (float)exp2(fmax(racc, -1100.0));
@@ -364,7 +381,7 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
     }
 }
 
-// Warp 5, one thread: per chunk, once its K~ is formed (or, for vanilla, its
+// Warp 9, one thread: per chunk, once its K~ is formed (or, for vanilla, its
 // tile has landed and been masked), S^T += V^T K~ (A = the value tile, B = K~,
 // both MN-major); the first MMA of an item overwrites the accumulator once the
 // previous item's epilogue has read it.  Items come from the same slot ring.
@@ -442,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = ms->tmem_base;
     if (warp == 0)
         dec_producer<kGla>(ms, smem, a, &tk, &tv, &tg, lane);
-    else if (warp == 5) {
+    else if (warp == kWarpMma) {
         if (lane == 0) dec_mma<kGla>(ms, smem, a, tmem);
     } else
         dec_workers<kGla>(ms, smem, a, tmem, tid - 32);
@@ -451,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // Drain: every MMA this CTA issued has completed before tensor memory is freed (after an abort some
     // may still run).  A drain that runs out of polls is reported; the memory is freed all the same.
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         if (lane == 0) {
             mma_commit(&ms->drain);
             uint32_t i = 0;
