@@ -83,7 +83,6 @@ struct DecMisc {
     uint64_t drain;
     uint64_t slot_full[kItemSlots], slot_read[kItemSlots];
     DecSlot slots[kItemSlots];
-    alignas(16) float w[kC];            // scalar families: the weights of the current chunk
     alignas(16) float gprod[2][kD];     // GLA: the gate product of each half chunk, per feature
     int abort_flag;
     uint32_t tmem_base;
@@ -204,7 +203,7 @@ __device__ void dec_producer(DecMisc* ms, uint8_t* smem, const DecArgs& a, const
 
 // Weighted keys of one chunk, K~ = hi + lo (bf16 pair, same swizzled layout as
 // the key tile): 16-byte chunk q of the tile holds features i0..i0+7 of token
-// t.  wt(t, i0, f[8]) fills the eight weights.
+// t.  wt(m, t, i0, f[8]) fills the eight weights of the thread's m-th piece.
 template <typename WF>
 __device__ __forceinline__ void form_kt(const uint8_t* ktile, uint8_t* hi, uint8_t* lo, int w, WF wt) {
 #pragma unroll
@@ -213,7 +212,7 @@ __device__ __forceinline__ void form_kt(const uint8_t* ktile, uint8_t* hi, uint8
         const uint32_t off = (cc >> 3) * 8192 + t * 128 + ((((uint32_t)cc & 7) ^ (t & 7)) << 4);
         const uint4 x = *reinterpret_cast<const uint4*>(ktile + off);
         float f[8];
-        wt(t, 64 * (cc >> 3) + 8 * (cc & 7), f);
+        wt(m, t, 64 * (cc >> 3) + 8 * (cc & 7), f);
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
         uint32_t h[4], l[4];
 #pragma unroll
@@ -234,12 +233,12 @@ __device__ __forceinline__ void form_kt(const uint8_t* ktile, uint8_t* hi, uint8
 constexpr uint32_t kIdesc = idesc(1, 128, 128, true, true);  // S^T += V^T K~: both operands MN-major
 
 // Warps 1-8 (w = 0..255).  The accumulator holds S^T: its lane n is column n
-// of S.  The scalar families sum log2 decays in float within a chunk and
-// across chunks in double (the running decay of the chunks already taken); T
-// is 2 to the total.  GLA multiplies: thread w takes feature w % 128 over half
-// w / 128 of the chunk's tokens, the weights are suffix products of the gates
-// in fp32 (the two halves joined through shared memory) times the running
-// product of the chunks already taken, kept in double; T is that product.
+// of S.  RetNet's weights are a closed form.  Mamba2 and GLA multiply: a
+// token's weight is the suffix product of the gates after it in its chunk, in
+// fp32, times the product over the chunks already taken, kept in double; T is
+// that product at the end.  Mamba2: a shuffle scan over the 64 tokens (two a
+// lane) in every warp.  GLA: thread w takes feature w % 128 over half w / 128
+// of the chunk's tokens, the halves joined through shared memory.
 template <bool kGla>
 __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32_t tmem, int w) {
     using Ly = Layout<kGla>;
@@ -253,15 +252,22 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
         if (w == 0) mbar_arrive(&ms->slot_read[s]);
         if (it.nc < 0) return;
         const float lg = fam == kRETNET ? log2f(fmaxf(a.gamma[(int64_t)it.layer * a.n_heads + it.head], FLT_MIN)) : 0.f;
-        double racc = 0.0;   // scalar families: log2 decay of the chunks taken so far
-        double rprod = 1.0;  // GLA: the decay of feature w % 128 over the chunks taken so far
-        float apre[2] = {1.f, 1.f};  // Mamba2: the gates of the next chunk to take (prefetched one chunk ahead)
-        if (fam == kMAMBA2 && w < 32) {
-            const int c0 = it.nc - 1;
-            const int64_t t0 = it.b0 + (int64_t)c0 * kC;
-            for (int e = 0; e < 2; ++e)
-                if (t0 + 2 * w + e < it.b1)
-                    apre[e] = a.alpha[tok_row(it.layer, t0 + 2 * w + e, it.head, a.n_tokens, a.n_heads)];
+        // The decay over the chunks taken so far: of feature w % 128 (GLA) or of the head (Mamba2).
+        double rprod = 1.0;
+        // Mamba2: the gates of tokens 2 lane + {0, 1} of the chunk taken now (acur) and of the one taken next
+        // (an1); each chunk's are loaded two chunks before it is taken, and every warp scans them itself.
+        // Tokens past the body end read as 1.
+        float acur[2] = {1.f, 1.f}, an1[2] = {1.f, 1.f};
+        auto load_gates = [&](int cc, float (&g)[2]) {
+            const int64_t tc = it.b0 + (int64_t)cc * kC;
+            for (int e = 0; e < 2; ++e) {
+                const int64_t t = tc + 2 * (w & 31) + e;
+                g[e] = t < it.b1 ? a.alpha[tok_row(it.layer, t, it.head, a.n_tokens, a.n_heads)] : 1.f;
+            }
+        };
+        if (fam == kMAMBA2) {
+            load_gates(it.nc - 1, acur);
+            if (it.nc >= 2) load_gates(it.nc - 2, an1);
         }
         for (int jj = 0; jj < it.nc; ++jj) {
             const uint32_t j = it.j0 + jj, st = j % Ly::kStages, u = j / Ly::kStages;
@@ -271,7 +277,7 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
             bool ok = dec_wait(&ms->full[st], u & 1, ms, a);
             // K~ buffer j % 2 was last read by the MMAs of chunk j - 2
             ok = ok && (j < 2 || dec_wait(&ms->done[(j - 2) % Ly::kStages], ((j - 2) / Ly::kStages) & 1, ms, a));
-            if (!wall(ok)) return;
+            if (kGla ? !wall(ok) : !__all_sync(0xffffffffu, ok)) return;
             const uint8_t* ktile = smem + Ly::OFF_K + st * kTile;
             uint8_t* hi = smem + Ly::OFF_KT + (j & 1) * 2 * kTile;
             uint8_t* lo = hi + kTile;
@@ -297,7 +303,7 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
                 }
                 rprod *= (double)p0 * (double)p1;
                 wsync();
-                form_kt(ktile, hi, lo, w, [&](int t, int i0, float (&f)[8]) {
+                form_kt(ktile, hi, lo, w, [&](int, int t, int i0, float (&f)[8]) {
                     const float* src = gt + (i0 >> 5) * 2048 + t * 32 + (i0 & 31);
                     const float4 x0 = *reinterpret_cast<const float4*>(src);
                     const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
@@ -305,43 +311,42 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
                     f[4] = x1.x, f[5] = x1.y, f[6] = x1.z, f[7] = x1.w;
                 });
             } else if (fam != kVANILLA) {
-                if (w < 32) {  // the chunk's scalar weights (one warp, two tokens a lane)
-                    float l2[2], wt[2];
+                // The scalar weights of the tokens this thread's 16-byte pieces belong to (t = (w + 256 m) / 16,
+                // m = 0..3), formed by each warp itself: no barrier between the warps.
+                const int lane = w & 31;
+                float wm[4];
+                if (fam == kRETNET) {  // gamma to the number of body tokens after t (closed form)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 2 * w + e;
-                        l2[e] = (t < nvalid && fam == kMAMBA2) ? log2f(fmaxf(apre[e], FLT_MIN)) : 0.f;
+                    for (int m = 0; m < 4; ++m) {
+                        const int t = (w + kWorkers * m) >> 4;
+                        wm[m] = t < nvalid ? exp2f(fmaxf(lg * (float)(it.b1 - 1 - (t0 + t)), -149.f)) : 0.f;
                     }
-                    if (fam == kMAMBA2 && c > 0) {  // prefetch the gates of the chunk taken next (the previous one)
-                        const int64_t tn = it.b0 + (int64_t)(c - 1) * kC;
-                        for (int e = 0; e < 2; ++e)
-                            apre[e] = a.alpha[tok_row(it.layer, tn + 2 * w + e, it.head, a.n_tokens, a.n_heads)];
-                    }
-                    // exclusive suffix sum within the chunk (the tokens after t), by a shuffle scan over lanes
-                    float suf = l2[0] + l2[1];
+                } else {  // Mamba2: exclusive suffix products of a over the chunk, a shuffle scan in every warp
+                    const float a0 = acur[0], a1 = acur[1];
+                    acur[0] = an1[0], acur[1] = an1[1];
+                    if (c >= 2) load_gates(c - 2, an1);  // (the chunk taken two after this one)
+                    float suf = a0 * a1;  // inclusive suffix product over lanes >= lane
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const float y = __shfl_down_sync(0xffffffffu, suf, off);
-                        if (w + off < 32) suf += y;
+                        if (lane + off < 32) suf *= y;
                     }
                     const float after = __shfl_down_sync(0xffffffffu, suf, 1);
-                    const float e1 = (float)racc + (w < 31 ? after : 0.f), e0 = e1 + l2[1];
-                    if (fam == kRETNET) {  // gamma to the number of body tokens after t (closed form)
-                        wt[0] = exp2f(fmaxf(lg * (float)(it.b1 - 1 - (t0 + 2 * w)), -149.f));
-                        wt[1] = exp2f(fmaxf(lg * (float)(it.b1 - 2 - (t0 + 2 * w)), -149.f));
-                    } else {
-                        wt[0] = exp2f(fmaxf(e0, -149.f));
-                        wt[1] = exp2f(fmaxf(e1, -149.f));
-                    }
-                    ms->w[2 * w] = 2 * w < nvalid ? wt[0] : 0.f;
-                    ms->w[2 * w + 1] = 2 * w + 1 < nvalid ? wt[1] : 0.f;
-                    racc += (double)__shfl_sync(0xffffffffu, suf, 0);
-                }
-                wsync();
-                form_kt(ktile, hi, lo, w, [&](int t, int, float (&f)[8]) {
-                    const float x = ms->w[t];
+                    const float w1 = (float)rprod * (lane < 31 ? after : 1.f);  // token 2 lane + 1
+                    const float wt0 = 2 * lane < nvalid ? w1 * a1 : 0.f;
+                    const float wt1 = 2 * lane + 1 < nvalid ? w1 : 0.f;
+                    rprod *= (double)__shfl_sync(0xffffffffu, suf, 0);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = x;
+                    for (int m = 0; m < 4; ++m) {
+                        const int t = (w + kWorkers * m) >> 4;
+                        const float x0 = __shfl_sync(0xffffffffu, wt0, t >> 1);
+                        const float x1 = __shfl_sync(0xffffffffu, wt1, t >> 1);
+                        wm[m] = (t & 1) ? x1 : x0;
+                    }
+                }
+                form_kt(ktile, hi, lo, w, [&](int m, int, int, float (&f)[8]) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = wm[m];
                 });
             } else if (nvalid < kC) {
                 // vanilla: the MMA reads the key tile itself, so the rows past the body end are cleared
@@ -353,8 +358,8 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
                 }
             }
             fence_async_smem();
-            wsync();
-            if (w == 0) mbar_arrive(&ms->kt_ready[j & 1]);
+            __syncwarp();
+            if ((w & 31) == 0) mbar_arrive(&ms->kt_ready[j & 1]);  // one arrival per worker warp
         }
         // epilogue: thread n writes column n of S (coalesced across the warp), and T
         const uint32_t jl = it.j0 + it.nc - 1;
@@ -374,7 +379,7 @@ __device__ void dec_workers(DecMisc* ms, uint8_t* smem, const DecArgs& a, uint32
         if (fam == kGLA && w < kD) a.T_out[it.obj * kD + w] = (float)rprod;
         if (fam == kRETNET && w == 0)
             a.T_out[it.obj] = (float)pow((double)a.gamma[(int64_t)it.layer * a.n_heads + it.head], (double)(it.b1 - it.b0));
-        if (fam == kMAMBA2 && w == 0) a.T_out[it.obj] = (float)exp2(fmax(racc, -1100.0));
+        if (fam == kMAMBA2 && w == 0) a.T_out[it.obj] = (float)rprod;
         tc_fence_before();
         wsync();  // every lane has read the accumulator before the next item's first MMA overwrites it
         if (w == 0) mbar_arrive(&ms->acc_free);
@@ -440,8 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ms->slot_full[s], 1);
             mbar_init(&ms->slot_read[s], 2);  // the workers and the MMA warp
         }
-        mbar_init(&ms->kt_ready[0], 1);
-        mbar_init(&ms->kt_ready[1], 1);
+        mbar_init(&ms->kt_ready[0], kWorkers / 32);
+        mbar_init(&ms->kt_ready[1], kWorkers / 32);
         mbar_init(&ms->acc_free, 1);
         mbar_init(&ms->drain, 1);
         ms->abort_flag = 0;
