@@ -725,9 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kWarpMMA) {
         if (lane == 0) {
+            // every MMA has completed before tensor memory is freed; a drain that runs out of polls is
+            // reported (the result is then not to be trusted) and the memory freed all the same
             mma_commit(&ms->drain);
-            for (uint32_t i = 0; i < a.wait_limit && !mbar_try_wait(&ms->drain, 0); ++i) {
-            }
+            uint32_t i = 0;
+            while (i < a.wait_limit && !mbar_try_wait(&ms->drain, 0)) ++i;
+            if (i >= a.wait_limit) set_error(a.err, kErrTimeout);
         }
         __syncwarp();
     }
