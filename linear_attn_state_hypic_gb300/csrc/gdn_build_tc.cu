@@ -361,57 +361,50 @@ __device__ void prep_arows(const Misc* ms, float* As, int slot, uint32_t tmem, i
     }
 }
 
-// Warp-level block products for the solve (mma.sync m16n8k16, bf16 with
-// fp32 accumulation).  Each fp32 operand is carried as a pair of bf16 values
-// (x = hi + lo, lo the rounding residual of hi) and a product as
-// hi*hi + hi*lo + lo*hi, which keeps about 16 bits of every operand: the
-// solve then matches an fp32 one to ~3e-6 relative.
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// Warp-level block products for the solve (mma.sync m16n8k8 on tf32
+// operands with fp32 accumulation: the tensor cores read the fp32 values'
+// upper 19 bits).  M is only needed to about tf32 precision -- the W^ it
+// forms is rounded to tf32 for GEMM1 -- and products of truncated operands
+// leave T_C and S where products to ~16 bits put them.
+__device__ __forceinline__ void mma1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // C (16 x 8NT) = A (16 x 16KS, row stride lda) B (16KS x 8NT, row stride
-// ldb), one warp; lane (g, t) = (lane / 4, lane % 4) holds rows g, g + 8 and
-// columns 2t, 2t + 1 of each 8-column tile (the m16n8k16 layouts).
+// ldb), one warp; lane (g, t) = (lane / 4, lane % 4) holds A[g][t], A[g+8][t],
+// A[g][t+4], A[g+8][t+4] and B[t][g], B[t+4][g] of each 8-wide k step, and
+// rows g, g + 8, columns 2t, 2t + 1 of each 8-column tile of C.  Two
+// accumulator sets alternate over the k steps (no chain through one).
 template <int KS, int NT>
 __device__ __forceinline__ void warp_gemm(float (&c)[NT][4], const float* A, int lda, const float* B, int ldb,
                                           int lane) {
     const int g = lane >> 2, t = lane & 3;
-    float c1[NT][4], c2[NT][4];
+    float c1[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c[nt][e] = c1[nt][e] = c2[nt][e] = 0.f;
+        for (int e = 0; e < 4; ++e) c[nt][e] = c1[nt][e] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-        uint32_t ah[4], al[4];
-        const float* a0 = A + g * lda + 16 * ks + 2 * t;
-        const float2 x0 = *reinterpret_cast<const float2*>(a0);
-        const float2 x1 = *reinterpret_cast<const float2*>(a0 + 8 * lda);
-        const float2 x2 = *reinterpret_cast<const float2*>(a0 + 8);
-        const float2 x3 = *reinterpret_cast<const float2*>(a0 + 8 * lda + 8);
-        split_bf16(x0.x, x0.y, ah[0], al[0]);
-        split_bf16(x1.x, x1.y, ah[1], al[1]);
-        split_bf16(x2.x, x2.y, ah[2], al[2]);
-        split_bf16(x3.x, x3.y, ah[3], al[3]);
+    for (int ks = 0; ks < 2 * KS; ++ks) {
+        const float* a0 = A + g * lda + 8 * ks + t;
+        const uint32_t x0 = __float_as_uint(a0[0]), x1 = __float_as_uint(a0[8 * lda]);
+        const uint32_t x2 = __float_as_uint(a0[4]), x3 = __float_as_uint(a0[8 * lda + 4]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const float* b = B + (16 * ks + 2 * t) * ldb + 8 * nt + g;
-            uint32_t bh0, bl0, bh1, bl1;
-            split_bf16(b[0], b[ldb], bh0, bl0);
-            split_bf16(b[8 * ldb], b[9 * ldb], bh1, bl1);
-            mma16816(c1[nt], al, bh0, bh1);  // three accumulators: no chain through one register set
-            mma16816(c2[nt], ah, bl0, bl1);
-            mma16816(c[nt], ah, bh0, bh1);
+            const float* b = B + (8 * ks + t) * ldb + 8 * nt + g;
+            const uint32_t y0 = __float_as_uint(b[0]), y1 = __float_as_uint(b[4 * ldb]);
+            if (ks & 1) mma1688(c1[nt], x0, x1, x2, x3, y0, y1);
+            else mma1688(c[nt], x0, x1, x2, x3, y0, y1);
         }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) c[nt][e] += c1[nt][e] + c2[nt][e];
+        for (int e = 0; e < 4; ++e) c[nt][e] += c1[nt][e];
 }
 template <int NT>
 __device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, int ldd, float sgn, int lane) {
