@@ -24,28 +24,49 @@ size_t build_workspace_bytes(int n_seg) {
 }
 
 // ------------------------------------------------------------------ plan --
-// Rank of segment s = number of segments with a longer body, or an equal body
-// and a lower index; order[rank] = s.  Quadratic, one CTA (segment counts are
-// in the hundreds to thousands).
-__global__ void build_plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ skip, int n_seg,
-                                  int32_t* __restrict__ order, unsigned* __restrict__ counter) {
-    for (int s = threadIdx.x; s < n_seg; s += blockDim.x) {
-        const int ls = cu[s + 1] - cu[s] - (skip ? skip[s] : 0);
-        int rank = 0;
-        for (int j = 0; j < n_seg; ++j) {
-            const int lj = cu[j + 1] - cu[j] - (skip ? skip[j] : 0);
-            rank += (lj > ls) || (lj == ls && j < s);
+// Longest-body-first order of the segments (ties: lower index first), by rank:
+// the rank of segment s is the number of segments that come before it.  Each
+// CTA ranks 64 segments, four threads per segment counting over every fourth
+// segment of a tile of body lengths staged in shared memory; the four counts
+// are summed by shuffles.  Block 0 also zeroes the work counter.
+constexpr int kPlanSegs = 64, kPlanThreads = 256, kPlanTile = 1024;
+
+__device__ __forceinline__ int body_len(const int32_t* cu, const int32_t* skip, int s) {
+    return cu[s + 1] - cu[s] - (skip ? skip[s] : 0);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) build_plan_kernel(const int32_t* __restrict__ cu,
+                                                                  const int32_t* __restrict__ skip, int n_seg,
+                                                                  int32_t* __restrict__ order,
+                                                                  unsigned* __restrict__ counter) {
+    __shared__ int len[kPlanTile];
+    const int tid = threadIdx.x, part = tid & 3;
+    const int s = blockIdx.x * kPlanSegs + (tid >> 2);
+    const int ls = s < n_seg ? body_len(cu, skip, s) : 0;
+    int rank = 0;
+    for (int j0 = 0; j0 < n_seg; j0 += kPlanTile) {
+        const int m = n_seg - j0 < kPlanTile ? n_seg - j0 : kPlanTile;
+        for (int e = tid; e < m; e += kPlanThreads) len[e] = body_len(cu, skip, j0 + e);
+        __syncthreads();
+        for (int e = part; e < m; e += 4) {
+            const int lj = len[e];
+            rank += (lj > ls) || (lj == ls && j0 + e < s);
         }
-        order[rank] = s;
+        __syncthreads();
     }
-    if (threadIdx.x == 0) counter[0] = 0u;
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    if (part == 0 && s < n_seg) order[rank] = s;
+    if (blockIdx.x == 0 && tid == 0) counter[0] = 0u;
 }
 
 cudaError_t launch_build_plan(const BuildParams& p, void* workspace, cudaStream_t s) {
     int32_t* order = reinterpret_cast<int32_t*>(workspace);
     unsigned* counter = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(workspace) +
                                                     build_workspace_bytes(p.n_seg) - 256);
-    if (p.n_seg > 0) build_plan_kernel<<<1, 1024, 0, s>>>(p.cu, p.skip, p.n_seg, order, counter);
+    if (p.n_seg > 0)
+        build_plan_kernel<<<(p.n_seg + kPlanSegs - 1) / kPlanSegs, kPlanThreads, 0, s>>>(p.cu, p.skip, p.n_seg, order,
+                                                                                          counter);
     return cudaGetLastError();
 }
 
