@@ -416,8 +416,45 @@ __device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, in
     }
 }
 
-// (I + A)^-1 in place, A strictly lower triangular 64 x 64 (row stride kAS),
-// by recursive doubling on the block-triangular inverse
+// The operand forms of M, K-major 64 x 64 bf16 (128-byte rows, 128-byte
+// swizzle): -M Diag(b) as a hi + lo pair at bt and bt + 8192 (the W^T
+// product, to about 16 bits; negated so that GEMM1 yields -X), and M Diag(b uf)
+// at bt + 16384 (the U~ product).  Each block of M is written by the solve
+// level that finishes it; the blocks above the diagonal are zero in every
+// chunk and are written once, when the kernel starts.
+__device__ __forceinline__ uint32_t form_off(int r, int j) {
+    return (uint32_t)r * 128u + ((uint32_t)((j >> 3) ^ (r & 7)) << 4) + (uint32_t)(j & 7) * 2u;
+}
+// Element (r, j).
+__device__ __forceinline__ void form_write1(uint8_t* bt, int r, int j, float m, float beta, float uf) {
+    const float mv = m * beta, nm = -mv;
+    const uint32_t hx = __float_as_uint(nm) & 0xffff0000u;
+    const uint32_t off = form_off(r, j);
+    *reinterpret_cast<uint16_t*>(bt + off) = (uint16_t)(hx >> 16);
+    *reinterpret_cast<__nv_bfloat16*>(bt + 8192 + off) = __float2bfloat16_rn(nm - __uint_as_float(hx));
+    *reinterpret_cast<__nv_bfloat16*>(bt + 16384 + off) = __float2bfloat16_rn(mv * uf);
+}
+// Elements (r, j) and (r, j + 1), j even.
+__device__ __forceinline__ void form_write2(uint8_t* bt, int r, int j, float m0, float m1, const float* beta,
+                                            const float* uf) {
+    const float mv0 = m0 * beta[j], mv1 = m1 * beta[j + 1];
+    uint32_t hi, lo;
+    split_bf16(-mv0, -mv1, hi, lo);
+    const uint32_t off = form_off(r, j);
+    *reinterpret_cast<uint32_t*>(bt + off) = hi;
+    *reinterpret_cast<uint32_t*>(bt + 8192 + off) = lo;
+    *reinterpret_cast<uint32_t*>(bt + 16384 + off) = pack_bf16(mv0 * uf[j], mv1 * uf[j + 1]);
+}
+// A 16 x 8 tile of M from a warp_gemm fragment times sgn, rows r0.., columns c0..
+__device__ __forceinline__ void form_tile(uint8_t* bt, int r0, int c0, const float (&c)[4], float sgn,
+                                          const float* beta, const float* uf, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    form_write2(bt, r0 + g, c0 + 2 * t, sgn * c[0], sgn * c[1], beta, uf);
+    form_write2(bt, r0 + g + 8, c0 + 2 * t, sgn * c[2], sgn * c[3], beta, uf);
+}
+
+// (I + A)^-1, A strictly lower triangular 64 x 64 (row stride kAS), by
+// recursive doubling on the block-triangular inverse
 //   [[L11, 0], [L21, L22]]^-1 = [[M11, 0], [-M22 L21 M11, M22]]:
 //   level 1: the four 16 x 16 diagonal blocks, forward substitution by
 //            columns (threads 0..63, one column each);
@@ -426,8 +463,10 @@ __device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, in
 //   level 3: the lower-left 32 x 32 block, from the two 32 x 32 inverses
 //            (warp w: 16 x 8 tile w of it).
 // The products run over full blocks: the zero upper parts of the triangular
-// factors make that exact.  Ptmp holds the left products.
-__device__ void prep_solve(float* As, float* Ptmp, int p, int bar) {
+// factors make that exact.  Levels 1 and 2 keep their blocks in place (the
+// later levels read them); every level writes its blocks' operand forms into
+// bt.  Ptmp holds the left products.
+__device__ void prep_solve(float* As, float* Ptmp, uint8_t* bt, const float* beta, const float* uf, int p, int bar) {
     const int w = p >> 5, lane = p & 31;
     if (p < kC) {  // level 1
         const int b = p >> 4, c = p & 15;
@@ -444,6 +483,10 @@ __device__ void prep_solve(float* As, float* Ptmp, int p, int bar) {
         float* Mb = As + 16 * b * kAS + 16 * b + c;
 #pragma unroll
         for (int i = 0; i < 16; ++i) Mb[i * kAS] = s[i];
+        const int j = 16 * b + c;
+        const float bj = beta[j], uj = uf[j];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) form_write1(bt, 16 * b + i, j, s[i], bj, uj);
     }
     named_sync(bar, kPrepThreads);
     {  // level 2: P = A_{x+1,x} M_xx, then M_{x+1,x} = -M_{x+1,x+1} P, x = 0, 2
@@ -458,11 +501,12 @@ __device__ void prep_solve(float* As, float* Ptmp, int p, int bar) {
         if (w < 4) {
             warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * (x + 1), kAS, P + 8 * nt, 20, lane);
             warp_store<1>(c, As + 16 * (x + 1) * kAS + 16 * x + 8 * nt, kAS, -1.f, lane);
+            form_tile(bt, 16 * (x + 1), 16 * x + 8 * nt, c[0], -1.f, beta, uf, lane);
         }
     }
     named_sync(bar, kPrepThreads);
     {  // level 3: P = A[32:64, 0:32] M[0:32, 0:32], then M[32:64, 0:32] = -M[32:64, 32:64] P
-        // (8 tiles of 16 x 8, taken in turn by the group's warps)
+        // (8 tiles of 16 x 8, taken in turn by the group's warps; the result only goes into the forms)
         constexpr int kWarps = kPrepThreads / 32;
         float c[8 / kWarps][1][4];
 #pragma unroll
@@ -484,46 +528,9 @@ __device__ void prep_solve(float* As, float* Ptmp, int p, int bar) {
 #pragma unroll
         for (int i = 0; i < 8 / kWarps; ++i) {
             const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
-            warp_store<1>(c[i], As + (32 + r0) * kAS + c0, kAS, -1.f, lane);
+            form_tile(bt, 32 + r0, c0, c[i][0], -1.f, beta, uf, lane);
         }
     }
-    named_sync(bar, kPrepThreads);
-}
-
-// The forms of M as K-major 64 x 64 bf16 operands (128-byte rows, 128-byte
-// swizzle): -M Diag(b) as a hi + lo pair at bt and bt + 8192 (the W^T
-// product, to about 16 bits; negated so that GEMM1 yields -X), and M Diag(b uf)
-// at bt + 16384 (the U~ product).  Thread p writes a quarter of a row.
-__device__ void prep_write_forms(const Misc* ms, const float* As, uint32_t bt, int slot, int p) {
-#pragma unroll 1
-  for (int u = p; u < 256; u += kPrepThreads) {
-    const int t = u >> 2, qr = u & 3;
-    const float* row = As + t * kAS + 16 * qr;
-    const float* beta = ms->beta[slot] + 16 * qr;
-    const float* uf = ms->uf[slot] + 16 * qr;
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-        const float4 x0 = *reinterpret_cast<const float4*>(row + 8 * ch);
-        const float4 x1 = *reinterpret_cast<const float4*>(row + 8 * ch + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(beta + 8 * ch);
-        const float4 b1 = *reinterpret_cast<const float4*>(beta + 8 * ch + 4);
-        const float4 u0 = *reinterpret_cast<const float4*>(uf + 8 * ch);
-        const float4 u1 = *reinterpret_cast<const float4*>(uf + 8 * ch + 4);
-        const float mv[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
-                             x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
-        const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t wh[4], wl[4], wu[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            split_bf16(-mv[2 * jj], -mv[2 * jj + 1], wh[jj], wl[jj]);
-            wu[jj] = pack_bf16(mv[2 * jj] * uv[2 * jj], mv[2 * jj + 1] * uv[2 * jj + 1]);
-        }
-        const uint32_t off = t * 128u + ((uint32_t)((2 * qr + ch) ^ (t & 7)) << 4);
-        st_shared_v4(bt + off, wh[0], wh[1], wh[2], wh[3]);
-        st_shared_v4(bt + 8192u + off, wl[0], wl[1], wl[2], wl[3]);
-        st_shared_v4(bt + 16384u + off, wu[0], wu[1], wu[2], wu[3]);
-    }
-  }
 }
 
 // ---------------------------------------------------------- state roles --
@@ -854,13 +861,12 @@ __device__ void issue_t_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t 
     }
 }
 
-// Warps 4-11: gram -> A^ -> M = (I + A^)^-1 -> its operand forms, chunk
+// Warps 4-11: gram -> A^ -> M = (I + A^)^-1 and its operand forms, chunk
 // after chunk (p: thread index among them).
 __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t g, int nc, int p, int q,
                           int lane) {
     float* As = reinterpret_cast<float*>(smem + OFF_AS);
     float* Ptmp = reinterpret_cast<float*>(smem + OFF_PT);
-    const uint32_t bt = smem_u32(smem) + OFF_BT;
     for (int c = 0; c < nc; ++c) {
         const uint32_t gc = g + c;
         const int slot = gc % kGateSlots;
@@ -872,11 +878,10 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         tc_fence_before();
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->g_read);
-        prep_solve(As, Ptmp, p, 1);
-        // the buffer's previous forms (chunk gc - 2) have been read (the buffer's phases are waited in order)
+        // the forms buffer's previous forms (chunk gc - 2) have been read (its phases are waited in order)
         if (!wg_all(1, gc < 2 || wait_bar(&ms->bt_free[gc & 1], ((gc >> 1) - 1) & 1, ms, a), kPrepThreads))
             return;
-        prep_write_forms(ms, As, bt + (gc & 1) * kBT, slot, p);
+        prep_solve(As, Ptmp, smem + OFF_BT + (gc & 1) * kBT, ms->beta[slot], ms->uf[slot], p, 1);
         fence_async_smem();
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->that_ready[gc & 1]);
@@ -1074,6 +1079,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmv);
     }
     if (warp == kWarpIssP) tmem_alloc(&ms->tmem_base, 512);
+    for (uint32_t e = tid; e < 2 * kBT / 16; e += kThreads)  // the forms' zero blocks (written once)
+        *reinterpret_cast<uint4*>(smem + OFF_BT + 16 * e) = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
