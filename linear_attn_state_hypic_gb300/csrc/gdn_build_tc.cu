@@ -425,15 +425,6 @@ __device__ __forceinline__ void warp_store(const float (&c)[NT][4], float* D, in
 __device__ __forceinline__ uint32_t form_off(int r, int j) {
     return (uint32_t)r * 128u + ((uint32_t)((j >> 3) ^ (r & 7)) << 4) + (uint32_t)(j & 7) * 2u;
 }
-// Element (r, j).
-__device__ __forceinline__ void form_write1(uint8_t* bt, int r, int j, float m, float beta, float uf) {
-    const float mv = m * beta, nm = -mv;
-    const uint32_t hx = __float_as_uint(nm) & 0xffff0000u;
-    const uint32_t off = form_off(r, j);
-    *reinterpret_cast<uint16_t*>(bt + off) = (uint16_t)(hx >> 16);
-    *reinterpret_cast<__nv_bfloat16*>(bt + 8192 + off) = __float2bfloat16_rn(nm - __uint_as_float(hx));
-    *reinterpret_cast<__nv_bfloat16*>(bt + 16384 + off) = __float2bfloat16_rn(mv * uf);
-}
 // Elements (r, j) and (r, j + 1), j even.
 __device__ __forceinline__ void form_write2(uint8_t* bt, int r, int j, float m0, float m1, const float* beta,
                                             const float* uf) {
@@ -464,8 +455,9 @@ __device__ __forceinline__ void form_tile(uint8_t* bt, int r0, int c0, const flo
 //            (warp w: 16 x 8 tile w of it).
 // The products run over full blocks: the zero upper parts of the triangular
 // factors make that exact.  Levels 1 and 2 keep their blocks in place (the
-// later levels read them); every level writes its blocks' operand forms into
-// bt.  Ptmp holds the left products.
+// later levels read them); the forms of level 1's blocks are written by the
+// warps that level 2 leaves idle, those of levels 2 and 3 from the MMA
+// fragments.  Ptmp holds the left products.
 __device__ void prep_solve(float* As, float* Ptmp, uint8_t* bt, const float* beta, const float* uf, int p, int bar) {
     const int w = p >> 5, lane = p & 31;
     if (p < kC) {  // level 1
@@ -483,12 +475,16 @@ __device__ void prep_solve(float* As, float* Ptmp, uint8_t* bt, const float* bet
         float* Mb = As + 16 * b * kAS + 16 * b + c;
 #pragma unroll
         for (int i = 0; i < 16; ++i) Mb[i * kAS] = s[i];
-        const int j = 16 * b + c;
-        const float bj = beta[j], uj = uf[j];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) form_write1(bt, 16 * b + i, j, s[i], bj, uj);
     }
     named_sync(bar, kPrepThreads);
+    if (w >= 4) {  // the diagonal blocks' forms, two elements a thread at a time, while level 2 runs
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int q = p - 128 + 128 * e, b = q >> 7, i = (q >> 3) & 15, j = 2 * (q & 7);
+            const float* m = As + (16 * b + i) * kAS + 16 * b + j;
+            form_write2(bt, 16 * b + i, 16 * b + j, m[0], m[1], beta, uf);
+        }
+    }
     {  // level 2: P = A_{x+1,x} M_xx, then M_{x+1,x} = -M_{x+1,x+1} P, x = 0, 2
         const int x = 2 * ((w >> 1) & 1), nt = w & 1;
         float* P = Ptmp + ((w >> 1) & 1) * 320;  // 16 x 16, row stride 20
