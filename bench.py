@@ -63,21 +63,38 @@ def load_peaks():
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples nvidia-smi clocks and throttle reasons every 50 ms while running;
+    summary() keeps the samples received inside the timed region (mark it with
+    begin() and end())."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
-        self.index = index
+        self.index = index  # CUDA ordinal; nvidia-smi is given the device's UUID when torch knows it
         self.rows = []
         self.proc = None
+        self.t0 = self.t1 = None
+
+    def _smi_id(self):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(self.index)
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self._smi_id()}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -89,7 +106,7 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
-                self.rows.append(parts)
+                self.rows.append((time.time(), parts))
 
     def __exit__(self, *exc):
         if self.proc:
@@ -100,14 +117,19 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        if not self.rows:
+        rows = self.rows
+        if self.t0 is not None:  # (a sample is received up to one period after it is taken)
+            t1 = self.t1 if self.t1 is not None else float("inf")
+            rows = [r for r in rows if self.t0 <= r[0] <= t1 + 0.06]
+        rows = [r[1] for r in rows]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(rows)}
 
 
 # ------------------------------------------------------------ our arm ----
@@ -266,19 +288,21 @@ def time_segment_parallel(args, rank, world, device):
     torch.cuda.set_device(device)
     req = SegmentParallelRequest(B, seed=0, device=device, rank=rank, world=world, n_batches=args.sp_batches)
     sp = torch.cuda.current_stream().cuda_stream
-    for _ in range(args.warmup):
-        req.run_step(sp)
-    torch.cuda.synchronize()
-    B.check_device(sp)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    with ClockSampler(torch.cuda.current_device()) as clk:  # (started before the warm-up: nvidia-smi needs a moment)
+        for _ in range(args.warmup):
+            req.run_step(sp)
+        torch.cuda.synchronize()
+        B.check_device(sp)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        clk.begin()
         start.record()
         for _ in range(args.steps):
             req.run_step(sp)
         stop.record()
         torch.cuda.synchronize()
+        clk.end()
     barrier(world)
     B.check_device(sp)
     ms = allreduce_max(start.elapsed_time(stop), world)
@@ -318,19 +342,21 @@ def time_our_arm(args, rank, world, device):
     req = LongRequest(B, seed=rank, device=device)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
-    for _ in range(args.warmup):
-        req.run_step(sp)
-    B.check_device(sp)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    with ClockSampler(torch.cuda.current_device()) as clk:  # (started before the warm-up: nvidia-smi needs a moment)
+        for _ in range(args.warmup):
+            req.run_step(sp)
+        B.check_device(sp)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        clk.begin()
         start.record()
         for s in range(args.steps):
             req.run_step(sp, ev[s])
         stop.record()
         torch.cuda.synchronize()
+        clk.end()
     barrier(world)
     B.check_device(sp)
     ms = start.elapsed_time(stop)
@@ -731,7 +757,7 @@ def workload_config(n_seg=None):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--mode", choices=["auto", "segment_parallel", "replicas"], default="auto",
