@@ -69,6 +69,7 @@ struct Misc {
     float beta[kU];
     int tok0, nv;
     int item;
+    float red[4];  // chain transition: the warps' column maxima
     int abort_flag;
     uint32_t tmem_base;
 };
@@ -85,6 +86,8 @@ struct CtArgs {
     const int32_t* seg_idx;
     const float* S0;
     float* S_out;
+    float* T_out;       // chain transition: each chain's own T (mantissa) ...
+    int32_t* T_exp_out;  // ... and its exponent
     unsigned* counter;
     unsigned* err;
     uint32_t wait_limit;
@@ -152,7 +155,7 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
 // range in seg_idx; lh: (layer, head) index.
 
 __device__ void producer_role(Misc* ms, uint8_t* smem, const CtArgs& a, const CUtensorMap* tmT,
-                              const CUtensorMap* tmS, uint32_t gs, uint32_t gj, int c0, int len, int lh) {
+                              const CUtensorMap* tmS, uint32_t gs, uint32_t gj, int c0, int len, int lh, bool load_sp) {
     const int LH = a.n_layers * a.n_heads;
     for (int j = 0; j < len; ++j) {
         const int p = a.seg_idx[c0 + j];
@@ -163,6 +166,7 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const CtArgs& a, const CU
             mbar_expect_tx(&ms->full[buf], kSliceBytes);
             tma_load_2d(smem + OFF_RING + buf * 2 * kSliceBytes, tmT, &ms->full[buf], 32 * s, row);
         }
+        if (!load_sp) continue;
         const uint32_t g = gj + j;
         if (g >= 1 && !wait_bar(&ms->sp_empty, (g - 1) & 1, ms, a)) return;
         mbar_expect_tx(&ms->sp_full, 4 * kSliceBytes);
@@ -658,8 +662,93 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
     }
 }
 
+// Chain-transition epilogue: the state is T_chain, from I, and each step
+// leaves T_p T_chain in TM_D.  It is brought back to a largest entry in
+// [1, 2) by a power of two (the 4 warps' maxima through shared memory), the
+// shift and the pair's exponent are added to T_chain's exponent, and the
+// result is split into the next step's A (the last step writes T_out and
+// T_exp_out).  Thread n owns column n.
+__device__ void epilogue_role_T(Misc* ms, const CtArgs& a, uint32_t tmem, uint32_t gj, int c0, int len, int lh,
+                                int64_t obj, int q, int lane) {
+    const int n = 32 * q + lane;
+    const int LH = a.n_layers * a.n_heads;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    float* out = a.T_out + obj * kD * kD;
+    if (len == 0) {  // empty chain: the identity
+        for (int i = 0; i < kD; ++i) out[i * kD + n] = i == n ? 1.f : 0.f;
+        if (n == 0) a.T_exp_out[obj] = 0;
+        return;
+    }
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {  // A for the first step: I (column n = e_n; the lo part is 0)
+        uint32_t h[32], l[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            h[jj] = 32 * cb + jj == n ? 0x3f800000u : 0u;
+            l[jj] = 0u;
+        }
+        tmem_st32(tl + TM_AB + 32 * cb, h);
+        tmem_st32(tl + TM_AS + 32 * cb, l);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    named_sync(4);
+    if (n == 0) mbar_arrive(&ms->a_ready);
+    int texp = 0;
+    for (int j = 0; j < len; ++j) {
+        const uint32_t g = gj + j;
+        const int p = a.seg_idx[c0 + j];
+        const int e = a.T_exp ? a.T_exp[p * LH + lh] : 0;
+        if (!wg_all(4, wait_bar(&ms->d_done, g & 1, ms, a))) return;
+        tc_fence_after();
+        float m = 0.f;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t x[32];
+            tmem_ld32(tl + TM_D + 32 * cb, x);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) m = fmaxf(m, fabsf(__uint_as_float(x[jj])));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) ms->red[q] = m;
+        named_sync(4);
+        m = fmaxf(fmaxf(ms->red[0], ms->red[1]), fmaxf(ms->red[2], ms->red[3]));
+        const int er = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
+        const float sc = ldexpf(1.f, -er);
+        texp += e + er;
+        const bool last = j + 1 == len;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t x[32];
+            tmem_ld32(tl + TM_D + 32 * cb, x);
+            tmem_wait_ld();
+            if (last) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) out[(32 * cb + jj) * kD + n] = __uint_as_float(x[jj]) * sc;
+            } else {
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t h[16], l[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]) * sc, h[jj], l[jj]);
+                    tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
+                    tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
+                }
+            }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        named_sync(4);  // (also: every warp has read the maxima before the next step rewrites them)
+        if (!last && n == 0) mbar_arrive(&ms->a_ready);
+    }
+    if (n == 0) a.T_exp_out[obj] = texp;
+}
+
 // ---------------------------------------------------------------- kernel --
-template <bool kSeam>
+// kSeam: the fused reuse chain; kTrans: each chain's own transition instead of its state.
+template <bool kSeam, bool kTrans>
 __global__ void __launch_bounds__(kThreads, 1)
     compose_tc_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmS, const CtArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -702,13 +791,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = a.cu_chain[chain], len = a.cu_chain[chain + 1] - c0;
         const int64_t obj = (int64_t)chain * LH + lh;
         if (warp == kWarpTMA) {
-            if (lane == 0) producer_role(ms, smem, a, &tmT, &tmS, gs, gj, c0, len, lh);
+            if (lane == 0) producer_role(ms, smem, a, &tmT, &tmS, gs, gj, c0, len, lh, !kTrans);
         } else if (warp == kWarpMMA) {
             if (lane == 0) mma_role(ms, smem, a, tmem, gs, gj, len);
         } else if (warp < kWarpEpi0) {
             convert_role<kSeam>(ms, smem, a, gs, gu, c0, len, lh, tid - 32 * kWarpCvt0);
         } else if (kSeam) {
             epilogue_role_seam(ms, smem, a, tmem, gj, gu, c0, len, lh, obj, warp & 3, lane);
+        } else if (kTrans) {
+            epilogue_role_T(ms, a, tmem, gj, c0, len, lh, obj, warp & 3, lane);
         } else {
             epilogue_role(ms, smem, a, tmem, gj, c0, len, lh, obj, warp & 3, lane);
         }
@@ -778,13 +869,13 @@ bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const float
 }  // namespace
 
 bool compose_tc_supported(const ComposeParams& p) {
-    return (p.family == kGDN || p.family == kKDA) && !p.T_out && p.dk == kD && p.dv == kD && p.n_pairs > 0 &&
+    return (p.family == kGDN || p.family == kKDA) && p.dk == kD && p.dv == kD && p.n_pairs > 0 &&
            (int64_t)p.n_pairs * p.n_layers * p.n_heads * kD < INT32_MAX && encode_fn() != nullptr;
 }
 
 namespace {
 
-template <bool kSeam>
+template <bool kSeam, bool kTrans = false>
 cudaError_t launch_tc(const ComposeParams& p, CtArgs a, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -802,16 +893,18 @@ cudaError_t launch_tc(const ComposeParams& p, CtArgs a, cudaStream_t s) {
     a.seg_idx = p.seg_idx;
     a.S0 = p.S0;
     a.S_out = p.S_out;
+    a.T_out = p.T_out;
+    a.T_exp_out = p.T_exp_out;
     a.counter = nullptr;
     a.wait_limit = 1u << 26;
     if (a.n_items == 0) return cudaSuccess;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel<kSeam>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(compose_tc_kernel<kSeam, kTrans>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = a.n_items < sms ? a.n_items : sms;
-    compose_tc_kernel<kSeam><<<grid, kThreads, kSmemBytes, s>>>(tT, tS, a);
+    compose_tc_kernel<kSeam, kTrans><<<grid, kThreads, kSmemBytes, s>>>(tT, tS, a);
     return cudaGetLastError();
 }
 
@@ -820,7 +913,9 @@ cudaError_t launch_tc(const ComposeParams& p, CtArgs a, cudaStream_t s) {
 cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_t s) {
     CtArgs a = {};
     a.err = err;
-    return launch_tc<false>(p, a, s);
+    cudaError_t e = launch_tc<false>(p, a, s);
+    if (e == cudaSuccess && p.T_out) e = launch_tc<false, true>(p, a, s);  // each chain's own transition
+    return e;
 }
 
 bool chain_tc_supported(const ChainParams& p) {  // (the fused seam units run the GDN recurrence)

@@ -85,11 +85,12 @@ def test_chain_transition(B, fam, dk, dv, with_s0):
     np.testing.assert_array_equal(got[2], T_ref[2])  # the empty chain: the identity
 
 
-@pytest.mark.parametrize("fam", ["gdn", "kda"])
-def test_chain_transition_strong_decay(B, fam):
+@pytest.mark.parametrize("fam,d", [("gdn", 32), ("kda", 32), ("gdn", 128)])
+def test_chain_transition_strong_decay(B, fam, d):
     """Pairs of 256-token segments with strong decay: a chain of 8 multiplies
-    their transitions far below the float32 range; the exponent keeps it."""
-    L, H, d = 1, 2, 32
+    their transitions far below the float32 range; the exponent keeps it (at
+    d = 128 on the tensor-core compose's transition mode)."""
+    L, H = 1, 2
     Tt, Te, S32, T64 = pair_table(fam, 7, 4, L, H, d, d, 256, lo=0.8)
     cu, idx = np.array([0, 8], np.int32), np.array([0, 1, 2, 3, 3, 2, 1, 0], np.int32)
     out, T, T_exp = B.compose(fam, dev(S32), cu, idx, T_tab=dev(Tt), T_exp_tab=dev(Te), want_T=True)
@@ -100,7 +101,7 @@ def test_chain_transition_strong_decay(B, fam):
     assert_rel(gdn_T64(T, T_exp), T_ref, TOL_F32, what=f"{fam} chain transition (strong decay)")
 
 
-@pytest.mark.parametrize("fam,d", [("gdn", 64), ("kda", 32), ("mamba2", 32), ("gla", 32)])
+@pytest.mark.parametrize("fam,d", [("gdn", 64), ("kda", 32), ("mamba2", 32), ("gla", 32), ("gdn", 128)])
 def test_tree_of_chains(B, fam, d):
     """Level 1: chains (p0 p1), (p2 p3), (p4 p5) with T_out, from zero; level 2:
     one chain over the three resulting pairs.  It equals the flat chain
