@@ -453,6 +453,9 @@ __device__ __forceinline__ void form_tile(uint8_t* bt, int r0, int c0, const flo
 //            w < 4: block pair w / 2, 8-column tile w % 2);
 //   level 3: the lower-left 32 x 32 block, from the two 32 x 32 inverses
 //            (warp w: 16 x 8 tile w of it).
+// Within a level, a warp waits only for the warps whose products it reads:
+// none at level 2 (each warp's second product reads only its own tile of the
+// first), its partner w ^ 4 at level 3 (named barriers 4-7, 64 threads).
 // The products run over full blocks: the zero upper parts of the triangular
 // factors make that exact.  Levels 1 and 2 keep their blocks in place (the
 // later levels read them); the forms of level 1's blocks are written by the
@@ -492,9 +495,7 @@ __device__ void prep_solve(float* As, float* Ptmp, uint8_t* bt, const float* bet
         if (w < 4) {
             warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * x, kAS, As + 16 * x * kAS + 16 * x + 8 * nt, kAS, lane);
             warp_store<1>(c, P + 8 * nt, 20, 1.f, lane);
-        }
-        named_sync(bar, kPrepThreads);
-        if (w < 4) {
+            __syncwarp();  // (the second product reads only the columns of P this warp wrote)
             warp_gemm<1, 1>(c, As + 16 * (x + 1) * kAS + 16 * (x + 1), kAS, P + 8 * nt, 20, lane);
             warp_store<1>(c, As + 16 * (x + 1) * kAS + 16 * x + 8 * nt, kAS, -1.f, lane);
             form_tile(bt, 16 * (x + 1), 16 * x + 8 * nt, c[0], -1.f, beta, uf, lane);
@@ -515,7 +516,9 @@ __device__ void prep_solve(float* As, float* Ptmp, uint8_t* bt, const float* bet
             const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
             warp_store<1>(c[i], Ptmp + r0 * 36 + c0, 36, 1.f, lane);  // 32 x 32, row stride 36
         }
-        named_sync(bar, kPrepThreads);
+        // the second products read P's columns c0..c0+7, written by warps w and w ^ 4 (rows 0-15, 16-31)
+        static_assert(kWarps == 8, "level 3's pair barriers assume eight prep warps");
+        named_sync(4 + (w & 3), 64);
 #pragma unroll
         for (int i = 0; i < 8 / kWarps; ++i) {
             const int tw = w + kWarps * i, r0 = 16 * (tw >> 2), c0 = 8 * (tw & 3);
