@@ -43,12 +43,12 @@ FLOP_PER_TOKEN_HEAD = 180_224      # chunk-64 low-rank GDN build (gram, W, U, tw
 COMPOSE_BYTES = 131_072            # T_p + S_p (fp32, d=128) streamed per head-compose
 SEAM_TOKEN_BYTES = 3 * 256 + 8 + 512  # per seam token-head: q, k, v bf16 in, a, b fp32 in, o fp32 out
 # DRAM bytes per algorithmic byte of the build kernel, from an ncu capture of
-# the 32-segment x 32-head ragged batch (820.4 MB of traffic: 719.4 MB read,
-# 101.0 MB written, for 837.9 MB of inputs and outputs; output still in L2
+# the 32-segment x 32-head ragged batch (820.2 MB of traffic: 719.1 MB read,
+# 101.1 MB written, for 837.9 MB of inputs and outputs; output still in L2
 # when the kernel ends is not counted as written); the full launch is too
 # large to capture, and its traffic scales with the same units (token-heads
 # in, (segment, head) out).
-BUILD_TRAFFIC_RATIO = 820.43 / 837.89
+BUILD_TRAFFIC_RATIO = 820.18 / 837.89
 BUILD_IN_BYTES_PER_TOKEN_HEAD = 520   # k, v bf16 (2 x 256 B) + alpha, beta fp32
 COMPOSE_TABLE_DRAM_RATIO = 9.14 / 17.4  # DRAM / algorithmic bytes of the shared compose table (ncu)
 BUILD_OUT_BYTES_PER_ITEM = 131_076    # T_C and S(C|0) fp32 (2 x 64 KB) + exponent
