@@ -871,15 +871,15 @@ __device__ void prep_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tme
         const int slot = gc % kGateSlots;
         bool ok = wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a);
         ok = ok && wait_bar(&ms->g_done, gc & 1, ms, a);
+        // the forms buffer's previous forms (chunk gc - 2) have been read (its phases are waited in order;
+        // waited here rather than before the solve: one barrier of the prep warps fewer per chunk)
+        ok = ok && (gc < 2 || wait_bar(&ms->bt_free[gc & 1], ((gc >> 1) - 1) & 1, ms, a));
         if (!wg_all(1, ok, kPrepThreads)) return;
         tc_fence_after();
         prep_arows(ms, As, slot, tmem, q, p >> 7, lane);
         tc_fence_before();
         named_sync(1, kPrepThreads);
         if (p == 0) mbar_arrive(&ms->g_read);
-        // the forms buffer's previous forms (chunk gc - 2) have been read (its phases are waited in order)
-        if (!wg_all(1, gc < 2 || wait_bar(&ms->bt_free[gc & 1], ((gc >> 1) - 1) & 1, ms, a), kPrepThreads))
-            return;
         prep_solve(As, Ptmp, smem + OFF_BT + (gc & 1) * kBT, ms->beta[slot], ms->uf[slot], p, 1);
         fence_async_smem();
         named_sync(1, kPrepThreads);
