@@ -1005,9 +1005,10 @@ __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         tc_fence_after();
         state_pass<false>(tl + TM_XS);
         tc_fence_before();
-        named_sync(2);
-        if (n == 0) mbar_arrive(&ms->y_ready_s);
+        // one barrier for both: every thread's S pass is written, and GEMM1 of the T half (issued with that
+        // of the S half, nearly always done by now) is committed
         if (!wg_all(2, wait_bar(&ms->x_done_t, gc & 1, ms, a))) return false;
+        if (n == 0) mbar_arrive(&ms->y_ready_s);
         tc_fence_after();
         state_pass<true>(tl + TM_XT);
         tc_fence_before();
