@@ -947,13 +947,10 @@ __device__ void publish_item(Misc* ms, const TcArgs& a, int k, int s, int lane) 
 // soon as the W operand is written.  Returns false once the CTA aborted.
 // (Converting the next W before the passes, to overlap GEMM1, measured slower:
 // the next W^T is then seldom ready and the passes wait for it.)
-// (gates: the next chunk's gate tables, waited in the same barrier when it belongs to this item)
 __device__ void convert_next_w(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, uint32_t ng, int q, int lane,
-                               bool& ok, uint64_t* gates = nullptr, uint32_t gates_parity = 0) {
+                               bool& ok) {
     // (the buffer was last read by GEMM1 of chunk ng - 1, whose completion the passes of that chunk waited for)
-    ok = wait_bar(&ms->w_done, ng & 1, ms, a);
-    ok = ok && (!gates || wait_bar(gates, gates_parity, ms, a));
-    ok = wg_all(2, ok);
+    ok = wg_all(2, wait_bar(&ms->w_done, ng & 1, ms, a));
     if (!ok) return;
     tc_fence_after();
     convert_w(smem, tmem, q, lane);
@@ -972,18 +969,12 @@ __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
     const uint32_t tl = tmem + ((32u * q) << 16);
     int E = 0;
     float sum_lc = 0.f;
-    bool ready = false;  // pre_done of the current chunk already signalled (its plan read into pl_next)
-    ChunkPlan pl_next;
+    bool ready = false;  // pre_done of the current chunk already signalled
     for (int c = 0; c < it.nc; ++c) {
         const uint32_t gc = it.g + c;
         const int slot = gc % kGateSlots;
-        ChunkPlan pl;
-        if (ready) {
-            pl = pl_next;  // (its gate tables were waited for with the W operand)
-        } else {
-            if (!wg_all(2, wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a))) return false;
-            pl = ms->plan[slot];
-        }
+        if (!wg_all(2, wait_bar(&ms->gready[slot], (gc / kGateSlots) & 1, ms, a))) return false;
+        const ChunkPlan pl = ms->plan[slot];
         sum_lc = pl.sum_lc;
         if (!ready) {
             if (pl.rn && c > 0) {  // renormalise the state GEMM2 of the previous chunk left
@@ -1005,10 +996,9 @@ __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
         tc_fence_after();
         state_pass<false>(tl + TM_XS);
         tc_fence_before();
-        // one barrier for both: every thread's S pass is written, and GEMM1 of the T half (issued with that
-        // of the S half, nearly always done by now) is committed
-        if (!wg_all(2, wait_bar(&ms->x_done_t, gc & 1, ms, a))) return false;
+        named_sync(2);
         if (n == 0) mbar_arrive(&ms->y_ready_s);
+        if (!wg_all(2, wait_bar(&ms->x_done_t, gc & 1, ms, a))) return false;
         tc_fence_after();
         state_pass<true>(tl + TM_XT);
         tc_fence_before();
@@ -1026,18 +1016,17 @@ __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
             has_next = next.nc > 0;
             ng = next.g;
         }
-        const uint32_t g1 = gc + 1;
-        const int s1 = g1 % kGateSlots;
         if (has_next) {
             bool ok;
-            if (c + 1 < it.nc) convert_next_w(ms, smem, a, tmem, ng, q, lane, ok, &ms->gready[s1], (g1 / kGateSlots) & 1);
-            else convert_next_w(ms, smem, a, tmem, ng, q, lane, ok);
+            convert_next_w(ms, smem, a, tmem, ng, q, lane, ok);
             if (!ok) return false;
         }
         ready = false;
         if (c + 1 < it.nc) {  // the next chunk of this item: ready at once unless it renormalises
-            pl_next = ms->plan[s1];
-            if (!pl_next.rn) {
+            const uint32_t g1 = gc + 1;
+            const int s1 = g1 % kGateSlots;
+            if (!wg_all(2, wait_bar(&ms->gready[s1], (g1 / kGateSlots) & 1, ms, a))) return false;
+            if (!ms->plan[s1].rn) {
                 if (n == 0) mbar_arrive(&ms->pre_done);
                 ready = true;
             }
