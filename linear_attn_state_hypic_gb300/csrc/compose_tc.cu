@@ -18,7 +18,8 @@
 // the chain ends; the HBM traffic is the pair stream, 128 KB per step.
 //
 // Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5
-// split the T slices (hi in place, lo beside it), warps 6-9 the epilogue.
+// split the T slices (hi in place, lo beside it) and, in the reuse chain,
+// build the seam units' operands; warps 6-9 the epilogue.
 // One CTA per SM, persistent over (chain, layer, head) items ordered
 // (layer, head)-major so that chains sharing a pair table run together.
 #include <cuda.h>
@@ -48,20 +49,33 @@ constexpr int kWarpTMA = 0, kWarpMMA = 1, kWarpCvt0 = 2, kWarpEpi0 = 6;
 constexpr uint32_t kSliceBytes = kD * 32 * 4;                    // 128 rows x 32 fp32 = 16 KB
 constexpr uint32_t OFF_RING = 0;                                 // kRing x (hi 16 KB, lo 16 KB)
 constexpr uint32_t OFF_SP = OFF_RING + kRing * 2 * kSliceBytes;  // S_p: 4 blocks [128 rows][32 cols] fp32
-// Reuse chain only: one seam unit (up to kU seam tokens) as the epilogue reads it.
+// Reuse chain only: one seam unit (up to kU seam tokens).
 constexpr int kU = 8;
+// B operand of the unit's dot products (M = 128 state columns, N = 2 kU, K = 128):
+// rows 0..kU-1 = -W, rows kU..2kU-1 = g_t q_t, K-major with the 128-byte swizzle
+// in four 32-column slices of 2 KB; hi, then lo.
+constexpr uint32_t kWqSlice = 2 * kU * 128;                      // 16 rows x 128 B
+constexpr uint32_t kWqBytes = 4 * kWqSlice;                      // 8 KB
+constexpr uint32_t OFF_WQ = OFF_SP + 4 * kSliceBytes;
+// B operand of the unit's rank-kU update (N = 128 state rows, K = kU): K^T,
+// K-major without swizzle (core matrices of 8 rows x 4 values; the two K halves
+// 128 bytes apart, 8-row groups 256 bytes apart); hi, then lo.
+constexpr uint32_t kKtBytes = kD * kU * 4;                       // 4 KB
+constexpr uint32_t OFF_KT = OFF_WQ + 2 * kWqBytes;
+// the unit's k and q rows, for its k.k and q.k products
 constexpr int kUR = kD + 4;                                      // row stride (floats): rows fall in distinct banks
 constexpr uint32_t kUnitRows = kU * kUR * 4;                     // [kU][kUR] fp32
-constexpr uint32_t OFF_SK = OFF_SP + 4 * kSliceBytes;            // k rows
-constexpr uint32_t OFF_SQ = OFF_SK + kUnitRows;                  // g_t q_t rows
-constexpr uint32_t OFF_SW = OFF_SQ + kUnitRows;                  // W = That Diag(g) K rows
-constexpr uint32_t OFF_SU = OFF_SW + kUnitRows;                  // U = That V rows
-constexpr uint32_t OFF_MISC = OFF_SU + kUnitRows;
+constexpr uint32_t OFF_SK = OFF_KT + 2 * kKtBytes;
+constexpr uint32_t OFF_SQ = OFF_SK + kUnitRows;
+constexpr uint32_t OFF_MISC = OFF_SQ + kUnitRows;
+static_assert(OFF_WQ % 1024 == 0, "128-byte swizzle atoms are 1024-byte aligned");
 
 struct Misc {
     uint64_t full[kRing], cvt[kRing], empty[kRing];
     uint64_t sp_full, sp_empty, d_done, a_ready, drain;
-    uint64_t seam_ready, seam_free;  // unit tables written / read
+    uint64_t seam_ready, seam_free;  // unit operands written / consumed
+    uint64_t r_go, r_done;           // A = split x ready for the unit's dot products / products in TM_R
+    uint64_t c_go, u_done;           // C^T in TM_C / rank-kU update added to TM_D
     // the current seam unit: tokens [tok0, tok0 + nv); g = in-unit decay prefix
     float kk[kU][kU], qk[kU][kU], th[kU][kU], thg[kU][kU];  // k.k then A, q.k, That, That Diag(g)
     float M[kU][kU];                 // (q_t . k_s) g_t / g_s, s <= t
@@ -77,7 +91,12 @@ constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t TM_D = 0, TM_AB = 128, TM_AS = 256;  // accumulator, A hi, A lo
+// Reuse chain: the seam unit's products (lane n: u'_s = U[s][n] - W_s . x in
+// columns 384..391, g_t q_t . x in 392..399) and its coefficients C^T (hi in
+// 400..407, lo in 408..415).
+constexpr uint32_t TM_R = 384, TM_C = 400;
 constexpr uint32_t ID_T = idesc(2, 128, 128, false, false);
+constexpr uint32_t ID_R = idesc(2, 128, 2 * kU, false, false);
 
 struct CtArgs {
     int n_layers, n_heads, n_pairs, n_chains, n_items;
@@ -174,8 +193,46 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const CtArgs& a, const CU
     }
 }
 
-__device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gs, uint32_t gj, int len) {
+// Reuse chain: the MMAs of the seam units of step js (global unit counter gu).
+// Per unit: the dot products TM_R += x (-W; g q)^T over the split state in
+// TM_AB / TM_AS (3 x tf32, N = 2 kU, K = 128), then, once the epilogue has
+// written C^T, the rank-kU update TM_D += C^T K (3 x tf32, K = kU).
+__device__ bool mma_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, int js, uint32_t& gu) {
+    int tb;
+    const int nu = step_units(a, js, tb);
+    const uint32_t wq = smem_u32(smem) + OFF_WQ, kt = smem_u32(smem) + OFF_KT;
+    for (int k = 0; k < nu; ++k) {
+        if (!wait_bar(&ms->seam_ready, gu & 1, ms, a) || !wait_bar(&ms->r_go, gu & 1, ms, a)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int s = 0; s < kSlices; ++s) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t b = wq + s * kWqSlice + kk * 32, acol = 32 * s + 8 * kk;
+                const uint64_t bh = sdesc_sw128(b, 0, 1024), bl = sdesc_sw128(b + kWqBytes, 0, 1024);
+                mma_tf32_ts(tmem + TM_R, tmem + TM_AB + acol, bh, ID_R, true);
+                mma_tf32_ts(tmem + TM_R, tmem + TM_AB + acol, bl, ID_R, true);
+                mma_tf32_ts(tmem + TM_R, tmem + TM_AS + acol, bh, ID_R, true);
+            }
+        }
+        mma_commit(&ms->r_done);
+        if (!wait_bar(&ms->c_go, gu & 1, ms, a)) return false;
+        tc_fence_after();
+        const uint64_t kh = sdesc_plain(kt, 128, 256), kl = sdesc_plain(kt + kKtBytes, 128, 256);
+        mma_tf32_ts(tmem + TM_D, tmem + TM_C, kh, ID_T, true);
+        mma_tf32_ts(tmem + TM_D, tmem + TM_C, kl, ID_T, true);
+        mma_tf32_ts(tmem + TM_D, tmem + TM_C + kU, kh, ID_T, true);
+        mma_commit(&ms->u_done);
+        ++gu;
+    }
+    return true;
+}
+
+template <bool kSeam>
+__device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gs, uint32_t gj,
+                         uint32_t gu, int c0, int len) {
     const uint32_t ring = smem_u32(smem) + OFF_RING;
+    if (kSeam && len > 0 && !mma_units(ms, smem, a, tmem, c0, gu)) return;
     for (int j = 0; j < len; ++j) {
         if (!wait_bar(&ms->a_ready, (gj + j) & 1, ms, a)) return;
         tc_fence_after();
@@ -195,6 +252,7 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem
             mma_commit(&ms->empty[buf]);
         }
         mma_commit(&ms->d_done);
+        if (kSeam && j + 1 < len && !mma_units(ms, smem, a, tmem, c0 + j + 1, gu)) return;
     }
 }
 
@@ -209,23 +267,29 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem
 //     o_t[n] = S_t[:, n] . q_t = g_t q_t . x + sum_{s<=t} (q_t . k_s)(g_t/g_s) u'_s,
 // and the unit ends at t = w (the padded tokens past w have a = 1, b = 0,
 // k = q = v = 0: identity steps).  The converter warpgroup builds the unit's
-// tables in shared memory while the MMAs of the previous compose run; the
-// epilogue applies them column by column.
+// operands while the MMAs of the previous compose run: -W and g q as the B
+// operand of the dot products, U as their accumulator's starting value in
+// tensor memory, K^T for the update and the small tables.  The dot products
+// and the update g_w x + K^T c run on the tensor cores; the epilogue takes
+// o and the coefficients c_s = (g_w/g_s) u'_s column by column between them.
 
 __device__ __forceinline__ float load_tok(const void* base, int bf16, int64_t row, int i) {
     return bf16 ? __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(base) + row * kD + i))
                 : __ldg(reinterpret_cast<const float*>(base) + row * kD + i);
 }
 
-// The tables of unit gu (tokens [tok0, tok0 + nv) of (layer, head) lh).
-// t: converter thread 0..127 (= feature index for the row loads).
-__device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int tok0, int nv, uint32_t gu, int t) {
+// The operands of unit gu (tokens [tok0, tok0 + nv) of (layer, head) lh).
+// t: converter thread 0..127 (= feature index of the k and q row loads).
+__device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, int lh, int tok0, int nv,
+                          uint32_t gu, int t) {
     if (gu >= 1 && !wg_all(3, wait_bar(&ms->seam_free, (gu - 1) & 1, ms, a))) return false;
     const int layer = lh / a.n_heads, head = lh % a.n_heads;
+    // converter warp 2 + t/32 reaches the TMEM lanes of quarter (t/32 + 2) mod 4:
+    // this thread starts the products of state column fl there
+    const uint32_t lq = 32u * ((t / 32 + 2) & 3);
+    const int fl = lq + (t & 31);
     float* Kf = reinterpret_cast<float*>(smem + OFF_SK);
     float* Qf = reinterpret_cast<float*>(smem + OFF_SQ);
-    float* Wf = reinterpret_cast<float*>(smem + OFF_SW);
-    float* Uf = reinterpret_cast<float*>(smem + OFF_SU);
     // every load is issued before any shared-memory store (the stores could
     // otherwise alias the loads for the compiler and serialise them)
     float kr[kU], qr[kU], vr[kU], ga = 1.f, gb = 0.f;
@@ -234,7 +298,7 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
         const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + (u < nv ? u : 0)) * a.n_heads + head;
         kr[u] = load_tok(a.k, a.in_bf16, row, t);
         qr[u] = load_tok(a.q, a.in_bf16, row, t);
-        vr[u] = load_tok(a.v, a.in_bf16, row, t);
+        vr[u] = load_tok(a.v, a.in_bf16, row, fl);
     }
     if (t < kU && t < nv) {
         const int64_t row = ((int64_t)layer * a.n_tokens + tok0 + t) * a.n_heads + head;
@@ -244,9 +308,11 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
         const bool valid = u < nv;
-        Kf[u * kUR + t] = valid ? kr[u] : 0.f;
-        Qf[u * kUR + t] = valid ? qr[u] : 0.f;
+        kr[u] = valid ? kr[u] : 0.f;
+        qr[u] = valid ? qr[u] : 0.f;
         vr[u] = valid ? vr[u] : 0.f;
+        Kf[u * kUR + t] = kr[u];
+        Qf[u * kUR + t] = qr[u];
     }
     if (t < kU) {
         ms->lg[t] = log2f(fmaxf(ga, FLT_MIN));
@@ -305,173 +371,149 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int 
         }
     }
     named_sync(3);
+    uint8_t* wq = smem + OFF_WQ;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {  // W, U and g_u q_u: column t
-        float w = 0.f, uu = 0.f;
+    for (int u = 0; u < kU; ++u) {  // feature t of rows u of -W and of g_u q_u, split hi/lo
+        float w = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 <= u; ++s2) {
-            w = fmaf(ms->thg[u][s2], Kf[s2 * kUR + t], w);
-            uu = fmaf(ms->th[u][s2], vr[s2], uu);
+        for (int s2 = 0; s2 <= u; ++s2) w = fmaf(ms->thg[u][s2], kr[s2], w);
+        uint32_t h, l;
+        const uint32_t ow = sw128_offset(u, t, 4, kWqSlice), oq = sw128_offset(kU + u, t, 4, kWqSlice);
+        split_tf32(-w, h, l);
+        *reinterpret_cast<uint32_t*>(wq + ow) = h;
+        *reinterpret_cast<uint32_t*>(wq + kWqBytes + ow) = l;
+        split_tf32(ms->g[u] * qr[u], h, l);
+        *reinterpret_cast<uint32_t*>(wq + oq) = h;
+        *reinterpret_cast<uint32_t*>(wq + kWqBytes + oq) = l;
+    }
+    {  // row t of K^T, split hi/lo
+        uint4 h0, l0, h1, l1;
+        split_tf32(kr[0], h0.x, l0.x), split_tf32(kr[1], h0.y, l0.y);
+        split_tf32(kr[2], h0.z, l0.z), split_tf32(kr[3], h0.w, l0.w);
+        split_tf32(kr[4], h1.x, l1.x), split_tf32(kr[5], h1.y, l1.y);
+        split_tf32(kr[6], h1.z, l1.z), split_tf32(kr[7], h1.w, l1.w);
+        uint8_t* kt = smem + OFF_KT + (t >> 3) * 256 + (t & 7) * 16;
+        *reinterpret_cast<uint4*>(kt) = h0;
+        *reinterpret_cast<uint4*>(kt + 128) = h1;
+        *reinterpret_cast<uint4*>(kt + kKtBytes) = l0;
+        *reinterpret_cast<uint4*>(kt + kKtBytes + 128) = l1;
+    }
+    {  // the products' starting value in lane fl: U[s][fl] = (That V)[s][fl], and 0 for g q . x
+        uint32_t r[2 * kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            float uu = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 <= u; ++s2) uu = fmaf(ms->th[u][s2], vr[s2], uu);
+            r[u] = __float_as_uint(uu);
+            r[kU + u] = 0u;
         }
-        Wf[u * kUR + t] = w;
-        Uf[u * kUR + t] = uu;
-        Qf[u * kUR + t] *= ms->g[u];
+        tmem_st16(tmem + (lq << 16) + TM_R, r);
+        tmem_wait_st();
     }
     if (t == 0) {
         ms->tok0 = tok0;
         ms->nv = nv;
     }
+    fence_async_smem();
+    tc_fence_before();
     named_sync(3);
     if (t == 0) mbar_arrive(&ms->seam_ready);
     return true;
 }
 
 // The units of step js (global unit counter gu) for (layer, head) lh.
-__device__ bool prep_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, int lh, int js, uint32_t& gu, int t) {
+__device__ bool prep_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, int lh, int js, uint32_t& gu,
+                                int t) {
     int tb;
     const int nu = step_units(a, js, tb);
     const int w = a.cu_step[js + 1] - tb;
     for (int k = 0; k < nu; ++k) {
         const int nv = w - kU * k < kU ? w - kU * k : kU;
-        if (!prep_unit(ms, smem, a, lh, tb + kU * k, nv, gu, t)) return false;
+        if (!prep_unit(ms, smem, a, tmem, lh, tb + kU * k, nv, gu, t)) return false;
         ++gu;
     }
     return true;
 }
 
-// Applies the units of step js to the state in TM_D; the last unit writes the
-// split A operand of the next compose instead.  The two passes read the
-// state in the .16x256b shape: thread t of warp q holds lanes (columns of the
-// state) L_j = 32q + t/4 + 8j, j = 0..3, at a quarter of the rows i, so every
-// table value it loads from shared memory serves four columns.  The dot
-// products are then summed over the four threads that share t/4 (a
-// reduce-scatter by shuffles) and thread t finishes column L_{t%4}.
-__device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tl, int lh, int js, uint32_t& gu,
-                                 int n) {
+// One seam unit on the state, epilogue thread n = TMEM lane n = state column
+// n.  On entry TM_AB / TM_AS hold the column x split hi/lo and TM_D holds
+// g_w x.  The MMAs leave u'_s and g_s q_s . x in TM_R; this thread writes o_t
+// and C^T (c_s = (g_w/g_s) u'_s, split hi/lo) to TM_C, and the rank-kU MMAs
+// add K^T c to TM_D.
+__device__ bool seam_unit(Misc* ms, const CtArgs& a, uint32_t tl, int layer, int head, uint32_t gu, int n) {
+    tc_fence_before();
+    named_sync(4);
+    if (n == 0) mbar_arrive(&ms->r_go);
+    if (!wg_all(4, wait_bar(&ms->r_done, gu & 1, ms, a))) return false;
+    tc_fence_after();
+    uint32_t r[2 * kU];
+    tmem_ld16(tl + TM_R, r);
+    tmem_wait_ld();
+    const int nv = ms->nv, tok0 = ms->tok0;
+    float up[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) up[u] = __uint_as_float(r[u]);
+    uint32_t cv[2 * kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        float o = __uint_as_float(r[kU + u]);
+#pragma unroll
+        for (int s2 = 0; s2 <= u; ++s2) o = fmaf(ms->M[u][s2], up[s2], o);
+        if (u < nv) a.o_out[(((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head) * kD + n] = o;
+        split_tf32(ms->sc[u] * up[u], cv[u], cv[kU + u]);
+    }
+    tmem_st16(tl + TM_C, cv);
+    tmem_wait_st();
+    tc_fence_before();
+    named_sync(4);  // (also: every column has read the unit's tables)
+    if (n == 0) mbar_arrive(&ms->c_go);
+    if (!wg_all(4, wait_bar(&ms->u_done, gu & 1, ms, a))) return false;
+    tc_fence_after();
+    if (n == 0) mbar_arrive(&ms->seam_free);  // the unit's operands have been consumed
+    return true;
+}
+
+// TM_D -> the A operand, split hi/lo; with rescale also TM_D <- gw TM_D.
+__device__ void split_state(uint32_t tl, bool rescale, float gw) {
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32];
+        tmem_ld32(tl + TM_D + 32 * cb, x);
+        tmem_wait_ld();
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t h[16], l[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]), h[jj], l[jj]);
+            tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
+            tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
+        }
+        if (rescale) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(gw * __uint_as_float(x[jj]));
+            tmem_st32(tl + TM_D + 32 * cb, x);
+        }
+    }
+    tmem_wait_st();
+}
+
+// Applies the units of step js to the state; on entry as for seam_unit (the
+// first unit's g_w x in TM_D), on return the A operand of the next compose.
+__device__ bool apply_step_units(Misc* ms, const CtArgs& a, uint32_t tl, int lh, int js, uint32_t& gu, int n) {
     int tb;
     const int nu = step_units(a, js, tb);
     const int layer = lh / a.n_heads, head = lh % a.n_heads;
-    const float* Kf = reinterpret_cast<const float*>(smem + OFF_SK);
-    const float* Qf = reinterpret_cast<const float*>(smem + OFF_SQ);
-    const float* Wf = reinterpret_cast<const float*>(smem + OFF_SW);
-    const float* Uf = reinterpret_cast<const float*>(smem + OFF_SU);
-    const int t = n & 31, r4 = t >> 2, c4 = t & 3;
-    const int nl = (n & ~31) + r4 + 8 * c4;       // the column this thread finishes
-    const uint32_t lb0 = tl, lb1 = tl + (16u << 16);  // lanes +0..15 and +16..31 of the quarter
     for (int k = 0; k < nu; ++k) {
-        if (!wg_all(4, wait_bar(&ms->seam_ready, gu & 1, ms, a))) return false;
-        float acc[4][2 * kU];  // [column L_j][W_u . x for u < kU, g_u q_u . x after]
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int d = 0; d < 2 * kU; ++d) acc[j][d] = 0.f;
-#pragma unroll 1
-        for (int bb = 0; bb < 16; ++bb) {  // pass 1, 8 rows at a time
-            uint32_t xa[4], xb[4];
-            tmem_ld16x256b_x1(lb0 + TM_D + 8 * bb, xa);
-            tmem_ld16x256b_x1(lb1 + TM_D + 8 * bb, xb);
-            tmem_wait_ld();
-            const int i0 = 8 * bb + 2 * c4;
-            const float x[4][2] = {{__uint_as_float(xa[0]), __uint_as_float(xa[1])},
-                                   {__uint_as_float(xa[2]), __uint_as_float(xa[3])},
-                                   {__uint_as_float(xb[0]), __uint_as_float(xb[1])},
-                                   {__uint_as_float(xb[2]), __uint_as_float(xb[3])}};
-#pragma unroll
-            for (int dd = 0; dd < 2 * kU; ++dd) {
-                const float2 w = *reinterpret_cast<const float2*>((dd < kU ? Wf + dd * kUR : Qf + (dd - kU) * kUR) + i0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[j][dd] = fmaf(w.x, x[j][0], fmaf(w.y, x[j][1], acc[j][dd]));
-            }
-        }
-        // reduce-scatter over the four threads of the row group: thread c4 ends
-        // with the full sums of column L_{c4}
-        const bool h2 = c4 & 2, h1 = c4 & 1;
-        float pr[2][2 * kU];
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int d = 0; d < 2 * kU; ++d) {
-                const float mine = h2 ? acc[2 + j][d] : acc[j][d];
-                const float other = h2 ? acc[j][d] : acc[2 + j][d];
-                pr[j][d] = mine + __shfl_xor_sync(0xffffffffu, other, 2);
-            }
-        float fin[2 * kU];
-#pragma unroll
-        for (int d = 0; d < 2 * kU; ++d) {
-            const float mine = h1 ? pr[1][d] : pr[0][d];
-            const float other = h1 ? pr[0][d] : pr[1][d];
-            fin[d] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
-        }
-        float up[kU], c[kU];
-        const int nv = ms->nv, tok0 = ms->tok0;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) up[u] = Uf[u * kUR + nl] - fin[u];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            float o = fin[kU + u];
-#pragma unroll
-            for (int s2 = 0; s2 <= u; ++s2) o = fmaf(ms->M[u][s2], up[s2], o);
-            if (u < nv) a.o_out[(((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head) * kD + nl] = o;
-            c[u] = ms->sc[u] * up[u];
-        }
-        float cc[4][kU];  // the coefficients of this thread's four columns
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int u = 0; u < kU; ++u) cc[j][u] = __shfl_sync(0xffffffffu, c[u], (t & ~3) | j);
-        const float gw = ms->g[kU - 1];
-        const bool last = k + 1 == nu;
-#pragma unroll 1
-        for (int bb = 0; bb < 16; ++bb) {  // pass 2: x <- g_w x + sum_s (g_w/g_s) k_s u'_s, 8 rows at a time
-            uint32_t xa[4], xb[4];
-            tmem_ld16x256b_x1(lb0 + TM_D + 8 * bb, xa);
-            tmem_ld16x256b_x1(lb1 + TM_D + 8 * bb, xb);
-            tmem_wait_ld();
-            const int i0 = 8 * bb + 2 * c4;
-            float y[4][2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                y[0][e] = gw * __uint_as_float(xa[e]);
-                y[1][e] = gw * __uint_as_float(xa[2 + e]);
-                y[2][e] = gw * __uint_as_float(xb[e]);
-                y[3][e] = gw * __uint_as_float(xb[2 + e]);
-            }
-#pragma unroll
-            for (int s2 = 0; s2 < kU; ++s2) {
-                const float2 k2 = *reinterpret_cast<const float2*>(Kf + s2 * kUR + i0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    y[j][0] = fmaf(k2.x, cc[j][s2], y[j][0]);
-                    y[j][1] = fmaf(k2.y, cc[j][s2], y[j][1]);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                xa[e] = __float_as_uint(y[0][e]);
-                xa[2 + e] = __float_as_uint(y[1][e]);
-                xb[e] = __float_as_uint(y[2][e]);
-                xb[2 + e] = __float_as_uint(y[3][e]);
-            }
-            if (last) {  // the A operand of the next compose, split hi/lo
-                uint32_t ha[4], la[4], hb[4], lbv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    split_tf32(__uint_as_float(xa[e]), ha[e], la[e]);
-                    split_tf32(__uint_as_float(xb[e]), hb[e], lbv[e]);
-                }
-                tmem_st16x256b_x1(lb0 + TM_AB + 8 * bb, ha);
-                tmem_st16x256b_x1(lb1 + TM_AB + 8 * bb, hb);
-                tmem_st16x256b_x1(lb0 + TM_AS + 8 * bb, la);
-                tmem_st16x256b_x1(lb1 + TM_AS + 8 * bb, lbv);
-            } else {
-                tmem_st16x256b_x1(lb0 + TM_D + 8 * bb, xa);
-                tmem_st16x256b_x1(lb1 + TM_D + 8 * bb, xb);
-            }
-        }
-        tmem_wait_st();
-        named_sync(4);  // every column has read the unit's tables
-        if (n == 0) mbar_arrive(&ms->seam_free);
+        if (!seam_unit(ms, a, tl, layer, head, gu, n)) return false;
         ++gu;
+        const bool more = k + 1 < nu;
+        float gw = 0.f;
+        if (more) {  // the next unit's decay over its tokens
+            if (!wg_all(4, wait_bar(&ms->seam_ready, gu & 1, ms, a))) return false;
+            gw = ms->g[kU - 1];
+        }
+        split_state(tl, more, gw);
     }
     return true;
 }
@@ -480,9 +522,9 @@ __device__ bool apply_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint3
 // Reuse chain: also the seam units, those of step 0 first and those of step
 // j + 1 while the MMAs of step j run.
 template <bool kSeam>
-__device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t gs, uint32_t gu, int c0, int len,
-                             int lh, int t) {
-    if (kSeam && len > 0 && !prep_step_units(ms, smem, a, lh, c0, gu, t)) return;
+__device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gs, uint32_t gu, int c0,
+                             int len, int lh, int t) {
+    if (kSeam && len > 0 && !prep_step_units(ms, smem, a, tmem, lh, c0, gu, t)) return;
     for (int j = 0; j < len; ++j) {
         for (int s = 0; s < kSlices; ++s) {
             const uint32_t gsi = gs + kSlices * j + s, buf = gsi % kRing;
@@ -505,7 +547,7 @@ __device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t 
             named_sync(3);
             if (t == 0) mbar_arrive(&ms->cvt[buf]);
         }
-        if (kSeam && j + 1 < len && !prep_step_units(ms, smem, a, lh, c0 + j + 1, gu, t)) return;
+        if (kSeam && j + 1 < len && !prep_step_units(ms, smem, a, tmem, lh, c0 + j + 1, gu, t)) return;
     }
 }
 
@@ -574,9 +616,11 @@ __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t
 
 // Reuse-chain epilogue: as epilogue_role, with the seam units of step j + 1
 // applied to the composed column before it becomes the A operand of step
-// j + 1 (and those of step 0 to the start state).
-__device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gj,
-                                   uint32_t gu, int c0, int len, int lh, int64_t obj, int q, int lane) {
+// j + 1 (and those of step 0 to the start state).  Before a unit the column
+// goes to the A operand (split hi/lo, for the unit's dot products) and, times
+// the unit's g_w, to TM_D.
+__device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gj, uint32_t gu,
+                                   int c0, int len, int lh, int64_t obj, int q, int lane) {
     const int n = 32 * q + lane;
     const int LH = a.n_layers * a.n_heads;
     const uint32_t tl = tmem + ((32u * q) << 16);
@@ -587,27 +631,33 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
         return;
     }
     int tb;
-    if (step_units(a, c0, tb) == 0) {  // A for the first step: the start state, split hi/lo
+    const bool seam0 = step_units(a, c0, tb) > 0;
+    float gw = 0.f;
+    if (seam0) {
+        if (!wg_all(4, wait_bar(&ms->seam_ready, gu & 1, ms, a))) return;
+        gw = ms->g[kU - 1];
+    }
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {  // the start state, split hi/lo (and g_w S0 before a seam)
+        uint32_t x[32];
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            uint32_t h[32], l[32];
+        for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(s0 ? s0[(32 * cb + jj) * kD + n] : 0.f);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) split_tf32(s0 ? s0[(32 * cb + jj) * kD + n] : 0.f, h[jj], l[jj]);
-            tmem_st32(tl + TM_AB + 32 * cb, h);
-            tmem_st32(tl + TM_AS + 32 * cb, l);
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t h[16], l[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]), h[jj], l[jj]);
+            tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
+            tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
         }
-        tmem_wait_st();
-    } else {  // the start state through the seam of step 0
+        if (seam0) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            uint32_t x[32];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(s0 ? s0[(32 * cb + jj) * kD + n] : 0.f);
+            for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(gw * __uint_as_float(x[jj]));
             tmem_st32(tl + TM_D + 32 * cb, x);
         }
-        tmem_wait_st();
-        if (!apply_step_units(ms, smem, a, tl, lh, c0, gu, n)) return;
     }
+    tmem_wait_st();
+    if (seam0 && !apply_step_units(ms, a, tl, lh, c0, gu, n)) return;
     tc_fence_before();
     named_sync(4);
     if (n == 0) mbar_arrive(&ms->a_ready);
@@ -616,12 +666,14 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
         const uint32_t g = gj + j;
         const int p = a.seg_idx[c0 + j];
         const int e = a.T_exp ? a.T_exp[p * LH + lh] : 0;
-        bool ok = wait_bar(&ms->d_done, g & 1, ms, a);
-        ok = ok && wait_bar(&ms->sp_full, g & 1, ms, a);
-        if (!wg_all(4, ok)) return;
-        tc_fence_after();
         const bool last = j + 1 == len;
         const bool seam = !last && step_units(a, c0 + j + 1, tb) > 0;
+        bool ok = wait_bar(&ms->d_done, g & 1, ms, a);
+        ok = ok && wait_bar(&ms->sp_full, g & 1, ms, a);
+        ok = ok && (!seam || wait_bar(&ms->seam_ready, gu & 1, ms, a));
+        if (!wg_all(4, ok)) return;
+        tc_fence_after();
+        gw = seam ? ms->g[kU - 1] : 0.f;
         // 2^e as two factors (each exact for |e| <= 252): T~ S 2^e underflows
         // only where it is negligible against S_p
         const float f1 = exp2f((float)(e / 2)), f2 = exp2f((float)(e - e / 2));
@@ -637,9 +689,7 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
                 if (last) out[i * kD + n] = v;
                 x[jj] = __float_as_uint(v);
             }
-            if (seam) {
-                tmem_st32(tl + TM_D + 32 * cb, x);
-            } else if (!last) {
+            if (!last) {
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
                     uint32_t h[16], l[16];
@@ -649,11 +699,16 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
                     tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
                 }
             }
+            if (seam) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(gw * __uint_as_float(x[jj]));
+                tmem_st32(tl + TM_D + 32 * cb, x);
+            }
         }
         tmem_wait_st();
         named_sync(4);
         if (n == 0) mbar_arrive(&ms->sp_empty);  // S_p has been read
-        if (seam && !apply_step_units(ms, smem, a, tl, lh, c0 + j + 1, gu, n)) return;
+        if (seam && !apply_step_units(ms, a, tl, lh, c0 + j + 1, gu, n)) return;
         if (!last) {
             tc_fence_before();
             named_sync(4);
@@ -771,6 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms->drain, 1);
         mbar_init(&ms->seam_ready, 1);
         mbar_init(&ms->seam_free, 1);
+        mbar_init(&ms->r_go, 1);
+        mbar_init(&ms->r_done, 1);
+        mbar_init(&ms->c_go, 1);
+        mbar_init(&ms->u_done, 1);
         ms->abort_flag = 0;
         fence_mbar_init();
     }
@@ -793,9 +852,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kWarpTMA) {
             if (lane == 0) producer_role(ms, smem, a, &tmT, &tmS, gs, gj, c0, len, lh, !kTrans);
         } else if (warp == kWarpMMA) {
-            if (lane == 0) mma_role(ms, smem, a, tmem, gs, gj, len);
+            if (lane == 0) mma_role<kSeam>(ms, smem, a, tmem, gs, gj, gu, c0, len);
         } else if (warp < kWarpEpi0) {
-            convert_role<kSeam>(ms, smem, a, gs, gu, c0, len, lh, tid - 32 * kWarpCvt0);
+            convert_role<kSeam>(ms, smem, a, tmem, gs, gu, c0, len, lh, tid - 32 * kWarpCvt0);
         } else if (kSeam) {
             epilogue_role_seam(ms, smem, a, tmem, gj, gu, c0, len, lh, obj, warp & 3, lane);
         } else if (kTrans) {

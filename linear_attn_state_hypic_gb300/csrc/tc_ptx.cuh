@@ -196,6 +196,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Shared-memory matrix descriptor of a K-major operand without swizzle: core
+// matrices of 8 rows x 16 bytes stored as 128 contiguous bytes; lbo = byte
+// distance between core matrices adjacent in K, sbo = between 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05 (swizzle field 0: none)
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16 / kind::tf32 with fp32
 // accumulation.  ab_fmt: 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32).
 // a_mn / b_mn: operand is MN-major (transposed) rather than K-major.
