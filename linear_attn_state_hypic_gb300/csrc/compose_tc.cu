@@ -51,17 +51,18 @@ constexpr uint32_t OFF_RING = 0;                                 // kRing x (hi 
 constexpr uint32_t OFF_SP = OFF_RING + kRing * 2 * kSliceBytes;  // S_p: 4 blocks [128 rows][32 cols] fp32
 // Reuse chain only: one seam unit (up to kU seam tokens).
 constexpr int kU = 8;
-// B operand of the unit's dot products (M = 128 state columns, N = 2 kU, K = 128):
-// rows 0..kU-1 = -W, rows kU..2kU-1 = g_t q_t, K-major with the 128-byte swizzle
-// in four 32-column slices of 2 KB; hi, then lo.
-constexpr uint32_t kWqSlice = 2 * kU * 128;                      // 16 rows x 128 B
-constexpr uint32_t kWqBytes = 4 * kWqSlice;                      // 8 KB
+// B operand of the unit's dot products (M = 128 state columns, K = 128): rows
+// 0..7 = -W hi, 8..15 = g_t q_t hi, 16..23 = -W lo, 24..31 = g_t q_t lo, K-major
+// with the 128-byte swizzle in four 32-column slices of 4 KB.  The hi operand
+// A_hi of the state takes all 32 rows (N = 32), its lo A_lo the first 16.
+constexpr uint32_t kWqSlice = 4 * kU * 128;                      // 32 rows x 128 B
+constexpr uint32_t kWqBytes = 4 * kWqSlice;                      // 16 KB
 constexpr uint32_t OFF_WQ = OFF_SP + 4 * kSliceBytes;
 // B operand of the unit's rank-kU update (N = 128 state rows, K = kU): K^T,
 // K-major without swizzle (core matrices of 8 rows x 4 values; the two K halves
 // 128 bytes apart, 8-row groups 256 bytes apart); hi, then lo.
 constexpr uint32_t kKtBytes = kD * kU * 4;                       // 4 KB
-constexpr uint32_t OFF_KT = OFF_WQ + 2 * kWqBytes;
+constexpr uint32_t OFF_KT = OFF_WQ + kWqBytes;
 // the unit's k and q rows, for its k.k and q.k products
 constexpr int kUR = kD + 4;                                      // row stride (floats): rows fall in distinct banks
 constexpr uint32_t kUnitRows = kU * kUR * 4;                     // [kU][kUR] fp32
@@ -74,8 +75,10 @@ struct Misc {
     uint64_t full[kRing], cvt[kRing], empty[kRing];
     uint64_t sp_full, sp_empty, d_done, a_ready, drain;
     uint64_t seam_ready, seam_free;  // unit operands written / consumed
-    uint64_t r_go, r_done;           // A = split x ready for the unit's dot products / products in TM_R
-    uint64_t c_go, u_done;           // C^T in TM_C / rank-kU update added to TM_D
+    // reuse chain: the 32 A columns (state rows) 32s..32s+31 split for the next compose / for the
+    // unit's dot products (one arrival per epilogue warp); the products in TM_R; C^T in TM_C;
+    // the rank-kU update added to TM_D
+    uint64_t a_go[kSlices], r_go[kSlices], r_done, c_go, u_done;
     // the current seam unit: tokens [tok0, tok0 + nv); g = in-unit decay prefix
     float kk[kU][kU], qk[kU][kU], th[kU][kU], thg[kU][kU];  // k.k then A, q.k, That, That Diag(g)
     float M[kU][kU];                 // (q_t . k_s) g_t / g_s, s <= t
@@ -91,12 +94,12 @@ constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t TM_D = 0, TM_AB = 128, TM_AS = 256;  // accumulator, A hi, A lo
-// Reuse chain: the seam unit's products (lane n: u'_s = U[s][n] - W_s . x in
-// columns 384..391, g_t q_t . x in 392..399) and its coefficients C^T (hi in
-// 400..407, lo in 408..415).
-constexpr uint32_t TM_R = 384, TM_C = 400;
+// Reuse chain: the seam unit's products, lane n: u'_s = U[s][n] - W_s . x is the
+// sum of columns 384 + s and 400 + s, g_s q_s . x that of 392 + s and 408 + s;
+// its coefficients C^T: hi in 416..423, lo in 424..431.
+constexpr uint32_t TM_R = 384, TM_C = 416;
 constexpr uint32_t ID_T = idesc(2, 128, 128, false, false);
-constexpr uint32_t ID_R = idesc(2, 128, 2 * kU, false, false);
+constexpr uint32_t ID_R32 = idesc(2, 128, 4 * kU, false, false), ID_R16 = idesc(2, 128, 2 * kU, false, false);
 
 struct CtArgs {
     int n_layers, n_heads, n_pairs, n_chains, n_items;
@@ -195,24 +198,25 @@ __device__ void producer_role(Misc* ms, uint8_t* smem, const CtArgs& a, const CU
 
 // Reuse chain: the MMAs of the seam units of step js (global unit counter gu).
 // Per unit: the dot products TM_R += x (-W; g q)^T over the split state in
-// TM_AB / TM_AS (3 x tf32, N = 2 kU, K = 128), then, once the epilogue has
-// written C^T, the rank-kU update TM_D += C^T K (3 x tf32, K = kU).
+// TM_AB / TM_AS (3 x tf32 as A_hi (B_hi; B_lo) + A_lo B_hi, K = 128), a K-slice
+// as soon as the epilogue has written it, then, once the epilogue has written
+// C^T, the rank-kU update TM_D += C^T K (3 x tf32, K = kU).
 __device__ bool mma_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, int js, uint32_t& gu) {
     int tb;
     const int nu = step_units(a, js, tb);
     const uint32_t wq = smem_u32(smem) + OFF_WQ, kt = smem_u32(smem) + OFF_KT;
     for (int k = 0; k < nu; ++k) {
-        if (!wait_bar(&ms->seam_ready, gu & 1, ms, a) || !wait_bar(&ms->r_go, gu & 1, ms, a)) return false;
-        tc_fence_after();
+        if (!wait_bar(&ms->seam_ready, gu & 1, ms, a)) return false;
 #pragma unroll 1
         for (int s = 0; s < kSlices; ++s) {
+            if (!wait_bar(&ms->r_go[s], gu & 1, ms, a)) return false;
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t b = wq + s * kWqSlice + kk * 32, acol = 32 * s + 8 * kk;
-                const uint64_t bh = sdesc_sw128(b, 0, 1024), bl = sdesc_sw128(b + kWqBytes, 0, 1024);
-                mma_tf32_ts(tmem + TM_R, tmem + TM_AB + acol, bh, ID_R, true);
-                mma_tf32_ts(tmem + TM_R, tmem + TM_AB + acol, bl, ID_R, true);
-                mma_tf32_ts(tmem + TM_R, tmem + TM_AS + acol, bh, ID_R, true);
+                const uint32_t acol = 32 * s + 8 * kk;
+                const uint64_t b = sdesc_sw128(wq + s * kWqSlice + kk * 32, 0, 1024);
+                mma_tf32_ts(tmem + TM_R, tmem + TM_AB + acol, b, ID_R32, true);
+                mma_tf32_ts(tmem + TM_R, tmem + TM_AS + acol, b, ID_R16, true);
             }
         }
         mma_commit(&ms->r_done);
@@ -234,10 +238,11 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem
     const uint32_t ring = smem_u32(smem) + OFF_RING;
     if (kSeam && len > 0 && !mma_units(ms, smem, a, tmem, c0, gu)) return;
     for (int j = 0; j < len; ++j) {
-        if (!wait_bar(&ms->a_ready, (gj + j) & 1, ms, a)) return;
+        if (!kSeam && !wait_bar(&ms->a_ready, (gj + j) & 1, ms, a)) return;
         tc_fence_after();
         for (int s = 0; s < kSlices; ++s) {
             const uint32_t gsi = gs + kSlices * j + s, buf = gsi % kRing;
+            if (kSeam && !wait_bar(&ms->a_go[s], (gj + j) & 1, ms, a)) return;
             if (!wait_bar(&ms->cvt[buf], (gsi / kRing) & 1, ms, a)) return;
             tc_fence_after();
             const uint32_t hi = ring + buf * 2 * kSliceBytes, lo = hi + kSliceBytes;
@@ -378,13 +383,12 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tme
 #pragma unroll
         for (int s2 = 0; s2 <= u; ++s2) w = fmaf(ms->thg[u][s2], kr[s2], w);
         uint32_t h, l;
-        const uint32_t ow = sw128_offset(u, t, 4, kWqSlice), oq = sw128_offset(kU + u, t, 4, kWqSlice);
         split_tf32(-w, h, l);
-        *reinterpret_cast<uint32_t*>(wq + ow) = h;
-        *reinterpret_cast<uint32_t*>(wq + kWqBytes + ow) = l;
+        *reinterpret_cast<uint32_t*>(wq + sw128_offset(u, t, 4, kWqSlice)) = h;
+        *reinterpret_cast<uint32_t*>(wq + sw128_offset(2 * kU + u, t, 4, kWqSlice)) = l;
         split_tf32(ms->g[u] * qr[u], h, l);
-        *reinterpret_cast<uint32_t*>(wq + oq) = h;
-        *reinterpret_cast<uint32_t*>(wq + kWqBytes + oq) = l;
+        *reinterpret_cast<uint32_t*>(wq + sw128_offset(kU + u, t, 4, kWqSlice)) = h;
+        *reinterpret_cast<uint32_t*>(wq + sw128_offset(3 * kU + u, t, 4, kWqSlice)) = l;
     }
     {  // row t of K^T, split hi/lo
         uint4 h0, l0, h1, l1;
@@ -398,17 +402,17 @@ __device__ bool prep_unit(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tme
         *reinterpret_cast<uint4*>(kt + kKtBytes) = l0;
         *reinterpret_cast<uint4*>(kt + kKtBytes + 128) = l1;
     }
-    {  // the products' starting value in lane fl: U[s][fl] = (That V)[s][fl], and 0 for g q . x
-        uint32_t r[2 * kU];
+    {  // the products' starting value in lane fl: U[s][fl] = (That V)[s][fl], and 0 elsewhere
+        uint32_t r[4 * kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             float uu = 0.f;
 #pragma unroll
             for (int s2 = 0; s2 <= u; ++s2) uu = fmaf(ms->th[u][s2], vr[s2], uu);
             r[u] = __float_as_uint(uu);
-            r[kU + u] = 0u;
+            r[kU + u] = r[2 * kU + u] = r[3 * kU + u] = 0u;
         }
-        tmem_st16(tmem + (lq << 16) + TM_R, r);
+        tmem_st32(tmem + (lq << 16) + TM_R, r);
         tmem_wait_st();
     }
     if (t == 0) {
@@ -436,28 +440,34 @@ __device__ bool prep_step_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32
     return true;
 }
 
-// One seam unit on the state, epilogue thread n = TMEM lane n = state column
-// n.  On entry TM_AB / TM_AS hold the column x split hi/lo and TM_D holds
-// g_w x.  The MMAs leave u'_s and g_s q_s . x in TM_R; this thread writes o_t
-// and C^T (c_s = (g_w/g_s) u'_s, split hi/lo) to TM_C, and the rank-kU MMAs
-// add K^T c to TM_D.
-__device__ bool seam_unit(Misc* ms, const CtArgs& a, uint32_t tl, int layer, int head, uint32_t gu, int n) {
+// This warp's TMEM stores are complete and ordered before the MMAs that
+// follow: one arrival (of the four epilogue warps') on bar.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+    tmem_wait_st();
     tc_fence_before();
-    named_sync(4);
-    if (n == 0) mbar_arrive(&ms->r_go);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+// One seam unit on the state, epilogue thread n = TMEM lane n = state column
+// n.  On entry TM_AB / TM_AS hold the column x split hi/lo (each K-slice
+// announced on r_go as it was written) and TM_D holds g_w x.  The MMAs leave
+// u'_s and g_s q_s . x in TM_R; this thread writes o_t and C^T (c_s =
+// (g_w/g_s) u'_s, split hi/lo) to TM_C, and the rank-kU MMAs add K^T c to TM_D.
+__device__ bool seam_unit(Misc* ms, const CtArgs& a, uint32_t tl, int layer, int head, uint32_t gu, int n) {
     if (!wg_all(4, wait_bar(&ms->r_done, gu & 1, ms, a))) return false;
     tc_fence_after();
-    uint32_t r[2 * kU];
-    tmem_ld16(tl + TM_R, r);
+    uint32_t r[4 * kU];
+    tmem_ld32(tl + TM_R, r);
     tmem_wait_ld();
     const int nv = ms->nv, tok0 = ms->tok0;
     float up[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) up[u] = __uint_as_float(r[u]);
+    for (int u = 0; u < kU; ++u) up[u] = __uint_as_float(r[u]) + __uint_as_float(r[2 * kU + u]);
     uint32_t cv[2 * kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-        float o = __uint_as_float(r[kU + u]);
+        float o = __uint_as_float(r[kU + u]) + __uint_as_float(r[3 * kU + u]);
 #pragma unroll
         for (int s2 = 0; s2 <= u; ++s2) o = fmaf(ms->M[u][s2], up[s2], o);
         if (u < nv) a.o_out[(((int64_t)layer * a.n_tokens + tok0 + u) * a.n_heads + head) * kD + n] = o;
@@ -474,32 +484,61 @@ __device__ bool seam_unit(Misc* ms, const CtArgs& a, uint32_t tl, int layer, int
     return true;
 }
 
-// TM_D -> the A operand, split hi/lo; with rescale also TM_D <- gw TM_D.
-__device__ void split_state(uint32_t tl, bool rescale, float gw) {
+// TM_D -> the A operand, split hi/lo, each K-slice announced as it is written.
+// rescale (another unit follows): also TM_D <- gw TM_D, slices on r_go.
+// Otherwise (the next compose follows, and its first MMA overwrites TM_D):
+// all of TM_D is read first, slices on a_go.
+__device__ void split_state(Misc* ms, uint32_t tl, bool rescale, float gw, int lane) {
+    if (rescale) {
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t x[32];
-        tmem_ld32(tl + TM_D + 32 * cb, x);
-        tmem_wait_ld();
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t x[32];
+            tmem_ld32(tl + TM_D + 32 * cb, x);
+            tmem_wait_ld();
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-            uint32_t h[16], l[16];
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t h[16], l[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]), h[jj], l[jj]);
-            tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
-            tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
-        }
-        if (rescale) {
+                for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]), h[jj], l[jj]);
+                tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
+                tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
+            }
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(gw * __uint_as_float(x[jj]));
             tmem_st32(tl + TM_D + 32 * cb, x);
+            warp_arrive(&ms->r_go[cb], lane);
+        }
+        return;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // two K-slices at a time
+        uint32_t x[2][32];
+        tmem_ld32(tl + TM_D + 64 * half, x[0]);
+        tmem_ld32(tl + TM_D + 64 * half + 32, x[1]);
+        tmem_wait_ld();
+        if (half == 1) {  // all of TM_D has been read
+            warp_arrive(&ms->a_go[0], lane);
+            warp_arrive(&ms->a_go[1], lane);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int cb = 2 * half + c;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t h[16], l[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[c][16 * hb + jj]), h[jj], l[jj]);
+                tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
+                tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
+            }
+            if (half == 1) warp_arrive(&ms->a_go[cb], lane);
         }
     }
-    tmem_wait_st();
 }
 
 // Applies the units of step js to the state; on entry as for seam_unit (the
-// first unit's g_w x in TM_D), on return the A operand of the next compose.
+// first unit's g_w x in TM_D), on return the A operand of the next compose,
+// announced on a_go.
 __device__ bool apply_step_units(Misc* ms, const CtArgs& a, uint32_t tl, int lh, int js, uint32_t& gu, int n) {
     int tb;
     const int nu = step_units(a, js, tb);
@@ -513,7 +552,7 @@ __device__ bool apply_step_units(Misc* ms, const CtArgs& a, uint32_t tl, int lh,
             if (!wg_all(4, wait_bar(&ms->seam_ready, gu & 1, ms, a))) return false;
             gw = ms->g[kU - 1];
         }
-        split_state(tl, more, gw);
+        split_state(ms, tl, more, gw, n & 31);
     }
     return true;
 }
@@ -617,8 +656,9 @@ __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t
 // Reuse-chain epilogue: as epilogue_role, with the seam units of step j + 1
 // applied to the composed column before it becomes the A operand of step
 // j + 1 (and those of step 0 to the start state).  Before a unit the column
-// goes to the A operand (split hi/lo, for the unit's dot products) and, times
-// the unit's g_w, to TM_D.
+// goes to the A operand (split hi/lo, for the unit's dot products, a K-slice
+// at a time on r_go) and, times the unit's g_w, to TM_D.  The A operand of a
+// compose is announced a K-slice at a time on a_go.
 __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gj, uint32_t gu,
                                    int c0, int len, int lh, int64_t obj, int q, int lane) {
     const int n = 32 * q + lane;
@@ -655,12 +695,9 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
             for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(gw * __uint_as_float(x[jj]));
             tmem_st32(tl + TM_D + 32 * cb, x);
         }
+        warp_arrive(seam0 ? &ms->r_go[cb] : &ms->a_go[cb], lane);
     }
-    tmem_wait_st();
     if (seam0 && !apply_step_units(ms, a, tl, lh, c0, gu, n)) return;
-    tc_fence_before();
-    named_sync(4);
-    if (n == 0) mbar_arrive(&ms->a_ready);
     const float* sp = reinterpret_cast<const float*>(smem + OFF_SP) + (n >> 5) * (kSliceBytes / 4) + (n & 31);
     for (int j = 0; j < len; ++j) {
         const uint32_t g = gj + j;
@@ -703,17 +740,15 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(gw * __uint_as_float(x[jj]));
                 tmem_st32(tl + TM_D + 32 * cb, x);
+                warp_arrive(&ms->r_go[cb], lane);
             }
         }
         tmem_wait_st();
+        if (!last && !seam)  // all of TM_D has been read: the next compose may overwrite it
+            for (int cb = 0; cb < 4; ++cb) warp_arrive(&ms->a_go[cb], lane);
         named_sync(4);
         if (n == 0) mbar_arrive(&ms->sp_empty);  // S_p has been read
         if (seam && !apply_step_units(ms, a, tl, lh, c0 + j + 1, gu, n)) return;
-        if (!last) {
-            tc_fence_before();
-            named_sync(4);
-            if (n == 0) mbar_arrive(&ms->a_ready);
-        }
     }
 }
 
@@ -826,7 +861,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms->drain, 1);
         mbar_init(&ms->seam_ready, 1);
         mbar_init(&ms->seam_free, 1);
-        mbar_init(&ms->r_go, 1);
+        for (int b = 0; b < kSlices; ++b) {
+            mbar_init(&ms->a_go[b], 4);
+            mbar_init(&ms->r_go[b], 4);
+        }
         mbar_init(&ms->r_done, 1);
         mbar_init(&ms->c_go, 1);
         mbar_init(&ms->u_done, 1);
