@@ -629,13 +629,15 @@ __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t
         for (int cb = 0; cb < 4; ++cb) {
             uint32_t x[32];
             tmem_ld32(tl + TM_D + 32 * cb, x);
+            float spv[32];  // (all loaded before any store: the stores to out could alias them)
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) spv[jj] = sp[(32 * cb + jj) * 32];
             tmem_wait_ld();
             uint32_t h[32], l[32];
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-                const int i = 32 * cb + jj;
-                const float v = ldexpf(__uint_as_float(x[jj]), e) + sp[i * 32];
-                if (last) out[i * kD + n] = v;
+                const float v = ldexpf(__uint_as_float(x[jj]), e) + spv[jj];
+                if (last) out[(32 * cb + jj) * kD + n] = v;
                 else split_tf32(v, h[jj], l[jj]);
             }
             if (!last) {
@@ -718,13 +720,15 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
         for (int cb = 0; cb < 4; ++cb) {
             uint32_t x[32];
             tmem_ld32(tl + TM_D + 32 * cb, x);
+            float spv[32];  // (all loaded before any store: the stores to out could alias them)
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) spv[jj] = sp[(32 * cb + jj) * 32];
             tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int i = 32 * cb + jj;
-                const float v = fmaf(__uint_as_float(x[jj]) * f1, f2, sp[i * 32]);
-                if (last) out[i * kD + n] = v;
-                x[jj] = __float_as_uint(v);
+            for (int jj = 0; jj < 32; ++jj) x[jj] = __float_as_uint(fmaf(__uint_as_float(x[jj]) * f1, f2, spv[jj]));
+            if (last) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) out[(32 * cb + jj) * kD + n] = __uint_as_float(x[jj]);
             }
             if (!last) {
 #pragma unroll

@@ -29,7 +29,7 @@ def B():
     return binding
 
 
-def make_case(seed, fam, L, H, d, n_pairs, chain_lens, widths, dtype, with_s0):
+def make_case(seed, fam, L, H, d, n_pairs, chain_lens, widths, dtype, with_s0, variant="faithful"):
     rng = np.random.default_rng(seed)
     n_chains = len(chain_lens)
     cu_chain = np.concatenate([[0], np.cumsum(chain_lens)]).astype(np.int32)
@@ -54,7 +54,7 @@ def make_case(seed, fam, L, H, d, n_pairs, chain_lens, widths, dtype, with_s0):
         q, k, v = (synth.round_bf16(x) for x in (q, k, v))
     gates = {}
     if fam == "gdn":
-        gates["alpha"], gates["beta"] = synth.gdn_gates(rng, (L, N, H))
+        gates["alpha"], gates["beta"] = synth.gdn_gates(rng, (L, N, H), variant)
     elif fam == "retnet":
         gates["gamma"] = rng.uniform(0.8, 0.99, (L, H)).astype(np.float32)
     elif fam == "gla":
@@ -114,6 +114,17 @@ def test_chain_fused_gdn_d128(B, dtype, with_s0):
     c = make_case(11, "gdn", L=2, H=3, d=128, n_pairs=5, chain_lens=[4, 0, 3, 1],
                   widths=[0, 8, 3, 17, 8, 1, 9, 0], dtype=dtype, with_s0=with_s0)
     check(B, "gdn", c, dtype, TOL_F32)
+
+
+@pytest.mark.parametrize("variant", ["faithful", "fastdecay"])
+def test_chain_fused_gdn_d128_gaps_and_full_units(B, variant):
+    """Steps without a seam inside a chain (the next compose takes the composed
+    column as it is), consecutive ones, windows of exactly one, two and three full
+    units, a chain that starts without a seam, and fast decay (alpha in
+    [0.05, 0.6]: a unit's decay down to ~1e-11)."""
+    c = make_case(14, "gdn", L=1, H=2, d=128, n_pairs=4, chain_lens=[6, 2],
+                  widths=[8, 0, 16, 0, 0, 24, 0, 5], dtype="f32", with_s0=True, variant=variant)
+    check(B, "gdn", c, "f32", TOL_F32)
 
 
 def test_chain_fused_matches_step_by_step_calls(B):
