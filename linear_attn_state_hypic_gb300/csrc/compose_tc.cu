@@ -232,17 +232,17 @@ __device__ bool mma_units(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tme
     return true;
 }
 
-template <bool kSeam>
+template <bool kSeam, bool kTrans>
 __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gs, uint32_t gj,
                          uint32_t gu, int c0, int len) {
     const uint32_t ring = smem_u32(smem) + OFF_RING;
     if (kSeam && len > 0 && !mma_units(ms, smem, a, tmem, c0, gu)) return;
     for (int j = 0; j < len; ++j) {
-        if (!kSeam && !wait_bar(&ms->a_ready, (gj + j) & 1, ms, a)) return;
+        if (kTrans && !wait_bar(&ms->a_ready, (gj + j) & 1, ms, a)) return;
         tc_fence_after();
         for (int s = 0; s < kSlices; ++s) {
             const uint32_t gsi = gs + kSlices * j + s, buf = gsi % kRing;
-            if (kSeam && !wait_bar(&ms->a_go[s], (gj + j) & 1, ms, a)) return;
+            if (!kTrans && !wait_bar(&ms->a_go[s], (gj + j) & 1, ms, a)) return;
             if (!wait_bar(&ms->cvt[buf], (gsi / kRing) & 1, ms, a)) return;
             tc_fence_after();
             const uint32_t hi = ring + buf * 2 * kSliceBytes, lo = hi + kSliceBytes;
@@ -590,7 +590,9 @@ __device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t 
     }
 }
 
-// Epilogue: thread n owns TMEM lane n = column n of the state.
+// Epilogue: thread n owns TMEM lane n = column n of the state.  The next
+// step's A operand is announced a K-slice at a time on a_go, once all of
+// TM_D has been read (the next compose's first MMA overwrites it).
 __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem, uint32_t gj, int c0, int len,
                               int lh, int64_t obj, int q, int lane) {
     const int n = 32 * q + lane;
@@ -602,19 +604,15 @@ __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t
         for (int i = 0; i < kD; ++i) out[i * kD + n] = s0 ? s0[i * kD + n] : 0.f;
         return;
     }
-    // A for the first step: the start state (column n), split hi/lo.
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {  // A for the first step: the start state (column n), split hi/lo
         uint32_t h[32], l[32];
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) split_tf32(s0 ? s0[(32 * cb + jj) * kD + n] : 0.f, h[jj], l[jj]);
         tmem_st32(tl + TM_AB + 32 * cb, h);
         tmem_st32(tl + TM_AS + 32 * cb, l);
+        warp_arrive(&ms->a_go[cb], lane);
     }
-    tmem_wait_st();
-    tc_fence_before();
-    named_sync(4);
-    if (n == 0) mbar_arrive(&ms->a_ready);
     const float* sp = reinterpret_cast<const float*>(smem + OFF_SP) + (n >> 5) * (kSliceBytes / 4) + (n & 31);
     for (int j = 0; j < len; ++j) {
         const uint32_t g = gj + j;
@@ -624,34 +622,51 @@ __device__ void epilogue_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t
         ok = ok && wait_bar(&ms->sp_full, g & 1, ms, a);
         if (!wg_all(4, ok)) return;
         tc_fence_after();
-        const bool last = j + 1 == len;
+        // 2^e as two factors (each exact for |e| <= 252)
+        const float f1 = exp2f((float)(e / 2)), f2 = exp2f((float)(e - e / 2));
+        if (j + 1 == len) {  // the end state
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tl + TM_D + 32 * cb, x);
+                float spv[32];  // (all loaded before any store: the stores to out could alias them)
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            uint32_t x[32];
-            tmem_ld32(tl + TM_D + 32 * cb, x);
-            float spv[32];  // (all loaded before any store: the stores to out could alias them)
+                for (int jj = 0; jj < 32; ++jj) spv[jj] = sp[(32 * cb + jj) * 32];
+                tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) spv[jj] = sp[(32 * cb + jj) * 32];
-            tmem_wait_ld();
-            uint32_t h[32], l[32];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const float v = ldexpf(__uint_as_float(x[jj]), e) + spv[jj];
-                if (last) out[(32 * cb + jj) * kD + n] = v;
-                else split_tf32(v, h[jj], l[jj]);
+                for (int jj = 0; jj < 32; ++jj)
+                    out[(32 * cb + jj) * kD + n] = fmaf(__uint_as_float(x[jj]) * f1, f2, spv[jj]);
             }
-            if (!last) {
-                tmem_st32(tl + TM_AB + 32 * cb, h);
-                tmem_st32(tl + TM_AS + 32 * cb, l);
+        } else {
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {  // two K-slices at a time
+                uint32_t x[2][32];
+                tmem_ld32(tl + TM_D + 64 * half, x[0]);
+                tmem_ld32(tl + TM_D + 64 * half + 32, x[1]);
+                tmem_wait_ld();
+                if (half == 1) {  // all of TM_D has been read
+                    warp_arrive(&ms->a_go[0], lane);
+                    warp_arrive(&ms->a_go[1], lane);
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int cb = 2 * half + c;
+                    float spv[32];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) spv[jj] = sp[(32 * cb + jj) * 32];
+                    uint32_t h[32], l[32];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        split_tf32(fmaf(__uint_as_float(x[c][jj]) * f1, f2, spv[jj]), h[jj], l[jj]);
+                    tmem_st32(tl + TM_AB + 32 * cb, h);
+                    tmem_st32(tl + TM_AS + 32 * cb, l);
+                    if (half == 1) warp_arrive(&ms->a_go[cb], lane);
+                }
             }
         }
         tmem_wait_st();
-        tc_fence_before();
         named_sync(4);
-        if (n == 0) {
-            mbar_arrive(&ms->sp_empty);
-            if (!last) mbar_arrive(&ms->a_ready);
-        }
+        if (n == 0) mbar_arrive(&ms->sp_empty);  // S_p has been read
     }
 }
 
@@ -894,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kWarpTMA) {
             if (lane == 0) producer_role(ms, smem, a, &tmT, &tmS, gs, gj, c0, len, lh, !kTrans);
         } else if (warp == kWarpMMA) {
-            if (lane == 0) mma_role<kSeam>(ms, smem, a, tmem, gs, gj, gu, c0, len);
+            if (lane == 0) mma_role<kSeam, kTrans>(ms, smem, a, tmem, gs, gj, gu, c0, len);
         } else if (warp < kWarpEpi0) {
             convert_role<kSeam>(ms, smem, a, tmem, gs, gu, c0, len, lh, tid - 32 * kWarpCvt0);
         } else if (kSeam) {
