@@ -50,7 +50,7 @@ SEAM_TOKEN_BYTES = 3 * 256 + 8 + 512  # per seam token-head: q, k, v bf16 in, a,
 # in, (segment, head) out).
 BUILD_TRAFFIC_RATIO = 820.18 / 837.89
 BUILD_IN_BYTES_PER_TOKEN_HEAD = 520   # k, v bf16 (2 x 256 B) + alpha, beta fp32
-COMPOSE_TABLE_DRAM_RATIO = 9.14 / 17.4  # DRAM / algorithmic bytes of the shared compose table (ncu)
+COMPOSE_TABLE_DRAM_RATIO = 8.042 / 17.381  # DRAM / algorithmic bytes of the shared compose table (ncu)
 BUILD_OUT_BYTES_PER_ITEM = 131_076    # T_C and S(C|0) fp32 (2 x 64 KB) + exponent
 
 
@@ -578,7 +578,7 @@ def time_compose_table(steps, device, n_layers=30, shared=True):
          "algorithmic_bytes": algo, "gbs_algorithmic": algo / (ms / 1e3) / 1e9}
     if shared:
         # DRAM bytes per algorithmic byte from an ncu capture of the same kernel on the 4-layer table
-        # (9.14 GB of DRAM traffic for 17.4 GB algorithmic): chains that share a (layer, head) pair
+        # (8.04 GB of DRAM traffic for 17.38 GB algorithmic): chains that share a (layer, head) pair
         # re-read it from L2
         r["dram_bytes_est"] = algo * COMPOSE_TABLE_DRAM_RATIO
         r["gbs_dram_est"] = r["dram_bytes_est"] / (ms / 1e3) / 1e9
