@@ -73,7 +73,7 @@ static_assert(OFF_WQ % 1024 == 0, "128-byte swizzle atoms are 1024-byte aligned"
 
 struct Misc {
     uint64_t full[kRing], cvt[kRing], empty[kRing];
-    uint64_t sp_full, sp_empty, d_done, a_ready, drain;
+    uint64_t sp_full, sp_empty, d_done, drain;
     uint64_t seam_ready, seam_free;  // unit operands written / consumed
     // reuse chain: the 32 A columns (state rows) 32s..32s+31 split for the next compose / for the
     // unit's dot products (one arrival per epilogue warp); the products in TM_R; C^T in TM_C;
@@ -238,11 +238,9 @@ __device__ void mma_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t tmem
     const uint32_t ring = smem_u32(smem) + OFF_RING;
     if (kSeam && len > 0 && !mma_units(ms, smem, a, tmem, c0, gu)) return;
     for (int j = 0; j < len; ++j) {
-        if (kTrans && !wait_bar(&ms->a_ready, (gj + j) & 1, ms, a)) return;
-        tc_fence_after();
         for (int s = 0; s < kSlices; ++s) {
             const uint32_t gsi = gs + kSlices * j + s, buf = gsi % kRing;
-            if (!kTrans && !wait_bar(&ms->a_go[s], (gj + j) & 1, ms, a)) return;
+            if (!wait_bar(&ms->a_go[s], (gj + j) & 1, ms, a)) return;
             if (!wait_bar(&ms->cvt[buf], (gsi / kRing) & 1, ms, a)) return;
             tc_fence_after();
             const uint32_t hi = ring + buf * 2 * kSliceBytes, lo = hi + kSliceBytes;
@@ -772,11 +770,16 @@ __device__ void epilogue_role_seam(Misc* ms, uint8_t* smem, const CtArgs& a, uin
 }
 
 // Chain-transition epilogue: the state is T_chain, from I, and each step
-// leaves T_p T_chain in TM_D.  It is brought back to a largest entry in
-// [1, 2) by a power of two (the 4 warps' maxima through shared memory), the
-// shift and the pair's exponent are added to T_chain's exponent, and the
-// result is split into the next step's A (the last step writes T_out and
-// T_exp_out).  Thread n owns column n.
+// leaves T_p T_chain in TM_D.  The stored state is kept near unit size by a
+// power of two: step j divides by 2^s_j with s_j the exponent of the largest
+// entry of the previous stored state (1 for I), so the stored entries stay
+// within a factor of about |T~_p| of 1, and T_chain = stored * 2^texp with
+// texp += e_p + s_j.  That takes one pass over the accumulator (scale, the
+// next maximum, the split into the next A, announced a K-slice at a time once
+// all of TM_D has been read).  The last step instead scales by the exponent
+// of its own maximum, so that T_out's largest entry lies in [1, 2), and writes
+// T_out and T_exp_out.  Thread n owns column n; the four warps' maxima meet in
+// shared memory.
 __device__ void epilogue_role_T(Misc* ms, const CtArgs& a, uint32_t tmem, uint32_t gj, int c0, int len, int lh,
                                 int64_t obj, int q, int lane) {
     const int n = 32 * q + lane;
@@ -798,12 +801,9 @@ __device__ void epilogue_role_T(Misc* ms, const CtArgs& a, uint32_t tmem, uint32
         }
         tmem_st32(tl + TM_AB + 32 * cb, h);
         tmem_st32(tl + TM_AS + 32 * cb, l);
+        warp_arrive(&ms->a_go[cb], lane);
     }
-    tmem_wait_st();
-    tc_fence_before();
-    named_sync(4);
-    if (n == 0) mbar_arrive(&ms->a_ready);
-    int texp = 0;
+    int texp = 0, shift = 0;  // shift: exponent of the stored state's largest entry
     for (int j = 0; j < len; ++j) {
         const uint32_t g = gj + j;
         const int p = a.seg_idx[c0 + j];
@@ -811,46 +811,66 @@ __device__ void epilogue_role_T(Misc* ms, const CtArgs& a, uint32_t tmem, uint32
         if (!wg_all(4, wait_bar(&ms->d_done, g & 1, ms, a))) return;
         tc_fence_after();
         float m = 0.f;
+        if (j + 1 == len) {  // the exact maximum, then T_out with its largest entry in [1, 2)
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-            uint32_t x[32];
-            tmem_ld32(tl + TM_D + 32 * cb, x);
-            tmem_wait_ld();
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tl + TM_D + 32 * cb, x);
+                tmem_wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) m = fmaxf(m, fabsf(__uint_as_float(x[jj])));
+                for (int jj = 0; jj < 32; ++jj) m = fmaxf(m, fabsf(__uint_as_float(x[jj])));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) ms->red[q] = m;
+            named_sync(4);
+            m = fmaxf(fmaxf(ms->red[0], ms->red[1]), fmaxf(ms->red[2], ms->red[3]));
+            const int er = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
+            const float sc = ldexpf(1.f, -er);
+            texp += e + er;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tl + TM_D + 32 * cb, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) out[(32 * cb + jj) * kD + n] = __uint_as_float(x[jj]) * sc;
+            }
+            break;
+        }
+        const float sc = ldexpf(1.f, -shift);
+        texp += e + shift;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {  // two K-slices at a time
+            uint32_t x[2][32];
+            tmem_ld32(tl + TM_D + 64 * half, x[0]);
+            tmem_ld32(tl + TM_D + 64 * half + 32, x[1]);
+            tmem_wait_ld();
+            if (half == 1) {  // all of TM_D has been read
+                warp_arrive(&ms->a_go[0], lane);
+                warp_arrive(&ms->a_go[1], lane);
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int cb = 2 * half + c;
+                uint32_t h[32], l[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const float y = __uint_as_float(x[c][jj]) * sc;
+                    m = fmaxf(m, fabsf(y));
+                    split_tf32(y, h[jj], l[jj]);
+                }
+                tmem_st32(tl + TM_AB + 32 * cb, h);
+                tmem_st32(tl + TM_AS + 32 * cb, l);
+                if (half == 1) warp_arrive(&ms->a_go[cb], lane);
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) ms->red[q] = m;
-        named_sync(4);
+        named_sync(4);  // (the next step's first barrier orders these reads before the next writes)
         m = fmaxf(fmaxf(ms->red[0], ms->red[1]), fmaxf(ms->red[2], ms->red[3]));
-        const int er = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
-        const float sc = ldexpf(1.f, -er);
-        texp += e + er;
-        const bool last = j + 1 == len;
-#pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
-            uint32_t x[32];
-            tmem_ld32(tl + TM_D + 32 * cb, x);
-            tmem_wait_ld();
-            if (last) {
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) out[(32 * cb + jj) * kD + n] = __uint_as_float(x[jj]) * sc;
-            } else {
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t h[16], l[16];
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) split_tf32(__uint_as_float(x[16 * hb + jj]) * sc, h[jj], l[jj]);
-                    tmem_st16(tl + TM_AB + 32 * cb + 16 * hb, h);
-                    tmem_st16(tl + TM_AS + 32 * cb + 16 * hb, l);
-                }
-            }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        named_sync(4);  // (also: every warp has read the maxima before the next step rewrites them)
-        if (!last && n == 0) mbar_arrive(&ms->a_ready);
+        shift = (m > 0.f && m < INFINITY) ? ilogbf(m) : 0;
     }
     if (n == 0) a.T_exp_out[obj] = texp;
 }
@@ -876,7 +896,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms->sp_full, 1);
         mbar_init(&ms->sp_empty, 1);
         mbar_init(&ms->d_done, 1);
-        mbar_init(&ms->a_ready, 1);
         mbar_init(&ms->drain, 1);
         mbar_init(&ms->seam_ready, 1);
         mbar_init(&ms->seam_free, 1);
