@@ -210,10 +210,6 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
     hi = __byte_perm(hx, hy, 0x7632);
     lo = pack_bf16(x - __uint_as_float(hx), y - __uint_as_float(hy));
 }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
 // x rounded to tf32 (nearest, ties away from zero) by integer arithmetic on
 // its bits: add half a tf32 unit of the last place, then clear the 13 low bits.
 __device__ __forceinline__ float tf32_round(float x) {
@@ -645,10 +641,12 @@ __device__ void convert_w(uint8_t* smem, uint32_t tmem, int q, int lane) {
     }
 }
 
-// End of an item: T_C = mantissa * 2^exp with the mantissa's largest entry in
-// [1, 2), from D''_T and its scale 2^F; S(C|0) as is (the last chunk ends at
-// the true scale).  Thread n writes column n (coalesced across the warp).
-__device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, float F, uint32_t tmem, int q, int lane) {
+// End of an item, T half: T_C = mantissa * 2^exp with the mantissa's largest
+// entry in [1, 2), from D''_T and its scale 2^F.  Each 32-column chunk of
+// D''_T is reset to the identity's as soon as it has been read, so that the
+// next item may start on it.  Thread n writes column n (coalesced across the
+// warp).
+__device__ void state_epilogue_T(Misc* ms, const TcArgs& a, int64_t obj, float F, uint32_t tmem, int q, int lane) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
     const float m = state_reduce_max(row_absmax(tl + TM_DT), ms->red, q, lane);
@@ -658,23 +656,35 @@ __device__ void state_epilogue(Misc* ms, const TcArgs& a, int64_t obj, float F, 
     const int ef = (ms_ > 0.f && ms_ < INFINITY) ? ilogbf(ms_) : 0;
     const float f = ldexpf(sc, -ef);
     float* T = a.T_out + obj * kD * kD;
-    float* S = a.S_out + obj * kD * kD;
-    uint32_t x[32];
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32], id[32];
         tmem_ld32(tl + TM_DT + 32 * cb, x);
         tmem_wait_ld();
 #pragma unroll
+        for (int j = 0; j < 32; ++j) id[j] = (32 * cb + j == n) ? 0x3f800000u : 0u;
+        tmem_st32(tl + TM_DT + 32 * cb, id);
+#pragma unroll
         for (int j = 0; j < 32; ++j) T[(32 * cb + j) * kD + n] = __uint_as_float(x[j]) * f;
     }
+    tmem_wait_st();
+    if (n == 0) a.T_exp[obj] = (int)Fi + ef;
+}
+// S half: S(C|0) as is (the last chunk ends at the true scale).  D''_S is not
+// reset: an item's first chunk skips GEMM1 of the S half (X_S = U~, as S
+// starts at 0) and its first GEMM2 MMA overwrites D''_S.
+__device__ void state_epilogue_S(const TcArgs& a, int64_t obj, uint32_t tmem, int q, int lane) {
+    const int n = 32 * q + lane;
+    const uint32_t tl = tmem + ((32u * q) << 16);
+    float* S = a.S_out + obj * kD * kD;
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32];
         tmem_ld32(tl + TM_DS + 32 * cb, x);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[(32 * cb + j) * kD + n] = __uint_as_float(x[j]);
     }
-    if (n == 0) a.T_exp[obj] = (int)Fi + ef;
 }
 
 // All n threads of named barrier `id` agree: true only if every one passed true.
@@ -807,13 +817,16 @@ __device__ void issue_s_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t 
         }
         mma_commit(&ms->emptyV[gc % kVStages]);
         mma_commit(&ms->bt_free[gc & 1]);
-        // GEMM1 (tf32, A = the state in tensor memory): X_S += D''_S (-W^)^T
-        if (!issuer_wait(&ms->w_cvt[gc & 1], (gc >> 1) & 1, ms, a)) return;
-        if (!issuer_wait(&ms->pre_done, gc & 1, ms, a)) return;
-        tc_fence_after();
+        // GEMM1 (tf32, A = the state in tensor memory): X_S += D''_S (-W^)^T; not in an item's first
+        // chunk, where S is 0 (and D''_S may still be being written out)
+        if (c > 0) {
+            if (!issuer_wait(&ms->w_cvt[gc & 1], (gc >> 1) & 1, ms, a)) return;
+            if (!issuer_wait(&ms->pre_done, gc & 1, ms, a)) return;
+            tc_fence_after();
 #pragma unroll 4
-        for (int k = 0; k < 16; ++k)
-            mma_tf32_ts(tmem + TM_XS, tmem + TM_DS + 8 * k, bw + 512 * (k >> 2) + 2 * (k & 3), ID_G1, true);
+            for (int k = 0; k < 16; ++k)
+                mma_tf32_ts(tmem + TM_XS, tmem + TM_DS + 8 * k, bw + 512 * (k >> 2) + 2 * (k & 3), ID_G1, true);
+        }
         mma_commit(&ms->x_done_s);
         // GEMM2 (bf16, A = the pass's output in tensor memory): D''_S += X_S K
         if (!issuer_wait(&ms->y_ready_s, gc & 1, ms, a)) return;
@@ -821,7 +834,8 @@ __device__ void issue_s_role(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t 
         {
             const uint64_t kt = sdesc_sw128(sb + OFF_K + (gc % kKStages) * kTile, 8192, 1024);
 #pragma unroll 1
-            for (int k = 0; k < 4; ++k) mma_bf16_ts(tmem + TM_DS, tmem + TM_XS + 8 * k, kt + 128 * k, ID_G2S, true);
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_ts(tmem + TM_DS, tmem + TM_XS + 8 * k, kt + 128 * k, ID_G2S, c > 0 || k > 0);
         }
         mma_commit(&ms->d_ready_s);
         mma_commit(&ms->emptyK[gc % kKStages]);
@@ -963,13 +977,16 @@ __device__ void convert_next_w(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_
     }
 }
 
+// first_ready: pre_done of the item's first chunk already signalled (by the
+// previous item's epilogue); on return, whether this item's epilogue signalled
+// that of the next item's first chunk.
 __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tmem, const ItemSlot& it, ItemSlot& next,
-                           int k, int q, int lane) {
+                           int k, int q, int lane, bool& first_ready) {
     const int n = 32 * q + lane;
     const uint32_t tl = tmem + ((32u * q) << 16);
     int E = 0;
     float sum_lc = 0.f;
-    bool ready = false;  // pre_done of the current chunk already signalled
+    bool ready = first_ready;  // pre_done of the current chunk already signalled
     for (int c = 0; c < it.nc; ++c) {
         const uint32_t gc = it.g + c;
         const int slot = gc % kGateSlots;
@@ -1037,8 +1054,14 @@ __device__ bool state_item(Misc* ms, uint8_t* smem, const TcArgs& a, uint32_t tm
     ok = ok && wait_bar(&ms->d_ready_t, last & 1, ms, a);
     if (!wg_all(2, ok)) return false;
     tc_fence_after();
-    state_epilogue(ms, a, it.obj, (float)E + sum_lc, tmem, q, lane);
-    state_init(tmem, q, lane);  // (I, 0) for the next item
+    state_epilogue_T(ms, a, it.obj, (float)E + sum_lc, tmem, q, lane);
+    // D''_T is the identity's again: the next item's first chunk may start (its first chunk never
+    // renormalises), while S is written out
+    tc_fence_before();
+    named_sync(2);
+    first_ready = next.nc > 0;
+    if (first_ready && n == 0) mbar_arrive(&ms->pre_done);
+    state_epilogue_S(a, it.obj, tmem, q, lane);
     return true;
 }
 
@@ -1103,8 +1126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 32 * kWarpState0) mbar_arrive(&ms->slot_read[0]);
             if (it.nc > 0) convert_next_w(ms, smem, a, tmem, it.g, q, lane, ok);
         }
+        bool first_ready = false;
         for (int k = 0; ok && it.nc > 0; ++k) {
-            if (!state_item(ms, smem, a, tmem, it, next, k, q, lane)) break;
+            if (!state_item(ms, smem, a, tmem, it, next, k, q, lane, first_ready)) break;
             it = next;
             if (*(volatile int*)&ms->abort_flag) break;
         }
