@@ -48,7 +48,7 @@ SEAM_TOKEN_BYTES = 3 * 256 + 8 + 512  # per seam token-head: q, k, v bf16 in, a,
 # when the kernel ends is not counted as written); the full launch is too
 # large to capture, and its traffic scales with the same units (token-heads
 # in, (segment, head) out).
-BUILD_TRAFFIC_RATIO = 820.18 / 837.89
+BUILD_TRAFFIC_RATIO = 819.81 / 837.89
 BUILD_IN_BYTES_PER_TOKEN_HEAD = 520   # k, v bf16 (2 x 256 B) + alpha, beta fp32
 COMPOSE_TABLE_DRAM_RATIO = 8.042 / 17.381  # DRAM / algorithmic bytes of the shared compose table (ncu)
 BUILD_OUT_BYTES_PER_ITEM = 131_076    # T_C and S(C|0) fp32 (2 x 64 KB) + exponent
