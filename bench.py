@@ -633,6 +633,50 @@ def time_reuse_chain(steps, warmup, device, n_layers=30, H=32, d=128, n_steps=77
             "ms_per_call": ms, "algorithmic_bytes": algo, "gbs_algorithmic": algo / (ms / 1e3) / 1e9}
 
 
+def time_seam_advance(steps, warmup, device, n_layers=30, H=32, d=128, n_seams=76, w=8):
+    """hypic_seam_advance on the long request's seams (GDN, d=128, bf16 q/k/v,
+    fp32 gates): n_seams windows of w tokens for every (layer, head), each state
+    advanced in place.  Algorithmic bytes: the state read and written
+    (2 x 65,536 B per seam-head), q, k, v (bf16) and alpha, beta (fp32) per
+    token-head in, o (fp32) out.  Returns timing and the algorithmic-byte rate."""
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    N = n_seams * w
+    def rows():
+        x = torch.randn((n_layers, N, H, d), generator=g, device=device)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    q, k = rows(), rows()
+    v = torch.randn((n_layers, N, H, d), generator=g, device=device).to(torch.bfloat16)
+    alpha = 0.85 + 0.15 * torch.rand((n_layers, N, H), generator=g, device=device)
+    beta = torch.rand((n_layers, N, H), generator=g, device=device)
+    state = torch.randn((n_seams, n_layers, H, d, d), generator=g, device=device) / d ** 0.5
+    o = torch.empty((n_layers, N, H, d), dtype=torch.float32, device=device)
+    cu = np.arange(0, N + 1, w, dtype=np.int32)
+    cu_dev = torch.from_numpy(cu).to(device)
+    sp = torch.cuda.current_stream().cuda_stream
+    for _ in range(warmup):
+        B.seam_advance("gdn", q, k, v, cu, alpha=alpha, beta=beta, state_in=state, state_out=state, o_out=o,
+                       stream=sp, cu_seam_dev=cu_dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        B.seam_advance("gdn", q, k, v, cu, alpha=alpha, beta=beta, state_in=state, state_out=state, o_out=o,
+                       stream=sp, cu_seam_dev=cu_dev)
+    e1.record()
+    torch.cuda.synchronize()
+    B.check_device(sp)
+    ms = e0.elapsed_time(e1) / steps
+    seam_heads = n_seams * n_layers * H
+    algo = seam_heads * 2 * d * d * 4 + N * n_layers * H * (3 * d * 2 + 8 + d * 4)
+    return {"workload": (f"seam advance: {n_seams} windows of {w} tokens x {n_layers} layers x {H} heads, "
+                         f"GDN d={d}, bf16 q/k/v, state in place"),
+            "ms_per_call": ms, "seam_heads_per_s": seam_heads / (ms / 1e3), "algorithmic_bytes": algo,
+            "gbs_algorithmic": algo / (ms / 1e3) / 1e9}
+
+
 def time_decay_build(family, steps, warmup, device, n_layers=30, H=32, d=128, n_tokens=100_000):
     """hypic_segment_build of a decay family (retnet, mamba2, gla, vanilla) over
     the long request's segments (100k tokens, U[512,2048] lengths, no seam
@@ -697,6 +741,7 @@ def run_case(args, device):
                     heads, d=128, bf16 (one layer);
     compose_table -- hypic_compose on the compose table with --layers layers;
     reuse_chain -- hypic_reuse_chain over the long request's chain;
+    seam_advance -- hypic_seam_advance on the long request's seams (GDN);
     decay_build -- a decay family's build at serving scale (--family)."""
     import torch
     from linear_attn_state_hypic_gb300 import binding as B
@@ -710,6 +755,11 @@ def run_case(args, device):
         return
     if args.case == "decay_build":
         r = time_decay_build(args.family, args.steps, args.warmup, device, n_layers=args.layers)
+        r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
+        print(json.dumps({"case": args.case, **r}))
+        return
+    if args.case == "seam_advance":
+        r = time_seam_advance(args.steps, args.warmup, device, n_layers=args.layers)
         r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
         print(json.dumps({"case": args.case, **r}))
         return
@@ -769,7 +819,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--no-compose-table", action="store_true")
-    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table", "reuse_chain", "decay_build"],
+    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table", "reuse_chain", "decay_build",
+                                      "seam_advance"],
                     default="long_request",
                     help="long_request is the benchmark; the others time one kernel (for profiling)")
     ap.add_argument("--layers", type=int, default=30, help="layers of the compose_table, reuse_chain, decay_build cases")
