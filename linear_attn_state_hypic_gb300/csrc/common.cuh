@@ -42,12 +42,26 @@ __device__ __forceinline__ int64_t tok_row(int layer, int64_t tok, int head, int
 
 // Stage rows [t0, t0 + n) of one (layer, head) of a [L][N][H][D] array into
 // shared memory as f32, dst[t][0..D).  All threads of the block take part.
+// A thread issues kBatch loads before it stores any of them: a store could
+// alias a later load for the compiler, which would otherwise wait for each
+// load in turn.
 template <int D>
 __device__ __forceinline__ void stage_rows(float* dst, const void* src, int dt, int layer, int64_t t0, int n,
                                            int head, int64_t n_tokens, int H) {
-    for (int e = threadIdx.x; e < n * D; e += blockDim.x) {
-        const int t = e / D, i = e % D;
-        dst[e] = load_in(src, dt, tok_row(layer, t0 + t, head, n_tokens, H) * D + i);
+    constexpr int kBatch = 8;
+    const int total = n * D, step = blockDim.x;
+    for (int e0 = threadIdx.x; e0 < total; e0 += kBatch * step) {
+        float x[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int e = e0 + b * step;
+            x[b] = e < total ? load_in(src, dt, tok_row(layer, t0 + e / D, head, n_tokens, H) * D + e % D) : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int e = e0 + b * step;
+            if (e < total) dst[e] = x[b];
+        }
     }
 }
 
