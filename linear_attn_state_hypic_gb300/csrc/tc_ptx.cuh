@@ -103,6 +103,25 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
 }
 
 // ---------------------------------------------------------------- fences --
+// Contiguous copy global -> shared by the bulk-copy engine; its bytes
+// complete on bar (which expects them).  Addresses and size: multiples of 16.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+// Asynchronous copies global -> shared of 16 or 4 bytes by the issuing thread
+// (completed by cp_async_wait_all of the same thread).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_async_smem() {  // generic-proxy smem writes -> async proxy (MMA, TMA)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
