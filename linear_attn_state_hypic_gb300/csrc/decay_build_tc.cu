@@ -204,15 +204,25 @@ __device__ void dec_producer(DecMisc* ms, uint8_t* smem, const DecArgs& a, const
 // Weighted keys of one chunk, K~ = hi + lo (bf16 pair, same swizzled layout as
 // the key tile): 16-byte chunk q of the tile holds features i0..i0+7 of token
 // t.  wt(m, t, i0, f[8]) fills the eight weights of the thread's m-th piece.
+// The four pieces' keys and weights are all read before any store (a store
+// could alias a later read for the compiler and hold it back).
 template <typename WF>
 __device__ __forceinline__ void form_kt(const uint8_t* ktile, uint8_t* hi, uint8_t* lo, int w, WF wt) {
+    uint4 xk[4];
+    float fk[4][8];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const int q = w + kWorkers * m, t = q >> 4, cc = q & 15;
         const uint32_t off = (cc >> 3) * 8192 + t * 128 + ((((uint32_t)cc & 7) ^ (t & 7)) << 4);
-        const uint4 x = *reinterpret_cast<const uint4*>(ktile + off);
-        float f[8];
-        wt(m, t, 64 * (cc >> 3) + 8 * (cc & 7), f);
+        xk[m] = *reinterpret_cast<const uint4*>(ktile + off);
+        wt(m, t, 64 * (cc >> 3) + 8 * (cc & 7), fk[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int q = w + kWorkers * m, t = q >> 4, cc = q & 15;
+        const uint32_t off = (cc >> 3) * 8192 + t * 128 + ((((uint32_t)cc & 7) ^ (t & 7)) << 4);
+        const uint4 x = xk[m];
+        const float* f = fk[m];
         const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
         uint32_t h[4], l[4];
 #pragma unroll
