@@ -568,10 +568,13 @@ __device__ void convert_role(Misc* ms, uint8_t* smem, const CtArgs& a, uint32_t 
             if (!wg_all(3, wait_bar(&ms->full[buf], (gsi / kRing) & 1, ms, a))) return;
             uint8_t* hi = smem + OFF_RING + buf * 2 * kSliceBytes;
             uint8_t* lo = hi + kSliceBytes;
+            float4 xs[8];  // (all read before any store: the stores could alias the reads for the compiler)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) xs[k] = *reinterpret_cast<const float4*>(hi + k * 2048 + t * 16);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t off = k * 2048 + t * 16;
-                const float4 x = *reinterpret_cast<const float4*>(hi + off);
+                const float4 x = xs[k];
                 uint4 h, l;
                 split_tf32(x.x, h.x, l.x);
                 split_tf32(x.y, h.y, l.y);
