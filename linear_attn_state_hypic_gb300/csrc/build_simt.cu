@@ -109,25 +109,51 @@ __global__ void __launch_bounds__(DK + DV) gdn_build_simt_kernel(BuildParams p, 
         stage_gate(bs, p.beta, layer, t0, n, head, p.n_tokens, p.n_heads, 1.f);
         __syncthreads();
         for (int t = 0; t < n; ++t) {
-            const float* kt = ks + t * DK;
-            if (kda) {
-                const float* gt = gs + t * DK;
-#pragma unroll
-                for (int i = 0; i < DK; ++i) col[i] *= gt[i];
-            }
+            const float4* kt = reinterpret_cast<const float4*>(ks + t * DK);
             float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+            if (kda) {  // the per-channel gate applied to the column as the dot product reads it
+                const float4* gt = reinterpret_cast<const float4*>(gs + t * DK);
 #pragma unroll
-            for (int i = 0; i < DK; i += 4) {
-                u0 = fmaf(kt[i], col[i], u0);
-                u1 = fmaf(kt[i + 1], col[i + 1], u1);
-                u2 = fmaf(kt[i + 2], col[i + 2], u2);
-                u3 = fmaf(kt[i + 3], col[i + 3], u3);
+                for (int i = 0; i < DK / 4; ++i) {
+                    const float4 k4 = kt[i], g4 = gt[i];
+                    col[4 * i] *= g4.x, col[4 * i + 1] *= g4.y, col[4 * i + 2] *= g4.z, col[4 * i + 3] *= g4.w;
+                    u0 = fmaf(k4.x, col[4 * i], u0);
+                    u1 = fmaf(k4.y, col[4 * i + 1], u1);
+                    u2 = fmaf(k4.z, col[4 * i + 2], u2);
+                    u3 = fmaf(k4.w, col[4 * i + 3], u3);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < DK / 4; ++i) {
+                    const float4 k4 = kt[i];
+                    u0 = fmaf(k4.x, col[4 * i], u0);
+                    u1 = fmaf(k4.y, col[4 * i + 1], u1);
+                    u2 = fmaf(k4.z, col[4 * i + 2], u2);
+                    u3 = fmaf(k4.w, col[4 * i + 3], u3);
+                }
             }
             const float u = (u0 + u1) + (u2 + u3);
             const float a = kda ? 1.f : as[t], b = bs[t];
             const float w = isT ? -a * b * u : b * (vs[t * DV + (c - DK)] - a * u);
+            if (kda) {
 #pragma unroll
-            for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], w, a * col[i]);
+                for (int i = 0; i < DK / 4; ++i) {
+                    const float4 k4 = kt[i];
+                    col[4 * i] = fmaf(k4.x, w, col[4 * i]);
+                    col[4 * i + 1] = fmaf(k4.y, w, col[4 * i + 1]);
+                    col[4 * i + 2] = fmaf(k4.z, w, col[4 * i + 2]);
+                    col[4 * i + 3] = fmaf(k4.w, w, col[4 * i + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < DK / 4; ++i) {
+                    const float4 k4 = kt[i];
+                    col[4 * i] = fmaf(k4.x, w, a * col[4 * i]);
+                    col[4 * i + 1] = fmaf(k4.y, w, a * col[4 * i + 1]);
+                    col[4 * i + 2] = fmaf(k4.z, w, a * col[4 * i + 2]);
+                    col[4 * i + 3] = fmaf(k4.w, w, a * col[4 * i + 3]);
+                }
+            }
         }
         float m = 0.f;
         if (isT)
