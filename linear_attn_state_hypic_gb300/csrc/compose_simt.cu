@@ -50,21 +50,31 @@ __global__ void __launch_bounds__(2 * D) compose_gdn_simt_kernel(ComposeParams p
         __syncthreads();
         const int ex = p.T_exp_tab ? p.T_exp_tab[pobj] : 0;
         const float* Sp = p.S_tab + pobj * D * D;
-        for (int i = 0; i < D; ++i) {
-            const float* Ti = Ts + i * D;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        constexpr int kRows = D < 16 ? D : 16;  // rows a batch: their S_p values loaded before any store
+#pragma unroll 1
+        for (int i0 = 0; i0 < D; i0 += kRows) {
+            float spv[kRows];
 #pragma unroll
-            for (int m = 0; m < D; m += 4) {
-                a0 = fmaf(Ti[m], col[m], a0);
-                a1 = fmaf(Ti[m + 1], col[m + 1], a1);
-                a2 = fmaf(Ti[m + 2], col[m + 2], a2);
-                a3 = fmaf(Ti[m + 3], col[m + 3], a3);
+            for (int r = 0; r < kRows; ++r) spv[r] = isT ? 0.f : Sp[(i0 + r) * D + c];
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const int i = i0 + r;
+                const float4* Ti = reinterpret_cast<const float4*>(Ts + i * D);
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                for (int m = 0; m < D / 4; ++m) {
+                    const float4 t4 = Ti[m];
+                    a0 = fmaf(t4.x, col[4 * m], a0);
+                    a1 = fmaf(t4.y, col[4 * m + 1], a1);
+                    a2 = fmaf(t4.z, col[4 * m + 2], a2);
+                    a3 = fmaf(t4.w, col[4 * m + 3], a3);
+                }
+                const float acc = (a0 + a1) + (a2 + a3);
+                if (isT)
+                    Tn[i * D + c] = acc;
+                else
+                    Sn[i * D + c] = ldexpf(acc, ex) + spv[r];
             }
-            const float acc = (a0 + a1) + (a2 + a3);
-            if (isT)
-                Tn[i * D + c] = acc;
-            else
-                Sn[i * D + c] = ldexpf(acc, ex) + Sp[i * D + c];
         }
 #pragma unroll
         for (int i = 0; i < D; ++i) col[i] = (isT ? Tn : Sn)[i * D + c];
