@@ -38,17 +38,43 @@ __global__ void __launch_bounds__(128) rope_kernel(RopeParams p) {
         sn[tid] = (float)sin(a);
     }
     __syncthreads();
+    // (loads are issued kB at a time before their stores: a store could alias a later load for
+    // the compiler, which would otherwise wait for each load in turn)
+    constexpr int kB = 8;
     if (tid < dv) {  // S <- R S: thread j rotates column j
         float* S = p.S + obj * dk * dv;
-        for (int i = 0; i < h; ++i) {
-            const float x1 = S[(int64_t)i * dv + tid], x2 = S[(int64_t)(i + h) * dv + tid];
-            S[(int64_t)i * dv + tid] = x1 * cs[i] - x2 * sn[i];
-            S[(int64_t)(i + h) * dv + tid] = x2 * cs[i] + x1 * sn[i];
+        for (int i0 = 0; i0 < h; i0 += kB) {
+            float x1[kB], x2[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b)
+                if (i0 + b < h) {
+                    x1[b] = S[(int64_t)(i0 + b) * dv + tid];
+                    x2[b] = S[(int64_t)(i0 + b + h) * dv + tid];
+                }
+#pragma unroll
+            for (int b = 0; b < kB; ++b)
+                if (i0 + b < h) {
+                    const int i = i0 + b;
+                    S[(int64_t)i * dv + tid] = x1[b] * cs[i] - x2[b] * sn[i];
+                    S[(int64_t)(i + h) * dv + tid] = x2[b] * cs[i] + x1[b] * sn[i];
+                }
         }
     }
     if (!p.T) return;
     float* T = p.T + obj * dk * dk;
-    for (int e = tid; e < dk * dk; e += blockDim.x) Ts[(e / dk) * ld + e % dk] = T[e];
+    for (int e0 = tid; e0 < dk * dk; e0 += kB * blockDim.x) {
+        float x[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int e = e0 + b * blockDim.x;
+            if (e < dk * dk) x[b] = T[e];
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int e = e0 + b * blockDim.x;
+            if (e < dk * dk) Ts[(e / dk) * ld + e % dk] = x[b];
+        }
+    }
     __syncthreads();
     if (tid < dk)  // rows: R T (thread j, column j)
         for (int i = 0; i < h; ++i) {
