@@ -217,19 +217,28 @@ __global__ void __launch_bounds__(DK > DV ? DK : DV) decay_build_simt_kernel(Bui
         __syncthreads();
         if (c < DV) {
             for (int t = 0; t < n; ++t) {
-                const float* kt = ks + t * DK;
+                const float4* kt = reinterpret_cast<const float4*>(ks + t * DK);
                 const float vj = vs[t * DV + c];
                 if (fam == kGLA) {
-                    const float* gt = gs + t * DK;
+                    const float4* gt = reinterpret_cast<const float4*>(gs + t * DK);
 #pragma unroll
-                    for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, gt[i] * col[i]);
-                } else if (fam == kMAMBA2) {
-                    const float at = as[t];
+                    for (int i = 0; i < DK / 4; ++i) {
+                        const float4 k4 = kt[i], g4 = gt[i];
+                        col[4 * i] = fmaf(k4.x, vj, g4.x * col[4 * i]);
+                        col[4 * i + 1] = fmaf(k4.y, vj, g4.y * col[4 * i + 1]);
+                        col[4 * i + 2] = fmaf(k4.z, vj, g4.z * col[4 * i + 2]);
+                        col[4 * i + 3] = fmaf(k4.w, vj, g4.w * col[4 * i + 3]);
+                    }
+                } else {  // Mamba2 (a_t), RetNet (gamma), vanilla (1)
+                    const float d = fam == kMAMBA2 ? as[t] : gm;
 #pragma unroll
-                    for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, at * col[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < DK; ++i) col[i] = fmaf(kt[i], vj, gm * col[i]);
+                    for (int i = 0; i < DK / 4; ++i) {
+                        const float4 k4 = kt[i];
+                        col[4 * i] = fmaf(k4.x, vj, d * col[4 * i]);
+                        col[4 * i + 1] = fmaf(k4.y, vj, d * col[4 * i + 1]);
+                        col[4 * i + 2] = fmaf(k4.z, vj, d * col[4 * i + 2]);
+                        col[4 * i + 3] = fmaf(k4.w, vj, d * col[4 * i + 3]);
+                    }
                 }
             }
         }
