@@ -119,6 +119,38 @@ def test_seam_advance(B, fam, dtype, d, inplace):
     assert_rel(host(o), ref_o, tol, axes=(-1,), what=f"{fam} seam outputs")
 
 
+@pytest.mark.parametrize("fam,dtype,d", [("kda", "bf16", 128), ("mamba2", "f32", 64), ("gdn", "f32", 32)])
+def test_seam_advance_from_zero_long_windows(B, fam, dtype, d):
+    """No start state (zeros, nothing copied in), windows longer than the tokens
+    a seam-head takes ahead (8), and many seam-heads per CTA.  The outputs are
+    checked per (layer, head) over all tokens: from a zero state some outputs are
+    small differences of decayed terms, and a per-row relative error would
+    divide the fp32 rounding of the state by their tiny norms."""
+    rng = np.random.default_rng(100 + d)
+    lens = [17, 9, 0, 33, 8, 1, 24, 16] * 6
+    cu = synth.cu_from_lengths(lens)
+    n, Lyr, H = int(cu[-1]), 2, 5
+    rb = synth.round_bf16 if dtype == "bf16" else (lambda x: x)
+    unit = lambda s: (lambda x: x / np.linalg.norm(x, axis=-1, keepdims=True))(rng.standard_normal(s)).astype(np.float32)
+    q, k = rb(unit((Lyr, n, H, d))), rb(unit((Lyr, n, H, d)))
+    v = rb(rng.standard_normal((Lyr, n, H, d)).astype(np.float32))
+    okw = {}
+    if fam == "gdn":
+        okw["alpha"], okw["beta"] = synth.gdn_gates(rng, (Lyr, n, H), "middecay")
+    if fam == "kda":
+        okw["g"] = rng.uniform(0.85, 1, (Lyr, n, H, d)).astype(np.float32)
+        okw["beta"] = rng.uniform(0, 1, (Lyr, n, H)).astype(np.float32)
+    if fam == "mamba2":
+        okw["alpha"] = rng.uniform(0.85, 1, (Lyr, n, H)).astype(np.float32)
+    kw = {key: dev(val) for key, val in okw.items()}
+    s_out, o = B.seam_advance(fam, dev(q, dtype), dev(k, dtype), dev(v, dtype), cu, **kw)
+    B.check_device()
+    ref_s, ref_o = orc.seam(fam, q, k, v, cu, state_in=None, **okw)
+    tol = TOL_BF16 if dtype == "bf16" else TOL_F32
+    assert_rel(host(s_out), ref_s, tol, what=f"{fam} seam state from zero")
+    assert_rel(host(o), ref_o, tol, axes=(1, 3), what=f"{fam} seam outputs from zero")
+
+
 def reuse_path(B, inp_dev, cu, skip, seam_tok, n_layers, H, d, q_seam, alpha=None, beta=None):
     """Build every body, then advance a running state through the chain:
     state = pair(seg 0); for each internal segment: seam advance over its
