@@ -14,8 +14,10 @@
 // T_p (row-major, K-major as stored) is the B operand streamed by TMA in four
 // 32-column K-slices.  Per step: MMA = 3 x (M=128, N=128, K=128) tf32;
 // epilogue (TMEM lane n): D row n * 2^e_p + column n of S_p (TMA-staged),
-// split again into the next step's A.  The state never leaves the SM until
-// the chain ends; the HBM traffic is the pair stream, 128 KB per step.
+// split again into the next step's A, which is announced a K-slice at a time
+// (once all of D has been read) so that the next step's MMAs start while the
+// epilogue still writes.  The state never leaves the SM until the chain
+// ends; the HBM traffic is the pair stream, 128 KB per step.
 //
 // Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2-5
 // split the T slices (hi in place, lo beside it) and, in the reuse chain,
