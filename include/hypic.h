@@ -151,14 +151,19 @@ typedef struct {
     float* S_out;
 } hypic_build_args;
 
-/* Bytes of device scratch the build needs for these arguments (plan and
-   work counter).  Returns 0 when the arguments are invalid. */
+/* Bytes of device scratch the build needs for these arguments: the plan and
+   work counter (a few KB); for KDA at dk = dv = 128 with bf16 k and v also the
+   tables of its tensor-core path, 128 KB per 64-token chunk, layer and head,
+   for at most 4 GiB of chunks at a time (more only when one segment alone
+   needs more).  Returns 0 when the arguments are invalid. */
 HYPIC_API size_t hypic_build_workspace_size(const hypic_build_args* args);
 
 /* Launch the build on `stream`.  `workspace` is device memory of at least
    hypic_build_workspace_size(args) bytes, 256-byte aligned, owned by the
    caller and not used by any other call until this one completes on the
-   stream.  Returns HYPIC_ERR_WORKSPACE when it is NULL or too small. */
+   stream.  Returns HYPIC_ERR_WORKSPACE when it is NULL or too small.  KDA at
+   d = 128 (bf16) takes its segments in batches whose chunk tables fit the
+   workspace. */
 HYPIC_API hypic_status hypic_segment_build(const hypic_build_args* args, void* workspace,
                                  size_t workspace_bytes, hypic_stream_t stream);
 
@@ -324,6 +329,8 @@ HYPIC_API hypic_status hypic_reuse_chain(const hypic_chain_args* args, void* wor
  *     serialise them.
  *   - The call itself allocates nothing (no cudaMalloc, no allocating library
  *     routine).
+ *   - KDA at d = 128 runs its CUDA-core kernel here: the chunk tables of its
+ *     tensor-core path do not fit the fixed array.
  */
 #define HYPIC_NOALLOC_MAX_SEGMENTS 16384
 HYPIC_API hypic_status hypic_segment_build_noalloc(const hypic_build_args* args, hypic_stream_t stream);

@@ -161,6 +161,8 @@ BuildParams to_params(const hypic_build_args* a) {
     p.n_tokens = a->n_tokens;
     p.cu = a->cu_seqlens;
     p.skip = a->seam_skip;
+    p.cu_host = a->cu_seqlens_host;
+    p.skip_host = a->seam_skip_host;
     p.k = a->k;
     p.v = a->v;
     p.alpha = a->alpha;
@@ -177,15 +179,20 @@ BuildParams to_params(const hypic_build_args* a) {
 
 extern "C" size_t hypic_build_workspace_size(const hypic_build_args* args) {
     if (check_build(args) != HYPIC_OK) return 0;
+    const BuildParams p = to_params(args);
+    if (args->n_segments > 0 && kda_build_tc_supported(p)) return kda_build_tc_workspace_bytes(p);
     return build_workspace_bytes(args->n_segments);
 }
 
-extern "C" hypic_status hypic_segment_build(const hypic_build_args* args, void* workspace, size_t workspace_bytes,
-                                            hypic_stream_t stream) {
+namespace hypic {
+// The build with `tables` = false needs only the plan and counter in its
+// workspace: KDA then runs its CUDA-core kernel (the no-alloc build).
+hypic_status segment_build_impl(const hypic_build_args* args, void* workspace, size_t workspace_bytes,
+                                hypic_stream_t stream, bool tables) {
     hypic_status st = check_build(args);
     if (st != HYPIC_OK) return st;
     if (args->n_segments == 0) return HYPIC_OK;
-    const size_t need = build_workspace_bytes(args->n_segments);
+    const size_t need = tables ? hypic_build_workspace_size(args) : build_workspace_bytes(args->n_segments);
     if (!workspace || workspace_bytes < need)
         return fail(HYPIC_ERR_WORKSPACE, "workspace %p of %zu bytes, need %zu", workspace, workspace_bytes, need);
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -203,11 +210,20 @@ extern "C" hypic_status hypic_segment_build(const hypic_build_args* args, void* 
     } else if (decay_build_tc_supported(p)) {
         e = launch_decay_build_tc(p, workspace, err, s);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core decay-family build launch");
+    } else if (tables && kda_build_tc_supported(p)) {
+        e = launch_kda_build_tc(p, workspace, workspace_bytes, err, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core KDA build launch");
     } else {
         e = launch_build_simt(p, workspace, err, s);
         if (e != cudaSuccess) return cuda_fail(e, "build launch");
     }
     return HYPIC_OK;
+}
+}  // namespace hypic
+
+extern "C" hypic_status hypic_segment_build(const hypic_build_args* args, void* workspace, size_t workspace_bytes,
+                                            hypic_stream_t stream) {
+    return segment_build_impl(args, workspace, workspace_bytes, stream, true);
 }
 
 // ---------------------------------------------------------------- compose --

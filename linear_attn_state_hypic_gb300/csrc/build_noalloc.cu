@@ -11,6 +11,8 @@
 
 namespace hypic {
 void set_detail(const char* msg);  // api.cu: sets hypic_last_error_detail()
+hypic_status segment_build_impl(const hypic_build_args* args, void* workspace, size_t workspace_bytes,
+                                hypic_stream_t stream, bool tables);  // api.cu
 }
 
 namespace {
@@ -42,8 +44,10 @@ extern "C" hypic_status hypic_segment_build_noalloc(const hypic_build_args* args
         hypic::set_detail(msg);
         return HYPIC_ERR_WORKSPACE;
     }
-    const size_t need = hypic_build_workspace_size(args);
-    if (need == 0) return hypic_segment_build(args, nullptr, 0, stream);  // reports the argument error
+    if (hypic_build_workspace_size(args) == 0) return hypic_segment_build(args, nullptr, 0, stream);  // the argument error
+    // The plan and counter only: KDA, whose tensor-core path needs its chunk tables, runs its CUDA-core
+    // kernel here.
+    const size_t need = hypic::build_workspace_bytes(args->n_segments);
     if (need > kNoallocBytes) {
         snprintf(msg, sizeof(msg), "no-alloc build: needs %zu bytes of scratch, the fixed array holds %zu", need,
                  kNoallocBytes);
@@ -57,5 +61,5 @@ extern "C" hypic_status hypic_segment_build_noalloc(const hypic_build_args* args
         hypic::set_detail(msg);
         return HYPIC_ERR_CUDA;
     }
-    return hypic_segment_build(args, ws, kNoallocBytes, stream);
+    return hypic::segment_build_impl(args, ws, kNoallocBytes, stream, false);
 }

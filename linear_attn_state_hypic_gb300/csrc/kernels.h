@@ -11,6 +11,8 @@ struct BuildParams {
     int64_t n_tokens;
     const int32_t* cu;    // [n_seg+1]
     const int32_t* skip;  // [n_seg] or null
+    const int32_t* cu_host = nullptr;    // host copies of cu and skip (batch planning)
+    const int32_t* skip_host = nullptr;
     const void* k;
     const void* v;
     const float* alpha;
@@ -72,7 +74,19 @@ bool gdn_build_tc_supported(const BuildParams& p);
 cudaError_t launch_decay_build_tc(const BuildParams& p, void* workspace, unsigned* err, cudaStream_t s);
 bool decay_build_tc_supported(const BuildParams& p);
 
+// KDA (d = 128, bf16 k/v) on the tensor cores: every 64-token chunk's own pair,
+// then the chunk pairs of each segment chained by the tensor-core compose.
+// The chunk tables live in the workspace, whose size kda_build_tc_workspace_bytes
+// reports (segments are taken in batches whose tables fit it).
+bool kda_build_tc_supported(const BuildParams& p);
+size_t kda_build_tc_workspace_bytes(const BuildParams& p);
+cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t workspace_bytes, unsigned* err,
+                                cudaStream_t s);
+
 cudaError_t launch_compose(const ComposeParams& p, unsigned* err, cudaStream_t s);
+cudaError_t launch_compose_simt(const ComposeParams& p, unsigned* err, cudaStream_t s);
+cudaError_t launch_compose_tc(const ComposeParams& p, unsigned* err, cudaStream_t s);
+bool compose_tc_supported(const ComposeParams& p);
 cudaError_t launch_seam(const SeamParams& p, unsigned* err, cudaStream_t s);
 
 // Reuse chain: the compose chain of `c` with, before step j, a seam advance

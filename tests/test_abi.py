@@ -376,3 +376,24 @@ def test_conv_rejections(B, mutate, status):
     mutate(a, cu)
     assert B.hypic_conv_warmup(a, None) == status
     assert B.lib.hypic_last_error_detail().decode()
+
+
+def test_build_workspace_holds_kda_chunk_tables(B):
+    """KDA at d = 128 with bf16 k and v: the reported workspace also holds the
+    chunk tables of its tensor-core path (T and S of every 64-token chunk,
+    layer and head: 128 KB each); other dims and dtypes need only the plan."""
+    plan_args, keep0 = base_build(B, 0)
+    plan = B.hypic_build_workspace_size(plan_args)
+    a, keep = base_build(B, 4)            # bodies of 64 and 80 tokens: 1 + 2 chunks, 1 layer x 2 heads
+    need = B.hypic_build_workspace_size(a)
+    tables = 3 * 2 * 128 * 1024
+    assert plan + tables <= need < plan + tables + 8192
+    assert run_build(B, a, ws=need - 1) == B.ERR_WORKSPACE
+    a.in_dtype = 0                        # fp32 inputs: the CUDA-core kernel
+    assert B.hypic_build_workspace_size(a) == plan
+    a.in_dtype, a.dk, a.dv = 1, 64, 64    # d = 64: the CUDA-core kernel
+    assert B.hypic_build_workspace_size(a) == plan
+    sk = np.array([64, 80], np.int32)     # every body empty: nothing to tabulate
+    a.dk, a.dv = 128, 128
+    a.seam_skip, a.seam_skip_host = fake(8), sk.ctypes.data
+    assert B.hypic_build_workspace_size(a) == plan
