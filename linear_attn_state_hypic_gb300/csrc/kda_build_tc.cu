@@ -11,40 +11,47 @@
 //
 // How.  The body of a segment is cut into chunks of 64 tokens.  A chunk's own
 // pair depends on nothing outside the chunk, so all chunks of all segments,
-// layers and heads are formed at once (one CTA each), into a table in the
-// workspace; the composition law then chains each segment's chunk pairs in
-// order (the compose's state mode gives S(C|0) from a zero state, its
-// transition mode T_C), which is exact up to rounding.
-// Chunk pair.  Inside a chunk let g_t = a_1 ... a_t (per channel, g_0 = 1) and
-// g_C its last value.  The rescaled state Diag(g_t)^-1 S_t takes one
-// generalised Householder step per token, I - b_t x_t y_t^T with x_t = k_t / g_t
-// and y_t = k_t * g_t, so the chunk's product is I - X^T W (WY form) with
+// layers and heads are formed independently into a table in the workspace;
+// the composition law then chains each segment's chunk pairs in order (the
+// compose's state mode gives S(C|0) from a zero state, its transition mode
+// T_C), which is exact up to rounding.
+// Chunk pair.  Inside a chunk let g_t = a_1 ... a_t (per channel) and g_C its
+// last value.  The rescaled state Diag(g_t)^-1 S_t takes one generalised
+// Householder step per token, I - b_t x_t y_t^T with x_t = k_t / g_t and
+// y_t = k_t * g_t, so the chunk's product is I - X^T W (WY form) with
 //     w_t = b_t (y_t - sum_{s<t} G_ts w_s),  u_t = b_t (v_t - sum_{s<t} G_ts u_s),
 //     G_ts = y_t . x_s = sum_c k_t[c] k_s[c] (a_{s+1} ... a_t)[c],
 // and, with kbar_t = k_t * (a_{t+1} ... a_L) (= k_t g_C / g_t),
 //     T_chunk = Diag(g_C) - Kbar^T W,   S_chunk = Kbar^T U.
-// Every factor is a product of gates over a token range, formed as a running
-// product (never a ratio of two prefix products, which leaves the fp32 range
-// for strong gates), so the chunk pair is in range for any a_t in [0, 1].
-// Steps (512 threads, one CTA per chunk, layer and head):
-//   stage    keys (fp32), values (bf16), gates, b
-//   kbar     reverse running products, written as the bf16 hi + lo operand Kbar^T
-//   gram     G_ts for s < t: thread (s, channel group) carries k_s times the gates
-//            after s and meets every later key (fp32, CUDA cores)
-//   solve    [-W | U] by forward substitution, one column per thread (fp32)
-//   MMA      D = Kbar^T [-W | U]: bf16 M = 128, N = 256, K = 64, hi + lo pairs
-//            (three products, about 16 significant bits each side), fp32 in tensor memory
+// Gate products over token ranges come from 16-token block products joined by
+// the blocks' totals (never a ratio), so g_t, kbar_t and y_t are in range for
+// any a_t in [0, 1].  The gram is the bf16 MMA Y X^T in hi + lo pairs when
+// every channel's g_C is at least 2^-100 (x_t = k_t / g_t then stays below
+// 2^100 |k_t|); otherwise the chunk forms it on CUDA cores from running
+// products of the gates (k_s times the gates after s, met by every later key),
+// exact for any gate.
+// Steps of a chunk (512 threads; persistent CTAs, the next chunk's keys,
+// values, gates and b loaded by cp.async while this one finishes):
+//   scan     16-token block products per channel -> g_C, g_t, Kbar^T (bf16 hi + lo operand)
+//   gram     Y, X operands -> G = Y X^T (M = 64, N = 64, K = 128, three products) -> b_t G_ts
+//   solve    Tinv = (I + L)^-1, L_ts = b_t G_ts (16 x 16 diagonal blocks by forward
+//            substitution, the blocks below from them), then [-W | U]^T = X'^T Tinv^T with
+//            x_t = [-b_t k_t g_t | b_t v_t]: M = 128 (twice), N = 64, K = 64 MMAs in hi + lo pairs
+//   MMA      D = Kbar^T [-W | U]: M = 128, N = 256, K = 64 in hi + lo pairs (three
+//            products), fp32 in tensor memory
 //   write    T_chunk = Diag(g_C) + D_left, normalised by a power of two (its exponent
-//            kept beside it), and S_chunk = D_right
+//            kept beside it), and S_chunk = D_right, one tensor-memory pass on 16 warps
 // The chunk tables cost 128 KB per chunk, layer and head; segments are taken
 // in batches whose tables fit the workspace.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -61,32 +68,44 @@ constexpr int kThreads = 512;
 constexpr int64_t kPairBytes = 2 * kD * kD * 4;  // T and S of one chunk, layer and head
 
 // Shared memory map (bytes).  The MMA operands are K-major without swizzle:
-// core matrices of 8 rows x 8 tokens (16 bytes a row), the 8 of a row group
-// adjacent along the tokens (128 bytes apart), row groups 1024 bytes apart.
-constexpr uint32_t OFF_KF = 0;               // keys, fp32 [64 t][128 c]
-constexpr uint32_t OFF_GA = OFF_KF + 32768;  // gates a, fp32 [64 t][128 c]
-constexpr uint32_t OFF_VB = OFF_GA + 32768;  // values, bf16 [64 t][128 c]
-constexpr uint32_t OFF_L = OFF_VB + 16384;   // b_t G_ts for s < t, 0 elsewhere: fp32 [64 t][64 s]
+// core matrices of 8 rows x 16 bytes, adjacent along K 128 bytes apart, row
+// groups 1024 (K = 64 tokens) or 2048 (K = 128 channels) bytes apart.
+constexpr uint32_t OFF_KB = 0;               // keys, bf16 [64 t][128 c]; 16-byte chunk q of row t at q ^ (t & 15)
+constexpr uint32_t OFF_VB = OFF_KB + 16384;  // values, bf16 [64 t][128 c]
+constexpr uint32_t OFF_GA = OFF_VB + 16384;  // gates, fp32 [64 t][128 c]; chunk q of row t at q ^ (t & 31);
+                                             // then g_t when the gram runs on the tensor cores
+constexpr uint32_t OFF_L = OFF_GA + 32768;   // b_t G_ts for s < t, 0 elsewhere: fp32 [64 t][64 s]
 constexpr uint32_t OFF_A = OFF_L + 16384;    // Kbar^T hi, lo: bf16 [128 i][64 t], 16 KB each
-constexpr uint32_t OFF_B = OFF_A + 32768;    // [-W | U]^T hi, lo: bf16 [256 j][64 t], 32 KB each
-constexpr uint32_t OFF_MISC = OFF_B + 65536;
+constexpr uint32_t OFF_B = OFF_A + 32768;    // [-W | U]^T hi, lo: bf16 [256 j][64 t], 32 KB each; before
+                                             // them the gram operands Y hi, lo, X hi, lo: bf16 [64 t][128 c]
+constexpr uint32_t OFF_TI = OFF_B + 65536;    // Tinv = (I + L)^-1: fp32 [64 t][64 s]
+constexpr uint32_t OFF_TIO = OFF_TI + 16384;  // Tinv hi, lo: bf16 [64 t][64 s] operand, 8 KB each
+constexpr uint32_t OFF_R = OFF_TIO + 16384;   // solve scratch: fp32 [16][48]
+constexpr uint32_t OFF_MISC = OFF_R + 3072;
+constexpr uint32_t OFF_STAGE = OFF_A;         // T_chunk, S_chunk boxes for the TMA stores (128 KB over
+                                              // the operands, read by then): 4 + 4 boxes of 128 rows x 32
 
 struct KMisc {
-    uint64_t mma_done;
+    uint64_t gram_done, solve_done, pair_done;
     uint32_t tmem_base;
     int pad;
-    float gC[kD];     // g_C per channel
-    float beta[kC];   // b_t (0 past the body end)
-    float red[4];     // max |T| of each T warp
+    float beta[kC];      // b_t of the staged chunk (0 past the body end)
+    float gC[kD];        // g_C per channel
+    float btot[4][kD];   // gate product of each 16-token block, per channel
+    float red[16];       // max |T| of each T warp
 };
 constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(KMisc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_PAIR = 0, TM_GRAM = 256, TM_SOLVE = 384;
 constexpr uint32_t ID_PAIR = idesc(1, 128, 256, false, false);  // D = Kbar^T [-W | U], both K-major
+constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);    // G = Y X^T, both K-major
+constexpr uint32_t ID_SOLVE = idesc(1, 128, 64, false, false);  // [-W | U]^T = X'^T Tinv^T, half of the rows
+constexpr float kSafeGC = 0x1p-100f;
 
 struct ChunkArgs {
-    int n_layers, n_heads, seg0;
+    int n_layers, n_heads, seg0, n_items;
     int64_t n_tokens;
     const int32_t* cu;
     const int32_t* skip;
@@ -96,16 +115,45 @@ struct ChunkArgs {
     const __nv_bfloat16* v;
     const float* g;
     const float* beta;
-    float* T_tab;       // [chunks][L][H][128][128] mantissa
+    float* T_tab;        // [chunks][L][H][128][128] mantissa
     int32_t* T_exp_tab;  // [chunks][L][H]
-    float* S_tab;       // [chunks][L][H][128][128]
+    float* S_tab;        // [chunks][L][H][128][128]
     unsigned* err;
     uint64_t wait_ns;
 };
 
-// Byte offset of (row, token) in a K-major operand of 64 tokens.
+struct Item {
+    int64_t t0, obj;
+    int n, layer, head;
+};
+
+__device__ __forceinline__ Item decode(const ChunkArgs& a, int item) {
+    const int LH = a.n_layers * a.n_heads;
+    const int p = item / LH, lh = item % LH;
+    const int seg = a.chunk_seg[p];
+    const int64_t b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0), b1 = a.cu[seg + 1];
+    Item it;
+    it.t0 = b0 + (int64_t)(p - a.cu_chunk[seg - a.seg0]) * kC;
+    it.n = (int)(b1 - it.t0 < kC ? b1 - it.t0 : kC);
+    it.layer = lh / a.n_heads;
+    it.head = lh % a.n_heads;
+    it.obj = (int64_t)p * LH + lh;
+    return it;
+}
+
+// Byte offsets: key (t, c) in the staged tile, gate (t, c), and (row, token)
+// in a K-major operand of 64 tokens.
+__device__ __forceinline__ uint32_t kb_off(int t, int c) {
+    return (uint32_t)(t * 256 + ((((c >> 3) ^ (t & 15))) << 4) + (c & 7) * 2);
+}
+__device__ __forceinline__ uint32_t ga_off(int t, int c) {
+    return (uint32_t)(t * 512 + ((((c >> 2) ^ (t & 31))) << 4) + (c & 3) * 4);
+}
 __device__ __forceinline__ uint32_t core_off(int row, int t) {
     return (uint32_t)((row >> 3) * 1024 + (t >> 3) * 128 + (row & 7) * 16 + (t & 7) * 2);
+}
+__device__ __forceinline__ float bf_at(const uint8_t* p) {
+    return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(p)) << 16);
 }
 
 // x = hi + lo as a pair of bf16 (hi rounded to nearest, lo the rounded rest).
@@ -117,7 +165,7 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& h, uint32_t
     l = *reinterpret_cast<const uint32_t*>(&ll);
 }
 
-// Eight consecutive tokens of one operand row, as hi and lo 16-byte pieces.
+// Eight consecutive K elements of one operand row, as hi and lo 16-byte pieces.
 __device__ __forceinline__ void store_row8(uint8_t* hi, uint8_t* lo, uint32_t off, const float (&x)[8]) {
     uint32_t h[4], l[4];
 #pragma unroll
@@ -132,270 +180,458 @@ __device__ __forceinline__ float scale_pow2(float x, int e) {
     return x * __int_as_float((e1 + 127) << 23) * __int_as_float((e2 + 127) << 23);
 }
 
-__device__ __noinline__ bool wait_done(uint64_t* bar, uint64_t wait_ns, unsigned* err) {
+__device__ __noinline__ bool wait_done(uint64_t* bar, uint32_t parity, uint64_t wait_ns, unsigned* err) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
         for (int j = 0; j < 16; ++j)
-            if (mbar_try_wait(bar, 0)) return true;
+            if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > wait_ns) break;
     }
     set_error(err, kErrTimeout);
     return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) kda_chunk_pair_kernel(const ChunkArgs a) {
+// The chunk's keys, values and gates (rows past the body end zero-filled) and
+// b, by cp.async of every thread.
+__device__ __forceinline__ void prefetch(uint8_t* smem, KMisc* ms, const ChunkArgs& a, const Item& it, int tid) {
+    const int64_t rs = (int64_t)a.n_heads * kD;
+    const int64_t row0 = tok_row(it.layer, it.t0, it.head, a.n_tokens, a.n_heads) * kD;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int e = tid + kThreads * m, t = e >> 4, q = e & 15;
+        const bool ok = t < it.n;
+        const int64_t off = ok ? row0 + t * rs + 8 * q : row0;
+        cp_async16_zfill(smem + OFF_KB + t * 256 + ((q ^ (t & 15)) << 4), a.k + off, ok);
+        cp_async16_zfill(smem + OFF_VB + t * 256 + q * 16, a.v + off, ok);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int e = tid + kThreads * m, t = e >> 5, q = e & 31;
+        const bool ok = t < it.n;
+        cp_async16_zfill(smem + OFF_GA + t * 512 + ((q ^ (t & 31)) << 4), a.g + (ok ? row0 + t * rs + 4 * q : row0), ok);
+    }
+    if (tid < kC) {
+        const bool ok = tid < it.n;
+        const int64_t r = tok_row(it.layer, it.t0 + (ok ? tid : 0), it.head, a.n_tokens, a.n_heads);
+        cp_async4_zfill(&ms->beta[tid], a.beta + r, ok);
+    }
+    cp_async_commit();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_chunk_pair_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmS,
+                          const ChunkArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     KMisc* ms = reinterpret_cast<KMisc*>(smem + OFF_MISC);
-    float* KF = reinterpret_cast<float*>(smem + OFF_KF);
-    float* GA = reinterpret_cast<float*>(smem + OFF_GA);
-    const __nv_bfloat16* VB = reinterpret_cast<const __nv_bfloat16*>(smem + OFF_VB);
     float* L = reinterpret_cast<float*>(smem + OFF_L);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int LH = a.n_layers * a.n_heads;
-    const int p = blockIdx.x / LH, lh = blockIdx.x % LH;
-    const int layer = lh / a.n_heads, head = lh % a.n_heads;
-    const int seg = a.chunk_seg[p];
-    const int64_t b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0), b1 = a.cu[seg + 1];
-    const int64_t t0 = b0 + (int64_t)(p - a.cu_chunk[seg - a.seg0]) * kC;
-    const int n = (int)(b1 - t0 < kC ? b1 - t0 : kC);
-    if (n <= 0) {  // the batch plan makes this unreachable
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled staging boxes need 1024-byte alignment
         if (tid == 0) set_error(a.err, kErrBadIndex);
         return;
     }
     if (tid == 0) {
-        mbar_init(&ms->mma_done, 1);
+        mbar_init(&ms->gram_done, 1);
+        mbar_init(&ms->solve_done, 1);
+        mbar_init(&ms->pair_done, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&ms->tmem_base, kTmemCols);
-
-    // ---- stage: every load of a thread issued before its stores
-    {
-        const int64_t rs = (int64_t)a.n_heads * kD;  // elements between consecutive tokens
-        const int64_t row0 = tok_row(layer, t0, head, a.n_tokens, a.n_heads) * kD;
-        uint4 xk[2], xv[2];
-        float4 xg[4];
-        float bt = 0.f;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int e = tid + kThreads * m, t = e >> 4, q = e & 15;
-            const bool ok = t < n;
-            xk[m] = ok ? *reinterpret_cast<const uint4*>(a.k + row0 + t * rs + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
-            xv[m] = ok ? *reinterpret_cast<const uint4*>(a.v + row0 + t * rs + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int e = tid + kThreads * m, t = e >> 5, q = e & 31;
-            xg[m] = t < n ? *reinterpret_cast<const float4*>(a.g + row0 + t * rs + 4 * q)
-                          : make_float4(1.f, 1.f, 1.f, 1.f);
-        }
-        if (tid < kC && tid < n) bt = a.beta[tok_row(layer, t0 + tid, head, a.n_tokens, a.n_heads)];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int e = tid + kThreads * m, t = e >> 4, q = e & 15;
-            const uint32_t w[4] = {xk[m].x, xk[m].y, xk[m].z, xk[m].w};
-            float4* dk = reinterpret_cast<float4*>(KF + t * kD + 8 * q);
-            dk[0] = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xffff0000u),
-                                __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xffff0000u));
-            dk[1] = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xffff0000u),
-                                __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xffff0000u));
-            *reinterpret_cast<uint4*>(smem + OFF_VB + (t * kD + 8 * q) * 2) = xv[m];
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) reinterpret_cast<float4*>(GA)[tid + kThreads * m] = xg[m];
-        if (tid < kC) ms->beta[tid] = bt;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) reinterpret_cast<float4*>(L)[tid + kThreads * m] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    if ((int)blockIdx.x < a.n_items) prefetch(smem, ms, a, decode(a, blockIdx.x), tid);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
+    uint32_t n_gram = 0, n_pair = 0;
 
-    // ---- kbar: thread c < 128 runs over channel c from the last token back
-    if (tid < kD) {
-        const int c = tid;
-        uint8_t* hi = smem + OFF_A;
-        uint8_t* lo = hi + 16384;
-        float suf = 1.f;  // gates after token t
 #pragma unroll 1
-        for (int q = 7; q >= 0; --q) {
-            float x[8];
-#pragma unroll
-            for (int e = 7; e >= 0; --e) {
-                const int t = 8 * q + e;
-                x[e] = KF[t * kD + c] * suf;
-                suf *= GA[t * kD + c];
-            }
-            store_row8(hi, lo, core_off(c, 8 * q), x);
-        }
-        ms->gC[c] = suf;
-        fence_async_smem();
-    }
+    for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+        const Item it = decode(a, item);
+        cp_async_wait_all();
+        if (tid == 0) cp_bulk_wait_read();  // the previous chunk's stores have read the staging area
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
 
-    // ---- gram: thread (s, group) holds k_s over the channels 4 group + 32 m + e (m, e < 4), times
-    // the gates after s, and forms its part of G_ts for every later token t; the eight groups of a
-    // column are adjacent lanes and meet by shuffles.  A warp holds columns 4 warp .. 4 warp + 3, so
-    // its loop starts at t = 4 warp + 1.
-    {
-        const int s = tid >> 3, grp = tid & 7;
-        float z[16];
+        // ---- scan: thread (channel c, block b) over tokens 16 b .. 16 b + 15
+        bool safe;
+        {
+            const int c = tid & (kD - 1), blk = tid >> 7;
+            float al[16], pi[16], sg[16];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float4 x = *reinterpret_cast<const float4*>(KF + s * kD + 4 * grp + 32 * m);
-            z[4 * m] = x.x, z[4 * m + 1] = x.y, z[4 * m + 2] = x.z, z[4 * m + 3] = x.w;
-        }
-#pragma unroll 1
-        for (int t = 4 * warp + 1; t < n; ++t) {
-            float4 ga[4], kt[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                ga[m] = *reinterpret_cast<const float4*>(GA + t * kD + 4 * grp + 32 * m);
-                kt[m] = *reinterpret_cast<const float4*>(KF + t * kD + 4 * grp + 32 * m);
+            for (int e = 0; e < 16; ++e) {
+                const int t = 16 * blk + e;
+                al[e] = t < it.n ? *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c)) : 1.f;
             }
-            const bool act = t > s;
-            if (act) {
+            pi[0] = al[0];
+#pragma unroll
+            for (int e = 1; e < 16; ++e) pi[e] = pi[e - 1] * al[e];
+            sg[15] = 1.f;
+#pragma unroll
+            for (int e = 14; e >= 0; --e) sg[e] = sg[e + 1] * al[e + 1];
+            ms->btot[blk][c] = pi[15];
+            __syncthreads();
+            float E = 1.f, F = 1.f;  // gate products of the blocks before and after this one
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float P = ms->btot[b][c];
+                if (b < blk) E *= P;
+                if (b > blk) F *= P;
+            }
+            const float gC = ((ms->btot[0][c] * ms->btot[1][c]) * ms->btot[2][c]) * ms->btot[3][c];
+            if (blk == 0) ms->gC[c] = gC;
+            uint8_t* ahi = smem + OFF_A;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int tt = 8 * h + e;
+                    x[e] = bf_at(smem + OFF_KB + kb_off(16 * blk + tt, c)) * (sg[tt] * F);
+                }
+                store_row8(ahi, ahi + 16384, core_off(c, 16 * blk + 8 * h), x);
+            }
+            fence_async_smem();
+            safe = __syncthreads_and(gC >= kSafeGC) != 0;
+            if (safe)
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    *reinterpret_cast<float*>(smem + OFF_GA + ga_off(16 * blk + e, c)) = E * pi[e];
+        }
+
+        if (safe) {
+            // ---- gram operands: task (channel octet q8, token t); Y = k g, X = k / g
+            __syncthreads();  // every g_t written
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int task = tid + kThreads * m, q8 = task >> 6, t = task & 63;
+                const uint4 kx = *reinterpret_cast<const uint4*>(smem + OFF_KB + t * 256 + ((q8 ^ (t & 15)) << 4));
+                const float4 g0 = *reinterpret_cast<const float4*>(smem + OFF_GA + t * 512 + (((2 * q8) ^ (t & 31)) << 4));
+                const float4 g1 =
+                    *reinterpret_cast<const float4*>(smem + OFF_GA + t * 512 + (((2 * q8 + 1) ^ (t & 31)) << 4));
+                const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
+                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                float y[8], x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float kv = __uint_as_float((e & 1) ? (kw[e >> 1] & 0xffff0000u) : (kw[e >> 1] << 16));
+                    y[e] = kv * gv[e];
+                    x[e] = kv * __frcp_rn(gv[e]);
+                }
+                const uint32_t off = (uint32_t)((t >> 3) * 2048 + q8 * 128 + (t & 7) * 16);
+                store_row8(smem + OFF_B, smem + OFF_B + 16384, off, y);
+                store_row8(smem + OFF_B + 32768, smem + OFF_B + 49152, off, x);
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t sb = smem_u32(smem);
+                const uint32_t yh = sb + OFF_B, yl = yh + 16384, xh = yh + 32768, xl = yh + 49152;
+#pragma unroll 1
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t dyh = sdesc_plain(yh + 256 * kk, 128, 2048), dyl = sdesc_plain(yl + 256 * kk, 128, 2048);
+                    const uint64_t dxh = sdesc_plain(xh + 256 * kk, 128, 2048), dxl = sdesc_plain(xl + 256 * kk, 128, 2048);
+                    mma_bf16_ss(tmem + TM_GRAM, dyh, dxh, ID_GRAM, kk > 0);
+                    mma_bf16_ss(tmem + TM_GRAM, dyh, dxl, ID_GRAM, true);
+                    mma_bf16_ss(tmem + TM_GRAM, dyl, dxh, ID_GRAM, true);
+                }
+                mma_commit(&ms->gram_done);
+            }
+            __syncwarp();
+            const bool ok = __syncthreads_and(wait_done(&ms->gram_done, n_gram & 1, a.wait_ns, a.err)) != 0;
+            ++n_gram;
+            if (!ok) break;
+            tc_fence_after();
+            // b_t G_ts for s < t: warp (quarter q, columns 16 cb ..); row 16 q + l of the M = 64
+            // accumulator sits in lane 32 q + l, l < 16
+            {
+                const int q = warp & 3, cb = warp >> 2;
+                uint32_t gv[16];
+                tmem_ld16(tmem + ((32u * q) << 16) + TM_GRAM + 16 * cb, gv);
+                tmem_wait_ld();
+                if (lane < 16) {
+                    const int t = 16 * q + lane;
+                    const float coef = ms->beta[t];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        const int s = 16 * cb + e;
+                        float4 o;
+                        o.x = s < t ? coef * __uint_as_float(gv[e]) : 0.f;
+                        o.y = s + 1 < t ? coef * __uint_as_float(gv[e + 1]) : 0.f;
+                        o.z = s + 2 < t ? coef * __uint_as_float(gv[e + 2]) : 0.f;
+                        o.w = s + 3 < t ? coef * __uint_as_float(gv[e + 3]) : 0.f;
+                        *reinterpret_cast<float4*>(L + t * kC + s) = o;
+                    }
+                }
+            }
+        } else {
+            // ---- gram on CUDA cores, exact for any gate: thread (s, group) holds k_s over the
+            // channels 4 group + 32 m + e, times the gates after s, and meets every later key
+#pragma unroll
+            for (int m = 0; m < 2; ++m) reinterpret_cast<float4*>(L)[tid + kThreads * m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncthreads();
+            const int s = tid >> 3, grp = tid & 7;
+            float z[16];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) z[4 * m + e] = bf_at(smem + OFF_KB + kb_off(s, 4 * grp + 32 * m + e));
+#pragma unroll 1
+            for (int t = 4 * warp + 1; t < it.n; ++t) {
+                float4 ga[4];
+                uint2 kt[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    z[4 * m] *= ga[m].x, z[4 * m + 1] *= ga[m].y, z[4 * m + 2] *= ga[m].z, z[4 * m + 3] *= ga[m].w;
+                    const int c0 = 4 * grp + 32 * m;
+                    ga[m] = *reinterpret_cast<const float4*>(smem + OFF_GA + ga_off(t, c0));
+                    kt[m] = *reinterpret_cast<const uint2*>(smem + OFF_KB + kb_off(t, c0));
                 }
+                if (t > s) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        z[4 * m] *= ga[m].x, z[4 * m + 1] *= ga[m].y, z[4 * m + 2] *= ga[m].z, z[4 * m + 3] *= ga[m].w;
+                    }
+                }
+                float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    p0 = fmaf(__uint_as_float(kt[m].x << 16), z[4 * m], p0);
+                    p1 = fmaf(__uint_as_float(kt[m].x & 0xffff0000u), z[4 * m + 1], p1);
+                    p0 = fmaf(__uint_as_float(kt[m].y << 16), z[4 * m + 2], p0);
+                    p1 = fmaf(__uint_as_float(kt[m].y & 0xffff0000u), z[4 * m + 3], p1);
+                }
+                float pr = p0 + p1;
+                pr += __shfl_xor_sync(0xffffffffu, pr, 1);
+                pr += __shfl_xor_sync(0xffffffffu, pr, 2);
+                pr += __shfl_xor_sync(0xffffffffu, pr, 4);
+                if (t > s && grp == 0) L[t * kC + s] = ms->beta[t] * pr;
             }
-            float p0 = 0.f, p1 = 0.f;
+        }
+        __syncthreads();
+
+        // ---- solve: (I + L) [-W | U] = X' with rows x_t = [-b_t k_t g_t | b_t v_t], as
+        // [-W | U]^T = X'^T Tinv^T on the tensor cores, Tinv = (I + L)^-1 formed on CUDA cores.
+        if (!safe) {  // the gates were kept for the CUDA-core gram: now g_t as on the other path
+            const int c = tid & (kD - 1), blk = tid >> 7;
+            float E = 1.f, gp[16];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (b < blk) E *= ms->btot[b][c];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int t = 16 * blk + e;
+                gp[e] = t < it.n ? *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c)) : 1.f;
+            }
+            float pr = E;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                pr *= gp[e];
+                *reinterpret_cast<float*>(smem + OFF_GA + ga_off(16 * blk + e, c)) = pr;
+            }
+            __syncthreads();
+        }
+        {
+            // X'^T rows j (K-major over the chunk's tokens), task (octet o, row j): eight tokens
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                p0 = fmaf(kt[m].x, z[4 * m], p0);
-                p1 = fmaf(kt[m].y, z[4 * m + 1], p1);
-                p0 = fmaf(kt[m].z, z[4 * m + 2], p0);
-                p1 = fmaf(kt[m].w, z[4 * m + 3], p1);
+                const int task = tid + kThreads * m, j = task & 255, o = task >> 8;
+                const bool isw = j < kD;
+                const int c = isw ? j : j - kD;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int t = 8 * o + e;
+                    x[e] = isw ? -ms->beta[t] * bf_at(smem + OFF_KB + kb_off(t, c)) *
+                                     *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c))
+                               : ms->beta[t] * bf_at(smem + OFF_VB + (t * kD + c) * 2);
+                }
+                store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 8 * o), x);
             }
-            float pr = p0 + p1;
-            pr += __shfl_xor_sync(0xffffffffu, pr, 1);
-            pr += __shfl_xor_sync(0xffffffffu, pr, 2);
-            pr += __shfl_xor_sync(0xffffffffu, pr, 4);
-            if (act && grp == 0) L[t * kC + s] = ms->beta[t] * pr;
-        }
-    }
-    __syncthreads();
-
-    // ---- solve: thread j < 256 forms column j of [-W | U] over the chunk's tokens.
-    if (tid < 2 * kD) {
-        const int j = tid;
-        const bool isw = j < kD;
-        const int c = isw ? j : j - kD;
-        float w[kC];
-        float gp = 1.f;  // g_t of channel c
+            fence_async_smem();
+            // Tinv starts as zero; its 16 x 16 diagonal blocks (I + L_II)^-1 by forward substitution
+            // (thread: block I, column r)
+            float* TI = reinterpret_cast<float*>(smem + OFF_TI);
 #pragma unroll
-        for (int t = 0; t < kC; ++t) {
-            float x;
-            if (isw) {
-                gp *= GA[t * kD + c];
-                x = -ms->beta[t] * KF[t * kD + c] * gp;
-            } else {
-                x = ms->beta[t] * __bfloat162float(VB[t * kD + c]);
+            for (int m = 0; m < 2; ++m) reinterpret_cast<float4*>(TI)[tid + kThreads * m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncthreads();
+            if (tid < 64) {
+                const int I = tid >> 4, r = tid & 15;
+                float y[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const float* Lr = L + (16 * I + t) * kC + 16 * I;
+                    float acc = t == r ? 1.f : 0.f;
+#pragma unroll
+                    for (int u = 0; u < t; ++u) acc = fmaf(-Lr[u], y[u], acc);
+                    y[t] = acc;
+                    TI[(16 * I + t) * kC + 16 * I + r] = acc;
+                }
             }
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; 4 * m < t; ++m) {
-                const float4 l4 = *reinterpret_cast<const float4*>(L + t * kC + 4 * m);
-                acc[m & 3] = fmaf(l4.x, w[4 * m], acc[m & 3]);
-                if (4 * m + 1 < t) acc[m & 3] = fmaf(l4.y, w[4 * m + 1], acc[m & 3]);
-                if (4 * m + 2 < t) acc[m & 3] = fmaf(l4.z, w[4 * m + 2], acc[m & 3]);
-                if (4 * m + 3 < t) acc[m & 3] = fmaf(l4.w, w[4 * m + 3], acc[m & 3]);
+        }
+        __syncthreads();
+        // ---- the staged tiles are read: load the next chunk while this one finishes
+        if (item + (int)gridDim.x < a.n_items) prefetch(smem, ms, a, decode(a, item + gridDim.x), tid);
+        {
+            // off-diagonal blocks, row block I = 1..3: R_J = sum_{K=J}^{I-1} L_IK Tinv_KJ, then
+            // Tinv_IJ = -Tinv_II R_J
+            float* TI = reinterpret_cast<float*>(smem + OFF_TI);
+            float* R = reinterpret_cast<float*>(smem + OFF_R);
+#pragma unroll 1
+            for (int I = 1; I < 4; ++I) {
+                const int w16 = 16 * I;
+                for (int o = tid; o < 16 * w16; o += kThreads) {
+                    const int tt = o / w16, col = o % w16, J = col >> 4;
+                    const float* Lr = L + (w16 + tt) * kC;
+                    float acc = 0.f;
+                    for (int s = 16 * J; s < w16; ++s) acc = fmaf(Lr[s], TI[s * kC + col], acc);
+                    R[tt * 48 + col] = acc;
+                }
+                __syncthreads();
+                for (int o = tid; o < 16 * w16; o += kThreads) {
+                    const int tt = o / w16, col = o % w16;
+                    const float* Dr = TI + (w16 + tt) * kC + w16;
+                    float acc = 0.f;
+                    for (int u = 0; u <= tt; ++u) acc = fmaf(Dr[u], R[u * 48 + col], acc);
+                    TI[(w16 + tt) * kC + col] = -acc;
+                }
+                __syncthreads();
             }
-            w[t] = x - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+            // Tinv as the bf16 hi + lo operand (rows t, K-major over s): task (row t, octet o)
+            {
+                const int t = tid >> 3, o = tid & 7;
+                const float4 a0 = *reinterpret_cast<const float4*>(TI + t * kC + 8 * o);
+                const float4 a1 = *reinterpret_cast<const float4*>(TI + t * kC + 8 * o + 4);
+                const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                store_row8(smem + OFF_TIO, smem + OFF_TIO + 8192, core_off(t, 8 * o), x);
+            }
+            fence_async_smem();
         }
-        uint8_t* hi = smem + OFF_B;
-        uint8_t* lo = hi + 32768;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = w[8 * q + e];
-            store_row8(hi, lo, core_off(j, 8 * q), x);
-        }
-        fence_async_smem();
-    }
-    __syncthreads();
-
-    // ---- MMA: D = Kbar^T [-W | U] = hi hi + hi lo + lo hi, four steps of 16 tokens
-    if (tid == 0) {
+        tc_fence_before();
+        __syncthreads();
         tc_fence_after();
-        const uint32_t sb = smem_u32(smem);
-        const uint32_t ah = sb + OFF_A, al = ah + 16384, bh = sb + OFF_B, bl = bh + 32768;
+        if (tid == 0) {
+            const uint32_t sb = smem_u32(smem);
+            const uint32_t xh = sb + OFF_B, xl = xh + 32768, th = sb + OFF_TIO, tlo = th + 8192;
 #pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t dah = sdesc_plain(ah + 256 * kk, 128, 1024), dal = sdesc_plain(al + 256 * kk, 128, 1024);
-            const uint64_t dbh = sdesc_plain(bh + 256 * kk, 128, 1024), dbl = sdesc_plain(bl + 256 * kk, 128, 1024);
-            mma_bf16_ss(tmem, dah, dbh, ID_PAIR, kk > 0);
-            mma_bf16_ss(tmem, dah, dbl, ID_PAIR, true);
-            mma_bf16_ss(tmem, dal, dbh, ID_PAIR, true);
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll 1
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t dxh = sdesc_plain(xh + 16384 * hf + 256 * kk, 128, 1024),
+                                   dxl = sdesc_plain(xl + 16384 * hf + 256 * kk, 128, 1024);
+                    const uint64_t dth = sdesc_plain(th + 256 * kk, 128, 1024), dtl = sdesc_plain(tlo + 256 * kk, 128, 1024);
+                    const uint32_t d = tmem + TM_SOLVE + 64 * hf;
+                    mma_bf16_ss(d, dxh, dth, ID_SOLVE, kk > 0);
+                    mma_bf16_ss(d, dxh, dtl, ID_SOLVE, true);
+                    mma_bf16_ss(d, dxl, dth, ID_SOLVE, true);
+                }
+            mma_commit(&ms->solve_done);
         }
-        mma_commit(&ms->mma_done);
-    }
-    __syncwarp();
-    const bool ok = warp < 8 ? wait_done(&ms->mma_done, a.wait_ns, a.err) : true;
-    tc_fence_after();
+        __syncwarp();
+        {
+            const bool ok = __syncthreads_and(wait_done(&ms->solve_done, n_pair & 1, a.wait_ns, a.err)) != 0;
+            if (!ok) break;
+        }
+        tc_fence_after();
+        {
+            // [-W | U]^T into the B operand: warp (quarter q, half hf, token half ch)
+            const int q = warp & 3, hf = (warp >> 2) & 1, ch = warp >> 3, j = 128 * hf + 32 * q + lane;
+            uint32_t xv[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + TM_SOLVE + 64 * hf + 32 * ch, xv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int o = 0; o < 4; ++o) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(xv[8 * o + e]);
+                store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 32 * ch + 8 * o), x);
+            }
+            fence_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
 
-    // ---- write: warps 0-3 T_chunk (row i = lane of the accumulator), warps 4-7 S_chunk
-    const int64_t obj = (int64_t)p * LH + lh;
-    if (warp < 8) {
-        const int i = 32 * (warp & 3) + lane;
-        const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        if (warp < 4) {
-            const float gci = ms->gC[i];
-            float mx = 0.f;
-            if (ok) {
+        // ---- MMA: D = Kbar^T [-W | U] = hi hi + hi lo + lo hi, four steps of 16 tokens
+        if (tid == 0) {
+            const uint32_t sb = smem_u32(smem);
+            const uint32_t ah = sb + OFF_A, al = ah + 16384, bh = sb + OFF_B, bl = bh + 32768;
 #pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t x[32];
-                    tmem_ld32(tl + 32 * cb, x);
-                    tmem_wait_ld();
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t dah = sdesc_plain(ah + 256 * kk, 128, 1024), dal = sdesc_plain(al + 256 * kk, 128, 1024);
+                const uint64_t dbh = sdesc_plain(bh + 256 * kk, 128, 1024), dbl = sdesc_plain(bl + 256 * kk, 128, 1024);
+                mma_bf16_ss(tmem + TM_PAIR, dah, dbh, ID_PAIR, kk > 0);
+                mma_bf16_ss(tmem + TM_PAIR, dah, dbl, ID_PAIR, true);
+                mma_bf16_ss(tmem + TM_PAIR, dal, dbh, ID_PAIR, true);
+            }
+            mma_commit(&ms->pair_done);
+        }
+        __syncwarp();
+        const bool ok = __syncthreads_and(wait_done(&ms->pair_done, n_pair & 1, a.wait_ns, a.err)) != 0;
+        ++n_pair;
+        if (!ok) break;
+        tc_fence_after();
+
+        // ---- write: warp (quarter q, part r): r = 0, 1 columns 64 r .. of T_chunk, r = 2, 3 of S_chunk,
+        // staged as 32-column boxes (128-byte swizzle) in the operand area, then stored by TMA
+        {
+            const int q = warp & 3, r = warp >> 2, i = 32 * q + lane;
+            const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + TM_PAIR + 64 * r;
+            uint32_t x0[32], x1[32];
+            tmem_ld32(tl, x0);
+            tmem_ld32(tl + 32, x1);
+            tmem_wait_ld();
+            int ex = 0;
+            if (r < 2) {
+                const float gci = ms->gC[i];
+                float mx = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float y = __uint_as_float(x[e]) + (32 * cb + e == i ? gci : 0.f);
-                        mx = fmaxf(mx, fabsf(y));
-                    }
+                for (int e = 0; e < 32; ++e) {
+                    x0[e] = __float_as_uint(__uint_as_float(x0[e]) + (64 * r + e == i ? gci : 0.f));
+                    x1[e] = __float_as_uint(__uint_as_float(x1[e]) + (64 * r + 32 + e == i ? gci : 0.f));
+                    mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(x0[e])), fabsf(__uint_as_float(x1[e]))));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) ms->red[warp] = mx;
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                float M = 0.f;
+#pragma unroll
+                for (int wv = 0; wv < 8; ++wv) M = fmaxf(M, ms->red[wv]);
+                ex = (M > 0.f && isfinite(M)) ? ilogbf(M) : 0;
+                if (i == 0 && r == 0) a.T_exp_tab[it.obj] = ex;
+            }
+            // box b of this warp's 64 columns: row i at i * 128, 16-byte chunk j at j ^ (i & 7)
+            uint8_t* box = smem + OFF_STAGE + (uint32_t)r * 32768;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const uint32_t* xs = b ? x1 : x0;
+                uint8_t* row = box + b * 16384 + i * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float4 v = make_float4(__uint_as_float(xs[4 * j]), __uint_as_float(xs[4 * j + 1]),
+                                           __uint_as_float(xs[4 * j + 2]), __uint_as_float(xs[4 * j + 3]));
+                    if (r < 2)
+                        v = make_float4(scale_pow2(v.x, -ex), scale_pow2(v.y, -ex), scale_pow2(v.z, -ex),
+                                        scale_pow2(v.w, -ex));
+                    *reinterpret_cast<float4*>(row + ((j ^ (i & 7)) << 4)) = v;
                 }
             }
+            fence_async_smem();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const int y = (int)(it.obj * kD);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) ms->red[warp] = mx;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            const float M = fmaxf(fmaxf(ms->red[0], ms->red[1]), fmaxf(ms->red[2], ms->red[3]));
-            const int ex = (M > 0.f && isfinite(M)) ? ilogbf(M) : 0;
-            if (ok) {
-                float* T = a.T_tab + obj * kD * kD + (int64_t)i * kD;
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t x[32];
-                    tmem_ld32(tl + 32 * cb, x);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        float y[4];
-#pragma unroll
-                        for (int f = 0; f < 4; ++f)
-                            y[f] = scale_pow2(__uint_as_float(x[e + f]) + (32 * cb + e + f == i ? gci : 0.f), -ex);
-                        *reinterpret_cast<float4*>(T + 32 * cb + e) = make_float4(y[0], y[1], y[2], y[3]);
-                    }
-                }
-                if (i == 0) a.T_exp_tab[obj] = ex;
+            for (int b = 0; b < 4; ++b) {
+                tma_store_2d(&tmT, smem + OFF_STAGE + b * 16384, 32 * b, y);
+                tma_store_2d(&tmS, smem + OFF_STAGE + 65536 + b * 16384, 32 * b, y);
             }
-        } else if (ok) {
-            float* S = a.S_tab + obj * kD * kD + (int64_t)i * kD;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t x[32];
-                tmem_ld32(tl + kD + 32 * cb, x);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(S + 32 * cb + e) = make_float4(
-                        __uint_as_float(x[e]), __uint_as_float(x[e + 1]), __uint_as_float(x[e + 2]),
-                        __uint_as_float(x[e + 3]));
-            }
+            cp_bulk_commit();
         }
     }
+    if (tid == 0) cp_bulk_wait_all();
+    cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -494,6 +730,32 @@ int64_t cap_for(int n_seg, int LH, size_t bytes) {
     return cap;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_kda() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A pair table [rows][128] fp32 as a 2-D tensor: boxes of 32 columns x 128 rows, 128-byte swizzle.
+bool table_map(CUtensorMap* m, float* base, uint64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn_kda();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kD}, es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count_kda() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -542,7 +804,8 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
     int32_t* t_exp = reinterpret_cast<int32_t*>(ws + ly.t_exp);
     float* t_tab = reinterpret_cast<float*>(ws + ly.t_tab);
     float* s_tab = reinterpret_cast<float*>(ws + ly.s_tab);
-    if (sm_count_kda() <= 0) return cudaErrorInvalidDevice;
+    const int sms = sm_count_kda();
+    if (sms <= 0) return cudaErrorInvalidDevice;
     cudaError_t e = cudaFuncSetAttribute(kda_chunk_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -573,7 +836,12 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
             a.S_tab = s_tab;
             a.err = err;
             a.wait_ns = 2000000000ull;
-            kda_chunk_pair_kernel<<<(unsigned)(np * LH), kThreads, kSmemBytes, s>>>(a);
+            a.n_items = (int)(np * LH);
+            const int grid = a.n_items < sms ? a.n_items : sms;
+            CUtensorMap tmT, tmS;
+            if (!table_map(&tmT, t_tab, (uint64_t)np * LH * kD) || !table_map(&tmS, s_tab, (uint64_t)np * LH * kD))
+                return cudaErrorInvalidValue;
+            kda_chunk_pair_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmT, tmS, a);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         ComposeParams c;
