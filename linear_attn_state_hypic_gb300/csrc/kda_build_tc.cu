@@ -174,6 +174,13 @@ __device__ __forceinline__ void store_row8(uint8_t* hi, uint8_t* lo, uint32_t of
     *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// 1 / x to about one ulp (x normal).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // x * 2^e for any int e with the result in range (two exact power-of-two factors).
 __device__ __forceinline__ float scale_pow2(float x, int e) {
     const int e1 = e / 2, e2 = e - e1;
@@ -237,7 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&ms->tmem_base, kTmemCols);
-    if ((int)blockIdx.x < a.n_items) prefetch(smem, ms, a, decode(a, blockIdx.x), tid);
+    Item nxt = {};  // the next item, decoded when its loads are issued
+    if ((int)blockIdx.x < a.n_items) {
+        nxt = decode(a, blockIdx.x);
+        prefetch(smem, ms, a, nxt, tid);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 #pragma unroll 1
     for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-        const Item it = decode(a, item);
+        const Item it = nxt;
         cp_async_wait_all();
         if (tid == 0) cp_bulk_wait_read();  // the previous chunk's stores have read the staging area
         tc_fence_before();
@@ -316,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 8; ++e) {
                     const float kv = __uint_as_float((e & 1) ? (kw[e >> 1] & 0xffff0000u) : (kw[e >> 1] << 16));
                     y[e] = kv * gv[e];
-                    x[e] = kv * __frcp_rn(gv[e]);
+                    x[e] = kv * rcp_approx(gv[e]);
                 }
                 const uint32_t off = (uint32_t)((t >> 3) * 2048 + q8 * 128 + (t & 7) * 16);
                 store_row8(smem + OFF_B, smem + OFF_B + 16384, off, y);
@@ -432,29 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncthreads();
         }
         {
-            // X'^T rows j (K-major over the chunk's tokens), task (octet o, row j): eight tokens
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int task = tid + kThreads * m, j = task & 255, o = task >> 8;
-                const bool isw = j < kD;
-                const int c = isw ? j : j - kD;
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int t = 8 * o + e;
-                    x[e] = isw ? -ms->beta[t] * bf_at(smem + OFF_KB + kb_off(t, c)) *
-                                     *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c))
-                               : ms->beta[t] * bf_at(smem + OFF_VB + (t * kD + c) * 2);
-                }
-                store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 8 * o), x);
-            }
-            fence_async_smem();
-            // Tinv starts as zero; its 16 x 16 diagonal blocks (I + L_II)^-1 by forward substitution
-            // (thread: block I, column r)
+            // warps 0-1: the 16 x 16 diagonal blocks of Tinv, (I + L_II)^-1 by forward substitution
+            // (thread: block I, column r); the other warps: X'^T rows j (K-major over the chunk's
+            // tokens), task (octet o, row j) of eight tokens, and zeros in the blocks above the diagonal
             float* TI = reinterpret_cast<float*>(smem + OFF_TI);
-#pragma unroll
-            for (int m = 0; m < 2; ++m) reinterpret_cast<float4*>(TI)[tid + kThreads * m] = make_float4(0.f, 0.f, 0.f, 0.f);
-            __syncthreads();
             if (tid < 64) {
                 const int I = tid >> 4, r = tid & 15;
                 float y[16];
@@ -467,33 +459,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                     y[t] = acc;
                     TI[(16 * I + t) * kC + 16 * I + r] = acc;
                 }
+            } else {
+                for (int task = tid - 64; task < 2048; task += kThreads - 64) {
+                    const int j = task & 255, o = task >> 8;
+                    const bool isw = j < kD;
+                    const int c = isw ? j : j - kD;
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int t = 8 * o + e;
+                        x[e] = isw ? -ms->beta[t] * bf_at(smem + OFF_KB + kb_off(t, c)) *
+                                         *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c))
+                                   : ms->beta[t] * bf_at(smem + OFF_VB + (t * kD + c) * 2);
+                    }
+                    store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 8 * o), x);
+                }
+                fence_async_smem();
+                // blocks (I, J), I < J: row t = 16 I + tt, columns 16 J .. 16 J + 15 (four float4 each)
+                for (int e = tid - 64; e < 6 * 16 * 4; e += kThreads - 64) {
+                    const int blkp = e >> 6, rem = e & 63, tt = rem >> 2, q4 = rem & 3;
+                    const int I = blkp < 3 ? 0 : (blkp < 5 ? 1 : 2);
+                    const int J = blkp < 3 ? blkp + 1 : (blkp < 5 ? blkp - 1 : 3);
+                    *reinterpret_cast<float4*>(TI + (16 * I + tt) * kC + 16 * J + 4 * q4) = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
         }
         __syncthreads();
         // ---- the staged tiles are read: load the next chunk while this one finishes
-        if (item + (int)gridDim.x < a.n_items) prefetch(smem, ms, a, decode(a, item + gridDim.x), tid);
+        if (item + (int)gridDim.x < a.n_items) {
+            nxt = decode(a, item + gridDim.x);
+            prefetch(smem, ms, a, nxt, tid);
+        }
         {
             // off-diagonal blocks, row block I = 1..3: R_J = sum_{K=J}^{I-1} L_IK Tinv_KJ, then
-            // Tinv_IJ = -Tinv_II R_J
+            // Tinv_IJ = -Tinv_II R_J; thread: column col < 16 I, rows 4 g4 .. 4 g4 + 3 of the block row
             float* TI = reinterpret_cast<float*>(smem + OFF_TI);
             float* R = reinterpret_cast<float*>(smem + OFF_R);
-#pragma unroll 1
+#pragma unroll
             for (int I = 1; I < 4; ++I) {
                 const int w16 = 16 * I;
-                for (int o = tid; o < 16 * w16; o += kThreads) {
-                    const int tt = o / w16, col = o % w16, J = col >> 4;
-                    const float* Lr = L + (w16 + tt) * kC;
-                    float acc = 0.f;
-                    for (int s = 16 * J; s < w16; ++s) acc = fmaf(Lr[s], TI[s * kC + col], acc);
-                    R[tt * 48 + col] = acc;
+                if (tid < 4 * w16) {
+                    const int col = tid % w16, g4 = tid / w16, J = col >> 4;
+                    const float* L0 = L + (w16 + 4 * g4) * kC;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int s4 = 4 * J; s4 < 4 * I; ++s4) {
+                        float tv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) tv[e] = TI[(4 * s4 + e) * kC + col];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 l = *reinterpret_cast<const float4*>(L0 + k * kC + 4 * s4);
+                            acc[k] = fmaf(l.x, tv[0], fmaf(l.y, tv[1], fmaf(l.z, tv[2], fmaf(l.w, tv[3], acc[k]))));
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) R[(4 * g4 + k) * 48 + col] = acc[k];
                 }
                 __syncthreads();
-                for (int o = tid; o < 16 * w16; o += kThreads) {
-                    const int tt = o / w16, col = o % w16;
-                    const float* Dr = TI + (w16 + tt) * kC + w16;
-                    float acc = 0.f;
-                    for (int u = 0; u <= tt; ++u) acc = fmaf(Dr[u], R[u * 48 + col], acc);
-                    TI[(w16 + tt) * kC + col] = -acc;
+                if (tid < 4 * w16) {
+                    const int col = tid % w16, g4 = tid / w16;
+                    const float* D0 = TI + (w16 + 4 * g4) * kC + w16;  // rows of Tinv_II (zero above the diagonal)
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int u4 = 0; u4 <= g4; ++u4) {
+                        float rv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) rv[e] = R[(4 * u4 + e) * 48 + col];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 d = *reinterpret_cast<const float4*>(D0 + k * kC + 4 * u4);
+                            acc[k] = fmaf(d.x, rv[0], fmaf(d.y, rv[1], fmaf(d.z, rv[2], fmaf(d.w, rv[3], acc[k]))));
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) TI[(w16 + 4 * g4 + k) * kC + col] = -acc[k];
                 }
                 __syncthreads();
             }
