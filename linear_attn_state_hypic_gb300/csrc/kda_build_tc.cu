@@ -105,12 +105,10 @@ constexpr uint32_t ID_SOLVE = idesc(1, 128, 64, false, false);  // [-W | U]^T = 
 constexpr float kSafeGC = 0x1p-100f;
 
 struct ChunkArgs {
-    int n_layers, n_heads, seg0, n_items;
+    int n_layers, n_heads, n_items;
     int64_t n_tokens;
-    const int32_t* cu;
-    const int32_t* skip;
-    const int32_t* cu_chunk;   // [batch segments + 1]: first chunk of each segment of the batch
-    const int32_t* chunk_seg;  // [batch chunks]: the segment of each chunk
+    const int64_t* chunk_t0;  // [batch chunks]: first token of each chunk
+    const int32_t* chunk_n;   // [batch chunks]: its tokens (1..64)
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
     const float* g;
@@ -130,11 +128,9 @@ struct Item {
 __device__ __forceinline__ Item decode(const ChunkArgs& a, int item) {
     const int LH = a.n_layers * a.n_heads;
     const int p = item / LH, lh = item % LH;
-    const int seg = a.chunk_seg[p];
-    const int64_t b0 = (int64_t)a.cu[seg] + (a.skip ? a.skip[seg] : 0), b1 = a.cu[seg + 1];
     Item it;
-    it.t0 = b0 + (int64_t)(p - a.cu_chunk[seg - a.seg0]) * kC;
-    it.n = (int)(b1 - it.t0 < kC ? b1 - it.t0 : kC);
+    it.t0 = a.chunk_t0[p];
+    it.n = a.chunk_n[p];
     it.layer = lh / a.n_heads;
     it.head = lh % a.n_heads;
     it.obj = (int64_t)p * LH + lh;
@@ -258,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
     for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
         const Item it = nxt;
+        const bool more = item + (int)gridDim.x < a.n_items;
+        if (more) nxt = decode(a, item + gridDim.x);  // loads issued here, used at the prefetch
         cp_async_wait_all();
-        if (tid == 0) cp_bulk_wait_read();  // the previous chunk's stores have read the staging area
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -281,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 14; e >= 0; --e) sg[e] = sg[e + 1] * al[e + 1];
             ms->btot[blk][c] = pi[15];
+            if (tid == 0) cp_bulk_wait_read();  // the previous chunk's stores have read the staging area
             __syncthreads();
             float E = 1.f, F = 1.f;  // gate products of the blocks before and after this one
 #pragma unroll
@@ -486,10 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         // ---- the staged tiles are read: load the next chunk while this one finishes
-        if (item + (int)gridDim.x < a.n_items) {
-            nxt = decode(a, item + gridDim.x);
-            prefetch(smem, ms, a, nxt, tid);
-        }
+        if (more) prefetch(smem, ms, a, nxt, tid);
         {
             // off-diagonal blocks, row block I = 1..3: R_J = sum_{K=J}^{I-1} L_IK Tinv_KJ, then
             // Tinv_IJ = -Tinv_II R_J; thread: column col < 16 I, rows 4 g4 .. 4 g4 + 3 of the block row
@@ -679,10 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // The batch's chunk index: cu_chunk[i] = first chunk of segment seg0 + i (i <= nseg),
-// chunk_seg[c] = its segment, iota[c] = c.  One block of 1024 threads.
+// chunk_t0[c], chunk_n[c] = the first token and the tokens of chunk c, iota[c] = c.
+// One block of 1024 threads.
 __global__ void __launch_bounds__(1024) kda_batch_plan_kernel(const int32_t* cu, const int32_t* skip, int seg0,
-                                                              int nseg, int32_t* cu_chunk, int32_t* chunk_seg,
-                                                              int32_t* iota) {
+                                                              int nseg, int32_t* cu_chunk, int64_t* chunk_t0,
+                                                              int32_t* chunk_n, int32_t* iota) {
     __shared__ int32_t wsum[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -722,7 +718,11 @@ __global__ void __launch_bounds__(1024) kda_batch_plan_kernel(const int32_t* cu,
     }
     for (int i = tid; i < nseg; i += 1024)
         for (int c = cu_chunk[i]; c < cu_chunk[i + 1]; ++c) {
-            chunk_seg[c] = seg0 + i;
+            const int s = seg0 + i;
+            const int64_t b0 = (int64_t)cu[s] + (skip ? skip[s] : 0) + (int64_t)(c - cu_chunk[i]) * kC;
+            const int64_t rest = cu[s + 1] - b0;
+            chunk_t0[c] = b0;
+            chunk_n[c] = (int32_t)(rest < kC ? rest : kC);
             iota[c] = c;
         }
 }
@@ -742,15 +742,16 @@ void chunk_counts(const BuildParams& p, std::vector<int64_t>& nc, int64_t& total
 }
 
 // Workspace of the tensor-core path for batches of up to `cap` chunks:
-// [build plan][cu_chunk][chunk_seg][iota][T_exp_tab][T_tab][S_tab].
+// [build plan][cu_chunk][chunk_t0][chunk_n][iota][T_exp_tab][T_tab][S_tab].
 struct KdaLayout {
-    size_t cu_chunk, chunk_seg, iota, t_exp, t_tab, s_tab, end;
+    size_t cu_chunk, chunk_t0, chunk_n, iota, t_exp, t_tab, s_tab, end;
 };
 KdaLayout kda_layout(int n_seg, int64_t cap, int LH) {
     KdaLayout l;
     l.cu_chunk = build_workspace_bytes(n_seg);
-    l.chunk_seg = l.cu_chunk + al256(((size_t)n_seg + 1) * 4);
-    l.iota = l.chunk_seg + al256((size_t)cap * 4);
+    l.chunk_t0 = l.cu_chunk + al256(((size_t)n_seg + 1) * 4);
+    l.chunk_n = l.chunk_t0 + al256((size_t)cap * 8);
+    l.iota = l.chunk_n + al256((size_t)cap * 4);
     l.t_exp = l.iota + al256((size_t)cap * 4);
     l.t_tab = l.t_exp + al256((size_t)cap * LH * 4);
     l.s_tab = l.t_tab + (size_t)cap * LH * kD * kD * 4;
@@ -764,7 +765,7 @@ constexpr size_t kTableCap = (size_t)4 << 30;  // bytes of chunk tables the repo
 int64_t cap_for(int n_seg, int LH, size_t bytes) {
     const size_t fixed = kda_layout(n_seg, 0, LH).end;
     if (bytes <= fixed) return 0;
-    const size_t per = (size_t)LH * (kPairBytes + 4) + 8;
+    const size_t per = (size_t)LH * (kPairBytes + 4) + 16;
     int64_t cap = (int64_t)((bytes - fixed) / per);
     while (cap > 0 && kda_layout(n_seg, cap, LH).end > bytes) --cap;  // padding
     return cap;
@@ -839,7 +840,8 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
     const KdaLayout ly = kda_layout(p.n_seg, cap, LH);
     char* ws = static_cast<char*>(workspace);
     int32_t* cu_chunk = reinterpret_cast<int32_t*>(ws + ly.cu_chunk);
-    int32_t* chunk_seg = reinterpret_cast<int32_t*>(ws + ly.chunk_seg);
+    int64_t* chunk_t0 = reinterpret_cast<int64_t*>(ws + ly.chunk_t0);
+    int32_t* chunk_n = reinterpret_cast<int32_t*>(ws + ly.chunk_n);
     int32_t* iota = reinterpret_cast<int32_t*>(ws + ly.iota);
     int32_t* t_exp = reinterpret_cast<int32_t*>(ws + ly.t_exp);
     float* t_tab = reinterpret_cast<float*>(ws + ly.t_tab);
@@ -855,18 +857,15 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
         int64_t np = 0;
         while (s1 < p.n_seg && np + nc[s1] <= cap) np += nc[s1++];
         const int nb = s1 - s0;
-        kda_batch_plan_kernel<<<1, 1024, 0, s>>>(p.cu, p.skip, s0, nb, cu_chunk, chunk_seg, iota);
+        kda_batch_plan_kernel<<<1, 1024, 0, s>>>(p.cu, p.skip, s0, nb, cu_chunk, chunk_t0, chunk_n, iota);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (np > 0) {
             ChunkArgs a;
             a.n_layers = L;
             a.n_heads = H;
-            a.seg0 = s0;
             a.n_tokens = p.n_tokens;
-            a.cu = p.cu;
-            a.skip = p.skip;
-            a.cu_chunk = cu_chunk;
-            a.chunk_seg = chunk_seg;
+            a.chunk_t0 = chunk_t0;
+            a.chunk_n = chunk_n;
             a.k = static_cast<const __nv_bfloat16*>(p.k);
             a.v = static_cast<const __nv_bfloat16*>(p.v);
             a.g = p.g;
