@@ -735,6 +735,78 @@ def time_decay_build(family, steps, warmup, device, n_layers=30, H=32, d=128, n_
             "tflops": n_tokens * LH * 2 * d * d * (2 if family != "vanilla" else 1) / (ms / 1e3) / 1e12}
 
 
+def time_kda_build(steps, warmup, device, n_layers=1, H=32, d=128, n_tokens=100_000):
+    """hypic_segment_build of KDA over the long request's segments (100k tokens,
+    U[512,2048] lengths, no seam window) for n_layers x H heads, bf16 keys and
+    values, per-channel gates a ~ U(0.85, 1), b ~ U(0, 1).  The tensor-core path
+    (chunk pairs, then the compose of each segment's chunks) against the
+    CUDA-core kernel on the same inputs (the no-alloc build runs KDA there).
+    Bytes: algorithmic = keys, values, gates and b in, T and S out; path = that
+    plus the chunk tables (T and S of every 64-token chunk written once, read by
+    the compose's state and transition launches: 64 KB x 5 per chunk and head)."""
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+    from linear_attn_state_hypic_gb300 import synth
+    lengths = synth.long_request_lengths(0, n_tokens)
+    cu = synth.cu_from_lengths(lengths)
+    n_seg = len(lengths)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(0)
+    k = torch.empty((n_layers, n_tokens, H, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    g = torch.empty((n_layers, n_tokens, H, d), dtype=torch.float32, device=device)
+    for layer in range(n_layers):
+        x = torch.randn((n_tokens, H, d), generator=gen, device=device)
+        k[layer] = (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+        v[layer] = torch.randn((n_tokens, H, d), generator=gen, device=device).to(torch.bfloat16)
+        g[layer] = torch.rand((n_tokens, H, d), generator=gen, device=device) * 0.15 + 0.85
+        del x
+    beta = torch.rand((n_layers, n_tokens, H), generator=gen, device=device)
+    out = B.alloc_build_outputs("kda", n_seg, n_layers, H, d, d, device)
+    out2 = B.alloc_build_outputs("kda", n_seg, n_layers, H, d, d, device)
+    a, keep = B.build_args("kda", k, v, cu, g=g, beta=beta, T_out=out[0], T_exp_out=out[1], S_out=out[2])
+    a2, keep2 = B.build_args("kda", k, v, cu, g=g, beta=beta, T_out=out2[0], T_exp_out=out2[1], S_out=out2[2])
+    need = B.hypic_build_workspace_size(a)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+
+    def tc():
+        B._check(B.hypic_segment_build(a, B._ptr(ws), ws.numel(), B._stream(None)))
+
+    def cores():
+        B._check(B.hypic_segment_build_noalloc(a2, B._stream(None)))
+
+    def timed(f, n):
+        for _ in range(warmup):
+            f()
+        torch.cuda.synchronize()
+        B.check_device()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        B.check_device()
+        return e0.elapsed_time(e1) / n
+
+    ms = timed(tc, steps)
+    ms_cores = timed(cores, max(1, steps // 2))
+    S1, S2 = out[2].double(), out2[2].double()
+    rel_s = float((S1 - S2).norm() / S2.norm())
+    LH = n_layers * H
+    n_chunks = int(sum((int(x) + 63) // 64 for x in lengths))
+    algo = n_tokens * LH * (2 * d * 2 + 4 * d + 4) + n_seg * LH * (2 * d * d * 4 + 4)
+    path = algo + n_chunks * LH * 5 * d * d * 4
+    del keep, keep2
+    return {"workload": (f"kda build: {n_layers} layers x {H} heads, d={d}, bf16 k/v, fp32 gates, {n_tokens} tokens "
+                         f"in {n_seg} segments of U[512,2048] tokens ({n_chunks} chunks of 64)"),
+            "ms_per_call": ms, "ms_per_call_cuda_cores": ms_cores, "speedup_vs_cuda_cores": ms_cores / ms,
+            "tokens_per_s": n_tokens / (ms / 1e3), "token_heads_per_s": n_tokens * LH / (ms / 1e3),
+            "workspace_bytes": need, "algorithmic_bytes": algo, "path_bytes": path,
+            "gbs_algorithmic": algo / (ms / 1e3) / 1e9, "gbs_path": path / (ms / 1e3) / 1e9,
+            "rel_S_tc_vs_cuda_cores": rel_s}
+
+
 def run_case(args, device):
     """Single-kernel cases used for profiling (one JSON line each):
     ragged_build -- the build of 32 ragged segments (U[512,2048] tokens) x 32
@@ -742,7 +814,9 @@ def run_case(args, device):
     compose_table -- hypic_compose on the compose table with --layers layers;
     reuse_chain -- hypic_reuse_chain over the long request's chain;
     seam_advance -- hypic_seam_advance on the long request's seams (GDN);
-    decay_build -- a decay family's build at serving scale (--family)."""
+    decay_build -- a decay family's build at serving scale (--family);
+    kda_build -- KDA's build over the long request's segments (--layers), the
+                 tensor-core path against the CUDA-core kernel."""
     import torch
     from linear_attn_state_hypic_gb300 import binding as B
     from linear_attn_state_hypic_gb300 import synth
@@ -751,6 +825,11 @@ def run_case(args, device):
     if args.case == "compose_table":
         r = time_compose_table(args.steps, device, n_layers=args.layers)
         r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
+        print(json.dumps({"case": args.case, **r}))
+        return
+    if args.case == "kda_build":
+        r = time_kda_build(args.steps, args.warmup, device, n_layers=args.layers, n_tokens=args.tokens)
+        r["frac_hbm_path"] = r["gbs_path"] / peaks["hbm_gbs"]
         print(json.dumps({"case": args.case, **r}))
         return
     if args.case == "decay_build":
@@ -819,11 +898,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--no-compose-table", action="store_true")
-    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table", "reuse_chain", "decay_build",
+    ap.add_argument("--case", choices=["long_request", "ragged_build", "compose_table", "reuse_chain", "decay_build", "kda_build",
                                       "seam_advance"],
                     default="long_request",
                     help="long_request is the benchmark; the others time one kernel (for profiling)")
-    ap.add_argument("--layers", type=int, default=30, help="layers of the compose_table, reuse_chain, decay_build cases")
+    ap.add_argument("--tokens", type=int, default=100_000, help="request tokens of the kda_build case")
+    ap.add_argument("--layers", type=int, default=30, help="layers of the compose_table, reuse_chain, decay_build, kda_build cases")
     ap.add_argument("--family", choices=["retnet", "mamba2", "gla", "vanilla"], default="retnet",
                     help="family of the decay_build case")
     args = ap.parse_args()
