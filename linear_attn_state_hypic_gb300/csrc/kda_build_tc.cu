@@ -35,10 +35,11 @@
 //   scan     16-token block products per channel -> g_C, g_t, Kbar^T (bf16 hi + lo operand)
 //   gram     Y, X operands -> G = Y X^T (M = 64, N = 64, K = 128, three products) -> b_t G_ts
 //   solve    Tinv = (I + L)^-1, L_ts = b_t G_ts (16 x 16 diagonal blocks by forward
-//            substitution, the blocks below from them), then [-W | U]^T = X'^T Tinv^T with
-//            x_t = [-b_t k_t g_t | b_t v_t]: M = 128 (twice), N = 64, K = 64 MMAs in hi + lo pairs
-//   MMA      D = Kbar^T [-W | U]: M = 128, N = 256, K = 64 in hi + lo pairs (three
-//            products), fp32 in tensor memory
+//            substitution, the blocks below from them); [-W | U] = Tinv X' with rows
+//            x_t = [-b_t k_t g_t | b_t v_t], so the pair is Kbar^T Tinv X': first
+//            P = Kbar^T Tinv (M = 128, N = 64, K = 64 MMAs in hi + lo pairs)
+//   MMA      D = P X': M = 128, N = 256, K = 64 in hi + lo pairs (three products), fp32 in
+//            tensor memory
 //   write    T_chunk = Diag(g_C) + D_left, normalised by a power of two (its exponent
 //            kept beside it), and S_chunk = D_right, one tensor-memory pass on 16 warps
 // The chunk tables cost 128 KB per chunk, layer and head; segments are taken
@@ -75,11 +76,11 @@ constexpr uint32_t OFF_VB = OFF_KB + 16384;  // values, bf16 [64 t][128 c]
 constexpr uint32_t OFF_GA = OFF_VB + 16384;  // gates, fp32 [64 t][128 c]; chunk q of row t at q ^ (t & 31);
                                              // then g_t when the gram runs on the tensor cores
 constexpr uint32_t OFF_L = OFF_GA + 32768;   // b_t G_ts for s < t, 0 elsewhere: fp32 [64 t][64 s]
-constexpr uint32_t OFF_A = OFF_L + 16384;    // Kbar^T hi, lo: bf16 [128 i][64 t], 16 KB each
-constexpr uint32_t OFF_B = OFF_A + 32768;    // [-W | U]^T hi, lo: bf16 [256 j][64 t], 32 KB each; before
-                                             // them the gram operands Y hi, lo, X hi, lo: bf16 [64 t][128 c]
+constexpr uint32_t OFF_A = OFF_L + 16384;    // Kbar^T, then P = Kbar^T Tinv: hi, lo bf16 [128 i][64 t], 16 KB each
+constexpr uint32_t OFF_B = OFF_A + 32768;    // X'^T hi, lo: bf16 [256 j][64 t], 32 KB each; before them
+                                             // the gram operands Y hi, lo, X hi, lo: bf16 [64 t][128 c]
 constexpr uint32_t OFF_TI = OFF_B + 65536;    // Tinv = (I + L)^-1: fp32 [64 t][64 s]
-constexpr uint32_t OFF_TIO = OFF_TI + 16384;  // Tinv hi, lo: bf16 [64 t][64 s] operand, 8 KB each
+constexpr uint32_t OFF_TIO = OFF_TI + 16384;  // Tinv^T hi, lo: bf16 [64 t][64 s] operand, 8 KB each
 constexpr uint32_t OFF_R = OFF_TIO + 16384;   // solve scratch: fp32 [16][48]
 constexpr uint32_t OFF_MISC = OFF_R + 3072;
 constexpr uint32_t OFF_STAGE = OFF_A;         // T_chunk, S_chunk boxes for the TMA stores (128 KB over
@@ -99,9 +100,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_PAIR = 0, TM_GRAM = 256, TM_SOLVE = 384;
-constexpr uint32_t ID_PAIR = idesc(1, 128, 256, false, false);  // D = Kbar^T [-W | U], both K-major
+constexpr uint32_t ID_PAIR = idesc(1, 128, 256, false, false);  // D = P X' = Kbar^T [-W | U], both K-major
 constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);    // G = Y X^T, both K-major
-constexpr uint32_t ID_SOLVE = idesc(1, 128, 64, false, false);  // [-W | U]^T = X'^T Tinv^T, half of the rows
+constexpr uint32_t ID_SOLVE = idesc(1, 128, 64, false, false);  // P = Kbar^T Tinv
 constexpr float kSafeGC = 0x1p-100f;
 
 struct ChunkArgs {
@@ -419,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
 
-        // ---- solve: (I + L) [-W | U] = X' with rows x_t = [-b_t k_t g_t | b_t v_t], as
-        // [-W | U]^T = X'^T Tinv^T on the tensor cores, Tinv = (I + L)^-1 formed on CUDA cores.
+        // ---- solve: (I + L) [-W | U] = X' with rows x_t = [-b_t k_t g_t | b_t v_t]: Tinv = (I + L)^-1
+        // formed on CUDA cores, then Kbar^T [-W | U] = (Kbar^T Tinv) X' on the tensor cores.
         if (!safe) {  // the gates were kept for the CUDA-core gram: now g_t as on the other path
             const int c = tid & (kD - 1), blk = tid >> 7;
             float E = 1.f, gp[16];
@@ -532,12 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncthreads();
             }
-            // Tinv as the bf16 hi + lo operand (rows t, K-major over s): task (row t, octet o)
+            // Tinv^T as the bf16 hi + lo operand (rows t, K-major over s: Tinv[s][t]): task (row t, octet o)
             {
-                const int t = tid >> 3, o = tid & 7;
-                const float4 a0 = *reinterpret_cast<const float4*>(TI + t * kC + 8 * o);
-                const float4 a1 = *reinterpret_cast<const float4*>(TI + t * kC + 8 * o + 4);
-                const float x[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const int t = tid & 63, o = tid >> 6;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = TI[(8 * o + e) * kC + t];
                 store_row8(smem + OFF_TIO, smem + OFF_TIO + 8192, core_off(t, 8 * o), x);
             }
             fence_async_smem();
@@ -545,21 +546,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        // P = Kbar^T Tinv (M = 128, N = 64, K = 64 in hi + lo pairs), then P as the A operand in place
+        // of Kbar^T: the pair is D = P X'.
         if (tid == 0) {
             const uint32_t sb = smem_u32(smem);
-            const uint32_t xh = sb + OFF_B, xl = xh + 32768, th = sb + OFF_TIO, tlo = th + 8192;
+            const uint32_t ah = sb + OFF_A, al = ah + 16384, th = sb + OFF_TIO, tlo = th + 8192;
 #pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf)
-#pragma unroll 1
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t dxh = sdesc_plain(xh + 16384 * hf + 256 * kk, 128, 1024),
-                                   dxl = sdesc_plain(xl + 16384 * hf + 256 * kk, 128, 1024);
-                    const uint64_t dth = sdesc_plain(th + 256 * kk, 128, 1024), dtl = sdesc_plain(tlo + 256 * kk, 128, 1024);
-                    const uint32_t d = tmem + TM_SOLVE + 64 * hf;
-                    mma_bf16_ss(d, dxh, dth, ID_SOLVE, kk > 0);
-                    mma_bf16_ss(d, dxh, dtl, ID_SOLVE, true);
-                    mma_bf16_ss(d, dxl, dth, ID_SOLVE, true);
-                }
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t dah = sdesc_plain(ah + 256 * kk, 128, 1024), dal = sdesc_plain(al + 256 * kk, 128, 1024);
+                const uint64_t dth = sdesc_plain(th + 256 * kk, 128, 1024), dtl = sdesc_plain(tlo + 256 * kk, 128, 1024);
+                mma_bf16_ss(tmem + TM_SOLVE, dah, dth, ID_SOLVE, kk > 0);
+                mma_bf16_ss(tmem + TM_SOLVE, dah, dtl, ID_SOLVE, true);
+                mma_bf16_ss(tmem + TM_SOLVE, dal, dth, ID_SOLVE, true);
+            }
             mma_commit(&ms->solve_done);
         }
         __syncwarp();
@@ -569,17 +568,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         {
-            // [-W | U]^T into the B operand: warp (quarter q, half hf, token half ch)
-            const int q = warp & 3, hf = (warp >> 2) & 1, ch = warp >> 3, j = 128 * hf + 32 * q + lane;
-            uint32_t xv[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + TM_SOLVE + 64 * hf + 32 * ch, xv);
+            // warp (quarter q, token quarter cq): rows i = 32 q + lane, tokens 16 cq .. 16 cq + 15
+            const int q = warp & 3, cq = warp >> 2, i = 32 * q + lane;
+            uint32_t xv[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + TM_SOLVE + 16 * cq, xv);
             tmem_wait_ld();
 #pragma unroll
-            for (int o = 0; o < 4; ++o) {
+            for (int o = 0; o < 2; ++o) {
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(xv[8 * o + e]);
-                store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 32 * ch + 8 * o), x);
+                store_row8(smem + OFF_A, smem + OFF_A + 16384, core_off(i, 16 * cq + 8 * o), x);
             }
             fence_async_smem();
         }
@@ -587,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         tc_fence_after();
 
-        // ---- MMA: D = Kbar^T [-W | U] = hi hi + hi lo + lo hi, four steps of 16 tokens
+        // ---- MMA: D = P X' = Kbar^T [-W | U], hi hi + hi lo + lo hi, four steps of 16 tokens
         if (tid == 0) {
             const uint32_t sb = smem_u32(smem);
             const uint32_t ah = sb + OFF_A, al = ah + 16384, bh = sb + OFF_B, bl = bh + 32768;
