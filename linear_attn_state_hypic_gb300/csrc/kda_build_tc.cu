@@ -498,8 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col = tid % w16, g4 = tid / w16, J = col >> 4;
                     const float* L0 = L + (w16 + 4 * g4) * kC;
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int s4 = 4 * J; s4 < 4 * I; ++s4) {
+#pragma unroll
+                    for (int s4 = 0; s4 < 4 * I; ++s4) {
+                        if (s4 < 4 * J) continue;  // the blocks left of J hold no term
                         float tv[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) tv[e] = TI[(4 * s4 + e) * kC + col];
@@ -517,8 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col = tid % w16, g4 = tid / w16;
                     const float* D0 = TI + (w16 + 4 * g4) * kC + w16;  // rows of Tinv_II (zero above the diagonal)
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int u4 = 0; u4 <= g4; ++u4) {
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        if (u4 > g4) break;  // Tinv_II is zero above its diagonal
                         float rv[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) rv[e] = R[(4 * u4 + e) * 48 + col];
