@@ -198,20 +198,21 @@ __device__ __noinline__ bool wait_done(uint64_t* bar, uint32_t parity, uint64_t 
 
 // The chunk's keys, values and gates (rows past the body end zero-filled) and
 // b, by cp.async of every thread.
+template <int kNthr>
 __device__ __forceinline__ void prefetch(uint8_t* smem, KMisc* ms, const ChunkArgs& a, const Item& it, int tid) {
     const int64_t rs = (int64_t)a.n_heads * kD;
     const int64_t row0 = tok_row(it.layer, it.t0, it.head, a.n_tokens, a.n_heads) * kD;
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int e = tid + kThreads * m, t = e >> 4, q = e & 15;
+    for (int m = 0; m < 1024 / kNthr; ++m) {
+        const int e = tid + kNthr * m, t = e >> 4, q = e & 15;
         const bool ok = t < it.n;
         const int64_t off = ok ? row0 + t * rs + 8 * q : row0;
         cp_async16_zfill(smem + OFF_KB + t * 256 + ((q ^ (t & 15)) << 4), a.k + off, ok);
         cp_async16_zfill(smem + OFF_VB + t * 256 + q * 16, a.v + off, ok);
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int e = tid + kThreads * m, t = e >> 5, q = e & 31;
+    for (int m = 0; m < 2048 / kNthr; ++m) {
+        const int e = tid + kNthr * m, t = e >> 5, q = e & 31;
         const bool ok = t < it.n;
         cp_async16_zfill(smem + OFF_GA + t * 512 + ((q ^ (t & 31)) << 4), a.g + (ok ? row0 + t * rs + 4 * q : row0), ok);
     }
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Item nxt = {};  // the next item, decoded when its loads are issued
     if ((int)blockIdx.x < a.n_items) {
         nxt = decode(a, blockIdx.x);
-        prefetch(smem, ms, a, nxt, tid);
+        prefetch<kThreads>(smem, ms, a, nxt, tid);
     }
     tc_fence_before();
     __syncthreads();
@@ -484,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        // ---- the staged tiles are read: load the next chunk while this one finishes
-        if (more) prefetch(smem, ms, a, nxt, tid);
-        {
+        // ---- the staged tiles are read: warps 8-15 load the next chunk while warps 0-7 finish Tinv
+        if (warp >= 8) {
+            if (more) prefetch<kThreads / 2>(smem, ms, a, nxt, tid - kThreads / 2);
+        } else {
             // off-diagonal blocks, row block I = 1..3: R_J = sum_{K=J}^{I-1} L_IK Tinv_KJ, then
             // Tinv_IJ = -Tinv_II R_J; thread: column col < 16 I, rows 4 g4 .. 4 g4 + 3 of the block row
             float* TI = reinterpret_cast<float*>(smem + OFF_TI);
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) R[(4 * g4 + k) * 48 + col] = acc[k];
                 }
-                __syncthreads();
+                asm volatile("bar.sync 2, 256;" ::: "memory");
                 if (tid < 4 * w16) {
                     const int col = tid % w16, g4 = tid / w16;
                     const float* D0 = TI + (w16 + 4 * g4) * kC + w16;  // rows of Tinv_II (zero above the diagonal)
@@ -533,11 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) TI[(w16 + 4 * g4 + k) * kC + col] = -acc[k];
                 }
-                __syncthreads();
+                asm volatile("bar.sync 2, 256;" ::: "memory");
             }
             // Tinv^T as the bf16 hi + lo operand (rows t, K-major over s: Tinv[s][t]): task (row t, octet o)
-            {
-                const int t = tid & 63, o = tid >> 6;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int task = tid + 256 * m, t = task & 63, o = task >> 6;
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = TI[(8 * o + e) * kC + t];
