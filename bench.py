@@ -847,6 +847,15 @@ def run_case(args, device):
         r["frac_hbm"] = r["gbs_algorithmic"] / peaks["hbm_gbs"]
         print(json.dumps({"case": args.case, **r}))
         return
+    print(json.dumps({"case": args.case, **time_ragged_build(args.steps, args.warmup, device, peaks, peak_src)}))
+
+
+def time_ragged_build(steps, warmup, device, peaks, peak_src):
+    """hypic_segment_build of GDN on 32 ragged segments (U[512,2048] tokens) x 32 heads, d=128,
+    bf16, one layer: the build kernel alone at a small scale, against the bf16 peaks."""
+    import torch
+    from linear_attn_state_hypic_gb300 import binding as B
+    from linear_attn_state_hypic_gb300 import synth
     inp = synth.gdn_ragged(seed=0)
     k = torch.from_numpy(inp["k"]).to(torch.bfloat16).to(device)
     v = torch.from_numpy(inp["v"]).to(torch.bfloat16).to(device)
@@ -854,23 +863,24 @@ def run_case(args, device):
     b = torch.from_numpy(inp["beta"]).to(device)
     cu = inp["cu_seqlens"]
     out = B.alloc_build_outputs("gdn", len(cu) - 1, 1, 32, 128, 128, device)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         B.segment_build("gdn", k, v, cu, alpha=a, beta=b, out=out)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         B.segment_build("gdn", k, v, cu, alpha=a, beta=b, out=out)
     e1.record()
     torch.cuda.synchronize()
     B.check_device()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     ntok = int(cu[-1])
     tf = ntok * 32 * FLOP_PER_TOKEN_HEAD / (ms / 1e3) / 1e12
-    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    print(json.dumps({"case": args.case, "ms_per_call": ms, "tokens": ntok, "heads": 32,
-                      "tokens_per_s": ntok / (ms / 1e3), "tflops": tf, "frac_bf16": tf / peak_t,
-                      "peak_source": peak_src}))
+    return {"workload": "GDN build: 32 segments of U[512,2048] tokens x 32 heads, d=128, bf16 k/v, one layer",
+            "ms_per_call": ms, "tokens": ntok, "heads": 32, "tokens_per_s": ntok / (ms / 1e3), "tflops": tf,
+            "frac_bf16_burst": tf / peaks["bf16_tflops"],
+            "frac_bf16_sustained": tf / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+            "peak_source": peak_src}
 
 
 def workload_config(n_seg=None):
@@ -1018,6 +1028,7 @@ def main():
         ctab["no_sharing"] = ns
     if rank != 0:
         return
+    ragged = time_ragged_build(max(3, args.steps), args.warmup, device, peaks, peak_src)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -1039,7 +1050,7 @@ def main():
                      "traffic_note": "dram bytes per launch, scaled from an ncu capture of a 32x32 ragged batch",
                      "peak_source": f"{peak_src} bf16 burst (the kernel is timed alone, per call)",
                      "frac_of_sustained": build_tflops / peak_ts, "flop_per_token_head": FLOP_PER_TOKEN_HEAD},
-        "compose_table": ctab,
+        "compose_table": ctab, "ragged_build": ragged,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": res["launches"], "clocks": res["clocks"],
     }
     print(json.dumps(line))
