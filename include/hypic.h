@@ -154,8 +154,9 @@ typedef struct {
 /* Bytes of device scratch the build needs for these arguments: the plan and
    work counter (a few KB); for KDA at dk = dv = 128 with bf16 k and v also the
    tables of its tensor-core path, 128 KB per 64-token chunk, layer and head,
-   for at most 4 GiB of chunks at a time (more only when one segment alone
-   needs more).  Returns 0 when the arguments are invalid. */
+   for at most 4 GiB of chunks at a time (a longer segment is built in parts,
+   each chained after the pair of the parts before it).  Returns 0 when the
+   arguments are invalid. */
 HYPIC_API size_t hypic_build_workspace_size(const hypic_build_args* args);
 
 /* Launch the build on `stream`.  `workspace` is device memory of at least

@@ -43,7 +43,9 @@
 //   write    T_chunk = Diag(g_C) + D_left, normalised by a power of two (its exponent
 //            kept beside it), and S_chunk = D_right, one tensor-memory pass on 16 warps
 // The chunk tables cost 128 KB per chunk, layer and head; segments are taken
-// in batches whose tables fit the workspace.
+// in batches whose tables fit the workspace (up to 4 GiB of them), and a
+// segment longer than a batch in parts: each part's chain starts with the pair
+// of the parts before it, copied into the table's first slot.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -731,6 +733,24 @@ __global__ void __launch_bounds__(1024) kda_batch_plan_kernel(const int32_t* cu,
         }
 }
 
+// One part of a segment too long for a batch: chunks c0 .. c0 + m - 1 of segment `seg` into
+// table slots off .. off + m - 1 (slot 0 holds the pair of the chunks before them when off = 1),
+// cu_chunk = {0, off + m}, iota over the off + m slots.  One block.
+__global__ void kda_part_plan_kernel(const int32_t* cu, const int32_t* skip, int seg, int64_t c0, int m, int off,
+                                     int32_t* cu_chunk, int64_t* chunk_t0, int32_t* chunk_n, int32_t* iota) {
+    const int64_t b0 = (int64_t)cu[seg] + (skip ? skip[seg] : 0), b1 = cu[seg + 1];
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+        const int64_t t0 = b0 + (c0 + i) * kC, rest = b1 - t0;
+        chunk_t0[off + i] = t0;
+        chunk_n[off + i] = (int32_t)(rest < kC ? rest : kC);
+    }
+    for (int j = threadIdx.x; j < off + m; j += blockDim.x) iota[j] = j;
+    if (threadIdx.x == 0) {
+        cu_chunk[0] = 0;
+        cu_chunk[1] = off + m;
+    }
+}
+
 size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Chunks of each segment's body and the largest of them, from the host copies.
@@ -810,6 +830,15 @@ int sm_count_kda() {
 
 }  // namespace
 
+// Chunks a batch of the reported workspace holds: all of them, up to 4 GiB of tables, and at
+// least 2 (a part of a long segment needs the pair before it plus one chunk).
+int64_t reported_cap(const BuildParams& p, int64_t total) {
+    const int64_t LH = (int64_t)p.n_layers * p.n_heads;
+    const int64_t by_cap = (int64_t)(kTableCap / ((size_t)LH * kPairBytes));
+    int64_t cap = total < by_cap ? total : by_cap;
+    return cap < 2 ? 2 : cap;
+}
+
 bool kda_build_tc_supported(const BuildParams& p) {
     if (!(p.family == kKDA && p.dk == kD && p.dv == kD && p.in_dtype == kBF16 && p.n_tokens > 0 && p.cu_host &&
           p.g && p.beta && (reinterpret_cast<uintptr_t>(p.g) & 15u) == 0))
@@ -818,19 +847,15 @@ bool kda_build_tc_supported(const BuildParams& p) {
     int64_t total, most;
     chunk_counts(p, nc, total, most);
     const int64_t LH = (int64_t)p.n_layers * p.n_heads;
-    // one segment's chunk pairs must fit a compose table (32-bit TMA row index)
-    return total > 0 && most * LH * kD < INT32_MAX;
+    // a batch's chunk tables as one compose table (32-bit TMA row index)
+    return total > 0 && reported_cap(p, total) * LH * kD < INT32_MAX;
 }
 
 size_t kda_build_tc_workspace_bytes(const BuildParams& p) {
     std::vector<int64_t> nc;
     int64_t total, most;
     chunk_counts(p, nc, total, most);
-    const int LH = p.n_layers * p.n_heads;
-    const int64_t by_cap = (int64_t)(kTableCap / ((size_t)LH * kPairBytes));
-    int64_t cap = total < by_cap ? total : by_cap;
-    if (cap < most) cap = most;
-    return kda_layout(p.n_seg, cap, LH).end;
+    return kda_layout(p.n_seg, reported_cap(p, total), p.n_layers * p.n_heads).end;
 }
 
 cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t workspace_bytes, unsigned* err,
@@ -840,7 +865,7 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
     chunk_counts(p, nc, total, most);
     const int L = p.n_layers, H = p.n_heads, LH = L * H;
     const int64_t cap = cap_for(p.n_seg, LH, workspace_bytes);
-    if (cap < most || total == 0) return cudaErrorInvalidValue;
+    if (cap < 2 || total == 0) return cudaErrorInvalidValue;
     const KdaLayout ly = kda_layout(p.n_seg, cap, LH);
     char* ws = static_cast<char*>(workspace);
     int32_t* cu_chunk = reinterpret_cast<int32_t*>(ws + ly.cu_chunk);
@@ -856,37 +881,34 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t plane = (int64_t)kD * kD;
-    for (int s0 = 0; s0 < p.n_seg;) {
-        int s1 = s0;
-        int64_t np = 0;
-        while (s1 < p.n_seg && np + nc[s1] <= cap) np += nc[s1++];
-        const int nb = s1 - s0;
-        kda_batch_plan_kernel<<<1, 1024, 0, s>>>(p.cu, p.skip, s0, nb, cu_chunk, chunk_t0, chunk_n, iota);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (np > 0) {
-            ChunkArgs a;
-            a.n_layers = L;
-            a.n_heads = H;
-            a.n_tokens = p.n_tokens;
-            a.chunk_t0 = chunk_t0;
-            a.chunk_n = chunk_n;
-            a.k = static_cast<const __nv_bfloat16*>(p.k);
-            a.v = static_cast<const __nv_bfloat16*>(p.v);
-            a.g = p.g;
-            a.beta = p.beta;
-            a.T_tab = t_tab;
-            a.T_exp_tab = t_exp;
-            a.S_tab = s_tab;
-            a.err = err;
-            a.wait_ns = 2000000000ull;
-            a.n_items = (int)(np * LH);
-            const int grid = a.n_items < sms ? a.n_items : sms;
-            CUtensorMap tmT, tmS;
-            if (!table_map(&tmT, t_tab, (uint64_t)np * LH * kD) || !table_map(&tmS, s_tab, (uint64_t)np * LH * kD))
-                return cudaErrorInvalidValue;
-            kda_chunk_pair_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmT, tmS, a);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        }
+
+    // The pairs of np chunks (already planned) into table slots off .. off + np - 1.
+    auto chunk_pairs = [&](int64_t np, int64_t off) -> cudaError_t {
+        ChunkArgs a;
+        a.n_layers = L;
+        a.n_heads = H;
+        a.n_tokens = p.n_tokens;
+        a.chunk_t0 = chunk_t0 + off;
+        a.chunk_n = chunk_n + off;
+        a.k = static_cast<const __nv_bfloat16*>(p.k);
+        a.v = static_cast<const __nv_bfloat16*>(p.v);
+        a.g = p.g;
+        a.beta = p.beta;
+        a.T_tab = t_tab + off * LH * plane;
+        a.T_exp_tab = t_exp + off * LH;
+        a.S_tab = s_tab + off * LH * plane;
+        a.err = err;
+        a.wait_ns = 2000000000ull;
+        a.n_items = (int)(np * LH);
+        const int grid = a.n_items < sms ? a.n_items : sms;
+        CUtensorMap tmT, tmS;
+        if (!table_map(&tmT, a.T_tab, (uint64_t)np * LH * kD) || !table_map(&tmS, a.S_tab, (uint64_t)np * LH * kD))
+            return cudaErrorInvalidValue;
+        kda_chunk_pair_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmT, tmS, a);
+        return cudaGetLastError();
+    };
+    // Chains cu_chunk[0..nb] over the np table slots into the outputs of segments s0 .. s0 + nb - 1.
+    auto compose = [&](int s0, int nb, int64_t np) -> cudaError_t {
         ComposeParams c;
         c.family = kKDA;
         c.n_layers = L;
@@ -903,8 +925,45 @@ cudaError_t launch_kda_build_tc(const BuildParams& p, void* workspace, size_t wo
         c.S_out = p.S_out + (int64_t)s0 * LH * plane;
         c.T_out = p.T_out + (int64_t)s0 * LH * plane;
         c.T_exp_out = p.T_exp + (int64_t)s0 * LH;
-        e = np > 0 && compose_tc_supported(c) ? launch_compose_tc(c, err, s) : launch_compose_simt(c, err, s);
-        if (e != cudaSuccess) return e;
+        return np > 0 && compose_tc_supported(c) ? launch_compose_tc(c, err, s) : launch_compose_simt(c, err, s);
+    };
+
+    for (int s0 = 0; s0 < p.n_seg;) {
+        if (nc[s0] > cap) {
+            // A segment longer than a batch, in parts: the first part's chunks from slot 0, each later
+            // part's after slot 0, which holds the segment's pair so far (the composition law makes
+            // that pair followed by the part's chunks the pair of everything up to the part's end).
+            for (int64_t c0 = 0; c0 < nc[s0];) {
+                const int off = c0 > 0 ? 1 : 0;
+                const int64_t m = (nc[s0] - c0 < cap - off) ? nc[s0] - c0 : cap - off;
+                if (off) {
+                    const size_t tb = (size_t)LH * plane * sizeof(float);
+                    if ((e = cudaMemcpyAsync(t_tab, p.T_out + (int64_t)s0 * LH * plane, tb, cudaMemcpyDeviceToDevice,
+                                             s)) != cudaSuccess ||
+                        (e = cudaMemcpyAsync(t_exp, p.T_exp + (int64_t)s0 * LH, (size_t)LH * sizeof(int32_t),
+                                             cudaMemcpyDeviceToDevice, s)) != cudaSuccess ||
+                        (e = cudaMemcpyAsync(s_tab, p.S_out + (int64_t)s0 * LH * plane, tb, cudaMemcpyDeviceToDevice,
+                                             s)) != cudaSuccess)
+                        return e;
+                }
+                kda_part_plan_kernel<<<1, 256, 0, s>>>(p.cu, p.skip, s0, c0, (int)m, off, cu_chunk, chunk_t0, chunk_n,
+                                                       iota);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+                if ((e = chunk_pairs(m, off)) != cudaSuccess) return e;
+                if ((e = compose(s0, 1, m + off)) != cudaSuccess) return e;
+                c0 += m;
+            }
+            ++s0;
+            continue;
+        }
+        int s1 = s0;
+        int64_t np = 0;
+        while (s1 < p.n_seg && nc[s1] <= cap && np + nc[s1] <= cap) np += nc[s1++];
+        const int nb = s1 - s0;
+        kda_batch_plan_kernel<<<1, 1024, 0, s>>>(p.cu, p.skip, s0, nb, cu_chunk, chunk_t0, chunk_n, iota);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (np > 0 && (e = chunk_pairs(np, 0)) != cudaSuccess) return e;
+        if ((e = compose(s0, nb, np)) != cudaSuccess) return e;
         s0 = s1;
     }
     return cudaSuccess;

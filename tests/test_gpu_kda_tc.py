@@ -113,3 +113,25 @@ def test_kda_tc_matches_cuda_core_build_over_batches(B):
                                  beta=np.ascontiguousarray(bb))
         assert_rel(host(S)[s:s + 1, :, :4], So, TOL_BF16, what=f"S of segment {s}")
         assert_rel(gdn_T64(T, T_exp)[s:s + 1, :, :4], To, TOL_BF16, what=f"T of segment {s}")
+
+
+def test_kda_tc_segment_longer_than_a_batch(B):
+    """A segment whose chunk tables alone exceed the 4 GiB the workspace holds
+    (36,000 tokens x 64 heads: 563 chunks of 64 x 64 heads x 128 KB), between
+    two short ones: the tensor-core path builds it in parts, each chained after
+    the pair of the parts before it (composition law).  Gates near 1 keep T_C
+    of the long segment inside the fp64 range of the oracle.  Every pair agrees
+    with the CUDA-core build; two heads of the long segment with the oracle."""
+    rng = np.random.default_rng(405)
+    lengths = [300, 36000, 200]
+    cu, k, v, g, beta = kda_inputs(rng, lengths, 1, 64, glo=0.999)
+    assert ((36000 + 63) // 64) * 64 * 128 * 1024 > 4 << 30
+    T, T_exp, S = build(B, k, v, g, beta, cu)
+    Tn, Tn_exp, Sn = build(B, k, v, g, beta, cu, noalloc=True)
+    assert_rel(host(S), host(Sn), 1e-3, what="S, tensor cores vs CUDA cores")
+    assert_rel(gdn_T64(T, T_exp), gdn_T64(Tn, Tn_exp), 1e-3, what="T, tensor cores vs CUDA cores")
+    sl = slice(int(cu[1]), int(cu[2]))
+    kk, vv, gg, bb = (np.ascontiguousarray(x[:, sl, :2]) for x in (k, v, g, beta))
+    To, So = orc.build_pairs("kda", kk, vv, np.array([0, sl.stop - sl.start], np.int32), g=gg, beta=bb)
+    assert_rel(host(S)[1:2, :, :2], So, TOL_BF16, what="S of the long segment")
+    assert_rel(gdn_T64(T, T_exp)[1:2, :, :2], To, TOL_BF16, what="T of the long segment")
