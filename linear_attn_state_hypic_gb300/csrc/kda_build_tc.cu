@@ -31,7 +31,8 @@
 // products of the gates (k_s times the gates after s, met by every later key),
 // exact for any gate.
 // Steps of a chunk (512 threads; persistent CTAs, the next chunk's keys,
-// values, gates and b loaded by cp.async while this one finishes):
+// values, gates and b loaded by cp.async on warps 8-15 while warps 0-7 finish
+// Tinv):
 //   scan     16-token block products per channel -> g_C, g_t, Kbar^T (bf16 hi + lo operand)
 //   gram     Y, X operands -> G = Y X^T (M = 64, N = 64, K = 128, three products) -> b_t G_ts
 //   solve    Tinv = (I + L)^-1, L_ts = b_t G_ts (16 x 16 diagonal blocks by forward
@@ -41,7 +42,8 @@
 //   MMA      D = P X': M = 128, N = 256, K = 64 in hi + lo pairs (three products), fp32 in
 //            tensor memory
 //   write    T_chunk = Diag(g_C) + D_left, normalised by a power of two (its exponent
-//            kept beside it), and S_chunk = D_right, one tensor-memory pass on 16 warps
+//            kept beside it), and S_chunk = D_right, one tensor-memory pass on 16 warps into
+//            128-byte-swizzled boxes over the spent operands, written out by TMA tile stores
 // The chunk tables cost 128 KB per chunk, layer and head; segments are taken
 // in batches whose tables fit the workspace (up to 4 GiB of them), and a
 // segment longer than a batch in parts: each part's chain starts with the pair
