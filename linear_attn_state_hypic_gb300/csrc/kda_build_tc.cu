@@ -80,15 +80,18 @@ constexpr uint32_t OFF_VB = OFF_KB + 16384;  // values, bf16 [64 t][128 c]
 constexpr uint32_t OFF_GA = OFF_VB + 16384;  // gates, fp32 [64 t][128 c]; chunk q of row t at q ^ (t & 31);
                                              // then g_t when the gram runs on the tensor cores
 constexpr uint32_t OFF_L = OFF_GA + 32768;   // b_t G_ts for s < t, 0 elsewhere: fp32 [64 t][64 s]
-constexpr uint32_t OFF_A = OFF_L + 16384;    // Kbar^T, then P = Kbar^T Tinv: hi, lo bf16 [128 i][64 t], 16 KB each
-constexpr uint32_t OFF_B = OFF_A + 32768;    // X'^T hi, lo: bf16 [256 j][64 t], 32 KB each; before them
+constexpr uint32_t OFF_B = OFF_L + 16384;    // X'^T hi, lo: bf16 [256 j][64 t], 32 KB each; before them
                                              // the gram operands Y hi, lo, X hi, lo: bf16 [64 t][128 c]
-constexpr uint32_t OFF_TI = OFF_B + 65536;    // Tinv = (I + L)^-1: fp32 [64 t][64 s]
+constexpr uint32_t OFF_A = OFF_B + 65536;    // Kbar^T, then P = Kbar^T Tinv: hi, lo bf16 [128 i][64 t], 16 KB each
+constexpr uint32_t OFF_TI = OFF_A + 32768;    // Tinv = (I + L)^-1: fp32 [64 t][64 s]
 constexpr uint32_t OFF_TIO = OFF_TI + 16384;  // Tinv^T hi, lo: bf16 [64 t][64 s] operand, 8 KB each
 constexpr uint32_t OFF_R = OFF_TIO + 16384;   // solve scratch: fp32 [16][48]
 constexpr uint32_t OFF_MISC = OFF_R + 3072;
-constexpr uint32_t OFF_STAGE = OFF_A;         // T_chunk, S_chunk boxes for the TMA stores (128 KB over
-                                              // the operands, read by then): 4 + 4 boxes of 128 rows x 32
+constexpr uint32_t OFF_STAGE_S = OFF_B;       // S_chunk as 4 boxes of 128 rows x 32 (128-byte swizzle) over
+                                              // X'^T; its stores go first, so the next chunk's gram operands
+                                              // find the region read
+constexpr uint32_t OFF_STAGE_T = OFF_A;       // T_chunk's 4 boxes over P, Tinv and its operand (64 KB), free
+                                              // in the next chunk until its X' stage
 
 struct KMisc {
     uint64_t gram_done, solve_done, pair_done;
@@ -262,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = nxt;
         const bool more = item + (int)gridDim.x < a.n_items;
         if (more) nxt = decode(a, item + gridDim.x);  // loads issued here, used at the prefetch
-        cp_async_wait_all();
+        // After the first chunk only warps 8-15 have loads in flight (they issue the prefetch); in
+        // thread 0 the wait would also cover the pair's bulk stores.
+        if (item == (int)blockIdx.x || warp >= 8) cp_async_wait_all();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 14; e >= 0; --e) sg[e] = sg[e + 1] * al[e + 1];
             ms->btot[blk][c] = pi[15];
-            if (tid == 0) cp_bulk_wait_read();  // the previous chunk's stores have read the staging area
+            if (tid == 0) cp_bulk_wait_read_n<1>();  // the previous chunk's S stores have read their boxes
             __syncthreads();
             float E = 1.f, F = 1.f;  // gate products of the blocks before and after this one
 #pragma unroll
@@ -295,23 +300,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float gC = ((ms->btot[0][c] * ms->btot[1][c]) * ms->btot[2][c]) * ms->btot[3][c];
             if (blk == 0) ms->gC[c] = gC;
-            uint8_t* ahi = smem + OFF_A;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int tt = 8 * h + e;
-                    x[e] = bf_at(smem + OFF_KB + kb_off(16 * blk + tt, c)) * (sg[tt] * F);
-                }
-                store_row8(ahi, ahi + 16384, core_off(c, 16 * blk + 8 * h), x);
-            }
-            fence_async_smem();
             safe = __syncthreads_and(gC >= kSafeGC) != 0;
-            if (safe)
+            if (safe) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     *reinterpret_cast<float*>(smem + OFF_GA + ga_off(16 * blk + e, c)) = E * pi[e];
+            } else {
+                // Kbar^T from the gates themselves (k_t g_C / g_t is not in range here), once the previous
+                // chunk's T stores have read the A region; the other path forms it beside the gram MMAs
+                if (tid == 0) cp_bulk_wait_read();
+                __syncthreads();
+                uint8_t* ahi = smem + OFF_A;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int tt = 8 * h + e;
+                        x[e] = bf_at(smem + OFF_KB + kb_off(16 * blk + tt, c)) * (sg[tt] * F);
+                    }
+                    store_row8(ahi, ahi + 16384, core_off(c, 16 * blk + 8 * h), x);
+                }
+                fence_async_smem();
+            }
         }
 
         if (safe) {
@@ -353,6 +364,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&ms->gram_done);
             }
+            // Kbar^T (k_t g_C / g_t) while the gram's MMAs run, once the previous chunk's T stores have
+            // read the A region: task (row i, tokens 8 o ..)
+            if (tid == 0) cp_bulk_wait_read();
+            __syncthreads();
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int task = tid + kThreads * m, i = task & (kD - 1), o = task >> 7;
+                const float gci = ms->gC[i];
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int t = 8 * o + e;
+                    x[e] = bf_at(smem + OFF_KB + kb_off(t, i)) *
+                           (gci * rcp_approx(*reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, i))));
+                }
+                store_row8(smem + OFF_A, smem + OFF_A + 16384, core_off(i, 8 * o), x);
+            }
+            fence_async_smem();
             __syncwarp();
             const bool ok = __syncthreads_and(wait_done(&ms->gram_done, n_gram & 1, a.wait_ns, a.err)) != 0;
             ++n_gram;
@@ -423,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t > s && grp == 0) L[t * kC + s] = ms->beta[t] * pr;
             }
         }
+        if (tid == 0) cp_bulk_wait_read();  // the previous chunk's T stores have read the A region
         __syncthreads();
 
         // ---- solve: (I + L) [-W | U] = X' with rows x_t = [-b_t k_t g_t | b_t v_t]: Tinv = (I + L)^-1
@@ -645,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i == 0 && r == 0) a.T_exp_tab[it.obj] = ex;
             }
             // box b of this warp's 64 columns: row i at i * 128, 16-byte chunk j at j ^ (i & 7)
-            uint8_t* box = smem + OFF_STAGE + (uint32_t)r * 32768;
+            uint8_t* box = smem + (r < 2 ? OFF_STAGE_T + (uint32_t)r * 32768 : OFF_STAGE_S + (uint32_t)(r - 2) * 32768);
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const uint32_t* xs = b ? x1 : x0;
@@ -666,10 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             const int y = (int)(it.obj * kD);
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                tma_store_2d(&tmT, smem + OFF_STAGE + b * 16384, 32 * b, y);
-                tma_store_2d(&tmS, smem + OFF_STAGE + 65536 + b * 16384, 32 * b, y);
-            }
+            for (int b = 0; b < 4; ++b) tma_store_2d(&tmS, smem + OFF_STAGE_S + b * 16384, 32 * b, y);
+            cp_bulk_commit();
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tma_store_2d(&tmT, smem + OFF_STAGE_T + b * 16384, 32 * b, y);
             cp_bulk_commit();
         }
     }

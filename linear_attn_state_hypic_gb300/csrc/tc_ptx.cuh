@@ -113,6 +113,11 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, 
 }
 __device__ __forceinline__ void cp_bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// At most N of this thread's bulk groups still reading their shared memory.
+template <int N>
+__device__ __forceinline__ void cp_bulk_wait_read_n() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- fences --
