@@ -484,15 +484,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid < 64) {
                 const int I = tid >> 4, r = tid & 15;
                 float y[16];
+                // every load before any store (a store could alias a later load for the compiler)
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const float* Lr = L + (16 * I + t) * kC + 16 * I;
+                    const float4* Lr = reinterpret_cast<const float4*>(L + (16 * I + t) * kC + 16 * I);
                     float acc = t == r ? 1.f : 0.f;
 #pragma unroll
-                    for (int u = 0; u < t; ++u) acc = fmaf(-Lr[u], y[u], acc);
+                    for (int q = 0; 4 * q < t; ++q) {
+                        const float4 l4 = Lr[q];
+                        acc = fmaf(-l4.x, y[4 * q], acc);
+                        if (4 * q + 1 < t) acc = fmaf(-l4.y, y[4 * q + 1], acc);
+                        if (4 * q + 2 < t) acc = fmaf(-l4.z, y[4 * q + 2], acc);
+                        if (4 * q + 3 < t) acc = fmaf(-l4.w, y[4 * q + 3], acc);
+                    }
                     y[t] = acc;
-                    TI[(16 * I + t) * kC + 16 * I + r] = acc;
                 }
+#pragma unroll
+                for (int t = 0; t < 16; ++t) TI[(16 * I + t) * kC + 16 * I + r] = y[t];
             } else {
                 for (int task = tid - 64; task < 2048; task += kThreads - 64) {
                     const int j = task & 255, o = task >> 8;
