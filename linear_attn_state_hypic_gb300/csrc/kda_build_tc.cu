@@ -506,13 +506,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int j = task & 255, o = task >> 8;
                     const bool isw = j < kD;
                     const int c = isw ? j : j - kD;
+                    const float4 b0 = *reinterpret_cast<const float4*>(&ms->beta[8 * o]);
+                    const float4 b1 = *reinterpret_cast<const float4*>(&ms->beta[8 * o + 4]);
+                    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                     float x[8];
+                    if (isw) {
+                        // token t = 8 o + e: the swizzled chunk of channel c is (c / 8) ^ (t & 15) in the
+                        // keys, (c / 4) ^ (t & 31) in the gates; the parts fixed by the task hoisted
+                        const uint8_t* kr = smem + OFF_KB + 8 * o * 256 + (c & 7) * 2;
+                        const uint8_t* gr = smem + OFF_GA + 8 * o * 512 + (c & 3) * 4;
+                        const int kq = (c >> 3) ^ ((8 * o) & 15), gq = (c >> 2) ^ ((8 * o) & 31);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int t = 8 * o + e;
-                        x[e] = isw ? -ms->beta[t] * bf_at(smem + OFF_KB + kb_off(t, c)) *
-                                         *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c))
-                                   : ms->beta[t] * bf_at(smem + OFF_VB + (t * kD + c) * 2);
+                        for (int e = 0; e < 8; ++e)
+                            x[e] = -bv[e] * bf_at(kr + e * 256 + ((kq ^ e) << 4)) *
+                                   *reinterpret_cast<const float*>(gr + e * 512 + ((gq ^ e) << 4));
+                    } else {
+                        const uint8_t* vr = smem + OFF_VB + (8 * o * kD + c) * 2;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = bv[e] * bf_at(vr + e * kD * 2);
                     }
                     store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 8 * o), x);
                 }
