@@ -276,12 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool safe;
         {
             const int c = tid & (kD - 1), blk = tid >> 7;
+            // token t = 16 blk + e of channel c: gate chunk (c / 4) ^ (t & 31), the thread's parts hoisted
+            uint8_t* gr = smem + OFF_GA + 16 * blk * 512 + (c & 3) * 4;
+            const int gq = (c >> 2) ^ ((16 * blk) & 31);
             float al[16], pi[16], sg[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int t = 16 * blk + e;
-                al[e] = t < it.n ? *reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, c)) : 1.f;
-            }
+            for (int e = 0; e < 16; ++e)
+                al[e] = 16 * blk + e < it.n ? *reinterpret_cast<const float*>(gr + e * 512 + ((gq ^ e) << 4)) : 1.f;
             pi[0] = al[0];
 #pragma unroll
             for (int e = 1; e < 16; ++e) pi[e] = pi[e - 1] * al[e];
@@ -303,8 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             safe = __syncthreads_and(gC >= kSafeGC) != 0;
             if (safe) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    *reinterpret_cast<float*>(smem + OFF_GA + ga_off(16 * blk + e, c)) = E * pi[e];
+                for (int e = 0; e < 16; ++e) *reinterpret_cast<float*>(gr + e * 512 + ((gq ^ e) << 4)) = E * pi[e];
             } else {
                 // Kbar^T from the gates themselves (k_t g_C / g_t is not in range here), once the previous
                 // chunk's T stores have read the A region; the other path forms it beside the gram MMAs
@@ -372,13 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int m = 0; m < 2; ++m) {
                 const int task = tid + kThreads * m, i = task & (kD - 1), o = task >> 7;
                 const float gci = ms->gC[i];
+                // token t = 8 o + e: swizzled chunks (i / 8) ^ (t & 15) and (i / 4) ^ (t & 31), the task's
+                // parts hoisted
+                const uint8_t* kr = smem + OFF_KB + 8 * o * 256 + (i & 7) * 2;
+                const uint8_t* gr = smem + OFF_GA + 8 * o * 512 + (i & 3) * 4;
+                const int kq = (i >> 3) ^ ((8 * o) & 15), gq = (i >> 2) ^ ((8 * o) & 31);
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int t = 8 * o + e;
-                    x[e] = bf_at(smem + OFF_KB + kb_off(t, i)) *
-                           (gci * rcp_approx(*reinterpret_cast<const float*>(smem + OFF_GA + ga_off(t, i))));
-                }
+                for (int e = 0; e < 8; ++e)
+                    x[e] = bf_at(kr + e * 256 + ((kq ^ e) << 4)) *
+                           (gci * rcp_approx(*reinterpret_cast<const float*>(gr + e * 512 + ((gq ^ e) << 4))));
                 store_row8(smem + OFF_A, smem + OFF_A + 16384, core_off(i, 8 * o), x);
             }
             fence_async_smem();
