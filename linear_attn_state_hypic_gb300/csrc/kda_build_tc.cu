@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_smem();
             __syncthreads();
-            if (tid == 0) {
+            if (tid == kThreads - 32) {  // lane 0 of warp 15 issues; warps 0-14 go on to Kbar^T
                 tc_fence_after();
                 const uint32_t sb = smem_u32(smem);
                 const uint32_t yh = sb + OFF_B, yl = yh + 16384, xh = yh + 32768, xl = yh + 49152;
@@ -364,13 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&ms->gram_done);
             }
-            // Kbar^T (k_t g_C / g_t) while the gram's MMAs run, once the previous chunk's T stores have
-            // read the A region: task (row i, tokens 8 o ..)
-            if (tid == 0) cp_bulk_wait_read();
-            __syncthreads();
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int task = tid + kThreads * m, i = task & (kD - 1), o = task >> 7;
+            // Kbar^T (k_t g_C / g_t) on warps 0-14 while the gram's MMAs run, once the previous chunk's
+            // T stores have read the A region: task (row i, tokens 8 o ..)
+            if (warp < 15) {
+                if (tid == 0) cp_bulk_wait_read();
+                asm volatile("bar.sync 3, 480;" ::: "memory");
+            }
+            for (int task = tid; warp < 15 && task < 1024; task += kThreads - 32) {
+                const int i = task & (kD - 1), o = task >> 7;
                 const float gci = ms->gC[i];
                 // token t = 8 o + e: swizzled chunks (i / 8) ^ (t & 15) and (i / 4) ^ (t & 31), the task's
                 // parts hoisted
