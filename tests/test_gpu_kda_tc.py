@@ -135,3 +135,35 @@ def test_kda_tc_segment_longer_than_a_batch(B):
     To, So = orc.build_pairs("kda", kk, vv, np.array([0, sl.stop - sl.start], np.int32), g=gg, beta=bb)
     assert_rel(host(S)[1:2, :, :2], So, TOL_BF16, what="S of the long segment")
     assert_rel(gdn_T64(T, T_exp)[1:2, :, :2], To, TOL_BF16, what="T of the long segment")
+
+
+def test_kda_tc_safe_and_guarded_chunks_in_one_call(B):
+    """Most chunks have gates in [0.85, 1) and take the tensor-core gram; in a
+    few, some channels' gates are ~1e-3, so the chunk's decay leaves the range
+    of k / g_t and it forms its gram from running products on CUDA cores.  Both
+    kinds of chunk in one launch, against the oracle."""
+    rng = np.random.default_rng(406)
+    lengths = [640, 300, 129]
+    cu, k, v, g, beta = kda_inputs(rng, lengths, 1, 4)
+    g[0, 64:128, :, :5] = 1e-3       # chunk 1 of segment 0: g_C of those channels ~1e-192
+    g[0, 700:710, 1, 60:64] = 1e-4   # inside segment 1, one head
+    T, T_exp, S = build(B, k, v, g, beta, cu)
+    To, So = orc.build_pairs("kda", k, v, cu, g=g, beta=beta)
+    assert_rel(host(S), So, TOL_BF16, what="kda S (mixed chunks)")
+    assert_rel(gdn_T64(T, T_exp), To, TOL_BF16, what="kda T (mixed chunks)")
+
+
+def test_kda_tc_zero_beta_is_the_gate_product(B):
+    """b = 0: every delta step is the identity, so T_C = Diag(prod_t a_t) and
+    S = 0 (a closed form, no oracle)."""
+    rng = np.random.default_rng(407)
+    lengths = [200, 64, 1]
+    cu, k, v, g, beta = kda_inputs(rng, lengths, 1, 3, glo=0.9)
+    beta[:] = 0.0
+    T, T_exp, S = build(B, k, v, g, beta, cu)
+    assert np.all(host(S) == 0)
+    Tg = gdn_T64(T, T_exp)
+    for s in range(len(lengths)):
+        prod = np.prod(g[0, int(cu[s]):int(cu[s + 1])].astype(np.float64), axis=0)  # [H][d]
+        want = np.stack([np.diag(prod[h]) for h in range(3)])[None]
+        np.testing.assert_allclose(Tg[s], want, rtol=1e-5, atol=0)
