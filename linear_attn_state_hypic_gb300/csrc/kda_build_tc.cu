@@ -35,8 +35,8 @@
 // Tinv):
 //   scan     16-token block products per channel -> g_C, g_t, Kbar^T (bf16 hi + lo operand)
 //   gram     Y, X operands -> G = Y X^T (M = 64, N = 64, K = 128, three products) -> b_t G_ts
-//   solve    Tinv = (I + L)^-1, L_ts = b_t G_ts (16 x 16 diagonal blocks by forward
-//            substitution, the blocks below from them); [-W | U] = Tinv X' with rows
+//   solve    Tinv = (I + L)^-1, L_ts = b_t G_ts (32 x 32 diagonal blocks by forward
+//            substitution, the block below from them); [-W | U] = Tinv X' with rows
 //            x_t = [-b_t k_t g_t | b_t v_t], so the pair is Kbar^T Tinv X': first
 //            P = Kbar^T Tinv (M = 128, N = 64, K = 64 MMAs in hi + lo pairs)
 //   MMA      D = P X': M = 128, N = 256, K = 64 in hi + lo pairs (three products), fp32 in
@@ -85,8 +85,8 @@ constexpr uint32_t OFF_B = OFF_L + 16384;    // X'^T hi, lo: bf16 [256 j][64 t],
 constexpr uint32_t OFF_A = OFF_B + 65536;    // Kbar^T, then P = Kbar^T Tinv: hi, lo bf16 [128 i][64 t], 16 KB each
 constexpr uint32_t OFF_TI = OFF_A + 32768;    // Tinv = (I + L)^-1: fp32 [64 t][64 s]
 constexpr uint32_t OFF_TIO = OFF_TI + 16384;  // Tinv^T hi, lo: bf16 [64 t][64 s] operand, 8 KB each
-constexpr uint32_t OFF_R = OFF_TIO + 16384;   // solve scratch: fp32 [16][48]
-constexpr uint32_t OFF_MISC = OFF_R + 3072;
+constexpr uint32_t OFF_R = OFF_TIO + 16384;   // solve scratch: fp32 [32][32]
+constexpr uint32_t OFF_MISC = OFF_R + 4096;
 constexpr uint32_t OFF_STAGE_S = OFF_B;       // S_chunk as 4 boxes of 128 rows x 32 (128-byte swizzle) over
                                               // X'^T; its stores go first, so the next chunk's gram operands
                                               // find the region read
@@ -481,17 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncthreads();
         }
         {
-            // warps 0-1: the 16 x 16 diagonal blocks of Tinv, (I + L_II)^-1 by forward substitution
+            // warps 0-1: the 32 x 32 diagonal blocks of Tinv, (I + L_II)^-1 by forward substitution
             // (thread: block I, column r); the other warps: X'^T rows j (K-major over the chunk's
-            // tokens), task (octet o, row j) of eight tokens, and zeros in the blocks above the diagonal
+            // tokens), task (octet o, row j) of eight tokens, and zeros in the block above the diagonal
             float* TI = reinterpret_cast<float*>(smem + OFF_TI);
             if (tid < 64) {
-                const int I = tid >> 4, r = tid & 15;
-                float y[16];
+                const int I = tid >> 5, r = tid & 31;
+                float y[32];
                 // every load before any store (a store could alias a later load for the compiler)
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float4* Lr = reinterpret_cast<const float4*>(L + (16 * I + t) * kC + 16 * I);
+                for (int t = 0; t < 32; ++t) {
+                    const float4* Lr = reinterpret_cast<const float4*>(L + (32 * I + t) * kC + 32 * I);
                     float acc = t == r ? 1.f : 0.f;
 #pragma unroll
                     for (int q = 0; 4 * q < t; ++q) {
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     y[t] = acc;
                 }
 #pragma unroll
-                for (int t = 0; t < 16; ++t) TI[(16 * I + t) * kC + 16 * I + r] = y[t];
+                for (int t = 0; t < 32; ++t) TI[(32 * I + t) * kC + 32 * I + r] = y[t];
             } else {
                 for (int task = tid - 64; task < 2048; task += kThreads - 64) {
                     const int j = task & 255, o = task >> 8;
@@ -532,13 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_row8(smem + OFF_B, smem + OFF_B + 32768, core_off(j, 8 * o), x);
                 }
                 fence_async_smem();
-                // blocks (I, J), I < J: row t = 16 I + tt, columns 16 J .. 16 J + 15 (four float4 each)
-                for (int e = tid - 64; e < 6 * 16 * 4; e += kThreads - 64) {
-                    const int blkp = e >> 6, rem = e & 63, tt = rem >> 2, q4 = rem & 3;
-                    const int I = blkp < 3 ? 0 : (blkp < 5 ? 1 : 2);
-                    const int J = blkp < 3 ? blkp + 1 : (blkp < 5 ? blkp - 1 : 3);
-                    *reinterpret_cast<float4*>(TI + (16 * I + tt) * kC + 16 * J + 4 * q4) = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                // the block above the diagonal: rows 0-31, columns 32-63 (eight float4 a row)
+                for (int e = tid - 64; e < 32 * 8; e += kThreads - 64)
+                    *reinterpret_cast<float4*>(TI + (e >> 3) * kC + 32 + 4 * (e & 7)) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         __syncthreads();
@@ -546,54 +542,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp >= 8) {
             if (more) prefetch<kThreads / 2>(smem, ms, a, nxt, tid - kThreads / 2);
         } else {
-            // off-diagonal blocks, row block I = 1..3: R_J = sum_{K=J}^{I-1} L_IK Tinv_KJ, then
-            // Tinv_IJ = -Tinv_II R_J; thread: column col < 16 I, rows 4 g4 .. 4 g4 + 3 of the block row
+            // the block below the diagonal: Tinv_10 = -Tinv_11 (L_10 Tinv_00), 32 x 32 each; thread:
+            // column col, rows 4 g4 .. 4 g4 + 3
             float* TI = reinterpret_cast<float*>(smem + OFF_TI);
             float* R = reinterpret_cast<float*>(smem + OFF_R);
+            const int col = tid & 31, g4 = tid >> 5;
+            {
+                const float* L0 = L + (32 + 4 * g4) * kC;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int I = 1; I < 4; ++I) {
-                const int w16 = 16 * I;
-                if (tid < 4 * w16) {
-                    const int col = tid % w16, g4 = tid / w16, J = col >> 4;
-                    const float* L0 = L + (w16 + 4 * g4) * kC;
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int s4 = 0; s4 < 8; ++s4) {
+                    float tv[4];
 #pragma unroll
-                    for (int s4 = 0; s4 < 4 * I; ++s4) {
-                        if (s4 < 4 * J) continue;  // the blocks left of J hold no term
-                        float tv[4];
+                    for (int e = 0; e < 4; ++e) tv[e] = TI[(4 * s4 + e) * kC + col];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) tv[e] = TI[(4 * s4 + e) * kC + col];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float4 l = *reinterpret_cast<const float4*>(L0 + k * kC + 4 * s4);
-                            acc[k] = fmaf(l.x, tv[0], fmaf(l.y, tv[1], fmaf(l.z, tv[2], fmaf(l.w, tv[3], acc[k]))));
-                        }
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 l = *reinterpret_cast<const float4*>(L0 + k * kC + 4 * s4);
+                        acc[k] = fmaf(l.x, tv[0], fmaf(l.y, tv[1], fmaf(l.z, tv[2], fmaf(l.w, tv[3], acc[k]))));
                     }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) R[(4 * g4 + k) * 48 + col] = acc[k];
                 }
-                asm volatile("bar.sync 2, 256;" ::: "memory");
-                if (tid < 4 * w16) {
-                    const int col = tid % w16, g4 = tid / w16;
-                    const float* D0 = TI + (w16 + 4 * g4) * kC + w16;  // rows of Tinv_II (zero above the diagonal)
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int u4 = 0; u4 < 4; ++u4) {
-                        if (u4 > g4) break;  // Tinv_II is zero above its diagonal
-                        float rv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) rv[e] = R[(4 * u4 + e) * 48 + col];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float4 d = *reinterpret_cast<const float4*>(D0 + k * kC + 4 * u4);
-                            acc[k] = fmaf(d.x, rv[0], fmaf(d.y, rv[1], fmaf(d.z, rv[2], fmaf(d.w, rv[3], acc[k]))));
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) TI[(w16 + 4 * g4 + k) * kC + col] = -acc[k];
-                }
-                asm volatile("bar.sync 2, 256;" ::: "memory");
+                for (int k = 0; k < 4; ++k) R[(4 * g4 + k) * 32 + col] = acc[k];
             }
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            {
+                const float* D0 = TI + (32 + 4 * g4) * kC + 32;  // rows of Tinv_11 (zero above the diagonal)
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    if (u4 > g4) break;
+                    float rv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) rv[e] = R[(4 * u4 + e) * 32 + col];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 d = *reinterpret_cast<const float4*>(D0 + k * kC + 4 * u4);
+                        acc[k] = fmaf(d.x, rv[0], fmaf(d.y, rv[1], fmaf(d.z, rv[2], fmaf(d.w, rv[3], acc[k]))));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) TI[(32 + 4 * g4 + k) * kC + col] = -acc[k];
+            }
+            asm volatile("bar.sync 2, 256;" ::: "memory");
             // Tinv^T as the bf16 hi + lo operand (rows t, K-major over s: Tinv[s][t]): task (row t, octet o)
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
