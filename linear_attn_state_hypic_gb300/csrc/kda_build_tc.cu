@@ -70,6 +70,7 @@ using namespace tc;
 
 constexpr int kD = 128, kC = 64;
 constexpr int kThreads = 512;
+constexpr int kSStoreB = 128;  // the thread that stores the second half of S_chunk (thread 0 the first, and T)
 constexpr int64_t kPairBytes = 2 * kD * kD * 4;  // T and S of one chunk, layer and head
 
 // Shared memory map (bytes).  The MMA operands are K-major without swizzle:
@@ -185,12 +186,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
-// x * 2^e for any int e with the result in range (two exact power-of-two factors).
-__device__ __forceinline__ float scale_pow2(float x, int e) {
-    const int e1 = e / 2, e2 = e - e1;
-    return x * __int_as_float((e1 + 127) << 23) * __int_as_float((e2 + 127) << 23);
-}
-
 __device__ __noinline__ bool wait_done(uint64_t* bar, uint32_t parity, uint64_t wait_ns, unsigned* err) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
@@ -266,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = item + (int)gridDim.x < a.n_items;
         if (more) nxt = decode(a, item + gridDim.x);  // loads issued here, used at the prefetch
         // After the first chunk only warps 8-15 have loads in flight (they issue the prefetch); in
-        // thread 0 the wait would also cover the pair's bulk stores.
+        // threads 0 and kSStoreB (warps 0 and 4) the wait would also cover the pair's bulk stores.
         if (item == (int)blockIdx.x || warp >= 8) cp_async_wait_all();
         tc_fence_before();
         __syncthreads();
@@ -290,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 14; e >= 0; --e) sg[e] = sg[e + 1] * al[e + 1];
             ms->btot[blk][c] = pi[15];
-            if (tid == 0) cp_bulk_wait_read_n<1>();  // the previous chunk's S stores have read their boxes
             __syncthreads();
             float E = 1.f, F = 1.f;  // gate products of the blocks before and after this one
 #pragma unroll
@@ -308,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // Kbar^T from the gates themselves (k_t g_C / g_t is not in range here), once the previous
                 // chunk's T stores have read the A region; the other path forms it beside the gram MMAs
-                if (tid == 0) cp_bulk_wait_read();
+                if (tid == 0 || tid == kSStoreB) cp_bulk_wait_read();
                 __syncthreads();
                 uint8_t* ahi = smem + OFF_A;
 #pragma unroll
@@ -326,7 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if (safe) {
-            // ---- gram operands: task (channel octet q8, token t); Y = k g, X = k / g
+            // ---- gram operands: task (channel octet q8, token t); Y = k g, X = k / g, over the boxes
+            // that the previous chunk's S stores have read by now (the other path waited above)
+            if (tid == 0) cp_bulk_wait_read_n<1>();
+            if (tid == kSStoreB) cp_bulk_wait_read();
             __syncthreads();  // every g_t written
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
@@ -488,13 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid < 64) {
                 const int I = tid >> 5, r = tid & 31;
                 float y[32];
-                // every load before any store (a store could alias a later load for the compiler)
+                // every load before any store (a store could alias a later load for the compiler); the
+                // inner loop has a fixed trip count, so that it unrolls in full and y stays in registers
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
                     const float4* Lr = reinterpret_cast<const float4*>(L + (32 * I + t) * kC + 32 * I);
                     float acc = t == r ? 1.f : 0.f;
 #pragma unroll
-                    for (int q = 0; 4 * q < t; ++q) {
+                    for (int q = 0; q < 8; ++q) {
+                        if (4 * q >= t) continue;
                         const float4 l4 = Lr[q];
                         acc = fmaf(-l4.x, y[4 * q], acc);
                         if (4 * q + 1 < t) acc = fmaf(-l4.y, y[4 * q + 1], acc);
@@ -658,37 +657,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
 
-        // ---- write: warp (quarter q, part r): r = 0, 1 columns 64 r .. of T_chunk, r = 2, 3 of S_chunk,
-        // staged as 32-column boxes (128-byte swizzle) in the operand area, then stored by TMA
+        // ---- write: warp (quarter q, part r): r = 0, 1 columns 64 r .. of S_chunk, r = 2, 3 columns
+        // 64 (r - 2) .. of T_chunk, staged as 32-column boxes (128-byte swizzle) in the operand area,
+        // then stored by TMA: each S part as soon as its four warps have staged it (the next chunk's
+        // gram operands go over the S boxes), T after the whole CTA
         {
             const int q = warp & 3, r = warp >> 2, i = 32 * q + lane;
-            const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + TM_PAIR + 64 * r;
+            const bool isT = r >= 2;
+            const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + TM_PAIR + (isT ? 64 * (r - 2) : 128 + 64 * r);
             uint32_t x0[32], x1[32];
             tmem_ld32(tl, x0);
             tmem_ld32(tl + 32, x1);
             tmem_wait_ld();
             int ex = 0;
-            if (r < 2) {
-                const float gci = ms->gC[i];
+            float s1 = 1.f, s2 = 1.f;
+            bool two = false;
+            if (isT) {
+                // Diag(g_C): element (i, i) lies in this warp's 64 columns when r - 2 = q / 2, at column
+                // 32 (q & 1) + lane of them (x1 for odd q, x0 for even q)
+                if (r - 2 == (q >> 1)) {
+                    const float gci = ms->gC[i];
+                    if (q & 1) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e == lane) x1[e] = __float_as_uint(__uint_as_float(x1[e]) + gci);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e == lane) x0[e] = __float_as_uint(__uint_as_float(x0[e]) + gci);
+                    }
+                }
                 float mx = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    x0[e] = __float_as_uint(__uint_as_float(x0[e]) + (64 * r + e == i ? gci : 0.f));
-                    x1[e] = __float_as_uint(__uint_as_float(x1[e]) + (64 * r + 32 + e == i ? gci : 0.f));
+                for (int e = 0; e < 32; ++e)
                     mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(x0[e])), fabsf(__uint_as_float(x1[e]))));
-                }
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 if (lane == 0) ms->red[warp] = mx;
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 float M = 0.f;
 #pragma unroll
-                for (int wv = 0; wv < 8; ++wv) M = fmaxf(M, ms->red[wv]);
+                for (int wv = 8; wv < 16; ++wv) M = fmaxf(M, ms->red[wv]);
                 ex = (M > 0.f && isfinite(M)) ? ilogbf(M) : 0;
-                if (i == 0 && r == 0) a.T_exp_tab[it.obj] = ex;
+                if (i == 0 && r == 2) a.T_exp_tab[it.obj] = ex;
+                // 2^-ex as one normal factor where it is one, else as two
+                two = ex < -126 || ex > 126;
+                const int e1 = two ? -ex / 2 : -ex, e2 = -ex - e1;
+                s1 = __int_as_float((e1 + 127) << 23);
+                s2 = __int_as_float((e2 + 127) << 23);
             }
             // box b of this warp's 64 columns: row i at i * 128, 16-byte chunk j at j ^ (i & 7)
-            uint8_t* box = smem + (r < 2 ? OFF_STAGE_T + (uint32_t)r * 32768 : OFF_STAGE_S + (uint32_t)(r - 2) * 32768);
+            uint8_t* box = smem + (isT ? OFF_STAGE_T + (uint32_t)(r - 2) * 32768 : OFF_STAGE_S + (uint32_t)r * 32768);
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const uint32_t* xs = b ? x1 : x0;
@@ -697,26 +716,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 8; ++j) {
                     float4 v = make_float4(__uint_as_float(xs[4 * j]), __uint_as_float(xs[4 * j + 1]),
                                            __uint_as_float(xs[4 * j + 2]), __uint_as_float(xs[4 * j + 3]));
-                    if (r < 2)
-                        v = make_float4(scale_pow2(v.x, -ex), scale_pow2(v.y, -ex), scale_pow2(v.z, -ex),
-                                        scale_pow2(v.w, -ex));
+                    if (isT) {
+                        v = make_float4(v.x * s1, v.y * s1, v.z * s1, v.w * s1);
+                        if (two) v = make_float4(v.x * s2, v.y * s2, v.z * s2, v.w * s2);
+                    }
                     *reinterpret_cast<float4*>(row + ((j ^ (i & 7)) << 4)) = v;
                 }
             }
             fence_async_smem();
+            if (!isT) {
+                // the four warps of S part r, then its two boxes by thread 0 (r = 0) or kSStoreB (r = 1)
+                if (r == 0)
+                    asm volatile("bar.sync 4, 128;" ::: "memory");
+                else
+                    asm volatile("bar.sync 5, 128;" ::: "memory");
+                if (q == 0 && lane == 0) {
+                    const int y = (int)(it.obj * kD);
+                    tma_store_2d(&tmS, smem + OFF_STAGE_S + r * 32768, 64 * r, y);
+                    tma_store_2d(&tmS, smem + OFF_STAGE_S + r * 32768 + 16384, 64 * r + 32, y);
+                    cp_bulk_commit();
+                }
+            }
         }
         __syncthreads();
         if (tid == 0) {
             const int y = (int)(it.obj * kD);
 #pragma unroll
-            for (int b = 0; b < 4; ++b) tma_store_2d(&tmS, smem + OFF_STAGE_S + b * 16384, 32 * b, y);
-            cp_bulk_commit();
-#pragma unroll
             for (int b = 0; b < 4; ++b) tma_store_2d(&tmT, smem + OFF_STAGE_T + b * 16384, 32 * b, y);
             cp_bulk_commit();
         }
     }
-    if (tid == 0) cp_bulk_wait_all();
+    if (tid == 0 || tid == kSStoreB) cp_bulk_wait_all();
     cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
