@@ -76,12 +76,15 @@ constexpr int64_t kPairBytes = 2 * kD * kD * 4;  // T and S of one chunk, layer 
 // Shared memory map (bytes).  The MMA operands are K-major without swizzle:
 // core matrices of 8 rows x 16 bytes, adjacent along K 128 bytes apart, row
 // groups 1024 (K = 64 tokens) or 2048 (K = 128 channels) bytes apart.
+// L's rows are kLs floats apart: a warp's lanes, one row each, then write 16-byte pieces of the same
+// columns without bank conflicts (4 banks further per row)
+constexpr int kLs = 68;
 constexpr uint32_t OFF_KB = 0;               // keys, bf16 [64 t][128 c]; 16-byte chunk q of row t at q ^ (t & 15)
 constexpr uint32_t OFF_VB = OFF_KB + 16384;  // values, bf16 [64 t][128 c]
 constexpr uint32_t OFF_GA = OFF_VB + 16384;  // gates, fp32 [64 t][128 c]; chunk q of row t at q ^ (t & 31);
                                              // then g_t when the gram runs on the tensor cores
-constexpr uint32_t OFF_L = OFF_GA + 32768;   // b_t G_ts for s < t, 0 elsewhere: fp32 [64 t][64 s]
-constexpr uint32_t OFF_B = OFF_L + 16384;    // X'^T hi, lo: bf16 [256 j][64 t], 32 KB each; before them
+constexpr uint32_t OFF_L = OFF_GA + 32768;   // b_t G_ts for s < t, 0 elsewhere: fp32 [64 t][64 s], rows kLs apart
+constexpr uint32_t OFF_B = OFF_L + 17408;    // X'^T hi, lo: bf16 [256 j][64 t], 32 KB each; before them
                                              // the gram operands Y hi, lo, X hi, lo: bf16 [64 t][128 c]
 constexpr uint32_t OFF_A = OFF_B + 65536;    // Kbar^T, then P = Kbar^T Tinv: hi, lo bf16 [128 i][64 t], 16 KB each
 constexpr uint32_t OFF_TI = OFF_A + 32768;    // Tinv = (I + L)^-1: fp32 [64 t][64 s]
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         o.y = s + 1 < t ? coef * __uint_as_float(gv[e + 1]) : 0.f;
                         o.z = s + 2 < t ? coef * __uint_as_float(gv[e + 2]) : 0.f;
                         o.w = s + 3 < t ? coef * __uint_as_float(gv[e + 3]) : 0.f;
-                        *reinterpret_cast<float4*>(L + t * kC + s) = o;
+                        *reinterpret_cast<float4*>(L + t * kLs + s) = o;
                     }
                 }
             }
@@ -414,7 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- gram on CUDA cores, exact for any gate: thread (s, group) holds k_s over the
             // channels 4 group + 32 m + e, times the gates after s, and meets every later key
 #pragma unroll
-            for (int m = 0; m < 2; ++m) reinterpret_cast<float4*>(L)[tid + kThreads * m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int m = 0; m < 3; ++m)
+                if (tid + kThreads * m < 64 * kLs / 4)
+                    reinterpret_cast<float4*>(L)[tid + kThreads * m] = make_float4(0.f, 0.f, 0.f, 0.f);
             __syncthreads();
             const int s = tid >> 3, grp = tid & 7;
             float z[16];
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pr += __shfl_xor_sync(0xffffffffu, pr, 1);
                 pr += __shfl_xor_sync(0xffffffffu, pr, 2);
                 pr += __shfl_xor_sync(0xffffffffu, pr, 4);
-                if (t > s && grp == 0) L[t * kC + s] = ms->beta[t] * pr;
+                if (t > s && grp == 0) L[t * kLs + s] = ms->beta[t] * pr;
             }
         }
         if (tid == 0) cp_bulk_wait_read();  // the previous chunk's T stores have read the A region
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // inner loop has a fixed trip count, so that it unrolls in full and y stays in registers
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
-                    const float4* Lr = reinterpret_cast<const float4*>(L + (32 * I + t) * kC + 32 * I);
+                    const float4* Lr = reinterpret_cast<const float4*>(L + (32 * I + t) * kLs + 32 * I);
                     float acc = t == r ? 1.f : 0.f;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -547,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* R = reinterpret_cast<float*>(smem + OFF_R);
             const int col = tid & 31, g4 = tid >> 5;
             {
-                const float* L0 = L + (32 + 4 * g4) * kC;
+                const float* L0 = L + (32 + 4 * g4) * kLs;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int s4 = 0; s4 < 8; ++s4) {
@@ -556,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 4; ++e) tv[e] = TI[(4 * s4 + e) * kC + col];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float4 l = *reinterpret_cast<const float4*>(L0 + k * kC + 4 * s4);
+                        const float4 l = *reinterpret_cast<const float4*>(L0 + k * kLs + 4 * s4);
                         acc[k] = fmaf(l.x, tv[0], fmaf(l.y, tv[1], fmaf(l.z, tv[2], fmaf(l.w, tv[3], acc[k]))));
                     }
                 }
