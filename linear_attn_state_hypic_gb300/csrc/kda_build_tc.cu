@@ -34,7 +34,8 @@
 // values, gates and b loaded by cp.async on warps 8-15 while warps 0-7 finish
 // Tinv):
 //   scan     16-token block products per channel -> g_C, g_t, Kbar^T (bf16 hi + lo operand)
-//   gram     Y, X operands -> G = Y X^T (M = 64, N = 64, K = 128, three products) -> b_t G_ts
+//   gram     Y, X operands -> [Yhi; Ylo] [Xhi; Xlo]^T (M = N = 128, K = 128: the four
+//            hi/lo products of G = Y X^T in one accumulator) -> b_t G_ts
 //   solve    Tinv = (I + L)^-1, L_ts = b_t G_ts (32 x 32 diagonal blocks by forward
 //            substitution, the block below from them); [-W | U] = Tinv X' with rows
 //            x_t = [-b_t k_t g_t | b_t v_t], so the pair is Kbar^T Tinv X': first
@@ -44,6 +45,7 @@
 //   write    T_chunk = Diag(g_C) + D_left, normalised by a power of two (its exponent
 //            kept beside it), and S_chunk = D_right, one tensor-memory pass on 16 warps into
 //            128-byte-swizzled boxes over the spent operands, written out by TMA tile stores
+//            (each half of S as soon as its four warps have staged it)
 // The chunk tables cost 128 KB per chunk, layer and head; segments are taken
 // in batches whose tables fit the workspace (up to 4 GiB of them), and a
 // segment longer than a batch in parts: each part's chain starts with the pair
@@ -112,7 +114,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_PAIR = 0, TM_GRAM = 256, TM_SOLVE = 384;
 constexpr uint32_t ID_PAIR = idesc(1, 128, 256, false, false);  // D = P X' = Kbar^T [-W | U], both K-major
-constexpr uint32_t ID_GRAM = idesc(1, 64, 64, false, false);    // G = Y X^T, both K-major
+constexpr uint32_t ID_GRAM = idesc(1, 128, 128, false, false);  // [Yhi; Ylo] [Xhi; Xlo]^T, both K-major
 constexpr uint32_t ID_SOLVE = idesc(1, 128, 64, false, false);  // P = Kbar^T Tinv
 constexpr float kSafeGC = 0x1p-100f;
 
@@ -353,15 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == kThreads - 32) {  // lane 0 of warp 15 issues; warps 0-14 go on to Kbar^T
                 tc_fence_after();
                 const uint32_t sb = smem_u32(smem);
-                const uint32_t yh = sb + OFF_B, yl = yh + 16384, xh = yh + 32768, xl = yh + 49152;
+                const uint32_t yh = sb + OFF_B, xh = yh + 32768;
+                // Y lo follows Y hi and X lo follows X hi at the 8-row group stride, so [Yhi; Ylo] and
+                // [Xhi; Xlo] are M = 128 and N = 128 operands: one MMA a K step gives all four products
 #pragma unroll 1
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t dyh = sdesc_plain(yh + 256 * kk, 128, 2048), dyl = sdesc_plain(yl + 256 * kk, 128, 2048);
-                    const uint64_t dxh = sdesc_plain(xh + 256 * kk, 128, 2048), dxl = sdesc_plain(xl + 256 * kk, 128, 2048);
-                    mma_bf16_ss(tmem + TM_GRAM, dyh, dxh, ID_GRAM, kk > 0);
-                    mma_bf16_ss(tmem + TM_GRAM, dyh, dxl, ID_GRAM, true);
-                    mma_bf16_ss(tmem + TM_GRAM, dyl, dxh, ID_GRAM, true);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ss(tmem + TM_GRAM, sdesc_plain(yh + 256 * kk, 128, 2048), sdesc_plain(xh + 256 * kk, 128, 2048),
+                                ID_GRAM, kk > 0);
                 mma_commit(&ms->gram_done);
             }
             // Kbar^T (k_t g_C / g_t) on warps 0-14 while the gram's MMAs run, once the previous chunk's
@@ -391,25 +391,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++n_gram;
             if (!ok) break;
             tc_fence_after();
-            // b_t G_ts for s < t: warp (quarter q, columns 16 cb ..); row 16 q + l of the M = 64
-            // accumulator sits in lane 32 q + l, l < 16
+            // b_t G_ts for s < t, G = Yhi Xhi + Yhi Xlo + Ylo Xhi + Ylo Xlo: accumulator rows 64 + t hold
+            // the Y lo products and columns 64 + s the X lo ones. Warp (quarter q, columns 16 cb ..):
+            // quarters 2 and 3 leave their sums in L, then quarters 0 and 1 add theirs, scale and mask.
             {
-                const int q = warp & 3, cb = warp >> 2;
-                uint32_t gv[16];
-                tmem_ld16(tmem + ((32u * q) << 16) + TM_GRAM + 16 * cb, gv);
+                const int q = warp & 3, cb = warp >> 2, t = 32 * (q & 1) + lane;
+                uint32_t g0[16], g1[16];
+                tmem_ld16(tmem + ((32u * q) << 16) + TM_GRAM + 16 * cb, g0);
+                tmem_ld16(tmem + ((32u * q) << 16) + TM_GRAM + 64 + 16 * cb, g1);
                 tmem_wait_ld();
-                if (lane < 16) {
-                    const int t = 16 * q + lane;
+                float4* Lr = reinterpret_cast<float4*>(L + t * kLs + 16 * cb);
+                if (q >= 2) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        Lr[e / 4] = make_float4(__uint_as_float(g0[e]) + __uint_as_float(g1[e]),
+                                                __uint_as_float(g0[e + 1]) + __uint_as_float(g1[e + 1]),
+                                                __uint_as_float(g0[e + 2]) + __uint_as_float(g1[e + 2]),
+                                                __uint_as_float(g0[e + 3]) + __uint_as_float(g1[e + 3]));
+                }
+                __syncthreads();
+                if (q < 2) {
                     const float coef = ms->beta[t];
 #pragma unroll
                     for (int e = 0; e < 16; e += 4) {
                         const int s = 16 * cb + e;
+                        const float4 lo = Lr[e / 4];
                         float4 o;
-                        o.x = s < t ? coef * __uint_as_float(gv[e]) : 0.f;
-                        o.y = s + 1 < t ? coef * __uint_as_float(gv[e + 1]) : 0.f;
-                        o.z = s + 2 < t ? coef * __uint_as_float(gv[e + 2]) : 0.f;
-                        o.w = s + 3 < t ? coef * __uint_as_float(gv[e + 3]) : 0.f;
-                        *reinterpret_cast<float4*>(L + t * kLs + s) = o;
+                        o.x = s < t ? coef * ((__uint_as_float(g0[e]) + __uint_as_float(g1[e])) + lo.x) : 0.f;
+                        o.y = s + 1 < t ? coef * ((__uint_as_float(g0[e + 1]) + __uint_as_float(g1[e + 1])) + lo.y) : 0.f;
+                        o.z = s + 2 < t ? coef * ((__uint_as_float(g0[e + 2]) + __uint_as_float(g1[e + 2])) + lo.z) : 0.f;
+                        o.w = s + 3 < t ? coef * ((__uint_as_float(g0[e + 3]) + __uint_as_float(g1[e + 3])) + lo.w) : 0.f;
+                        Lr[e / 4] = o;
                     }
                 }
             }
