@@ -94,10 +94,10 @@ constexpr uint32_t OFF_TIO = OFF_TI + 16384;  // Tinv^T hi, lo: bf16 [64 t][64 s
 constexpr uint32_t OFF_R = OFF_TIO + 16384;   // solve scratch: fp32 [32][32]
 constexpr uint32_t OFF_MISC = OFF_R + 4096;
 constexpr uint32_t OFF_STAGE_S = OFF_B;       // S_chunk as 4 boxes of 128 rows x 32 (128-byte swizzle) over
-                                              // X'^T; its stores go first, so the next chunk's gram operands
-                                              // find the region read
-constexpr uint32_t OFF_STAGE_T = OFF_A;       // T_chunk's 4 boxes over P, Tinv and its operand (64 KB), free
-                                              // in the next chunk until its X' stage
+                                              // X'^T; each half is stored as soon as it is staged, so the
+                                              // next chunk's gram operands find the region read
+constexpr uint32_t OFF_STAGE_T = OFF_A;       // T_chunk's 4 boxes over P, Tinv and its operand (64 KB): the
+                                              // next chunk waits for their read before it forms Kbar^T there
 
 struct KMisc {
     uint64_t gram_done, solve_done, pair_done;
