@@ -378,6 +378,27 @@ def test_conv_rejections(B, mutate, status):
     assert B.lib.hypic_last_error_detail().decode()
 
 
+def test_build_workspace_caps_kda_chunk_tables(B):
+    """The reported KDA workspace holds at most 4 GiB of chunk tables (128 KB per
+    chunk, layer and head), and never fewer than two chunks' tables, so that a
+    long request is built in batches and a segment longer than a batch in parts."""
+    pair = 128 * 1024
+    for L, H, lengths, chunks in (
+        (30, 32, (640000, 64), (4 << 30) // (30 * 32 * pair)),   # 10,001 chunks, 34 fit 4 GiB
+        (100, 1000, (640, 64), 2),                               # one chunk of tables > 4 GiB
+        (1, 2, (64, 80), 3),                                     # everything fits: all 3 chunks
+    ):
+        a, keep = base_build(B, 4, lengths=lengths)
+        a.n_layers, a.n_heads = L, H
+        a.in_dtype = 0                    # fp32 inputs: the CUDA-core kernel, plan only
+        plan = B.hypic_build_workspace_size(a)
+        a.in_dtype = 1
+        need = B.hypic_build_workspace_size(a)
+        LH = L * H
+        assert chunks * LH * pair <= need - plan < (chunks + 1) * LH * pair, (L, H, lengths)
+        assert run_build(B, a, ws=need - 1) == B.ERR_WORKSPACE
+
+
 def test_build_workspace_holds_kda_chunk_tables(B):
     """KDA at d = 128 with bf16 k and v: the reported workspace also holds the
     chunk tables of its tensor-core path (T and S of every 64-token chunk,
